@@ -1,0 +1,255 @@
+"""Seeded synthetic inputs for the quantized GEMM workloads.
+
+This module is shared by the tests, the smoke check and the benchmark.  It
+holds the workload recipes (shapes, value distributions, seeds) and the
+input-side encoders that turn real-valued draws into operand bytes (E4M3,
+packed E2M1, UE8M0 scales, int8).  It contains none of the GEMM's arithmetic,
+imports neither the oracle nor the CUDA package, and the oracle and the GPU
+consume exactly the bytes produced here.
+
+Recipes (the model-projection shapes of the pages, with synthetic values):
+
+* INT8 row/column-scaled: A, B int8 uniform in [-127, 127]; sa[M], sb[N]
+  fp32 uniform in [1e-3, 1e-2]; bias bf16 from N(0, 1).  Draw order A, B,
+  sa, sb, bias.
+* MXFP8: A from bf16 N(0, 1) with 1% of entries (seeded uniform mask) x20;
+  B from bf16 N(0, 0.02); both MX-quantized to E4M3 + UE8M0 per 32 along K.
+* MXFP4: A, B from bf16 N(0, 1), MX-quantized to packed E2M1 + UE8M0.
+* FP8 per-token x per-channel: A N(0, 1), W N(0, 0.02); per-row scale
+  s = amax/448 (1 for an all-zero row), q = E4M3(x / s).
+
+Every generator is a pure function of (shape, seed).
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import numpy as np
+
+FMT_MXFP8_E4M3 = 1
+FMT_MXFP4_E2M1 = 2
+
+_ROW_CHUNK = 2048  # rows drawn per chunk; part of the recipe (fixes the stream order)
+
+
+# ----------------------------------------------------------------------------
+# input-side encoders
+# ----------------------------------------------------------------------------
+
+def to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """float32 -> bf16 bit patterns, round to nearest even (finite inputs)."""
+    u = np.ascontiguousarray(x, np.float32).view(np.uint32).astype(np.uint64)
+    u = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    return u.astype(np.uint16)
+
+
+def from_bf16_bits(b: np.ndarray) -> np.ndarray:
+    return (np.asarray(b, np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+def encode_e4m3(q: np.ndarray) -> np.ndarray:
+    """Round to the nearest E4M3FN value (ties to even), saturating at 448."""
+    q = np.asarray(q, np.float64)
+    sign = np.signbit(q).astype(np.uint8)
+    a = np.minimum(np.abs(q), 448.0)
+    _, e = np.frexp(a)
+    ex = np.maximum(e - 1, -6)                   # binade exponent, subnormals share -6
+    quantum = np.ldexp(1.0, ex - 3)              # 3 mantissa bits
+    r = np.rint(a / quantum) * quantum
+    _, e2 = np.frexp(r)
+    er = e2 - 1
+    normal = r >= 2.0 ** -6
+    exp_field = np.where(normal, er + 7, 0).astype(np.int64)
+    man_field = np.where(normal, np.rint((r / np.ldexp(1.0, er) - 1.0) * 8.0),
+                         np.rint(r / 2.0 ** -9)).astype(np.int64)
+    return ((sign.astype(np.int64) << 7) | (exp_field << 3) | man_field).astype(np.uint8)
+
+
+def encode_e2m1(q: np.ndarray) -> np.ndarray:
+    """Round to the nearest E2M1 value (ties to even), saturating at 6; one code per byte."""
+    q = np.asarray(q, np.float64)
+    sign = np.signbit(q).astype(np.int64)
+    a = np.minimum(np.abs(q), 6.0)
+    _, e = np.frexp(a)
+    ex = np.maximum(e - 1, 0)
+    quantum = np.ldexp(1.0, ex - 1)              # 1 mantissa bit
+    r = np.rint(a / quantum) * quantum
+    _, e2 = np.frexp(r)
+    er = e2 - 1
+    normal = r >= 1.0
+    exp_field = np.where(normal, er + 1, 0).astype(np.int64)
+    man_field = np.where(normal, np.rint((r / np.ldexp(1.0, er) - 1.0) * 2.0),
+                         np.rint(r / 0.5)).astype(np.int64)
+    return ((sign << 3) | (exp_field << 1) | man_field).astype(np.uint8)
+
+
+def pack_e2m1(codes: np.ndarray) -> np.ndarray:
+    """[rows, K] nibble codes -> [rows, K/2] bytes; element 2i in the low nibble."""
+    codes = np.asarray(codes, np.uint8)
+    return (codes[:, 0::2] & 0xF) | ((codes[:, 1::2] & 0xF) << 4)
+
+
+def unpack_e2m1(packed: np.ndarray) -> np.ndarray:
+    packed = np.asarray(packed, np.uint8)
+    out = np.empty((packed.shape[0], packed.shape[1] * 2), np.uint8)
+    out[:, 0::2] = packed & 0xF
+    out[:, 1::2] = packed >> 4
+    return out
+
+
+def mx_quantize(x: np.ndarray, fmt: int):
+    """MX-quantize [rows, K] reals along K in blocks of 32.
+
+    Returns (operand bytes, scale bytes [rows, K/32]).  Shared exponent
+    floor(log2(amax)) - emax (8 for E4M3, 2 for E2M1) clamped to [-127, 127],
+    code 0 for an all-zero block; elements x / 2^s rounded to nearest even
+    and saturated.  MXFP4 operands come back packed two per byte.
+    """
+    x = np.asarray(x, np.float64)
+    rows, K = x.shape
+    if K % 32:
+        raise ValueError("K must be a multiple of 32")
+    blk = x.reshape(rows, K // 32, 32)
+    amax = np.abs(blk).max(axis=2)
+    _, e = np.frexp(amax)
+    emax = 8 if fmt == FMT_MXFP8_E4M3 else 2
+    sexp = np.clip(e - 1 - emax, -127, 127)
+    sexp = np.where(amax == 0.0, -127, sexp)
+    q = np.ldexp(blk, -sexp[:, :, None]).reshape(rows, K)
+    if fmt == FMT_MXFP8_E4M3:
+        codes = encode_e4m3(q)
+    else:
+        codes = pack_e2m1(encode_e2m1(q))
+    return codes, (sexp + 127).astype(np.uint8)
+
+
+def ptpc_quantize(x: np.ndarray):
+    """Per-row E4M3 quantization with scale amax/448 (1 for an all-zero row)."""
+    x = np.asarray(x, np.float32)
+    amax = np.abs(x).max(axis=1)
+    s = (amax / np.float32(448.0)).astype(np.float32)
+    s = np.where(amax == 0, np.float32(1.0), s).astype(np.float32)
+    q = (x / s[:, None]).astype(np.float32)
+    return encode_e4m3(q), s
+
+
+# ----------------------------------------------------------------------------
+# workloads
+# ----------------------------------------------------------------------------
+
+@dataclass
+class Int8Problem:
+    A: np.ndarray      # int8 [M, K]
+    B: np.ndarray      # int8 [N, K]
+    sa: np.ndarray     # fp32 [M]
+    sb: np.ndarray     # fp32 [N]
+    bias: np.ndarray | None  # bf16 bits [N]
+    M: int
+    N: int
+    K: int
+
+
+@dataclass
+class Fp8Problem:
+    A: np.ndarray      # e4m3 bytes [M, K]
+    B: np.ndarray      # e4m3 bytes [N, K]
+    sa: np.ndarray
+    sb: np.ndarray
+    bias: np.ndarray | None
+    M: int
+    N: int
+    K: int
+
+
+@dataclass
+class MxProblem:
+    fmt: int
+    A: np.ndarray      # [M, K] (MXFP8) or [M, K/2] (MXFP4) bytes
+    sA: np.ndarray     # ue8m0 [M, K/32]
+    B: np.ndarray
+    sB: np.ndarray
+    bias: np.ndarray | None
+    M: int
+    N: int
+    K: int
+
+
+def _normal_rows(rng, rows, K, std, fn):
+    """Draw [rows, K] N(0, std^2) in fixed row chunks, rounded to bf16, then fn(chunk)."""
+    outs = []
+    for r0 in range(0, rows, _ROW_CHUNK):
+        r = min(_ROW_CHUNK, rows - r0)
+        x = rng.standard_normal((r, K), dtype=np.float32)
+        if std != 1.0:
+            x *= np.float32(std)
+        outs.append(fn(x))
+    return outs
+
+
+def int8_problem(M: int, N: int, K: int, seed: int = 0, bias: bool = True) -> Int8Problem:
+    rng = np.random.default_rng(seed)
+    A = rng.integers(-127, 128, size=(M, K), dtype=np.int8)
+    B = rng.integers(-127, 128, size=(N, K), dtype=np.int8)
+    sa = rng.uniform(1e-3, 1e-2, size=M).astype(np.float32)
+    sb = rng.uniform(1e-3, 1e-2, size=N).astype(np.float32)
+    bb = to_bf16_bits(rng.standard_normal(N).astype(np.float32))
+    return Int8Problem(A, B, sa, sb, bb if bias else None, M, N, K)
+
+
+def mx_problem(fmt: int, M: int, N: int, K: int, seed: int = 0, bias: bool = False) -> MxProblem:
+    rng = np.random.default_rng(seed)
+
+    def quant(x):
+        return mx_quantize(from_bf16_bits(to_bf16_bits(x)), fmt)
+
+    if fmt == FMT_MXFP8_E4M3:
+        def a_chunk(x):
+            mask = rng.uniform(size=x.shape) < 0.01
+            x[mask] *= np.float32(20.0)
+            return quant(x)
+        a_parts = _normal_rows(rng, M, K, 1.0, a_chunk)
+        b_parts = _normal_rows(rng, N, K, 0.02, quant)
+    elif fmt == FMT_MXFP4_E2M1:
+        a_parts = _normal_rows(rng, M, K, 1.0, quant)
+        b_parts = _normal_rows(rng, N, K, 1.0, quant)
+    else:
+        raise ValueError("unknown MX format")
+    A = np.concatenate([p[0] for p in a_parts]) if a_parts else np.zeros((0, K), np.uint8)
+    sA = np.concatenate([p[1] for p in a_parts]) if a_parts else np.zeros((0, K // 32), np.uint8)
+    B = np.concatenate([p[0] for p in b_parts])
+    sB = np.concatenate([p[1] for p in b_parts])
+    bb = to_bf16_bits(rng.standard_normal(N).astype(np.float32)) if bias else None
+    return MxProblem(fmt, A, sA, B, sB, bb, M, N, K)
+
+
+def fp8_problem(M: int, N: int, K: int, seed: int = 0, bias: bool = False) -> Fp8Problem:
+    rng = np.random.default_rng(seed)
+    a_parts = _normal_rows(rng, M, K, 1.0, ptpc_quantize)
+    b_parts = _normal_rows(rng, N, K, 0.02, ptpc_quantize)
+    A = np.concatenate([p[0] for p in a_parts])
+    sa = np.concatenate([p[1] for p in a_parts]).astype(np.float32)
+    B = np.concatenate([p[0] for p in b_parts])
+    sb = np.concatenate([p[1] for p in b_parts]).astype(np.float32)
+    bb = to_bf16_bits(rng.standard_normal(N).astype(np.float32)) if bias else None
+    return Fp8Problem(A, B, sa, sb, bb, M, N, K)
+
+
+def sample_tiles(M: int, N: int, count: int, seed: int, tile: int = 128):
+    """A seeded sample of output tiles plus every ragged edge tile.
+
+    Returns a list of (m0, m1, n0, n1).  The last row-block and the last
+    column-block are always included (they hold the ragged edges)."""
+    rng = np.random.default_rng(seed + 7919)
+    mt = (M + tile - 1) // tile
+    nt = (N + tile - 1) // tile
+    picks = set()
+    for _ in range(count):
+        picks.add((int(rng.integers(mt)), int(rng.integers(nt))))
+    picks.add((mt - 1, nt - 1))
+    picks.add((mt - 1, int(rng.integers(nt))))
+    picks.add((int(rng.integers(mt)), nt - 1))
+    picks.add((0, 0))
+    out = []
+    for bm, bn in sorted(picks):
+        out.append((bm * tile, min(M, bm * tile + tile), bn * tile, min(N, bn * tile + tile)))
+    return out

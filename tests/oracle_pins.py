@@ -1,0 +1,371 @@
+"""Pins of the CPU oracle to facts outside itself.
+
+Each ``check_*`` takes a loaded oracle library handle and raises
+AssertionError when the oracle disagrees with the fact it pins.  The same
+checks run against the real oracle (test_oracle_pins.py) and against
+deliberately broken copies of it (test_oracle_mutants.py), which shows that a
+plausible mistake anywhere in the oracle fails at least one of them.
+
+What each pin rests on:
+* format anchor values of the OCP MX v1.0 element formats (1.0, largest
+  normal, smallest normal/subnormal, NaN codes, the E2M1 value list),
+  monotonicity and sign symmetry, and PyTorch's independent float8 casts;
+* IEEE bf16 round-to-nearest-even, via PyTorch's float32 -> bfloat16 cast and
+  the classic tie cases;
+* the INT8 contraction against numpy's int64 matmul (a library routine) and
+  against closed forms (identity B, constant extremes, hand-worked sums);
+* the epilogue association (acc*sa)*sb the comfy-kitchen PR #174 update
+  "Keep the cached INT8 epilogue scale order exact" fixes, signed zero
+  without bias (same PR, "Preserve signed zero without INT8 bias"), and
+  exact power-of-two scale invariance;
+* the MX block structure against closed forms (constant elements with
+  per-block scale codes), the exact doubling when every scale code of A
+  grows by one, and a numpy float64 matmul of independently decoded values.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+import qk_inputs
+
+E2M1_OCP_VALUES = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]  # OCP MX v1.0, E2M1 magnitudes
+
+
+def _torch_e4m3(codes):
+    return torch.tensor(np.asarray(codes, np.uint8)).view(torch.float8_e4m3fn).double().numpy()
+
+
+def _torch_ue8m0(codes):
+    return torch.tensor(np.asarray(codes, np.uint8)).view(torch.float8_e8m0fnu).double().numpy()
+
+
+def _torch_bf16_bits(x):
+    return torch.tensor(np.asarray(x, np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def _same_or_both_nan(a, b):
+    a = np.asarray(a, np.float64)
+    b = np.asarray(b, np.float64)
+    return bool(np.all((a == b) | (np.isnan(a) & np.isnan(b))))
+
+
+# ---------------------------------------------------------------- formats
+
+def check_e4m3_decode(lib):
+    d = oracle.decode_e4m3(np.arange(256), lib)
+    assert d[0x38] == 1.0
+    assert d[0x7E] == 448.0
+    assert d[0x08] == 2.0 ** -6
+    assert d[0x01] == 2.0 ** -9
+    assert d[0x07] == 7 * 2.0 ** -9
+    assert d[0x00] == 0.0 and not np.signbit(d[0x00])
+    assert d[0x80] == 0.0 and np.signbit(d[0x80])
+    assert np.isnan(d[0x7F]) and np.isnan(d[0xFF])
+    assert np.sum(np.isnan(d)) == 2
+    pos = d[:0x7F]
+    assert np.all(np.diff(pos) > 0), "codes 0x00..0x7E must increase strictly"
+    assert _same_or_both_nan(d[0x80:], -d[:0x80])
+    assert _same_or_both_nan(d, _torch_e4m3(np.arange(256)))
+
+
+def check_e2m1_decode(lib):
+    d = oracle.decode_e2m1(np.arange(16), lib)
+    assert list(d[:8]) == E2M1_OCP_VALUES
+    assert list(-d[8:]) == E2M1_OCP_VALUES
+    assert np.signbit(d[8])
+
+
+def check_ue8m0_decode(lib):
+    d = oracle.decode_ue8m0(np.arange(256), lib)
+    assert d[127] == 1.0 and d[128] == 2.0 and d[126] == 0.5
+    assert d[0] == 2.0 ** -127 and d[254] == 2.0 ** 127
+    assert np.isnan(d[255])
+    assert _same_or_both_nan(d, _torch_ue8m0(np.arange(256)))
+
+
+def check_bf16_rne(lib):
+    f = lambda bits: np.array([bits], np.uint32).view(np.float32)[0]
+    assert oracle.f32_to_bf16([f(0x3F808000)], lib)[0] == 0x3F80  # tie, even stays
+    assert oracle.f32_to_bf16([f(0x3F818000)], lib)[0] == 0x3F82  # tie, odd rounds up
+    assert oracle.f32_to_bf16([f(0x3F808001)], lib)[0] == 0x3F81
+    assert oracle.f32_to_bf16([f(0x7F7FFFFF)], lib)[0] == 0x7F80  # overflow -> +Inf
+    assert oracle.f32_to_bf16([f(0x80000000)], lib)[0] == 0x8000  # -0 kept
+    nanb = oracle.f32_to_bf16([np.float32(np.nan)], lib)[0]
+    assert (nanb & 0x7F80) == 0x7F80 and (nanb & 0x7F) != 0
+    rng = np.random.default_rng(11)
+    bits = rng.integers(0, 2 ** 32, size=4000, dtype=np.uint64).astype(np.uint32)
+    x = bits.view(np.float32)
+    x = x[np.isfinite(x)]
+    assert np.array_equal(oracle.f32_to_bf16(x, lib), _torch_bf16_bits(x))
+
+
+def check_encoders(lib):
+    # every finite code round-trips
+    for c in range(256):
+        v = oracle.decode_e4m3([c], lib)[0]
+        if not np.isnan(v):
+            assert oracle.encode_e4m3([v], lib)[0] == c
+    for c in range(16):
+        assert oracle.encode_e2m1([oracle.decode_e2m1([c], lib)[0]], lib)[0] == c
+    # ties to even and saturation
+    assert oracle.encode_e4m3([1.0625], lib)[0] == 0x38
+    assert oracle.encode_e4m3([1.1875], lib)[0] == 0x3A
+    assert oracle.encode_e4m3([2.0 ** -10], lib)[0] == 0x00
+    assert oracle.encode_e4m3([15 * 2.0 ** -10], lib)[0] == 0x08
+    assert oracle.encode_e4m3([470.0], lib)[0] == 0x7E
+    assert oracle.encode_e4m3([-1e9], lib)[0] == 0xFE
+    assert list(oracle.encode_e2m1([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, 100.0], lib)) == [0, 2, 2, 4, 4, 6, 6, 7]
+    # agrees with torch's float8_e4m3fn cast inside the finite range
+    rng = np.random.default_rng(5)
+    r = rng.standard_normal(3000) * 40
+    r = r[np.abs(r) < 448]
+    ours = oracle.encode_e4m3(r, lib)
+    theirs = torch.tensor(r).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(ours, theirs)
+
+
+def check_mx_quantize_block(lib):
+    codes, sc = oracle.mx_quantize_block(oracle.FMT_MXFP8_E4M3, np.ones(32), lib)
+    assert sc == 127 - 8 and np.all(codes == 0x78)          # 1.0 * 2^8 = 256
+    codes, sc = oracle.mx_quantize_block(oracle.FMT_MXFP4_E2M1, np.ones(32), lib)
+    assert sc == 127 - 2 and np.all(codes == 0x6)           # 1.0 * 2^2 = 4
+    codes, sc = oracle.mx_quantize_block(oracle.FMT_MXFP8_E4M3, np.zeros(32), lib)
+    assert sc == 0 and np.all(codes == 0)
+    # an independent vectorised encoder (the input generator's) agrees
+    rng = np.random.default_rng(3)
+    for fmt in (oracle.FMT_MXFP8_E4M3, oracle.FMT_MXFP4_E2M1):
+        x = (rng.standard_normal((6, 32)) * np.exp(rng.uniform(-8, 8, (6, 1)))).astype(np.float32)
+        x[0, 5] *= 30.0
+        qc, qs = qk_inputs.mx_quantize(x, fmt)
+        if fmt == oracle.FMT_MXFP4_E2M1:
+            qc = qk_inputs.unpack_e2m1(qc)
+        for r in range(6):
+            c, s = oracle.mx_quantize_block(fmt, x[r], lib)
+            assert s == qs[r, 0]
+            assert np.array_equal(c, qc[r])
+
+
+# ---------------------------------------------------------------- INT8
+
+def check_int8_acc_vs_numpy(lib):
+    rng = np.random.default_rng(21)
+    for (M, N, K) in [(3, 5, 16), (17, 9, 48), (33, 40, 160)]:
+        A = rng.integers(-128, 128, (M, K), dtype=np.int8)
+        B = rng.integers(-128, 128, (N, K), dtype=np.int8)
+        A[0, :] = -128
+        B[0, :] = -128
+        sa = np.ones(M, np.float32)
+        sb = np.ones(N, np.float32)
+        _, acc = oracle.gemm_int8_rowwise(A, B, sa, sb, return_acc=True, lib=lib)
+        ref = A.astype(np.int64) @ B.astype(np.int64).T
+        assert np.array_equal(acc, ref)
+        # sub-region indexing agrees with the full result
+        sub, acc2 = oracle.gemm_int8_rowwise(A, B, sa, sb, m0=1, m1=M, n0=2, n1=N, return_acc=True, lib=lib)
+        assert np.array_equal(acc2, ref[1:, 2:])
+
+
+def check_int8_hand_examples(lib):
+    # (M,N,K) = (1,1,16): 1+2+...+16 = 136, exact in bf16
+    A = np.arange(1, 17, dtype=np.int8).reshape(1, 16)
+    B = np.ones((1, 16), np.int8)
+    out = oracle.gemm_int8_rowwise(A, B, np.ones(1, np.float32), np.ones(1, np.float32), lib=lib)
+    assert out[0, 0] == 0x4308  # 136.0
+    # (2,3,32): rows a0 = +1 x32, a1 = alternating +2,-2; cols b0 = 1s, b1 = k mod 4, b2 = -1 for first 8 else 0
+    a = np.zeros((2, 32), np.int8)
+    a[0] = 1
+    a[1, 0::2] = 2
+    a[1, 1::2] = -2
+    b = np.zeros((3, 32), np.int8)
+    b[0] = 1
+    b[1] = np.arange(32) % 4
+    b[2, :8] = -1
+    # by hand: acc[0] = [32, 48, -8]; acc[1] = [0, 2*(0-1+2-3)*8 = -32, 2*(-1+1)*4 = 0]
+    _, acc = oracle.gemm_int8_rowwise(a, b, np.ones(2, np.float32), np.ones(3, np.float32), return_acc=True, lib=lib)
+    assert acc.tolist() == [[32, 48, -8], [0, -32, 0]]
+
+
+def check_int8_identity_and_extremes(lib):
+    rng = np.random.default_rng(4)
+    K = 64
+    A = rng.integers(-128, 128, (7, K), dtype=np.int8)
+    out = oracle.gemm_int8_rowwise(A, np.eye(K, dtype=np.int8), np.ones(7, np.float32), np.ones(K, np.float32), lib=lib)
+    assert np.array_equal(out, _torch_bf16_bits(A.astype(np.float32)))  # int8 values are exact in bf16
+    A = np.full((2, 1024), -128, np.int8)
+    B = np.full((2, 1024), -128, np.int8)
+    B[1] = 127
+    _, acc = oracle.gemm_int8_rowwise(A, B, np.ones(2, np.float32), np.ones(2, np.float32), return_acc=True, lib=lib)
+    assert acc[0, 0] == 1024 * 16384 and acc[0, 1] == -1024 * 16256
+    # 2^31 does not fit in int32 -> the oracle refuses
+    A = np.full((1, 131072), -128, np.int8)
+    try:
+        oracle.gemm_int8_rowwise(A, A, np.ones(1, np.float32), np.ones(1, np.float32), lib=lib)
+    except ValueError:
+        pass
+    else:
+        raise AssertionError("int32 overflow not reported")
+
+
+def _find_association_witness():
+    """A (acc, sa, sb) with bf16((acc*sa)*sb) != bf16(acc*(sa*sb)) in IEEE fp32."""
+    rng = np.random.default_rng(12345)
+    acc = rng.integers(-2 ** 24, 2 ** 24, 200000).astype(np.float32)
+    sa = rng.uniform(1e-3, 1e-2, 200000).astype(np.float32)
+    sb = rng.uniform(1e-3, 1e-2, 200000).astype(np.float32)
+    left = _torch_bf16_bits((acc * sa) * sb)
+    right = _torch_bf16_bits(acc * (sa * sb))
+    idx = np.nonzero(left != right)[0]
+    assert idx.size > 0
+    return [(int(acc[i]), sa[i], sb[i], left[i], right[i]) for i in idx[:8]]
+
+
+def _int8_rows_for_acc(acc):
+    """One A row and one B row of int8 whose dot product is exactly ``acc``."""
+    mag = abs(int(acc))
+    q, r = divmod(mag, 127)
+    q1, q0 = divmod(q, 127)          # mag = 127*127*q1 + 127*q0 + r
+    K = ((q1 + 2 + 15) // 16) * 16
+    a = np.zeros((1, K), np.int16)
+    b = np.zeros((1, K), np.int16)
+    a[0, :q1] = 127
+    b[0, :q1] = 127
+    a[0, q1], b[0, q1] = 127, q0
+    a[0, q1 + 1], b[0, q1 + 1] = 1, r
+    if acc < 0:
+        b = -b
+    return a.astype(np.int8), b.astype(np.int8)
+
+
+def check_int8_epilogue_order(lib):
+    for acc, sa, sb, left, right in _find_association_witness():
+        a, b = _int8_rows_for_acc(acc)
+        out, got = oracle.gemm_int8_rowwise(a, b, np.array([sa], np.float32), np.array([sb], np.float32),
+                                            return_acc=True, lib=lib)
+        assert got[0, 0] == acc
+        assert out[0, 0] == left and out[0, 0] != right
+
+
+def check_int8_signed_zero(lib):
+    a = np.zeros((1, 16), np.int8)
+    b = np.ones((1, 16), np.int8)
+    out = oracle.gemm_int8_rowwise(a, b, np.array([-0.5], np.float32), np.array([0.25], np.float32), lib=lib)
+    assert out[0, 0] == 0x8000  # 0 * (-0.5) = -0, kept without bias
+    out = oracle.gemm_int8_rowwise(a, b, np.array([-0.5], np.float32), np.array([0.25], np.float32),
+                                   bias=np.array([0x0000], np.uint16), lib=lib)
+    assert out[0, 0] == 0x0000  # -0 + +0 = +0 under round-to-nearest
+    a[0, 0] = -3
+    out = oracle.gemm_int8_rowwise(a, b, np.array([1.0], np.float32), np.array([0.0], np.float32), lib=lib)
+    assert out[0, 0] == 0x8000  # (-3 * 1) * (+0) = -0
+    out = oracle.gemm_int8_rowwise(a, b, np.array([1.0], np.float32), np.array([1.0], np.float32),
+                                   bias=np.array([0x3F80], np.uint16), lib=lib)
+    assert out[0, 0] == _torch_bf16_bits(np.array([-2.0], np.float32))[0]
+
+
+def check_int8_pow2_invariance(lib):
+    p = qk_inputs.int8_problem(24, 40, 96, seed=9, bias=False)
+    base = oracle.gemm_int8_rowwise(p.A, p.B, p.sa, p.sb, lib=lib)
+    for k in (1, 3, -2):
+        out = oracle.gemm_int8_rowwise(p.A, p.B, p.sa * np.float32(2.0 ** k), p.sb, lib=lib)
+        expect = _torch_bf16_bits(qk_inputs.from_bf16_bits(base) * np.float32(2.0 ** k))
+        assert np.array_equal(out, expect)
+    # bias is added to the scaled product of row m and column n
+    bias = qk_inputs.to_bf16_bits(np.linspace(-3, 3, 40).astype(np.float32))
+    out = oracle.gemm_int8_rowwise(p.A, p.B, p.sa, p.sb, bias=bias, lib=lib)
+    zero = oracle.gemm_int8_rowwise(np.zeros_like(p.A), p.B, p.sa, p.sb, bias=bias, lib=lib)
+    assert np.array_equal(zero, np.broadcast_to(bias, zero.shape))
+    assert not np.array_equal(out, base)
+
+
+# ---------------------------------------------------------------- FP8 per-token x per-channel
+
+def check_fp8_vs_numpy(lib):
+    rng = np.random.default_rng(31)
+    M, N, K = 9, 13, 96
+    A = rng.integers(0, 256, (M, K), dtype=np.uint8)
+    B = rng.integers(0, 256, (N, K), dtype=np.uint8)
+    A[(A & 0x7F) == 0x7F] = 0x11  # no NaN codes
+    B[(B & 0x7F) == 0x7F] = 0x22
+    sa = rng.uniform(0.5, 2, M).astype(np.float32)
+    sb = rng.uniform(0.5, 2, N).astype(np.float32)
+    bias = qk_inputs.to_bf16_bits(rng.standard_normal(N).astype(np.float32))
+    ref = oracle.gemm_fp8_rowwise(A, B, sa, sb, bias=bias, lib=lib)
+    acc = _torch_e4m3(A) @ _torch_e4m3(B).T  # exact: every partial sum fits in 53 bits
+    expect = acc * sa.astype(np.float64)[:, None] * sb.astype(np.float64)[None, :] \
+        + qk_inputs.from_bf16_bits(bias).astype(np.float64)[None, :]
+    assert np.allclose(ref, expect, rtol=1e-15, atol=1e-12)
+    sub = oracle.gemm_fp8_rowwise(A, B, sa, sb, bias=bias, m0=2, m1=7, n0=3, n1=13, lib=lib)
+    assert np.array_equal(sub, ref[2:7, 3:13])
+
+
+# ---------------------------------------------------------------- MX
+
+def _mx_ones(fmt, M, N, K):
+    one = 0x38 if fmt == oracle.FMT_MXFP8_E4M3 else 0x2
+    if fmt == oracle.FMT_MXFP8_E4M3:
+        A = np.full((M, K), one, np.uint8)
+        B = np.full((N, K), one, np.uint8)
+    else:
+        A = np.full((M, K // 2), one | (one << 4), np.uint8)
+        B = np.full((N, K // 2), one | (one << 4), np.uint8)
+    return A, B
+
+
+def check_mx_block_structure(lib):
+    for fmt in (oracle.FMT_MXFP8_E4M3, oracle.FMT_MXFP4_E2M1):
+        M, N, K = 3, 4, 256
+        A, B = _mx_ones(fmt, M, N, K)
+        nb = K // 32
+        delta_a = np.arange(M)[:, None] * 2 + np.arange(nb)[None, :] - 3     # per row, per block
+        delta_b = (np.arange(N)[:, None] - np.arange(nb)[None, :] % 3)       # per column, per block
+        sA = (127 + delta_a).astype(np.uint8)
+        sB = (127 + delta_b).astype(np.uint8)
+        ref = oracle.gemm_mx(fmt, A, sA, B, sB, lib=lib)
+        expect = np.zeros((M, N))
+        for m in range(M):
+            for n in range(N):
+                expect[m, n] = sum(32.0 * 2.0 ** (delta_a[m, b] + delta_b[n, b]) for b in range(nb))
+        assert np.array_equal(ref, expect)
+
+
+def check_mx_scale_doubling(lib):
+    for fmt in (oracle.FMT_MXFP8_E4M3, oracle.FMT_MXFP4_E2M1):
+        p = qk_inputs.mx_problem(fmt, 8, 12, 128, seed=2)
+        base = oracle.gemm_mx(fmt, p.A, p.sA, p.B, p.sB, lib=lib)
+        up = oracle.gemm_mx(fmt, p.A, p.sA + 1, p.B, p.sB, lib=lib)
+        assert np.array_equal(up, 2.0 * base)
+
+
+def _dequant(fmt, X, sX, K):
+    if fmt == oracle.FMT_MXFP8_E4M3:
+        v = _torch_e4m3(X)
+    else:
+        v = np.asarray(E2M1_OCP_VALUES * 2)[qk_inputs.unpack_e2m1(X)]
+        v = np.where(qk_inputs.unpack_e2m1(X) >= 8, -v, v)
+    return v * np.repeat(_torch_ue8m0(sX), 32, axis=1)
+
+
+def check_mx_vs_numpy(lib):
+    for fmt in (oracle.FMT_MXFP8_E4M3, oracle.FMT_MXFP4_E2M1):
+        p = qk_inputs.mx_problem(fmt, 10, 14, 192, seed=8, bias=True)
+        ref = oracle.gemm_mx(fmt, p.A, p.sA, p.B, p.sB, bias=p.bias, lib=lib)
+        expect = _dequant(fmt, p.A, p.sA, p.K) @ _dequant(fmt, p.B, p.sB, p.K).T \
+            + qk_inputs.from_bf16_bits(p.bias).astype(np.float64)[None, :]
+        assert np.allclose(ref, expect, rtol=1e-14, atol=1e-14)
+        # nibble order: element 2i is the low nibble (0x21 -> 0.5 then 1.0)
+    A = np.zeros((1, 16), np.uint8)
+    A[0, 0] = 0x21
+    B = np.zeros((1, 16), np.uint8)
+    B[0, 0] = 0x02   # element 0 = 1.0, element 1 = 0
+    ref = oracle.gemm_mx(oracle.FMT_MXFP4_E2M1, A, np.full((1, 1), 127, np.uint8), B,
+                         np.full((1, 1), 127, np.uint8), lib=lib)
+    assert ref[0, 0] == 0.5
+
+
+ALL_CHECKS = [
+    check_e4m3_decode, check_e2m1_decode, check_ue8m0_decode, check_bf16_rne, check_encoders,
+    check_mx_quantize_block, check_int8_acc_vs_numpy, check_int8_hand_examples,
+    check_int8_identity_and_extremes, check_int8_epilogue_order, check_int8_signed_zero,
+    check_int8_pow2_invariance, check_fp8_vs_numpy, check_mx_block_structure,
+    check_mx_scale_doubling, check_mx_vs_numpy,
+]

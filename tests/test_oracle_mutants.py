@@ -1,0 +1,72 @@
+"""Planted mistakes in the oracle must fail at least one pin (CPU only).
+
+Each mutant is a copy of oracle/qk_oracle.c with one plausible slip (a wrong
+bias, a dropped term, a swapped index, a transposed operand, the other
+epilogue association ...), compiled to a temporary library.  The pins of
+oracle_pins.py run against it; at least one must fail.
+
+The E2M1 nibble order is deliberately not among them: swapping it in both
+operands permutes element pairs inside one 32-element block, which leaves
+every GEMM result unchanged, so no GEMM-level pin can (or needs to) see it.
+"""
+import os
+import shutil
+import tempfile
+
+import pytest
+
+import oracle
+from oracle_pins import ALL_CHECKS
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "qk_oracle.c")
+
+MUTANTS = {
+    "epilogue_association": ("x = x * sa[m];\n      x = x * sb[n];", "x = x * (sa[m] * sb[n]);"),
+    "int8_bias_dropped": ("if (bias) x = x + qko_bf16_to_f32(bias[n]);", "(void)bias;"),
+    "int8_transposed_B": ("acc += (int64_t)a[k] * (int64_t)b[k];", "acc += (int64_t)a[k] * (int64_t)B[k * N + n];"),
+    "int8_range_check_dropped": ("if (acc > INT32_MAX || acc < INT32_MIN) bad = 1;", ""),
+    "e4m3_exponent_bias": ("mag = ldexp(1.0 + (double)m / 8.0, (int)e - 7);", "mag = ldexp(1.0 + (double)m / 8.0, (int)e - 8);"),
+    "e4m3_subnormal": ("mag = ldexp((double)m / 8.0, 1 - 7);", "mag = ldexp((double)m / 8.0, 0 - 7);"),
+    "e4m3_no_nan": ("if (e == 15u && m == 7u) return NAN;", ""),
+    "e2m1_exponent_bias": ("mag = ldexp(1.0 + (double)m / 2.0, (int)e - 1);", "mag = ldexp(1.0 + (double)m / 2.0, (int)e - 2);"),
+    "ue8m0_bias": ("return ldexp(1.0, (int)code - 127);", "return ldexp(1.0, (int)code - 128);"),
+    "bf16_truncates": ("u += 0x7fffu + lsb;", "(void)lsb;"),
+    "fp4_decoded_as_e4m3": ("return g_e2m1[nib];", "return g_e4m3[nib];"),
+    "mx_block_index_dropped": ("g_ue8m0[sB[n * kb + blk]]", "g_ue8m0[sB[n * kb]]"),
+    "mx_b_scale_dropped": ("acc += g_ue8m0[sA[m * kb + blk]] * g_ue8m0[sB[n * kb + blk]] * inner;",
+                           "acc += g_ue8m0[sA[m * kb + blk]] * inner;"),
+    "fp8_wrong_column_scale": ("double x = acc * (double)sa[m] * (double)sb[n];",
+                               "double x = acc * (double)sa[m] * (double)sb[m % N];"),
+    "fp8_bias_sign": ("if (bias) x += (double)qko_bf16_to_f32(bias[n]);", "if (bias) x -= (double)qko_bf16_to_f32(bias[n]);"),
+    "encoder_ties_away": ("(err == best_err && (c & 1u) == 0u)", "(err == best_err && c > best)"),
+    "mx_emax": ("int emax = (fmt == QKO_FMT_MXFP8_E4M3) ? 8 : 2;", "int emax = (fmt == QKO_FMT_MXFP8_E4M3) ? 7 : 2;"),
+}
+
+
+@pytest.fixture(scope="module")
+def mutant_dir():
+    d = tempfile.mkdtemp(prefix="qk_oracle_mutants_")
+    yield d
+    shutil.rmtree(d, ignore_errors=True)
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_planted_mistake_is_caught(name, mutant_dir):
+    old, new = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation anchor for {name} not found exactly once"
+    msrc = os.path.join(mutant_dir, f"{name}.c")
+    with open(msrc, "w") as f:
+        f.write(src.replace(old, new))
+    lib_path = os.path.join(mutant_dir, f"lib{name}.so")
+    import subprocess
+    subprocess.run(["gcc", "-O2", "-fopenmp", "-ffp-contract=off", "-std=c99", "-shared", "-fPIC",
+                    "-o", lib_path, msrc, "-lm"], check=True)
+    lib = oracle.load(lib_path)
+    failures = []
+    for check in ALL_CHECKS:
+        try:
+            check(lib)
+        except (AssertionError, ValueError):
+            failures.append(check.__name__)
+    assert failures, f"mutant {name} passed every pin"
