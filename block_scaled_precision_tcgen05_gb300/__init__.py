@@ -1,0 +1,221 @@
+"""Block-scaled / quantized GEMM for GB300 (sm_103a).
+
+Python binding of ``libqk.so`` (C ABI declared in ``include/qk.h``).  This
+module only marshals arguments: shape/dtype/device checks, raw pointers and
+the current CUDA stream.  Every step of the GEMM runs in the library's CUDA
+kernels; there is no CPU or PyTorch fallback, and every call fails loudly when
+the library has not been built.
+
+    out = gemm_int8_rowwise(A, B, sa, sb, bias=None, out=None)
+    out = gemm_fp8_rowwise(A, B, sa, sb, bias=None, out=None)
+    out = gemm_mx(fmt, A, sA, B, sB, bias=None, out=None)
+
+Operands follow the ABI: A [M, K] and B [N, K] K-major (MXFP4: [rows, K/2]
+packed bytes), out [M, N] bf16.  E4M3/E2M1/UE8M0 bytes are passed as uint8
+tensors.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from .build import LIB as LIB_PATH
+
+QK_OK = 0
+QK_ERR_ARG = 1
+QK_ERR_ALIGN = 2
+QK_ERR_RANGE = 3
+QK_ERR_ARCH = 4
+QK_ERR_CUDA = 5
+QK_ERR_TIMEOUT = 6
+QK_ERR_NOMEM = 7
+
+FMT_MXFP8_E4M3 = 1
+FMT_MXFP4_E2M1 = 2
+
+# every symbol include/qk.h declares
+EXPORTS = (
+    "qk_gemm_int8_rowwise",
+    "qk_gemm_mx",
+    "qk_gemm_fp8_rowwise",
+    "qk_status_string",
+    "qk_device_status",
+    "qk_set_wait_timeout_ns",
+    "qk_wait_timeout_probe",
+    "qk_launch_count",
+    "qk_release",
+    "qk_version",
+)
+
+
+class QkError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(msg)
+        self.status = status
+
+
+_lib = None
+
+
+def _declare(lib):
+    c = ctypes
+    P = c.c_void_p
+    i64 = c.c_int64
+    lib.qk_gemm_int8_rowwise.argtypes = [P, P, P, P, P, P, i64, i64, i64, P]
+    lib.qk_gemm_int8_rowwise.restype = c.c_int
+    lib.qk_gemm_fp8_rowwise.argtypes = [P, P, P, P, P, P, i64, i64, i64, P]
+    lib.qk_gemm_fp8_rowwise.restype = c.c_int
+    lib.qk_gemm_mx.argtypes = [c.c_int, P, P, P, P, P, P, i64, i64, i64, P]
+    lib.qk_gemm_mx.restype = c.c_int
+    lib.qk_status_string.argtypes = [c.c_int]
+    lib.qk_status_string.restype = c.c_char_p
+    lib.qk_device_status.argtypes = [c.POINTER(c.c_uint64), c.c_int]
+    lib.qk_device_status.restype = c.c_int
+    lib.qk_set_wait_timeout_ns.argtypes = [c.c_uint64]
+    lib.qk_set_wait_timeout_ns.restype = None
+    lib.qk_wait_timeout_probe.argtypes = [c.c_uint64, P]
+    lib.qk_wait_timeout_probe.restype = c.c_int
+    lib.qk_launch_count.argtypes = []
+    lib.qk_launch_count.restype = c.c_uint64
+    lib.qk_release.argtypes = []
+    lib.qk_release.restype = c.c_int
+    lib.qk_version.argtypes = []
+    lib.qk_version.restype = c.c_int
+
+
+def load_library(path: str | None = None):
+    """The ctypes handle of libqk.so; raises if the library was never built."""
+    global _lib
+    if path is not None:
+        lib = ctypes.CDLL(path)
+        _declare(lib)
+        return lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build it with block_scaled_precision_tcgen05_gb300.build.build(); "
+                "there is no fallback implementation")
+        lib = ctypes.CDLL(LIB_PATH)
+        _declare(lib)
+        _lib = lib
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return load_library().qk_status_string(int(status)).decode()
+
+
+def check(status: int) -> None:
+    if status != QK_OK:
+        raise QkError(status, status_string(status))
+
+
+def _stream_handle(device):
+    import torch
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _expect(t, name, dtype, shape, device):
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise ValueError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must have dtype {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if t.device != device:
+        raise ValueError(f"{name} must be on {device}, got {t.device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _out(out, M, N, device):
+    import torch
+    if out is None:
+        return torch.empty((M, N), dtype=torch.bfloat16, device=device)
+    _expect(out, "out", torch.bfloat16, (M, N), device)
+    return out
+
+
+def gemm_int8_rowwise(A, B, sa, sb, bias=None, out=None):
+    """out = bf16(((float)(A @ B^T) * sa[:, None]) * sb[None, :] (+ bias)), bit-exact."""
+    import torch
+    if A.dim() != 2 or B.dim() != 2:
+        raise ValueError("A and B must be 2-D")
+    M, K = A.shape
+    N = B.shape[0]
+    dev = A.device
+    if dev.type != "cuda":
+        raise ValueError("operands must be CUDA tensors")
+    _expect(A, "A", torch.int8, (M, K), dev)
+    _expect(B, "B", torch.int8, (N, K), dev)
+    _expect(sa, "sa", torch.float32, (M,), dev)
+    _expect(sb, "sb", torch.float32, (N,), dev)
+    if bias is not None:
+        _expect(bias, "bias", torch.bfloat16, (N,), dev)
+    out = _out(out, M, N, dev)
+    check(load_library().qk_gemm_int8_rowwise(_ptr(A), _ptr(B), _ptr(sa), _ptr(sb), _ptr(bias), _ptr(out),
+                                              M, N, K, _stream_handle(dev)))
+    return out
+
+
+def gemm_fp8_rowwise(A, B, sa, sb, bias=None, out=None):
+    """FP8 E4M3 GEMM with per-token sa[M] and per-channel sb[N] fp32 scales (uint8 E4M3 bytes in)."""
+    import torch
+    M, K = A.shape
+    N = B.shape[0]
+    dev = A.device
+    if dev.type != "cuda":
+        raise ValueError("operands must be CUDA tensors")
+    _expect(A, "A", torch.uint8, (M, K), dev)
+    _expect(B, "B", torch.uint8, (N, K), dev)
+    _expect(sa, "sa", torch.float32, (M,), dev)
+    _expect(sb, "sb", torch.float32, (N,), dev)
+    if bias is not None:
+        _expect(bias, "bias", torch.bfloat16, (N,), dev)
+    out = _out(out, M, N, dev)
+    check(load_library().qk_gemm_fp8_rowwise(_ptr(A), _ptr(B), _ptr(sa), _ptr(sb), _ptr(bias), _ptr(out),
+                                             M, N, K, _stream_handle(dev)))
+    return out
+
+
+def gemm_mx(fmt, A, sA, B, sB, bias=None, out=None):
+    """MX block-scaled GEMM.  fmt FMT_MXFP8_E4M3 ([rows, K] bytes) or FMT_MXFP4_E2M1 ([rows, K/2] bytes);
+    sA [M, K/32], sB [N, K/32] raw UE8M0 bytes."""
+    import torch
+    if fmt not in (FMT_MXFP8_E4M3, FMT_MXFP4_E2M1):
+        raise ValueError("unknown MX format")
+    M, kbytes = A.shape
+    N = B.shape[0]
+    K = kbytes * (2 if fmt == FMT_MXFP4_E2M1 else 1)
+    dev = A.device
+    if dev.type != "cuda":
+        raise ValueError("operands must be CUDA tensors")
+    _expect(A, "A", torch.uint8, (M, kbytes), dev)
+    _expect(B, "B", torch.uint8, (N, kbytes), dev)
+    _expect(sA, "sA", torch.uint8, (M, K // 32), dev)
+    _expect(sB, "sB", torch.uint8, (N, K // 32), dev)
+    if bias is not None:
+        _expect(bias, "bias", torch.bfloat16, (N,), dev)
+    out = _out(out, M, N, dev)
+    check(load_library().qk_gemm_mx(int(fmt), _ptr(A), _ptr(sA), _ptr(B), _ptr(sB), _ptr(bias), _ptr(out),
+                                    M, N, K, _stream_handle(dev)))
+    return out
+
+
+def device_status(clear: bool = True) -> int:
+    w = ctypes.c_uint64(0)
+    check(load_library().qk_device_status(ctypes.byref(w), 1 if clear else 0))
+    return int(w.value)
+
+
+def set_wait_timeout_ns(ns: int) -> None:
+    load_library().qk_set_wait_timeout_ns(int(ns))
+
+
+def launch_count() -> int:
+    return int(load_library().qk_launch_count())

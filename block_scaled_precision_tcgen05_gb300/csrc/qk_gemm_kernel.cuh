@@ -1,0 +1,537 @@
+// qk_gemm_kernel.cuh -- the persistent, warp-specialised tcgen05 GEMM
+//
+//     out[m,n] = bf16( epilogue( sum_k A[m,k] * B[n,k] ) )
+//
+// A [M,K] and B [N,K] are K-major.  One CTA per SM walks output tiles of
+// 128 x BN in a grouped-M raster.  Roles (256 threads):
+//   warp 0      TMA producer: A/B tiles of 128-byte K rows into a STAGES-deep
+//               shared-memory ring (128-byte swizzle).
+//   warp 1      MMA issuer: allocates TMEM, copies stage scale factors to TMEM
+//               (MX kinds), issues tcgen05.mma into a TMEM accumulator and
+//               releases ring slots / accumulators with tcgen05.commit.
+//   warp 2      scale stager (MX kinds): reads the raw row-major UE8M0 bytes
+//               and writes them into the shared-memory order tcgen05.cp wants.
+//   warps 4..7  epilogue: TMEM -> registers, fixed-order scale/bias epilogue,
+//               round-to-nearest-even bf16, stores; warp 4+q owns TMEM lanes
+//               32q..32q+31, i.e. tile rows 32q..32q+31.
+//
+// Kinds:
+//   F16   exact INT8: int8 operands converted to f16 beforehand (exact), f16
+//         MMA with fp32 accumulation.  Accumulation restarts every chunk of
+//         at most 1024 K (every partial sum is then an integer below 2^24,
+//         exact in fp32); the epilogue drains each chunk to int32 and adds
+//         them in a TMEM-resident int32 sum, so the result is the exact
+//         integer dot product.
+//   F8    E4M3 x E4M3 with fp32 accumulation (per-token x per-channel FP8).
+//   MXF8  E4M3 with one UE8M0 scale per 32 K (block_scale, scale_vec::1X).
+//   MXF4  packed E2M1 with one UE8M0 scale per 32 K (kind::mxf4, 2X).
+//
+// Epilogue order (comfy-kitchen PR #174, Summary and the update "Keep the
+// cached INT8 epilogue scale order exact"): x = float(acc); x = x*sa[m];
+// x = x*sb[n]; if bias: x = x + float(bias[n]); out = bf16_rne(x).  Without
+// bias no add happens, so a -0 survives ("Preserve signed zero without INT8
+// bias").  MX kinds: out = bf16_rne(acc (+ bias)).
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include "qk_device.cuh"
+
+namespace qk {
+
+enum class Kind : int { F16 = 0, F8 = 1, MXF8 = 2, MXF4 = 3 };
+
+struct GemmParams {
+  int M, N, K;
+  int num_kb;                 // k-blocks (ring stages) per tile
+  int num_m_blocks, num_n_blocks, num_tiles;
+  int chunk_kb;               // k-blocks per exact accumulation chunk (F16); == num_kb otherwise
+  int num_chunks;             // ceil(num_kb / chunk_kb)
+  const float* sa;            // [M] row scales (F16, F8)
+  const float* sb;            // [N] column scales (F16, F8)
+  const uint16_t* bias;       // [N] bf16 bits, nullable
+  uint16_t* out;              // [M, N] bf16 bits
+  const uint8_t* sA;          // [M, sf_cols] UE8M0 (MX)
+  const uint8_t* sB;          // [N, sf_cols] UE8M0 (MX)
+  int sf_cols;                // K / 32
+  unsigned long long* err;    // device error word
+  uint64_t timeout_ns;        // bound on every barrier wait
+};
+
+template <Kind KIND, int BN_, int STAGES_, int ACC_BUFS_>
+struct GemmCfg {
+  static constexpr Kind kind = KIND;
+  static constexpr int BM = 128;
+  static constexpr int BN = BN_;
+  static constexpr int STAGES = STAGES_;
+  static constexpr int ACC_BUFS = ACC_BUFS_;
+  static constexpr int ROW_BYTES = 128;  // bytes of K per row per ring stage (one swizzle row)
+  static constexpr int K_ELEMS = KIND == Kind::F16 ? 64 : (KIND == Kind::MXF4 ? 256 : 128);
+  static constexpr int TMA_K = KIND == Kind::F16 ? 64 : 128;  // tensor-map elements per stage along K
+  static constexpr int UMMA_K = KIND == Kind::F16 ? 16 : (KIND == Kind::MXF4 ? 64 : 32);
+  static constexpr int K_STEPS = K_ELEMS / UMMA_K;  // 4 MMAs of 32 bytes of K each
+  static constexpr bool MX = KIND == Kind::MXF8 || KIND == Kind::MXF4;
+  static constexpr bool INT_CHUNKS = KIND == Kind::F16;
+  static constexpr bool ROWWISE = KIND == Kind::F16 || KIND == Kind::F8;
+
+  static constexpr int SF_PER_STAGE = MX ? K_ELEMS / 32 : 0;  // scale bytes per row per stage
+  static constexpr int SF_ATOMS_K = SF_PER_STAGE / 4;         // 4 scale bytes per 32-bit TMEM column
+  static constexpr int NB128 = (BN + 127) / 128;              // 128-row blocks of the B tile
+  static constexpr int SFA_BYTES = SF_ATOMS_K * 512;
+  static constexpr int SFB_BYTES = SF_ATOMS_K * NB128 * 512;
+  static constexpr int SF_STAGE_BYTES = SFA_BYTES + SFB_BYTES;
+
+  static constexpr int A_BYTES = BM * ROW_BYTES;
+  static constexpr int B_BYTES = BN * ROW_BYTES;
+  static constexpr uint32_t STAGE_TX = A_BYTES + B_BYTES;
+
+  static constexpr int OFF_A = 0;
+  static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
+  static constexpr int OFF_SF = OFF_B + STAGES * B_BYTES;
+  static constexpr int OFF_BAR = OFF_SF + STAGES * SF_STAGE_BYTES;
+  static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC_BUFS + 1;
+  static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
+  static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack to align the base to 1024
+
+  static constexpr int COL_ACC = 0;
+  static constexpr int COL_SUM = ACC_BUFS * BN;
+  static constexpr int COL_SF = COL_SUM + (INT_CHUNKS ? BN : 0);
+  static constexpr int SF_COLS_A = SF_ATOMS_K * 4;
+  static constexpr int SF_COLS_B = SF_ATOMS_K * NB128 * 4;
+  static constexpr int SF_COLS_STAGE = MX ? SF_COLS_A + SF_COLS_B : 0;
+  static constexpr int COLS_USED = COL_SF + STAGES * SF_COLS_STAGE;
+  static constexpr int TMEM_COLS = COLS_USED <= 32    ? 32
+                                   : COLS_USED <= 64  ? 64
+                                   : COLS_USED <= 128 ? 128
+                                   : COLS_USED <= 256 ? 256
+                                                      : 512;
+
+  static constexpr int NUM_THREADS = 256;
+  static constexpr int GROUP_M = 8;
+
+  static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "tile N");
+  static_assert(COLS_USED <= 512, "TMEM budget");
+  static_assert(SMEM_BYTES <= 232448, "shared-memory budget");
+  static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "swizzle atoms need 1024-byte alignment");
+
+  // kind::f16: D fp32 (1), A/B f16 (0).  kind::f8f6f4: A/B E4M3 (0).
+  // kind::mxf8f6f4: E4M3 (0).  kind::mxf4: E2M1 (1).
+  __host__ __device__ static constexpr uint32_t idesc(uint32_t a_sf_id, uint32_t b_sf_id) {
+    return KIND == Kind::F16    ? make_idesc_dense(1, 0, 0, BM, BN)
+           : KIND == Kind::F8   ? make_idesc_dense(1, 0, 0, BM, BN)
+           : KIND == Kind::MXF8 ? make_idesc_block_scaled(0, 0, BM, BN, a_sf_id, b_sf_id)
+                                : make_idesc_block_scaled(1, 1, BM, BN, a_sf_id, b_sf_id);
+  }
+};
+
+template <int GROUP_M>
+__device__ __forceinline__ void tile_coords(const GemmParams& p, int t, int& mb, int& nb) {
+  const int group_tiles = GROUP_M * p.num_n_blocks;
+  const int g = t / group_tiles;
+  const int first_m = g * GROUP_M;
+  const int gm = min(p.num_m_blocks - first_m, GROUP_M);
+  const int local = t - g * group_tiles;
+  mb = first_m + local % gm;
+  nb = local / gm;
+}
+
+// Four consecutive UE8M0 bytes of one scale row, little-endian; zero outside
+// the matrix (the matching operand elements are zero-filled by TMA).
+__device__ __forceinline__ uint32_t load_sf4(const uint8_t* s, int row, int rows, int col, int cols) {
+  if (row >= rows || col >= cols) return 0u;
+  const uint8_t* rp = s + static_cast<size_t>(row) * static_cast<size_t>(cols);
+  if ((cols & 3) == 0) return __ldg(reinterpret_cast<const uint32_t*>(rp + col));
+  uint32_t v = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    if (col + i < cols) v |= static_cast<uint32_t>(__ldg(rp + col + i)) << (8 * i);
+  return v;
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+               : "memory");
+}
+
+__device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
+  return __uint_as_float(static_cast<uint32_t>(b) << 16);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const uint32_t l = __bfloat16_as_ushort(__float2bfloat16_rn(lo));
+  const uint32_t h = __bfloat16_as_ushort(__float2bfloat16_rn(hi));
+  return l | (h << 16);
+}
+
+// Epilogue of 32 consecutive columns [n0, n0+32) of one row m.
+// INT_ACC: v holds int32 sums; otherwise fp32 bit patterns.
+template <bool ROWWISE, bool INT_ACC>
+__device__ __forceinline__ void epilogue_row32(const GemmParams& p, int m, int n0, float sam,
+                                               const uint32_t (&v)[32]) {
+  const bool full = n0 + 32 <= p.N;
+  float sbv[32];
+  float bv[32];
+  const bool has_bias = p.bias != nullptr;
+  if (full) {
+    if constexpr (ROWWISE) {
+      const float4* s4 = reinterpret_cast<const float4*>(p.sb + n0);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float4 t = __ldg(s4 + i);
+        sbv[4 * i + 0] = t.x;
+        sbv[4 * i + 1] = t.y;
+        sbv[4 * i + 2] = t.z;
+        sbv[4 * i + 3] = t.w;
+      }
+    }
+    if (has_bias) {
+      const uint4* b4 = reinterpret_cast<const uint4*>(p.bias + n0);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint4 t = __ldg(b4 + i);
+        const uint32_t w[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          bv[8 * i + 2 * j + 0] = __uint_as_float(w[j] << 16);
+          bv[8 * i + 2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+        }
+      }
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const int n = n0 + i;
+      if constexpr (ROWWISE) sbv[i] = n < p.N ? __ldg(p.sb + n) : 0.f;
+      bv[i] = (has_bias && n < p.N) ? bf16_bits_to_float(__ldg(p.bias + n)) : 0.f;
+    }
+  }
+  uint32_t packed[16];
+#pragma unroll
+  for (int i = 0; i < 32; i += 2) {
+    float x[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      float t = INT_ACC ? __int2float_rn(static_cast<int>(v[i + j])) : __uint_as_float(v[i + j]);
+      if constexpr (ROWWISE) {
+        t = __fmul_rn(t, sam);
+        t = __fmul_rn(t, sbv[i + j]);
+      }
+      if (has_bias) t = __fadd_rn(t, bv[i + j]);
+      x[j] = t;
+    }
+    packed[i / 2] = pack_bf16x2(x[0], x[1]);
+  }
+  uint16_t* dst = p.out + static_cast<size_t>(m) * static_cast<size_t>(p.N) + n0;
+  if (full) {
+    uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) d4[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      if (n0 + 8 * i < p.N)  // N is a multiple of 8
+        reinterpret_cast<uint4*>(dst)[i] =
+            make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+  }
+}
+
+template <class C>
+__global__ void __launch_bounds__(C::NUM_THREADS, 1)
+    qk_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* empty = full + C::STAGES;
+  uint64_t* acc_full = empty + C::STAGES;
+  uint64_t* acc_empty = acc_full + C::ACC_BUFS;
+  uint64_t* drain = acc_empty + C::ACC_BUFS;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_MISC + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+#pragma unroll 1
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&full[s], C::MX ? 2u : 1u);
+      mbar_init(&empty[s], 1u);
+    }
+#pragma unroll 1
+    for (int a = 0; a < C::ACC_BUFS; ++a) {
+      mbar_init(&acc_full[a], 1u);
+      mbar_init(&acc_empty[a], 4u);
+    }
+    mbar_init(drain, 1u);
+    *abort_flag = 0u;
+    fence_mbar_init();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+  const WaitCtl w{abort_flag, p.err, p.timeout_ns};
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      long long issued = 0;
+      bool ok = true;
+#pragma unroll 1
+      for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+        int mb, nb;
+        tile_coords<C::GROUP_M>(p, t, mb, nb);
+#pragma unroll 1
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, w, kSiteProducerEmpty)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[stage], C::STAGE_TX);
+          tma_load_2d(smem + C::OFF_A + stage * C::A_BYTES, &tmA, &full[stage], kb * C::TMA_K, mb * C::BM);
+          tma_load_2d(smem + C::OFF_B + stage * C::B_BYTES, &tmB, &full[stage], kb * C::TMA_K, nb * C::BN);
+          ++issued;
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // Do not leave the CTA with tile loads in flight: wait (bounded) for the
+      // most recent load of every ring slot.
+      const WaitCtl wd{abort_flag, p.err, p.timeout_ns};
+#pragma unroll 1
+      for (long long i = 0; i < (issued < C::STAGES ? issued : C::STAGES); ++i) {
+        const long long L = issued - 1 - i;
+        uint64_t* bar = &full[static_cast<int>(L % C::STAGES)];
+        const uint32_t par = static_cast<uint32_t>((L / C::STAGES) & 1);
+        const uint32_t a = smem_u32(bar);
+        const uint64_t t0 = global_timer_ns();
+        while (!mbar_try_wait(a, par)) {
+          if (global_timer_ns() - t0 > wd.timeout_ns) {
+            report_error(p.err, kDevErrTimeout, kSiteProducerDrain, static_cast<uint32_t>(L));
+            break;
+          }
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t acc_iter = 0;
+      bool ok = true;
+#pragma unroll 1
+      for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+#pragma unroll 1
+        for (int c = 0; ok && c < p.num_chunks; ++c) {
+          const int a = static_cast<int>(acc_iter % C::ACC_BUFS);
+          const uint32_t aph = (acc_iter / C::ACC_BUFS) & 1u;
+          if (!mbar_wait(&acc_empty[a], aph ^ 1u, w, kSiteMmaAccEmpty)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t d_tmem = tmem + static_cast<uint32_t>(C::COL_ACC + a * C::BN);
+          const int kb0 = c * p.chunk_kb;
+          const int kb1 = min(p.num_kb, kb0 + p.chunk_kb);
+#pragma unroll 1
+          for (int kb = kb0; kb < kb1; ++kb) {
+            if (!mbar_wait(&full[stage], phase, w, kSiteMmaFull)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after_sync();
+            const uint32_t sf_tmem = tmem + static_cast<uint32_t>(C::COL_SF + stage * C::SF_COLS_STAGE);
+            if constexpr (C::MX) {
+              const uint32_t sf_smem = smem_u32(smem + C::OFF_SF + stage * C::SF_STAGE_BYTES);
+#pragma unroll
+              for (int i = 0; i < C::SF_ATOMS_K; ++i)
+                tmem_cp_32x128b_warpx4(sf_tmem + 4 * i, make_smem_desc(sf_smem + 512 * i, 128, 128, 0));
+#pragma unroll
+              for (int i = 0; i < C::SF_ATOMS_K * C::NB128; ++i)
+                tmem_cp_32x128b_warpx4(sf_tmem + C::SF_COLS_A + 4 * i,
+                                       make_smem_desc(sf_smem + C::SFA_BYTES + 512 * i, 128, 128, 0));
+            }
+            const uint64_t adesc = make_desc_kmajor_sw128(smem_u32(smem + C::OFF_A + stage * C::A_BYTES));
+            const uint64_t bdesc = make_desc_kmajor_sw128(smem_u32(smem + C::OFF_B + stage * C::B_BYTES));
+            int ksteps = C::K_STEPS;
+            if (kb == p.num_kb - 1) {
+              const int rem = p.K - kb * C::K_ELEMS;
+              ksteps = min(C::K_STEPS, (rem + C::UMMA_K - 1) / C::UMMA_K);
+            }
+#pragma unroll
+            for (int j = 0; j < C::K_STEPS; ++j) {
+              if (j < ksteps) {
+                const uint32_t accum = (kb > kb0 || j > 0) ? 1u : 0u;
+                const uint64_t ad = adesc + static_cast<uint64_t>((j * 32) >> 4);
+                const uint64_t bd = bdesc + static_cast<uint64_t>((j * 32) >> 4);
+                if constexpr (C::kind == Kind::F16) {
+                  umma_f16(d_tmem, ad, bd, C::idesc(0, 0), accum);
+                } else if constexpr (C::kind == Kind::F8) {
+                  umma_f8f6f4(d_tmem, ad, bd, C::idesc(0, 0), accum);
+                } else if constexpr (C::kind == Kind::MXF8) {
+                  // one scale byte per row per MMA: byte j of the stage's column
+                  umma_mxf8f6f4(d_tmem, ad, bd, C::idesc(j, j), sf_tmem, sf_tmem + C::SF_COLS_A, accum);
+                } else {
+                  // two scale bytes per row per MMA: bytes 2(j%2), 2(j%2)+1 of column group j/2
+                  const uint32_t g = static_cast<uint32_t>(j >> 1);
+                  const uint32_t id = static_cast<uint32_t>((j & 1) * 2);
+                  umma_mxf4(d_tmem, ad, bd, C::idesc(id, id), sf_tmem + 4 * g,
+                            sf_tmem + C::SF_COLS_A + 4 * C::NB128 * g, accum);
+                }
+              }
+            }
+            umma_commit(&empty[stage]);
+            if (++stage == C::STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+          if (!ok) break;
+          umma_commit(&acc_full[a]);
+          ++acc_iter;
+        }
+      }
+      // Every MMA and copy this thread issued completes before TMEM is freed.
+      umma_commit(drain);
+      const uint32_t da = smem_u32(drain);
+      const uint64_t t0 = global_timer_ns();
+      while (!mbar_try_wait(da, 0u)) {
+        if (global_timer_ns() - t0 > p.timeout_ns) {
+          report_error(p.err, kDevErrTimeout, kSiteDrain, 0u);
+          break;
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 2) {
+    // ---------------- scale stager (MX) ----------------
+    if constexpr (C::MX) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+#pragma unroll 1
+      for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+        int mb, nb;
+        tile_coords<C::GROUP_M>(p, t, mb, nb);
+#pragma unroll 1
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, w, kSiteScaleEmpty)) {
+            ok = false;
+            break;
+          }
+          const uint32_t sf = smem_u32(smem + C::OFF_SF + stage * C::SF_STAGE_BYTES);
+          const int col0 = kb * C::SF_PER_STAGE;
+          // A atom g: 128 rows x 4 bytes; row r = 32j + lane lives in 16-byte
+          // line `lane`, word j.
+#pragma unroll
+          for (int g = 0; g < C::SF_ATOMS_K; ++g) {
+            uint32_t v[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              v[j] = load_sf4(p.sA, mb * C::BM + 32 * j + lane, p.M, col0 + 4 * g, p.sf_cols);
+            st_shared_v4(sf + 512 * g + 16 * lane, v[0], v[1], v[2], v[3]);
+          }
+#pragma unroll
+          for (int g = 0; g < C::SF_ATOMS_K; ++g) {
+#pragma unroll
+            for (int rb = 0; rb < C::NB128; ++rb) {
+              uint32_t v[4];
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                v[j] = load_sf4(p.sB, nb * C::BN + rb * 128 + 32 * j + lane, p.N, col0 + 4 * g, p.sf_cols);
+              st_shared_v4(sf + C::SFA_BYTES + 512 * (g * C::NB128 + rb) + 16 * lane, v[0], v[1], v[2], v[3]);
+            }
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&full[stage]);
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ---------------- epilogue ----------------
+    const int q = warp - 4;
+    const int r = q * 32 + lane;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16);
+    uint32_t acc_iter = 0;
+    bool ok = true;
+#pragma unroll 1
+    for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+      int mb, nb;
+      tile_coords<C::GROUP_M>(p, t, mb, nb);
+      const int m = mb * C::BM + r;
+      const bool row_ok = m < p.M;
+      float sam = 1.f;
+      if constexpr (C::ROWWISE) sam = row_ok ? __ldg(p.sa + m) : 0.f;
+      const int n_tile = nb * C::BN;
+#pragma unroll 1
+      for (int c = 0; c < p.num_chunks; ++c) {
+        const int a = static_cast<int>(acc_iter % C::ACC_BUFS);
+        const uint32_t aph = (acc_iter / C::ACC_BUFS) & 1u;
+        if (!mbar_wait(&acc_full[a], aph, w, kSiteEpiAccFull)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        const bool last = c == p.num_chunks - 1;
+#pragma unroll 1
+        for (int g = 0; g < C::BN / 32; ++g) {
+          const int n0 = n_tile + 32 * g;
+          uint32_t v[32];
+          tmem_ld_32cols(lane_base + static_cast<uint32_t>(C::COL_ACC + a * C::BN + 32 * g), v);
+          tmem_wait_ld();
+          if constexpr (C::INT_CHUNKS) {
+            // chunk result: an exact integer below 2^24 in magnitude
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = static_cast<uint32_t>(__float2int_rn(__uint_as_float(v[i])));
+            if (c > 0) {
+              uint32_t s[32];
+              tmem_ld_32cols(lane_base + static_cast<uint32_t>(C::COL_SUM + 32 * g), s);
+              tmem_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 32; ++i) v[i] += s[i];
+            }
+            if (!last) {
+              tmem_st_32cols(lane_base + static_cast<uint32_t>(C::COL_SUM + 32 * g), v);
+            } else if (row_ok && n0 < p.N) {
+              epilogue_row32<true, true>(p, m, n0, sam, v);
+            }
+          } else {
+            if (row_ok && n0 < p.N) epilogue_row32<C::ROWWISE, false>(p, m, n0, sam, v);
+          }
+        }
+        if constexpr (C::INT_CHUNKS) tmem_wait_st();
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[a]);
+        ++acc_iter;
+      }
+    }
+    __syncwarp();
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
+}
+
+}  // namespace qk

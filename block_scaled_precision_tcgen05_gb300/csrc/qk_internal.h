@@ -1,0 +1,43 @@
+// qk_internal.h -- host-side plumbing shared by the libqk.so translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "../../include/qk.h"
+
+namespace qk {
+
+struct DeviceInfo {
+  int sm_count = 0;
+  int cc_major = 0;
+  int cc_minor = 0;
+  unsigned long long* err_word = nullptr;  // device address of the status word
+  cudaMemPool_t pool = nullptr;            // stream-ordered workspace pool
+};
+
+// Cached facts about the current device; nullptr and *status set on failure.
+const DeviceInfo* current_device(int* status);
+
+// 2-D tiled tensor map over a row-major [rows, inner] matrix with a 128-byte
+// swizzle and zero fill outside the matrix.  Returns QK_OK or QK_ERR_CUDA.
+int encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t inner, uint64_t rows,
+                   uint64_t row_pitch_bytes, uint32_t box_inner, uint32_t box_rows);
+
+uint64_t wait_timeout_ns();
+void count_launches(uint64_t n);
+
+// Per-format launchers (arguments already validated).
+int launch_int8_rowwise(const int8_t* A, const int8_t* B, const float* sa, const float* sb, const uint16_t* bias,
+                        uint16_t* out, int M, int N, int K, const DeviceInfo& dev, cudaStream_t stream);
+int launch_fp8_rowwise(const uint8_t* A, const uint8_t* B, const float* sa, const float* sb, const uint16_t* bias,
+                       uint16_t* out, int M, int N, int K, const DeviceInfo& dev, cudaStream_t stream);
+int launch_mxfp8(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const uint8_t* sB, const uint16_t* bias,
+                 uint16_t* out, int M, int N, int K, const DeviceInfo& dev, cudaStream_t stream);
+int launch_mxfp4(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const uint8_t* sB, const uint16_t* bias,
+                 uint16_t* out, int M, int N, int K, const DeviceInfo& dev, cudaStream_t stream);
+int launch_wait_probe(uint64_t timeout_ns, const DeviceInfo& dev, cudaStream_t stream);
+
+}  // namespace qk

@@ -1,0 +1,44 @@
+// qk_launch.cuh -- host-side launch of one GEMM kernel configuration.
+#pragma once
+
+#include "qk_gemm_kernel.cuh"
+#include "qk_internal.h"
+
+namespace qk {
+
+inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+// Fills the tile/k-block bookkeeping of GemmParams for configuration C.
+template <class C>
+void plan_tiles(GemmParams& p, int M, int N, int K) {
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.num_kb = ceil_div(K, C::K_ELEMS);
+  p.num_m_blocks = ceil_div(M, C::BM);
+  p.num_n_blocks = ceil_div(N, C::BN);
+  p.num_tiles = p.num_m_blocks * p.num_n_blocks;
+  if (C::INT_CHUNKS) {
+    // 1024 K per chunk: |partial| <= 1024 * 2^14 = 2^24, exact in fp32.
+    p.chunk_kb = 1024 / C::K_ELEMS;
+  } else {
+    p.chunk_kb = p.num_kb;
+  }
+  p.num_chunks = ceil_div(p.num_kb, p.chunk_kb);
+}
+
+template <class C>
+int launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, const DeviceInfo& dev,
+                cudaStream_t stream) {
+  auto kernel = qk_gemm_kernel<C>;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  if (e != cudaSuccess) return QK_ERR_CUDA;
+  const int grid = p.num_tiles < dev.sm_count ? p.num_tiles : dev.sm_count;
+  kernel<<<grid, C::NUM_THREADS, C::SMEM_BYTES, stream>>>(ta, tb, p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return QK_ERR_CUDA;
+  count_launches(1);
+  return QK_OK;
+}
+
+}  // namespace qk

@@ -1,0 +1,31 @@
+// qk_mxfp4.cu -- MXFP4 (packed E2M1 elements, one UE8M0 scale per 32 K) GEMM
+// on tcgen05.mma kind::mxf4.block_scale.scale_vec::2X, which reads the
+// packed 4-bit operands directly (ROCm/FlyDSL PR #990: MXFP4 with per-1x32
+// scales).  Operands are [rows, K/2] bytes, element 2i in the low nibble.
+#include "qk_launch.cuh"
+
+namespace qk {
+
+using CfgMxfp4 = GemmCfg<Kind::MXF4, 256, 4, 1>;
+
+int launch_mxfp4(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const uint8_t* sB, const uint16_t* bias,
+                 uint16_t* out, int M, int N, int K, const DeviceInfo& dev, cudaStream_t stream) {
+  using C = CfgMxfp4;
+  CUtensorMap ta, tb;
+  const uint64_t kb = static_cast<uint64_t>(K) / 2;  // bytes per row
+  int st = encode_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, kb, M, kb, C::TMA_K, C::BM);
+  if (st == QK_OK) st = encode_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, kb, N, kb, C::TMA_K, C::BN);
+  if (st != QK_OK) return st;
+  GemmParams p{};
+  plan_tiles<C>(p, M, N, K);
+  p.bias = bias;
+  p.out = out;
+  p.sA = sA;
+  p.sB = sB;
+  p.sf_cols = K / 32;
+  p.err = dev.err_word;
+  p.timeout_ns = wait_timeout_ns();
+  return launch_gemm<C>(ta, tb, p, dev, stream);
+}
+
+}  // namespace qk

@@ -1,0 +1,30 @@
+// qk_mxfp8.cu -- MXFP8 (E4M3 elements, one UE8M0 scale per 32 K) GEMM on
+// tcgen05.mma kind::mxf8f6f4.block_scale.scale_vec::1X.  The raw row-major
+// [rows, K/32] scale bytes (ROCm/mori PR #806, "What") are staged per ring
+// slot by the kernel's scale warp and moved to TMEM with tcgen05.cp.
+#include "qk_launch.cuh"
+
+namespace qk {
+
+using CfgMxfp8 = GemmCfg<Kind::MXF8, 256, 4, 1>;
+
+int launch_mxfp8(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const uint8_t* sB, const uint16_t* bias,
+                 uint16_t* out, int M, int N, int K, const DeviceInfo& dev, cudaStream_t stream) {
+  using C = CfgMxfp8;
+  CUtensorMap ta, tb;
+  int st = encode_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, K, M, K, C::TMA_K, C::BM);
+  if (st == QK_OK) st = encode_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, K, N, K, C::TMA_K, C::BN);
+  if (st != QK_OK) return st;
+  GemmParams p{};
+  plan_tiles<C>(p, M, N, K);
+  p.bias = bias;
+  p.out = out;
+  p.sA = sA;
+  p.sB = sB;
+  p.sf_cols = K / 32;
+  p.err = dev.err_word;
+  p.timeout_ns = wait_timeout_ns();
+  return launch_gemm<C>(ta, tb, p, dev, stream);
+}
+
+}  // namespace qk

@@ -1,0 +1,162 @@
+/*
+ * qk.h -- C ABI of libqk.so, block-scaled / quantized GEMM on GB300 (sm_103a).
+ *
+ * Every entry point computes
+ *
+ *     out[m, n] = bf16_rne( epilogue( sum_k A[m, k] * B[n, k] ) )
+ *
+ * with A [M, K] and B [N, K] both K-major (row-major, contiguous, leading
+ * dimension = K elements), and out [M, N] row-major bf16 (leading dimension
+ * N).  All pointers are DEVICE pointers owned by the caller; the library never
+ * frees them and keeps no reference to them once the call returns.
+ *
+ * Calls are stream-ordered and asynchronous: they validate their arguments on
+ * the host, enqueue kernels on `stream` (a cudaStream_t; NULL = the legacy
+ * default stream of the current device) and return.  Faults inside the
+ * kernels surface at the caller's next synchronisation; bounded waits inside
+ * the kernels that give up are recorded in a device status word
+ * (qk_device_status).  The device is the current CUDA device.
+ *
+ * bf16 values (bias, out) are passed as their 16-bit patterns (uint16_t).
+ * M == 0 or N == 0 is an empty product: nothing is launched and QK_OK is
+ * returned.  K must be >= 1.
+ *
+ * Sources (web pages, cited by title and section):
+ *  - comfy-kitchen PR #174 "Optimize HIP WMMA INT8 GEMM staging, epilogue,
+ *    and deep-K tiling": Summary, Validation, and the updates "Keep the cached
+ *    INT8 epilogue scale order exact" and "Preserve signed zero without INT8
+ *    bias".
+ *  - ROCm/mori PR #806 "perf(gemm-ar): mxfp8 with row-major scales staged
+ *    through LDS": section "What" (raw row-major ue8m0 scales, any M).
+ *  - ROCm/FlyDSL PR #990 "[fp4_gemm_4wave] MXFP4 GEMM perf optimize":
+ *    MXFP4 with per-1x32 ue8m0 scales.
+ *  - ROCm/aiter PR #6262: "Technical Details" (caller-owned out=, shape and
+ *    dtype checks; FP8 A8W8 GEMM with per-token and per-channel scales).
+ */
+#ifndef QK_H_
+#define QK_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t, passed as an opaque handle. */
+typedef void* qk_stream_t;
+
+/* ---- status codes ------------------------------------------------------- */
+#define QK_OK 0
+#define QK_ERR_ARG 1      /* null required pointer, negative size, K == 0, unknown format */
+#define QK_ERR_ALIGN 2    /* a pointer not 16-byte aligned, N % 8 != 0, or K not a multiple of 16 (32 for MX) */
+#define QK_ERR_RANGE 3    /* INT8: K > 131056, so the int32 accumulator could overflow; sizes beyond 2^31-1 */
+#define QK_ERR_ARCH 4     /* the current device is not compute capability 10.3 (GB300) */
+#define QK_ERR_CUDA 5     /* a CUDA runtime/driver call or a kernel launch failed */
+#define QK_ERR_TIMEOUT 6  /* a bounded wait inside a kernel gave up (see qk_device_status) */
+#define QK_ERR_NOMEM 7    /* the library's stream-ordered workspace could not be allocated */
+
+/* ---- operand formats for qk_gemm_mx ------------------------------------ */
+#define QK_FMT_MXFP8_E4M3 1 /* A, B: one E4M3 byte per element */
+#define QK_FMT_MXFP4_E2M1 2 /* A, B: two E2M1 codes per byte, element 2i in the low nibble */
+
+/*
+ * INT8 GEMM with per-row and per-column fp32 scales and an optional bias.
+ * (comfy-kitchen PR #174, Summary: "cache row/column scales and bias values
+ * in the rowwise epilogue"; update "Keep the cached INT8 epilogue scale order
+ * exact"; Validation: bit-exact, "max absolute error 0.0".)
+ *
+ *   acc      = sum_k A[m,k] * B[n,k]                  exact, int32
+ *   x        = (float)acc                             round to nearest even
+ *   x        = x * sa[m];  x = x * sb[n]              two fp32 roundings, in this order
+ *   if bias:   x = x + (float)bias[n]                 one fp32 add (no FMA)
+ *   out[m,n] = bf16 round-to-nearest-even(x)
+ * Without bias no add is made, so a -0 produced by the products is kept.
+ *
+ *   A    int8  [M, K]        B    int8 [N, K]
+ *   sa   fp32  [M]           sb   fp32 [N]
+ *   bias bf16  [N] or NULL   out  bf16 [M, N]
+ * Requirements: all pointers 16-byte aligned; N % 8 == 0; K % 16 == 0;
+ * 1 <= K <= 131056.  The result is bit-identical to the definition above.
+ * Internally the operands are widened to f16 in a library-owned, stream-
+ * ordered workspace of (M + N) * K * 2 bytes that is released back to the
+ * library's pool at the end of the call (on the stream).
+ */
+int qk_gemm_int8_rowwise(const int8_t* A, const int8_t* B, const float* sa, const float* sb,
+                         const uint16_t* bias, uint16_t* out, int64_t M, int64_t N, int64_t K,
+                         qk_stream_t stream);
+
+/*
+ * MX block-scaled GEMM (ROCm/mori PR #806, "What": "the same 32-wide ue8m0
+ * GEMM ... taking A's scales as [M, K/32] ... uint8, row major"; ROCm/FlyDSL
+ * PR #990: MXFP4 "per1x32" scales).
+ *
+ *   out[m,n] = bf16_rne( sum_b 2^(sA[m,b]-127) * 2^(sB[n,b]-127)
+ *                          * sum_{j<32} A[m,32b+j] * B[n,32b+j]   (+ bias[n]) )
+ * accumulated in fp32 on the tensor cores (the summation order is free).
+ *
+ *   fmt  QK_FMT_MXFP8_E4M3: A [M, K] bytes, B [N, K] bytes (E4M3FN)
+ *        QK_FMT_MXFP4_E2M1: A [M, K/2] bytes, B [N, K/2] bytes (packed E2M1)
+ *   sA   uint8 [M, K/32]  raw row-major UE8M0 exponents (bias 127)
+ *   sB   uint8 [N, K/32]
+ *   bias bf16 [N] or NULL;  out bf16 [M, N]
+ * Requirements: A, B, out, bias 16-byte aligned; sA, sB 4-byte aligned;
+ * N % 8 == 0; K % 32 == 0.  Any M >= 1 is accepted without padding.
+ */
+int qk_gemm_mx(int fmt, const void* A, const uint8_t* sA, const void* B, const uint8_t* sB,
+               const uint16_t* bias, uint16_t* out, int64_t M, int64_t N, int64_t K, qk_stream_t stream);
+
+/*
+ * FP8 E4M3 GEMM with per-token (row) and per-channel (column) fp32 scales
+ * (ROCm/aiter PR #6262, gemm_a8w8_bpreshuffle with per-token/per-channel
+ * scales; ROCm/mori PR #806, the "ptpc" kind).  Same epilogue as
+ * qk_gemm_int8_rowwise, with acc the fp32 tensor-core sum of the decoded
+ * E4M3 products.
+ *   A uint8 [M, K] E4M3FN; B uint8 [N, K] E4M3FN; sa fp32 [M]; sb fp32 [N];
+ *   bias bf16 [N] or NULL; out bf16 [M, N].
+ * Requirements: as qk_gemm_int8_rowwise, without the K upper bound.
+ */
+int qk_gemm_fp8_rowwise(const uint8_t* A, const uint8_t* B, const float* sa, const float* sb,
+                        const uint16_t* bias, uint16_t* out, int64_t M, int64_t N, int64_t K,
+                        qk_stream_t stream);
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char* qk_status_string(int status);
+
+/*
+ * Reads (and with clear != 0, resets) the current device's status word that
+ * kernels set when a bounded wait gives up.  0 means no failure was recorded.
+ * Layout: bits 63..56 code (1 = timeout), 55..48 site, 47..32 CTA index,
+ * 31..0 detail.  Synchronises the device first.  Returns QK_OK or
+ * QK_ERR_CUDA; *word may be NULL.
+ */
+int qk_device_status(uint64_t* word, int clear);
+
+/*
+ * Bound, in nanoseconds, on every barrier wait inside the kernels (default
+ * 1e9, or QK_WAIT_TIMEOUT_MS from the environment).  0 restores the default.
+ */
+void qk_set_wait_timeout_ns(uint64_t ns);
+
+/*
+ * Launches one block whose barrier wait can never complete, with a wait
+ * bound of timeout_ns, synchronises the stream and returns QK_ERR_TIMEOUT if
+ * the kernel reported the give-up in the status word (the word is cleared),
+ * QK_OK if it did not.  Exercises the failure path of the bounded waits
+ * without faulting the GPU.
+ */
+int qk_wait_timeout_probe(uint64_t timeout_ns, qk_stream_t stream);
+
+/* Number of kernels this library has launched in this process. */
+uint64_t qk_launch_count(void);
+
+/* Frees the library's cached workspace memory on the current device. */
+int qk_release(void);
+
+/* ABI version (major * 100 + minor). */
+int qk_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QK_H_ */
