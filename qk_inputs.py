@@ -38,8 +38,8 @@ _ROW_CHUNK = 2048  # rows drawn per chunk; part of the recipe (fixes the stream 
 
 def to_bf16_bits(x: np.ndarray) -> np.ndarray:
     """float32 -> bf16 bit patterns, round to nearest even (finite inputs)."""
-    u = np.ascontiguousarray(x, np.float32).view(np.uint32).astype(np.uint64)
-    u = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    u = np.ascontiguousarray(x, np.float32).view(np.uint32)
+    u = (u + (np.uint32(0x7FFF) + ((u >> np.uint32(16)) & np.uint32(1)))) >> np.uint32(16)
     return u.astype(np.uint16)
 
 
@@ -47,40 +47,40 @@ def from_bf16_bits(b: np.ndarray) -> np.ndarray:
     return (np.asarray(b, np.uint16).astype(np.uint32) << 16).view(np.float32)
 
 
+def _round_mantissa(a: np.ndarray, keep_bits: int) -> np.ndarray:
+    """Round non-negative float32 values to `keep_bits` mantissa bits, ties to
+    even, on the bit pattern; returns the rounded bit patterns (uint32)."""
+    drop = 23 - keep_bits
+    u = a.view(np.uint32)
+    lsb = (u >> np.uint32(drop)) & np.uint32(1)
+    r = u + (np.uint32((1 << (drop - 1)) - 1) + lsb)
+    return r & np.uint32(~((1 << drop) - 1) & 0xFFFFFFFF)
+
+
 def encode_e4m3(q: np.ndarray) -> np.ndarray:
     """Round to the nearest E4M3FN value (ties to even), saturating at 448."""
-    q = np.asarray(q, np.float64)
-    sign = np.signbit(q).astype(np.uint8)
-    a = np.minimum(np.abs(q), 448.0)
-    _, e = np.frexp(a)
-    ex = np.maximum(e - 1, -6)                   # binade exponent, subnormals share -6
-    quantum = np.ldexp(1.0, ex - 3)              # 3 mantissa bits
-    r = np.rint(a / quantum) * quantum
-    _, e2 = np.frexp(r)
-    er = e2 - 1
-    normal = r >= 2.0 ** -6
-    exp_field = np.where(normal, er + 7, 0).astype(np.int64)
-    man_field = np.where(normal, np.rint((r / np.ldexp(1.0, er) - 1.0) * 8.0),
-                         np.rint(r / 2.0 ** -9)).astype(np.int64)
-    return ((sign.astype(np.int64) << 7) | (exp_field << 3) | man_field).astype(np.uint8)
+    q = np.asarray(q, np.float32)
+    sign = (q.view(np.uint32) >> np.uint32(31)).astype(np.uint8) << np.uint8(7)
+    a = np.minimum(np.abs(q), np.float32(448.0))
+    r = _round_mantissa(a, 3)
+    exp = (r >> np.uint32(23)).astype(np.int32) - 127
+    normal_code = (((exp + 7) << 3) | ((r >> np.uint32(20)) & np.uint32(7)).astype(np.int32))
+    sub_code = np.rint(a * np.float32(512.0)).astype(np.int32)        # multiples of 2^-9; 8 -> 2^-6
+    code = np.where(a < np.float32(2.0 ** -6), sub_code, normal_code).astype(np.uint8)
+    return code | sign
 
 
 def encode_e2m1(q: np.ndarray) -> np.ndarray:
     """Round to the nearest E2M1 value (ties to even), saturating at 6; one code per byte."""
-    q = np.asarray(q, np.float64)
-    sign = np.signbit(q).astype(np.int64)
-    a = np.minimum(np.abs(q), 6.0)
-    _, e = np.frexp(a)
-    ex = np.maximum(e - 1, 0)
-    quantum = np.ldexp(1.0, ex - 1)              # 1 mantissa bit
-    r = np.rint(a / quantum) * quantum
-    _, e2 = np.frexp(r)
-    er = e2 - 1
-    normal = r >= 1.0
-    exp_field = np.where(normal, er + 1, 0).astype(np.int64)
-    man_field = np.where(normal, np.rint((r / np.ldexp(1.0, er) - 1.0) * 2.0),
-                         np.rint(r / 0.5)).astype(np.int64)
-    return ((sign << 3) | (exp_field << 1) | man_field).astype(np.uint8)
+    q = np.asarray(q, np.float32)
+    sign = (q.view(np.uint32) >> np.uint32(31)).astype(np.uint8) << np.uint8(3)
+    a = np.minimum(np.abs(q), np.float32(6.0))
+    r = _round_mantissa(a, 1)
+    exp = (r >> np.uint32(23)).astype(np.int32) - 127
+    normal_code = ((exp + 1) << 1) | ((r >> np.uint32(22)) & np.uint32(1)).astype(np.int32)
+    sub_code = np.rint(a * np.float32(2.0)).astype(np.int32)          # 0, 0.5, (1.0 -> code 2)
+    code = np.where(a < np.float32(1.0), sub_code, normal_code).astype(np.uint8)
+    return code | sign
 
 
 def pack_e2m1(codes: np.ndarray) -> np.ndarray:
@@ -105,17 +105,18 @@ def mx_quantize(x: np.ndarray, fmt: int):
     code 0 for an all-zero block; elements x / 2^s rounded to nearest even
     and saturated.  MXFP4 operands come back packed two per byte.
     """
-    x = np.asarray(x, np.float64)
+    x = np.asarray(x, np.float32)
     rows, K = x.shape
     if K % 32:
         raise ValueError("K must be a multiple of 32")
     blk = x.reshape(rows, K // 32, 32)
     amax = np.abs(blk).max(axis=2)
-    _, e = np.frexp(amax)
+    _, e = np.frexp(amax.astype(np.float64))
     emax = 8 if fmt == FMT_MXFP8_E4M3 else 2
     sexp = np.clip(e - 1 - emax, -127, 127)
-    sexp = np.where(amax == 0.0, -127, sexp)
-    q = np.ldexp(blk, -sexp[:, :, None]).reshape(rows, K)
+    sexp = np.where(amax == 0.0, -127, sexp).astype(np.int32)
+    inv = np.ldexp(np.float32(1.0), -sexp).astype(np.float32)  # always a normal float32
+    q = (blk * inv[:, :, None]).reshape(rows, K)                 # exact power-of-two scaling
     if fmt == FMT_MXFP8_E4M3:
         codes = encode_e4m3(q)
     else:
