@@ -43,6 +43,8 @@ EXPORTS = (
     "qk_set_wait_timeout_ns",
     "qk_wait_timeout_probe",
     "qk_launch_count",
+    "qk_profile_enable",
+    "qk_profile_read",
     "qk_release",
     "qk_version",
 )
@@ -55,6 +57,10 @@ class QkError(RuntimeError):
 
 
 _lib = None
+
+
+class KernelStats(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char_p), ("launches", ctypes.c_uint64), ("total_ms", ctypes.c_double)]
 
 
 def _declare(lib):
@@ -77,6 +83,10 @@ def _declare(lib):
     lib.qk_wait_timeout_probe.restype = c.c_int
     lib.qk_launch_count.argtypes = []
     lib.qk_launch_count.restype = c.c_uint64
+    lib.qk_profile_enable.argtypes = [c.c_int]
+    lib.qk_profile_enable.restype = None
+    lib.qk_profile_read.argtypes = [c.POINTER(KernelStats), c.c_int, c.POINTER(c.c_int), c.c_int]
+    lib.qk_profile_read.restype = c.c_int
     lib.qk_release.argtypes = []
     lib.qk_release.restype = c.c_int
     lib.qk_version.argtypes = []
@@ -219,3 +229,17 @@ def set_wait_timeout_ns(ns: int) -> None:
 
 def launch_count() -> int:
     return int(load_library().qk_launch_count())
+
+
+def profile_enable(on: bool = True) -> None:
+    """Record a CUDA event pair around every kernel the library launches."""
+    load_library().qk_profile_enable(1 if on else 0)
+
+
+def profile_read(reset: bool = True) -> dict:
+    """{kernel name: (launches, total ms)} for the kernels timed so far."""
+    lib = load_library()
+    arr = (KernelStats * 16)()
+    n = ctypes.c_int(0)
+    check(lib.qk_profile_read(arr, 16, ctypes.byref(n), 1 if reset else 0))
+    return {arr[i].name.decode(): (int(arr[i].launches), float(arr[i].total_ms)) for i in range(min(n.value, 16))}

@@ -7,6 +7,7 @@
 #include <cstdint>
 #include <cstdlib>
 #include <mutex>
+#include <vector>
 
 #include "qk_device.cuh"
 #include "qk_internal.h"
@@ -45,6 +46,48 @@ uint64_t wait_timeout_ns() {
 }
 
 void count_launches(uint64_t n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+namespace {
+
+const char* const kKernelNames[kKNumKinds] = {"int8_to_f16", "gemm_int8_f16", "gemm_fp8",
+                                              "gemm_mxfp8",  "gemm_mxfp4",    "wait_probe"};
+
+struct PendingTiming {
+  int kind;
+  cudaEvent_t start, end;
+};
+
+std::atomic<int> g_profile_on{0};
+std::mutex g_prof_mu;
+std::vector<PendingTiming> g_pending;
+uint64_t g_prof_launches[kKNumKinds];
+double g_prof_ms[kKNumKinds];
+
+}  // namespace
+
+LaunchTimer::LaunchTimer(int kind, cudaStream_t stream) : kind_(kind), stream_(stream) {
+  if (!g_profile_on.load(std::memory_order_relaxed)) return;
+  if (cudaEventCreate(&start_) != cudaSuccess || cudaEventRecord(start_, stream_) != cudaSuccess) {
+    cudaGetLastError();
+    if (start_) cudaEventDestroy(start_);
+    start_ = nullptr;
+  }
+}
+
+void LaunchTimer::done() {
+  if (!start_) return;
+  cudaEvent_t end = nullptr;
+  if (cudaEventCreate(&end) != cudaSuccess || cudaEventRecord(end, stream_) != cudaSuccess) {
+    cudaGetLastError();
+    cudaEventDestroy(start_);
+    if (end) cudaEventDestroy(end);
+    start_ = nullptr;
+    return;
+  }
+  std::lock_guard<std::mutex> lock(g_prof_mu);
+  g_pending.push_back({kind_, start_, end});
+  start_ = nullptr;
+}
 
 const DeviceInfo* current_device(int* status) {
   int dev = -1;
@@ -134,7 +177,9 @@ __global__ void qk_wait_probe_kernel(unsigned long long* err, uint64_t timeout_n
 }
 
 int launch_wait_probe(uint64_t timeout_ns, const DeviceInfo& dev, cudaStream_t stream) {
+  LaunchTimer timer(kKWaitProbe, stream);
   qk_wait_probe_kernel<<<1, 32, 0, stream>>>(dev.err_word, timeout_ns);
+  timer.done();
   if (cudaGetLastError() != cudaSuccess) return QK_ERR_CUDA;
   count_launches(1);
   return QK_OK;
@@ -268,6 +313,44 @@ int qk_wait_timeout_probe(uint64_t timeout_ns, qk_stream_t stream) {
 }
 
 uint64_t qk_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+void qk_profile_enable(int on) { g_profile_on.store(on ? 1 : 0, std::memory_order_relaxed); }
+
+int qk_profile_read(qk_kernel_stats* stats, int max, int* count, int reset) {
+  std::lock_guard<std::mutex> lock(g_prof_mu);
+  int st = QK_OK;
+  for (const PendingTiming& t : g_pending) {
+    float ms = 0.f;
+    if (cudaEventSynchronize(t.end) == cudaSuccess && cudaEventElapsedTime(&ms, t.start, t.end) == cudaSuccess) {
+      g_prof_launches[t.kind] += 1;
+      g_prof_ms[t.kind] += ms;
+    } else {
+      cudaGetLastError();
+      st = QK_ERR_CUDA;
+    }
+    cudaEventDestroy(t.start);
+    cudaEventDestroy(t.end);
+  }
+  g_pending.clear();
+  int n = 0;
+  for (int k = 0; k < kKNumKinds; ++k) {
+    if (g_prof_launches[k] == 0) continue;
+    if (stats && n < max) {
+      stats[n].name = kKernelNames[k];
+      stats[n].launches = g_prof_launches[k];
+      stats[n].total_ms = g_prof_ms[k];
+    }
+    ++n;
+  }
+  if (count) *count = n;
+  if (reset) {
+    for (int k = 0; k < kKNumKinds; ++k) {
+      g_prof_launches[k] = 0;
+      g_prof_ms[k] = 0.0;
+    }
+  }
+  return st;
+}
 
 int qk_release(void) {
   int st;

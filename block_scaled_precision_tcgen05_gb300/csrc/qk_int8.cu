@@ -69,9 +69,11 @@ int launch_int8_rowwise(const int8_t* A, const int8_t* B, const float* sa, const
   long long blocks = (na + nb + 255) / 256;
   const long long cap = static_cast<long long>(dev.sm_count) * 8;
   if (blocks > cap) blocks = cap;
+  LaunchTimer timer(kKInt8ToF16, stream);
   qk_int8_to_f16_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(
       reinterpret_cast<const uint4*>(A), reinterpret_cast<uint4*>(a16), na, reinterpret_cast<const uint4*>(B),
       reinterpret_cast<uint4*>(b16), nb);
+  timer.done();
   int st = cudaGetLastError() == cudaSuccess ? QK_OK : QK_ERR_CUDA;
   if (st == QK_OK) count_launches(1);
 

@@ -29,6 +29,26 @@ int encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base
 uint64_t wait_timeout_ns();
 void count_launches(uint64_t n);
 
+// Kernel kinds for the optional per-kernel timing (order of kKernelNames).
+enum KernelKind : int {
+  kKInt8ToF16 = 0,
+  kKGemmInt8 = 1,
+  kKGemmFp8 = 2,
+  kKGemmMxfp8 = 3,
+  kKGemmMxfp4 = 4,
+  kKWaitProbe = 5,
+  kKNumKinds = 6,
+};
+
+// Brackets one kernel launch with an event pair when timing is enabled.
+struct LaunchTimer {
+  LaunchTimer(int kind, cudaStream_t stream);
+  void done();  // call right after the launch
+  int kind_;
+  cudaStream_t stream_;
+  cudaEvent_t start_ = nullptr;
+};
+
 // Per-format launchers (arguments already validated).
 int launch_int8_rowwise(const int8_t* A, const int8_t* B, const float* sa, const float* sb, const uint16_t* bias,
                         uint16_t* out, int M, int N, int K, const DeviceInfo& dev, cudaStream_t stream);

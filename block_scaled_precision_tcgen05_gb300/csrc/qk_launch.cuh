@@ -28,13 +28,20 @@ void plan_tiles(GemmParams& p, int M, int N, int K) {
 }
 
 template <class C>
+constexpr int kernel_kind() {
+  return C::kind == Kind::F16 ? kKGemmInt8 : C::kind == Kind::F8 ? kKGemmFp8 : C::kind == Kind::MXF8 ? kKGemmMxfp8 : kKGemmMxfp4;
+}
+
+template <class C>
 int launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, const DeviceInfo& dev,
                 cudaStream_t stream) {
   auto kernel = qk_gemm_kernel<C>;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return QK_ERR_CUDA;
   const int grid = p.num_tiles < dev.sm_count ? p.num_tiles : dev.sm_count;
+  LaunchTimer timer(kernel_kind<C>(), stream);
   kernel<<<grid, C::NUM_THREADS, C::SMEM_BYTES, stream>>>(ta, tb, p);
+  timer.done();
   e = cudaGetLastError();
   if (e != cudaSuccess) return QK_ERR_CUDA;
   count_launches(1);

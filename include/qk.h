@@ -149,6 +149,24 @@ int qk_wait_timeout_probe(uint64_t timeout_ns, qk_stream_t stream);
 /* Number of kernels this library has launched in this process. */
 uint64_t qk_launch_count(void);
 
+/*
+ * Kernel timing.  While enabled, the library records a CUDA event pair on the
+ * launch stream around every kernel it launches.  qk_profile_read waits for
+ * the recorded events, adds their durations to per-kernel totals, and copies
+ * up to `max` entries (one per kernel kind that ran) into `stats`; *count
+ * receives the number of entries.  reset != 0 clears the totals afterwards.
+ * Kernel names: "int8_to_f16", "gemm_int8_f16", "gemm_fp8", "gemm_mxfp8",
+ * "gemm_mxfp4", "wait_probe".
+ */
+typedef struct {
+  const char* name;   /* static storage */
+  uint64_t launches;
+  double total_ms;
+} qk_kernel_stats;
+
+void qk_profile_enable(int on);
+int qk_profile_read(qk_kernel_stats* stats, int max, int* count, int reset);
+
 /* Frees the library's cached workspace memory on the current device. */
 int qk_release(void);
 

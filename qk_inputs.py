@@ -10,15 +10,16 @@ consume exactly the bytes produced here.
 Recipes (the model-projection shapes of the pages, with synthetic values):
 
 * INT8 row/column-scaled: A, B int8 uniform in [-127, 127]; sa[M], sb[N]
-  fp32 uniform in [1e-3, 1e-2]; bias bf16 from N(0, 1).  Draw order A, B,
-  sa, sb, bias.
+  fp32 uniform in [1e-3, 1e-2]; bias bf16 from N(0, 1).
 * MXFP8: A from bf16 N(0, 1) with 1% of entries (seeded uniform mask) x20;
   B from bf16 N(0, 0.02); both MX-quantized to E4M3 + UE8M0 per 32 along K.
 * MXFP4: A, B from bf16 N(0, 1), MX-quantized to packed E2M1 + UE8M0.
 * FP8 per-token x per-channel: A N(0, 1), W N(0, 0.02); per-row scale
   s = amax/448 (1 for an all-zero row), q = E4M3(x / s).
 
-Every generator is a pure function of (shape, seed).
+Every generator is a pure function of (shape, seed).  Each operand draws from
+its own stream, numpy default_rng([seed, tag]) with tag 0 = A, 1 = B, 2 = sa,
+3 = sb, 4 = bias, so a weight matrix does not depend on M.
 """
 from __future__ import annotations
 
@@ -187,52 +188,70 @@ def _normal_rows(rng, rows, K, std, fn):
     return outs
 
 
+TAG_A, TAG_B, TAG_SA, TAG_SB, TAG_BIAS = 0, 1, 2, 3, 4
+
+
+def _rng(seed: int, tag: int):
+    return np.random.default_rng([int(seed), int(tag)])
+
+
+def bias_bits(N: int, seed: int) -> np.ndarray:
+    return to_bf16_bits(_rng(seed, TAG_BIAS).standard_normal(N).astype(np.float32))
+
+
 def int8_problem(M: int, N: int, K: int, seed: int = 0, bias: bool = True) -> Int8Problem:
-    rng = np.random.default_rng(seed)
-    A = rng.integers(-127, 128, size=(M, K), dtype=np.int8)
-    B = rng.integers(-127, 128, size=(N, K), dtype=np.int8)
-    sa = rng.uniform(1e-3, 1e-2, size=M).astype(np.float32)
-    sb = rng.uniform(1e-3, 1e-2, size=N).astype(np.float32)
-    bb = to_bf16_bits(rng.standard_normal(N).astype(np.float32))
-    return Int8Problem(A, B, sa, sb, bb if bias else None, M, N, K)
+    A = _rng(seed, TAG_A).integers(-127, 128, size=(M, K), dtype=np.int8)
+    B = _rng(seed, TAG_B).integers(-127, 128, size=(N, K), dtype=np.int8)
+    sa = _rng(seed, TAG_SA).uniform(1e-3, 1e-2, size=M).astype(np.float32)
+    sb = _rng(seed, TAG_SB).uniform(1e-3, 1e-2, size=N).astype(np.float32)
+    return Int8Problem(A, B, sa, sb, bias_bits(N, seed) if bias else None, M, N, K)
 
 
-def mx_problem(fmt: int, M: int, N: int, K: int, seed: int = 0, bias: bool = False) -> MxProblem:
-    rng = np.random.default_rng(seed)
+def _cat(parts, idx, empty_shape, dtype):
+    return np.concatenate([p[idx] for p in parts]) if parts else np.zeros(empty_shape, dtype)
+
+
+def mx_operand(fmt: int, rows: int, K: int, seed: int, tag: int):
+    """(bytes, scales) of one MX operand of the recipe: tag TAG_A or TAG_B."""
+    rng = _rng(seed, tag)
 
     def quant(x):
         return mx_quantize(from_bf16_bits(to_bf16_bits(x)), fmt)
 
-    if fmt == FMT_MXFP8_E4M3:
-        def a_chunk(x):
+    if fmt == FMT_MXFP8_E4M3 and tag == TAG_A:
+        def chunk(x):
             mask = rng.uniform(size=x.shape) < 0.01
             x[mask] *= np.float32(20.0)
             return quant(x)
-        a_parts = _normal_rows(rng, M, K, 1.0, a_chunk)
-        b_parts = _normal_rows(rng, N, K, 0.02, quant)
+        parts = _normal_rows(rng, rows, K, 1.0, chunk)
+    elif fmt == FMT_MXFP8_E4M3:
+        parts = _normal_rows(rng, rows, K, 0.02, quant)
     elif fmt == FMT_MXFP4_E2M1:
-        a_parts = _normal_rows(rng, M, K, 1.0, quant)
-        b_parts = _normal_rows(rng, N, K, 1.0, quant)
+        parts = _normal_rows(rng, rows, K, 1.0, quant)
     else:
         raise ValueError("unknown MX format")
-    A = np.concatenate([p[0] for p in a_parts]) if a_parts else np.zeros((0, K), np.uint8)
-    sA = np.concatenate([p[1] for p in a_parts]) if a_parts else np.zeros((0, K // 32), np.uint8)
-    B = np.concatenate([p[0] for p in b_parts])
-    sB = np.concatenate([p[1] for p in b_parts])
-    bb = to_bf16_bits(rng.standard_normal(N).astype(np.float32)) if bias else None
-    return MxProblem(fmt, A, sA, B, sB, bb, M, N, K)
+    width = K if fmt == FMT_MXFP8_E4M3 else K // 2
+    return _cat(parts, 0, (0, width), np.uint8), _cat(parts, 1, (0, K // 32), np.uint8)
 
 
-def fp8_problem(M: int, N: int, K: int, seed: int = 0, bias: bool = False) -> Fp8Problem:
-    rng = np.random.default_rng(seed)
-    a_parts = _normal_rows(rng, M, K, 1.0, ptpc_quantize)
-    b_parts = _normal_rows(rng, N, K, 0.02, ptpc_quantize)
-    A = np.concatenate([p[0] for p in a_parts])
-    sa = np.concatenate([p[1] for p in a_parts]).astype(np.float32)
-    B = np.concatenate([p[0] for p in b_parts])
-    sb = np.concatenate([p[1] for p in b_parts]).astype(np.float32)
-    bb = to_bf16_bits(rng.standard_normal(N).astype(np.float32)) if bias else None
-    return Fp8Problem(A, B, sa, sb, bb, M, N, K)
+def mx_problem(fmt: int, M: int, N: int, K: int, seed: int = 0, bias: bool = False) -> MxProblem:
+    A, sA = mx_operand(fmt, M, K, seed, TAG_A)
+    B, sB = mx_operand(fmt, N, K, seed, TAG_B)
+    return MxProblem(fmt, A, sA, B, sB, bias_bits(N, seed) if bias else None, M, N, K)
+
+
+def fp8_operand(rows: int, K: int, seed: int, tag: int):
+    """(E4M3 bytes, fp32 row scales) of one per-token / per-channel operand: A ~ N(0,1), W ~ N(0,0.02)."""
+    rng = _rng(seed, tag)
+    parts = _normal_rows(rng, rows, K, 1.0 if tag == TAG_A else 0.02, ptpc_quantize)
+    return _cat(parts, 0, (0, K), np.uint8), _cat(parts, 1, (0,), np.float32).astype(np.float32)
+
+
+def fp8_problem(M: int, N: int, K: int, seed: int = 0, bias: bool = False, weights=None) -> Fp8Problem:
+    """weights: an optional precomputed fp8_operand(N, K, seed, TAG_B)."""
+    A, sa = fp8_operand(M, K, seed, TAG_A)
+    B, sb = weights if weights is not None else fp8_operand(N, K, seed, TAG_B)
+    return Fp8Problem(A, B, sa, sb, bias_bits(N, seed) if bias else None, M, N, K)
 
 
 def sample_tiles(M: int, N: int, count: int, seed: int, tile: int = 128):
