@@ -29,6 +29,7 @@ QK_ERR_ARCH = 4
 QK_ERR_CUDA = 5
 QK_ERR_TIMEOUT = 6
 QK_ERR_NOMEM = 7
+QK_ERR_SCRATCH = 8
 
 FMT_MXFP8_E4M3 = 1
 FMT_MXFP4_E2M1 = 2
@@ -36,6 +37,7 @@ FMT_MXFP4_E2M1 = 2
 # every symbol include/qk.h declares
 EXPORTS = (
     "qk_gemm_int8_rowwise",
+    "qk_gemm_int8_rowwise_noalloc",
     "qk_gemm_mx",
     "qk_gemm_fp8_rowwise",
     "qk_status_string",
@@ -69,6 +71,8 @@ def _declare(lib):
     i64 = c.c_int64
     lib.qk_gemm_int8_rowwise.argtypes = [P, P, P, P, P, P, i64, i64, i64, P]
     lib.qk_gemm_int8_rowwise.restype = c.c_int
+    lib.qk_gemm_int8_rowwise_noalloc.argtypes = [P, P, P, P, P, P, i64, i64, i64, P]
+    lib.qk_gemm_int8_rowwise_noalloc.restype = c.c_int
     lib.qk_gemm_fp8_rowwise.argtypes = [P, P, P, P, P, P, i64, i64, i64, P]
     lib.qk_gemm_fp8_rowwise.restype = c.c_int
     lib.qk_gemm_mx.argtypes = [c.c_int, P, P, P, P, P, P, i64, i64, i64, P]
@@ -170,6 +174,29 @@ def gemm_int8_rowwise(A, B, sa, sb, bias=None, out=None):
     out = _out(out, M, N, dev)
     check(load_library().qk_gemm_int8_rowwise(_ptr(A), _ptr(B), _ptr(sa), _ptr(sb), _ptr(bias), _ptr(out),
                                               M, N, K, _stream_handle(dev)))
+    return out
+
+
+def gemm_int8_rowwise_noalloc(A, B, sa, sb, bias=None, out=None):
+    """gemm_int8_rowwise without any allocation inside the library: the operands are widened in a
+    fixed 32 MiB scratch array ((M + N) * K * 2 bytes at most).  For callers that cannot let a library
+    allocate device memory.  Calls that can overlap on the GPU share that array and race; `out` must be
+    passed in by the caller (the binding does not allocate it either)."""
+    import torch
+    if out is None:
+        raise ValueError("out must be provided: this entry point allocates nothing")
+    M, K = A.shape
+    N = B.shape[0]
+    dev = A.device
+    _expect(A, "A", torch.int8, (M, K), dev)
+    _expect(B, "B", torch.int8, (N, K), dev)
+    _expect(sa, "sa", torch.float32, (M,), dev)
+    _expect(sb, "sb", torch.float32, (N,), dev)
+    if bias is not None:
+        _expect(bias, "bias", torch.bfloat16, (N,), dev)
+    _expect(out, "out", torch.bfloat16, (M, N), dev)
+    check(load_library().qk_gemm_int8_rowwise_noalloc(_ptr(A), _ptr(B), _ptr(sa), _ptr(sb), _ptr(bias), _ptr(out),
+                                                      M, N, K, _stream_handle(dev)))
     return out
 
 

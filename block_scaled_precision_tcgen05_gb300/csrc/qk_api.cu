@@ -89,7 +89,7 @@ void LaunchTimer::done() {
   start_ = nullptr;
 }
 
-const DeviceInfo* current_device(int* status) {
+const DeviceInfo* current_device_basics(int* status) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
     cudaGetLastError();
@@ -103,6 +103,7 @@ const DeviceInfo* current_device(int* status) {
     return nullptr;
   }
   DeviceInfo info;
+  info.device = dev;
   if (cudaDeviceGetAttribute(&info.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&info.cc_major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&info.cc_minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
@@ -120,17 +121,6 @@ const DeviceInfo* current_device(int* status) {
     *status = QK_ERR_CUDA;
     return nullptr;
   }
-  cudaMemPoolProps props = {};
-  props.allocType = cudaMemAllocationTypePinned;
-  props.location.type = cudaMemLocationTypeDevice;
-  props.location.id = dev;
-  if (cudaMemPoolCreate(&info.pool, &props) != cudaSuccess) {
-    cudaGetLastError();
-    *status = QK_ERR_CUDA;
-    return nullptr;
-  }
-  uint64_t keep = UINT64_MAX;  // keep freed workspace cached in the pool
-  cudaMemPoolSetAttribute(info.pool, cudaMemPoolAttrReleaseThreshold, &keep);
   if (!g_encode) {
     void* fn = nullptr;
     cudaDriverEntryPointQueryResult q;
@@ -146,6 +136,28 @@ const DeviceInfo* current_device(int* status) {
   g_dev[dev] = info;
   g_dev_state[dev] = 1;
   return &g_dev[dev];
+}
+
+const DeviceInfo* current_device(int* status) {
+  const DeviceInfo* basics = current_device_basics(status);
+  if (!basics) return nullptr;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceInfo& info = g_dev[basics->device];
+  if (info.pool) return &info;
+  cudaMemPoolProps props = {};
+  props.allocType = cudaMemAllocationTypePinned;
+  props.location.type = cudaMemLocationTypeDevice;
+  props.location.id = info.device;
+  cudaMemPool_t pool = nullptr;
+  if (cudaMemPoolCreate(&pool, &props) != cudaSuccess) {
+    cudaGetLastError();
+    *status = QK_ERR_CUDA;
+    return nullptr;
+  }
+  uint64_t keep = UINT64_MAX;  // keep freed workspace cached in the pool
+  cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
+  info.pool = pool;
+  return &info;
 }
 
 int encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t inner, uint64_t rows,
@@ -272,6 +284,8 @@ const char* qk_status_string(int status) {
     case QK_ERR_CUDA: return "QK_ERR_CUDA: a CUDA call or kernel launch failed";
     case QK_ERR_TIMEOUT: return "QK_ERR_TIMEOUT: a bounded wait inside a kernel gave up";
     case QK_ERR_NOMEM: return "QK_ERR_NOMEM: workspace allocation failed";
+    case QK_ERR_SCRATCH:
+      return "QK_ERR_SCRATCH: (M + N) * K * 2 bytes exceed the 32 MiB scratch of qk_gemm_int8_rowwise_noalloc";
     default: return "QK_ERR_UNKNOWN";
   }
 }

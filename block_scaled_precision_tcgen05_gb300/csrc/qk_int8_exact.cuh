@@ -1,0 +1,97 @@
+// qk_int8_exact.cuh -- the two kernels of the exact INT8 GEMM on the f16 tensor
+// pipe and the launch sequence that runs them over a given f16 workspace.
+//
+// sm_103a has no integer tcgen05.mma kind, so the int8 operands are widened
+// to f16 (every int8 value is exact in f16) by a bandwidth-bound pass, and
+// the f16 MMA accumulates in fp32 in chunks of at most 1024 K: every partial
+// sum is then an integer of magnitude at most 1024 * 128 * 128 = 2^24, which
+// fp32 holds exactly.  The epilogue drains each chunk to int32 and adds the
+// chunks, so the accumulator is the exact integer dot product, and the
+// fixed-order epilogue of comfy-kitchen PR #174 (update "Keep the cached INT8
+// epilogue scale order exact") makes the bf16 result bit-identical to the
+// definition.
+#pragma once
+
+#include <cuda_fp16.h>
+
+#include "qk_launch.cuh"
+
+namespace qk {
+
+using CfgInt8 = GemmCfg<Kind::F16, 128, 6, 2>;
+
+// Widens 16 int8 values per thread-iteration to f16.  Byte x becomes the f16
+// bit pattern 0x6400 | (x + 128), i.e. the value 1024 + x + 128, and one
+// exact subtraction of 1152 leaves x.
+__device__ __forceinline__ uint4 widen8(uint32_t w, uint32_t w2) {
+  const __half2 bias = __float2half2_rn(1152.f);
+  uint32_t o[4];
+  const uint32_t in[2] = {w ^ 0x80808080u, w2 ^ 0x80808080u};
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    uint32_t lo = __byte_perm(in[j], 0x64646464u, 0x4140);
+    uint32_t hi = __byte_perm(in[j], 0x64646464u, 0x4342);
+    __half2 hlo = __hsub2(*reinterpret_cast<__half2*>(&lo), bias);
+    __half2 hhi = __hsub2(*reinterpret_cast<__half2*>(&hi), bias);
+    o[2 * j] = *reinterpret_cast<uint32_t*>(&hlo);
+    o[2 * j + 1] = *reinterpret_cast<uint32_t*>(&hhi);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+static __global__ void __launch_bounds__(256) qk_int8_to_f16_kernel(const uint4* __restrict__ a, uint4* __restrict__ a16,
+                                                              long long na, const uint4* __restrict__ b,
+                                                              uint4* __restrict__ b16, long long nb) {
+  const long long total = na + nb;
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+#pragma unroll 1
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total; i += stride) {
+    const bool in_a = i < na;
+    const long long j = in_a ? i : i - na;
+    const uint4 s = __ldcs(in_a ? a + j : b + j);
+    uint4* d = in_a ? a16 + 2 * j : b16 + 2 * j;
+    d[0] = widen8(s.x, s.y);
+    d[1] = widen8(s.z, s.w);
+  }
+}
+
+// Widens A and B into a16 [M, K] and b16 [N, K] (caller-provided device
+// memory) and runs the GEMM over them, both on `stream`.
+static inline int widen_and_gemm_int8(const int8_t* A, const int8_t* B, const float* sa, const float* sb,
+                                      const uint16_t* bias, uint16_t* out, int M, int N, int K, uint16_t* a16,
+                                      uint16_t* b16, const DeviceInfo& dev, cudaStream_t stream) {
+  using C = CfgInt8;
+  const size_t a_elems = static_cast<size_t>(M) * K;
+  const size_t b_elems = static_cast<size_t>(N) * K;
+  const long long na = static_cast<long long>(a_elems / 16), nb = static_cast<long long>(b_elems / 16);
+  long long blocks = (na + nb + 255) / 256;
+  const long long cap = static_cast<long long>(dev.sm_count) * 8;
+  if (blocks > cap) blocks = cap;
+  LaunchTimer timer(kKInt8ToF16, stream);
+  qk_int8_to_f16_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(
+      reinterpret_cast<const uint4*>(A), reinterpret_cast<uint4*>(a16), na, reinterpret_cast<const uint4*>(B),
+      reinterpret_cast<uint4*>(b16), nb);
+  timer.done();
+  int st = cudaGetLastError() == cudaSuccess ? QK_OK : QK_ERR_CUDA;
+  if (st == QK_OK) count_launches(1);
+
+  CUtensorMap ta, tb;
+  if (st == QK_OK)
+    st = encode_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a16, K, M, static_cast<uint64_t>(K) * 2, C::TMA_K, C::BM);
+  if (st == QK_OK)
+    st = encode_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, b16, K, N, static_cast<uint64_t>(K) * 2, C::TMA_K, C::BN);
+  if (st == QK_OK) {
+    GemmParams p{};
+    plan_tiles<C>(p, M, N, K);
+    p.sa = sa;
+    p.sb = sb;
+    p.bias = bias;
+    p.out = out;
+    p.err = dev.err_word;
+    p.timeout_ns = wait_timeout_ns();
+    st = launch_gemm<C>(ta, tb, p, dev, stream);
+  }
+  return st;
+}
+
+}  // namespace qk

@@ -11,6 +11,7 @@
 namespace qk {
 
 struct DeviceInfo {
+  int device = -1;
   int sm_count = 0;
   int cc_major = 0;
   int cc_minor = 0;
@@ -18,8 +19,11 @@ struct DeviceInfo {
   cudaMemPool_t pool = nullptr;            // stream-ordered workspace pool
 };
 
-// Cached facts about the current device; nullptr and *status set on failure.
+// Cached facts about the current device, with its workspace pool created on
+// first use; nullptr and *status set on failure.
 const DeviceInfo* current_device(int* status);
+// The same facts without creating the workspace pool (pool may be null).
+const DeviceInfo* current_device_basics(int* status);
 
 // 2-D tiled tensor map over a row-major [rows, inner] matrix with a 128-byte
 // swizzle and zero fill outside the matrix.  Returns QK_OK or QK_ERR_CUDA.

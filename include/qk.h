@@ -54,6 +54,7 @@ typedef void* qk_stream_t;
 #define QK_ERR_CUDA 5     /* a CUDA runtime/driver call or a kernel launch failed */
 #define QK_ERR_TIMEOUT 6  /* a bounded wait inside a kernel gave up (see qk_device_status) */
 #define QK_ERR_NOMEM 7    /* the library's stream-ordered workspace could not be allocated */
+#define QK_ERR_SCRATCH 8  /* the problem needs more than the fixed scratch of qk_gemm_int8_rowwise_noalloc */
 
 /* ---- operand formats for qk_gemm_mx ------------------------------------ */
 #define QK_FMT_MXFP8_E4M3 1 /* A, B: one E4M3 byte per element */
@@ -84,6 +85,32 @@ typedef void* qk_stream_t;
 int qk_gemm_int8_rowwise(const int8_t* A, const int8_t* B, const float* sa, const float* sb,
                          const uint16_t* bias, uint16_t* out, int64_t M, int64_t N, int64_t K,
                          qk_stream_t stream);
+
+/*
+ * qk_gemm_int8_rowwise without any memory allocation.  (The pages have no
+ * counterpart; this entry point exists for callers that cannot let a library
+ * allocate device memory: a process that gave all of HBM to its own
+ * allocator, a hot loop that must not pay for or block on allocator calls, or
+ * a policy that forbids a library to take memory behind the caller's back.)
+ *
+ * Same arguments, requirements and bit-identical result as
+ * qk_gemm_int8_rowwise.  Instead of a pooled workspace it widens A and B into
+ * one 32 MiB scratch array compiled into libqk.so, which every GPU that loads
+ * the library holds until the process exits.  It calls no cudaMalloc,
+ * cudaFree, memory-pool or other allocating routine.
+ *   - (M + N) * K * 2 must not exceed 32 MiB (33554432 bytes); larger
+ *     problems return QK_ERR_SCRATCH without launching anything.
+ *   - All calls on a device share that array: calls whose kernels can
+ *     overlap on the GPU (unordered streams) race and give wrong results.
+ *     Calls ordered on one stream are safe.  The array keeps the last call's
+ *     contents; no part of it needs to start at zero.
+ *   - The first call on a device looks up the array's device address (and,
+ *     as for every entry point, the device's attributes) with that device
+ *     current; make this first call before any stream capture.
+ */
+int qk_gemm_int8_rowwise_noalloc(const int8_t* A, const int8_t* B, const float* sa, const float* sb,
+                                 const uint16_t* bias, uint16_t* out, int64_t M, int64_t N, int64_t K,
+                                 qk_stream_t stream);
 
 /*
  * MX block-scaled GEMM (ROCm/mori PR #806, "What": "the same 32-wide ue8m0
