@@ -160,17 +160,40 @@ const DeviceInfo* current_device(int* status) {
   return &info;
 }
 
-int encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t inner, uint64_t rows,
-                   uint64_t row_pitch_bytes, uint32_t box_inner, uint32_t box_rows) {
+namespace {
+
+int encode_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t inner, uint64_t rows,
+              uint64_t row_pitch_bytes, uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle swizzle) {
   if (!g_encode) return QK_ERR_CUDA;
   const cuuint64_t dims[2] = {inner, rows};
   const cuuint64_t strides[1] = {row_pitch_bytes};
   const cuuint32_t box[2] = {box_inner, box_rows};
   const cuuint32_t estr[2] = {1, 1};
   const CUresult r = g_encode(map, dtype, 2, const_cast<void*>(base), dims, strides, box, estr,
-                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? QK_OK : QK_ERR_CUDA;
+}
+
+}  // namespace
+
+int encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t inner, uint64_t rows,
+                   uint64_t row_pitch_bytes, uint32_t box_inner, uint32_t box_rows) {
+  return encode_2d(map, dtype, base, inner, rows, row_pitch_bytes, box_inner, box_rows, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+int encode_tmap_2d_plain(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t inner,
+                         uint64_t rows, uint64_t row_pitch_bytes, uint32_t box_inner, uint32_t box_rows) {
+  return encode_2d(map, dtype, base, inner, rows, row_pitch_bytes, box_inner, box_rows, CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
+int raster_group_m() {
+  static const int g = [] {
+    const char* s = std::getenv("QK_GROUP_M");
+    const int v = (s && *s) ? std::atoi(s) : 0;
+    return (v >= 1 && v <= 4096) ? v : 8;
+  }();
+  return g;
 }
 
 __global__ void qk_wait_probe_kernel(unsigned long long* err, uint64_t timeout_ns) {

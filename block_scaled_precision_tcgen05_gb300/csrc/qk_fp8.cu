@@ -22,7 +22,7 @@ int launch_fp8_rowwise(const uint8_t* A, const uint8_t* B, const float* sa, cons
   p.out = out;
   p.err = dev.err_word;
   p.timeout_ns = wait_timeout_ns();
-  return launch_gemm<C>(ta, tb, p, dev, stream);
+  return launch_gemm<C>(ta, tb, ta, tb, p, dev, stream);
 }
 
 }  // namespace qk

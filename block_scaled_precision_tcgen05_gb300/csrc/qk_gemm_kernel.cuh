@@ -54,6 +54,8 @@ struct GemmParams {
   const uint8_t* sA;          // [M, sf_cols] UE8M0 (MX)
   const uint8_t* sB;          // [N, sf_cols] UE8M0 (MX)
   int sf_cols;                // K / 32
+  int sf_tma;                 // MX: scale rows fetched by TMA (sf_cols % 16 == 0, 16-byte aligned)
+  int group_m;                // row-blocks per raster group
   unsigned long long* err;    // device error word
   uint64_t timeout_ns;        // bound on every barrier wait
 };
@@ -85,11 +87,21 @@ struct GemmCfg {
   static constexpr int B_BYTES = BN * ROW_BYTES;
   static constexpr uint32_t STAGE_TX = A_BYTES + B_BYTES;
 
+  // Raw scale rows fetched by TMA: 16 bytes (16 scales) per row per fetch,
+  // i.e. RAW_KB ring stages' worth, double-buffered.
+  static constexpr int RAW_KB = MX ? 16 / SF_PER_STAGE : 1;
+  static constexpr int RAW_A_BYTES = MX ? BM * 16 : 0;
+  static constexpr int RAW_B_BYTES = MX ? NB128 * 128 * 16 : 0;
+  static constexpr int RAW_STAGE_BYTES = RAW_A_BYTES + RAW_B_BYTES;
+  static constexpr uint32_t RAW_TX = MX ? 16 * (BM + BN) : 0;
+  static constexpr int RAW_BUFS = MX ? 2 : 0;
+
   static constexpr int OFF_A = 0;
   static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
   static constexpr int OFF_SF = OFF_B + STAGES * B_BYTES;
-  static constexpr int OFF_BAR = OFF_SF + STAGES * SF_STAGE_BYTES;
-  static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC_BUFS + 1;
+  static constexpr int OFF_RAW = OFF_SF + STAGES * SF_STAGE_BYTES;
+  static constexpr int OFF_BAR = OFF_RAW + RAW_BUFS * RAW_STAGE_BYTES;
+  static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC_BUFS + 1 + RAW_BUFS;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack to align the base to 1024
 
@@ -107,7 +119,6 @@ struct GemmCfg {
                                                       : 512;
 
   static constexpr int NUM_THREADS = 256;
-  static constexpr int GROUP_M = 8;
 
   static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "tile N");
   static_assert(COLS_USED <= 512, "TMEM budget");
@@ -124,12 +135,11 @@ struct GemmCfg {
   }
 };
 
-template <int GROUP_M>
 __device__ __forceinline__ void tile_coords(const GemmParams& p, int t, int& mb, int& nb) {
-  const int group_tiles = GROUP_M * p.num_n_blocks;
+  const int group_tiles = p.group_m * p.num_n_blocks;
   const int g = t / group_tiles;
-  const int first_m = g * GROUP_M;
-  const int gm = min(p.num_m_blocks - first_m, GROUP_M);
+  const int first_m = g * p.group_m;
+  const int gm = min(p.num_m_blocks - first_m, p.group_m);
   const int local = t - g * group_tiles;
   mb = first_m + local % gm;
   nb = local / gm;
@@ -145,6 +155,17 @@ __device__ __forceinline__ uint32_t load_sf4(const uint8_t* s, int row, int rows
 #pragma unroll
   for (int i = 0; i < 4; ++i)
     if (col + i < cols) v |= static_cast<uint32_t>(__ldg(rp + col + i)) << (8 * i);
+  return v;
+}
+
+__device__ __forceinline__ uint32_t word_of(const uint4& v, int w) {
+  return w == 0 ? v.x : w == 1 ? v.y : w == 2 ? v.z : v.w;
+}
+
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr)
+               : "memory");
   return v;
 }
 
@@ -235,9 +256,170 @@ __device__ __forceinline__ void epilogue_row32(const GemmParams& p, int m, int n
   }
 }
 
+// Writes one ring stage's scale atoms from per-lane scale words.
+// a[j] holds 4 scale bytes of tile row 32j + lane (A), b[rb*4 + j] of B row
+// rb*128 + 32j + lane; atom g of the stage takes word `w0 + g`.
+template <class C>
+__device__ __forceinline__ void write_scale_atoms(uint32_t sf, int lane, const uint4 (&a)[4],
+                                                  const uint4 (&b)[4 * C::NB128], int w0) {
+#pragma unroll
+  for (int g = 0; g < C::SF_ATOMS_K; ++g) {
+    const int wd = w0 + g;
+    st_shared_v4(sf + 512 * g + 16 * lane, word_of(a[0], wd), word_of(a[1], wd), word_of(a[2], wd),
+                 word_of(a[3], wd));
+#pragma unroll
+    for (int rb = 0; rb < C::NB128; ++rb)
+      st_shared_v4(sf + C::SFA_BYTES + 512 * (g * C::NB128 + rb) + 16 * lane, word_of(b[4 * rb + 0], wd),
+                   word_of(b[4 * rb + 1], wd), word_of(b[4 * rb + 2], wd), word_of(b[4 * rb + 3], wd));
+  }
+}
+
+// Scale staging with TMA: one elected lane fetches 16 bytes of every scale row
+// of the tile (RAW_KB ring stages' worth) into a double-buffered raw area,
+// one fetch ahead (also across tiles); the warp then rearranges each stage's
+// scale bytes into the 512-byte atoms tcgen05.cp reads.  Shared loads and
+// stores are 16 bytes per lane over contiguous 512-byte spans (no bank
+// conflicts).
+template <class C>
+__device__ __forceinline__ void scale_stager_tma(const GemmParams& p, const CUtensorMap* tmSA,
+                                                 const CUtensorMap* tmSB, uint8_t* smem, uint64_t* full,
+                                                 uint64_t* empty, uint64_t* raw_full, const WaitCtl& w, int lane) {
+  const int n_raw = (p.num_kb + C::RAW_KB - 1) / C::RAW_KB;
+  auto issue = [&](int t, int r, uint32_t slot) {
+    int mb, nb;
+    tile_coords(p, t, mb, nb);
+    uint8_t* raw = smem + C::OFF_RAW + slot * C::RAW_STAGE_BYTES;
+    mbar_arrive_expect_tx(&raw_full[slot], C::RAW_TX);
+    tma_load_2d(raw, tmSA, &raw_full[slot], r * 16, mb * C::BM);
+    tma_load_2d(raw + C::RAW_A_BYTES, tmSB, &raw_full[slot], r * 16, nb * C::BN);
+  };
+  int stage = 0;
+  uint32_t phase = 0;
+  uint32_t seq = 0;     // raw fetches consumed so far
+  uint32_t issued = 0;  // raw fetches issued so far (same value in every lane)
+  int t = blockIdx.x;
+  int r = 0;
+  if (t < p.num_tiles) {
+    if (lane == 0) issue(t, 0, 0);
+    issued = 1;
+  }
+#pragma unroll 1
+  while (t < p.num_tiles) {
+    // prefetch the next fetch into the other slot (its previous contents were
+    // consumed by this warp in the previous iteration)
+    int t2 = t, r2 = r + 1;
+    if (r2 == n_raw) {
+      t2 = t + gridDim.x;
+      r2 = 0;
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (t2 < p.num_tiles) {
+      if (lane == 0) issue(t2, r2, (seq + 1) & 1u);
+      ++issued;
+    }
+    const uint32_t slot = seq & 1u;
+    if (!mbar_wait(&raw_full[slot], (seq >> 1) & 1u, w, kSiteScaleEmpty)) break;
+    const uint32_t raw = smem_u32(smem + C::OFF_RAW + slot * C::RAW_STAGE_BYTES);
+    uint4 a[4];
+    uint4 b[4 * C::NB128];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) a[j] = ld_shared_v4(raw + 16 * (32 * j + lane));
+#pragma unroll
+    for (int i = 0; i < 4 * C::NB128; ++i) b[i] = ld_shared_v4(raw + C::RAW_A_BYTES + 16 * (32 * i + lane));
+    ++seq;
+    bool ok = true;
+#pragma unroll
+    for (int sub = 0; sub < C::RAW_KB; ++sub) {
+      const int kb = r * C::RAW_KB + sub;
+      if (kb < p.num_kb) {
+        if (!mbar_wait(&empty[stage], phase ^ 1u, w, kSiteScaleEmpty)) {
+          ok = false;
+          break;
+        }
+        write_scale_atoms<C>(smem_u32(smem + C::OFF_SF + stage * C::SF_STAGE_BYTES), lane, a, b,
+                             sub * C::SF_ATOMS_K);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&full[stage]);
+        if (++stage == C::STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    if (!ok) break;
+    t = t2;
+    r = r2;
+  }
+  // leave no fetch in flight: wait (bounded) for every issued, unconsumed one
+#pragma unroll 1
+  for (uint32_t i = seq; i < issued; ++i) {
+    const uint32_t a = smem_u32(&raw_full[i & 1u]);
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait(a, (i >> 1) & 1u)) {
+      if (global_timer_ns() - t0 > p.timeout_ns) {
+        report_error(p.err, kDevErrTimeout, kSiteProducerDrain, i);
+        break;
+      }
+    }
+  }
+}
+
+// Scale staging with plain loads (any K % 32 == 0): per ring stage, four
+// scale bytes per row and atom, one 32-bit load each.
+template <class C>
+__device__ __forceinline__ void scale_stager_ldg(const GemmParams& p, uint8_t* smem, uint64_t* full, uint64_t* empty,
+                                                 const WaitCtl& w, int lane) {
+  int stage = 0;
+  uint32_t phase = 0;
+  bool ok = true;
+#pragma unroll 1
+  for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+    int mb, nb;
+    tile_coords(p, t, mb, nb);
+#pragma unroll 1
+    for (int kb = 0; kb < p.num_kb; ++kb) {
+      if (!mbar_wait(&empty[stage], phase ^ 1u, w, kSiteScaleEmpty)) {
+        ok = false;
+        break;
+      }
+      const uint32_t sf = smem_u32(smem + C::OFF_SF + stage * C::SF_STAGE_BYTES);
+      const int col0 = kb * C::SF_PER_STAGE;
+      // atom g: 128 rows x 4 bytes; row r = 32j + lane lives in 16-byte line `lane`, word j
+#pragma unroll
+      for (int g = 0; g < C::SF_ATOMS_K; ++g) {
+        uint32_t v[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) v[j] = load_sf4(p.sA, mb * C::BM + 32 * j + lane, p.M, col0 + 4 * g, p.sf_cols);
+        st_shared_v4(sf + 512 * g + 16 * lane, v[0], v[1], v[2], v[3]);
+      }
+#pragma unroll
+      for (int g = 0; g < C::SF_ATOMS_K; ++g) {
+#pragma unroll
+        for (int rb = 0; rb < C::NB128; ++rb) {
+          uint32_t v[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            v[j] = load_sf4(p.sB, nb * C::BN + rb * 128 + 32 * j + lane, p.N, col0 + 4 * g, p.sf_cols);
+          st_shared_v4(sf + C::SFA_BYTES + 512 * (g * C::NB128 + rb) + 16 * lane, v[0], v[1], v[2], v[3]);
+        }
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&full[stage]);
+      if (++stage == C::STAGES) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+  }
+}
+
 template <class C>
 __global__ void __launch_bounds__(C::NUM_THREADS, 1)
     qk_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
                    const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -246,6 +428,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
   uint64_t* acc_full = empty + C::STAGES;
   uint64_t* acc_empty = acc_full + C::ACC_BUFS;
   uint64_t* drain = acc_empty + C::ACC_BUFS;
+  uint64_t* raw_full = drain + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_MISC + 4);
 
@@ -264,10 +447,16 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
       mbar_init(&acc_empty[a], 4u);
     }
     mbar_init(drain, 1u);
+#pragma unroll 1
+    for (int b = 0; b < C::RAW_BUFS; ++b) mbar_init(&raw_full[b], 1u);
     *abort_flag = 0u;
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    if (C::MX && p.sf_tma) {
+      tma_prefetch_desc(&tmSA);
+      tma_prefetch_desc(&tmSB);
+    }
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, C::TMEM_COLS);
@@ -289,7 +478,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
 #pragma unroll 1
       for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
         int mb, nb;
-        tile_coords<C::GROUP_M>(p, t, mb, nb);
+        tile_coords(p, t, mb, nb);
 #pragma unroll 1
         for (int kb = 0; kb < p.num_kb; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, w, kSiteProducerEmpty)) {
@@ -419,50 +608,10 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
   } else if (warp == 2) {
     // ---------------- scale stager (MX) ----------------
     if constexpr (C::MX) {
-      int stage = 0;
-      uint32_t phase = 0;
-      bool ok = true;
-#pragma unroll 1
-      for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
-        int mb, nb;
-        tile_coords<C::GROUP_M>(p, t, mb, nb);
-#pragma unroll 1
-        for (int kb = 0; kb < p.num_kb; ++kb) {
-          if (!mbar_wait(&empty[stage], phase ^ 1u, w, kSiteScaleEmpty)) {
-            ok = false;
-            break;
-          }
-          const uint32_t sf = smem_u32(smem + C::OFF_SF + stage * C::SF_STAGE_BYTES);
-          const int col0 = kb * C::SF_PER_STAGE;
-          // A atom g: 128 rows x 4 bytes; row r = 32j + lane lives in 16-byte
-          // line `lane`, word j.
-#pragma unroll
-          for (int g = 0; g < C::SF_ATOMS_K; ++g) {
-            uint32_t v[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-              v[j] = load_sf4(p.sA, mb * C::BM + 32 * j + lane, p.M, col0 + 4 * g, p.sf_cols);
-            st_shared_v4(sf + 512 * g + 16 * lane, v[0], v[1], v[2], v[3]);
-          }
-#pragma unroll
-          for (int g = 0; g < C::SF_ATOMS_K; ++g) {
-#pragma unroll
-            for (int rb = 0; rb < C::NB128; ++rb) {
-              uint32_t v[4];
-#pragma unroll
-              for (int j = 0; j < 4; ++j)
-                v[j] = load_sf4(p.sB, nb * C::BN + rb * 128 + 32 * j + lane, p.N, col0 + 4 * g, p.sf_cols);
-              st_shared_v4(sf + C::SFA_BYTES + 512 * (g * C::NB128 + rb) + 16 * lane, v[0], v[1], v[2], v[3]);
-            }
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&full[stage]);
-          if (++stage == C::STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
+      if (p.sf_tma) {
+        scale_stager_tma<C>(p, &tmSA, &tmSB, smem, full, empty, raw_full, w, lane);
+      } else {
+        scale_stager_ldg<C>(p, smem, full, empty, w, lane);
       }
     }
     __syncwarp();
@@ -476,7 +625,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
 #pragma unroll 1
     for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
       int mb, nb;
-      tile_coords<C::GROUP_M>(p, t, mb, nb);
+      tile_coords(p, t, mb, nb);
       const int m = mb * C::BM + r;
       const bool row_ok = m < p.M;
       float sam = 1.f;

@@ -89,7 +89,7 @@ static inline int widen_and_gemm_int8(const int8_t* A, const int8_t* B, const fl
     p.out = out;
     p.err = dev.err_word;
     p.timeout_ns = wait_timeout_ns();
-    st = launch_gemm<C>(ta, tb, p, dev, stream);
+    st = launch_gemm<C>(ta, tb, ta, tb, p, dev, stream);
   }
   return st;
 }

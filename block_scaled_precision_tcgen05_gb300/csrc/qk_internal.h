@@ -30,6 +30,10 @@ const DeviceInfo* current_device_basics(int* status);
 int encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t inner, uint64_t rows,
                    uint64_t row_pitch_bytes, uint32_t box_inner, uint32_t box_rows);
 
+// The same without swizzle (raw byte rows, e.g. scale factors).
+int encode_tmap_2d_plain(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t inner,
+                         uint64_t rows, uint64_t row_pitch_bytes, uint32_t box_inner, uint32_t box_rows);
+
 uint64_t wait_timeout_ns();
 void count_launches(uint64_t n);
 

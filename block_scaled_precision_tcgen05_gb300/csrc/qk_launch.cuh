@@ -9,8 +9,12 @@ namespace qk {
 inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
 // Fills the tile/k-block bookkeeping of GemmParams for configuration C.
+// Row-blocks per raster group: QK_GROUP_M from the environment, else 8.
+int raster_group_m();
+
 template <class C>
 void plan_tiles(GemmParams& p, int M, int N, int K) {
+  p.group_m = raster_group_m();
   p.M = M;
   p.N = N;
   p.K = K;
@@ -32,15 +36,16 @@ constexpr int kernel_kind() {
   return C::kind == Kind::F16 ? kKGemmInt8 : C::kind == Kind::F8 ? kKGemmFp8 : C::kind == Kind::MXF8 ? kKGemmMxfp8 : kKGemmMxfp4;
 }
 
+// tsa / tsb: tensor maps of the raw scale rows (MX with p.sf_tma), else any map.
 template <class C>
-int launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, const DeviceInfo& dev,
-                cudaStream_t stream) {
+int launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsa, const CUtensorMap& tsb,
+                const GemmParams& p, const DeviceInfo& dev, cudaStream_t stream) {
   auto kernel = qk_gemm_kernel<C>;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return QK_ERR_CUDA;
   const int grid = p.num_tiles < dev.sm_count ? p.num_tiles : dev.sm_count;
   LaunchTimer timer(kernel_kind<C>(), stream);
-  kernel<<<grid, C::NUM_THREADS, C::SMEM_BYTES, stream>>>(ta, tb, p);
+  kernel<<<grid, C::NUM_THREADS, C::SMEM_BYTES, stream>>>(ta, tb, tsa, tsb, p);
   timer.done();
   e = cudaGetLastError();
   if (e != cudaSuccess) return QK_ERR_CUDA;

@@ -24,7 +24,19 @@ int launch_mxfp8(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const ui
   p.sf_cols = K / 32;
   p.err = dev.err_word;
   p.timeout_ns = wait_timeout_ns();
-  return launch_gemm<C>(ta, tb, p, dev, stream);
+  // Raw scale rows go through TMA when their pitch (K/32 bytes) and base
+  // addresses allow it (16-byte multiples); otherwise the scale warp loads them.
+  CUtensorMap tsa = ta, tsb = tb;
+  p.sf_tma = (p.sf_cols % 16 == 0 && (reinterpret_cast<uintptr_t>(sA) & 15u) == 0 &&
+              (reinterpret_cast<uintptr_t>(sB) & 15u) == 0)
+                 ? 1
+                 : 0;
+  if (p.sf_tma) {
+    st = encode_tmap_2d_plain(&tsa, CU_TENSOR_MAP_DATA_TYPE_UINT8, sA, p.sf_cols, M, p.sf_cols, 16, C::BM);
+    if (st == QK_OK) st = encode_tmap_2d_plain(&tsb, CU_TENSOR_MAP_DATA_TYPE_UINT8, sB, p.sf_cols, N, p.sf_cols, 16, C::BN);
+    if (st != QK_OK) return st;
+  }
+  return launch_gemm<C>(ta, tb, tsa, tsb, p, dev, stream);
 }
 
 }  // namespace qk
