@@ -41,6 +41,12 @@ namespace qk {
 
 enum class Kind : int { F16 = 0, F8 = 1, MXF8 = 2, MXF4 = 3 };
 
+// How the scale warp gets raw scale rows (MX kinds):
+//   kSfTma    TMA boxes of 16 bytes per row (K % 512 == 0, 16-byte aligned rows)
+//   kSfAsync  per-lane 4-byte cp.async into the same raw buffers (K % 128 == 0)
+//   kSfLoads  per-stage 32-bit loads straight into the atoms (any K % 32 == 0)
+enum : int { kSfLoads = 0, kSfTma = 1, kSfAsync = 2 };
+
 struct GemmParams {
   int M, N, K;
   int num_kb;                 // k-blocks (ring stages) per tile
@@ -54,17 +60,24 @@ struct GemmParams {
   const uint8_t* sA;          // [M, sf_cols] UE8M0 (MX)
   const uint8_t* sB;          // [N, sf_cols] UE8M0 (MX)
   int sf_cols;                // K / 32
-  int sf_tma;                 // MX: scale rows fetched by TMA (sf_cols % 16 == 0, 16-byte aligned)
+  int sf_mode;                // MX scale staging: kSfTma, kSfAsync or kSfLoads
   int group_m;                // row-blocks per raster group
   unsigned long long* err;    // device error word
   uint64_t timeout_ns;        // bound on every barrier wait
 };
 
-template <Kind KIND, int BN_, int STAGES_, int ACC_BUFS_>
+// PAIR_: a cluster of two CTAs computes a (2*128) x BN tile with 2-SM MMAs
+// (cta_group::2): each CTA holds 128 rows of A and BN/2 rows of B, the
+// leader CTA issues the MMAs, each CTA's TMEM receives its 128 rows of D.
+template <Kind KIND, int BN_, int STAGES_, int ACC_BUFS_, bool PAIR_ = false>
 struct GemmCfg {
   static constexpr Kind kind = KIND;
-  static constexpr int BM = 128;
-  static constexpr int BN = BN_;
+  static constexpr bool PAIR = PAIR_;
+  static constexpr int CTAS = PAIR ? 2 : 1;
+  static constexpr int BM = 128;                 // rows of A (and D) per CTA
+  static constexpr int MMA_M = BM * CTAS;        // rows of a tile
+  static constexpr int BN = BN_;                 // columns of a tile
+  static constexpr int B_ROWS = BN / CTAS;       // rows of B per CTA
   static constexpr int STAGES = STAGES_;
   static constexpr int ACC_BUFS = ACC_BUFS_;
   static constexpr int ROW_BYTES = 128;  // bytes of K per row per ring stage (one swizzle row)
@@ -84,8 +97,8 @@ struct GemmCfg {
   static constexpr int SF_STAGE_BYTES = SFA_BYTES + SFB_BYTES;
 
   static constexpr int A_BYTES = BM * ROW_BYTES;
-  static constexpr int B_BYTES = BN * ROW_BYTES;
-  static constexpr uint32_t STAGE_TX = A_BYTES + B_BYTES;
+  static constexpr int B_BYTES = B_ROWS * ROW_BYTES;
+  static constexpr uint32_t STAGE_TX = CTAS * (A_BYTES + B_BYTES);  // bytes one ring stage receives per tile
 
   // Raw scale rows fetched by TMA: 16 bytes (16 scales) per row per fetch,
   // i.e. RAW_KB ring stages' worth, double-buffered.
@@ -121,6 +134,7 @@ struct GemmCfg {
   static constexpr int NUM_THREADS = 256;
 
   static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "tile N");
+  static_assert(!(PAIR && MX), "CTA pairs are used for the dense kinds only");
   static_assert(COLS_USED <= 512, "TMEM budget");
   static_assert(SMEM_BYTES <= 232448, "shared-memory budget");
   static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "swizzle atoms need 1024-byte alignment");
@@ -128,8 +142,8 @@ struct GemmCfg {
   // kind::f16: D fp32 (1), A/B f16 (0).  kind::f8f6f4: A/B E4M3 (0).
   // kind::mxf8f6f4: E4M3 (0).  kind::mxf4: E2M1 (1).
   __host__ __device__ static constexpr uint32_t idesc(uint32_t a_sf_id, uint32_t b_sf_id) {
-    return KIND == Kind::F16    ? make_idesc_dense(1, 0, 0, BM, BN)
-           : KIND == Kind::F8   ? make_idesc_dense(1, 0, 0, BM, BN)
+    return KIND == Kind::F16    ? make_idesc_dense(1, 0, 0, MMA_M, BN)
+           : KIND == Kind::F8   ? make_idesc_dense(1, 0, 0, MMA_M, BN)
            : KIND == Kind::MXF8 ? make_idesc_block_scaled(0, 0, BM, BN, a_sf_id, b_sf_id)
                                 : make_idesc_block_scaled(1, 1, BM, BN, a_sf_id, b_sf_id);
   }
@@ -274,24 +288,66 @@ __device__ __forceinline__ void write_scale_atoms(uint32_t sf, int lane, const u
   }
 }
 
-// Scale staging with TMA: one elected lane fetches 16 bytes of every scale row
-// of the tile (RAW_KB ring stages' worth) into a double-buffered raw area,
-// one fetch ahead (also across tiles); the warp then rearranges each stage's
-// scale bytes into the 512-byte atoms tcgen05.cp reads.  Shared loads and
-// stores are 16 bytes per lane over contiguous 512-byte spans (no bank
-// conflicts).
+__device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// Raw fetch by the whole warp with 4-byte cp.async: lane l copies the 16-byte
+// chunk `r` of scale rows l + 32i (A: 128 rows, B: NB128*128 rows), zero-filled
+// past the matrix; each lane's copies arrive once on `bar` when they land.
 template <class C>
-__device__ __forceinline__ void scale_stager_tma(const GemmParams& p, const CUtensorMap* tmSA,
+__device__ __forceinline__ void raw_fetch_async(const GemmParams& p, uint32_t raw, uint64_t* bar, int mb, int nb,
+                                                int r, int lane) {
+  const int col0 = r * 16;
+#pragma unroll
+  for (int i = 0; i < 4 + 4 * C::NB128; ++i) {
+    const bool is_a = i < 4;
+    const int local = 32 * (is_a ? i : i - 4) + lane;
+    const int row = is_a ? mb * C::BM + local : nb * C::BN + local;
+    const int rows = is_a ? p.M : p.N;
+    const uint8_t* base = is_a ? p.sA : p.sB;
+    const uint32_t dst = raw + (is_a ? 0 : C::RAW_A_BYTES) + 16 * local;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int col = col0 + 4 * q;
+      const bool ok = row < rows && col < p.sf_cols;
+      const uint8_t* src = ok ? base + static_cast<size_t>(row) * static_cast<size_t>(p.sf_cols) + col : base;
+      cp_async_4(dst + 4 * q, src, ok ? 4u : 0u);
+    }
+  }
+  cp_async_arrive_noinc(bar);
+}
+
+// Scale staging from raw rows: 16 bytes of every scale row of the tile
+// (RAW_KB ring stages' worth) are fetched into a double-buffered raw area, one
+// fetch ahead (also across tiles) -- by TMA from one elected lane, or by
+// per-lane cp.async when the row pitch rules TMA out; the warp then
+// rearranges each stage's scale bytes into the 512-byte atoms tcgen05.cp
+// reads.  Shared loads and stores are 16 bytes per lane over contiguous
+// 512-byte spans (no bank conflicts).
+template <class C>
+__device__ __forceinline__ void scale_stager_raw(const GemmParams& p, const CUtensorMap* tmSA,
                                                  const CUtensorMap* tmSB, uint8_t* smem, uint64_t* full,
                                                  uint64_t* empty, uint64_t* raw_full, const WaitCtl& w, int lane) {
   const int n_raw = (p.num_kb + C::RAW_KB - 1) / C::RAW_KB;
+  const bool by_tma = p.sf_mode == kSfTma;
   auto issue = [&](int t, int r, uint32_t slot) {
     int mb, nb;
     tile_coords(p, t, mb, nb);
     uint8_t* raw = smem + C::OFF_RAW + slot * C::RAW_STAGE_BYTES;
-    mbar_arrive_expect_tx(&raw_full[slot], C::RAW_TX);
-    tma_load_2d(raw, tmSA, &raw_full[slot], r * 16, mb * C::BM);
-    tma_load_2d(raw + C::RAW_A_BYTES, tmSB, &raw_full[slot], r * 16, nb * C::BN);
+    if (by_tma) {
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&raw_full[slot], C::RAW_TX);
+        tma_load_2d(raw, tmSA, &raw_full[slot], r * 16, mb * C::BM);
+        tma_load_2d(raw + C::RAW_A_BYTES, tmSB, &raw_full[slot], r * 16, nb * C::BN);
+      }
+    } else {
+      raw_fetch_async<C>(p, smem_u32(raw), &raw_full[slot], mb, nb, r, lane);
+    }
   };
   int stage = 0;
   uint32_t phase = 0;
@@ -300,7 +356,7 @@ __device__ __forceinline__ void scale_stager_tma(const GemmParams& p, const CUte
   int t = blockIdx.x;
   int r = 0;
   if (t < p.num_tiles) {
-    if (lane == 0) issue(t, 0, 0);
+    issue(t, 0, 0);
     issued = 1;
   }
 #pragma unroll 1
@@ -315,7 +371,7 @@ __device__ __forceinline__ void scale_stager_tma(const GemmParams& p, const CUte
     fence_proxy_async_smem();
     __syncwarp();
     if (t2 < p.num_tiles) {
-      if (lane == 0) issue(t2, r2, (seq + 1) & 1u);
+      issue(t2, r2, (seq + 1) & 1u);
       ++issued;
     }
     const uint32_t slot = seq & 1u;
@@ -434,6 +490,11 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const uint32_t rank = C::PAIR ? cluster_ctarank() : 0u;  // CTA within the pair
+  const bool leader = rank == 0u;                           // issues the MMAs
+  // tiles are walked per cluster (one CTA or a pair)
+  const int tile0 = static_cast<int>(blockIdx.x) / C::CTAS;
+  const int tile_step = static_cast<int>(gridDim.x) / C::CTAS;
 
   if (threadIdx.x == 0) {
 #pragma unroll 1
@@ -444,26 +505,32 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
 #pragma unroll 1
     for (int a = 0; a < C::ACC_BUFS; ++a) {
       mbar_init(&acc_full[a], 1u);
-      mbar_init(&acc_empty[a], 4u);
+      mbar_init(&acc_empty[a], 4u * C::CTAS);
     }
     mbar_init(drain, 1u);
 #pragma unroll 1
-    for (int b = 0; b < C::RAW_BUFS; ++b) mbar_init(&raw_full[b], 1u);
+    for (int b = 0; b < C::RAW_BUFS; ++b) mbar_init(&raw_full[b], p.sf_mode == kSfAsync ? 32u : 1u);
     *abort_flag = 0u;
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
-    if (C::MX && p.sf_tma) {
+    if (C::MX && p.sf_mode == kSfTma) {
       tma_prefetch_desc(&tmSA);
       tma_prefetch_desc(&tmSB);
     }
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, C::TMEM_COLS);
-    tmem_relinquish();
+    if constexpr (C::PAIR) {
+      tmem_alloc_pair(tmem_slot, C::TMEM_COLS);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(tmem_slot, C::TMEM_COLS);
+      tmem_relinquish();
+    }
   }
   tc_fence_before_sync();
   __syncthreads();
+  if constexpr (C::PAIR) cluster_sync();  // peers' barriers exist before anyone signals them
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
   const WaitCtl w{abort_flag, p.err, p.timeout_ns};
@@ -476,18 +543,29 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
       long long issued = 0;
       bool ok = true;
 #pragma unroll 1
-      for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+      // in a pair, both CTAs' loads complete on the leader's ring barriers
+      const uint32_t full_leader = C::PAIR ? mapa_shared(smem_u32(&full[0]), 0u) : 0u;
+      for (int t = tile0; ok && t < p.num_tiles; t += tile_step) {
         int mb, nb;
         tile_coords(p, t, mb, nb);
+        const int a_row = mb * C::MMA_M + static_cast<int>(rank) * C::BM;
+        const int b_row = nb * C::BN + static_cast<int>(rank) * C::B_ROWS;
 #pragma unroll 1
         for (int kb = 0; kb < p.num_kb; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, w, kSiteProducerEmpty)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&full[stage], C::STAGE_TX);
-          tma_load_2d(smem + C::OFF_A + stage * C::A_BYTES, &tmA, &full[stage], kb * C::TMA_K, mb * C::BM);
-          tma_load_2d(smem + C::OFF_B + stage * C::B_BYTES, &tmB, &full[stage], kb * C::TMA_K, nb * C::BN);
+          if constexpr (C::PAIR) {
+            if (leader) mbar_arrive_expect_tx(&full[stage], C::STAGE_TX);
+            const uint32_t fb = full_leader + 8u * static_cast<uint32_t>(stage);
+            tma_load_2d_pair(smem + C::OFF_A + stage * C::A_BYTES, &tmA, fb, kb * C::TMA_K, a_row);
+            tma_load_2d_pair(smem + C::OFF_B + stage * C::B_BYTES, &tmB, fb, kb * C::TMA_K, b_row);
+          } else {
+            mbar_arrive_expect_tx(&full[stage], C::STAGE_TX);
+            tma_load_2d(smem + C::OFF_A + stage * C::A_BYTES, &tmA, &full[stage], kb * C::TMA_K, a_row);
+            tma_load_2d(smem + C::OFF_B + stage * C::B_BYTES, &tmB, &full[stage], kb * C::TMA_K, b_row);
+          }
           ++issued;
           if (++stage == C::STAGES) {
             stage = 0;
@@ -496,10 +574,13 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
         }
       }
       // Do not leave the CTA with tile loads in flight: wait (bounded) for the
-      // most recent load of every ring slot.
+      // most recent load of every ring slot.  In a pair only the leader's
+      // barriers count the loads; the peer is held by the final cluster
+      // barrier until the leader has seen them land.
       const WaitCtl wd{abort_flag, p.err, p.timeout_ns};
+      const long long drain_n = leader ? (issued < C::STAGES ? issued : C::STAGES) : 0;
 #pragma unroll 1
-      for (long long i = 0; i < (issued < C::STAGES ? issued : C::STAGES); ++i) {
+      for (long long i = 0; i < drain_n; ++i) {
         const long long L = issued - 1 - i;
         uint64_t* bar = &full[static_cast<int>(L % C::STAGES)];
         const uint32_t par = static_cast<uint32_t>((L / C::STAGES) & 1);
@@ -515,19 +596,21 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
     }
     __syncwarp();
   } else if (warp == 1) {
-    // ---------------- MMA issuer ----------------
-    if (lane == 0) {
+    // ---------------- MMA issuer (the leader CTA of a pair) ----------------
+    if (lane == 0 && leader) {
       int stage = 0;
       uint32_t phase = 0;
       uint32_t acc_iter = 0;
       bool ok = true;
 #pragma unroll 1
-      for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+      for (int t = tile0; ok && t < p.num_tiles; t += tile_step) {
 #pragma unroll 1
         for (int c = 0; ok && c < p.num_chunks; ++c) {
           const int a = static_cast<int>(acc_iter % C::ACC_BUFS);
           const uint32_t aph = (acc_iter / C::ACC_BUFS) & 1u;
-          if (!mbar_wait(&acc_empty[a], aph ^ 1u, w, kSiteMmaAccEmpty)) {
+          const bool got = C::PAIR ? mbar_wait_cluster(&acc_empty[a], aph ^ 1u, w, kSiteMmaAccEmpty)
+                                   : mbar_wait(&acc_empty[a], aph ^ 1u, w, kSiteMmaAccEmpty);
+          if (!got) {
             ok = false;
             break;
           }
@@ -566,7 +649,11 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                 const uint32_t accum = (kb > kb0 || j > 0) ? 1u : 0u;
                 const uint64_t ad = adesc + static_cast<uint64_t>((j * 32) >> 4);
                 const uint64_t bd = bdesc + static_cast<uint64_t>((j * 32) >> 4);
-                if constexpr (C::kind == Kind::F16) {
+                if constexpr (C::kind == Kind::F16 && C::PAIR) {
+                  umma_f16_pair(d_tmem, ad, bd, C::idesc(0, 0), accum);
+                } else if constexpr (C::kind == Kind::F8 && C::PAIR) {
+                  umma_f8f6f4_pair(d_tmem, ad, bd, C::idesc(0, 0), accum);
+                } else if constexpr (C::kind == Kind::F16) {
                   umma_f16(d_tmem, ad, bd, C::idesc(0, 0), accum);
                 } else if constexpr (C::kind == Kind::F8) {
                   umma_f8f6f4(d_tmem, ad, bd, C::idesc(0, 0), accum);
@@ -582,19 +669,31 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                 }
               }
             }
-            umma_commit(&empty[stage]);
+            if constexpr (C::PAIR) {
+              umma_commit_pair_multicast(&empty[stage], 0x3);  // frees the slot in both CTAs
+            } else {
+              umma_commit(&empty[stage]);
+            }
             if (++stage == C::STAGES) {
               stage = 0;
               phase ^= 1u;
             }
           }
           if (!ok) break;
-          umma_commit(&acc_full[a]);
+          if constexpr (C::PAIR) {
+            umma_commit_pair_multicast(&acc_full[a], 0x3);
+          } else {
+            umma_commit(&acc_full[a]);
+          }
           ++acc_iter;
         }
       }
       // Every MMA and copy this thread issued completes before TMEM is freed.
-      umma_commit(drain);
+      if constexpr (C::PAIR) {
+        umma_commit_pair(drain);
+      } else {
+        umma_commit(drain);
+      }
       const uint32_t da = smem_u32(drain);
       const uint64_t t0 = global_timer_ns();
       while (!mbar_try_wait(da, 0u)) {
@@ -608,8 +707,8 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
   } else if (warp == 2) {
     // ---------------- scale stager (MX) ----------------
     if constexpr (C::MX) {
-      if (p.sf_tma) {
-        scale_stager_tma<C>(p, &tmSA, &tmSB, smem, full, empty, raw_full, w, lane);
+      if (p.sf_mode == kSfTma || p.sf_mode == kSfAsync) {
+        scale_stager_raw<C>(p, &tmSA, &tmSB, smem, full, empty, raw_full, w, lane);
       } else {
         scale_stager_ldg<C>(p, smem, full, empty, w, lane);
       }
@@ -622,11 +721,13 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16);
     uint32_t acc_iter = 0;
     bool ok = true;
+    // accumulator releases go to the leader CTA's barrier
+    const uint32_t acc_empty_leader = C::PAIR ? mapa_shared(smem_u32(&acc_empty[0]), 0u) : 0u;
 #pragma unroll 1
-    for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+    for (int t = tile0; ok && t < p.num_tiles; t += tile_step) {
       int mb, nb;
       tile_coords(p, t, mb, nb);
-      const int m = mb * C::BM + r;
+      const int m = mb * C::MMA_M + static_cast<int>(rank) * C::BM + r;
       const bool row_ok = m < p.M;
       float sam = 1.f;
       if constexpr (C::ROWWISE) sam = row_ok ? __ldg(p.sa + m) : 0.f;
@@ -641,6 +742,10 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
         }
         tc_fence_after_sync();
         const bool last = c == p.num_chunks - 1;
+        // With one accumulator the final chunk's totals go back to the TMEM sum
+        // region first, so the accumulator is released before the slow part
+        // (scaling, rounding, stores) and the next tile's MMAs can start.
+        const bool early_release = C::INT_CHUNKS && C::ACC_BUFS == 1 && last;
 #pragma unroll 1
         for (int g = 0; g < C::BN / 32; ++g) {
           const int n0 = n_tile + 32 * g;
@@ -658,7 +763,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
 #pragma unroll
               for (int i = 0; i < 32; ++i) v[i] += s[i];
             }
-            if (!last) {
+            if (!last || early_release) {
               tmem_st_32cols(lane_base + static_cast<uint32_t>(C::COL_SUM + 32 * g), v);
             } else if (row_ok && n0 < p.N) {
               epilogue_row32<true, true>(p, m, n0, sam, v);
@@ -670,7 +775,23 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
         if constexpr (C::INT_CHUNKS) tmem_wait_st();
         tc_fence_before_sync();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&acc_empty[a]);
+        if (lane == 0) {
+          if constexpr (C::PAIR) {
+            mbar_arrive_cluster(acc_empty_leader + 8u * static_cast<uint32_t>(a));
+          } else {
+            mbar_arrive(&acc_empty[a]);
+          }
+        }
+        if (early_release) {
+#pragma unroll 1
+          for (int g = 0; g < C::BN / 32; ++g) {
+            const int n0 = n_tile + 32 * g;
+            uint32_t v[32];
+            tmem_ld_32cols(lane_base + static_cast<uint32_t>(C::COL_SUM + 32 * g), v);
+            tmem_wait_ld();
+            if (row_ok && n0 < p.N) epilogue_row32<true, true>(p, m, n0, sam, v);
+          }
+        }
         ++acc_iter;
       }
     }
@@ -679,8 +800,15 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
 
   tc_fence_before_sync();
   __syncthreads();
+  if constexpr (C::PAIR) cluster_sync();  // the pair finishes together; TMEM is freed by both
   tc_fence_after_sync();
-  if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
+  if (warp == 1) {
+    if constexpr (C::PAIR) {
+      tmem_dealloc_pair(tmem, C::TMEM_COLS);
+    } else {
+      tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+  }
 }
 
 }  // namespace qk

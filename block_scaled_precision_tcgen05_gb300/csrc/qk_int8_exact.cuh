@@ -18,7 +18,9 @@
 
 namespace qk {
 
-using CfgInt8 = GemmCfg<Kind::F16, 128, 6, 2>;
+// 256 x 256 tiles per CTA pair: one fp32 accumulator (256 columns) and the
+// int32 running sums (256 columns) fill the 512 TMEM columns of each SM.
+using CfgInt8 = GemmCfg<Kind::F16, 256, 6, 1, true>;
 
 // Widens 16 int8 values per thread-iteration to f16.  Byte x becomes the f16
 // bit pattern 0x6400 | (x + 128), i.e. the value 1024 + x + 128, and one
@@ -79,7 +81,7 @@ static inline int widen_and_gemm_int8(const int8_t* A, const int8_t* B, const fl
   if (st == QK_OK)
     st = encode_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a16, K, M, static_cast<uint64_t>(K) * 2, C::TMA_K, C::BM);
   if (st == QK_OK)
-    st = encode_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, b16, K, N, static_cast<uint64_t>(K) * 2, C::TMA_K, C::BN);
+    st = encode_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, b16, K, N, static_cast<uint64_t>(K) * 2, C::TMA_K, C::B_ROWS);
   if (st == QK_OK) {
     GemmParams p{};
     plan_tiles<C>(p, M, N, K);

@@ -19,7 +19,7 @@ void plan_tiles(GemmParams& p, int M, int N, int K) {
   p.N = N;
   p.K = K;
   p.num_kb = ceil_div(K, C::K_ELEMS);
-  p.num_m_blocks = ceil_div(M, C::BM);
+  p.num_m_blocks = ceil_div(M, C::MMA_M);
   p.num_n_blocks = ceil_div(N, C::BN);
   p.num_tiles = p.num_m_blocks * p.num_n_blocks;
   if (C::INT_CHUNKS) {
@@ -43,12 +43,42 @@ int launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap&
   auto kernel = qk_gemm_kernel<C>;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return QK_ERR_CUDA;
-  const int grid = p.num_tiles < dev.sm_count ? p.num_tiles : dev.sm_count;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(C::NUM_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  int slots = dev.sm_count;  // concurrently resident CTAs (one per SM) or CTA pairs
+  if constexpr (C::PAIR) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    // how many pairs fit at once (SMs pair up within a GPC), computed once per device
+    static int cached[64];
+    int& clusters = cached[dev.device >= 0 && dev.device < 64 ? dev.device : 0];
+    if (clusters == 0) {
+      cfg.gridDim = dim3(2 * (dev.sm_count / 2), 1, 1);
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess || n <= 0) {
+        cudaGetLastError();
+        n = dev.sm_count / 2;
+      }
+      clusters = n;
+    }
+    slots = clusters;
+  }
+  const int ctas = (p.num_tiles < slots ? p.num_tiles : slots) * C::CTAS;
+  cfg.gridDim = dim3(ctas, 1, 1);
   LaunchTimer timer(kernel_kind<C>(), stream);
-  kernel<<<grid, C::NUM_THREADS, C::SMEM_BYTES, stream>>>(ta, tb, tsa, tsb, p);
+  e = cudaLaunchKernelEx(&cfg, kernel, ta, tb, tsa, tsb, p);
   timer.done();
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return QK_ERR_CUDA;
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return QK_ERR_CUDA;
+  }
   count_launches(1);
   return QK_OK;
 }

@@ -13,7 +13,7 @@ int launch_mxfp8(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const ui
   using C = CfgMxfp8;
   CUtensorMap ta, tb;
   int st = encode_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, K, M, K, C::TMA_K, C::BM);
-  if (st == QK_OK) st = encode_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, K, N, K, C::TMA_K, C::BN);
+  if (st == QK_OK) st = encode_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, K, N, K, C::TMA_K, C::B_ROWS);
   if (st != QK_OK) return st;
   GemmParams p{};
   plan_tiles<C>(p, M, N, K);
@@ -25,13 +25,12 @@ int launch_mxfp8(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const ui
   p.err = dev.err_word;
   p.timeout_ns = wait_timeout_ns();
   // Raw scale rows go through TMA when their pitch (K/32 bytes) and base
-  // addresses allow it (16-byte multiples); otherwise the scale warp loads them.
+  // addresses are 16-byte multiples, through cp.async when they are 4-byte
+  // multiples, else through per-stage loads.
   CUtensorMap tsa = ta, tsb = tb;
-  p.sf_tma = (p.sf_cols % 16 == 0 && (reinterpret_cast<uintptr_t>(sA) & 15u) == 0 &&
-              (reinterpret_cast<uintptr_t>(sB) & 15u) == 0)
-                 ? 1
-                 : 0;
-  if (p.sf_tma) {
+  const bool a16 = ((reinterpret_cast<uintptr_t>(sA) | reinterpret_cast<uintptr_t>(sB)) & 15u) == 0;
+  p.sf_mode = (p.sf_cols % 16 == 0 && a16) ? kSfTma : (p.sf_cols % 4 == 0 ? kSfAsync : kSfLoads);
+  if (p.sf_mode == kSfTma) {
     st = encode_tmap_2d_plain(&tsa, CU_TENSOR_MAP_DATA_TYPE_UINT8, sA, p.sf_cols, M, p.sf_cols, 16, C::BM);
     if (st == QK_OK) st = encode_tmap_2d_plain(&tsb, CU_TENSOR_MAP_DATA_TYPE_UINT8, sB, p.sf_cols, N, p.sf_cols, 16, C::BN);
     if (st != QK_OK) return st;
