@@ -69,7 +69,11 @@ struct GemmParams {
 // PAIR_: a cluster of two CTAs computes a (2*128) x BN tile with 2-SM MMAs
 // (cta_group::2): each CTA holds 128 rows of A and BN/2 rows of B, the
 // leader CTA issues the MMAs, each CTA's TMEM receives its 128 rows of D.
-template <Kind KIND, int BN_, int STAGES_, int ACC_BUFS_, bool PAIR_ = false>
+// EPI_WARPS_: epilogue warps (a multiple of 4; each group of four covers all
+// 128 TMEM lanes for BN / (EPI_WARPS_/4) columns).  For the exact INT8 kind,
+// 16 epilogue warps keep the int32 running sums in registers (64 columns per
+// thread) instead of TMEM, which frees TMEM for two accumulators.
+template <Kind KIND, int BN_, int STAGES_, int ACC_BUFS_, bool PAIR_ = false, int EPI_WARPS_ = 4>
 struct GemmCfg {
   static constexpr Kind kind = KIND;
   static constexpr bool PAIR = PAIR_;
@@ -88,6 +92,10 @@ struct GemmCfg {
   static constexpr bool MX = KIND == Kind::MXF8 || KIND == Kind::MXF4;
   static constexpr bool INT_CHUNKS = KIND == Kind::F16;
   static constexpr bool ROWWISE = KIND == Kind::F16 || KIND == Kind::F8;
+  static constexpr int EPI_WARPS = EPI_WARPS_;
+  static constexpr int EPI_PARTS = EPI_WARPS / 4;     // column parts of a tile
+  static constexpr int EPI_COLS = BN_ / EPI_PARTS;    // columns per epilogue warp
+  static constexpr bool REG_SUMS = INT_CHUNKS && EPI_WARPS == 16;
 
   static constexpr int SF_PER_STAGE = MX ? K_ELEMS / 32 : 0;  // scale bytes per row per stage
   static constexpr int SF_ATOMS_K = SF_PER_STAGE / 4;         // 4 scale bytes per 32-bit TMEM column
@@ -120,7 +128,7 @@ struct GemmCfg {
 
   static constexpr int COL_ACC = 0;
   static constexpr int COL_SUM = ACC_BUFS * BN;
-  static constexpr int COL_SF = COL_SUM + (INT_CHUNKS ? BN : 0);
+  static constexpr int COL_SF = COL_SUM + (INT_CHUNKS && !REG_SUMS ? BN : 0);
   static constexpr int SF_COLS_A = SF_ATOMS_K * 4;
   static constexpr int SF_COLS_B = SF_ATOMS_K * NB128 * 4;
   static constexpr int SF_COLS_STAGE = MX ? SF_COLS_A + SF_COLS_B : 0;
@@ -131,10 +139,12 @@ struct GemmCfg {
                                    : COLS_USED <= 256 ? 256
                                                       : 512;
 
-  static constexpr int NUM_THREADS = 256;
+  static constexpr int NUM_THREADS = 32 * (4 + EPI_WARPS);
 
   static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "tile N");
   static_assert(!(PAIR && MX), "CTA pairs are used for the dense kinds only");
+  static_assert(EPI_WARPS % 4 == 0 && EPI_COLS % 32 == 0, "epilogue split");
+  static_assert(!REG_SUMS || EPI_COLS == 64, "register sums hold 64 columns per thread");
   static_assert(COLS_USED <= 512, "TMEM budget");
   static_assert(SMEM_BYTES <= 232448, "shared-memory budget");
   static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "swizzle atoms need 1024-byte alignment");
@@ -198,75 +208,55 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return l | (h << 16);
 }
 
-// Epilogue of 32 consecutive columns [n0, n0+32) of one row m.
-// INT_ACC: v holds int32 sums; otherwise fp32 bit patterns.
-template <bool ROWWISE, bool INT_ACC>
+// Epilogue of 32 consecutive columns [n0, n0+32) of one row m, in four steps
+// of 8 columns (8 column scales, 8 biases and one 16-byte store live at a
+// time).  INT_ACC: v holds int32 sums; otherwise fp32 bit patterns.  N is a
+// multiple of 8, so every 8-column step is either fully inside or outside.
+template <bool ROWWISE, bool INT_ACC, int OFF = 0, int LEN = 32>
 __device__ __forceinline__ void epilogue_row32(const GemmParams& p, int m, int n0, float sam,
-                                               const uint32_t (&v)[32]) {
-  const bool full = n0 + 32 <= p.N;
-  float sbv[32];
-  float bv[32];
+                                               const uint32_t (&v)[LEN]) {
   const bool has_bias = p.bias != nullptr;
-  if (full) {
-    if constexpr (ROWWISE) {
-      const float4* s4 = reinterpret_cast<const float4*>(p.sb + n0);
+  uint16_t* dst = p.out + static_cast<size_t>(m) * static_cast<size_t>(p.N) + n0;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float4 t = __ldg(s4 + i);
-        sbv[4 * i + 0] = t.x;
-        sbv[4 * i + 1] = t.y;
-        sbv[4 * i + 2] = t.z;
-        sbv[4 * i + 3] = t.w;
+  for (int s8 = 0; s8 < 4; ++s8) {
+    const int n = n0 + 8 * s8;
+    if (n < p.N) {
+      float sbv[8];
+      float bv[8];
+      if constexpr (ROWWISE) {
+        const float4 t0 = __ldg(reinterpret_cast<const float4*>(p.sb + n));
+        const float4 t1 = __ldg(reinterpret_cast<const float4*>(p.sb + n) + 1);
+        sbv[0] = t0.x; sbv[1] = t0.y; sbv[2] = t0.z; sbv[3] = t0.w;
+        sbv[4] = t1.x; sbv[5] = t1.y; sbv[6] = t1.z; sbv[7] = t1.w;
       }
-    }
-    if (has_bias) {
-      const uint4* b4 = reinterpret_cast<const uint4*>(p.bias + n0);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint4 t = __ldg(b4 + i);
-        const uint32_t w[4] = {t.x, t.y, t.z, t.w};
+      if (has_bias) {
+        const uint4 t = __ldg(reinterpret_cast<const uint4*>(p.bias + n));
+        const uint32_t wv[4] = {t.x, t.y, t.z, t.w};
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          bv[8 * i + 2 * j + 0] = __uint_as_float(w[j] << 16);
-          bv[8 * i + 2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+          bv[2 * j + 0] = __uint_as_float(wv[j] << 16);
+          bv[2 * j + 1] = __uint_as_float(wv[j] & 0xFFFF0000u);
         }
       }
-    }
-  } else {
+      uint32_t packed[4];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const int n = n0 + i;
-      if constexpr (ROWWISE) sbv[i] = n < p.N ? __ldg(p.sb + n) : 0.f;
-      bv[i] = (has_bias && n < p.N) ? bf16_bits_to_float(__ldg(p.bias + n)) : 0.f;
-    }
-  }
-  uint32_t packed[16];
+      for (int i = 0; i < 8; i += 2) {
+        float x[2];
 #pragma unroll
-  for (int i = 0; i < 32; i += 2) {
-    float x[2];
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      float t = INT_ACC ? __int2float_rn(static_cast<int>(v[i + j])) : __uint_as_float(v[i + j]);
-      if constexpr (ROWWISE) {
-        t = __fmul_rn(t, sam);
-        t = __fmul_rn(t, sbv[i + j]);
+        for (int j = 0; j < 2; ++j) {
+          const uint32_t raw = v[OFF + 8 * s8 + i + j];
+          float t = INT_ACC ? __int2float_rn(static_cast<int>(raw)) : __uint_as_float(raw);
+          if constexpr (ROWWISE) {
+            t = __fmul_rn(t, sam);
+            t = __fmul_rn(t, sbv[i + j]);
+          }
+          if (has_bias) t = __fadd_rn(t, bv[i + j]);
+          x[j] = t;
+        }
+        packed[i / 2] = pack_bf16x2(x[0], x[1]);
       }
-      if (has_bias) t = __fadd_rn(t, bv[i + j]);
-      x[j] = t;
+      reinterpret_cast<uint4*>(dst)[s8] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
     }
-    packed[i / 2] = pack_bf16x2(x[0], x[1]);
-  }
-  uint16_t* dst = p.out + static_cast<size_t>(m) * static_cast<size_t>(p.N) + n0;
-  if (full) {
-    uint4* d4 = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) d4[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
-  } else {
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-      if (n0 + 8 * i < p.N)  // N is a multiple of 8
-        reinterpret_cast<uint4*>(dst)[i] =
-            make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
   }
 }
 
@@ -505,7 +495,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
 #pragma unroll 1
     for (int a = 0; a < C::ACC_BUFS; ++a) {
       mbar_init(&acc_full[a], 1u);
-      mbar_init(&acc_empty[a], 4u * C::CTAS);
+      mbar_init(&acc_empty[a], static_cast<uint32_t>(C::EPI_WARPS * C::CTAS));
     }
     mbar_init(drain, 1u);
 #pragma unroll 1
@@ -716,13 +706,26 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
     __syncwarp();
   } else if (warp >= 4) {
     // ---------------- epilogue ----------------
-    const int q = warp - 4;
+    const int q = warp & 3;                          // TMEM lane quarter of this warp
+    const int part = (warp - 4) >> 2;                // which EPI_COLS-wide column part
     const int r = q * 32 + lane;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16);
+    const int col_part = part * C::EPI_COLS;
     uint32_t acc_iter = 0;
     bool ok = true;
     // accumulator releases go to the leader CTA's barrier
     const uint32_t acc_empty_leader = C::PAIR ? mapa_shared(smem_u32(&acc_empty[0]), 0u) : 0u;
+    auto release = [&](int a) {
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) {
+        if constexpr (C::PAIR) {
+          mbar_arrive_cluster(acc_empty_leader + 8u * static_cast<uint32_t>(a));
+        } else {
+          mbar_arrive(&acc_empty[a]);
+        }
+      }
+    };
 #pragma unroll 1
     for (int t = tile0; ok && t < p.num_tiles; t += tile_step) {
       int mb, nb;
@@ -731,7 +734,8 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
       const bool row_ok = m < p.M;
       float sam = 1.f;
       if constexpr (C::ROWWISE) sam = row_ok ? __ldg(p.sa + m) : 0.f;
-      const int n_tile = nb * C::BN;
+      const int n_tile = nb * C::BN + col_part;
+      [[maybe_unused]] uint32_t sums[C::REG_SUMS ? C::EPI_COLS : 1];
 #pragma unroll 1
       for (int c = 0; c < p.num_chunks; ++c) {
         const int a = static_cast<int>(acc_iter % C::ACC_BUFS);
@@ -742,54 +746,70 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
         }
         tc_fence_after_sync();
         const bool last = c == p.num_chunks - 1;
-        // With one accumulator the final chunk's totals go back to the TMEM sum
-        // region first, so the accumulator is released before the slow part
-        // (scaling, rounding, stores) and the next tile's MMAs can start.
-        const bool early_release = C::INT_CHUNKS && C::ACC_BUFS == 1 && last;
-#pragma unroll 1
-        for (int g = 0; g < C::BN / 32; ++g) {
-          const int n0 = n_tile + 32 * g;
-          uint32_t v[32];
-          tmem_ld_32cols(lane_base + static_cast<uint32_t>(C::COL_ACC + a * C::BN + 32 * g), v);
-          tmem_wait_ld();
-          if constexpr (C::INT_CHUNKS) {
-            // chunk result: an exact integer below 2^24 in magnitude
+        const uint32_t acc_col = lane_base + static_cast<uint32_t>(C::COL_ACC + a * C::BN + col_part);
+        if constexpr (C::REG_SUMS) {
+          // drain the chunk into the register sums, free the accumulator, and
+          // after the last chunk run the epilogue from the registers
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = static_cast<uint32_t>(__float2int_rn(__uint_as_float(v[i])));
-            if (c > 0) {
-              uint32_t s[32];
-              tmem_ld_32cols(lane_base + static_cast<uint32_t>(C::COL_SUM + 32 * g), s);
-              tmem_wait_ld();
+          for (int g = 0; g < C::EPI_COLS / 16; ++g) {
+            uint32_t v[16];
+            tmem_ld_16cols(acc_col + 16 * g, v);
+            tmem_wait_ld();
 #pragma unroll
-              for (int i = 0; i < 32; ++i) v[i] += s[i];
+            for (int i = 0; i < 16; ++i) {
+              // chunk result: an exact integer below 2^24 in magnitude
+              const uint32_t x = static_cast<uint32_t>(__float2int_rn(__uint_as_float(v[i])));
+              sums[16 * g + i] = c == 0 ? x : sums[16 * g + i] + x;
             }
-            if (!last || early_release) {
-              tmem_st_32cols(lane_base + static_cast<uint32_t>(C::COL_SUM + 32 * g), v);
-            } else if (row_ok && n0 < p.N) {
-              epilogue_row32<true, true>(p, m, n0, sam, v);
-            }
-          } else {
-            if (row_ok && n0 < p.N) epilogue_row32<C::ROWWISE, false>(p, m, n0, sam, v);
           }
-        }
-        if constexpr (C::INT_CHUNKS) tmem_wait_st();
-        tc_fence_before_sync();
-        __syncwarp();
-        if (lane == 0) {
-          if constexpr (C::PAIR) {
-            mbar_arrive_cluster(acc_empty_leader + 8u * static_cast<uint32_t>(a));
-          } else {
-            mbar_arrive(&acc_empty[a]);
+          release(a);
+          if (last && row_ok) {
+            if (n_tile < p.N) epilogue_row32<true, true, 0, C::EPI_COLS>(p, m, n_tile, sam, sums);
+            if (n_tile + 32 < p.N) epilogue_row32<true, true, 32, C::EPI_COLS>(p, m, n_tile + 32, sam, sums);
           }
-        }
-        if (early_release) {
+        } else {
+          // With one accumulator the final chunk's totals go back to the TMEM
+          // sum region first, so the accumulator is released before the slow
+          // part (scaling, rounding, stores) and the next tile's MMAs start.
+          const bool early_release = C::INT_CHUNKS && C::ACC_BUFS == 1 && last;
 #pragma unroll 1
-          for (int g = 0; g < C::BN / 32; ++g) {
+          for (int g = 0; g < C::EPI_COLS / 32; ++g) {
             const int n0 = n_tile + 32 * g;
             uint32_t v[32];
-            tmem_ld_32cols(lane_base + static_cast<uint32_t>(C::COL_SUM + 32 * g), v);
+            tmem_ld_32cols(acc_col + 32 * g, v);
             tmem_wait_ld();
-            if (row_ok && n0 < p.N) epilogue_row32<true, true>(p, m, n0, sam, v);
+            if constexpr (C::INT_CHUNKS) {
+              // chunk result: an exact integer below 2^24 in magnitude
+#pragma unroll
+              for (int i = 0; i < 32; ++i) v[i] = static_cast<uint32_t>(__float2int_rn(__uint_as_float(v[i])));
+              const uint32_t sum_col = lane_base + static_cast<uint32_t>(C::COL_SUM + col_part + 32 * g);
+              if (c > 0) {
+                uint32_t sv[32];
+                tmem_ld_32cols(sum_col, sv);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] += sv[i];
+              }
+              if (!last || early_release) {
+                tmem_st_32cols(sum_col, v);
+              } else if (row_ok && n0 < p.N) {
+                epilogue_row32<true, true>(p, m, n0, sam, v);
+              }
+            } else {
+              if (row_ok && n0 < p.N) epilogue_row32<C::ROWWISE, false>(p, m, n0, sam, v);
+            }
+          }
+          if constexpr (C::INT_CHUNKS) tmem_wait_st();
+          release(a);
+          if (early_release) {
+#pragma unroll 1
+            for (int g = 0; g < C::EPI_COLS / 32; ++g) {
+              const int n0 = n_tile + 32 * g;
+              uint32_t v[32];
+              tmem_ld_32cols(lane_base + static_cast<uint32_t>(C::COL_SUM + col_part + 32 * g), v);
+              tmem_wait_ld();
+              if (row_ok && n0 < p.N) epilogue_row32<true, true>(p, m, n0, sam, v);
+            }
           }
         }
         ++acc_iter;

@@ -18,9 +18,10 @@
 
 namespace qk {
 
-// 256 x 256 tiles per CTA pair: one fp32 accumulator (256 columns) and the
-// int32 running sums (256 columns) fill the 512 TMEM columns of each SM.
-using CfgInt8 = GemmCfg<Kind::F16, 256, 6, 1, true>;
+// 256 x 256 tiles per CTA pair, two fp32 accumulators of 256 columns per SM
+// (all 512 TMEM columns); 16 epilogue warps keep the int32 running sums in
+// registers, so a chunk drains while the MMAs fill the other accumulator.
+using CfgInt8 = GemmCfg<Kind::F16, 256, 6, 2, true, 16>;
 
 // Widens 16 int8 values per thread-iteration to f16.  Byte x becomes the f16
 // bit pattern 0x6400 | (x + 128), i.e. the value 1024 + x + 128, and one

@@ -157,3 +157,27 @@ def test_fp8_exact_small_integers():
     got = host_bits(run_fp8(p))
     exact = (vals @ wv.T).astype(np.float32)
     assert np.array_equal(got, qi.to_bf16_bits(exact))
+
+
+@pytest.mark.parametrize("fmt", FMTS, ids=FMT_IDS)
+@pytest.mark.parametrize("K,offset", [(1024, 0), (1024, 4), (896, 0), (96, 0)],
+                         ids=["tma", "async-misaligned", "async", "loads"])
+def test_mx_scale_staging_modes(fmt, K, offset):
+    # The kernel fetches scale rows by TMA (K % 512 == 0 and 16-byte aligned
+    # rows), by cp.async (K % 128 == 0 or rows only 4-byte aligned), or by
+    # per-stage loads (other K); every mode must give the same result.
+    import torch
+    from gpu_util import to_dev, nan_out, host_bits
+    import block_scaled_precision_tcgen05_gb300 as qk
+    M, N = 300, 264
+    p = qi.mx_problem(fmt, M, N, K, seed=K + offset)
+    def shifted(x):
+        flat = torch.zeros(x.size + 64, dtype=torch.uint8, device="cuda")
+        view = flat[offset:offset + x.size].view(x.shape)
+        view.copy_(to_dev(x))
+        return view
+    sA, sB = shifted(p.sA), shifted(p.sB)
+    out = nan_out(M, N)
+    qk.gemm_mx(fmt, to_dev(p.A), sA, to_dev(p.B), sB, None, out)
+    torch.cuda.synchronize()
+    assert_close(host_bits(out), oracle.gemm_mx(fmt, p.A, p.sA, p.B, p.sB), f"K={K} offset={offset}")
