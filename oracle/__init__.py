@@ -69,6 +69,8 @@ def _declare(lib):
     lib.qko_encode_e2m1.restype = c.c_uint8
     lib.qko_mx_quantize_block.argtypes = [c.c_int, P, P, P]
     lib.qko_mx_quantize_block.restype = None
+    lib.qko_ptpc_quantize_row.argtypes = [P, i64, P, P]
+    lib.qko_ptpc_quantize_row.restype = None
     lib.qko_gemm_int8_rowwise.argtypes = [P, P, P, P, P, P, i64, i64, i64, i64, i64, i64, i64, i64, P]
     lib.qko_gemm_int8_rowwise.restype = c.c_int
     lib.qko_gemm_fp8_rowwise.argtypes = [P, P, P, P, P, P, i64, i64, i64, i64, i64, i64, i64, i64]
@@ -155,6 +157,34 @@ def mx_quantize_block(fmt: int, v, lib=None):
     sc = np.zeros(1, np.uint8)
     lib.qko_mx_quantize_block(int(fmt), _ptr(v), _ptr(codes), _ptr(sc))
     return codes, int(sc[0])
+
+
+def ptpc_quantize(x, lib=None):
+    """Per-row E4M3 codes and fp32 scales of a [rows, K] float32 matrix."""
+    lib = lib or load()
+    x = _c(np.asarray(x, np.float32), np.float32)
+    rows, K = x.shape
+    codes = np.zeros((rows, K), np.uint8)
+    scales = np.zeros(rows, np.float32)
+    for r in range(rows):
+        lib.qko_ptpc_quantize_row(_ptr(x[r]), K, codes[r].ctypes.data_as(ctypes.c_void_p),
+                                  scales[r:].ctypes.data_as(ctypes.c_void_p))
+    return codes, scales
+
+
+def mx_quantize(fmt, x, lib=None):
+    """MX codes (one per byte, E2M1 unpacked) and scale bytes of a [rows, K] float32 matrix."""
+    lib = lib or load()
+    x = np.ascontiguousarray(np.asarray(x, np.float32))
+    rows, K = x.shape
+    codes = np.zeros((rows, K), np.uint8)
+    scales = np.zeros((rows, K // 32), np.uint8)
+    for r in range(rows):
+        for b in range(K // 32):
+            c, sc = mx_quantize_block(fmt, x[r, 32 * b:32 * b + 32], lib)
+            codes[r, 32 * b:32 * b + 32] = c
+            scales[r, b] = sc
+    return codes, scales
 
 
 def _region(M, N, m0, m1, n0, n1):

@@ -204,6 +204,27 @@ void qko_mx_quantize_block(int fmt, const float* v, uint8_t* codes, uint8_t* sca
   }
 }
 
+/* One row of per-token FP8 quantization (the step that feeds the FP8
+ * per-token x per-channel GEMM; ROCm/aiter PR #6262 "Technical Details",
+ * ROCm/mori PR #806 "ptpc"): amax over the row, scale s = amax / 448 in fp32
+ * (1 for an all-zero row), codes = E4M3(x / s) with the fp32 division
+ * rounded to nearest even, then rounded to nearest even E4M3, saturated. */
+void qko_ptpc_quantize_row(const float* x, int64_t K, uint8_t* codes, float* scale) {
+  build_tables();
+  float amax = 0.0f;
+  for (int64_t k = 0; k < K; ++k) {
+    float a = fabsf(x[k]);
+    if (a > amax) amax = a;
+  }
+  float s = amax / 448.0f;
+  if (amax == 0.0f) s = 1.0f;
+  *scale = s;
+  for (int64_t k = 0; k < K; ++k) {
+    float q = x[k] / s;
+    codes[k] = qko_encode_e4m3((double)q);
+  }
+}
+
 /* ------------------------------------------------------------------ */
 /* INT8 row/column-scaled GEMM  [CK174]                                */
 /* ------------------------------------------------------------------ */

@@ -147,6 +147,24 @@ def check_mx_quantize_block(lib):
             assert np.array_equal(c, qc[r])
 
 
+def check_ptpc_quantize(lib):
+    # closed forms: the row maximum maps to 448 exactly; an all-zero row takes scale 1
+    x = np.array([[0.0, 1.0, -2.0, 7.0], [0.0, 0.0, 0.0, 0.0], [-3.5, 0.25, 1e-6, 3.5]], np.float32)
+    codes, s = oracle.ptpc_quantize(x, lib)
+    assert s[0] == np.float32(7.0) / np.float32(448.0) and s[1] == 1.0
+    assert codes[0, 3] == 0x7E and codes[2, 0] == 0xFE and codes[2, 3] == 0x7E   # +-448
+    assert np.all(codes[1] == 0)
+    # every code decodes to within half an E4M3 step of x / s, and the codes agree
+    # with an independent vectorised implementation (the input generator's)
+    rng = np.random.default_rng(17)
+    x = (rng.standard_normal((5, 300)) * np.exp(rng.uniform(-6, 6, (5, 1)))).astype(np.float32)
+    codes, s = oracle.ptpc_quantize(x, lib)
+    q2, s2 = qk_inputs.ptpc_quantize(x)
+    assert np.array_equal(s, s2) and np.array_equal(codes, q2)
+    dec = oracle.decode_e4m3(codes, lib) * s.astype(np.float64)[:, None]
+    assert np.all(np.abs(dec - x) <= np.abs(x) * 2.0 ** -4 + s[:, None] * 2.0 ** -10)
+
+
 # ---------------------------------------------------------------- INT8
 
 def check_int8_acc_vs_numpy(lib):
@@ -364,7 +382,7 @@ def check_mx_vs_numpy(lib):
 
 ALL_CHECKS = [
     check_e4m3_decode, check_e2m1_decode, check_ue8m0_decode, check_bf16_rne, check_encoders,
-    check_mx_quantize_block, check_int8_acc_vs_numpy, check_int8_hand_examples,
+    check_mx_quantize_block, check_ptpc_quantize, check_int8_acc_vs_numpy, check_int8_hand_examples,
     check_int8_identity_and_extremes, check_int8_epilogue_order, check_int8_signed_zero,
     check_int8_pow2_invariance, check_fp8_vs_numpy, check_mx_block_structure,
     check_mx_scale_doubling, check_mx_vs_numpy,

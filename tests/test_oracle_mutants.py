@@ -39,6 +39,8 @@ MUTANTS = {
                                "double x = acc * (double)sa[m] * (double)sb[m % N];"),
     "fp8_bias_sign": ("if (bias) x += (double)qko_bf16_to_f32(bias[n]);", "if (bias) x -= (double)qko_bf16_to_f32(bias[n]);"),
     "encoder_ties_away": ("(err == best_err && (c & 1u) == 0u)", "(err == best_err && c > best)"),
+    "ptpc_scale_divisor": ("float s = amax / 448.0f;", "float s = amax / 240.0f;"),
+    "ptpc_zero_row_scale": ("if (amax == 0.0f) s = 1.0f;", "if (amax == 0.0f) s = 0.5f;"),
     "mx_emax": ("int emax = (fmt == QKO_FMT_MXFP8_E4M3) ? 8 : 2;", "int emax = (fmt == QKO_FMT_MXFP8_E4M3) ? 7 : 2;"),
 }
 
