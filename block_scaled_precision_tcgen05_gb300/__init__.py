@@ -40,6 +40,8 @@ EXPORTS = (
     "qk_gemm_int8_rowwise_noalloc",
     "qk_gemm_mx",
     "qk_gemm_fp8_rowwise",
+    "qk_quantize_mx",
+    "qk_quantize_ptpc",
     "qk_status_string",
     "qk_device_status",
     "qk_set_wait_timeout_ns",
@@ -77,6 +79,10 @@ def _declare(lib):
     lib.qk_gemm_fp8_rowwise.restype = c.c_int
     lib.qk_gemm_mx.argtypes = [c.c_int, P, P, P, P, P, P, i64, i64, i64, P]
     lib.qk_gemm_mx.restype = c.c_int
+    lib.qk_quantize_mx.argtypes = [c.c_int, P, P, P, i64, i64, P]
+    lib.qk_quantize_mx.restype = c.c_int
+    lib.qk_quantize_ptpc.argtypes = [P, P, P, i64, i64, P]
+    lib.qk_quantize_ptpc.restype = c.c_int
     lib.qk_status_string.argtypes = [c.c_int]
     lib.qk_status_string.restype = c.c_char_p
     lib.qk_device_status.argtypes = [c.POINTER(c.c_uint64), c.c_int]
@@ -242,6 +248,38 @@ def gemm_mx(fmt, A, sA, B, sB, bias=None, out=None):
     check(load_library().qk_gemm_mx(int(fmt), _ptr(A), _ptr(sA), _ptr(B), _ptr(sB), _ptr(bias), _ptr(out),
                                     M, N, K, _stream_handle(dev)))
     return out
+
+
+def quantize_mx(fmt, x, q=None, scales=None):
+    """MX-quantize a bf16 [rows, K] CUDA tensor along K: returns (q, scales) as uint8 tensors
+    ([rows, K] E4M3 or [rows, K/2] packed E2M1, and [rows, K/32] UE8M0)."""
+    import torch
+    if fmt not in (FMT_MXFP8_E4M3, FMT_MXFP4_E2M1):
+        raise ValueError("unknown MX format")
+    rows, K = x.shape
+    dev = x.device
+    _expect(x, "x", torch.bfloat16, (rows, K), dev)
+    width = K if fmt == FMT_MXFP8_E4M3 else K // 2
+    q = torch.empty((rows, width), dtype=torch.uint8, device=dev) if q is None else q
+    scales = torch.empty((rows, K // 32), dtype=torch.uint8, device=dev) if scales is None else scales
+    _expect(q, "q", torch.uint8, (rows, width), dev)
+    _expect(scales, "scales", torch.uint8, (rows, K // 32), dev)
+    check(load_library().qk_quantize_mx(int(fmt), _ptr(x), _ptr(q), _ptr(scales), rows, K, _stream_handle(dev)))
+    return q, scales
+
+
+def quantize_ptpc(x, q=None, scales=None):
+    """Per-row E4M3 quantization of a bf16 [rows, K] CUDA tensor: returns (q uint8 [rows, K], scales fp32 [rows])."""
+    import torch
+    rows, K = x.shape
+    dev = x.device
+    _expect(x, "x", torch.bfloat16, (rows, K), dev)
+    q = torch.empty((rows, K), dtype=torch.uint8, device=dev) if q is None else q
+    scales = torch.empty((rows,), dtype=torch.float32, device=dev) if scales is None else scales
+    _expect(q, "q", torch.uint8, (rows, K), dev)
+    _expect(scales, "scales", torch.float32, (rows,), dev)
+    check(load_library().qk_quantize_ptpc(_ptr(x), _ptr(q), _ptr(scales), rows, K, _stream_handle(dev)))
+    return q, scales
 
 
 def device_status(clear: bool = True) -> int:

@@ -49,8 +49,8 @@ void count_launches(uint64_t n) { g_launches.fetch_add(n, std::memory_order_rela
 
 namespace {
 
-const char* const kKernelNames[kKNumKinds] = {"int8_to_f16", "gemm_int8_f16", "gemm_fp8",
-                                              "gemm_mxfp8",  "gemm_mxfp4",    "wait_probe"};
+const char* const kKernelNames[kKNumKinds] = {"int8_to_f16", "gemm_int8_f16", "gemm_fp8", "gemm_mxfp8",
+                                              "gemm_mxfp4",  "wait_probe",    "quantize"};
 
 struct PendingTiming {
   int kind;
@@ -185,6 +185,16 @@ int encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base
 int encode_tmap_2d_plain(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t inner,
                          uint64_t rows, uint64_t row_pitch_bytes, uint32_t box_inner, uint32_t box_rows) {
   return encode_2d(map, dtype, base, inner, rows, row_pitch_bytes, box_inner, box_rows, CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
+int encode_tmap_out(CUtensorMap* map, void* out, uint64_t rows, uint64_t cols) {
+  return encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, out, cols, rows, cols * 2, 32, 32,
+                   CU_TENSOR_MAP_SWIZZLE_64B);
+}
+
+int kernel_variant(const char* env_name) {
+  const char* s = std::getenv(env_name);
+  return (s && *s >= '0' && *s <= '9') ? (*s - '0') : 0;
 }
 
 int raster_group_m() {

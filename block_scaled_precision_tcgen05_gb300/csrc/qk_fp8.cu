@@ -2,18 +2,22 @@
 // (ROCm/aiter PR #6262 gemm_a8w8_bpreshuffle semantics; ROCm/mori PR #806
 // "ptpc"), on tcgen05.mma kind::f8f6f4 with fp32 accumulation in TMEM.
 #include "qk_launch.cuh"
+#include "qk_skinny_kernel.cuh"
 
 namespace qk {
 
-// 256 x 256 tiles per CTA pair, two accumulators of 256 columns per SM.
-using CfgFp8 = GemmCfg<Kind::F8, 256, 6, 2, true>;
+// 256 x 256 tiles per CTA pair, two accumulators of 256 columns per SM, 8
+// epilogue warps writing through shared-memory staging blocks and bulk
+// tensor stores (with K as short as 1792 the epilogue sets the pace: 4 warps
+// storing straight to global memory reach 0.55 of this configuration's rate).
+using CfgFp8 = GemmCfg<Kind::F8, 256, 6, 2, true, 8, 1>;
 
-int launch_fp8_rowwise(const uint8_t* A, const uint8_t* B, const float* sa, const float* sb, const uint16_t* bias,
-                       uint16_t* out, int M, int N, int K, const DeviceInfo& dev, cudaStream_t stream) {
-  using C = CfgFp8;
+template <class C>
+static int launch_fp8_cfg(const uint8_t* A, const uint8_t* B, const float* sa, const float* sb, const uint16_t* bias,
+                          uint16_t* out, int M, int N, int K, const DeviceInfo& dev, cudaStream_t stream) {
   CUtensorMap ta, tb;
   int st = encode_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, K, M, K, C::TMA_K, C::BM);
-  if (st == QK_OK) st = encode_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, K, N, K, C::TMA_K, C::B_ROWS);
+  if (st == QK_OK) st = encode_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, K, N, K, C::TMA_K, C::B_LOAD_ROWS);
   if (st != QK_OK) return st;
   GemmParams p{};
   plan_tiles<C>(p, M, N, K);
@@ -24,6 +28,106 @@ int launch_fp8_rowwise(const uint8_t* A, const uint8_t* B, const float* sa, cons
   p.err = dev.err_word;
   p.timeout_ns = wait_timeout_ns();
   return launch_gemm<C>(ta, tb, ta, tb, p, dev, stream);
+}
+
+// Few rows (M <= 128): split-K, weight-streaming kernel (qk_skinny_kernel.cuh).
+template <int MT, int S>
+static int launch_skinny_cfg(const uint8_t* A, const uint8_t* B, const float* sa, const float* sb,
+                             const uint16_t* bias, uint16_t* out, int M, int N, int K, const DeviceInfo& dev,
+                             cudaStream_t stream, bool probe_only, int* fits) {
+  using C = SkinnyCfg<MT, S, MT <= 64 ? 6 : 4>;
+  auto kernel = qk_skinny_fp8_kernel<C>;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) != cudaSuccess)
+    return QK_ERR_CUDA;
+  const int n_tiles = ceil_div(N, C::NT);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(n_tiles * S, 1, 1);
+  cfg.blockDim = dim3(C::NUM_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = S;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (probe_only) {  // how many clusters of S fit at once
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) {
+      cudaGetLastError();
+      n = 0;
+    }
+    *fits = n;
+    return QK_OK;
+  }
+  CUtensorMap tw, ta;
+  int st = encode_tmap_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, K, N, K, 128, C::NT);
+  if (st == QK_OK) st = encode_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, K, M, K, 128, C::MT);
+  if (st != QK_OK) return st;
+  SkinnyParams p{};
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.num_kb = ceil_div(K, C::K_ELEMS);
+  p.kb_per_split = ceil_div(p.num_kb, S);
+  p.sa = sa;
+  p.sb = sb;
+  p.bias = bias;
+  p.out = out;
+  p.err = dev.err_word;
+  p.timeout_ns = wait_timeout_ns();
+  LaunchTimer timer(kKGemmFp8, stream);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, tw, ta, p);
+  timer.done();
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return QK_ERR_CUDA;
+  }
+  count_launches(1);
+  return QK_OK;
+}
+
+template <int MT>
+static int launch_skinny(const uint8_t* A, const uint8_t* B, const float* sa, const float* sb, const uint16_t* bias,
+                         uint16_t* out, int M, int N, int K, const DeviceInfo& dev, cudaStream_t stream) {
+  // Pick the split S (1, 2, 4, 8) that minimises waves(S) * (c0 + k-blocks per
+  // CTA), with c0 ~ 20 k-blocks' worth of fixed per-CTA time (launch, setup,
+  // reduction), as measured on the 64-row problems.
+  const int n_tiles = ceil_div(N, 128);
+  const int num_kb = ceil_div(K, 128);
+  int best = 1;
+  double best_cost = 1e30;
+  for (int S : {1, 2, 4, 8}) {
+    if (S > num_kb) break;
+    int fits = 0;
+    if (S == 1) launch_skinny_cfg<MT, 1>(A, B, sa, sb, bias, out, M, N, K, dev, stream, true, &fits);
+    if (S == 2) launch_skinny_cfg<MT, 2>(A, B, sa, sb, bias, out, M, N, K, dev, stream, true, &fits);
+    if (S == 4) launch_skinny_cfg<MT, 4>(A, B, sa, sb, bias, out, M, N, K, dev, stream, true, &fits);
+    if (S == 8) launch_skinny_cfg<MT, 8>(A, B, sa, sb, bias, out, M, N, K, dev, stream, true, &fits);
+    if (fits <= 0) continue;
+    const int waves = ceil_div(n_tiles, fits);
+    const double cost = static_cast<double>(waves) * (20.0 + ceil_div(num_kb, S));
+    if (cost < best_cost) {
+      best_cost = cost;
+      best = S;
+    }
+  }
+  switch (best) {
+    case 8: return launch_skinny_cfg<MT, 8>(A, B, sa, sb, bias, out, M, N, K, dev, stream, false, nullptr);
+    case 4: return launch_skinny_cfg<MT, 4>(A, B, sa, sb, bias, out, M, N, K, dev, stream, false, nullptr);
+    case 2: return launch_skinny_cfg<MT, 2>(A, B, sa, sb, bias, out, M, N, K, dev, stream, false, nullptr);
+    default: return launch_skinny_cfg<MT, 1>(A, B, sa, sb, bias, out, M, N, K, dev, stream, false, nullptr);
+  }
+}
+
+int launch_fp8_rowwise(const uint8_t* A, const uint8_t* B, const float* sa, const float* sb, const uint16_t* bias,
+                       uint16_t* out, int M, int N, int K, const DeviceInfo& dev, cudaStream_t stream) {
+  if (M <= 64 && kernel_variant("QK_FP8_SKINNY") == 0)
+    return launch_skinny<64>(A, B, sa, sb, bias, out, M, N, K, dev, stream);
+  if (M <= 128 && kernel_variant("QK_FP8_SKINNY") == 0)
+    return launch_skinny<128>(A, B, sa, sb, bias, out, M, N, K, dev, stream);
+  return launch_fp8_cfg<CfgFp8>(A, B, sa, sb, bias, out, M, N, K, dev, stream);
 }
 
 }  // namespace qk

@@ -73,15 +73,25 @@ struct GemmParams {
 // 128 TMEM lanes for BN / (EPI_WARPS_/4) columns).  For the exact INT8 kind,
 // 16 epilogue warps keep the int32 running sums in registers (64 columns per
 // thread) instead of TMEM, which frees TMEM for two accumulators.
-template <Kind KIND, int BN_, int STAGES_, int ACC_BUFS_, bool PAIR_ = false, int EPI_WARPS_ = 4>
+// OUT_BUFS_: shared-memory staging blocks per epilogue warp for bulk tensor
+// stores of the output; 0 = the epilogue stores straight to global memory.
+// MCAST_: a cluster of two CTAs, each computing its own 128 x BN tile with
+// one-CTA MMAs, shares the B tile: each CTA loads half of it and multicasts
+// that half into both CTAs' shared memory (a ring slot is refilled once both
+// CTAs' MMAs have released it).
+template <Kind KIND, int BN_, int STAGES_, int ACC_BUFS_, bool PAIR_ = false, int EPI_WARPS_ = 4,
+          int OUT_BUFS_ = 2, bool MCAST_ = false>
 struct GemmCfg {
   static constexpr Kind kind = KIND;
   static constexpr bool PAIR = PAIR_;
-  static constexpr int CTAS = PAIR ? 2 : 1;
+  static constexpr bool MCAST = MCAST_;
+  static constexpr int CTAS = (PAIR || MCAST) ? 2 : 1;  // CTAs of a cluster
   static constexpr int BM = 128;                 // rows of A (and D) per CTA
-  static constexpr int MMA_M = BM * CTAS;        // rows of a tile
+  static constexpr int TILE_M = BM * CTAS;       // rows of a cluster's tile
+  static constexpr int MMA_M = PAIR ? 256 : 128; // rows of one MMA
   static constexpr int BN = BN_;                 // columns of a tile
-  static constexpr int B_ROWS = BN / CTAS;       // rows of B per CTA
+  static constexpr int B_ROWS = PAIR ? BN / 2 : BN;   // rows of B in a CTA's shared memory
+  static constexpr int B_LOAD_ROWS = BN / CTAS;       // rows of B a CTA loads per stage
   static constexpr int STAGES = STAGES_;
   static constexpr int ACC_BUFS = ACC_BUFS_;
   static constexpr int ROW_BYTES = 128;  // bytes of K per row per ring stage (one swizzle row)
@@ -106,7 +116,9 @@ struct GemmCfg {
 
   static constexpr int A_BYTES = BM * ROW_BYTES;
   static constexpr int B_BYTES = B_ROWS * ROW_BYTES;
-  static constexpr uint32_t STAGE_TX = CTAS * (A_BYTES + B_BYTES);  // bytes one ring stage receives per tile
+  // bytes a ring stage's full barrier counts: a pair's leader counts both CTAs'
+  // loads; with B multicast each CTA receives its A and both halves of B
+  static constexpr uint32_t STAGE_TX = PAIR ? 2 * (A_BYTES + B_BYTES) : A_BYTES + B_BYTES;
 
   // Raw scale rows fetched by TMA: 16 bytes (16 scales) per row per fetch,
   // i.e. RAW_KB ring stages' worth, double-buffered.
@@ -121,7 +133,13 @@ struct GemmCfg {
   static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
   static constexpr int OFF_SF = OFF_B + STAGES * B_BYTES;
   static constexpr int OFF_RAW = OFF_SF + STAGES * SF_STAGE_BYTES;
-  static constexpr int OFF_BAR = OFF_RAW + RAW_BUFS * RAW_STAGE_BYTES;
+  // Output staging: each epilogue warp writes 32x32 bf16 blocks (2 KB, 64-byte
+  // swizzle) that a bulk tensor store copies to global memory.
+  static constexpr int OUT_BUFS = OUT_BUFS_;
+  static constexpr bool STORE_TMA = OUT_BUFS_ > 0;
+  static constexpr int OUT_BLOCK_BYTES = 32 * 32 * 2;
+  static constexpr int OFF_OUT = ((OFF_RAW + RAW_BUFS * RAW_STAGE_BYTES) + 1023) & ~1023;
+  static constexpr int OFF_BAR = OFF_OUT + EPI_WARPS * OUT_BUFS * OUT_BLOCK_BYTES;
   static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC_BUFS + 1 + RAW_BUFS;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack to align the base to 1024
@@ -142,20 +160,26 @@ struct GemmCfg {
   static constexpr int NUM_THREADS = 32 * (4 + EPI_WARPS);
 
   static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "tile N");
-  static_assert(!(PAIR && MX), "CTA pairs are used for the dense kinds only");
   static_assert(EPI_WARPS % 4 == 0 && EPI_COLS % 32 == 0, "epilogue split");
   static_assert(!REG_SUMS || EPI_COLS == 64, "register sums hold 64 columns per thread");
+  static_assert(!(PAIR && MCAST), "one cluster mode");
   static_assert(COLS_USED <= 512, "TMEM budget");
   static_assert(SMEM_BYTES <= 232448, "shared-memory budget");
   static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "swizzle atoms need 1024-byte alignment");
+
+  // Ring-slot arrivals: the producer's, plus (MX) the scale warp's; in a CTA
+  // pair each CTA stages the scale factors of its own 128 rows of A and of all
+  // BN rows of B at the same offsets, and both scale warps arrive on the
+  // leader's barrier.
+  static constexpr uint32_t FULL_ARRIVALS = 1 + (MX ? (PAIR ? 2 : 1) : 0);
 
   // kind::f16: D fp32 (1), A/B f16 (0).  kind::f8f6f4: A/B E4M3 (0).
   // kind::mxf8f6f4: E4M3 (0).  kind::mxf4: E2M1 (1).
   __host__ __device__ static constexpr uint32_t idesc(uint32_t a_sf_id, uint32_t b_sf_id) {
     return KIND == Kind::F16    ? make_idesc_dense(1, 0, 0, MMA_M, BN)
            : KIND == Kind::F8   ? make_idesc_dense(1, 0, 0, MMA_M, BN)
-           : KIND == Kind::MXF8 ? make_idesc_block_scaled(0, 0, BM, BN, a_sf_id, b_sf_id)
-                                : make_idesc_block_scaled(1, 1, BM, BN, a_sf_id, b_sf_id);
+           : KIND == Kind::MXF8 ? make_idesc_block_scaled(0, 0, MMA_M, BN, a_sf_id, b_sf_id)
+                                : make_idesc_block_scaled(1, 1, MMA_M, BN, a_sf_id, b_sf_id);
   }
 };
 
@@ -209,12 +233,62 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 }
 
 // Epilogue of 32 consecutive columns [n0, n0+32) of one row m, in four steps
-// of 8 columns (8 column scales, 8 biases and one 16-byte store live at a
-// time).  INT_ACC: v holds int32 sums; otherwise fp32 bit patterns.  N is a
-// multiple of 8, so every 8-column step is either fully inside or outside.
+// of 8 columns (8 column scales, 8 biases live at a time), written as bf16 to
+// row `lane` of a 32x32 staging block with the 64-byte swizzle the output
+// tensor map uses (16-byte chunk c of row r at 64r + 16(c ^ ((r >> 1) & 3))).
+// INT_ACC: v holds int32 sums; otherwise fp32 bit patterns.  Columns past N
+// (N is a multiple of 8) read no scale or bias; the bulk store clips them.
 template <bool ROWWISE, bool INT_ACC, int OFF = 0, int LEN = 32>
-__device__ __forceinline__ void epilogue_row32(const GemmParams& p, int m, int n0, float sam,
-                                               const uint32_t (&v)[LEN]) {
+__device__ __forceinline__ void epilogue_row32(const GemmParams& p, int n0, float sam, const uint32_t (&v)[LEN],
+                                               uint32_t block, int lane) {
+  const bool has_bias = p.bias != nullptr;
+#pragma unroll
+  for (int s8 = 0; s8 < 4; ++s8) {
+    const int n = n0 + 8 * s8;
+    const bool in = n < p.N;
+    float sbv[8];
+    float bv[8];
+    if constexpr (ROWWISE) {
+      const float4 t0 = in ? __ldg(reinterpret_cast<const float4*>(p.sb + n)) : make_float4(0.f, 0.f, 0.f, 0.f);
+      const float4 t1 = in ? __ldg(reinterpret_cast<const float4*>(p.sb + n) + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
+      sbv[0] = t0.x; sbv[1] = t0.y; sbv[2] = t0.z; sbv[3] = t0.w;
+      sbv[4] = t1.x; sbv[5] = t1.y; sbv[6] = t1.z; sbv[7] = t1.w;
+    }
+    if (has_bias) {
+      const uint4 t = in ? __ldg(reinterpret_cast<const uint4*>(p.bias + n)) : make_uint4(0u, 0u, 0u, 0u);
+      const uint32_t wv[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        bv[2 * j + 0] = __uint_as_float(wv[j] << 16);
+        bv[2 * j + 1] = __uint_as_float(wv[j] & 0xFFFF0000u);
+      }
+    }
+    uint32_t packed[4];
+#pragma unroll
+    for (int i = 0; i < 8; i += 2) {
+      float x[2];
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const uint32_t raw = v[OFF + 8 * s8 + i + j];
+        float t = INT_ACC ? __int2float_rn(static_cast<int>(raw)) : __uint_as_float(raw);
+        if constexpr (ROWWISE) {
+          t = __fmul_rn(t, sam);
+          t = __fmul_rn(t, sbv[i + j]);
+        }
+        if (has_bias) t = __fadd_rn(t, bv[i + j]);
+        x[j] = t;
+      }
+      packed[i / 2] = pack_bf16x2(x[0], x[1]);
+    }
+    st_shared_v4(block + 64 * lane + 16 * (s8 ^ ((lane >> 1) & 3)), packed[0], packed[1], packed[2], packed[3]);
+  }
+}
+
+// The same epilogue with the 8-column pieces stored straight to row m of the
+// output (16-byte stores; no staging).
+template <bool ROWWISE, bool INT_ACC, int OFF = 0, int LEN = 32>
+__device__ __forceinline__ void epilogue_row32_global(const GemmParams& p, int m, int n0, float sam,
+                                                      const uint32_t (&v)[LEN]) {
   const bool has_bias = p.bias != nullptr;
   uint16_t* dst = p.out + static_cast<size_t>(m) * static_cast<size_t>(p.N) + n0;
 #pragma unroll
@@ -260,6 +334,39 @@ __device__ __forceinline__ void epilogue_row32(const GemmParams& p, int m, int n
   }
 }
 
+// One epilogue warp's output block: waits until its staging buffer is free,
+// fills it (per lane one row), and issues the bulk store of the 32x32 block at
+// (row m_block, column n0).  `count` numbers the warp's blocks.
+template <bool INT, int OFF>
+struct EmitTag {
+  static constexpr bool kInt = INT;
+  static constexpr int kOff = OFF;
+};
+
+struct OutStager {
+  uint32_t base;    // this warp's first staging buffer (shared address)
+  uint32_t count;   // blocks issued so far
+};
+
+template <class C>
+__device__ __forceinline__ uint32_t out_block_acquire(OutStager& o, int lane) {
+  if (lane == 0) bulk_wait_group_read<(C::OUT_BUFS > 0 ? C::OUT_BUFS - 1 : 0)>();
+  __syncwarp();
+  return o.base + (o.count % (C::OUT_BUFS > 0 ? C::OUT_BUFS : 1)) * C::OUT_BLOCK_BYTES;
+}
+
+template <class C>
+__device__ __forceinline__ void out_block_release(OutStager& o, uint32_t block, const CUtensorMap* tmOut, int n0,
+                                                  int m_block, int lane) {
+  fence_proxy_async_smem();  // the block's generic writes before the bulk copy reads it
+  __syncwarp();
+  if (lane == 0) {
+    tma_store_2d(tmOut, block, n0, m_block);
+    bulk_commit_group();
+  }
+  ++o.count;
+}
+
 // Writes one ring stage's scale atoms from per-lane scale words.
 // a[j] holds 4 scale bytes of tile row 32j + lane (A), b[rb*4 + j] of B row
 // rb*128 + 32j + lane; atom g of the stage takes word `w0 + g`.
@@ -290,14 +397,14 @@ __device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
 // chunk `r` of scale rows l + 32i (A: 128 rows, B: NB128*128 rows), zero-filled
 // past the matrix; each lane's copies arrive once on `bar` when they land.
 template <class C>
-__device__ __forceinline__ void raw_fetch_async(const GemmParams& p, uint32_t raw, uint64_t* bar, int mb, int nb,
+__device__ __forceinline__ void raw_fetch_async(const GemmParams& p, uint32_t raw, uint64_t* bar, int a_row0, int nb,
                                                 int r, int lane) {
   const int col0 = r * 16;
 #pragma unroll
   for (int i = 0; i < 4 + 4 * C::NB128; ++i) {
     const bool is_a = i < 4;
     const int local = 32 * (is_a ? i : i - 4) + lane;
-    const int row = is_a ? mb * C::BM + local : nb * C::BN + local;
+    const int row = is_a ? a_row0 + local : nb * C::BN + local;
     const int rows = is_a ? p.M : p.N;
     const uint8_t* base = is_a ? p.sA : p.sB;
     const uint32_t dst = raw + (is_a ? 0 : C::RAW_A_BYTES) + 16 * local;
@@ -319,31 +426,44 @@ __device__ __forceinline__ void raw_fetch_async(const GemmParams& p, uint32_t ra
 // rearranges each stage's scale bytes into the 512-byte atoms tcgen05.cp
 // reads.  Shared loads and stores are 16 bytes per lane over contiguous
 // 512-byte spans (no bank conflicts).
+// Marks a ring slot's scale atoms as written: on the local full barrier, or in
+// a CTA pair on the leader's (given by its cluster address).
+template <class C>
+__device__ __forceinline__ void scale_slot_ready(uint64_t* full, uint32_t full_leader, int stage) {
+  if constexpr (C::PAIR) {
+    mbar_arrive_cluster(full_leader + 8u * static_cast<uint32_t>(stage));
+  } else {
+    mbar_arrive(&full[stage]);
+  }
+}
+
 template <class C>
 __device__ __forceinline__ void scale_stager_raw(const GemmParams& p, const CUtensorMap* tmSA,
                                                  const CUtensorMap* tmSB, uint8_t* smem, uint64_t* full,
-                                                 uint64_t* empty, uint64_t* raw_full, const WaitCtl& w, int lane) {
+                                                 uint64_t* empty, uint64_t* raw_full, const WaitCtl& w, int lane,
+                                                 int tile0, int tile_step, uint32_t rank, uint32_t full_leader) {
   const int n_raw = (p.num_kb + C::RAW_KB - 1) / C::RAW_KB;
   const bool by_tma = p.sf_mode == kSfTma;
   auto issue = [&](int t, int r, uint32_t slot) {
     int mb, nb;
     tile_coords(p, t, mb, nb);
     uint8_t* raw = smem + C::OFF_RAW + slot * C::RAW_STAGE_BYTES;
+    const int a_row = mb * C::TILE_M + static_cast<int>(rank) * C::BM;
     if (by_tma) {
       if (lane == 0) {
         mbar_arrive_expect_tx(&raw_full[slot], C::RAW_TX);
-        tma_load_2d(raw, tmSA, &raw_full[slot], r * 16, mb * C::BM);
+        tma_load_2d(raw, tmSA, &raw_full[slot], r * 16, a_row);
         tma_load_2d(raw + C::RAW_A_BYTES, tmSB, &raw_full[slot], r * 16, nb * C::BN);
       }
     } else {
-      raw_fetch_async<C>(p, smem_u32(raw), &raw_full[slot], mb, nb, r, lane);
+      raw_fetch_async<C>(p, smem_u32(raw), &raw_full[slot], a_row, nb, r, lane);
     }
   };
   int stage = 0;
   uint32_t phase = 0;
   uint32_t seq = 0;     // raw fetches consumed so far
   uint32_t issued = 0;  // raw fetches issued so far (same value in every lane)
-  int t = blockIdx.x;
+  int t = tile0;
   int r = 0;
   if (t < p.num_tiles) {
     issue(t, 0, 0);
@@ -355,7 +475,7 @@ __device__ __forceinline__ void scale_stager_raw(const GemmParams& p, const CUte
     // consumed by this warp in the previous iteration)
     int t2 = t, r2 = r + 1;
     if (r2 == n_raw) {
-      t2 = t + gridDim.x;
+      t2 = t + tile_step;
       r2 = 0;
     }
     fence_proxy_async_smem();
@@ -387,7 +507,7 @@ __device__ __forceinline__ void scale_stager_raw(const GemmParams& p, const CUte
                              sub * C::SF_ATOMS_K);
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&full[stage]);
+        if (lane == 0) scale_slot_ready<C>(full, full_leader, stage);
         if (++stage == C::STAGES) {
           stage = 0;
           phase ^= 1u;
@@ -416,14 +536,16 @@ __device__ __forceinline__ void scale_stager_raw(const GemmParams& p, const CUte
 // scale bytes per row and atom, one 32-bit load each.
 template <class C>
 __device__ __forceinline__ void scale_stager_ldg(const GemmParams& p, uint8_t* smem, uint64_t* full, uint64_t* empty,
-                                                 const WaitCtl& w, int lane) {
+                                                 const WaitCtl& w, int lane, int tile0, int tile_step, uint32_t rank,
+                                                 uint32_t full_leader) {
   int stage = 0;
   uint32_t phase = 0;
   bool ok = true;
 #pragma unroll 1
-  for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+  for (int t = tile0; ok && t < p.num_tiles; t += tile_step) {
     int mb, nb;
     tile_coords(p, t, mb, nb);
+    const int a_row = mb * C::TILE_M + static_cast<int>(rank) * C::BM;
 #pragma unroll 1
     for (int kb = 0; kb < p.num_kb; ++kb) {
       if (!mbar_wait(&empty[stage], phase ^ 1u, w, kSiteScaleEmpty)) {
@@ -437,7 +559,7 @@ __device__ __forceinline__ void scale_stager_ldg(const GemmParams& p, uint8_t* s
       for (int g = 0; g < C::SF_ATOMS_K; ++g) {
         uint32_t v[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) v[j] = load_sf4(p.sA, mb * C::BM + 32 * j + lane, p.M, col0 + 4 * g, p.sf_cols);
+        for (int j = 0; j < 4; ++j) v[j] = load_sf4(p.sA, a_row + 32 * j + lane, p.M, col0 + 4 * g, p.sf_cols);
         st_shared_v4(sf + 512 * g + 16 * lane, v[0], v[1], v[2], v[3]);
       }
 #pragma unroll
@@ -453,7 +575,7 @@ __device__ __forceinline__ void scale_stager_ldg(const GemmParams& p, uint8_t* s
       }
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&full[stage]);
+      if (lane == 0) scale_slot_ready<C>(full, full_leader, stage);
       if (++stage == C::STAGES) {
         stage = 0;
         phase ^= 1u;
@@ -466,7 +588,7 @@ template <class C>
 __global__ void __launch_bounds__(C::NUM_THREADS, 1)
     qk_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
-                   const GemmParams p) {
+                   const __grid_constant__ CUtensorMap tmOut, const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
@@ -480,8 +602,10 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const uint32_t rank = C::PAIR ? cluster_ctarank() : 0u;  // CTA within the pair
-  const bool leader = rank == 0u;                           // issues the MMAs
+  const uint32_t rank = C::CTAS > 1 ? cluster_ctarank() : 0u;  // CTA within the cluster
+  const bool leader = rank == 0u;                           // a pair's MMA issuer
+  // a pair issues its MMAs from the leader; multicast CTAs each issue their own
+  const bool issues_mma = C::PAIR ? leader : true;
   // tiles are walked per cluster (one CTA or a pair)
   const int tile0 = static_cast<int>(blockIdx.x) / C::CTAS;
   const int tile_step = static_cast<int>(gridDim.x) / C::CTAS;
@@ -489,13 +613,13 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
   if (threadIdx.x == 0) {
 #pragma unroll 1
     for (int s = 0; s < C::STAGES; ++s) {
-      mbar_init(&full[s], C::MX ? 2u : 1u);
-      mbar_init(&empty[s], 1u);
+      mbar_init(&full[s], C::FULL_ARRIVALS);
+      mbar_init(&empty[s], C::MCAST ? 2u : 1u);  // with B multicast both CTAs' MMAs release a slot
     }
 #pragma unroll 1
     for (int a = 0; a < C::ACC_BUFS; ++a) {
       mbar_init(&acc_full[a], 1u);
-      mbar_init(&acc_empty[a], static_cast<uint32_t>(C::EPI_WARPS * C::CTAS));
+      mbar_init(&acc_empty[a], static_cast<uint32_t>(C::EPI_WARPS * (C::PAIR ? 2 : 1)));
     }
     mbar_init(drain, 1u);
 #pragma unroll 1
@@ -504,6 +628,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmOut);
     if (C::MX && p.sf_mode == kSfTma) {
       tma_prefetch_desc(&tmSA);
       tma_prefetch_desc(&tmSB);
@@ -520,7 +645,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
   }
   tc_fence_before_sync();
   __syncthreads();
-  if constexpr (C::PAIR) cluster_sync();  // peers' barriers exist before anyone signals them
+  if constexpr (C::CTAS > 1) cluster_sync();  // peers' barriers exist before anyone signals them
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
   const WaitCtl w{abort_flag, p.err, p.timeout_ns};
@@ -532,14 +657,14 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
       uint32_t phase = 0;
       long long issued = 0;
       bool ok = true;
-#pragma unroll 1
       // in a pair, both CTAs' loads complete on the leader's ring barriers
       const uint32_t full_leader = C::PAIR ? mapa_shared(smem_u32(&full[0]), 0u) : 0u;
+#pragma unroll 1
       for (int t = tile0; ok && t < p.num_tiles; t += tile_step) {
         int mb, nb;
         tile_coords(p, t, mb, nb);
-        const int a_row = mb * C::MMA_M + static_cast<int>(rank) * C::BM;
-        const int b_row = nb * C::BN + static_cast<int>(rank) * C::B_ROWS;
+        const int a_row = mb * C::TILE_M + static_cast<int>(rank) * C::BM;
+        const int b_row = nb * C::BN + static_cast<int>(rank) * C::B_LOAD_ROWS;
 #pragma unroll 1
         for (int kb = 0; kb < p.num_kb; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, w, kSiteProducerEmpty)) {
@@ -551,6 +676,12 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
             const uint32_t fb = full_leader + 8u * static_cast<uint32_t>(stage);
             tma_load_2d_pair(smem + C::OFF_A + stage * C::A_BYTES, &tmA, fb, kb * C::TMA_K, a_row);
             tma_load_2d_pair(smem + C::OFF_B + stage * C::B_BYTES, &tmB, fb, kb * C::TMA_K, b_row);
+          } else if constexpr (C::MCAST) {
+            mbar_arrive_expect_tx(&full[stage], C::STAGE_TX);
+            tma_load_2d(smem + C::OFF_A + stage * C::A_BYTES, &tmA, &full[stage], kb * C::TMA_K, a_row);
+            // this CTA's half of B, into both CTAs at the half's offset
+            tma_load_2d_multicast(smem + C::OFF_B + stage * C::B_BYTES + rank * (C::B_LOAD_ROWS * C::ROW_BYTES), &tmB,
+                                  &full[stage], kb * C::TMA_K, b_row, 0x3);
           } else {
             mbar_arrive_expect_tx(&full[stage], C::STAGE_TX);
             tma_load_2d(smem + C::OFF_A + stage * C::A_BYTES, &tmA, &full[stage], kb * C::TMA_K, a_row);
@@ -568,7 +699,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
       // barriers count the loads; the peer is held by the final cluster
       // barrier until the leader has seen them land.
       const WaitCtl wd{abort_flag, p.err, p.timeout_ns};
-      const long long drain_n = leader ? (issued < C::STAGES ? issued : C::STAGES) : 0;
+      const long long drain_n = issues_mma ? (issued < C::STAGES ? issued : C::STAGES) : 0;
 #pragma unroll 1
       for (long long i = 0; i < drain_n; ++i) {
         const long long L = issued - 1 - i;
@@ -587,7 +718,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
     __syncwarp();
   } else if (warp == 1) {
     // ---------------- MMA issuer (the leader CTA of a pair) ----------------
-    if (lane == 0 && leader) {
+    if (lane == 0 && issues_mma) {
       int stage = 0;
       uint32_t phase = 0;
       uint32_t acc_iter = 0;
@@ -610,7 +741,10 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
           const int kb1 = min(p.num_kb, kb0 + p.chunk_kb);
 #pragma unroll 1
           for (int kb = kb0; kb < kb1; ++kb) {
-            if (!mbar_wait(&full[stage], phase, w, kSiteMmaFull)) {
+            // scale slots of a pair are released by the peer's scale warp too
+            const bool landed = (C::PAIR && C::MX) ? mbar_wait_cluster(&full[stage], phase, w, kSiteMmaFull)
+                                                   : mbar_wait(&full[stage], phase, w, kSiteMmaFull);
+            if (!landed) {
               ok = false;
               break;
             }
@@ -619,12 +753,17 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
             if constexpr (C::MX) {
               const uint32_t sf_smem = smem_u32(smem + C::OFF_SF + stage * C::SF_STAGE_BYTES);
 #pragma unroll
-              for (int i = 0; i < C::SF_ATOMS_K; ++i)
-                tmem_cp_32x128b_warpx4(sf_tmem + 4 * i, make_smem_desc(sf_smem + 512 * i, 128, 128, 0));
-#pragma unroll
-              for (int i = 0; i < C::SF_ATOMS_K * C::NB128; ++i)
-                tmem_cp_32x128b_warpx4(sf_tmem + C::SF_COLS_A + 4 * i,
-                                       make_smem_desc(sf_smem + C::SFA_BYTES + 512 * i, 128, 128, 0));
+              for (int i = 0; i < C::SF_ATOMS_K + C::SF_ATOMS_K * C::NB128; ++i) {
+                // atoms: A's first, then B's; TMEM columns in the same order
+                const uint32_t col = i < C::SF_ATOMS_K ? 4 * i : C::SF_COLS_A + 4 * (i - C::SF_ATOMS_K);
+                const uint32_t src = i < C::SF_ATOMS_K ? sf_smem + 512 * i
+                                                        : sf_smem + C::SFA_BYTES + 512 * (i - C::SF_ATOMS_K);
+                if constexpr (C::PAIR) {
+                  tmem_cp_32x128b_warpx4_pair(sf_tmem + col, make_smem_desc(src, 128, 128, 0));
+                } else {
+                  tmem_cp_32x128b_warpx4(sf_tmem + col, make_smem_desc(src, 128, 128, 0));
+                }
+              }
             }
             const uint64_t adesc = make_desc_kmajor_sw128(smem_u32(smem + C::OFF_A + stage * C::A_BYTES));
             const uint64_t bdesc = make_desc_kmajor_sw128(smem_u32(smem + C::OFF_B + stage * C::B_BYTES));
@@ -649,18 +788,29 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                   umma_f8f6f4(d_tmem, ad, bd, C::idesc(0, 0), accum);
                 } else if constexpr (C::kind == Kind::MXF8) {
                   // one scale byte per row per MMA: byte j of the stage's column
-                  umma_mxf8f6f4(d_tmem, ad, bd, C::idesc(j, j), sf_tmem, sf_tmem + C::SF_COLS_A, accum);
+                  if constexpr (C::PAIR) {
+                    umma_mxf8f6f4_pair(d_tmem, ad, bd, C::idesc(j, j), sf_tmem, sf_tmem + C::SF_COLS_A, accum);
+                  } else {
+                    umma_mxf8f6f4(d_tmem, ad, bd, C::idesc(j, j), sf_tmem, sf_tmem + C::SF_COLS_A, accum);
+                  }
                 } else {
                   // two scale bytes per row per MMA: bytes 2(j%2), 2(j%2)+1 of column group j/2
                   const uint32_t g = static_cast<uint32_t>(j >> 1);
                   const uint32_t id = static_cast<uint32_t>((j & 1) * 2);
-                  umma_mxf4(d_tmem, ad, bd, C::idesc(id, id), sf_tmem + 4 * g,
-                            sf_tmem + C::SF_COLS_A + 4 * C::NB128 * g, accum);
+                  if constexpr (C::PAIR) {
+                    umma_mxf4_pair(d_tmem, ad, bd, C::idesc(id, id), sf_tmem + 4 * g,
+                                   sf_tmem + C::SF_COLS_A + 4 * C::NB128 * g, accum);
+                  } else {
+                    umma_mxf4(d_tmem, ad, bd, C::idesc(id, id), sf_tmem + 4 * g,
+                              sf_tmem + C::SF_COLS_A + 4 * C::NB128 * g, accum);
+                  }
                 }
               }
             }
             if constexpr (C::PAIR) {
               umma_commit_pair_multicast(&empty[stage], 0x3);  // frees the slot in both CTAs
+            } else if constexpr (C::MCAST) {
+              umma_commit_multicast(&empty[stage], 0x3);  // both CTAs' producers refill this slot
             } else {
               umma_commit(&empty[stage]);
             }
@@ -697,10 +847,12 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
   } else if (warp == 2) {
     // ---------------- scale stager (MX) ----------------
     if constexpr (C::MX) {
+      const uint32_t full_leader = C::PAIR ? mapa_shared(smem_u32(&full[0]), 0u) : 0u;
       if (p.sf_mode == kSfTma || p.sf_mode == kSfAsync) {
-        scale_stager_raw<C>(p, &tmSA, &tmSB, smem, full, empty, raw_full, w, lane);
+        scale_stager_raw<C>(p, &tmSA, &tmSB, smem, full, empty, raw_full, w, lane, tile0, tile_step, rank,
+                            full_leader);
       } else {
-        scale_stager_ldg<C>(p, smem, full, empty, w, lane);
+        scale_stager_ldg<C>(p, smem, full, empty, w, lane, tile0, tile_step, rank, full_leader);
       }
     }
     __syncwarp();
@@ -711,6 +863,9 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
     const int r = q * 32 + lane;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16);
     const int col_part = part * C::EPI_COLS;
+    OutStager ostg{smem_u32(smem + C::OFF_OUT) +
+                       static_cast<uint32_t>((warp - 4) * C::OUT_BUFS * C::OUT_BLOCK_BYTES),
+                   0u};
     uint32_t acc_iter = 0;
     bool ok = true;
     // accumulator releases go to the leader CTA's barrier
@@ -730,8 +885,10 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
     for (int t = tile0; ok && t < p.num_tiles; t += tile_step) {
       int mb, nb;
       tile_coords(p, t, mb, nb);
-      const int m = mb * C::MMA_M + static_cast<int>(rank) * C::BM + r;
+      const int m_block = mb * C::TILE_M + static_cast<int>(rank) * C::BM + q * 32;  // row of lane 0
+      const int m = m_block + lane;
       const bool row_ok = m < p.M;
+      const bool block_ok = m_block < p.M;  // warp-uniform: any row of this block inside M
       float sam = 1.f;
       if constexpr (C::ROWWISE) sam = row_ok ? __ldg(p.sa + m) : 0.f;
       const int n_tile = nb * C::BN + col_part;
@@ -747,6 +904,19 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
         tc_fence_after_sync();
         const bool last = c == p.num_chunks - 1;
         const uint32_t acc_col = lane_base + static_cast<uint32_t>(C::COL_ACC + a * C::BN + col_part);
+        // stages and stores one 32x32 output block from 32 values per lane
+        auto emit = [&](auto tag, int n0, const auto& vals) {
+          constexpr bool kInt = decltype(tag)::kInt;
+          constexpr int kOff = decltype(tag)::kOff;
+          if (!(block_ok && n0 < p.N)) return;
+          if constexpr (C::STORE_TMA) {
+            const uint32_t block = out_block_acquire<C>(ostg, lane);
+            epilogue_row32<C::ROWWISE || kInt, kInt, kOff>(p, n0, sam, vals, block, lane);
+            out_block_release<C>(ostg, block, &tmOut, n0, m_block, lane);
+          } else if (row_ok) {
+            epilogue_row32_global<C::ROWWISE || kInt, kInt, kOff>(p, m, n0, sam, vals);
+          }
+        };
         if constexpr (C::REG_SUMS) {
           // drain the chunk into the register sums, free the accumulator, and
           // after the last chunk run the epilogue from the registers
@@ -763,9 +933,9 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
             }
           }
           release(a);
-          if (last && row_ok) {
-            if (n_tile < p.N) epilogue_row32<true, true, 0, C::EPI_COLS>(p, m, n_tile, sam, sums);
-            if (n_tile + 32 < p.N) epilogue_row32<true, true, 32, C::EPI_COLS>(p, m, n_tile + 32, sam, sums);
+          if (last) {
+            emit(EmitTag<true, 0>{}, n_tile, sums);
+            emit(EmitTag<true, 32>{}, n_tile + 32, sums);
           }
         } else {
           // With one accumulator the final chunk's totals go back to the TMEM
@@ -792,11 +962,11 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
               }
               if (!last || early_release) {
                 tmem_st_32cols(sum_col, v);
-              } else if (row_ok && n0 < p.N) {
-                epilogue_row32<true, true>(p, m, n0, sam, v);
+              } else {
+                emit(EmitTag<true, 0>{}, n0, v);
               }
             } else {
-              if (row_ok && n0 < p.N) epilogue_row32<C::ROWWISE, false>(p, m, n0, sam, v);
+              emit(EmitTag<false, 0>{}, n0, v);
             }
           }
           if constexpr (C::INT_CHUNKS) tmem_wait_st();
@@ -808,19 +978,20 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
               uint32_t v[32];
               tmem_ld_32cols(lane_base + static_cast<uint32_t>(C::COL_SUM + col_part + 32 * g), v);
               tmem_wait_ld();
-              if (row_ok && n0 < p.N) epilogue_row32<true, true>(p, m, n0, sam, v);
+              emit(EmitTag<true, 0>{}, n0, v);
             }
           }
         }
         ++acc_iter;
       }
     }
+    if (C::STORE_TMA && lane == 0) bulk_wait_group_all();  // stores finished reading shared memory
     __syncwarp();
   }
 
   tc_fence_before_sync();
   __syncthreads();
-  if constexpr (C::PAIR) cluster_sync();  // the pair finishes together; TMEM is freed by both
+  if constexpr (C::CTAS > 1) cluster_sync();  // the cluster finishes together (peers signal our barriers)
   tc_fence_after_sync();
   if (warp == 1) {
     if constexpr (C::PAIR) {

@@ -21,7 +21,7 @@ namespace qk {
 // 256 x 256 tiles per CTA pair, two fp32 accumulators of 256 columns per SM
 // (all 512 TMEM columns); 16 epilogue warps keep the int32 running sums in
 // registers, so a chunk drains while the MMAs fill the other accumulator.
-using CfgInt8 = GemmCfg<Kind::F16, 256, 6, 2, true, 16>;
+using CfgInt8 = GemmCfg<Kind::F16, 256, 6, 2, true, 16, 1>;
 
 // Widens 16 int8 values per thread-iteration to f16.  Byte x becomes the f16
 // bit pattern 0x6400 | (x + 128), i.e. the value 1024 + x + 128, and one
@@ -82,7 +82,7 @@ static inline int widen_and_gemm_int8(const int8_t* A, const int8_t* B, const fl
   if (st == QK_OK)
     st = encode_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a16, K, M, static_cast<uint64_t>(K) * 2, C::TMA_K, C::BM);
   if (st == QK_OK)
-    st = encode_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, b16, K, N, static_cast<uint64_t>(K) * 2, C::TMA_K, C::B_ROWS);
+    st = encode_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, b16, K, N, static_cast<uint64_t>(K) * 2, C::TMA_K, C::B_LOAD_ROWS);
   if (st == QK_OK) {
     GemmParams p{};
     plan_tiles<C>(p, M, N, K);

@@ -6,7 +6,7 @@
 
 #include <cstdint>
 
-#include "../../include/qk.h"
+#include "qk.h"
 
 namespace qk {
 
@@ -34,6 +34,9 @@ int encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base
 int encode_tmap_2d_plain(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t inner,
                          uint64_t rows, uint64_t row_pitch_bytes, uint32_t box_inner, uint32_t box_rows);
 
+// bf16 [rows, cols] output in 32x32 boxes with the 64-byte swizzle.
+int encode_tmap_out(CUtensorMap* map, void* out, uint64_t rows, uint64_t cols);
+
 uint64_t wait_timeout_ns();
 void count_launches(uint64_t n);
 
@@ -45,7 +48,8 @@ enum KernelKind : int {
   kKGemmMxfp8 = 3,
   kKGemmMxfp4 = 4,
   kKWaitProbe = 5,
-  kKNumKinds = 6,
+  kKQuantize = 6,
+  kKNumKinds = 7,
 };
 
 // Brackets one kernel launch with an event pair when timing is enabled.

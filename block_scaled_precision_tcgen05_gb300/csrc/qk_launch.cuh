@@ -11,6 +11,8 @@ inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
 // Fills the tile/k-block bookkeeping of GemmParams for configuration C.
 // Row-blocks per raster group: QK_GROUP_M from the environment, else 8.
 int raster_group_m();
+// Kernel variant index from an environment variable (0 if unset).
+int kernel_variant(const char* env_name);
 
 template <class C>
 void plan_tiles(GemmParams& p, int M, int N, int K) {
@@ -19,7 +21,7 @@ void plan_tiles(GemmParams& p, int M, int N, int K) {
   p.N = N;
   p.K = K;
   p.num_kb = ceil_div(K, C::K_ELEMS);
-  p.num_m_blocks = ceil_div(M, C::MMA_M);
+  p.num_m_blocks = ceil_div(M, C::TILE_M);
   p.num_n_blocks = ceil_div(N, C::BN);
   p.num_tiles = p.num_m_blocks * p.num_n_blocks;
   if (C::INT_CHUNKS) {
@@ -49,14 +51,14 @@ int launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap&
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   int slots = dev.sm_count;  // concurrently resident CTAs (one per SM) or CTA pairs
-  if constexpr (C::PAIR) {
+  if constexpr (C::CTAS > 1) {
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    // how many pairs fit at once (SMs pair up within a GPC), computed once per device
+    // how many clusters fit at once (SMs pair up within a GPC), computed once per device
     static int cached[64];
     int& clusters = cached[dev.device >= 0 && dev.device < 64 ? dev.device : 0];
     if (clusters == 0) {
@@ -72,8 +74,12 @@ int launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap&
   }
   const int ctas = (p.num_tiles < slots ? p.num_tiles : slots) * C::CTAS;
   cfg.gridDim = dim3(ctas, 1, 1);
+  // the output as 32x32 bf16 boxes with the 64-byte swizzle of the staging blocks
+  CUtensorMap tout;
+  if (encode_tmap_out(&tout, p.out, static_cast<uint64_t>(p.M), static_cast<uint64_t>(p.N)) != QK_OK)
+    return QK_ERR_CUDA;
   LaunchTimer timer(kernel_kind<C>(), stream);
-  e = cudaLaunchKernelEx(&cfg, kernel, ta, tb, tsa, tsb, p);
+  e = cudaLaunchKernelEx(&cfg, kernel, ta, tb, tsa, tsb, tout, p);
   timer.done();
   if (e != cudaSuccess) {
     cudaGetLastError();

@@ -6,15 +6,21 @@
 
 namespace qk {
 
-using CfgMxfp4 = GemmCfg<Kind::MXF4, 256, 4, 1>;
+// Two variants: 128 x 256 tiles on one CTA (4 stages, 4 epilogue warps), or
+// 256 x 256 tiles on a CTA pair (5 stages, 8 epilogue warps); one 256-column
+// accumulator per SM plus the scale-factor ring in TMEM either way.
+using CfgMxfp4Single = GemmCfg<Kind::MXF4, 256, 4, 1, false, 4, 1>;
+using CfgMxfp4Pair = GemmCfg<Kind::MXF4, 256, 5, 1, true, 8, 2>;
+using CfgMxfp4Mcast = GemmCfg<Kind::MXF4, 256, 4, 1, false, 4, 1, true>;
 
-int launch_mxfp4(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const uint8_t* sB, const uint16_t* bias,
-                 uint16_t* out, int M, int N, int K, const DeviceInfo& dev, cudaStream_t stream) {
-  using C = CfgMxfp4;
+template <class C>
+static int launch_mxfp4_cfg(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const uint8_t* sB,
+                      const uint16_t* bias, uint16_t* out, int M, int N, int K, const DeviceInfo& dev,
+                      cudaStream_t stream) {
   CUtensorMap ta, tb;
   const uint64_t kb = static_cast<uint64_t>(K) / 2;  // bytes per row
   int st = encode_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, kb, M, kb, C::TMA_K, C::BM);
-  if (st == QK_OK) st = encode_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, kb, N, kb, C::TMA_K, C::B_ROWS);
+  if (st == QK_OK) st = encode_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, kb, N, kb, C::TMA_K, C::B_LOAD_ROWS);
   if (st != QK_OK) return st;
   GemmParams p{};
   plan_tiles<C>(p, M, N, K);
@@ -37,6 +43,14 @@ int launch_mxfp4(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const ui
     if (st != QK_OK) return st;
   }
   return launch_gemm<C>(ta, tb, tsa, tsb, p, dev, stream);
+}
+
+int launch_mxfp4(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const uint8_t* sB, const uint16_t* bias,
+                 uint16_t* out, int M, int N, int K, const DeviceInfo& dev, cudaStream_t stream) {
+  const int v = kernel_variant("QK_MX_VARIANT");
+  if (v == 1) return launch_mxfp4_cfg<CfgMxfp4Pair>(A, sA, B, sB, bias, out, M, N, K, dev, stream);
+  if (v == 2) return launch_mxfp4_cfg<CfgMxfp4Mcast>(A, sA, B, sB, bias, out, M, N, K, dev, stream);
+  return launch_mxfp4_cfg<CfgMxfp4Single>(A, sA, B, sB, bias, out, M, N, K, dev, stream);
 }
 
 }  // namespace qk

@@ -6,14 +6,20 @@
 
 namespace qk {
 
-using CfgMxfp8 = GemmCfg<Kind::MXF8, 256, 4, 1>;
+// Two variants: 128 x 256 tiles on one CTA (4 stages, 4 epilogue warps), or
+// 256 x 256 tiles on a CTA pair (5 stages, 8 epilogue warps); one 256-column
+// accumulator per SM plus the scale-factor ring in TMEM either way.
+using CfgMxfp8Single = GemmCfg<Kind::MXF8, 256, 4, 1, false, 4, 1>;
+using CfgMxfp8Pair = GemmCfg<Kind::MXF8, 256, 5, 1, true, 8, 2>;
+using CfgMxfp8Mcast = GemmCfg<Kind::MXF8, 256, 4, 1, false, 4, 1, true>;
 
-int launch_mxfp8(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const uint8_t* sB, const uint16_t* bias,
-                 uint16_t* out, int M, int N, int K, const DeviceInfo& dev, cudaStream_t stream) {
-  using C = CfgMxfp8;
+template <class C>
+static int launch_mxfp8_cfg(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const uint8_t* sB,
+                      const uint16_t* bias, uint16_t* out, int M, int N, int K, const DeviceInfo& dev,
+                      cudaStream_t stream) {
   CUtensorMap ta, tb;
   int st = encode_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, K, M, K, C::TMA_K, C::BM);
-  if (st == QK_OK) st = encode_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, K, N, K, C::TMA_K, C::B_ROWS);
+  if (st == QK_OK) st = encode_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, K, N, K, C::TMA_K, C::B_LOAD_ROWS);
   if (st != QK_OK) return st;
   GemmParams p{};
   plan_tiles<C>(p, M, N, K);
@@ -36,6 +42,14 @@ int launch_mxfp8(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const ui
     if (st != QK_OK) return st;
   }
   return launch_gemm<C>(ta, tb, tsa, tsb, p, dev, stream);
+}
+
+int launch_mxfp8(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const uint8_t* sB, const uint16_t* bias,
+                 uint16_t* out, int M, int N, int K, const DeviceInfo& dev, cudaStream_t stream) {
+  const int v = kernel_variant("QK_MX_VARIANT");
+  if (v == 1) return launch_mxfp8_cfg<CfgMxfp8Pair>(A, sA, B, sB, bias, out, M, N, K, dev, stream);
+  if (v == 2) return launch_mxfp8_cfg<CfgMxfp8Mcast>(A, sA, B, sB, bias, out, M, N, K, dev, stream);
+  return launch_mxfp8_cfg<CfgMxfp8Single>(A, sA, B, sB, bias, out, M, N, K, dev, stream);
 }
 
 }  // namespace qk

@@ -1,0 +1,248 @@
+// qk_skinny_kernel.cuh -- FP8 per-token x per-channel GEMM for few rows
+// (M <= 128): the weight streams through HBM once and sets the time.
+//
+// The product is computed transposed, D^T[n, m] = sum_k B[n,k] A[m,k]: a
+// tile of 128 weight rows is the MMA's M operand (TMEM lanes = n), the M
+// activation rows, padded to MT, are its N operand (TMEM columns = m).  K is
+// split over a cluster of SPLITS CTAs; each CTA accumulates its K range in
+// TMEM, stages the fp32 partial in shared memory as [m][n], and after a
+// cluster barrier every CTA sums, in fixed order over the cluster, the rows
+// m it owns by reading its peers' partials through distributed shared
+// memory, then applies the fixed-order epilogue (x*sa[m])*sb[n] (+bias[n])
+// and writes bf16 rows of the output with coalesced stores.
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include "qk_device.cuh"
+#include "qk_gemm_kernel.cuh"
+
+namespace qk {
+
+struct SkinnyParams {
+  int M, N, K;
+  int num_kb;        // k-blocks of 128 elements
+  int kb_per_split;  // k-blocks per CTA of a cluster
+  const float* sa;
+  const float* sb;
+  const uint16_t* bias;
+  uint16_t* out;
+  unsigned long long* err;
+  uint64_t timeout_ns;
+};
+
+template <int MT_, int SPLITS_, int STAGES_>
+struct SkinnyCfg {
+  static constexpr int MT = MT_;          // padded activation rows (MMA N)
+  static constexpr int NT = 128;          // weight rows per tile (MMA M)
+  static constexpr int SPLITS = SPLITS_;  // CTAs of a cluster splitting K
+  static constexpr int STAGES = STAGES_;
+  static constexpr int K_ELEMS = 128;     // E4M3 elements per stage (one 128-byte swizzle row)
+  static constexpr int W_BYTES = NT * 128;
+  static constexpr int A_BYTES = MT * 128;
+  static constexpr uint32_t STAGE_TX = W_BYTES + A_BYTES;
+  static constexpr int OFF_W = 0;
+  static constexpr int OFF_A = OFF_W + STAGES * W_BYTES;
+  static constexpr int OFF_RED = OFF_A + STAGES * A_BYTES;  // fp32 partial [MT][NT]
+  static constexpr int RED_BYTES = MT * NT * 4;
+  static constexpr int OFF_BAR = OFF_RED + RED_BYTES;
+  static constexpr int OFF_MISC = OFF_BAR + (2 * STAGES + 2) * 8;
+  static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
+  static constexpr int TMEM_COLS = MT <= 32 ? 32 : MT <= 64 ? 64 : MT <= 128 ? 128 : 256;
+  static constexpr int ROWS_PER_CTA = MT / SPLITS;  // output rows each CTA reduces
+  static constexpr int NUM_THREADS = 256;
+  static_assert(MT % 32 == 0 && MT >= 32 && MT <= 128, "activation tile");
+  static_assert(MT % SPLITS == 0, "rows per split");
+  static_assert(SMEM_BYTES <= 232448, "shared-memory budget");
+  static constexpr uint32_t IDESC = make_idesc_dense(1, 0, 0, NT, MT);  // fp32 D, E4M3 x E4M3
+};
+
+// A load from another CTA's shared memory.  Not volatile: the partials it
+// reads are stable between the two cluster barriers, so the compiler may
+// issue all of a thread's loads before the first use.
+__device__ __forceinline__ float ld_shared_cluster_f32(uint32_t cluster_addr) {
+  float v;
+  asm("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(cluster_addr));
+  return v;
+}
+
+template <class C>
+__global__ void __launch_bounds__(C::NUM_THREADS, 1)
+    qk_skinny_fp8_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmA,
+                         const SkinnyParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* empty = full + C::STAGES;
+  uint64_t* acc_full = empty + C::STAGES;
+  uint64_t* drain = acc_full + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_MISC + 4);
+  float* red = reinterpret_cast<float*>(smem + C::OFF_RED);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int split = C::SPLITS > 1 ? static_cast<int>(cluster_ctarank()) : 0;
+  const int tile = static_cast<int>(blockIdx.x) / C::SPLITS;
+  const int n0 = tile * C::NT;
+  const int kb0 = split * p.kb_per_split;
+  const int kb1 = min(p.num_kb, kb0 + p.kb_per_split);
+
+  if (threadIdx.x == 0) {
+#pragma unroll 1
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&full[s], 1u);
+      mbar_init(&empty[s], 1u);
+    }
+    mbar_init(acc_full, 1u);
+    mbar_init(drain, 1u);
+    *abort_flag = 0u;
+    fence_mbar_init();
+    tma_prefetch_desc(&tmW);
+    tma_prefetch_desc(&tmA);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+  const WaitCtl w{abort_flag, p.err, p.timeout_ns};
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int issued = 0;
+#pragma unroll 1
+      for (int kb = kb0; kb < kb1; ++kb) {
+        if (!mbar_wait(&empty[stage], phase ^ 1u, w, kSiteProducerEmpty)) break;
+        mbar_arrive_expect_tx(&full[stage], C::STAGE_TX);
+        tma_load_2d(smem + C::OFF_W + stage * C::W_BYTES, &tmW, &full[stage], kb * C::K_ELEMS, n0);
+        tma_load_2d(smem + C::OFF_A + stage * C::A_BYTES, &tmA, &full[stage], kb * C::K_ELEMS, 0);
+        ++issued;
+        if (++stage == C::STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      // wait (bounded) for the last load of every ring slot before leaving
+#pragma unroll 1
+      for (int i = 0; i < (issued < C::STAGES ? issued : C::STAGES); ++i) {
+        const int L = issued - 1 - i;
+        const uint32_t a = smem_u32(&full[L % C::STAGES]);
+        const uint64_t t0 = global_timer_ns();
+        while (!mbar_try_wait(a, static_cast<uint32_t>((L / C::STAGES) & 1))) {
+          if (global_timer_ns() - t0 > p.timeout_ns) {
+            report_error(p.err, kDevErrTimeout, kSiteProducerDrain, static_cast<uint32_t>(L));
+            break;
+          }
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+#pragma unroll 1
+      for (int kb = kb0; kb < kb1; ++kb) {
+        if (!mbar_wait(&full[stage], phase, w, kSiteMmaFull)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        const uint64_t wdesc = make_desc_kmajor_sw128(smem_u32(smem + C::OFF_W + stage * C::W_BYTES));
+        const uint64_t adesc = make_desc_kmajor_sw128(smem_u32(smem + C::OFF_A + stage * C::A_BYTES));
+        int ksteps = 4;
+        if (kb == p.num_kb - 1) ksteps = min(4, (p.K - kb * C::K_ELEMS + 31) / 32);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (j < ksteps)
+            umma_f8f6f4(tmem, wdesc + static_cast<uint64_t>(2 * j), adesc + static_cast<uint64_t>(2 * j),
+                        C::IDESC, (kb > kb0 || j > 0) ? 1u : 0u);
+        umma_commit(&empty[stage]);
+        if (++stage == C::STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (ok) umma_commit(acc_full);
+      umma_commit(drain);
+      const uint32_t da = smem_u32(drain);
+      const uint64_t t0 = global_timer_ns();
+      while (!mbar_try_wait(da, 0u)) {
+        if (global_timer_ns() - t0 > p.timeout_ns) {
+          report_error(p.err, kDevErrTimeout, kSiteDrain, 0u);
+          break;
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // partial D^T (lane = weight row, column = activation row) -> red[m][n]
+    const int q = warp - 4;
+    const int nr = q * 32 + lane;
+    const bool have = kb1 > kb0 && mbar_wait(acc_full, 0u, w, kSiteEpiAccFull);
+    tc_fence_after_sync();
+#pragma unroll
+    for (int g = 0; g < C::MT / 32; ++g) {
+      uint32_t v[32];
+      if (have) {
+        tmem_ld_32cols(tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(32 * g), v);
+        tmem_wait_ld();
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = 0u;  // empty K range contributes zero
+      }
+#pragma unroll
+      for (int i = 0; i < 32; ++i) red[(32 * g + i) * C::NT + nr] = __uint_as_float(v[i]);
+    }
+    tc_fence_before_sync();
+  }
+
+  // every CTA of the cluster has staged its partial
+  __syncthreads();
+  if constexpr (C::SPLITS > 1) cluster_sync();
+
+  if (warp >= 4) {
+    const int t = (warp - 4) * 32 + lane;  // weight row within the tile
+    const int n = n0 + t;
+    const bool col_ok = n < p.N;
+    const float sbn = col_ok ? __ldg(p.sb + n) : 0.f;
+    const float bn = (col_ok && p.bias) ? __uint_as_float(static_cast<uint32_t>(__ldg(p.bias + n)) << 16) : 0.f;
+    const uint32_t red_base = smem_u32(red);
+#pragma unroll 1
+    for (int i = 0; i < C::ROWS_PER_CTA; ++i) {
+      const int m = split * C::ROWS_PER_CTA + i;
+      if (m >= p.M) break;
+      const uint32_t off = red_base + static_cast<uint32_t>((m * C::NT + t) * 4);
+      float part[C::SPLITS];
+#pragma unroll
+      for (int r = 0; r < C::SPLITS; ++r)
+        part[r] = C::SPLITS > 1 ? ld_shared_cluster_f32(mapa_shared(off, static_cast<uint32_t>(r)))
+                                : red[m * C::NT + t];
+      float sum = 0.f;
+#pragma unroll
+      for (int r = 0; r < C::SPLITS; ++r) sum = __fadd_rn(sum, part[r]);  // fixed order over the cluster
+      if (col_ok) {
+        float x = __fmul_rn(sum, __ldg(p.sa + m));
+        x = __fmul_rn(x, sbn);
+        if (p.bias) x = __fadd_rn(x, bn);
+        p.out[static_cast<size_t>(m) * static_cast<size_t>(p.N) + n] = __bfloat16_as_ushort(__float2bfloat16_rn(x));
+      }
+    }
+  }
+
+  // peers may still read this CTA's partial until everyone is past here
+  if constexpr (C::SPLITS > 1) cluster_sync();
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
+}
+
+}  // namespace qk

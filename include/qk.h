@@ -146,6 +146,30 @@ int qk_gemm_fp8_rowwise(const uint8_t* A, const uint8_t* B, const float* sa, con
                         const uint16_t* bias, uint16_t* out, int64_t M, int64_t N, int64_t K,
                         qk_stream_t stream);
 
+/*
+ * Quantizers that produce the operands above from bf16 data.
+ *
+ * qk_quantize_mx: MX block scaling along K (OCP 1x32, raw row-major scales
+ * as ROCm/mori PR #806 "What" holds them).  For each block of 32 elements of
+ * a row, s = floor(log2(amax)) - emax (8 for E4M3, 2 for E2M1), clamped to
+ * [-127, 127] and -127 for an all-zero block; scales[row, b] = s + 127;
+ * elements x * 2^-s rounded to nearest even and saturated to +-448 (E4M3)
+ * or +-6 (E2M1).  MXFP4 packs element 2i in the low nibble of byte i.
+ *   x      bf16 [rows, K]      q  [rows, K] (E4M3) or [rows, K/2] (E2M1) bytes
+ *   scales uint8 [rows, K/32]
+ * Requirements: x and q 16-byte aligned, K % 32 == 0.  Finite inputs.
+ *
+ * qk_quantize_ptpc: per-row FP8 (per-token scales, ROCm/aiter PR #6262):
+ * s = amax / 448 in fp32 (1 for an all-zero row), q = E4M3(x / s) with the
+ * division and the conversion rounding to nearest even, saturated.
+ *   x bf16 [rows, K]; q uint8 [rows, K]; scales fp32 [rows]
+ * Requirements: x and q 16-byte aligned, scales 4-byte aligned, K % 16 == 0.
+ * Both are bit-identical to these definitions; rows == 0 is a no-op.
+ */
+int qk_quantize_mx(int fmt, const uint16_t* x, uint8_t* q, uint8_t* scales, int64_t rows, int64_t K,
+                   qk_stream_t stream);
+int qk_quantize_ptpc(const uint16_t* x, uint8_t* q, float* scales, int64_t rows, int64_t K, qk_stream_t stream);
+
 /* Human-readable name of a status code (static storage, never NULL). */
 const char* qk_status_string(int status);
 
@@ -183,7 +207,7 @@ uint64_t qk_launch_count(void);
  * up to `max` entries (one per kernel kind that ran) into `stats`; *count
  * receives the number of entries.  reset != 0 clears the totals afterwards.
  * Kernel names: "int8_to_f16", "gemm_int8_f16", "gemm_fp8", "gemm_mxfp8",
- * "gemm_mxfp4", "wait_probe".
+ * "gemm_mxfp4", "wait_probe", "quantize".
  */
 typedef struct {
   const char* name;   /* static storage */
