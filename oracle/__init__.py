@@ -59,6 +59,8 @@ def _declare(lib):
     lib.qko_decode_e2m1.restype = c.c_double
     lib.qko_decode_ue8m0.argtypes = [c.c_uint8]
     lib.qko_decode_ue8m0.restype = c.c_double
+    lib.qko_decode_ue4m3.argtypes = [c.c_uint8]
+    lib.qko_decode_ue4m3.restype = c.c_double
     lib.qko_f32_to_bf16_rne.argtypes = [c.c_float]
     lib.qko_f32_to_bf16_rne.restype = c.c_uint16
     lib.qko_bf16_to_f32.argtypes = [c.c_uint16]
@@ -77,6 +79,10 @@ def _declare(lib):
     lib.qko_gemm_fp8_rowwise.restype = c.c_int
     lib.qko_gemm_mx.argtypes = [c.c_int, P, P, P, P, P, P, i64, i64, i64, i64, i64, i64, i64, i64]
     lib.qko_gemm_mx.restype = c.c_int
+    lib.qko_gemm_nvfp4.argtypes = [P, P, P, P, c.c_float, c.c_float, P, P, i64, i64, i64, i64, i64, i64, i64, i64]
+    lib.qko_gemm_nvfp4.restype = c.c_int
+    lib.qko_gemm_fp8_blockscale.argtypes = [P, P, P, P, P, P, i64, i64, i64, i64, i64, i64, i64, i64]
+    lib.qko_gemm_fp8_blockscale.restype = c.c_int
     lib.qko_num_threads.restype = c.c_int
     lib.qko_init()
 
@@ -126,6 +132,11 @@ def decode_e2m1(codes, lib=None):
 def decode_ue8m0(codes, lib=None):
     lib = lib or load()
     return np.array([lib.qko_decode_ue8m0(int(c)) for c in np.ravel(codes)]).reshape(np.shape(codes))
+
+
+def decode_ue4m3(codes, lib=None):
+    lib = lib or load()
+    return np.array([lib.qko_decode_ue4m3(int(c)) for c in np.ravel(codes)]).reshape(np.shape(codes))
 
 
 def f32_to_bf16(x, lib=None):
@@ -257,4 +268,52 @@ def gemm_mx(fmt, A, sA, B, sB, bias=None, K=None, m0=0, m1=None, n0=0, n1=None, 
                          n1 - n0, M, N, K, m0, m1, n0, n1)
     if rc != OK:
         raise ValueError(f"oracle mx gemm failed with code {rc}")
+    return ref
+
+
+def gemm_nvfp4(A, sA, B, sB, global_a=1.0, global_b=1.0, bias=None, m0=0, m1=None, n0=0, n1=None, lib=None):
+    """fp64 value, before bf16 rounding, of the NVFP4 GEMM (see qko_gemm_nvfp4).
+
+    ``A``/``B`` are packed E2M1 bytes [rows, K/2], ``sA``/``sB`` raw UE4M3
+    bytes [rows, K/16], ``global_a``/``global_b`` the per-tensor fp32 scales.
+    """
+    lib = lib or load()
+    A = _c(A, np.uint8)
+    B = _c(B, np.uint8)
+    sA = _c(sA, np.uint8)
+    sB = _c(sB, np.uint8)
+    bias = _c(bias, np.uint16)
+    M, N = A.shape[0], B.shape[0]
+    K = 2 * A.shape[1]
+    assert B.shape[1] == K // 2 and sA.shape == (M, K // 16) and sB.shape == (N, K // 16)
+    m0, m1, n0, n1 = _region(M, N, m0, m1, n0, n1)
+    ref = np.zeros((m1 - m0, n1 - n0), np.float64)
+    rc = lib.qko_gemm_nvfp4(_ptr(A), _ptr(sA), _ptr(B), _ptr(sB), float(np.float32(global_a)),
+                            float(np.float32(global_b)), _ptr(bias), _ptr(ref), n1 - n0, M, N, K, m0, m1, n0, n1)
+    if rc != OK:
+        raise ValueError(f"oracle nvfp4 gemm failed with code {rc}")
+    return ref
+
+
+def gemm_fp8_blockscale(A, B, sa, sb, bias=None, m0=0, m1=None, n0=0, n1=None, lib=None):
+    """fp64 value, before bf16 rounding, of the FP8 blockscale GEMM (see qko_gemm_fp8_blockscale).
+
+    ``sa`` is [M, ceil(K/128)] and ``sb`` [ceil(N/128), ceil(K/128)] fp32.
+    """
+    lib = lib or load()
+    A = _c(A, np.uint8)
+    B = _c(B, np.uint8)
+    sa = _c(sa, np.float32)
+    sb = _c(sb, np.float32)
+    bias = _c(bias, np.uint16)
+    M, K = A.shape
+    N = B.shape[0]
+    KB, NB = -(-K // 128), -(-N // 128)
+    assert B.shape[1] == K and sa.shape == (M, KB) and sb.shape == (NB, KB)
+    m0, m1, n0, n1 = _region(M, N, m0, m1, n0, n1)
+    ref = np.zeros((m1 - m0, n1 - n0), np.float64)
+    rc = lib.qko_gemm_fp8_blockscale(_ptr(A), _ptr(B), _ptr(sa), _ptr(sb), _ptr(bias), _ptr(ref),
+                                     n1 - n0, M, N, K, m0, m1, n0, n1)
+    if rc != OK:
+        raise ValueError(f"oracle fp8 blockscale gemm failed with code {rc}")
     return ref

@@ -25,10 +25,19 @@
  *           MXFP4 = e2m1 elements with per-1x32 ue8m0 scales, checked
  *           against an MXFP4-dequant reference.
  *  [AITER6262] ROCm/aiter PR #6262, "Technical Details": FP8 A8W8 GEMM with
- *           per-token x per-channel scales.
+ *           per-token x per-channel scales; its gemm_a4w4 signature takes
+ *           optional per-tensor global A and B scales for NVFP4.
+ *  [MORI806-BS] ROCm/mori PR #806, the pipeline-drain fix's measurements:
+ *           a "blockscale" FP8 GEMM kind (16384x7168x2048) beside ptpc and
+ *           mxfp8.  The block sizes are not stated on the page.
  * The element formats (E4M3FN, E2M1, UE8M0) are not defined on the pages;
  * they are restated here from the OCP Microscaling (MX) v1.0 format
  * definitions: sign/exponent/mantissa bit fields with the stated biases.
+ * NVFP4 is not defined on the pages either; it is restated from NVIDIA's
+ * published format: E2M1 elements, one unsigned E4M3 (UE4M3) scale per 16
+ * consecutive K-elements, and one fp32 scale per tensor.  "Blockscale" FP8
+ * is read as the DeepSeek-V3 layout: fp32 scales per 1x128 (row, K-block)
+ * of A and per 128x128 (N-block, K-block) of B.
  *
  * Arithmetic rules of this file:
  *  - INT8 accumulates in int64 and asserts the int32 range.
@@ -63,6 +72,7 @@
 static double g_e4m3[256];
 static double g_e2m1[16];
 static double g_ue8m0[256];
+static double g_ue4m3[256];
 static int g_tables_ready = 0;
 
 /* E4M3FN: bit 7 sign, bits 6..3 exponent (bias 7), bits 2..0 mantissa.
@@ -98,11 +108,23 @@ static double ue8m0_from_fields(unsigned code) {
   return ldexp(1.0, (int)code - 127);
 }
 
+/* UE4M3 (NVFP4 block scale): E4M3FN without the sign, so bit 7 is not part
+ * of the format.  Bits 6..3 exponent (bias 7), bits 2..0 mantissa, exponent
+ * field 0 subnormal, 0x7F NaN, 0x7E = 448 the largest.  Codes with bit 7
+ * set are outside the format and decode to NaN here. */
+static double ue4m3_from_fields(unsigned code) {
+  unsigned e = (code >> 3) & 15u, m = code & 7u;
+  if (code > 0x7Eu) return NAN;
+  if (e == 0u) return ldexp((double)m / 8.0, 1 - 7);
+  return ldexp(1.0 + (double)m / 8.0, (int)e - 7);
+}
+
 static void build_tables(void) {
   if (g_tables_ready) return;
   for (unsigned c = 0; c < 256u; ++c) g_e4m3[c] = e4m3_from_fields(c);
   for (unsigned c = 0; c < 16u; ++c) g_e2m1[c] = e2m1_from_fields(c);
   for (unsigned c = 0; c < 256u; ++c) g_ue8m0[c] = ue8m0_from_fields(c);
+  for (unsigned c = 0; c < 256u; ++c) g_ue4m3[c] = ue4m3_from_fields(c);
   g_tables_ready = 1;
 }
 
@@ -111,6 +133,7 @@ void qko_init(void) { build_tables(); }
 double qko_decode_e4m3(uint8_t code) { build_tables(); return g_e4m3[code]; }
 double qko_decode_e2m1(uint8_t nibble) { build_tables(); return g_e2m1[nibble & 15u]; }
 double qko_decode_ue8m0(uint8_t code) { build_tables(); return g_ue8m0[code]; }
+double qko_decode_ue4m3(uint8_t code) { build_tables(); return g_ue4m3[code]; }
 
 /* ------------------------------------------------------------------ */
 /* bf16                                                                */
@@ -332,6 +355,84 @@ int qko_gemm_mx(int fmt, const uint8_t* A, const uint8_t* sA, const uint8_t* B, 
           inner += mx_elem(fmt, a, k) * mx_elem(fmt, b, k);
         }
         acc += g_ue8m0[sA[m * kb + blk]] * g_ue8m0[sB[n * kb + blk]] * inner;
+      }
+      if (bias) acc += (double)qko_bf16_to_f32(bias[n]);
+      ref[(m - m0) * ldr + (n - n0)] = acc;
+    }
+  }
+  return QKO_OK;
+}
+
+/* ------------------------------------------------------------------ */
+/* NVFP4 block-scaled GEMM  [AITER6262] global scales                  */
+/* ------------------------------------------------------------------ */
+
+/* ref[(m-m0)*ldr + (n-n0)] =
+ *     ga * gb * sum_b ue4m3(sA[m,b]) * ue4m3(sB[n,b])
+ *                     * sum_{j<16} e2m1(A[m,16b+j]) * e2m1(B[n,16b+j])
+ *     (+ bias[n])
+ * in fp64.  A and B hold two E2M1 codes per byte (element 2i in the low
+ * nibble), K/2 bytes per row; sA [M, K/16] and sB [N, K/16] are raw
+ * row-major UE4M3 bytes; ga, gb are the per-tensor fp32 scales.  K must be a
+ * multiple of 16.  This is the value before bf16 rounding. */
+int qko_gemm_nvfp4(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const uint8_t* sB, float ga,
+                   float gb, const uint16_t* bias, double* ref, int64_t ldr, int64_t M, int64_t N, int64_t K,
+                   int64_t m0, int64_t m1, int64_t n0, int64_t n1) {
+  if (!A || !sA || !B || !sB || !ref || M < 0 || N < 0 || K < 0 || (K % 16) != 0) return QKO_ERR_ARG;
+  if (m0 < 0 || n0 < 0 || m1 > M || n1 > N || m0 > m1 || n0 > n1 || ldr < n1 - n0) return QKO_ERR_ARG;
+  build_tables();
+  const int64_t kb = K / 16;
+  const int64_t row_bytes = K / 2;
+#pragma omp parallel for collapse(2) schedule(static)
+  for (int64_t m = m0; m < m1; ++m) {
+    for (int64_t n = n0; n < n1; ++n) {
+      const uint8_t* a = A + m * row_bytes;
+      const uint8_t* b = B + n * row_bytes;
+      double acc = 0.0;
+      for (int64_t blk = 0; blk < kb; ++blk) {
+        double inner = 0.0;
+        for (int64_t j = 0; j < 16; ++j) {
+          int64_t k = blk * 16 + j;
+          inner += mx_elem(QKO_FMT_MXFP4_E2M1, a, k) * mx_elem(QKO_FMT_MXFP4_E2M1, b, k);
+        }
+        acc += g_ue4m3[sA[m * kb + blk]] * g_ue4m3[sB[n * kb + blk]] * inner;
+      }
+      acc *= (double)ga * (double)gb;
+      if (bias) acc += (double)qko_bf16_to_f32(bias[n]);
+      ref[(m - m0) * ldr + (n - n0)] = acc;
+    }
+  }
+  return QKO_OK;
+}
+
+/* ------------------------------------------------------------------ */
+/* FP8 blockscale GEMM  [MORI806-BS]                                   */
+/* ------------------------------------------------------------------ */
+
+/* ref[(m-m0)*ldr + (n-n0)] =
+ *     sum_g sa[m, g] * sb[n / 128, g] * sum_{k in K-block g} e4m3(A[m,k]) * e4m3(B[n,k])
+ *     (+ bias[n])
+ * in fp64, where K-block g covers k in [128 g, min(128 g + 128, K)).
+ * sa is [M, KB] and sb is [NB, KB] fp32, row-major, with KB = ceil(K/128)
+ * and NB = ceil(N/128).  This is the value before bf16 rounding. */
+int qko_gemm_fp8_blockscale(const uint8_t* A, const uint8_t* B, const float* sa, const float* sb,
+                            const uint16_t* bias, double* ref, int64_t ldr, int64_t M, int64_t N, int64_t K,
+                            int64_t m0, int64_t m1, int64_t n0, int64_t n1) {
+  if (!A || !B || !sa || !sb || !ref || M < 0 || N < 0 || K < 0) return QKO_ERR_ARG;
+  if (m0 < 0 || n0 < 0 || m1 > M || n1 > N || m0 > m1 || n0 > n1 || ldr < n1 - n0) return QKO_ERR_ARG;
+  build_tables();
+  const int64_t KB = (K + 127) / 128;
+#pragma omp parallel for collapse(2) schedule(static)
+  for (int64_t m = m0; m < m1; ++m) {
+    for (int64_t n = n0; n < n1; ++n) {
+      const uint8_t* a = A + m * K;
+      const uint8_t* b = B + n * K;
+      double acc = 0.0;
+      for (int64_t g = 0; g < KB; ++g) {
+        double inner = 0.0;
+        const int64_t k1 = (g + 1) * 128 < K ? (g + 1) * 128 : K;
+        for (int64_t k = g * 128; k < k1; ++k) inner += g_e4m3[a[k]] * g_e4m3[b[k]];
+        acc += (double)sa[m * KB + g] * (double)sb[(n / 128) * KB + g] * inner;
       }
       if (bias) acc += (double)qko_bf16_to_f32(bias[n]);
       ref[(m - m0) * ldr + (n - n0)] = acc;

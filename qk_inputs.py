@@ -16,6 +16,12 @@ Recipes (the model-projection shapes of the pages, with synthetic values):
 * MXFP4: A, B from bf16 N(0, 1), MX-quantized to packed E2M1 + UE8M0.
 * FP8 per-token x per-channel: A N(0, 1), W N(0, 0.02); per-row scale
   s = amax/448 (1 for an all-zero row), q = E4M3(x / s).
+* FP8 blockscale: A N(0, 1) with fp32 scales per 1x128 (row, K-block),
+  W N(0, 0.02) with fp32 scales per 128x128 block; s = amax/448 over the
+  group (1 for an all-zero group), q = E4M3(x / s).
+* NVFP4: A, B from bf16 N(0, 1); per-tensor fp32 scale g = amax/(448*6)
+  over the whole operand; per 16 K-elements a UE4M3 scale
+  s = E4M3((amax_block/6)/g) (saturating), elements E2M1(x/(s*g)).
 
 Every generator is a pure function of (shape, seed).  Each operand draws from
 its own stream, numpy default_rng([seed, tag]) with tag 0 = A, 1 = B, 2 = sa,
@@ -69,6 +75,14 @@ def encode_e4m3(q: np.ndarray) -> np.ndarray:
     sub_code = np.rint(a * np.float32(512.0)).astype(np.int32)        # multiples of 2^-9; 8 -> 2^-6
     code = np.where(a < np.float32(2.0 ** -6), sub_code, normal_code).astype(np.uint8)
     return code | sign
+
+
+def round_e4m3_value(a: np.ndarray) -> np.ndarray:
+    """The nearest E4M3FN value (ties to even) of non-negative float32 values, saturating at 448."""
+    a = np.minimum(np.asarray(a, np.float32), np.float32(448.0))
+    normal = _round_mantissa(a.copy(), 3).view(np.float32)
+    sub = (np.rint(a * np.float32(512.0)) / np.float32(512.0)).astype(np.float32)
+    return np.where(a < np.float32(2.0 ** -6), sub, normal).astype(np.float32)
 
 
 def encode_e2m1(q: np.ndarray) -> np.ndarray:
@@ -135,6 +149,49 @@ def ptpc_quantize(x: np.ndarray):
     return encode_e4m3(q), s
 
 
+def blockscale_quantize(x: np.ndarray, rows_per_block: int):
+    """E4M3 codes and fp32 scales per (rows_per_block x 128) group of [rows, K].
+
+    Scales are [ceil(rows/rows_per_block), ceil(K/128)]: s = amax/448 over the
+    group (1 for an all-zero group), q = E4M3(x / s) with x / s in fp32.
+    """
+    x = np.asarray(x, np.float32)
+    rows, K = x.shape
+    RB, KB = -(-rows // rows_per_block), -(-K // 128)
+    pad = np.zeros((RB * rows_per_block, KB * 128), np.float32)
+    pad[:rows, :K] = x
+    g = np.abs(pad.reshape(RB, rows_per_block, KB, 128)).max(axis=(1, 3))
+    s = (g / np.float32(448.0)).astype(np.float32)
+    s = np.where(g == 0, np.float32(1.0), s).astype(np.float32)
+    full = np.repeat(np.repeat(s, rows_per_block, axis=0), 128, axis=1)[:rows, :K]
+    q = (x / full).astype(np.float32)
+    return encode_e4m3(q), s
+
+
+def nvfp4_quantize(x: np.ndarray, global_scale: np.float32):
+    """NVFP4-quantize [rows, K] reals along K in blocks of 16 under a per-tensor scale.
+
+    Returns (packed E2M1 bytes [rows, K/2], UE4M3 scale bytes [rows, K/16]).
+    Block scale s = E4M3((amax/6)/g) saturating at 448; a block whose scale
+    rounds to zero gets zero elements; elements E2M1(x / (s*g)) in fp32.
+    """
+    x = np.asarray(x, np.float32)
+    rows, K = x.shape
+    if K % 16:
+        raise ValueError("K must be a multiple of 16")
+    g = np.float32(global_scale)
+    blk = x.reshape(rows, K // 16, 16)
+    amax = np.abs(blk).max(axis=2)
+    want = ((amax / np.float32(6.0)) / g).astype(np.float32)
+    sval = round_e4m3_value(want)
+    scodes = encode_e4m3(sval)
+    denom = (sval * g).astype(np.float32)
+    safe = np.where(denom > 0, denom, np.float32(1.0)).astype(np.float32)
+    q = (blk / safe[:, :, None]).astype(np.float32)
+    q = np.where((denom > 0)[:, :, None], q, np.float32(0.0)).reshape(rows, K)
+    return pack_e2m1(encode_e2m1(q)), scodes
+
+
 # ----------------------------------------------------------------------------
 # workloads
 # ----------------------------------------------------------------------------
@@ -170,6 +227,32 @@ class MxProblem:
     sA: np.ndarray     # ue8m0 [M, K/32]
     B: np.ndarray
     sB: np.ndarray
+    bias: np.ndarray | None
+    M: int
+    N: int
+    K: int
+
+
+@dataclass
+class BlockscaleProblem:
+    A: np.ndarray      # e4m3 bytes [M, K]
+    B: np.ndarray      # e4m3 bytes [N, K]
+    sa: np.ndarray     # fp32 [M, ceil(K/128)]
+    sb: np.ndarray     # fp32 [ceil(N/128), ceil(K/128)]
+    bias: np.ndarray | None
+    M: int
+    N: int
+    K: int
+
+
+@dataclass
+class Nvfp4Problem:
+    A: np.ndarray      # packed e2m1 [M, K/2]
+    sA: np.ndarray     # ue4m3 [M, K/16]
+    B: np.ndarray
+    sB: np.ndarray
+    global_a: float    # per-tensor fp32 scales
+    global_b: float
     bias: np.ndarray | None
     M: int
     N: int
@@ -273,3 +356,40 @@ def sample_tiles(M: int, N: int, count: int, seed: int, tile: int = 128):
     for bm, bn in sorted(picks):
         out.append((bm * tile, min(M, bm * tile + tile), bn * tile, min(N, bn * tile + tile)))
     return out
+
+
+def blockscale_operand(rows: int, K: int, seed: int, tag: int):
+    """(E4M3 bytes, fp32 scales) of one blockscale operand: A ~ N(0,1) per 1x128, W ~ N(0,0.02) per 128x128."""
+    rng = _rng(seed, tag)
+    rpb = 1 if tag == TAG_A else 128
+    parts = _normal_rows(rng, rows, K, 1.0 if tag == TAG_A else 0.02, lambda x: blockscale_quantize(x, rpb))
+    KB = -(-K // 128)
+    return _cat(parts, 0, (0, K), np.uint8), _cat(parts, 1, (0, KB), np.float32).astype(np.float32)
+
+
+def blockscale_problem(M: int, N: int, K: int, seed: int = 0, bias: bool = False) -> BlockscaleProblem:
+    A, sa = blockscale_operand(M, K, seed, TAG_A)
+    B, sb = blockscale_operand(N, K, seed, TAG_B)
+    return BlockscaleProblem(A, B, sa, sb, bias_bits(N, seed) if bias else None, M, N, K)
+
+
+def nvfp4_operand(rows: int, K: int, seed: int, tag: int):
+    """(packed E2M1, UE4M3 scales, per-tensor scale) of one NVFP4 operand from bf16 N(0, 1).
+
+    Two passes over the same seeded stream: the first finds the operand's
+    amax for the per-tensor scale amax/(448*6), the second quantizes.
+    """
+    def bf16(x):
+        return from_bf16_bits(to_bf16_bits(x))
+
+    amax = max([float(np.abs(bf16(x)).max()) for x in _normal_rows(_rng(seed, tag), rows, K, 1.0, lambda x: x)]
+               or [0.0])
+    g = np.float32(amax) / np.float32(448.0 * 6.0) if amax > 0 else np.float32(1.0)
+    parts = _normal_rows(_rng(seed, tag), rows, K, 1.0, lambda x: nvfp4_quantize(bf16(x), g))
+    return (_cat(parts, 0, (0, K // 2), np.uint8), _cat(parts, 1, (0, K // 16), np.uint8), float(g))
+
+
+def nvfp4_problem(M: int, N: int, K: int, seed: int = 0, bias: bool = False) -> Nvfp4Problem:
+    A, sA, ga = nvfp4_operand(M, K, seed, TAG_A)
+    B, sB, gb = nvfp4_operand(N, K, seed, TAG_B)
+    return Nvfp4Problem(A, sA, B, sB, ga, gb, bias_bits(N, seed) if bias else None, M, N, K)

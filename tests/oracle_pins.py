@@ -20,7 +20,16 @@ What each pin rests on:
   exact power-of-two scale invariance;
 * the MX block structure against closed forms (constant elements with
   per-block scale codes), the exact doubling when every scale code of A
-  grows by one, and a numpy float64 matmul of independently decoded values.
+  grows by one, and a numpy float64 matmul of independently decoded values;
+* NVFP4 (UE4M3 scales per 16 elements, per-tensor scales): the UE4M3 anchor
+  values and PyTorch's float8_e4m3fn cast, a closed form over the 16-element
+  blocks, a numpy matmul of independently decoded values, and the exact
+  reduction to MXFP4 when the scales are powers of two shared by each pair
+  of 16-blocks;
+* FP8 blockscale (fp32 scales per 1x128 of A and 128x128 of B): a closed
+  form over ragged K- and N-blocks, a numpy matmul of the blocks, and the
+  reduction to the per-token x per-channel GEMM when the scales do not vary
+  along K.
 """
 from __future__ import annotations
 
@@ -380,10 +389,137 @@ def check_mx_vs_numpy(lib):
     assert ref[0, 0] == 0.5
 
 
+# ---------------------------------------------------------------- NVFP4
+
+def check_ue4m3_decode(lib):
+    d = oracle.decode_ue4m3(np.arange(256), lib)
+    assert d[0x38] == 1.0 and d[0x7E] == 448.0
+    assert d[0x08] == 2.0 ** -6 and d[0x01] == 2.0 ** -9 and d[0x00] == 0.0
+    assert np.isnan(d[0x7F]) and np.all(np.isnan(d[0x80:]))   # bit 7 is not part of the format
+    assert np.array_equal(d[:0x7F], _torch_e4m3(np.arange(0x7F)))
+    assert np.all(np.diff(d[:0x7F]) > 0)
+
+
+def _nvfp4_ones(M, N, K):
+    return np.full((M, K // 2), 0x22, np.uint8), np.full((N, K // 2), 0x22, np.uint8)   # E2M1 1.0 everywhere
+
+
+def check_nvfp4_block_structure(lib):
+    M, N, K = 3, 5, 128
+    A, B = _nvfp4_ones(M, N, K)
+    nb = K // 16
+    rng = np.random.default_rng(17)
+    sA = rng.integers(0x08, 0x7F, (M, nb)).astype(np.uint8)    # normal UE4M3 codes, varied mantissas
+    sB = rng.integers(0x01, 0x7F, (N, nb)).astype(np.uint8)
+    ga, gb = np.float32(0.75), np.float32(3.0)
+    ref = oracle.gemm_nvfp4(A, sA, B, sB, ga, gb, lib=lib)
+    dA, dB = _torch_e4m3(sA), _torch_e4m3(sB)
+    expect = np.zeros((M, N))
+    for m in range(M):
+        for n in range(N):
+            expect[m, n] = sum(16.0 * dA[m, b] * dB[n, b] for b in range(nb)) * 0.75 * 3.0
+    assert np.allclose(ref, expect, rtol=1e-15, atol=0)
+
+
+def _e2m1_values(packed):
+    codes = qk_inputs.unpack_e2m1(packed)
+    v = np.asarray(E2M1_OCP_VALUES * 2)[codes]
+    return np.where(codes >= 8, -v, v)
+
+
+def check_nvfp4_vs_numpy(lib):
+    p = qk_inputs.nvfp4_problem(10, 14, 192, seed=8, bias=True)
+    ref = oracle.gemm_nvfp4(p.A, p.sA, p.B, p.sB, p.global_a, p.global_b, bias=p.bias, lib=lib)
+    a = _e2m1_values(p.A) * np.repeat(_torch_e4m3(p.sA), 16, axis=1)
+    b = _e2m1_values(p.B) * np.repeat(_torch_e4m3(p.sB), 16, axis=1)
+    expect = (a @ b.T) * float(np.float32(p.global_a)) * float(np.float32(p.global_b)) \
+        + qk_inputs.from_bf16_bits(p.bias).astype(np.float64)[None, :]
+    assert np.allclose(ref, expect, rtol=1e-13, atol=1e-13)
+    sub = oracle.gemm_nvfp4(p.A, p.sA, p.B, p.sB, p.global_a, p.global_b, bias=p.bias, m0=3, m1=9, n0=2, n1=11,
+                            lib=lib)
+    assert np.array_equal(sub, ref[3:9, 2:11])
+
+
+def check_nvfp4_reduces_to_mxfp4(lib):
+    # power-of-two UE4M3 scales (mantissa 0), equal over each pair of 16-blocks,
+    # with unit per-tensor scales: the same real numbers as MXFP4 with UE8M0
+    rng = np.random.default_rng(23)
+    M, N, K = 6, 9, 256
+    A = rng.integers(0, 256, (M, K // 2), dtype=np.uint8)
+    B = rng.integers(0, 256, (N, K // 2), dtype=np.uint8)
+    ea = rng.integers(-6, 9, (M, K // 32))
+    eb = rng.integers(-6, 9, (N, K // 32))
+    to_ue4m3 = lambda e: ((e + 7) << 3).astype(np.uint8)             # 2^e, e in [-6, 8]
+    sA16 = np.repeat(to_ue4m3(ea), 2, axis=1)
+    sB16 = np.repeat(to_ue4m3(eb), 2, axis=1)
+    nv = oracle.gemm_nvfp4(A, sA16, B, sB16, 1.0, 1.0, lib=lib)
+    mx = oracle.gemm_mx(oracle.FMT_MXFP4_E2M1, A, (ea + 127).astype(np.uint8), B, (eb + 127).astype(np.uint8),
+                        lib=lib)
+    assert np.array_equal(nv, mx)
+
+
+# ---------------------------------------------------------------- FP8 blockscale
+
+def check_blockscale_block_structure(lib):
+    M, N, K = 3, 300, 300             # ragged: K-blocks of 128, 128, 44; N-blocks of 128, 128, 44
+    A = np.full((M, K), 0x38, np.uint8)
+    B = np.full((N, K), 0x38, np.uint8)
+    KB, NB = 3, 3
+    sa = np.array([[2.0 ** g * (m + 1) for g in range(KB)] for m in range(M)], np.float32)
+    sb = np.array([[(nb + 1) * (1 if g != 1 else 0.5) for g in range(KB)] for nb in range(NB)], np.float32)
+    ref = oracle.gemm_fp8_blockscale(A, B, sa, sb, lib=lib)
+    lens = [128, 128, 44]
+    expect = np.zeros((M, N))
+    for m in range(M):
+        for n in range(N):
+            expect[m, n] = sum(lens[g] * 2.0 ** g * (m + 1) * (n // 128 + 1) * (1 if g != 1 else 0.5)
+                               for g in range(KB))
+    assert np.array_equal(ref, expect)
+
+
+def check_blockscale_vs_numpy(lib):
+    rng = np.random.default_rng(37)
+    M, N, K = 7, 140, 272
+    A = rng.integers(0, 256, (M, K), dtype=np.uint8)
+    B = rng.integers(0, 256, (N, K), dtype=np.uint8)
+    A[(A & 0x7F) == 0x7F] = 0x19
+    B[(B & 0x7F) == 0x7F] = 0x2A
+    KB, NB = 3, 2
+    sa = rng.uniform(0.5, 2, (M, KB)).astype(np.float32)
+    sb = rng.uniform(0.5, 2, (NB, KB)).astype(np.float32)
+    bias = qk_inputs.to_bf16_bits(rng.standard_normal(N).astype(np.float32))
+    ref = oracle.gemm_fp8_blockscale(A, B, sa, sb, bias=bias, lib=lib)
+    a, b = _torch_e4m3(A), _torch_e4m3(B)
+    expect = qk_inputs.from_bf16_bits(bias).astype(np.float64)[None, :].repeat(M, 0)
+    for g in range(KB):
+        ks = slice(128 * g, min(128 * g + 128, K))
+        part = a[:, ks] @ b[:, ks].T
+        expect = expect + part * sa[:, g].astype(np.float64)[:, None] \
+            * np.repeat(sb[:, g].astype(np.float64), 128)[None, :N]
+    # random E4M3 codes reach 448, so sums reach 1e6: compare at fp64 precision of that scale
+    assert np.allclose(ref, expect, rtol=1e-14, atol=1e-14 * np.abs(expect).max())
+    sub = oracle.gemm_fp8_blockscale(A, B, sa, sb, bias=bias, m0=1, m1=6, n0=100, n1=140, lib=lib)
+    assert np.array_equal(sub, ref[1:6, 100:140])
+
+
+def check_blockscale_reduces_to_ptpc(lib):
+    p = qk_inputs.fp8_problem(9, 260, 384, seed=5)
+    c = np.float32(0.013)
+    KB = 3
+    sa = np.repeat(p.sa[:, None], KB, axis=1)
+    sb = np.full((3, KB), c, np.float32)
+    bs = oracle.gemm_fp8_blockscale(p.A, p.B, sa, sb, lib=lib)
+    pt = oracle.gemm_fp8_rowwise(p.A, p.B, p.sa, np.full(p.N, c, np.float32), lib=lib)
+    # the same real number up to fp64 rounding (scaled per block vs once at the end)
+    assert np.allclose(bs, pt, rtol=1e-13, atol=1e-14 * np.abs(pt).max())
+
+
 ALL_CHECKS = [
     check_e4m3_decode, check_e2m1_decode, check_ue8m0_decode, check_bf16_rne, check_encoders,
     check_mx_quantize_block, check_ptpc_quantize, check_int8_acc_vs_numpy, check_int8_hand_examples,
     check_int8_identity_and_extremes, check_int8_epilogue_order, check_int8_signed_zero,
     check_int8_pow2_invariance, check_fp8_vs_numpy, check_mx_block_structure,
-    check_mx_scale_doubling, check_mx_vs_numpy,
+    check_mx_scale_doubling, check_mx_vs_numpy, check_ue4m3_decode, check_nvfp4_block_structure,
+    check_nvfp4_vs_numpy, check_nvfp4_reduces_to_mxfp4, check_blockscale_block_structure,
+    check_blockscale_vs_numpy, check_blockscale_reduces_to_ptpc,
 ]

@@ -42,6 +42,16 @@ MUTANTS = {
     "ptpc_scale_divisor": ("float s = amax / 448.0f;", "float s = amax / 240.0f;"),
     "ptpc_zero_row_scale": ("if (amax == 0.0f) s = 1.0f;", "if (amax == 0.0f) s = 0.5f;"),
     "mx_emax": ("int emax = (fmt == QKO_FMT_MXFP8_E4M3) ? 8 : 2;", "int emax = (fmt == QKO_FMT_MXFP8_E4M3) ? 7 : 2;"),
+    "ue4m3_exponent_bias": ("return ldexp(1.0 + (double)m / 8.0, (int)e - 7);",
+                            "return ldexp(1.0 + (double)m / 8.0, (int)e - 6);"),
+    "nvfp4_blocks_of_32": ("const int64_t kb = K / 16;", "const int64_t kb = K / 32;"),
+    "nvfp4_global_b_dropped": ("acc *= (double)ga * (double)gb;", "acc *= (double)ga;"),
+    "nvfp4_scales_read_as_ue8m0": ("acc += g_ue4m3[sA[m * kb + blk]] * g_ue4m3[sB[n * kb + blk]] * inner;",
+                                   "acc += g_ue8m0[sA[m * kb + blk]] * g_ue4m3[sB[n * kb + blk]] * inner;"),
+    "blockscale_b_block_index_dropped": ("(double)sb[(n / 128) * KB + g]", "(double)sb[g]"),
+    "blockscale_a_block_index_dropped": ("(double)sa[m * KB + g]", "(double)sa[m * KB]"),
+    "blockscale_bias_dropped": ("if (bias) acc += (double)qko_bf16_to_f32(bias[n]);\n      ref[(m - m0) * ldr + (n - n0)] = acc;\n    }\n  }\n  return QKO_OK;\n}\n\n/* Number",
+                                "(void)bias;\n      ref[(m - m0) * ldr + (n - n0)] = acc;\n    }\n  }\n  return QKO_OK;\n}\n\n/* Number"),
 }
 
 
