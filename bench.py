@@ -14,7 +14,7 @@ a device synchronize on both sides, CUDA events on the launching stream, the
 maximum over ranks.  The inputs (277 MB of int8 operands, 553 MB of f16
 copies, 1.29 GB of output) are larger than the 129 MB L2, so no flush is
 needed between headline steps; the secondary workloads, some of which fit in
-L2, flush it before every timed call.
+L2, flush it before every timed call by reading a 256 MB buffer.
 
 --impl reference times the CPU oracle on a bounded sample of the same
 workload (the reference arm of this build: the pages hold no runnable code).
@@ -253,44 +253,65 @@ def time_headline(qk, p, steps, warmup, dev, dist, sampler):
 
 
 def time_e2e(qk, p, steps, dev):
-    """The same calls through host buffers: pinned H2D of the inputs and D2H of the result inside the timed region."""
+    """The same calls through host buffers: each step copies its inputs from pinned host memory and
+    its result back to pinned host memory inside the timed region.  Three streams overlap step i's
+    GEMM with step i+1's input copies and step i-1's output copy (device buffers double-buffered)."""
     import numpy as np
     import torch
     pin = lambda x: torch.from_numpy(np.ascontiguousarray(x)).pin_memory()
     hA, hB, hsa, hsb = pin(p.A), pin(p.B), pin(p.sa), pin(p.sb)
     hbias = None if p.bias is None else pin(p.bias.view(np.int16)).view(torch.bfloat16)
-    hout = torch.empty((p.M, p.N), dtype=torch.bfloat16).pin_memory()
-    A = torch.empty_like(hA, device=dev)
-    B = torch.empty_like(hB, device=dev)
-    sa = torch.empty_like(hsa, device=dev)
-    sb = torch.empty_like(hsb, device=dev)
-    bias = None if hbias is None else torch.empty_like(hbias, device=dev)
-    out = torch.empty((p.M, p.N), dtype=torch.bfloat16, device=dev)
+    hout = [torch.empty((p.M, p.N), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    dA = [torch.empty_like(hA, device=dev) for _ in range(2)]
+    dB = [torch.empty_like(hB, device=dev) for _ in range(2)]
+    dsa = [torch.empty_like(hsa, device=dev) for _ in range(2)]
+    dsb = [torch.empty_like(hsb, device=dev) for _ in range(2)]
+    dbias = [None if hbias is None else torch.empty_like(hbias, device=dev) for _ in range(2)]
+    dout = [torch.empty((p.M, p.N), dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    s_in, s_comp, s_out = (torch.cuda.Stream(dev) for _ in range(3))
+    ev = lambda: torch.cuda.Event()
 
-    def step():
-        A.copy_(hA, non_blocking=True)
-        B.copy_(hB, non_blocking=True)
-        sa.copy_(hsa, non_blocking=True)
-        sb.copy_(hsb, non_blocking=True)
-        if bias is not None:
-            bias.copy_(hbias, non_blocking=True)
-        qk.gemm_int8_rowwise(A, B, sa, sb, bias, out)
-        hout.copy_(out, non_blocking=True)
+    def run(n):
+        in_done, comp_done, out_done = [], [], []
+        for i in range(n):
+            b = i % 2
+            with torch.cuda.stream(s_in):
+                if i >= 2:
+                    s_in.wait_event(comp_done[i - 2])      # buffer b's inputs consumed by GEMM i-2
+                dA[b].copy_(hA, non_blocking=True)
+                dB[b].copy_(hB, non_blocking=True)
+                dsa[b].copy_(hsa, non_blocking=True)
+                dsb[b].copy_(hsb, non_blocking=True)
+                if hbias is not None:
+                    dbias[b].copy_(hbias, non_blocking=True)
+                e = ev(); e.record(s_in); in_done.append(e)
+            with torch.cuda.stream(s_comp):
+                s_comp.wait_event(in_done[i])
+                if i >= 2:
+                    s_comp.wait_event(out_done[i - 2])     # output b read back by step i-2
+                qk.gemm_int8_rowwise(dA[b], dB[b], dsa[b], dsb[b], dbias[b], dout[b])
+                e = ev(); e.record(s_comp); comp_done.append(e)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(comp_done[i])
+                hout[b].copy_(dout[b], non_blocking=True)
+                e = ev(); e.record(s_out); out_done.append(e)
+        return out_done
 
-    step()
+    run(2)
     torch.cuda.synchronize(dev)
-    stream = torch.cuda.current_stream(dev)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(steps):
-        step()
-    e1.record(stream)
+    e0.record(s_in)
+    s_comp.wait_event(e0)
+    s_out.wait_event(e0)
+    out_done = run(steps)
+    s_out.wait_event(out_done[-1])
+    e1.record(s_out)
     torch.cuda.synchronize(dev)
     h2d = hA.numel() + hB.numel() + 4 * (hsa.numel() + hsb.numel()) + (0 if hbias is None else 2 * hbias.numel())
-    d2h = 2 * hout.numel()
+    d2h = 2 * hout[0].numel()
     ms = e0.elapsed_time(e1)
-    del A, B, sa, sb, bias, out, hA, hB, hout
+    del dA, dB, dsa, dsb, dbias, dout, hA, hB, hout
     torch.cuda.empty_cache()
     return ms, h2d, d2h
 
@@ -307,7 +328,9 @@ def time_calls(fn, iters, warmup, dev, flush):
     qk.profile_read(reset=True)
     qk.profile_enable(True)
     for _ in range(iters):
-        flush.zero_()
+        # read (not write) twice the L2's size: the timed call starts cold, with no
+        # dirty lines of the flush left in L2 for its own loads to write back
+        flush.sum(dtype=torch.int32)
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
@@ -322,18 +345,23 @@ def time_calls(fn, iters, warmup, dev, flush):
 
 def secondary_formats(qk, dev, peaks, which):
     """Other formats and shapes of the configurations, one line each (median of flushed calls)."""
+    import numpy as np
     import torch
     import qk_inputs as qi
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
     if which == "none":
         return []
     cases = [("mxfp8", (16384, 7168, 2048)), ("mxfp8", (32768, 7168, 1792)),
-             ("mxfp4", (8192, 8192, 16384)),
-             ("fp8_ptpc", (64, 2112, 7168)), ("fp8_ptpc", (16384, 7168, 1792)),
+             ("mxfp4", (8192, 8192, 16384)), ("nvfp4", (8192, 8192, 16384)),
+             ("fp8_blockscale", (16384, 7168, 2048)),
+             ("fp8_ptpc", (64, 2112, 7168)), ("fp8_ptpc", (64, 21504, 5376)), ("fp8_ptpc", (16384, 7168, 1792)),
+             ("fp8_ptpc", (32768, 7168, 1792)),
              ("int8_bias", (30000, 21504, 5376))]
     if which == "full":
         cases += [("mxfp4", (8192, 8192, 8192)), ("mxfp4", (16384, 16384, 8192)), ("mxfp4", (16384, 16384, 16384)),
-                  ("fp8_ptpc", (1024, 7168, 1792)), ("fp8_ptpc", (30000, 21504, 5376)), ("fp8_ptpc", (64, 21504, 5376))]
+                  ("fp8_ptpc", (1024, 7168, 1792)), ("fp8_ptpc", (30000, 21504, 5376)), ("fp8_ptpc", (64, 21504, 5376)),
+                  ("nvfp4", (16384, 16384, 16384)), ("fp8_blockscale", (32768, 7168, 1792)),
+                  ("fp8_blockscale", (30000, 21504, 5376))]
     results = []
     for kind, (M, N, K) in cases:
         t_gen = time.time()
@@ -346,6 +374,22 @@ def secondary_formats(qk, dev, peaks, which):
             dtype = "fp8" if kind == "mxfp8" else "fp4"
             kname = "gemm_mxfp8" if kind == "mxfp8" else "gemm_mxfp4"
             in_bytes = A.numel() + B.numel() + sA.numel() + sB.numel()
+        elif kind == "nvfp4":
+            p = qi.nvfp4_problem(M, N, K, seed=0)
+            A, sA, B, sB = (_to_dev(x, dev) for x in (p.A, p.sA, p.B, p.sB))
+            ga = _to_dev(np.array([p.global_a], np.float32), dev)
+            gb = _to_dev(np.array([p.global_b], np.float32), dev)
+            out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+            fn = lambda: qk.gemm_nvfp4(A, sA, B, sB, ga, gb, None, out)
+            dtype, kname = "fp4", "gemm_nvfp4"
+            in_bytes = A.numel() + B.numel() + sA.numel() + sB.numel() + 8
+        elif kind == "fp8_blockscale":
+            p = qi.blockscale_problem(M, N, K, seed=0)
+            A, B, sa, sb = (_to_dev(x, dev) for x in (p.A, p.B, p.sa, p.sb))
+            out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+            fn = lambda: qk.gemm_fp8_blockscale(A, B, sa, sb, None, out)
+            dtype, kname = "fp8", "gemm_fp8_blockscale"
+            in_bytes = A.numel() + B.numel() + 4 * (sa.numel() + sb.numel())
         elif kind == "fp8_ptpc":
             p = qi.fp8_problem(M, N, K, seed=0)
             A, B, sa, sb = (_to_dev(x, dev) for x in (p.A, p.B, p.sa, p.sb))
@@ -378,6 +422,23 @@ def secondary_formats(qk, dev, peaks, which):
         })
         del A, B, out
         torch.cuda.empty_cache()
+    # the quantizers that feed the GEMMs (bandwidth-bound: bf16 in, codes + scales out)
+    rows, K = 16384, 7168
+    rng = np.random.default_rng(0)
+    xb = torch.from_numpy(qi.to_bf16_bits(rng.standard_normal((rows, K), dtype=np.float32)).view(np.int16))
+    xb = xb.to(dev).view(torch.bfloat16)
+    for name, fn, out_bytes in (
+            ("quantize_mxfp8", lambda: qk.quantize_mx(qi.FMT_MXFP8_E4M3, xb), rows * K + rows * K // 32),
+            ("quantize_mxfp4", lambda: qk.quantize_mx(qi.FMT_MXFP4_E2M1, xb), rows * K // 2 + rows * K // 32),
+            ("quantize_ptpc", lambda: qk.quantize_ptpc(xb), rows * K + 4 * rows)):
+        ms, kstats = time_calls(fn, 10, 3, dev, flush)
+        klaunch, kms = kstats.get("quantize", (1, ms))
+        kavg = kms / max(klaunch, 1)
+        alg = 2 * rows * K + out_bytes
+        results.append({"format": name, "M": rows, "K": K, "ms": round(ms, 4), "kernel_ms": round(kavg, 4),
+                        "kernel_gbs": round(alg / kavg / 1e6, 1), "frac_of_hbm": round(alg / kavg / 1e6 / peaks["hbm_gbs"], 4)})
+    del xb
+    torch.cuda.empty_cache()
     return results
 
 
@@ -550,7 +611,8 @@ def main(argv=None):
             "gpu_launches": int(launches),
             "roofline": {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
                          "frac": round(achieved / peak, 4) if peak else None, "traffic": traffic,
-                         "kernel": "qk_gemm_kernel<F16, 128x128> (exact INT8 on the f16 pipe)",
+                         "kernel": "qk_gemm_kernel, exact INT8 on the f16 pipe: 256x256 tiles on 2-SM CTA pairs, "
+                                   "two TMEM accumulators, int32 sums in registers, bulk-store epilogue",
                          "peak_source": f"{peak_src} {'sustained' if sustained else 'burst'} bf16 (f16 rate)",
                          "kernel_ms": round(gavg, 4)},
             "secondary_kernel": {"name": "int8_to_f16", "ms": round(wavg, 4),

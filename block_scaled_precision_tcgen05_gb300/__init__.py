@@ -40,6 +40,8 @@ EXPORTS = (
     "qk_gemm_int8_rowwise_noalloc",
     "qk_gemm_mx",
     "qk_gemm_fp8_rowwise",
+    "qk_gemm_nvfp4",
+    "qk_gemm_fp8_blockscale",
     "qk_quantize_mx",
     "qk_quantize_ptpc",
     "qk_status_string",
@@ -79,6 +81,10 @@ def _declare(lib):
     lib.qk_gemm_fp8_rowwise.restype = c.c_int
     lib.qk_gemm_mx.argtypes = [c.c_int, P, P, P, P, P, P, i64, i64, i64, P]
     lib.qk_gemm_mx.restype = c.c_int
+    lib.qk_gemm_nvfp4.argtypes = [P, P, P, P, P, P, P, P, i64, i64, i64, P]
+    lib.qk_gemm_nvfp4.restype = c.c_int
+    lib.qk_gemm_fp8_blockscale.argtypes = [P, P, P, P, P, P, i64, i64, i64, P]
+    lib.qk_gemm_fp8_blockscale.restype = c.c_int
     lib.qk_quantize_mx.argtypes = [c.c_int, P, P, P, i64, i64, P]
     lib.qk_quantize_mx.restype = c.c_int
     lib.qk_quantize_ptpc.argtypes = [P, P, P, i64, i64, P]
@@ -247,6 +253,52 @@ def gemm_mx(fmt, A, sA, B, sB, bias=None, out=None):
     out = _out(out, M, N, dev)
     check(load_library().qk_gemm_mx(int(fmt), _ptr(A), _ptr(sA), _ptr(B), _ptr(sB), _ptr(bias), _ptr(out),
                                     M, N, K, _stream_handle(dev)))
+    return out
+
+
+def gemm_fp8_blockscale(A, B, sa, sb, bias=None, out=None):
+    """FP8 E4M3 GEMM with fp32 block scales: sa [M, ceil(K/128)], sb [ceil(N/128), ceil(K/128)]."""
+    import torch
+    M, K = A.shape
+    N = B.shape[0]
+    dev = A.device
+    if dev.type != "cuda":
+        raise ValueError("operands must be CUDA tensors")
+    KB, NB = -(-K // 128), -(-N // 128)
+    _expect(A, "A", torch.uint8, (M, K), dev)
+    _expect(B, "B", torch.uint8, (N, K), dev)
+    _expect(sa, "sa", torch.float32, (M, KB), dev)
+    _expect(sb, "sb", torch.float32, (NB, KB), dev)
+    if bias is not None:
+        _expect(bias, "bias", torch.bfloat16, (N,), dev)
+    out = _out(out, M, N, dev)
+    check(load_library().qk_gemm_fp8_blockscale(_ptr(A), _ptr(B), _ptr(sa), _ptr(sb), _ptr(bias), _ptr(out), M, N, K,
+                                                _stream_handle(dev)))
+    return out
+
+
+def gemm_nvfp4(A, sA, B, sB, global_a=None, global_b=None, bias=None, out=None):
+    """NVFP4 GEMM.  A [M, K/2], B [N, K/2] packed E2M1 bytes; sA [M, K/16], sB [N, K/16] raw UE4M3
+    bytes; global_a / global_b optional one-element fp32 CUDA tensors (per-tensor scales)."""
+    import torch
+    M, kbytes = A.shape
+    N = B.shape[0]
+    K = 2 * kbytes
+    dev = A.device
+    if dev.type != "cuda":
+        raise ValueError("operands must be CUDA tensors")
+    _expect(A, "A", torch.uint8, (M, kbytes), dev)
+    _expect(B, "B", torch.uint8, (N, kbytes), dev)
+    _expect(sA, "sA", torch.uint8, (M, K // 16), dev)
+    _expect(sB, "sB", torch.uint8, (N, K // 16), dev)
+    for name, g in (("global_a", global_a), ("global_b", global_b)):
+        if g is not None:
+            _expect(g, name, torch.float32, (1,), dev)
+    if bias is not None:
+        _expect(bias, "bias", torch.bfloat16, (N,), dev)
+    out = _out(out, M, N, dev)
+    check(load_library().qk_gemm_nvfp4(_ptr(A), _ptr(sA), _ptr(B), _ptr(sB), _ptr(global_a), _ptr(global_b),
+                                       _ptr(bias), _ptr(out), M, N, K, _stream_handle(dev)))
     return out
 
 

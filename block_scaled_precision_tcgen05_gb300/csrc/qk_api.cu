@@ -49,8 +49,9 @@ void count_launches(uint64_t n) { g_launches.fetch_add(n, std::memory_order_rela
 
 namespace {
 
-const char* const kKernelNames[kKNumKinds] = {"int8_to_f16", "gemm_int8_f16", "gemm_fp8", "gemm_mxfp8",
-                                              "gemm_mxfp4",  "wait_probe",    "quantize"};
+const char* const kKernelNames[kKNumKinds] = {"int8_to_f16", "gemm_int8_f16", "gemm_fp8",
+                                              "gemm_mxfp8",  "gemm_mxfp4",    "wait_probe",
+                                              "quantize",    "gemm_nvfp4",    "gemm_fp8_blockscale"};
 
 struct PendingTiming {
   int kind;

@@ -28,6 +28,7 @@ enum : uint32_t {
   kSiteDrain = 6,
   kSiteProducerDrain = 7,
   kSiteProbe = 8,
+  kSitePeerPartial = 9,  // stream-K: another CTA's partial of a shared tile
 };
 
 __device__ __forceinline__ void report_error(unsigned long long* err, uint32_t code, uint32_t site,
@@ -356,6 +357,19 @@ __device__ __forceinline__ void umma_mxf4(uint32_t d_tmem, uint64_t a_desc, uint
       : "memory");
 }
 
+// NVFP4: E2M1 x E2M1 with one UE4M3 scale per 16 K-elements (four per row
+// per MMA of K = 64).
+__device__ __forceinline__ void umma_nvf4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
+      : "memory");
+}
+
 // CTA-pair block-scaled MMAs (leader only); scale factors at the same TMEM
 // addresses in both CTAs.
 __device__ __forceinline__ void umma_mxf8f6f4_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
@@ -495,12 +509,14 @@ __host__ __device__ constexpr uint32_t make_idesc_dense(uint32_t d_fmt, uint32_t
 }
 
 // Instruction descriptor for the block-scaled kinds: B scale-factor byte
-// selector (bits 4..5), A and B formats, N>>3, scale type (bit 23, 1 =
-// UE8M0), M>>4, A scale-factor byte selector (bits 29..30).  D is fp32.
+// selector (bits 4..5), A and B formats, N>>3, scale type (bit 23: 1 =
+// UE8M0, 0 = UE4M3), M>>4, A scale-factor byte selector (bits 29..30).  D is
+// fp32.
 __host__ __device__ constexpr uint32_t make_idesc_block_scaled(uint32_t a_fmt, uint32_t b_fmt, int m, int n,
-                                                               uint32_t a_sf_id, uint32_t b_sf_id) {
+                                                               uint32_t a_sf_id, uint32_t b_sf_id,
+                                                               bool sf_ue8m0 = true) {
   return ((b_sf_id & 3u) << 4) | (a_fmt << 7) | (b_fmt << 10) | (static_cast<uint32_t>(n >> 3) << 17) |
-         (1u << 23) | (static_cast<uint32_t>(m >> 4) << 24) | ((a_sf_id & 3u) << 29);
+         ((sf_ue8m0 ? 1u : 0u) << 23) | (static_cast<uint32_t>(m >> 4) << 24) | ((a_sf_id & 3u) << 29);
 }
 
 }  // namespace qk

@@ -2,7 +2,10 @@
 // (ROCm/aiter PR #6262 gemm_a8w8_bpreshuffle semantics; ROCm/mori PR #806
 // "ptpc"), on tcgen05.mma kind::f8f6f4 with fp32 accumulation in TMEM.
 #include "qk_launch.cuh"
+#include <atomic>
+
 #include "qk_skinny_kernel.cuh"
+#include "qk_streamk_kernel.cuh"
 
 namespace qk {
 
@@ -30,7 +33,9 @@ static int launch_fp8_cfg(const uint8_t* A, const uint8_t* B, const float* sa, c
   return launch_gemm<C>(ta, tb, ta, tb, p, dev, stream);
 }
 
-// Few rows (M <= 128): split-K, weight-streaming kernel (qk_skinny_kernel.cuh).
+// Few rows, few weight tiles: split-K over a cluster of S CTAs with a DSMEM
+// reduction (qk_skinny_kernel.cuh), used when every tile's cluster fits on
+// the GPU at once.
 template <int MT, int S>
 static int launch_skinny_cfg(const uint8_t* A, const uint8_t* B, const float* sa, const float* sb,
                              const uint16_t* bias, uint16_t* out, int M, int N, int K, const DeviceInfo& dev,
@@ -52,13 +57,18 @@ static int launch_skinny_cfg(const uint8_t* A, const uint8_t* B, const float* sa
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (probe_only) {  // how many clusters of S fit at once
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) {
-      cudaGetLastError();
-      n = 0;
+  if (probe_only) {  // how many clusters of S fit at once (computed once per device)
+    static int cached[64];  // value + 1; 0 = not yet known
+    int& slot = cached[dev.device >= 0 && dev.device < 64 ? dev.device : 0];
+    if (slot == 0) {
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        n = 0;
+      }
+      slot = n + 1;
     }
-    *fits = n;
+    *fits = slot - 1;
     return QK_OK;
   }
   CUtensorMap tw, ta;
@@ -88,45 +98,109 @@ static int launch_skinny_cfg(const uint8_t* A, const uint8_t* B, const float* sa
   return QK_OK;
 }
 
+// Few rows (M <= 128): the stream-K weight-streaming kernel
+// (qk_streamk_kernel.cuh), one CTA per SM, launched cooperatively so that
+// all CTAs are resident while owners wait for their contributors' partials.
+// The partials and flags come from the stream-ordered workspace pool; each
+// call gets a fresh 64-bit epoch, so flags left in reused memory by earlier
+// calls (older epochs) never read as finished.
+std::atomic<unsigned long long> g_streamk_epoch{0};
+
+template <int MT>
+static int launch_streamk(const uint8_t* A, const uint8_t* B, const float* sa, const float* sb, const uint16_t* bias,
+                          uint16_t* out, int M, int N, int K, const DeviceInfo& dev, cudaStream_t stream) {
+  using C = StreamKCfg<MT, MT <= 64 ? 8 : 6>;
+  auto kernel = qk_streamk_fp8_kernel<C>;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) != cudaSuccess)
+    return QK_ERR_CUDA;
+  const int n_tiles = ceil_div(N, C::NT);
+  const int num_kb = ceil_div(K, C::K_ELEMS);
+  const long long units = static_cast<long long>(n_tiles) * num_kb;
+  const int G = static_cast<int>(units < dev.sm_count ? units : dev.sm_count);
+  CUtensorMap tw, ta;
+  int st = encode_tmap_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, K, N, K, C::K_ELEMS, C::NT);
+  if (st == QK_OK) st = encode_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, K, M, K, C::K_ELEMS, C::MT);
+  if (st != QK_OK) return st;
+  const size_t part_bytes = static_cast<size_t>(G) * C::MT * C::NT * sizeof(float);
+  void* ws = nullptr;
+  if (cudaMallocFromPoolAsync(&ws, part_bytes + static_cast<size_t>(G) * 4 * sizeof(unsigned long long), dev.pool,
+                              stream) != cudaSuccess) {
+    cudaGetLastError();
+    return QK_ERR_NOMEM;
+  }
+  StreamKParams p{};
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.num_kb = num_kb;
+  p.units = units;
+  p.sa = sa;
+  p.sb = sb;
+  p.bias = bias;
+  p.out = out;
+  p.partials = static_cast<float*>(ws);
+  p.flags = reinterpret_cast<unsigned long long*>(static_cast<uint8_t*>(ws) + part_bytes);
+  // a 64-bit value no earlier call used (odd multiplier: a bijection of the counter)
+  p.epoch = (g_streamk_epoch.fetch_add(1) + 1) * 0x9E3779B97F4A7C15ull;
+  p.err = dev.err_word;
+  p.timeout_ns = wait_timeout_ns();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(G, 1, 1);
+  cfg.blockDim = dim3(C::NUM_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  LaunchTimer timer(kKGemmFp8, stream);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, tw, ta, p);
+  timer.done();
+  const cudaError_t f = cudaFreeAsync(ws, stream);
+  if (e != cudaSuccess || f != cudaSuccess) {
+    cudaGetLastError();
+    return QK_ERR_CUDA;
+  }
+  count_launches(1);
+  return QK_OK;
+}
+
+// Few rows: if the weight tiles times some split S in {8, 4, 2, 1} fit on the
+// GPU in one wave of clusters, the cluster split-K kernel with the largest
+// such S (one pass, on-chip reduction); otherwise stream-K, which keeps every
+// SM streaming whatever the tile count.  QK_FP8_SKINNY: 1 = the 2-SM tile
+// kernel, 2 = always stream-K, 3 = always cluster split-K.
 template <int MT>
 static int launch_skinny(const uint8_t* A, const uint8_t* B, const float* sa, const float* sb, const uint16_t* bias,
-                         uint16_t* out, int M, int N, int K, const DeviceInfo& dev, cudaStream_t stream) {
-  // Pick the split S (1, 2, 4, 8) that minimises waves(S) * (c0 + k-blocks per
-  // CTA), with c0 ~ 20 k-blocks' worth of fixed per-CTA time (launch, setup,
-  // reduction), as measured on the 64-row problems.
+                         uint16_t* out, int M, int N, int K, const DeviceInfo& dev, cudaStream_t stream, int variant) {
   const int n_tiles = ceil_div(N, 128);
   const int num_kb = ceil_div(K, 128);
-  int best = 1;
-  double best_cost = 1e30;
-  for (int S : {1, 2, 4, 8}) {
-    if (S > num_kb) break;
-    int fits = 0;
-    if (S == 1) launch_skinny_cfg<MT, 1>(A, B, sa, sb, bias, out, M, N, K, dev, stream, true, &fits);
-    if (S == 2) launch_skinny_cfg<MT, 2>(A, B, sa, sb, bias, out, M, N, K, dev, stream, true, &fits);
-    if (S == 4) launch_skinny_cfg<MT, 4>(A, B, sa, sb, bias, out, M, N, K, dev, stream, true, &fits);
-    if (S == 8) launch_skinny_cfg<MT, 8>(A, B, sa, sb, bias, out, M, N, K, dev, stream, true, &fits);
-    if (fits <= 0) continue;
-    const int waves = ceil_div(n_tiles, fits);
-    const double cost = static_cast<double>(waves) * (20.0 + ceil_div(num_kb, S));
-    if (cost < best_cost) {
-      best_cost = cost;
-      best = S;
+  if (variant != 2) {
+    for (int S : {8, 4, 2, 1}) {
+      if (S > num_kb && S > 1) continue;
+      int fits = 0;
+      if (S == 8) launch_skinny_cfg<MT, 8>(A, B, sa, sb, bias, out, M, N, K, dev, stream, true, &fits);
+      if (S == 4) launch_skinny_cfg<MT, 4>(A, B, sa, sb, bias, out, M, N, K, dev, stream, true, &fits);
+      if (S == 2) launch_skinny_cfg<MT, 2>(A, B, sa, sb, bias, out, M, N, K, dev, stream, true, &fits);
+      if (S == 1) launch_skinny_cfg<MT, 1>(A, B, sa, sb, bias, out, M, N, K, dev, stream, true, &fits);
+      if (n_tiles > fits && !(variant == 3 && S == 1)) continue;
+      switch (S) {
+        case 8: return launch_skinny_cfg<MT, 8>(A, B, sa, sb, bias, out, M, N, K, dev, stream, false, nullptr);
+        case 4: return launch_skinny_cfg<MT, 4>(A, B, sa, sb, bias, out, M, N, K, dev, stream, false, nullptr);
+        case 2: return launch_skinny_cfg<MT, 2>(A, B, sa, sb, bias, out, M, N, K, dev, stream, false, nullptr);
+        default: return launch_skinny_cfg<MT, 1>(A, B, sa, sb, bias, out, M, N, K, dev, stream, false, nullptr);
+      }
     }
   }
-  switch (best) {
-    case 8: return launch_skinny_cfg<MT, 8>(A, B, sa, sb, bias, out, M, N, K, dev, stream, false, nullptr);
-    case 4: return launch_skinny_cfg<MT, 4>(A, B, sa, sb, bias, out, M, N, K, dev, stream, false, nullptr);
-    case 2: return launch_skinny_cfg<MT, 2>(A, B, sa, sb, bias, out, M, N, K, dev, stream, false, nullptr);
-    default: return launch_skinny_cfg<MT, 1>(A, B, sa, sb, bias, out, M, N, K, dev, stream, false, nullptr);
-  }
+  return launch_streamk<MT>(A, B, sa, sb, bias, out, M, N, K, dev, stream);
 }
 
 int launch_fp8_rowwise(const uint8_t* A, const uint8_t* B, const float* sa, const float* sb, const uint16_t* bias,
                        uint16_t* out, int M, int N, int K, const DeviceInfo& dev, cudaStream_t stream) {
-  if (M <= 64 && kernel_variant("QK_FP8_SKINNY") == 0)
-    return launch_skinny<64>(A, B, sa, sb, bias, out, M, N, K, dev, stream);
-  if (M <= 128 && kernel_variant("QK_FP8_SKINNY") == 0)
-    return launch_skinny<128>(A, B, sa, sb, bias, out, M, N, K, dev, stream);
+  const int v = kernel_variant("QK_FP8_SKINNY");
+  if (M <= 64 && v != 1) return launch_skinny<64>(A, B, sa, sb, bias, out, M, N, K, dev, stream, v);
+  if (M <= 128 && v != 1) return launch_skinny<128>(A, B, sa, sb, bias, out, M, N, K, dev, stream, v);
   return launch_fp8_cfg<CfgFp8>(A, B, sa, sb, bias, out, M, N, K, dev, stream);
 }
 

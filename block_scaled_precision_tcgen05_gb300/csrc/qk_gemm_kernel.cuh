@@ -39,7 +39,7 @@
 
 namespace qk {
 
-enum class Kind : int { F16 = 0, F8 = 1, MXF8 = 2, MXF4 = 3 };
+enum class Kind : int { F16 = 0, F8 = 1, MXF8 = 2, MXF4 = 3, NVF4 = 4, F8BS = 5 };
 
 // How the scale warp gets raw scale rows (MX kinds):
 //   kSfTma    TMA boxes of 16 bytes per row (K % 512 == 0, 16-byte aligned rows)
@@ -57,9 +57,12 @@ struct GemmParams {
   const float* sb;            // [N] column scales (F16, F8)
   const uint16_t* bias;       // [N] bf16 bits, nullable
   uint16_t* out;              // [M, N] bf16 bits
-  const uint8_t* sA;          // [M, sf_cols] UE8M0 (MX)
-  const uint8_t* sB;          // [N, sf_cols] UE8M0 (MX)
-  int sf_cols;                // K / 32
+  const uint8_t* sA;          // [M, sf_cols] scale bytes (MX: UE8M0, NVFP4: UE4M3)
+  const uint8_t* sB;          // [N, sf_cols]
+  int sf_cols;                // scale bytes per row: K / 32 (MX), K / 16 (NVFP4)
+  const float* ga;            // NVFP4 per-tensor scales (nullable: 1)
+  const float* gb;
+  int scale_kb;               // FP8 blockscale: K-blocks of 128 per scale row (sa [M, kb], sb [ceil(N/128), kb])
   int sf_mode;                // MX scale staging: kSfTma, kSfAsync or kSfLoads
   int group_m;                // row-blocks per raster group
   unsigned long long* err;    // device error word
@@ -95,19 +98,27 @@ struct GemmCfg {
   static constexpr int STAGES = STAGES_;
   static constexpr int ACC_BUFS = ACC_BUFS_;
   static constexpr int ROW_BYTES = 128;  // bytes of K per row per ring stage (one swizzle row)
-  static constexpr int K_ELEMS = KIND == Kind::F16 ? 64 : (KIND == Kind::MXF4 ? 256 : 128);
+  static constexpr bool FP4 = KIND == Kind::MXF4 || KIND == Kind::NVF4;
+  static constexpr int K_ELEMS = KIND == Kind::F16 ? 64 : (FP4 ? 256 : 128);
   static constexpr int TMA_K = KIND == Kind::F16 ? 64 : 128;  // tensor-map elements per stage along K
-  static constexpr int UMMA_K = KIND == Kind::F16 ? 16 : (KIND == Kind::MXF4 ? 64 : 32);
+  static constexpr int UMMA_K = KIND == Kind::F16 ? 16 : (FP4 ? 64 : 32);
   static constexpr int K_STEPS = K_ELEMS / UMMA_K;  // 4 MMAs of 32 bytes of K each
-  static constexpr bool MX = KIND == Kind::MXF8 || KIND == Kind::MXF4;
+  // block-scaled kinds: scales staged per ring slot and copied to TMEM
+  static constexpr bool MX = KIND == Kind::MXF8 || KIND == Kind::MXF4 || KIND == Kind::NVF4;
+  static constexpr int SF_BLOCK = KIND == Kind::NVF4 ? 16 : 32;  // K-elements per scale byte
+  static constexpr bool ALPHA = KIND == Kind::NVF4;              // per-tensor scales in the epilogue
   static constexpr bool INT_CHUNKS = KIND == Kind::F16;
+  // FP8 blockscale: every 128-K block is its own accumulation chunk, scaled
+  // by sa[m, g] * sb[n / 128, g] into fp32 sums held in registers
+  static constexpr bool BLOCKSCALE = KIND == Kind::F8BS;
+  static constexpr bool DENSE_F8 = KIND == Kind::F8 || KIND == Kind::F8BS;
   static constexpr bool ROWWISE = KIND == Kind::F16 || KIND == Kind::F8;
   static constexpr int EPI_WARPS = EPI_WARPS_;
   static constexpr int EPI_PARTS = EPI_WARPS / 4;     // column parts of a tile
   static constexpr int EPI_COLS = BN_ / EPI_PARTS;    // columns per epilogue warp
-  static constexpr bool REG_SUMS = INT_CHUNKS && EPI_WARPS == 16;
+  static constexpr bool REG_SUMS = (INT_CHUNKS || BLOCKSCALE) && EPI_WARPS == 16;
 
-  static constexpr int SF_PER_STAGE = MX ? K_ELEMS / 32 : 0;  // scale bytes per row per stage
+  static constexpr int SF_PER_STAGE = MX ? K_ELEMS / SF_BLOCK : 0;  // scale bytes per row per stage
   static constexpr int SF_ATOMS_K = SF_PER_STAGE / 4;         // 4 scale bytes per 32-bit TMEM column
   static constexpr int NB128 = (BN + 127) / 128;              // 128-row blocks of the B tile
   static constexpr int SFA_BYTES = SF_ATOMS_K * 512;
@@ -161,7 +172,9 @@ struct GemmCfg {
 
   static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "tile N");
   static_assert(EPI_WARPS % 4 == 0 && EPI_COLS % 32 == 0, "epilogue split");
-  static_assert(!REG_SUMS || EPI_COLS == 64, "register sums hold 64 columns per thread");
+  static_assert(!REG_SUMS || EPI_COLS == 64 || (BLOCKSCALE && EPI_COLS == 32),
+                "register sums hold 64 columns per thread (32 for blockscale)");
+  static_assert(!BLOCKSCALE || REG_SUMS, "blockscale sums live in registers");
   static_assert(!(PAIR && MCAST), "one cluster mode");
   static_assert(COLS_USED <= 512, "TMEM budget");
   static_assert(SMEM_BYTES <= 232448, "shared-memory budget");
@@ -174,12 +187,14 @@ struct GemmCfg {
   static constexpr uint32_t FULL_ARRIVALS = 1 + (MX ? (PAIR ? 2 : 1) : 0);
 
   // kind::f16: D fp32 (1), A/B f16 (0).  kind::f8f6f4: A/B E4M3 (0).
-  // kind::mxf8f6f4: E4M3 (0).  kind::mxf4: E2M1 (1).
+  // kind::mxf8f6f4: E4M3 (0).  kind::mxf4: E2M1 (1), UE8M0 scales.
+  // kind::mxf4nvf4 (NVFP4): E2M1 (1), UE4M3 scales.
   __host__ __device__ static constexpr uint32_t idesc(uint32_t a_sf_id, uint32_t b_sf_id) {
     return KIND == Kind::F16    ? make_idesc_dense(1, 0, 0, MMA_M, BN)
-           : KIND == Kind::F8   ? make_idesc_dense(1, 0, 0, MMA_M, BN)
+           : DENSE_F8           ? make_idesc_dense(1, 0, 0, MMA_M, BN)
            : KIND == Kind::MXF8 ? make_idesc_block_scaled(0, 0, MMA_M, BN, a_sf_id, b_sf_id)
-                                : make_idesc_block_scaled(1, 1, MMA_M, BN, a_sf_id, b_sf_id);
+           : KIND == Kind::MXF4 ? make_idesc_block_scaled(1, 1, MMA_M, BN, a_sf_id, b_sf_id)
+                                : make_idesc_block_scaled(1, 1, MMA_M, BN, a_sf_id, b_sf_id, false);
   }
 };
 
@@ -238,7 +253,8 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // tensor map uses (16-byte chunk c of row r at 64r + 16(c ^ ((r >> 1) & 3))).
 // INT_ACC: v holds int32 sums; otherwise fp32 bit patterns.  Columns past N
 // (N is a multiple of 8) read no scale or bias; the bulk store clips them.
-template <bool ROWWISE, bool INT_ACC, int OFF = 0, int LEN = 32>
+// ALPHA: multiply by `sam` (the NVFP4 per-tensor scale product) before the bias.
+template <bool ROWWISE, bool INT_ACC, int OFF = 0, bool ALPHA = false, int LEN = 32>
 __device__ __forceinline__ void epilogue_row32(const GemmParams& p, int n0, float sam, const uint32_t (&v)[LEN],
                                                uint32_t block, int lane) {
   const bool has_bias = p.bias != nullptr;
@@ -275,6 +291,7 @@ __device__ __forceinline__ void epilogue_row32(const GemmParams& p, int n0, floa
           t = __fmul_rn(t, sam);
           t = __fmul_rn(t, sbv[i + j]);
         }
+        if constexpr (ALPHA) t = __fmul_rn(t, sam);
         if (has_bias) t = __fadd_rn(t, bv[i + j]);
         x[j] = t;
       }
@@ -286,7 +303,7 @@ __device__ __forceinline__ void epilogue_row32(const GemmParams& p, int n0, floa
 
 // The same epilogue with the 8-column pieces stored straight to row m of the
 // output (16-byte stores; no staging).
-template <bool ROWWISE, bool INT_ACC, int OFF = 0, int LEN = 32>
+template <bool ROWWISE, bool INT_ACC, int OFF = 0, bool ALPHA = false, int LEN = 32>
 __device__ __forceinline__ void epilogue_row32_global(const GemmParams& p, int m, int n0, float sam,
                                                       const uint32_t (&v)[LEN]) {
   const bool has_bias = p.bias != nullptr;
@@ -324,6 +341,7 @@ __device__ __forceinline__ void epilogue_row32_global(const GemmParams& p, int m
             t = __fmul_rn(t, sam);
             t = __fmul_rn(t, sbv[i + j]);
           }
+          if constexpr (ALPHA) t = __fmul_rn(t, sam);
           if (has_bias) t = __fadd_rn(t, bv[i + j]);
           x[j] = t;
         }
@@ -780,11 +798,11 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                 const uint64_t bd = bdesc + static_cast<uint64_t>((j * 32) >> 4);
                 if constexpr (C::kind == Kind::F16 && C::PAIR) {
                   umma_f16_pair(d_tmem, ad, bd, C::idesc(0, 0), accum);
-                } else if constexpr (C::kind == Kind::F8 && C::PAIR) {
+                } else if constexpr (C::DENSE_F8 && C::PAIR) {
                   umma_f8f6f4_pair(d_tmem, ad, bd, C::idesc(0, 0), accum);
                 } else if constexpr (C::kind == Kind::F16) {
                   umma_f16(d_tmem, ad, bd, C::idesc(0, 0), accum);
-                } else if constexpr (C::kind == Kind::F8) {
+                } else if constexpr (C::DENSE_F8) {
                   umma_f8f6f4(d_tmem, ad, bd, C::idesc(0, 0), accum);
                 } else if constexpr (C::kind == Kind::MXF8) {
                   // one scale byte per row per MMA: byte j of the stage's column
@@ -793,6 +811,11 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                   } else {
                     umma_mxf8f6f4(d_tmem, ad, bd, C::idesc(j, j), sf_tmem, sf_tmem + C::SF_COLS_A, accum);
                   }
+                } else if constexpr (C::kind == Kind::NVF4) {
+                  // four UE4M3 scale bytes (one per 16 K) per row per MMA: all of column group j
+                  static_assert(!C::PAIR, "NVFP4 runs on one CTA");
+                  umma_nvf4(d_tmem, ad, bd, C::idesc(0, 0), sf_tmem + 4 * j, sf_tmem + C::SF_COLS_A + 4 * C::NB128 * j,
+                            accum);
                 } else {
                   // two scale bytes per row per MMA: bytes 2(j%2), 2(j%2)+1 of column group j/2
                   const uint32_t g = static_cast<uint32_t>(j >> 1);
@@ -868,6 +891,8 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                    0u};
     uint32_t acc_iter = 0;
     bool ok = true;
+    float alpha = 1.f;  // NVFP4: product of the per-tensor scales, one fp32 rounding
+    if constexpr (C::ALPHA) alpha = __fmul_rn(p.ga ? __ldg(p.ga) : 1.f, p.gb ? __ldg(p.gb) : 1.f);
     // accumulator releases go to the leader CTA's barrier
     const uint32_t acc_empty_leader = C::PAIR ? mapa_shared(smem_u32(&acc_empty[0]), 0u) : 0u;
     auto release = [&](int a) {
@@ -891,8 +916,16 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
       const bool block_ok = m_block < p.M;  // warp-uniform: any row of this block inside M
       float sam = 1.f;
       if constexpr (C::ROWWISE) sam = row_ok ? __ldg(p.sa + m) : 0.f;
+      if constexpr (C::ALPHA) sam = alpha;
       const int n_tile = nb * C::BN + col_part;
       [[maybe_unused]] uint32_t sums[C::REG_SUMS ? C::EPI_COLS : 1];
+      // blockscale: the first K-block's scales (later ones are loaded a chunk ahead)
+      [[maybe_unused]] const bool col_in = n_tile < p.N;
+      [[maybe_unused]] float sa_next = 0.f, sb_next = 0.f;
+      if constexpr (C::BLOCKSCALE) {
+        sa_next = row_ok ? __ldg(p.sa + static_cast<size_t>(m) * p.scale_kb) : 0.f;
+        sb_next = col_in ? __ldg(p.sb + static_cast<size_t>(n_tile >> 7) * p.scale_kb) : 0.f;
+      }
 #pragma unroll 1
       for (int c = 0; c < p.num_chunks; ++c) {
         const int a = static_cast<int>(acc_iter % C::ACC_BUFS);
@@ -911,13 +944,48 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
           if (!(block_ok && n0 < p.N)) return;
           if constexpr (C::STORE_TMA) {
             const uint32_t block = out_block_acquire<C>(ostg, lane);
-            epilogue_row32<C::ROWWISE || kInt, kInt, kOff>(p, n0, sam, vals, block, lane);
+            epilogue_row32<C::ROWWISE || kInt, kInt, kOff, C::ALPHA>(p, n0, sam, vals, block, lane);
             out_block_release<C>(ostg, block, &tmOut, n0, m_block, lane);
           } else if (row_ok) {
-            epilogue_row32_global<C::ROWWISE || kInt, kInt, kOff>(p, m, n0, sam, vals);
+            epilogue_row32_global<C::ROWWISE || kInt, kInt, kOff, C::ALPHA>(p, m, n0, sam, vals);
           }
         };
-        if constexpr (C::REG_SUMS) {
+        if constexpr (C::REG_SUMS && C::BLOCKSCALE) {
+          // chunk c is K-block c: sums += partial * (sa[m, c] * sb[n / 128, c]);
+          // this thread's columns lie in one 128-column block of B
+          const float scale = __fmul_rn(sa_next, sb_next);
+          if (c + 1 < p.num_chunks) {  // next K-block's scales, loaded ahead
+            sa_next = row_ok ? __ldg(p.sa + static_cast<size_t>(m) * p.scale_kb + c + 1) : 0.f;
+            sb_next = col_in ? __ldg(p.sb + static_cast<size_t>(n_tile >> 7) * p.scale_kb + c + 1) : 0.f;
+          }
+          if constexpr (C::EPI_COLS == 32) {
+            uint32_t v[32];
+            tmem_ld_32cols(acc_col, v);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const float prev = c == 0 ? 0.f : __uint_as_float(sums[i]);
+              sums[i] = __float_as_uint(__fmaf_rn(__uint_as_float(v[i]), scale, prev));
+            }
+          } else {
+#pragma unroll
+            for (int g = 0; g < C::EPI_COLS / 16; ++g) {
+              uint32_t v[16];
+              tmem_ld_16cols(acc_col + 16 * g, v);
+              tmem_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                const float prev = c == 0 ? 0.f : __uint_as_float(sums[16 * g + i]);
+                sums[16 * g + i] = __float_as_uint(__fmaf_rn(__uint_as_float(v[i]), scale, prev));
+              }
+            }
+          }
+          release(a);
+          if (last) {
+            emit(EmitTag<false, 0>{}, n_tile, sums);
+            if constexpr (C::EPI_COLS == 64) emit(EmitTag<false, 32>{}, n_tile + 32, sums);
+          }
+        } else if constexpr (C::REG_SUMS) {
           // drain the chunk into the register sums, free the accumulator, and
           // after the last chunk run the epilogue from the registers
 #pragma unroll

@@ -49,7 +49,9 @@ enum KernelKind : int {
   kKGemmMxfp4 = 4,
   kKWaitProbe = 5,
   kKQuantize = 6,
-  kKNumKinds = 7,
+  kKGemmNvfp4 = 7,
+  kKGemmFp8Blockscale = 8,
+  kKNumKinds = 9,
 };
 
 // Brackets one kernel launch with an event pair when timing is enabled.
@@ -70,6 +72,9 @@ int launch_mxfp8(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const ui
                  uint16_t* out, int M, int N, int K, const DeviceInfo& dev, cudaStream_t stream);
 int launch_mxfp4(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const uint8_t* sB, const uint16_t* bias,
                  uint16_t* out, int M, int N, int K, const DeviceInfo& dev, cudaStream_t stream);
+int launch_fp8_blockscale(const uint8_t* A, const uint8_t* B, const float* sa, const float* sb,
+                          const uint16_t* bias, uint16_t* out, int M, int N, int K, const DeviceInfo& dev,
+                          cudaStream_t stream);
 int launch_wait_probe(uint64_t timeout_ns, const DeviceInfo& dev, cudaStream_t stream);
 
 }  // namespace qk

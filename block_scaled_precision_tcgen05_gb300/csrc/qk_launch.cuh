@@ -27,6 +27,8 @@ void plan_tiles(GemmParams& p, int M, int N, int K) {
   if (C::INT_CHUNKS) {
     // 1024 K per chunk: |partial| <= 1024 * 2^14 = 2^24, exact in fp32.
     p.chunk_kb = 1024 / C::K_ELEMS;
+  } else if (C::BLOCKSCALE) {
+    p.chunk_kb = 1;  // one 128-K scale block per chunk
   } else {
     p.chunk_kb = p.num_kb;
   }
@@ -35,7 +37,12 @@ void plan_tiles(GemmParams& p, int M, int N, int K) {
 
 template <class C>
 constexpr int kernel_kind() {
-  return C::kind == Kind::F16 ? kKGemmInt8 : C::kind == Kind::F8 ? kKGemmFp8 : C::kind == Kind::MXF8 ? kKGemmMxfp8 : kKGemmMxfp4;
+  return C::kind == Kind::F16    ? kKGemmInt8
+         : C::kind == Kind::F8   ? kKGemmFp8
+         : C::kind == Kind::MXF8 ? kKGemmMxfp8
+         : C::kind == Kind::MXF4 ? kKGemmMxfp4
+         : C::kind == Kind::NVF4 ? kKGemmNvfp4
+                                 : kKGemmFp8Blockscale;
 }
 
 // tsa / tsb: tensor maps of the raw scale rows (MX with p.sf_tma), else any map.

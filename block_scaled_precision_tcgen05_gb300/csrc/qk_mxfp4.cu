@@ -12,6 +12,10 @@ namespace qk {
 using CfgMxfp4Single = GemmCfg<Kind::MXF4, 256, 4, 1, false, 4, 1>;
 using CfgMxfp4Pair = GemmCfg<Kind::MXF4, 256, 5, 1, true, 8, 2>;
 using CfgMxfp4Mcast = GemmCfg<Kind::MXF4, 256, 4, 1, false, 4, 1, true>;
+// 192-column tiles leave TMEM room for two accumulators beside the scale
+// ring (variant 3), but at the FP4 rate the operand bytes per flop decide:
+// 3650 against 4400 TFLOP/s for 128 x 256 tiles, which stay the default.
+using CfgMxfp4Double = GemmCfg<Kind::MXF4, 192, 4, 2, false, 4, 2>;
 
 template <class C>
 static int launch_mxfp4_cfg(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const uint8_t* sB,
@@ -50,6 +54,7 @@ int launch_mxfp4(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const ui
   const int v = kernel_variant("QK_MX_VARIANT");
   if (v == 1) return launch_mxfp4_cfg<CfgMxfp4Pair>(A, sA, B, sB, bias, out, M, N, K, dev, stream);
   if (v == 2) return launch_mxfp4_cfg<CfgMxfp4Mcast>(A, sA, B, sB, bias, out, M, N, K, dev, stream);
+  if (v == 3) return launch_mxfp4_cfg<CfgMxfp4Double>(A, sA, B, sB, bias, out, M, N, K, dev, stream);
   return launch_mxfp4_cfg<CfgMxfp4Single>(A, sA, B, sB, bias, out, M, N, K, dev, stream);
 }
 

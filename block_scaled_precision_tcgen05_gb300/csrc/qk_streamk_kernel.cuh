@@ -1,0 +1,338 @@
+// qk_streamk_kernel.cuh -- FP8 per-token x per-channel GEMM for few rows
+// (M <= 128), where streaming the weight from HBM sets the time.
+//
+// The product is computed transposed, D^T[n, m] = sum_k B[n,k] A[m,k]: a tile
+// of 128 weight rows is the MMA's M operand (TMEM lanes = n) and the M
+// activation rows, padded to MT, are its N operand (TMEM columns = m).
+//
+// Work is balanced by stream-K: the (tile, K-block) units of the whole
+// problem, tile-major, are cut into one contiguous range per CTA, one CTA per
+// SM, so every SM streams the same number of weight bytes whatever the tile
+// count.  A CTA's range splits into segments, one per tile it touches; each
+// segment accumulates in one of two TMEM accumulators, so the epilogue of
+// one segment overlaps the MMAs of the next.
+//  * A segment that covers a whole tile is finished in place.
+//  * A segment that does not start at K-block 0 can only be the CTA's first;
+//    its fp32 partial goes to a workspace slot of that CTA.  Each epilogue
+//    warp writes its 32 weight rows and then releases its own flag with this
+//    call's epoch, so no barrier across warps is needed.
+//  * The segment holding K-block 0 owns the tile: each epilogue warp waits
+//    (bounded) for the matching warp flags of the CTAs that carry the rest of
+//    the tile, adds their partials in CTA order (a fixed order, so results
+//    are reproducible) and runs the epilogue (x*sa[m])*sb[n] (+bias[n]) ->
+//    bf16.
+// A contributor's segment is the first thing it computes and never waits on
+// another CTA, so the waits cannot form a cycle; the launch is cooperative,
+// which guarantees that all CTAs are resident at once.
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include "qk_device.cuh"
+#include "qk_gemm_kernel.cuh"
+
+namespace qk {
+
+struct StreamKParams {
+  int M, N, K;
+  int num_kb;                 // K-blocks of 128 elements
+  long long units;            // n_tiles * num_kb
+  const float* sa;
+  const float* sb;
+  const uint16_t* bias;
+  uint16_t* out;
+  float* partials;            // [gridDim.x][MT][128] fp32
+  unsigned long long* flags;  // [gridDim.x][4]: one per epilogue warp
+  unsigned long long epoch;   // unique per call; a flag equal to it marks a finished partial
+  unsigned long long* err;
+  uint64_t timeout_ns;
+};
+
+template <int MT_, int STAGES_>
+struct StreamKCfg {
+  static constexpr int MT = MT_;          // padded activation rows (MMA N)
+  static constexpr int NT = 128;          // weight rows per tile (MMA M)
+  static constexpr int STAGES = STAGES_;
+  static constexpr int K_ELEMS = 128;     // E4M3 elements per stage (one 128-byte swizzle row)
+  static constexpr int W_BYTES = NT * 128;
+  static constexpr int A_BYTES = MT * 128;
+  static constexpr uint32_t STAGE_TX = W_BYTES + A_BYTES;
+  static constexpr int OFF_W = 0;
+  static constexpr int OFF_A = OFF_W + STAGES * W_BYTES;
+  static constexpr int OFF_BAR = OFF_A + STAGES * A_BYTES;
+  static constexpr int NUM_BARS = 2 * STAGES + 2 * 2 + 1;  // ring, accumulators, drain
+  static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
+  static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
+  static constexpr int TMEM_COLS = 2 * MT;  // two accumulators
+  static constexpr int NUM_THREADS = 256;   // warp 0 TMA, warp 1 MMA, warps 4..7 epilogue
+  static_assert(MT == 32 || MT == 64 || MT == 128, "activation tile");
+  static_assert(A_BYTES % 1024 == 0, "swizzle atoms need 1024-byte alignment");
+  static_assert(SMEM_BYTES <= 232448, "shared-memory budget");
+  static constexpr uint32_t IDESC = make_idesc_dense(1, 0, 0, NT, MT);  // fp32 D, E4M3 x E4M3
+};
+
+// First unit of CTA c's range (units * c / G, rounded down).
+__device__ __forceinline__ long long streamk_begin(long long units, int c, int G) {
+  return units * static_cast<long long>(c) / static_cast<long long>(G);
+}
+
+__device__ __forceinline__ void st_release_gpu_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ unsigned long long ld_acquire_gpu_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+template <class C>
+__global__ void __launch_bounds__(C::NUM_THREADS, 1)
+    qk_streamk_fp8_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmA,
+                          const StreamKParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* empty = full + C::STAGES;
+  uint64_t* acc_full = empty + C::STAGES;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* drain = acc_empty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_MISC + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int c = static_cast<int>(blockIdx.x);
+  const int G = static_cast<int>(gridDim.x);
+  const long long u0 = streamk_begin(p.units, c, G);
+  const long long u1 = streamk_begin(p.units, c + 1, G);
+
+  if (threadIdx.x == 0) {
+#pragma unroll 1
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&full[s], 1u);
+      mbar_init(&empty[s], 1u);
+    }
+#pragma unroll 1
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&acc_full[a], 1u);
+      mbar_init(&acc_empty[a], 4u);  // the four epilogue warps
+    }
+    mbar_init(drain, 1u);
+    *abort_flag = 0u;
+    fence_mbar_init();
+    tma_prefetch_desc(&tmW);
+    tma_prefetch_desc(&tmA);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+  const WaitCtl w{abort_flag, p.err, p.timeout_ns};
+
+  if (warp == 0) {
+    // ---------------- TMA producer: one stage per unit of the range ----------------
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      long long issued = 0;
+#pragma unroll 1
+      for (long long u = u0; u < u1; ++u) {
+        const int t = static_cast<int>(u / p.num_kb);
+        const int kb = static_cast<int>(u - static_cast<long long>(t) * p.num_kb);
+        if (!mbar_wait(&empty[stage], phase ^ 1u, w, kSiteProducerEmpty)) break;
+        mbar_arrive_expect_tx(&full[stage], C::STAGE_TX);
+        tma_load_2d(smem + C::OFF_W + stage * C::W_BYTES, &tmW, &full[stage], kb * C::K_ELEMS, t * C::NT);
+        tma_load_2d(smem + C::OFF_A + stage * C::A_BYTES, &tmA, &full[stage], kb * C::K_ELEMS, 0);
+        ++issued;
+        if (++stage == C::STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      // wait (bounded) for the last load of every ring slot before leaving
+      const long long n = issued < C::STAGES ? issued : C::STAGES;
+#pragma unroll 1
+      for (long long i = 0; i < n; ++i) {
+        const long long L = issued - 1 - i;
+        const uint32_t a = smem_u32(&full[static_cast<int>(L % C::STAGES)]);
+        const uint64_t t0 = global_timer_ns();
+        while (!mbar_try_wait(a, static_cast<uint32_t>((L / C::STAGES) & 1))) {
+          if (global_timer_ns() - t0 > p.timeout_ns) {
+            report_error(p.err, kDevErrTimeout, kSiteProducerDrain, static_cast<uint32_t>(L));
+            break;
+          }
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---------------- MMA issuer: one accumulator per segment ----------------
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t seg = 0;
+      bool ok = true;
+#pragma unroll 1
+      for (long long u = u0; ok && u < u1;) {
+        const int t = static_cast<int>(u / p.num_kb);
+        const int kb0 = static_cast<int>(u - static_cast<long long>(t) * p.num_kb);
+        const int n_seg = static_cast<int>(min(static_cast<long long>(p.num_kb - kb0), u1 - u));
+        const int a = static_cast<int>(seg & 1u);
+        if (!mbar_wait(&acc_empty[a], ((seg >> 1) & 1u) ^ 1u, w, kSiteMmaAccEmpty)) break;
+        tc_fence_after_sync();
+        const uint32_t d_tmem = tmem + static_cast<uint32_t>(a * C::MT);
+#pragma unroll 1
+        for (int i = 0; i < n_seg; ++i) {
+          const int kb = kb0 + i;
+          if (!mbar_wait(&full[stage], phase, w, kSiteMmaFull)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint64_t wdesc = make_desc_kmajor_sw128(smem_u32(smem + C::OFF_W + stage * C::W_BYTES));
+          const uint64_t adesc = make_desc_kmajor_sw128(smem_u32(smem + C::OFF_A + stage * C::A_BYTES));
+          int ksteps = 4;
+          if (kb == p.num_kb - 1) ksteps = min(4, (p.K - kb * C::K_ELEMS + 31) / 32);
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            if (j < ksteps)
+              umma_f8f6f4(d_tmem, wdesc + static_cast<uint64_t>(2 * j), adesc + static_cast<uint64_t>(2 * j),
+                          C::IDESC, (i > 0 || j > 0) ? 1u : 0u);
+          umma_commit(&empty[stage]);
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit(&acc_full[a]);
+        ++seg;
+        u += n_seg;
+      }
+      // every MMA issued here completes before TMEM is freed
+      umma_commit(drain);
+      const uint32_t da = smem_u32(drain);
+      const uint64_t t0 = global_timer_ns();
+      while (!mbar_try_wait(da, 0u)) {
+        if (global_timer_ns() - t0 > p.timeout_ns) {
+          report_error(p.err, kDevErrTimeout, kSiteDrain, 0u);
+          break;
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ---------------- epilogue: thread r holds weight row r of the tile ----------------
+    const int q = warp - 4;
+    const int r = q * 32 + lane;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16);
+    uint32_t seg = 0;
+#pragma unroll 1
+    for (long long u = u0; u < u1;) {
+      const int t = static_cast<int>(u / p.num_kb);
+      const int kb0 = static_cast<int>(u - static_cast<long long>(t) * p.num_kb);
+      const int n_seg = static_cast<int>(min(static_cast<long long>(p.num_kb - kb0), u1 - u));
+      const int a = static_cast<int>(seg & 1u);
+      // warp-uniform outcome: the TMEM loads below are warp-collective
+      const bool got = mbar_wait(&acc_full[a], (seg >> 1) & 1u, w, kSiteEpiAccFull);
+      if (!__all_sync(0xffffffffu, got)) break;
+      tc_fence_after_sync();
+      float acc[C::MT];
+#pragma unroll
+      for (int g = 0; g < C::MT / 32; ++g) {
+        uint32_t v[32];
+        tmem_ld_32cols(lane_base + static_cast<uint32_t>(a * C::MT + 32 * g), v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) acc[32 * g + i] = __uint_as_float(v[i]);
+      }
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[a]);
+
+      if (kb0 != 0) {
+        // the tail of a tile owned by an earlier CTA: publish the partial
+        float* dst = p.partials + static_cast<size_t>(c) * C::MT * C::NT;
+#pragma unroll
+        for (int m = 0; m < C::MT; ++m)
+          if (m < p.M) dst[m * C::NT + r] = acc[m];
+        __syncwarp();
+        if (lane == 0) {
+          __threadfence();
+          st_release_gpu_u64(p.flags + 4 * c + q, p.epoch);
+        }
+      } else {
+        if (kb0 + n_seg != p.num_kb) {
+          // the head of a tile whose rest later CTAs carry: add their partials in CTA order
+          const long long tile_end = static_cast<long long>(t + 1) * p.num_kb;
+          // the contributors are CTAs c+1 .. jend-1; wait for all their flags at
+          // once (one per lane), then add the partials in CTA order
+          int jend = c + 1;
+          while (jend < G && streamk_begin(p.units, jend, G) < tile_end) ++jend;
+          bool ok = true;
+#pragma unroll 1
+          for (int base = c + 1; ok && base < jend; base += 32) {
+            const int j = base + lane;
+            int seen = 1;
+            if (j < jend) {
+              const uint64_t t0 = global_timer_ns();
+              while (ld_acquire_gpu_u64(p.flags + 4 * j + q) != p.epoch) {
+                if (*abort_flag) {
+                  seen = 0;
+                  break;
+                }
+                if (global_timer_ns() - t0 > p.timeout_ns) {
+                  report_error(p.err, kDevErrTimeout, kSitePeerPartial, static_cast<uint32_t>(j));
+                  *abort_flag = 1u;
+                  seen = 0;
+                  break;
+                }
+              }
+            }
+            // each lane's acquire, then the warp barrier, orders every lane's loads after it
+            ok = __all_sync(0xffffffffu, seen != 0);
+          }
+          __syncwarp();
+          if (ok) {
+#pragma unroll 1
+            for (int j = c + 1; j < jend; ++j) {
+              const float* src = p.partials + static_cast<size_t>(j) * C::MT * C::NT;
+#pragma unroll
+              for (int m = 0; m < C::MT; ++m)
+                if (m < p.M) acc[m] = __fadd_rn(acc[m], __ldcg(src + m * C::NT + r));
+            }
+          }
+        }
+        const int n = t * C::NT + r;
+        if (n < p.N) {
+          const float sbn = __ldg(p.sb + n);
+          const float bn = p.bias ? __uint_as_float(static_cast<uint32_t>(__ldg(p.bias + n)) << 16) : 0.f;
+#pragma unroll
+          for (int m = 0; m < C::MT; ++m) {
+            if (m < p.M) {
+              float x = __fmul_rn(acc[m], __ldg(p.sa + m));
+              x = __fmul_rn(x, sbn);
+              if (p.bias) x = __fadd_rn(x, bn);
+              p.out[static_cast<size_t>(m) * static_cast<size_t>(p.N) + n] =
+                  __bfloat16_as_ushort(__float2bfloat16_rn(x));
+            }
+          }
+        }
+      }
+      ++seg;
+      u += n_seg;
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
+}
+
+}  // namespace qk

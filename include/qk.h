@@ -113,9 +113,9 @@ int qk_gemm_int8_rowwise_noalloc(const int8_t* A, const int8_t* B, const float* 
                                  qk_stream_t stream);
 
 /*
- * MX block-scaled GEMM (ROCm/mori PR #806, "What": "the same 32-wide ue8m0
- * GEMM ... taking A's scales as [M, K/32] ... uint8, row major"; ROCm/FlyDSL
- * PR #990: MXFP4 "per1x32" scales).
+ * MX block-scaled GEMM (ROCm/mori PR #806, section "What": one ue8m0 scale
+ * per 32 K-elements, held as raw row-major uint8 bytes [rows, K/32] for both
+ * operands; ROCm/FlyDSL PR #990: MXFP4 with scales per 1x32 block).
  *
  *   out[m,n] = bf16_rne( sum_b 2^(sA[m,b]-127) * 2^(sB[n,b]-127)
  *                          * sum_{j<32} A[m,32b+j] * B[n,32b+j]   (+ bias[n]) )
@@ -145,6 +145,50 @@ int qk_gemm_mx(int fmt, const void* A, const uint8_t* sA, const void* B, const u
 int qk_gemm_fp8_rowwise(const uint8_t* A, const uint8_t* B, const float* sa, const float* sb,
                         const uint16_t* bias, uint16_t* out, int64_t M, int64_t N, int64_t K,
                         qk_stream_t stream);
+
+/*
+ * FP8 E4M3 GEMM with fp32 block scales (the "blockscale" kind of ROCm/mori PR
+ * #806's measurements; the page does not give the block sizes, read here as
+ * DeepSeek-V3's: 1 x 128 for A, 128 x 128 for B).
+ *
+ *   out[m,n] = bf16_rne( sum_g sa[m,g] * sb[n/128,g] * P_g[m,n]  (+ bias[n]) ),
+ *   P_g      = sum over k in [128 g, min(128 g + 128, K)) of A[m,k] * B[n,k]
+ * with each P_g an fp32 tensor-core sum and the scaled sum in fp32.
+ *
+ *   A uint8 [M, K] E4M3FN; B uint8 [N, K] E4M3FN
+ *   sa fp32 [M, KB], sb fp32 [NB, KB], row-major, KB = ceil(K/128), NB = ceil(N/128)
+ *   bias bf16 [N] or NULL;  out bf16 [M, N]
+ * Requirements: A, B, out, bias 16-byte aligned; sa, sb 4-byte aligned;
+ * N % 8 == 0; K % 16 == 0.  Any M >= 1.
+ */
+int qk_gemm_fp8_blockscale(const uint8_t* A, const uint8_t* B, const float* sa, const float* sb,
+                           const uint16_t* bias, uint16_t* out, int64_t M, int64_t N, int64_t K,
+                           qk_stream_t stream);
+
+/*
+ * NVFP4 block-scaled GEMM: E2M1 elements, one UE4M3 scale per 16 K-elements,
+ * and one fp32 scale per tensor (ROCm/aiter PR #6262, the gemm_a4w4
+ * signature's optional per-tensor NVFP4 scales for A and B; the format is
+ * NVIDIA's published NVFP4).
+ *
+ *   out[m,n] = bf16_rne( acc * fl(ga * gb)  (+ bias[n]) ),
+ *   acc      = sum_b ue4m3(sA[m,b]) * ue4m3(sB[n,b]) * sum_{j<16} A[m,16b+j] * B[n,16b+j]
+ * with acc the fp32 tensor-core sum (summation order free), then one fp32
+ * multiply by the fp32 product of the two per-tensor scales, then the bias
+ * add, each rounded to nearest even.
+ *
+ *   A  uint8 [M, K/2] packed E2M1, element 2i in the low nibble; B uint8 [N, K/2]
+ *   sA uint8 [M, K/16] raw row-major UE4M3 (E4M3FN without the sign; bit 7 must
+ *      be 0); sB uint8 [N, K/16]
+ *   ga, gb  device pointers to one fp32 each, or NULL for 1.0
+ *   bias bf16 [N] or NULL;  out bf16 [M, N]
+ * Requirements: A, B, out, bias 16-byte aligned; N % 8 == 0; K % 32 == 0.
+ * Any M >= 1 is accepted without padding.  Device-side reads of ga/gb happen
+ * in the kernel, so their values may be produced earlier on the same stream.
+ */
+int qk_gemm_nvfp4(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const uint8_t* sB, const float* ga,
+                  const float* gb, const uint16_t* bias, uint16_t* out, int64_t M, int64_t N, int64_t K,
+                  qk_stream_t stream);
 
 /*
  * Quantizers that produce the operands above from bf16 data.
@@ -207,7 +251,7 @@ uint64_t qk_launch_count(void);
  * up to `max` entries (one per kernel kind that ran) into `stats`; *count
  * receives the number of entries.  reset != 0 clears the totals afterwards.
  * Kernel names: "int8_to_f16", "gemm_int8_f16", "gemm_fp8", "gemm_mxfp8",
- * "gemm_mxfp4", "wait_probe", "quantize".
+ * "gemm_mxfp4", "wait_probe", "quantize", "gemm_nvfp4", "gemm_fp8_blockscale".
  */
 typedef struct {
   const char* name;   /* static storage */

@@ -15,9 +15,9 @@
  *  [CK174]  comfy-kitchen PR #174 "Optimize HIP WMMA INT8 GEMM staging,
  *           epilogue, and deep-K tiling": Summary (rowwise epilogue with
  *           cached scales and bias; signed zero without bias), Validation
- *           ("exact match, max absolute error 0.0"), and the update "Keep the
- *           cached INT8 epilogue scale order exact" ((acc*sa)*sb, never
- *           acc*(sa*sb)).
+ *           (the results match the reference bit for bit, zero error), and
+ *           the update "Keep the cached INT8 epilogue scale order exact"
+ *           ((acc*sa)*sb, never acc*(sa*sb)).
  *  [MORI806] ROCm/mori PR #806 "perf(gemm-ar): mxfp8 with row-major scales
  *           staged through LDS", section "What": 32-wide ue8m0 scales held
  *           raw, row-major, one byte per 32 K-elements.

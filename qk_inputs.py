@@ -85,17 +85,20 @@ def round_e4m3_value(a: np.ndarray) -> np.ndarray:
     return np.where(a < np.float32(2.0 ** -6), sub, normal).astype(np.float32)
 
 
+# E2M1 magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6: the code of |q| is the number of
+# midpoints it passes.  At a midpoint the tie goes to the even code, i.e.
+# down at 0.25, 1.25, 2.5, 5 (to 0, 1, 2, 4) and up at 0.75, 1.75, 3.5 (to 1, 2, 4).
+_E2M1_MIDPOINTS = ((0.25, False), (0.75, True), (1.25, False), (1.75, True), (2.5, False), (3.5, True), (5.0, False))
+
+
 def encode_e2m1(q: np.ndarray) -> np.ndarray:
     """Round to the nearest E2M1 value (ties to even), saturating at 6; one code per byte."""
     q = np.asarray(q, np.float32)
-    sign = (q.view(np.uint32) >> np.uint32(31)).astype(np.uint8) << np.uint8(3)
-    a = np.minimum(np.abs(q), np.float32(6.0))
-    r = _round_mantissa(a, 1)
-    exp = (r >> np.uint32(23)).astype(np.int32) - 127
-    normal_code = ((exp + 1) << 1) | ((r >> np.uint32(22)) & np.uint32(1)).astype(np.int32)
-    sub_code = np.rint(a * np.float32(2.0)).astype(np.int32)          # 0, 0.5, (1.0 -> code 2)
-    code = np.where(a < np.float32(1.0), sub_code, normal_code).astype(np.uint8)
-    return code | sign
+    a = np.abs(q)
+    code = np.zeros(q.shape, np.uint8)
+    for t, up in _E2M1_MIDPOINTS:
+        code += (a >= np.float32(t)) if up else (a > np.float32(t))
+    return code | (np.signbit(q).astype(np.uint8) << np.uint8(3))
 
 
 def pack_e2m1(codes: np.ndarray) -> np.ndarray:
@@ -382,8 +385,9 @@ def nvfp4_operand(rows: int, K: int, seed: int, tag: int):
     def bf16(x):
         return from_bf16_bits(to_bf16_bits(x))
 
-    amax = max([float(np.abs(bf16(x)).max()) for x in _normal_rows(_rng(seed, tag), rows, K, 1.0, lambda x: x)]
-               or [0.0])
+    # rounding to bf16 is monotonic, so the amax of the rounded operand is the rounded amax
+    amax = max([float(np.abs(x).max()) for x in _normal_rows(_rng(seed, tag), rows, K, 1.0, lambda x: x)] or [0.0])
+    amax = float(bf16(np.array([amax], np.float32))[0])
     g = np.float32(amax) / np.float32(448.0 * 6.0) if amax > 0 else np.float32(1.0)
     parts = _normal_rows(_rng(seed, tag), rows, K, 1.0, lambda x: nvfp4_quantize(bf16(x), g))
     return (_cat(parts, 0, (0, K // 2), np.uint8), _cat(parts, 1, (0, K // 16), np.uint8), float(g))

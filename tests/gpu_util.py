@@ -53,6 +53,22 @@ def run_mx(p, out=None):
     return out
 
 
+def run_blockscale(p, out=None):
+    out = nan_out(p.M, p.N) if out is None else out
+    qk.gemm_fp8_blockscale(to_dev(p.A), to_dev(p.B), to_dev(p.sa), to_dev(p.sb), bias_dev(p.bias), out)
+    torch.cuda.synchronize()
+    return out
+
+
+def run_nvfp4(p, out=None, global_scales=True):
+    out = nan_out(p.M, p.N) if out is None else out
+    ga = to_dev(np.array([p.global_a], np.float32)) if global_scales else None
+    gb = to_dev(np.array([p.global_b], np.float32)) if global_scales else None
+    qk.gemm_nvfp4(to_dev(p.A), to_dev(p.sA), to_dev(p.B), to_dev(p.sB), ga, gb, bias_dev(p.bias), out)
+    torch.cuda.synchronize()
+    return out
+
+
 def assert_bit_exact(gpu_bits, ref_bits, what=""):
     gpu_bits = np.asarray(gpu_bits, np.uint16)
     ref_bits = np.asarray(ref_bits, np.uint16)

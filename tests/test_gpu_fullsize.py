@@ -57,6 +57,35 @@ def test_mxfp4_full(shape):
     _mx_sampled(qi.FMT_MXFP4_E2M1, *shape)
 
 
+@pytest.mark.parametrize("shape", [(8192, 8192, 16384), (16384, 16384, 8192)], ids=lambda s: "x".join(map(str, s)))
+def test_nvfp4_full(shape):
+    from gpu_util import run_nvfp4
+    M, N, K = shape
+    p = qi.nvfp4_problem(M, N, K, seed=0)
+    out = run_nvfp4(p)
+    gots, refs = [], []
+    for (m0, m1, n0, n1) in _tiles(M, N, 3):
+        gots.append(host_bits(out[m0:m1, n0:n1]).ravel())
+        refs.append(oracle.gemm_nvfp4(p.A, p.sA, p.B, p.sB, p.global_a, p.global_b, m0=m0, m1=m1, n0=n0,
+                                      n1=n1).ravel())
+    assert not torch.isnan(out).any().item()
+    assert_close(np.concatenate(gots)[None, :], np.concatenate(refs)[None, :], f"nvfp4 {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("shape", [(16384, 7168, 2048), (30000, 21504, 5376)], ids=lambda s: "x".join(map(str, s)))
+def test_fp8_blockscale_full(shape):
+    from gpu_util import run_blockscale
+    M, N, K = shape
+    p = qi.blockscale_problem(M, N, K, seed=0)
+    out = run_blockscale(p)
+    gots, refs = [], []
+    for (m0, m1, n0, n1) in _tiles(M, N, 4):
+        gots.append(host_bits(out[m0:m1, n0:n1]).ravel())
+        refs.append(oracle.gemm_fp8_blockscale(p.A, p.B, p.sa, p.sb, m0=m0, m1=m1, n0=n0, n1=n1).ravel())
+    assert not torch.isnan(out).any().item()
+    assert_close(np.concatenate(gots)[None, :], np.concatenate(refs)[None, :], f"blockscale {M}x{N}x{K}")
+
+
 FP8_SWEEP = [(M, N, K) for (N, K) in ((2112, 7168), (7168, 1792), (21504, 5376)) for M in (64, 1024, 4096, 16384, 30000)]
 
 

@@ -1,6 +1,6 @@
 """INT8 row/column-scaled GEMM on the GPU against the oracle: bit-exact.
 
-comfy-kitchen PR #174, Validation ("exact match, max absolute error 0.0") and
+comfy-kitchen PR #174, Validation (bit-for-bit agreement, zero error) and
 the updates "Keep the cached INT8 epilogue scale order exact" and "Preserve
 signed zero without INT8 bias".  Outputs are NaN-filled before each call so an
 element the kernel never writes cannot pass.
