@@ -510,6 +510,17 @@ def run_kernel_case(args):
         p = qi.fp8_problem(M, N, K, seed=0)
         A, B, sa, sb = (_to_dev(x, dev) for x in (p.A, p.B, p.sa, p.sb))
         fn = lambda out: qk.gemm_fp8_rowwise(A, B, sa, sb, None, out)
+    elif args.kernel_case == "blockscale":
+        p = qi.blockscale_problem(M, N, K, seed=0)
+        A, B, sa, sb = (_to_dev(x, dev) for x in (p.A, p.B, p.sa, p.sb))
+        fn = lambda out: qk.gemm_fp8_blockscale(A, B, sa, sb, None, out)
+    elif args.kernel_case == "nvfp4":
+        import numpy as np
+        p = qi.nvfp4_problem(M, N, K, seed=0)
+        A, sA, B, sB = (_to_dev(x, dev) for x in (p.A, p.sA, p.B, p.sB))
+        ga = _to_dev(np.array([p.global_a], np.float32), dev)
+        gb = _to_dev(np.array([p.global_b], np.float32), dev)
+        fn = lambda out: qk.gemm_nvfp4(A, sA, B, sB, ga, gb, None, out)
     else:
         fmt = qi.FMT_MXFP8_E4M3 if args.kernel_case == "mxfp8" else qi.FMT_MXFP4_E2M1
         p = qi.mx_problem(fmt, M, N, K, seed=0)
@@ -538,7 +549,7 @@ def main(argv=None):
     ap.add_argument("--formats", choices=["default", "none", "full"], default="default")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
-    ap.add_argument("--kernel-case", choices=["int8", "fp8", "mxfp8", "mxfp4"], default=None,
+    ap.add_argument("--kernel-case", choices=["int8", "fp8", "mxfp8", "mxfp4", "nvfp4", "blockscale"], default=None,
                     help="only run --iters calls of one kernel kind on --shape (profiler captures)")
     ap.add_argument("--shape", default="8192,8192,8192")
     ap.add_argument("--iters", type=int, default=3)

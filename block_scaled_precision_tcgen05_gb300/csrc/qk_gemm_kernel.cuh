@@ -182,8 +182,8 @@ struct GemmCfg {
 
   // Ring-slot arrivals: the producer's, plus (MX) the scale warp's; in a CTA
   // pair each CTA stages the scale factors of its own 128 rows of A and of all
-  // BN rows of B at the same offsets, and both scale warps arrive on the
-  // leader's barrier.
+  // BN rows of B at the same offsets, and the leader's barrier counts its own
+  // scale warp and the peer's relay.
   static constexpr uint32_t FULL_ARRIVALS = 1 + (MX ? (PAIR ? 2 : 1) : 0);
 
   // kind::f16: D fp32 (1), A/B f16 (0).  kind::f8f6f4: A/B E4M3 (0).
@@ -444,15 +444,13 @@ __device__ __forceinline__ void raw_fetch_async(const GemmParams& p, uint32_t ra
 // rearranges each stage's scale bytes into the 512-byte atoms tcgen05.cp
 // reads.  Shared loads and stores are 16 bytes per lane over contiguous
 // 512-byte spans (no bank conflicts).
-// Marks a ring slot's scale atoms as written: on the local full barrier, or in
-// a CTA pair on the leader's (given by its cluster address).
+// Marks a ring slot's scale atoms as written, on this CTA's full barrier.  In
+// a CTA pair the peer's barrier is a local gather that the peer's relay warp
+// forwards to the leader's with one cluster-scope arrive per slot, so the
+// scale warp itself never waits on a cluster-wide fence.
 template <class C>
-__device__ __forceinline__ void scale_slot_ready(uint64_t* full, uint32_t full_leader, int stage) {
-  if constexpr (C::PAIR) {
-    mbar_arrive_cluster(full_leader + 8u * static_cast<uint32_t>(stage));
-  } else {
-    mbar_arrive(&full[stage]);
-  }
+__device__ __forceinline__ void scale_slot_ready(uint64_t* full, uint32_t /*full_leader*/, int stage) {
+  mbar_arrive(&full[stage]);
 }
 
 template <class C>
@@ -631,13 +629,17 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
   if (threadIdx.x == 0) {
 #pragma unroll 1
     for (int s = 0; s < C::STAGES; ++s) {
-      mbar_init(&full[s], C::FULL_ARRIVALS);
+      // a pair's peer counts only its own scale warp (forwarded by its relay)
+      mbar_init(&full[s], C::PAIR && !leader ? 1u : C::FULL_ARRIVALS);
       mbar_init(&empty[s], C::MCAST ? 2u : 1u);  // with B multicast both CTAs' MMAs release a slot
     }
 #pragma unroll 1
     for (int a = 0; a < C::ACC_BUFS; ++a) {
       mbar_init(&acc_full[a], 1u);
-      mbar_init(&acc_empty[a], static_cast<uint32_t>(C::EPI_WARPS * (C::PAIR ? 2 : 1)));
+      // A pair's epilogue warps arrive on their own CTA's barrier; the peer's
+      // relay thread forwards the peer's completion to the leader, whose
+      // barrier therefore counts its own warps plus one relay arrival.
+      mbar_init(&acc_empty[a], static_cast<uint32_t>(C::EPI_WARPS + (C::PAIR && leader ? 1 : 0)));
     }
     mbar_init(drain, 1u);
 #pragma unroll 1
@@ -865,6 +867,26 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
           break;
         }
       }
+    } else if (C::PAIR && lane == 0) {
+      // ---------------- accumulator relay (the peer CTA of a pair) ----------------
+      // Once all of this CTA's epilogue warps have drained an accumulator,
+      // tell the leader's MMA issuer with one cluster-scope arrive.
+      const uint32_t acc_empty_leader = mapa_shared(smem_u32(&acc_empty[0]), 0u);
+      uint32_t acc_iter = 0;
+      bool ok = true;
+#pragma unroll 1
+      for (int t = tile0; ok && t < p.num_tiles; t += tile_step) {
+#pragma unroll 1
+        for (int c = 0; c < p.num_chunks; ++c) {
+          const int a = static_cast<int>(acc_iter % C::ACC_BUFS);
+          if (!mbar_wait(&acc_empty[a], (acc_iter / C::ACC_BUFS) & 1u, w, kSiteMmaAccEmpty)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_cluster(acc_empty_leader + 8u * static_cast<uint32_t>(a));
+          ++acc_iter;
+        }
+      }
     }
     __syncwarp();
   } else if (warp == 2) {
@@ -876,6 +898,32 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                             full_leader);
       } else {
         scale_stager_ldg<C>(p, smem, full, empty, w, lane, tile0, tile_step, rank, full_leader);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 3) {
+    // ---------------- scale relay (the peer CTA of an MX pair) ----------------
+    if constexpr (C::MX && C::PAIR) {
+      if (!leader && lane == 0) {
+        const uint32_t full_leader = mapa_shared(smem_u32(&full[0]), 0u);
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+#pragma unroll 1
+        for (int t = tile0; ok && t < p.num_tiles; t += tile_step) {
+#pragma unroll 1
+          for (int kb = 0; kb < p.num_kb; ++kb) {
+            if (!mbar_wait(&full[stage], phase, w, kSiteScaleEmpty)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_cluster(full_leader + 8u * static_cast<uint32_t>(stage));
+            if (++stage == C::STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+        }
       }
     }
     __syncwarp();
@@ -894,17 +942,12 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
     float alpha = 1.f;  // NVFP4: product of the per-tensor scales, one fp32 rounding
     if constexpr (C::ALPHA) alpha = __fmul_rn(p.ga ? __ldg(p.ga) : 1.f, p.gb ? __ldg(p.gb) : 1.f);
     // accumulator releases go to the leader CTA's barrier
-    const uint32_t acc_empty_leader = C::PAIR ? mapa_shared(smem_u32(&acc_empty[0]), 0u) : 0u;
+    // accumulator releases go to this CTA's barrier (cluster-scope arrives,
+    // which fence, are left to the peer's single relay thread)
     auto release = [&](int a) {
       tc_fence_before_sync();
       __syncwarp();
-      if (lane == 0) {
-        if constexpr (C::PAIR) {
-          mbar_arrive_cluster(acc_empty_leader + 8u * static_cast<uint32_t>(a));
-        } else {
-          mbar_arrive(&acc_empty[a]);
-        }
-      }
+      if (lane == 0) mbar_arrive(&acc_empty[a]);
     };
 #pragma unroll 1
     for (int t = tile0; ok && t < p.num_tiles; t += tile_step) {
@@ -954,10 +997,6 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
           // chunk c is K-block c: sums += partial * (sa[m, c] * sb[n / 128, c]);
           // this thread's columns lie in one 128-column block of B
           const float scale = __fmul_rn(sa_next, sb_next);
-          if (c + 1 < p.num_chunks) {  // next K-block's scales, loaded ahead
-            sa_next = row_ok ? __ldg(p.sa + static_cast<size_t>(m) * p.scale_kb + c + 1) : 0.f;
-            sb_next = col_in ? __ldg(p.sb + static_cast<size_t>(n_tile >> 7) * p.scale_kb + c + 1) : 0.f;
-          }
           if constexpr (C::EPI_COLS == 32) {
             uint32_t v[32];
             tmem_ld_32cols(acc_col, v);
@@ -981,6 +1020,10 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
             }
           }
           release(a);
+          if (c + 1 < p.num_chunks) {  // next K-block's scales, issued after the release
+            sa_next = row_ok ? __ldg(p.sa + static_cast<size_t>(m) * p.scale_kb + c + 1) : 0.f;
+            sb_next = col_in ? __ldg(p.sb + static_cast<size_t>(n_tile >> 7) * p.scale_kb + c + 1) : 0.f;
+          }
           if (last) {
             emit(EmitTag<false, 0>{}, n_tile, sums);
             if constexpr (C::EPI_COLS == 64) emit(EmitTag<false, 32>{}, n_tile + 32, sums);
