@@ -101,13 +101,18 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+# the sources the headline INT8 GEMM (widening pass + f16-pipe kernel) is built from
+HEADLINE_SOURCES = ("qk_api.cu", "qk_device.cuh", "qk_gemm_kernel.cuh", "qk_int8.cu", "qk_int8_exact.cuh",
+                    "qk_internal.h", "qk_launch.cuh")
+
+
 def kernel_source_hash() -> str:
+    """Hash of the headline kernel's sources: a committed DRAM-traffic figure counts only while it matches."""
     h = hashlib.sha1()
-    for name in sorted(os.listdir(CSRC)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(CSRC, name), "rb") as f:
-                h.update(name.encode())
-                h.update(f.read())
+    for path in [os.path.join(CSRC, n) for n in HEADLINE_SOURCES] + [os.path.join(ROOT, "include", "qk.h")]:
+        with open(path, "rb") as f:
+            h.update(os.path.basename(path).encode())
+            h.update(f.read())
     return h.hexdigest()[:16]
 
 

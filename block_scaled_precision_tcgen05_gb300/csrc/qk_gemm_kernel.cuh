@@ -931,7 +931,6 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
     // ---------------- epilogue ----------------
     const int q = warp & 3;                          // TMEM lane quarter of this warp
     const int part = (warp - 4) >> 2;                // which EPI_COLS-wide column part
-    const int r = q * 32 + lane;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16);
     const int col_part = part * C::EPI_COLS;
     OutStager ostg{smem_u32(smem + C::OFF_OUT) +
