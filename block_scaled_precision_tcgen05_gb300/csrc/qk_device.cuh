@@ -171,6 +171,14 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
+// Arrive on another CTA's barrier with the default (CTA-scope) release: no
+// cluster-wide fence.  For signals that carry no memory the receiver reads,
+// such as "my tcgen05.ld reads of an accumulator have completed" (guaranteed
+// by tcgen05.wait::ld before the arrive).
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
 // ---------------------------------------------------------------------------
 // TMA (cp.async.bulk.tensor) and proxy fences
 // ---------------------------------------------------------------------------
@@ -181,6 +189,16 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
           smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1)
       : "memory");
+}
+
+// Prefetch a box into L2 (no shared memory, no barrier): raises the number of
+// DRAM requests in flight beyond what the shared-memory ring holds.
+// Out-of-range boxes fetch nothing.
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int32_t c0, int32_t c1) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1)
+               : "memory");
 }
 
 // Multicast form: the box lands at the same offset in the shared memory of

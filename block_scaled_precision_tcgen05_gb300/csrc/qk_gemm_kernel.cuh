@@ -870,7 +870,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
     } else if (C::PAIR && lane == 0) {
       // ---------------- accumulator relay (the peer CTA of a pair) ----------------
       // Once all of this CTA's epilogue warps have drained an accumulator,
-      // tell the leader's MMA issuer with one cluster-scope arrive.
+      // tell the leader's MMA issuer with one remote arrive.
       const uint32_t acc_empty_leader = mapa_shared(smem_u32(&acc_empty[0]), 0u);
       uint32_t acc_iter = 0;
       bool ok = true;
@@ -883,7 +883,9 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
             ok = false;
             break;
           }
-          mbar_arrive_cluster(acc_empty_leader + 8u * static_cast<uint32_t>(a));
+          // CTA-scope release: the drained accumulator carries no data the
+          // leader reads, and tcgen05.wait::ld already completed the reads
+          mbar_arrive_remote(acc_empty_leader + 8u * static_cast<uint32_t>(a));
           ++acc_iter;
         }
       }
@@ -941,8 +943,8 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
     float alpha = 1.f;  // NVFP4: product of the per-tensor scales, one fp32 rounding
     if constexpr (C::ALPHA) alpha = __fmul_rn(p.ga ? __ldg(p.ga) : 1.f, p.gb ? __ldg(p.gb) : 1.f);
     // accumulator releases go to the leader CTA's barrier
-    // accumulator releases go to this CTA's barrier (cluster-scope arrives,
-    // which fence, are left to the peer's single relay thread)
+    // accumulator releases go to this CTA's barrier (the arrive on the
+    // leader's barrier is left to the peer's single relay thread)
     auto release = [&](int a) {
       tc_fence_before_sync();
       __syncwarp();
