@@ -191,16 +191,6 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
       : "memory");
 }
 
-// Prefetch a box into L2 (no shared memory, no barrier): raises the number of
-// DRAM requests in flight beyond what the shared-memory ring holds.
-// Out-of-range boxes fetch nothing.
-__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int32_t c0, int32_t c1) {
-  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
-                   reinterpret_cast<uint64_t>(map)),
-               "r"(c0), "r"(c1)
-               : "memory");
-}
-
 // Multicast form: the box lands at the same offset in the shared memory of
 // every CTA of cta_mask, and each of them counts its bytes on its own mbarrier
 // at the offset of `bar`.
