@@ -48,8 +48,9 @@ def test_mx_quantize_matches_oracle(fmt):
         [(int(r), int(c), hex(int(got[r, c])), hex(int(ref_codes[r, c]))) for r, c in bad[:6]])
 
 
-def test_ptpc_quantize_matches_oracle():
-    rows, K = 41, 2048
+@pytest.mark.parametrize("rows,K", [(41, 2048), (6, 16400)], ids=["row-in-registers", "row-read-twice"])
+def test_ptpc_quantize_matches_oracle(rows, K):
+    # rows up to 16384 elements stay in registers between the two passes; longer rows are read twice
     bits, x = _inputs(rows, K, 9)
     x[5] = 0.0                           # an all-zero row takes scale 1
     bits[5] = 0
