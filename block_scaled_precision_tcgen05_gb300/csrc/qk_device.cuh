@@ -402,6 +402,17 @@ __device__ __forceinline__ void umma_mxf4_pair(uint32_t d_tmem, uint64_t a_desc,
       : "memory");
 }
 
+__device__ __forceinline__ void umma_nvf4_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                               uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
+      : "memory");
+}
+
 // Arrives once on `bar` when every tcgen05 operation this thread issued so far
 // (MMAs, copies) has completed.
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {

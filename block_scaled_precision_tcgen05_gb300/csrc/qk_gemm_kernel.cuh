@@ -815,9 +815,13 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                   }
                 } else if constexpr (C::kind == Kind::NVF4) {
                   // four UE4M3 scale bytes (one per 16 K) per row per MMA: all of column group j
-                  static_assert(!C::PAIR, "NVFP4 runs on one CTA");
-                  umma_nvf4(d_tmem, ad, bd, C::idesc(0, 0), sf_tmem + 4 * j, sf_tmem + C::SF_COLS_A + 4 * C::NB128 * j,
-                            accum);
+                  if constexpr (C::PAIR) {
+                    umma_nvf4_pair(d_tmem, ad, bd, C::idesc(0, 0), sf_tmem + 4 * j,
+                                   sf_tmem + C::SF_COLS_A + 4 * C::NB128 * j, accum);
+                  } else {
+                    umma_nvf4(d_tmem, ad, bd, C::idesc(0, 0), sf_tmem + 4 * j,
+                              sf_tmem + C::SF_COLS_A + 4 * C::NB128 * j, accum);
+                  }
                 } else {
                   // two scale bytes per row per MMA: bytes 2(j%2), 2(j%2)+1 of column group j/2
                   const uint32_t g = static_cast<uint32_t>(j >> 1);
@@ -919,7 +923,11 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
               ok = false;
               break;
             }
-            mbar_arrive_cluster(full_leader + 8u * static_cast<uint32_t>(stage));
+            // CTA-scope release, no cluster-wide fence: the atoms stay in this
+            // CTA's shared memory, where the scale warp's fence.proxy.async and
+            // its completed local arrive (observed above) have already put them
+            // for the leader's copy to read.
+            mbar_arrive_remote(full_leader + 8u * static_cast<uint32_t>(stage));
             if (++stage == C::STAGES) {
               stage = 0;
               phase ^= 1u;

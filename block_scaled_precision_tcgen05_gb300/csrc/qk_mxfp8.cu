@@ -16,6 +16,8 @@ using CfgMxfp8Single = GemmCfg<Kind::MXF8, 256, 4, 1, false, 4, 1>;
 using CfgMxfp8Pair = GemmCfg<Kind::MXF8, 256, 5, 1, true, 8, 2>;
 using CfgMxfp8Mcast = GemmCfg<Kind::MXF8, 256, 4, 1, false, 4, 1, true>;
 using CfgMxfp8Double = GemmCfg<Kind::MXF8, 224, 4, 2, false, 4, 2>;
+// Variant 6: a CTA pair with two accumulators (224 columns each) beside the scale ring.
+using CfgMxfp8PairDouble = GemmCfg<Kind::MXF8, 224, 5, 2, true, 4, 2>;
 
 template <class C>
 static int launch_mxfp8_cfg(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const uint8_t* sB,
@@ -54,6 +56,7 @@ int launch_mxfp8(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const ui
   if (v == 1) return launch_mxfp8_cfg<CfgMxfp8Pair>(A, sA, B, sB, bias, out, M, N, K, dev, stream);
   if (v == 2) return launch_mxfp8_cfg<CfgMxfp8Mcast>(A, sA, B, sB, bias, out, M, N, K, dev, stream);
   if (v == 3) return launch_mxfp8_cfg<CfgMxfp8Single>(A, sA, B, sB, bias, out, M, N, K, dev, stream);
+  if (v == 6) return launch_mxfp8_cfg<CfgMxfp8PairDouble>(A, sA, B, sB, bias, out, M, N, K, dev, stream);
   return launch_mxfp8_cfg<CfgMxfp8Double>(A, sA, B, sB, bias, out, M, N, K, dev, stream);
 }
 
