@@ -116,7 +116,10 @@ struct GemmCfg {
   static constexpr int EPI_WARPS = EPI_WARPS_;
   static constexpr int EPI_PARTS = EPI_WARPS / 4;     // column parts of a tile
   static constexpr int EPI_COLS = BN_ / EPI_PARTS;    // columns per epilogue warp
-  static constexpr bool REG_SUMS = (INT_CHUNKS || BLOCKSCALE) && EPI_WARPS == 16;
+  // 16 epilogue warps hold 64 columns per thread in registers: the exact
+  // INT8 and blockscale kinds keep running sums there; the block-scaled kinds
+  // drain the accumulator into them and release it before the epilogue math.
+  static constexpr bool REG_SUMS = (INT_CHUNKS || BLOCKSCALE || MX) && EPI_WARPS == 16;
 
   static constexpr int SF_PER_STAGE = MX ? K_ELEMS / SF_BLOCK : 0;  // scale bytes per row per stage
   static constexpr int SF_ATOMS_K = SF_PER_STAGE / 4;         // 4 scale bytes per 32-bit TMEM column
@@ -1002,7 +1005,17 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
             epilogue_row32_global<C::ROWWISE || kInt, kInt, kOff, C::ALPHA>(p, m, n0, sam, vals);
           }
         };
-        if constexpr (C::REG_SUMS && C::BLOCKSCALE) {
+        if constexpr (C::REG_SUMS && C::MX) {
+          // one chunk per tile: four TMEM loads in flight, one wait, release the
+          // accumulator, then the epilogue from registers while the MMAs go on
+#pragma unroll
+          for (int g = 0; g < C::EPI_COLS / 16; ++g)
+            tmem_ld_16cols(acc_col + 16 * g, *reinterpret_cast<uint32_t(*)[16]>(&sums[16 * g]));
+          tmem_wait_ld();
+          release(a);
+          emit(EmitTag<false, 0>{}, n_tile, sums);
+          emit(EmitTag<false, 32>{}, n_tile + 32, sums);
+        } else if constexpr (C::REG_SUMS && C::BLOCKSCALE) {
           // chunk c is K-block c: sums += partial * (sa[m, c] * sb[n / 128, c]);
           // this thread's columns lie in one 128-column block of B
           const float scale = __fmul_rn(sa_next, sb_next);

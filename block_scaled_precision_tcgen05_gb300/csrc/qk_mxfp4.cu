@@ -7,21 +7,17 @@
 namespace qk {
 
 // Default: 256 x 256 tiles on a 2-SM CTA pair (each SM loads half of B: 32 KB
-// of operands per 256-K stage instead of 48), five stages, one accumulator.
-// Each CTA stages its own A scales and all of B's; the peer's relay warp
-// forwards each slot to the leader, whose cta_group::2 copies fill both CTAs'
-// TMEM.  4540-4790 TFLOP/s against 4330-4560 for the one-CTA 128 x 256
-// kernel (variant 4).  Variants 2 (B multicast), 3 (one CTA, two 192-column
-// accumulators) and 6 (a pair with two 192-column accumulators) are slower.
-using CfgMxfp4Single = GemmCfg<Kind::MXF4, 256, 4, 1, false, 4, 1>;
+// of operands per 256-K stage instead of 48), five stages, one accumulator
+// that 16 epilogue warps drain into registers (64 columns each) and release
+// before the epilogue math, so the next tile's MMAs start after the drain:
+// 4430-4940 TFLOP/s.  Each CTA stages its own A scales and all of B's; the
+// peer's relay warp forwards each slot to the leader, whose cta_group::2
+// copies fill both CTAs' TMEM.  Variant 1: the same pair with 8 epilogue
+// warps working from TMEM (4100-4780).  Variant 4: one CTA, 128 x 256
+// (3830-4560).
+using CfgMxfp4PairDrain = GemmCfg<Kind::MXF4, 256, 5, 1, true, 16, 1>;
 using CfgMxfp4Pair = GemmCfg<Kind::MXF4, 256, 5, 1, true, 8, 2>;
-using CfgMxfp4Mcast = GemmCfg<Kind::MXF4, 256, 4, 1, false, 4, 1, true>;
-// 192-column tiles leave TMEM room for two accumulators beside the scale
-// ring (variant 3), but at the FP4 rate the operand bytes per flop decide:
-// 3650 against 4400 TFLOP/s for one-CTA 128 x 256 tiles.
-using CfgMxfp4Double = GemmCfg<Kind::MXF4, 192, 4, 2, false, 4, 2>;
-// Variant 6: a CTA pair with two accumulators (192 columns each) beside the scale ring.
-using CfgMxfp4PairDouble = GemmCfg<Kind::MXF4, 192, 5, 2, true, 8, 2>;
+using CfgMxfp4Single = GemmCfg<Kind::MXF4, 256, 4, 1, false, 4, 1>;
 
 template <class C>
 static int launch_mxfp4_cfg(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const uint8_t* sB,
@@ -58,11 +54,9 @@ static int launch_mxfp4_cfg(const uint8_t* A, const uint8_t* sA, const uint8_t* 
 int launch_mxfp4(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const uint8_t* sB, const uint16_t* bias,
                  uint16_t* out, int M, int N, int K, const DeviceInfo& dev, cudaStream_t stream) {
   const int v = kernel_variant("QK_MX_VARIANT");
+  if (v == 1) return launch_mxfp4_cfg<CfgMxfp4Pair>(A, sA, B, sB, bias, out, M, N, K, dev, stream);
   if (v == 4) return launch_mxfp4_cfg<CfgMxfp4Single>(A, sA, B, sB, bias, out, M, N, K, dev, stream);
-  if (v == 2) return launch_mxfp4_cfg<CfgMxfp4Mcast>(A, sA, B, sB, bias, out, M, N, K, dev, stream);
-  if (v == 3) return launch_mxfp4_cfg<CfgMxfp4Double>(A, sA, B, sB, bias, out, M, N, K, dev, stream);
-  if (v == 6) return launch_mxfp4_cfg<CfgMxfp4PairDouble>(A, sA, B, sB, bias, out, M, N, K, dev, stream);
-  return launch_mxfp4_cfg<CfgMxfp4Pair>(A, sA, B, sB, bias, out, M, N, K, dev, stream);
+  return launch_mxfp4_cfg<CfgMxfp4PairDrain>(A, sA, B, sB, bias, out, M, N, K, dev, stream);
 }
 
 }  // namespace qk

@@ -6,18 +6,17 @@
 
 namespace qk {
 
-// Default: 128 x 224 tiles on one CTA with two TMEM accumulators (448
-// columns) beside the 4-slot scale ring (48 columns), so each tile's
-// epilogue overlaps the next tile's MMAs: 2380-2575 TFLOP/s against
-// 1780-2270 for 128 x 256 tiles with one accumulator, whose epilogue stalls
-// the MMAs (variant 3).  Variants 1 (256 x 256 on a CTA pair) and 2 (B
-// multicast across a cluster of two) keep one accumulator and are slower.
-using CfgMxfp8Single = GemmCfg<Kind::MXF8, 256, 4, 1, false, 4, 1>;
-using CfgMxfp8Pair = GemmCfg<Kind::MXF8, 256, 5, 1, true, 8, 2>;
-using CfgMxfp8Mcast = GemmCfg<Kind::MXF8, 256, 4, 1, false, 4, 1, true>;
+// Default: 256 x 256 tiles on a 2-SM CTA pair, five stages, one accumulator
+// drained by 16 epilogue warps into registers (64 columns each) and released
+// before the epilogue math: 2500-2510 TFLOP/s.  Variant 4: one CTA with
+// 128 x 224 tiles and two TMEM accumulators (448 columns) beside the 4-slot
+// scale ring, so each tile's epilogue overlaps the next tile's MMAs
+// (2370-2400).  Variant 1: the pair with 8 epilogue warps working from TMEM
+// (2010-2060).  One CTA with 128 x 256 tiles and one accumulator, whose
+// epilogue stalls the MMAs, measured 1780-2270.
+using CfgMxfp8PairDrain = GemmCfg<Kind::MXF8, 256, 5, 1, true, 16, 1>;
 using CfgMxfp8Double = GemmCfg<Kind::MXF8, 224, 4, 2, false, 4, 2>;
-// Variant 6: a CTA pair with two accumulators (224 columns each) beside the scale ring.
-using CfgMxfp8PairDouble = GemmCfg<Kind::MXF8, 224, 5, 2, true, 4, 2>;
+using CfgMxfp8Pair = GemmCfg<Kind::MXF8, 256, 5, 1, true, 8, 2>;
 
 template <class C>
 static int launch_mxfp8_cfg(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const uint8_t* sB,
@@ -54,10 +53,8 @@ int launch_mxfp8(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const ui
                  uint16_t* out, int M, int N, int K, const DeviceInfo& dev, cudaStream_t stream) {
   const int v = kernel_variant("QK_MX_VARIANT");
   if (v == 1) return launch_mxfp8_cfg<CfgMxfp8Pair>(A, sA, B, sB, bias, out, M, N, K, dev, stream);
-  if (v == 2) return launch_mxfp8_cfg<CfgMxfp8Mcast>(A, sA, B, sB, bias, out, M, N, K, dev, stream);
-  if (v == 3) return launch_mxfp8_cfg<CfgMxfp8Single>(A, sA, B, sB, bias, out, M, N, K, dev, stream);
-  if (v == 6) return launch_mxfp8_cfg<CfgMxfp8PairDouble>(A, sA, B, sB, bias, out, M, N, K, dev, stream);
-  return launch_mxfp8_cfg<CfgMxfp8Double>(A, sA, B, sB, bias, out, M, N, K, dev, stream);
+  if (v == 4) return launch_mxfp8_cfg<CfgMxfp8Double>(A, sA, B, sB, bias, out, M, N, K, dev, stream);
+  return launch_mxfp8_cfg<CfgMxfp8PairDrain>(A, sA, B, sB, bias, out, M, N, K, dev, stream);
 }
 
 }  // namespace qk

@@ -8,14 +8,15 @@
 
 namespace qk {
 
-// Default: 256 x 256 tiles on a 2-SM CTA pair, five stages, one accumulator
-// (3270-3430 TFLOP/s).  Variant 4: 128 x 256 tiles on one CTA; the 16 scale
-// bytes per row per stage take 6 KB of shared memory and 48 TMEM columns per
-// slot, so three stages fit (3180-3330).  Variant 3: 128 x 128 tiles with two
-// accumulators.
-using CfgNvfp4Single = GemmCfg<Kind::NVF4, 256, 3, 1, false, 4, 1>;
-using CfgNvfp4Double = GemmCfg<Kind::NVF4, 128, 4, 2, false, 4, 2>;
+// Default: 256 x 256 tiles on a 2-SM CTA pair, four stages, one accumulator
+// drained by 16 epilogue warps into registers and released before the
+// epilogue math (3400-3580 TFLOP/s).  Variant 1: the pair with five stages
+// and 8 epilogue warps working from TMEM (3260-3430).  Variant 4: 128 x 256
+// tiles on one CTA; the 16 scale bytes per row per stage take 6 KB of shared
+// memory and 48 TMEM columns per slot, so three stages fit (3180-3330).
+using CfgNvfp4PairDrain = GemmCfg<Kind::NVF4, 256, 4, 1, true, 16, 1>;
 using CfgNvfp4Pair = GemmCfg<Kind::NVF4, 256, 5, 1, true, 8, 1>;
+using CfgNvfp4Single = GemmCfg<Kind::NVF4, 256, 3, 1, false, 4, 1>;
 
 template <class C>
 static int launch_nvfp4_cfg(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const uint8_t* sB,
@@ -78,7 +79,7 @@ extern "C" int qk_gemm_nvfp4(const uint8_t* A, const uint8_t* sA, const uint8_t*
   const auto s = static_cast<cudaStream_t>(stream);
   const int m = static_cast<int>(M), n = static_cast<int>(N), k = static_cast<int>(K);
   const int v = kernel_variant("QK_MX_VARIANT");
-  if (v == 3) return launch_nvfp4_cfg<CfgNvfp4Double>(A, sA, B, sB, ga, gb, bias, out, m, n, k, *dev, s);
+  if (v == 1) return launch_nvfp4_cfg<CfgNvfp4Pair>(A, sA, B, sB, ga, gb, bias, out, m, n, k, *dev, s);
   if (v == 4) return launch_nvfp4_cfg<CfgNvfp4Single>(A, sA, B, sB, ga, gb, bias, out, m, n, k, *dev, s);
-  return launch_nvfp4_cfg<CfgNvfp4Pair>(A, sA, B, sB, ga, gb, bias, out, m, n, k, *dev, s);
+  return launch_nvfp4_cfg<CfgNvfp4PairDrain>(A, sA, B, sB, ga, gb, bias, out, m, n, k, *dev, s);
 }
