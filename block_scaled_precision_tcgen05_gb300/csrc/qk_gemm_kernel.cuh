@@ -78,17 +78,12 @@ struct GemmParams {
 // thread) instead of TMEM, which frees TMEM for two accumulators.
 // OUT_BUFS_: shared-memory staging blocks per epilogue warp for bulk tensor
 // stores of the output; 0 = the epilogue stores straight to global memory.
-// MCAST_: a cluster of two CTAs, each computing its own 128 x BN tile with
-// one-CTA MMAs, shares the B tile: each CTA loads half of it and multicasts
-// that half into both CTAs' shared memory (a ring slot is refilled once both
-// CTAs' MMAs have released it).
 template <Kind KIND, int BN_, int STAGES_, int ACC_BUFS_, bool PAIR_ = false, int EPI_WARPS_ = 4,
-          int OUT_BUFS_ = 2, bool MCAST_ = false>
+          int OUT_BUFS_ = 2>
 struct GemmCfg {
   static constexpr Kind kind = KIND;
   static constexpr bool PAIR = PAIR_;
-  static constexpr bool MCAST = MCAST_;
-  static constexpr int CTAS = (PAIR || MCAST) ? 2 : 1;  // CTAs of a cluster
+  static constexpr int CTAS = PAIR ? 2 : 1;  // CTAs of a cluster
   static constexpr int BM = 128;                 // rows of A (and D) per CTA
   static constexpr int TILE_M = BM * CTAS;       // rows of a cluster's tile
   static constexpr int MMA_M = PAIR ? 256 : 128; // rows of one MMA
@@ -131,7 +126,7 @@ struct GemmCfg {
   static constexpr int A_BYTES = BM * ROW_BYTES;
   static constexpr int B_BYTES = B_ROWS * ROW_BYTES;
   // bytes a ring stage's full barrier counts: a pair's leader counts both CTAs'
-  // loads; with B multicast each CTA receives its A and both halves of B
+  // loads
   static constexpr uint32_t STAGE_TX = PAIR ? 2 * (A_BYTES + B_BYTES) : A_BYTES + B_BYTES;
 
   // Raw scale rows fetched by TMA: 16 bytes (16 scales) per row per fetch,
@@ -178,7 +173,6 @@ struct GemmCfg {
   static_assert(!REG_SUMS || EPI_COLS == 64 || (BLOCKSCALE && EPI_COLS == 32),
                 "register sums hold 64 columns per thread (32 for blockscale)");
   static_assert(!BLOCKSCALE || REG_SUMS, "blockscale sums live in registers");
-  static_assert(!(PAIR && MCAST), "one cluster mode");
   static_assert(COLS_USED <= 512, "TMEM budget");
   static_assert(SMEM_BYTES <= 232448, "shared-memory budget");
   static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "swizzle atoms need 1024-byte alignment");
@@ -623,7 +617,6 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
   const int lane = threadIdx.x & 31;
   const uint32_t rank = C::CTAS > 1 ? cluster_ctarank() : 0u;  // CTA within the cluster
   const bool leader = rank == 0u;                           // a pair's MMA issuer
-  // a pair issues its MMAs from the leader; multicast CTAs each issue their own
   const bool issues_mma = C::PAIR ? leader : true;
   // tiles are walked per cluster (one CTA or a pair)
   const int tile0 = static_cast<int>(blockIdx.x) / C::CTAS;
@@ -634,7 +627,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
     for (int s = 0; s < C::STAGES; ++s) {
       // a pair's peer counts only its own scale warp (forwarded by its relay)
       mbar_init(&full[s], C::PAIR && !leader ? 1u : C::FULL_ARRIVALS);
-      mbar_init(&empty[s], C::MCAST ? 2u : 1u);  // with B multicast both CTAs' MMAs release a slot
+      mbar_init(&empty[s], 1u);
     }
 #pragma unroll 1
     for (int a = 0; a < C::ACC_BUFS; ++a) {
@@ -699,12 +692,6 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
             const uint32_t fb = full_leader + 8u * static_cast<uint32_t>(stage);
             tma_load_2d_pair(smem + C::OFF_A + stage * C::A_BYTES, &tmA, fb, kb * C::TMA_K, a_row);
             tma_load_2d_pair(smem + C::OFF_B + stage * C::B_BYTES, &tmB, fb, kb * C::TMA_K, b_row);
-          } else if constexpr (C::MCAST) {
-            mbar_arrive_expect_tx(&full[stage], C::STAGE_TX);
-            tma_load_2d(smem + C::OFF_A + stage * C::A_BYTES, &tmA, &full[stage], kb * C::TMA_K, a_row);
-            // this CTA's half of B, into both CTAs at the half's offset
-            tma_load_2d_multicast(smem + C::OFF_B + stage * C::B_BYTES + rank * (C::B_LOAD_ROWS * C::ROW_BYTES), &tmB,
-                                  &full[stage], kb * C::TMA_K, b_row, 0x3);
           } else {
             mbar_arrive_expect_tx(&full[stage], C::STAGE_TX);
             tma_load_2d(smem + C::OFF_A + stage * C::A_BYTES, &tmA, &full[stage], kb * C::TMA_K, a_row);
@@ -841,8 +828,6 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
             }
             if constexpr (C::PAIR) {
               umma_commit_pair_multicast(&empty[stage], 0x3);  // frees the slot in both CTAs
-            } else if constexpr (C::MCAST) {
-              umma_commit_multicast(&empty[stage], 0x3);  // both CTAs' producers refill this slot
             } else {
               umma_commit(&empty[stage]);
             }
