@@ -14,6 +14,11 @@ namespace qk {
 // tensor stores (with K as short as 1792 the epilogue sets the pace: 4 warps
 // storing straight to global memory reach 0.55 of this configuration's rate).
 using CfgFp8 = GemmCfg<Kind::F8, 256, 6, 2, true, 8, 1>;
+// With K <= 2048 a tile's MMAs take about as long as its epilogue, so 16
+// epilogue warps drain each accumulator into registers and release it before
+// the epilogue math: 2945 / 3068 TFLOP/s against 2840 / 3026 at K = 1792
+// (and 1% slower than CfgFp8 at K = 5376 and 8192).
+using CfgFp8Drain = GemmCfg<Kind::F8, 256, 6, 2, true, 16, 1>;
 
 template <class C>
 static int launch_fp8_cfg(const uint8_t* A, const uint8_t* B, const float* sa, const float* sb, const uint16_t* bias,
@@ -201,6 +206,7 @@ int launch_fp8_rowwise(const uint8_t* A, const uint8_t* B, const float* sa, cons
   const int v = kernel_variant("QK_FP8_SKINNY");
   if (M <= 64 && v != 1) return launch_skinny<64>(A, B, sa, sb, bias, out, M, N, K, dev, stream, v);
   if (M <= 128 && v != 1) return launch_skinny<128>(A, B, sa, sb, bias, out, M, N, K, dev, stream, v);
+  if (K <= 2048) return launch_fp8_cfg<CfgFp8Drain>(A, B, sa, sb, bias, out, M, N, K, dev, stream);
   return launch_fp8_cfg<CfgFp8>(A, B, sa, sb, bias, out, M, N, K, dev, stream);
 }
 

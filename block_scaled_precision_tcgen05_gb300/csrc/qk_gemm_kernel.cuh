@@ -114,7 +114,9 @@ struct GemmCfg {
   // 16 epilogue warps hold 64 columns per thread in registers: the exact
   // INT8 and blockscale kinds keep running sums there; the block-scaled kinds
   // drain the accumulator into them and release it before the epilogue math.
-  static constexpr bool REG_SUMS = (INT_CHUNKS || BLOCKSCALE || MX) && EPI_WARPS == 16;
+  static constexpr bool REG_SUMS = (INT_CHUNKS || BLOCKSCALE || MX || KIND == Kind::F8) && EPI_WARPS == 16;
+  // kinds whose one-chunk accumulator is drained into registers and released before the epilogue math
+  static constexpr bool REG_DRAIN = REG_SUMS && (MX || KIND == Kind::F8);
 
   static constexpr int SF_PER_STAGE = MX ? K_ELEMS / SF_BLOCK : 0;  // scale bytes per row per stage
   static constexpr int SF_ATOMS_K = SF_PER_STAGE / 4;         // 4 scale bytes per 32-bit TMEM column
@@ -990,7 +992,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
             epilogue_row32_global<C::ROWWISE || kInt, kInt, kOff, C::ALPHA>(p, m, n0, sam, vals);
           }
         };
-        if constexpr (C::REG_SUMS && C::MX) {
+        if constexpr (C::REG_DRAIN) {
           // one chunk per tile: four TMEM loads in flight, one wait, release the
           // accumulator, then the epilogue from registers while the MMAs go on
 #pragma unroll
