@@ -2,10 +2,9 @@
 // (ROCm/aiter PR #6262 gemm_a8w8_bpreshuffle semantics; ROCm/mori PR #806
 // "ptpc"), on tcgen05.mma kind::f8f6f4 with fp32 accumulation in TMEM.
 #include "qk_launch.cuh"
-#include <atomic>
 
 #include "qk_skinny_kernel.cuh"
-#include "qk_streamk_kernel.cuh"
+#include "qk_streamk_launch.cuh"
 
 namespace qk {
 
@@ -103,72 +102,19 @@ static int launch_skinny_cfg(const uint8_t* A, const uint8_t* B, const float* sa
   return QK_OK;
 }
 
-// Few rows (M <= 128): the stream-K weight-streaming kernel
-// (qk_streamk_kernel.cuh), one CTA per SM, launched cooperatively so that
-// all CTAs are resident while owners wait for their contributors' partials.
-// The partials and flags come from the stream-ordered workspace pool; each
-// call gets a fresh 64-bit epoch, so flags left in reused memory by earlier
-// calls (older epochs) never read as finished.
+// Few rows (M <= 128): the stream-K weight-streaming kernel in its FP8
+// per-token mode.
 std::atomic<unsigned long long> g_streamk_epoch{0};
 
 template <int MT>
 static int launch_streamk(const uint8_t* A, const uint8_t* B, const float* sa, const float* sb, const uint16_t* bias,
                           uint16_t* out, int M, int N, int K, const DeviceInfo& dev, cudaStream_t stream) {
-  using C = StreamKCfg<MT, MT <= 64 ? 8 : 6>;
-  auto kernel = qk_streamk_fp8_kernel<C>;
-  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) != cudaSuccess)
-    return QK_ERR_CUDA;
-  const int n_tiles = ceil_div(N, C::NT);
-  const int num_kb = ceil_div(K, C::K_ELEMS);
-  const long long units = static_cast<long long>(n_tiles) * num_kb;
-  const int G = static_cast<int>(units < dev.sm_count ? units : dev.sm_count);
-  CUtensorMap tw, ta;
-  int st = encode_tmap_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, K, N, K, C::K_ELEMS, C::NT);
-  if (st == QK_OK) st = encode_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, K, M, K, C::K_ELEMS, C::MT);
-  if (st != QK_OK) return st;
-  const size_t part_bytes = static_cast<size_t>(G) * C::MT * C::NT * sizeof(float);
-  void* ws = nullptr;
-  if (cudaMallocFromPoolAsync(&ws, part_bytes + static_cast<size_t>(G) * 4 * sizeof(unsigned long long), dev.pool,
-                              stream) != cudaSuccess) {
-    cudaGetLastError();
-    return QK_ERR_NOMEM;
-  }
   StreamKParams p{};
-  p.M = M;
-  p.N = N;
-  p.K = K;
-  p.num_kb = num_kb;
-  p.units = units;
   p.sa = sa;
   p.sb = sb;
   p.bias = bias;
   p.out = out;
-  p.partials = static_cast<float*>(ws);
-  p.flags = reinterpret_cast<unsigned long long*>(static_cast<uint8_t*>(ws) + part_bytes);
-  // a 64-bit value no earlier call used (odd multiplier: a bijection of the counter)
-  p.epoch = (g_streamk_epoch.fetch_add(1) + 1) * 0x9E3779B97F4A7C15ull;
-  p.err = dev.err_word;
-  p.timeout_ns = wait_timeout_ns();
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(G, 1, 1);
-  cfg.blockDim = dim3(C::NUM_THREADS, 1, 1);
-  cfg.dynamicSmemBytes = C::SMEM_BYTES;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  LaunchTimer timer(kKGemmFp8, stream);
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, tw, ta, p);
-  timer.done();
-  const cudaError_t f = cudaFreeAsync(ws, stream);
-  if (e != cudaSuccess || f != cudaSuccess) {
-    cudaGetLastError();
-    return QK_ERR_CUDA;
-  }
-  count_launches(1);
-  return QK_OK;
+  return launch_streamk_cfg<StreamKCfg<MT, MT <= 64 ? 8 : 6>>(A, B, p, M, N, K, kKGemmFp8, dev, stream);
 }
 
 // Few rows: if the weight tiles times some split S in {8, 4, 2, 1} fit on the

@@ -3,6 +3,7 @@
 // [rows, K/32] scale bytes (ROCm/mori PR #806, "What") are staged per ring
 // slot by the kernel's scale warp and moved to TMEM with tcgen05.cp.
 #include "qk_launch.cuh"
+#include "qk_streamk_launch.cuh"
 
 namespace qk {
 
@@ -49,9 +50,35 @@ static int launch_mxfp8_cfg(const uint8_t* A, const uint8_t* sA, const uint8_t* 
   return launch_gemm<C>(ta, tb, tsa, tsb, p, dev, stream);
 }
 
+// Few rows (M <= 128): the stream-K weight-streaming kernel in its MXFP8
+// mode, each SM streaming an equal share of the weight's 128 x 128 units.
+// It beats the tile kernel for M <= 64 once the weight holds about ten units
+// per SM: 43.7 against 49.3 us at 64 x 21504 x 5376, 21.8 against 24.5 at
+// 16 x 7168 x 4096; with fewer units (64 x 2112 x 7168: 42.7 against 33.0)
+// or 128 activation rows (128 x 21504 x 5376: 55.5 against 49.5) it loses.
+template <int MT>
+static int launch_mxfp8_streamk(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const uint8_t* sB,
+                                const uint16_t* bias, uint16_t* out, int M, int N, int K, const DeviceInfo& dev,
+                                cudaStream_t stream) {
+  StreamKParams p{};
+  p.sfa = sA;
+  p.sfw = sB;
+  p.sf_cols = K / 32;
+  p.bias = bias;
+  p.out = out;
+  return launch_streamk_cfg<StreamKCfg<MT, MT <= 64 ? 8 : 6, true>>(A, B, p, M, N, K, kKGemmMxfp8, dev, stream);
+}
+
 int launch_mxfp8(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const uint8_t* sB, const uint16_t* bias,
                  uint16_t* out, int M, int N, int K, const DeviceInfo& dev, cudaStream_t stream) {
   const int v = kernel_variant("QK_MX_VARIANT");
+  // QK_MX_SKINNY: 1 = always the tile kernel, 2 = stream-K whenever M <= 128
+  const int skinny = kernel_variant("QK_MX_SKINNY");
+  const long long units = static_cast<long long>(ceil_div(N, 128)) * ceil_div(K, 128);
+  if (M <= 128 && skinny != 1 && (skinny == 2 || (M <= 64 && units >= 10LL * dev.sm_count))) {
+    if (M <= 64) return launch_mxfp8_streamk<64>(A, sA, B, sB, bias, out, M, N, K, dev, stream);
+    return launch_mxfp8_streamk<128>(A, sA, B, sB, bias, out, M, N, K, dev, stream);
+  }
   if (v == 1) return launch_mxfp8_cfg<CfgMxfp8Pair>(A, sA, B, sB, bias, out, M, N, K, dev, stream);
   if (v == 4) return launch_mxfp8_cfg<CfgMxfp8Double>(A, sA, B, sB, bias, out, M, N, K, dev, stream);
   return launch_mxfp8_cfg<CfgMxfp8PairDrain>(A, sA, B, sB, bias, out, M, N, K, dev, stream);

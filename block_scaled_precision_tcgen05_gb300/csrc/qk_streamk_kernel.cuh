@@ -24,6 +24,14 @@
 // A contributor's segment is the first thing it computes and never waits on
 // another CTA, so the waits cannot form a cycle; the launch is cooperative,
 // which guarantees that all CTAs are resident at once.
+//
+// MXFP8 mode (MX_ = true): the MMAs are block-scaled (kind::mxf8f6f4,
+// scale_vec::1X).  With the operands swapped, the weight's UE8M0 scales are
+// the MMA's "A" scales and the activations' its "B" scales: per stage a
+// scale warp stages one 512-byte atom of each (128 weight rows, up to 128
+// activation rows; 4 scale bytes per row for the stage's 128 K), the MMA warp
+// copies both into the stage's TMEM slot, and the epilogue is bf16(acc
+// (+bias)) with no per-row scales.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -39,6 +47,9 @@ struct StreamKParams {
   long long units;            // n_tiles * num_kb
   const float* sa;
   const float* sb;
+  const uint8_t* sfa;         // MXFP8: activation UE8M0 scales [M, sf_cols]
+  const uint8_t* sfw;         // MXFP8: weight UE8M0 scales [N, sf_cols]
+  int sf_cols;                // K / 32
   const uint16_t* bias;
   uint16_t* out;
   float* partials;            // [gridDim.x][MT][128] fp32
@@ -48,8 +59,9 @@ struct StreamKParams {
   uint64_t timeout_ns;
 };
 
-template <int MT_, int STAGES_>
+template <int MT_, int STAGES_, bool MX_ = false>
 struct StreamKCfg {
+  static constexpr bool MX = MX_;         // MXFP8 block-scaled MMAs
   static constexpr int MT = MT_;          // padded activation rows (MMA N)
   static constexpr int NT = 128;          // weight rows per tile (MMA M)
   static constexpr int STAGES = STAGES_;
@@ -59,16 +71,25 @@ struct StreamKCfg {
   static constexpr uint32_t STAGE_TX = W_BYTES + A_BYTES;
   static constexpr int OFF_W = 0;
   static constexpr int OFF_A = OFF_W + STAGES * W_BYTES;
-  static constexpr int OFF_BAR = OFF_A + STAGES * A_BYTES;
+  static constexpr int SF_BYTES = MX ? 1024 : 0;  // per stage: the weight atom, then the activation atom
+  static constexpr int OFF_SF = OFF_A + STAGES * A_BYTES;
+  static constexpr int OFF_BAR = OFF_SF + STAGES * SF_BYTES;
   static constexpr int NUM_BARS = 2 * STAGES + 2 * 2 + 1;  // ring, accumulators, drain
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
-  static constexpr int TMEM_COLS = 2 * MT;  // two accumulators
+  static constexpr int COL_SF = 2 * MT;        // after the two accumulators
+  static constexpr int COLS_USED = COL_SF + (MX ? 8 * STAGES : 0);  // 8 scale columns per stage
+  static constexpr int TMEM_COLS = COLS_USED <= 64 ? 64 : COLS_USED <= 128 ? 128 : COLS_USED <= 256 ? 256 : 512;
   static constexpr int NUM_THREADS = 256;   // warp 0 TMA, warp 1 MMA, warps 4..7 epilogue
   static_assert(MT == 32 || MT == 64 || MT == 128, "activation tile");
   static_assert(A_BYTES % 1024 == 0, "swizzle atoms need 1024-byte alignment");
   static_assert(SMEM_BYTES <= 232448, "shared-memory budget");
   static constexpr uint32_t IDESC = make_idesc_dense(1, 0, 0, NT, MT);  // fp32 D, E4M3 x E4M3
+  static_assert(COLS_USED <= 512, "TMEM budget");
+  // block-scaled: E4M3 x E4M3, UE8M0 scale byte j of each row for the j-th MMA of K = 32
+  __host__ __device__ static constexpr uint32_t idesc_mx(uint32_t j) {
+    return make_idesc_block_scaled(0, 0, NT, MT, j, j);
+  }
 };
 
 // First unit of CTA c's range (units * c / G, rounded down).
@@ -110,7 +131,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
   if (threadIdx.x == 0) {
 #pragma unroll 1
     for (int s = 0; s < C::STAGES; ++s) {
-      mbar_init(&full[s], 1u);
+      mbar_init(&full[s], C::MX ? 2u : 1u);  // the TMA bytes (+ the scale warp's atoms)
       mbar_init(&empty[s], 1u);
     }
 #pragma unroll 1
@@ -198,11 +219,25 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
           const uint64_t adesc = make_desc_kmajor_sw128(smem_u32(smem + C::OFF_A + stage * C::A_BYTES));
           int ksteps = 4;
           if (kb == p.num_kb - 1) ksteps = min(4, (p.K - kb * C::K_ELEMS + 31) / 32);
+          if constexpr (C::MX) {
+            // this stage's scale atoms into its TMEM slot: weight ("A") then activation ("B")
+            const uint32_t sf_tmem = tmem + static_cast<uint32_t>(C::COL_SF + 8 * stage);
+            const uint32_t sf_smem = smem_u32(smem + C::OFF_SF + stage * C::SF_BYTES);
+            tmem_cp_32x128b_warpx4(sf_tmem, make_smem_desc(sf_smem, 128, 128, 0));
+            tmem_cp_32x128b_warpx4(sf_tmem + 4, make_smem_desc(sf_smem + 512, 128, 128, 0));
 #pragma unroll
-          for (int j = 0; j < 4; ++j)
-            if (j < ksteps)
-              umma_f8f6f4(d_tmem, wdesc + static_cast<uint64_t>(2 * j), adesc + static_cast<uint64_t>(2 * j),
-                          C::IDESC, (i > 0 || j > 0) ? 1u : 0u);
+            for (int j = 0; j < 4; ++j)
+              if (j < ksteps)
+                umma_mxf8f6f4(d_tmem, wdesc + static_cast<uint64_t>(2 * j), adesc + static_cast<uint64_t>(2 * j),
+                              C::idesc_mx(static_cast<uint32_t>(j)), sf_tmem, sf_tmem + 4,
+                              (i > 0 || j > 0) ? 1u : 0u);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              if (j < ksteps)
+                umma_f8f6f4(d_tmem, wdesc + static_cast<uint64_t>(2 * j), adesc + static_cast<uint64_t>(2 * j),
+                            C::IDESC, (i > 0 || j > 0) ? 1u : 0u);
+          }
           umma_commit(&empty[stage]);
           if (++stage == C::STAGES) {
             stage = 0;
@@ -222,6 +257,54 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
         if (global_timer_ns() - t0 > p.timeout_ns) {
           report_error(p.err, kDevErrTimeout, kSiteDrain, 0u);
           break;
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 2) {
+    // ---------------- scale warp (MXFP8): one pair of atoms per unit ----------------
+    if constexpr (C::MX) {
+      // Lane l loads the 4 scale bytes (this unit's 128 K) of weight rows 32j + l
+      // and activation rows 32j + l; an atom holds row r at byte 16 (r % 32) +
+      // 4 (r / 32), i.e. lane l's 16 bytes are its four rows' words.  Loads run
+      // D units ahead of the stores, in registers.
+      constexpr int D = 3;
+      constexpr int NA = C::MT / 32;
+      uint32_t vw[D][4], va[D][4];
+      auto load_unit = [&](long long v, uint32_t (&w4)[4], uint32_t (&a4)[4]) {
+        if (v >= u1) return;
+        const int tv = static_cast<int>(v / p.num_kb);
+        const int col = static_cast<int>(v - static_cast<long long>(tv) * p.num_kb) * 4;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) w4[j] = load_sf4(p.sfw, tv * C::NT + 32 * j + lane, p.N, col, p.sf_cols);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) a4[j] = j < NA ? load_sf4(p.sfa, 32 * j + lane, p.M, col, p.sf_cols) : 0u;
+      };
+#pragma unroll
+      for (int d = 0; d < D; ++d) load_unit(u0 + d, vw[d], va[d]);
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+#pragma unroll 1
+      for (long long u = u0; ok && u < u1; u += D) {
+#pragma unroll
+        for (int d = 0; d < D; ++d) {
+          if (!ok || u + d >= u1) break;
+          if (!mbar_wait(&empty[stage], phase ^ 1u, w, kSiteScaleEmpty)) {
+            ok = false;
+            break;
+          }
+          const uint32_t sf = smem_u32(smem + C::OFF_SF + stage * C::SF_BYTES);
+          st_shared_v4(sf + 16 * lane, vw[d][0], vw[d][1], vw[d][2], vw[d][3]);
+          st_shared_v4(sf + 512 + 16 * lane, va[d][0], va[d][1], va[d][2], va[d][3]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&full[stage]);
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+          load_unit(u + d + D, vw[d], va[d]);
         }
       }
     }
@@ -310,13 +393,16 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
         }
         const int n = t * C::NT + r;
         if (n < p.N) {
-          const float sbn = __ldg(p.sb + n);
+          const float sbn = C::MX ? 1.f : __ldg(p.sb + n);
           const float bn = p.bias ? __uint_as_float(static_cast<uint32_t>(__ldg(p.bias + n)) << 16) : 0.f;
 #pragma unroll
           for (int m = 0; m < C::MT; ++m) {
             if (m < p.M) {
-              float x = __fmul_rn(acc[m], __ldg(p.sa + m));
-              x = __fmul_rn(x, sbn);
+              float x = acc[m];
+              if constexpr (!C::MX) {
+                x = __fmul_rn(x, __ldg(p.sa + m));
+                x = __fmul_rn(x, sbn);
+              }
               if (p.bias) x = __fadd_rn(x, bn);
               p.out[static_cast<size_t>(m) * static_cast<size_t>(p.N) + n] =
                   __bfloat16_as_ushort(__float2bfloat16_rn(x));
