@@ -53,9 +53,9 @@ static int launch_mxfp8_cfg(const uint8_t* A, const uint8_t* sA, const uint8_t* 
 // Few rows (M <= 128): the stream-K weight-streaming kernel in its MXFP8
 // mode, each SM streaming an equal share of the weight's 128 x 128 units.
 // It beats the tile kernel for M <= 64 once the weight holds about ten units
-// per SM: 43.7 against 49.3 us at 64 x 21504 x 5376, 21.8 against 24.5 at
-// 16 x 7168 x 4096; with fewer units (64 x 2112 x 7168: 42.7 against 33.0)
-// or 128 activation rows (128 x 21504 x 5376: 55.5 against 49.5) it loses.
+// per SM: 37.2 against 49.8 us at 64 x 21504 x 5376, 23.0 against 24.6 at
+// 16 x 7168 x 4096; with fewer units (64 x 2112 x 7168: 43.7 against 33.1)
+// or 128 activation rows (128 x 21504 x 5376: 51.5 against 49.7) it loses.
 template <int MT>
 static int launch_mxfp8_streamk(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const uint8_t* sB,
                                 const uint16_t* bias, uint16_t* out, int M, int N, int K, const DeviceInfo& dev,

@@ -264,10 +264,70 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
   } else if (warp == 2) {
     // ---------------- scale warp (MXFP8): one pair of atoms per unit ----------------
     if constexpr (C::MX) {
-      // Lane l loads the 4 scale bytes (this unit's 128 K) of weight rows 32j + l
-      // and activation rows 32j + l; an atom holds row r at byte 16 (r % 32) +
-      // 4 (r / 32), i.e. lane l's 16 bytes are its four rows' words.  Loads run
-      // D units ahead of the stores, in registers.
+      // An atom holds row r's 4 scale bytes (one unit's 128 K) at byte
+      // 16 (r % 32) + 4 (r / 32): lane l writes the words of rows 32j + l.
+      if (p.sf_cols % 4 == 0) {
+        // 4-byte cp.async straight into the atoms, DA units in flight; each
+        // unit is one commit group, waited for before the proxy fence and the
+        // arrive.  Rows outside the matrix are zero-filled.
+        constexpr int DA = 4;
+        static_assert(DA < C::STAGES, "a slot is reissued only after the MMA has read it");
+        auto issue = [&](long long v, int st) {
+          const uint32_t sf = smem_u32(smem + C::OFF_SF + st * C::SF_BYTES);
+          const int tv = static_cast<int>(v / p.num_kb);
+          const int col = static_cast<int>(v - static_cast<long long>(tv) * p.num_kb) * 4;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int r = tv * C::NT + 32 * j + lane;
+            const bool in = r < p.N;
+            cp_async_4(sf + 16 * lane + 4 * j,
+                       in ? p.sfw + static_cast<size_t>(r) * static_cast<size_t>(p.sf_cols) + col : p.sfw,
+                       in ? 4u : 0u);
+          }
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int r = 32 * j + lane;
+            const bool in = r < p.M;
+            cp_async_4(sf + 512 + 16 * lane + 4 * j,
+                       in ? p.sfa + static_cast<size_t>(r) * static_cast<size_t>(p.sf_cols) + col : p.sfa,
+                       in ? 4u : 0u);
+          }
+        };
+        int is = 0, as = 0;  // slots of the next unit to issue / to publish
+        uint32_t iph = 0;
+        long long next = u0;
+        bool ok = true;
+        auto issue_next = [&]() {
+          if (next < u1) {
+            if (!mbar_wait(&empty[is], iph ^ 1u, w, kSiteScaleEmpty)) {
+              ok = false;
+              return;
+            }
+            issue(next, is);
+            ++next;
+            if (++is == C::STAGES) {
+              is = 0;
+              iph ^= 1u;
+            }
+          }
+          cp_async_commit();  // possibly empty: one group per unit index
+        };
+#pragma unroll 1
+        for (int d = 0; ok && d < DA; ++d) issue_next();
+#pragma unroll 1
+        for (long long u = u0; ok && u < u1; ++u) {
+          cp_async_wait_group<DA - 1>();  // unit u's group has landed
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&full[as]);
+          if (++as == C::STAGES) as = 0;
+          issue_next();
+        }
+        cp_async_wait_group<0>();
+        __syncwarp();
+      } else {
+      // K / 32 not a multiple of 4: byte-wise loads into registers, D units
+      // ahead of the stores.
       constexpr int D = 3;
       constexpr int NA = C::MT / 32;
       uint32_t vw[D][4], va[D][4];
@@ -306,6 +366,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
           }
           load_unit(u + d + D, vw[d], va[d]);
         }
+      }
       }
     }
     __syncwarp();

@@ -4,9 +4,10 @@ kernel's block-scaled mode, against the oracle within |gpu - ref| <=
 
 QK_MX_SKINNY=2 selects the mode.  The shapes cover one tile split over many
 CTAs, tiles shared by two or three CTAs, whole tiles per CTA, a ragged last
-K-block (K % 128 == 32 or 96), scale rows whose length K/32 is not a multiple
-of 4 (byte-wise scale loads), a ragged last weight tile and both activation
-tile heights (64 and 128 rows)."""
+K-block (K % 128 == 32 or 96), where the scale rows' length K/32 is not a
+multiple of 4 and the scale warp loads bytes into registers (with K % 128 ==
+0 it copies 4-byte words by cp.async), a ragged last weight tile and both
+activation tile heights (64 and 128 rows)."""
 import numpy as np
 import pytest
 
@@ -21,6 +22,7 @@ SHAPES = [
     (17, 136, 4064),     # two tiles, ragged last K-block, K/32 = 127
     (64, 2112, 7168),    # 17 tiles x 56 K-blocks
     (33, 7168, 1568),    # K/32 = 49: byte-wise scale loads
+    (7, 4096, 4096),     # K % 128 == 0: cp.async scale copies
     (65, 1000, 640),     # 128-row activation tile, ragged last weight tile
     (128, 19456, 256),   # whole tiles per CTA
 ]
