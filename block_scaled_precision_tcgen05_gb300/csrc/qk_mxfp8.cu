@@ -3,7 +3,7 @@
 // [rows, K/32] scale bytes (ROCm/mori PR #806, "What") are staged per ring
 // slot by the kernel's scale warp and moved to TMEM with tcgen05.cp.
 #include "qk_launch.cuh"
-#include "qk_streamk_launch.cuh"
+#include "qk_fewrow_launch.cuh"
 
 namespace qk {
 
@@ -50,34 +50,48 @@ static int launch_mxfp8_cfg(const uint8_t* A, const uint8_t* sA, const uint8_t* 
   return launch_gemm<C>(ta, tb, tsa, tsb, p, dev, stream);
 }
 
-// Few rows (M <= 128): the stream-K weight-streaming kernel in its MXFP8
-// mode, each SM streaming an equal share of the weight's 128 x 128 units.
-// It beats the tile kernel for M <= 64 once the weight holds about ten units
-// per SM: 37.2 against 49.8 us at 64 x 21504 x 5376, 23.0 against 24.6 at
-// 16 x 7168 x 4096; with fewer units (64 x 2112 x 7168: 43.7 against 33.1)
-// or 128 activation rows (128 x 21504 x 5376: 51.5 against 49.7) it loses.
-template <int MT>
-static int launch_mxfp8_streamk(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const uint8_t* sB,
-                                const uint16_t* bias, uint16_t* out, int M, int N, int K, const DeviceInfo& dev,
-                                cudaStream_t stream) {
-  StreamKParams p{};
-  p.sfa = sA;
-  p.sfw = sB;
-  p.sf_cols = K / 32;
-  p.bias = bias;
-  p.out = out;
-  return launch_streamk_cfg<StreamKCfg<MT, MT <= 64 ? 8 : 6, true>>(A, B, p, M, N, K, kKGemmMxfp8, dev, stream);
-}
-
+// Few rows (M <= 128): the few-row kernels' MXFP8 mode (qk_fewrow_launch.cuh).
+// Against the tile kernel (us): the cluster split-K kernel, when all tiles'
+// clusters fit in one wave, wins with a deep enough K range per CTA (at least
+// 6 K-blocks for M <= 64; S >= 4 for more rows) -- 64 x 2112 x 7168
+// 16.8 / 33.9, 64 x 4096 x 4096 15.2 / 23.9 (S = 4), 16 x 7168 x 4096
+// 18.6 / 24.6 and 1 x 7168 x 2048 12.6 / 18.1 (S = 2), 48 x 12288 x 2048
+// 16.8 (S = 1; stream-K 22.8), 128 x 2112 x 7168 20.7 / 33.4 -- and loses
+// with a short one:
+// 64 x 8192 x 1280 (5 K-blocks per CTA) 17.0 / 15.4, 128 x 7168 x 2048 (S = 2)
+// 22.8 / 17.3.  Otherwise the stream-K kernel wins for M <= 64 once the
+// weight holds about ten units per SM: 64 x 21504 x 5376 37.2 / 49.8; with
+// fewer units or 128 activation rows it loses (64 x 2112 x 7168: 43.7,
+// 128 x 21504 x 5376: 51.5 / 49.7).  QK_MX_SKINNY: 1 = always the tile
+// kernel, 2 = stream-K, 3 = cluster split-K, whenever M <= 128.
 int launch_mxfp8(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const uint8_t* sB, const uint16_t* bias,
                  uint16_t* out, int M, int N, int K, const DeviceInfo& dev, cudaStream_t stream) {
   const int v = kernel_variant("QK_MX_VARIANT");
-  // QK_MX_SKINNY: 1 = always the tile kernel, 2 = stream-K whenever M <= 128
   const int skinny = kernel_variant("QK_MX_SKINNY");
-  const long long units = static_cast<long long>(ceil_div(N, 128)) * ceil_div(K, 128);
-  if (M <= 128 && skinny != 1 && (skinny == 2 || (M <= 64 && units >= 10LL * dev.sm_count))) {
-    if (M <= 64) return launch_mxfp8_streamk<64>(A, sA, B, sB, bias, out, M, N, K, dev, stream);
-    return launch_mxfp8_streamk<128>(A, sA, B, sB, bias, out, M, N, K, dev, stream);
+  if (M <= 128 && skinny != 1) {
+    FewRowArgs args;
+    args.sfa = sA;
+    args.sfw = sB;
+    args.bias = bias;
+    args.out = out;
+    const long long units = static_cast<long long>(ceil_div(N, 128)) * ceil_div(K, 128);
+    if (skinny == 2) {
+      if (M <= 64) return launch_streamk<64, true>(A, B, args, M, N, K, kKGemmMxfp8, dev, stream);
+      return launch_streamk<128, true>(A, B, args, M, N, K, kKGemmMxfp8, dev, stream);
+    }
+    if (skinny == 3) {
+      if (M <= 64) return launch_cluster<64, true>(A, B, args, M, N, K, kKGemmMxfp8, dev, stream, true);
+      return launch_cluster<128, true>(A, B, args, M, N, K, kKGemmMxfp8, dev, stream, true);
+    }
+    if (M <= 64) {
+      const int st = launch_cluster<64, true>(A, B, args, M, N, K, kKGemmMxfp8, dev, stream, false, 1, 6);
+      if (st != QK_ERR_RANGE) return st;
+      if (units >= 10LL * dev.sm_count)
+        return launch_streamk<64, true>(A, B, args, M, N, K, kKGemmMxfp8, dev, stream);
+    } else {
+      const int st = launch_cluster<128, true>(A, B, args, M, N, K, kKGemmMxfp8, dev, stream, false, 4, 0);
+      if (st != QK_ERR_RANGE) return st;
+    }
   }
   if (v == 1) return launch_mxfp8_cfg<CfgMxfp8Pair>(A, sA, B, sB, bias, out, M, N, K, dev, stream);
   if (v == 4) return launch_mxfp8_cfg<CfgMxfp8Double>(A, sA, B, sB, bias, out, M, N, K, dev, stream);

@@ -10,11 +10,16 @@
 // m it owns by reading its peers' partials through distributed shared
 // memory, then applies the fixed-order epilogue (x*sa[m])*sb[n] (+bias[n])
 // and writes bf16 rows of the output with coalesced stores.
+//
+// MXFP8 mode (MX_ = true): block-scaled MMAs (kind::mxf8f6f4, scale_vec::1X)
+// with the scale staging of qk_fewrow_scales.cuh (a scale warp, 8 TMEM
+// columns per stage after the accumulator), and the epilogue bf16(x (+bias)).
 #pragma once
 
 #include <cuda_bf16.h>
 
 #include "qk_device.cuh"
+#include "qk_fewrow_scales.cuh"
 #include "qk_gemm_kernel.cuh"
 
 namespace qk {
@@ -25,14 +30,18 @@ struct SkinnyParams {
   int kb_per_split;  // k-blocks per CTA of a cluster
   const float* sa;
   const float* sb;
+  const uint8_t* sfa;  // MXFP8: activation UE8M0 scales [M, sf_cols]
+  const uint8_t* sfw;  // MXFP8: weight UE8M0 scales [N, sf_cols]
+  int sf_cols;         // K / 32
   const uint16_t* bias;
   uint16_t* out;
   unsigned long long* err;
   uint64_t timeout_ns;
 };
 
-template <int MT_, int SPLITS_, int STAGES_>
+template <int MT_, int SPLITS_, int STAGES_, bool MX_ = false>
 struct SkinnyCfg {
+  static constexpr bool MX = MX_;         // MXFP8 block-scaled MMAs
   static constexpr int MT = MT_;          // padded activation rows (MMA N)
   static constexpr int NT = 128;          // weight rows per tile (MMA M)
   static constexpr int SPLITS = SPLITS_;  // CTAs of a cluster splitting K
@@ -43,12 +52,16 @@ struct SkinnyCfg {
   static constexpr uint32_t STAGE_TX = W_BYTES + A_BYTES;
   static constexpr int OFF_W = 0;
   static constexpr int OFF_A = OFF_W + STAGES * W_BYTES;
-  static constexpr int OFF_RED = OFF_A + STAGES * A_BYTES;  // fp32 partial [MT][NT]
+  static constexpr int SF_BYTES = MX ? kFewRowSfBytes : 0;  // per stage: the weight atom, then the activation atom
+  static constexpr int OFF_SF = OFF_A + STAGES * A_BYTES;
+  static constexpr int OFF_RED = OFF_SF + STAGES * SF_BYTES;  // fp32 partial [MT][NT]
   static constexpr int RED_BYTES = MT * NT * 4;
   static constexpr int OFF_BAR = OFF_RED + RED_BYTES;
   static constexpr int OFF_MISC = OFF_BAR + (2 * STAGES + 2) * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
-  static constexpr int TMEM_COLS = MT <= 32 ? 32 : MT <= 64 ? 64 : MT <= 128 ? 128 : 256;
+  static constexpr int COL_SF = MT;  // after the accumulator
+  static constexpr int COLS_USED = MT + (MX ? 8 * STAGES : 0);
+  static constexpr int TMEM_COLS = COLS_USED <= 32 ? 32 : COLS_USED <= 64 ? 64 : COLS_USED <= 128 ? 128 : COLS_USED <= 256 ? 256 : 512;
   static constexpr int ROWS_PER_CTA = MT / SPLITS;  // output rows each CTA reduces
   static constexpr int NUM_THREADS = 256;
   static_assert(MT % 32 == 0 && MT >= 32 && MT <= 128, "activation tile");
@@ -91,7 +104,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
   if (threadIdx.x == 0) {
 #pragma unroll 1
     for (int s = 0; s < C::STAGES; ++s) {
-      mbar_init(&full[s], 1u);
+      mbar_init(&full[s], C::MX ? 2u : 1u);  // the TMA bytes (+ the scale warp's atoms)
       mbar_init(&empty[s], 1u);
     }
     mbar_init(acc_full, 1u);
@@ -159,11 +172,16 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
         const uint64_t adesc = make_desc_kmajor_sw128(smem_u32(smem + C::OFF_A + stage * C::A_BYTES));
         int ksteps = 4;
         if (kb == p.num_kb - 1) ksteps = min(4, (p.K - kb * C::K_ELEMS + 31) / 32);
+        if constexpr (C::MX) {
+          fewrow_mx_mmas(tmem, wdesc, adesc, tmem + static_cast<uint32_t>(C::COL_SF + 8 * stage),
+                         smem_u32(smem + C::OFF_SF + stage * C::SF_BYTES), ksteps, kb > kb0, C::NT, C::MT);
+        } else {
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-          if (j < ksteps)
-            umma_f8f6f4(tmem, wdesc + static_cast<uint64_t>(2 * j), adesc + static_cast<uint64_t>(2 * j),
-                        C::IDESC, (kb > kb0 || j > 0) ? 1u : 0u);
+          for (int j = 0; j < 4; ++j)
+            if (j < ksteps)
+              umma_f8f6f4(tmem, wdesc + static_cast<uint64_t>(2 * j), adesc + static_cast<uint64_t>(2 * j),
+                          C::IDESC, (kb > kb0 || j > 0) ? 1u : 0u);
+        }
         umma_commit(&empty[stage]);
         if (++stage == C::STAGES) {
           stage = 0;
@@ -180,6 +198,16 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
           break;
         }
       }
+    }
+    __syncwarp();
+  } else if (warp == 2) {
+    if constexpr (C::MX) {
+      auto unit = [&](long long i, int& w_row0, int& col) {
+        w_row0 = n0;
+        col = (kb0 + static_cast<int>(i)) * 4;
+      };
+      fewrow_stage_scales<C::STAGES>(p.sfw, p.sfa, p.N, p.M, p.sf_cols, smem + C::OFF_SF, full, empty,
+                                     kb1 > kb0 ? kb1 - kb0 : 0, unit, lane, w);
     }
     __syncwarp();
   } else if (warp >= 4) {
@@ -212,7 +240,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
     const int t = (warp - 4) * 32 + lane;  // weight row within the tile
     const int n = n0 + t;
     const bool col_ok = n < p.N;
-    const float sbn = col_ok ? __ldg(p.sb + n) : 0.f;
+    const float sbn = (col_ok && !C::MX) ? __ldg(p.sb + n) : 0.f;
     const float bn = (col_ok && p.bias) ? __uint_as_float(static_cast<uint32_t>(__ldg(p.bias + n)) << 16) : 0.f;
     const uint32_t red_base = smem_u32(red);
 #pragma unroll 1
@@ -229,8 +257,11 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
 #pragma unroll
       for (int r = 0; r < C::SPLITS; ++r) sum = __fadd_rn(sum, part[r]);  // fixed order over the cluster
       if (col_ok) {
-        float x = __fmul_rn(sum, __ldg(p.sa + m));
-        x = __fmul_rn(x, sbn);
+        float x = sum;
+        if constexpr (!C::MX) {
+          x = __fmul_rn(x, __ldg(p.sa + m));
+          x = __fmul_rn(x, sbn);
+        }
         if (p.bias) x = __fadd_rn(x, bn);
         p.out[static_cast<size_t>(m) * static_cast<size_t>(p.N) + n] = __bfloat16_as_ushort(__float2bfloat16_rn(x));
       }

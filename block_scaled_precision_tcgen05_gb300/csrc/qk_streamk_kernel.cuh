@@ -26,17 +26,15 @@
 // which guarantees that all CTAs are resident at once.
 //
 // MXFP8 mode (MX_ = true): the MMAs are block-scaled (kind::mxf8f6f4,
-// scale_vec::1X).  With the operands swapped, the weight's UE8M0 scales are
-// the MMA's "A" scales and the activations' its "B" scales: per stage a
-// scale warp stages one 512-byte atom of each (128 weight rows, up to 128
-// activation rows; 4 scale bytes per row for the stage's 128 K), the MMA warp
-// copies both into the stage's TMEM slot, and the epilogue is bf16(acc
-// (+bias)) with no per-row scales.
+// scale_vec::1X); a scale warp stages each unit's UE8M0 atoms
+// (qk_fewrow_scales.cuh), the MMA warp copies them into the stage's 8 TMEM
+// columns, and the epilogue is bf16(acc (+bias)) with no per-row scales.
 #pragma once
 
 #include <cuda_bf16.h>
 
 #include "qk_device.cuh"
+#include "qk_fewrow_scales.cuh"
 #include "qk_gemm_kernel.cuh"
 
 namespace qk {
@@ -71,7 +69,7 @@ struct StreamKCfg {
   static constexpr uint32_t STAGE_TX = W_BYTES + A_BYTES;
   static constexpr int OFF_W = 0;
   static constexpr int OFF_A = OFF_W + STAGES * W_BYTES;
-  static constexpr int SF_BYTES = MX ? 1024 : 0;  // per stage: the weight atom, then the activation atom
+  static constexpr int SF_BYTES = MX ? kFewRowSfBytes : 0;  // per stage: the weight atom, then the activation atom
   static constexpr int OFF_SF = OFF_A + STAGES * A_BYTES;
   static constexpr int OFF_BAR = OFF_SF + STAGES * SF_BYTES;
   static constexpr int NUM_BARS = 2 * STAGES + 2 * 2 + 1;  // ring, accumulators, drain
@@ -86,10 +84,6 @@ struct StreamKCfg {
   static_assert(SMEM_BYTES <= 232448, "shared-memory budget");
   static constexpr uint32_t IDESC = make_idesc_dense(1, 0, 0, NT, MT);  // fp32 D, E4M3 x E4M3
   static_assert(COLS_USED <= 512, "TMEM budget");
-  // block-scaled: E4M3 x E4M3, UE8M0 scale byte j of each row for the j-th MMA of K = 32
-  __host__ __device__ static constexpr uint32_t idesc_mx(uint32_t j) {
-    return make_idesc_block_scaled(0, 0, NT, MT, j, j);
-  }
 };
 
 // First unit of CTA c's range (units * c / G, rounded down).
@@ -220,17 +214,8 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
           int ksteps = 4;
           if (kb == p.num_kb - 1) ksteps = min(4, (p.K - kb * C::K_ELEMS + 31) / 32);
           if constexpr (C::MX) {
-            // this stage's scale atoms into its TMEM slot: weight ("A") then activation ("B")
-            const uint32_t sf_tmem = tmem + static_cast<uint32_t>(C::COL_SF + 8 * stage);
-            const uint32_t sf_smem = smem_u32(smem + C::OFF_SF + stage * C::SF_BYTES);
-            tmem_cp_32x128b_warpx4(sf_tmem, make_smem_desc(sf_smem, 128, 128, 0));
-            tmem_cp_32x128b_warpx4(sf_tmem + 4, make_smem_desc(sf_smem + 512, 128, 128, 0));
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-              if (j < ksteps)
-                umma_mxf8f6f4(d_tmem, wdesc + static_cast<uint64_t>(2 * j), adesc + static_cast<uint64_t>(2 * j),
-                              C::idesc_mx(static_cast<uint32_t>(j)), sf_tmem, sf_tmem + 4,
-                              (i > 0 || j > 0) ? 1u : 0u);
+            fewrow_mx_mmas(d_tmem, wdesc, adesc, tmem + static_cast<uint32_t>(C::COL_SF + 8 * stage),
+                           smem_u32(smem + C::OFF_SF + stage * C::SF_BYTES), ksteps, i > 0, C::NT, C::MT);
           } else {
 #pragma unroll
             for (int j = 0; j < 4; ++j)
@@ -264,110 +249,14 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
   } else if (warp == 2) {
     // ---------------- scale warp (MXFP8): one pair of atoms per unit ----------------
     if constexpr (C::MX) {
-      // An atom holds row r's 4 scale bytes (one unit's 128 K) at byte
-      // 16 (r % 32) + 4 (r / 32): lane l writes the words of rows 32j + l.
-      if (p.sf_cols % 4 == 0) {
-        // 4-byte cp.async straight into the atoms, DA units in flight; each
-        // unit is one commit group, waited for before the proxy fence and the
-        // arrive.  Rows outside the matrix are zero-filled.
-        constexpr int DA = 4;
-        static_assert(DA < C::STAGES, "a slot is reissued only after the MMA has read it");
-        auto issue = [&](long long v, int st) {
-          const uint32_t sf = smem_u32(smem + C::OFF_SF + st * C::SF_BYTES);
-          const int tv = static_cast<int>(v / p.num_kb);
-          const int col = static_cast<int>(v - static_cast<long long>(tv) * p.num_kb) * 4;
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int r = tv * C::NT + 32 * j + lane;
-            const bool in = r < p.N;
-            cp_async_4(sf + 16 * lane + 4 * j,
-                       in ? p.sfw + static_cast<size_t>(r) * static_cast<size_t>(p.sf_cols) + col : p.sfw,
-                       in ? 4u : 0u);
-          }
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int r = 32 * j + lane;
-            const bool in = r < p.M;
-            cp_async_4(sf + 512 + 16 * lane + 4 * j,
-                       in ? p.sfa + static_cast<size_t>(r) * static_cast<size_t>(p.sf_cols) + col : p.sfa,
-                       in ? 4u : 0u);
-          }
-        };
-        int is = 0, as = 0;  // slots of the next unit to issue / to publish
-        uint32_t iph = 0;
-        long long next = u0;
-        bool ok = true;
-        auto issue_next = [&]() {
-          if (next < u1) {
-            if (!mbar_wait(&empty[is], iph ^ 1u, w, kSiteScaleEmpty)) {
-              ok = false;
-              return;
-            }
-            issue(next, is);
-            ++next;
-            if (++is == C::STAGES) {
-              is = 0;
-              iph ^= 1u;
-            }
-          }
-          cp_async_commit();  // possibly empty: one group per unit index
-        };
-#pragma unroll 1
-        for (int d = 0; ok && d < DA; ++d) issue_next();
-#pragma unroll 1
-        for (long long u = u0; ok && u < u1; ++u) {
-          cp_async_wait_group<DA - 1>();  // unit u's group has landed
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&full[as]);
-          if (++as == C::STAGES) as = 0;
-          issue_next();
-        }
-        cp_async_wait_group<0>();
-        __syncwarp();
-      } else {
-      // K / 32 not a multiple of 4: byte-wise loads into registers, D units
-      // ahead of the stores.
-      constexpr int D = 3;
-      constexpr int NA = C::MT / 32;
-      uint32_t vw[D][4], va[D][4];
-      auto load_unit = [&](long long v, uint32_t (&w4)[4], uint32_t (&a4)[4]) {
-        if (v >= u1) return;
+      auto unit = [&](long long i, int& w_row0, int& col) {
+        const long long v = u0 + i;
         const int tv = static_cast<int>(v / p.num_kb);
-        const int col = static_cast<int>(v - static_cast<long long>(tv) * p.num_kb) * 4;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) w4[j] = load_sf4(p.sfw, tv * C::NT + 32 * j + lane, p.N, col, p.sf_cols);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) a4[j] = j < NA ? load_sf4(p.sfa, 32 * j + lane, p.M, col, p.sf_cols) : 0u;
+        w_row0 = tv * C::NT;
+        col = static_cast<int>(v - static_cast<long long>(tv) * p.num_kb) * 4;
       };
-#pragma unroll
-      for (int d = 0; d < D; ++d) load_unit(u0 + d, vw[d], va[d]);
-      int stage = 0;
-      uint32_t phase = 0;
-      bool ok = true;
-#pragma unroll 1
-      for (long long u = u0; ok && u < u1; u += D) {
-#pragma unroll
-        for (int d = 0; d < D; ++d) {
-          if (!ok || u + d >= u1) break;
-          if (!mbar_wait(&empty[stage], phase ^ 1u, w, kSiteScaleEmpty)) {
-            ok = false;
-            break;
-          }
-          const uint32_t sf = smem_u32(smem + C::OFF_SF + stage * C::SF_BYTES);
-          st_shared_v4(sf + 16 * lane, vw[d][0], vw[d][1], vw[d][2], vw[d][3]);
-          st_shared_v4(sf + 512 + 16 * lane, va[d][0], va[d][1], va[d][2], va[d][3]);
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&full[stage]);
-          if (++stage == C::STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
-          load_unit(u + d + D, vw[d], va[d]);
-        }
-      }
-      }
+      fewrow_stage_scales<C::STAGES>(p.sfw, p.sfa, p.N, p.M, p.sf_cols, smem + C::OFF_SF, full, empty, u1 - u0,
+                                     unit, lane, w);
     }
     __syncwarp();
   } else if (warp >= 4) {

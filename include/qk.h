@@ -128,10 +128,12 @@ int qk_gemm_int8_rowwise_noalloc(const int8_t* A, const int8_t* B, const float* 
  *   bias bf16 [N] or NULL;  out bf16 [M, N]
  * Requirements: A, B, out, bias 16-byte aligned; sA, sB 4-byte aligned;
  * N % 8 == 0; K % 32 == 0.  Any M >= 1 is accepted without padding.
- * MXFP8 with M <= 64 and at least ten 128 x 128 weight units per SM runs the
- * cooperative stream-K weight-streaming launch described under
- * qk_gemm_fp8_rowwise, with the same pooled workspace, the same QK_ERR_NOMEM
- * case and the same reproducible fixed-order reduction.
+ * MXFP8 with few rows runs the weight-streaming kernels described under
+ * qk_gemm_fp8_rowwise where they are faster: the cluster split-K kernel when
+ * all weight tiles' clusters fit on the GPU at once with a long enough K
+ * range per CTA; else, for M <= 64 and at least ten 128 x 128 weight units
+ * per SM, the cooperative stream-K launch, with the same pooled workspace,
+ * the same QK_ERR_NOMEM case and the same reproducible fixed-order reduction.
  */
 int qk_gemm_mx(int fmt, const void* A, const uint8_t* sA, const void* B, const uint8_t* sB,
                const uint16_t* bias, uint16_t* out, int64_t M, int64_t N, int64_t K, qk_stream_t stream);

@@ -1,9 +1,10 @@
-"""MXFP8 GEMM with few rows (M <= 128) on the stream-K weight-streaming
-kernel's block-scaled mode, against the oracle within |gpu - ref| <=
-1e-2*|ref| + 1e-2*rms(ref) and cosine >= 0.99999.
+"""MXFP8 GEMM with few rows (M <= 128) on the block-scaled modes of the two
+few-row kernels, stream-K (QK_MX_SKINNY=2) and cluster split-K
+(QK_MX_SKINNY=3), against the oracle within |gpu - ref| <= 1e-2*|ref| +
+1e-2*rms(ref) and cosine >= 0.99999.
 
-QK_MX_SKINNY=2 selects the mode.  The shapes cover one tile split over many
-CTAs, tiles shared by two or three CTAs, whole tiles per CTA, a ragged last
+The shapes cover one tile split over many CTAs (or over a cluster of 8),
+tiles shared by two or three CTAs, whole tiles per CTA, a ragged last
 K-block (K % 128 == 32 or 96), where the scale rows' length K/32 is not a
 multiple of 4 and the scale warp loads bytes into registers (with K % 128 ==
 0 it copies 4-byte words by cp.async), a ragged last weight tile and both
@@ -28,21 +29,22 @@ SHAPES = [
 ]
 
 
-@pytest.fixture
-def streamk(monkeypatch):
-    monkeypatch.setenv("QK_MX_SKINNY", "2")
+@pytest.fixture(params=["2", "3"], ids=["streamk", "cluster"])
+def fewrow(request, monkeypatch):
+    monkeypatch.setenv("QK_MX_SKINNY", request.param)
+    return request.param
 
 
 @pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
-def test_mxfp8_streamk_matches_oracle(streamk, shape):
+def test_mxfp8_fewrow_matches_oracle(fewrow, shape):
     M, N, K = shape
     p = qi.mx_problem(qi.FMT_MXFP8_E4M3, M, N, K, seed=M + N)
     got = host_bits(run_mx(p))
     ref = oracle.gemm_mx(p.fmt, p.A, p.sA, p.B, p.sB)
-    assert_close(got, ref, f"mxfp8 stream-K {shape}")
+    assert_close(got, ref, f"mxfp8 few-row mode {fewrow} {shape}")
 
 
-def test_mxfp8_streamk_bias_and_reproducible(streamk):
+def test_mxfp8_fewrow_bias_and_reproducible(fewrow):
     p = qi.mx_problem(qi.FMT_MXFP8_E4M3, 40, 3000, 3072, seed=5, bias=True)
     first = host_bits(run_mx(p))
     assert_close(first, oracle.gemm_mx(p.fmt, p.A, p.sA, p.B, p.sB, bias=p.bias), "bias")
@@ -50,11 +52,11 @@ def test_mxfp8_streamk_bias_and_reproducible(streamk):
         assert np.array_equal(host_bits(run_mx(p)), first), "fixed-order reduction must be reproducible"
 
 
-def test_mxfp8_streamk_exact_powers_of_two(streamk):
+def test_mxfp8_fewrow_exact_powers_of_two(fewrow):
     # elements in {0, +-1, +-2} and scales 2^e with |e| <= 3: every scaled
     # product is a multiple of 2^-6, and the partial sums of these random
     # signs stay far below 2^18, where such multiples are exact in fp32, so
-    # the stream-K split changes no bit
+    # the split of K changes no bit
     M, N, K = 48, 520, 8192
     rng = np.random.default_rng(3)
     vals = np.array([0.0, 1.0, -1.0, 2.0, -2.0], np.float32)
@@ -68,9 +70,13 @@ def test_mxfp8_streamk_exact_powers_of_two(streamk):
     assert np.array_equal(got, qi.to_bf16_bits(ref.astype(np.float32)))
 
 
-def test_mxfp8_default_dispatch_few_rows():
-    # 48 rows and 96 x 16 weight units (over ten per SM): the default
-    # dispatch picks the stream-K mode without the switch
-    p = qi.mx_problem(qi.FMT_MXFP8_E4M3, 48, 12288, 2048, seed=9, bias=True)
+@pytest.mark.parametrize("shape", [(32, 21504, 2048), (64, 2112, 7168), (48, 12288, 2048), (100, 2112, 4096)],
+                         ids=["streamk", "cluster", "cluster-s1", "cluster-128"])
+def test_mxfp8_default_dispatch_few_rows(shape):
+    # without the switch: 168 tiles (no cluster wave fits) x 16 K-blocks ->
+    # stream-K; 17 tiles with a long K -> cluster split-K; 96 tiles -> one
+    # CTA per tile; and the cluster kernel for 128 activation rows
+    M, N, K = shape
+    p = qi.mx_problem(qi.FMT_MXFP8_E4M3, M, N, K, seed=9, bias=True)
     got = host_bits(run_mx(p))
-    assert_close(got, oracle.gemm_mx(p.fmt, p.A, p.sA, p.B, p.sB, bias=p.bias), "default dispatch")
+    assert_close(got, oracle.gemm_mx(p.fmt, p.A, p.sA, p.B, p.sB, bias=p.bias), f"default dispatch {shape}")
