@@ -160,12 +160,13 @@ int launch_cluster_cfg(const uint8_t* A, const uint8_t* B, const FewRowArgs& arg
 // The cluster split-K kernel with the largest S in {8, 4, 2, 1} (S no larger
 // than the K-blocks) whose clusters for all weight tiles fit on the GPU in one
 // wave (one pass, on-chip reduction).  Returns QK_ERR_RANGE without launching
-// when no S fits, or when that S is below min_s or leaves a CTA fewer than
-// min_kb K-blocks; with `force` S = 1 runs in several waves if nothing fits.
+// when no S fits (*fits_one_wave = false), or when that S is below min_s or
+// leaves a CTA fewer than min_kb K-blocks (*fits_one_wave = true); with
+// `force` S = 1 runs in several waves if nothing fits.
 template <int MT, bool MX>
 int launch_cluster(const uint8_t* A, const uint8_t* B, const FewRowArgs& args, int M, int N, int K,
-                   int kernel_kind, const DeviceInfo& dev, cudaStream_t stream, bool force, int min_s = 1,
-                   int min_kb = 0) {
+                   int kernel_kind, const DeviceInfo& dev, cudaStream_t stream, bool force, int min_s,
+                   int min_kb, bool* fits_one_wave) {
   constexpr int ST = MT <= 64 ? 6 : 4;
   const int n_tiles = ceil_div(N, 128);
   const int num_kb = ceil_div(K, 128);
@@ -182,12 +183,13 @@ int launch_cluster(const uint8_t* A, const uint8_t* B, const FewRowArgs& args, i
       break;
     }
   }
+  *fits_one_wave = chosen != 0;
   if (!force) {
     if (chosen == 0 || chosen < min_s || ceil_div(num_kb, chosen) < min_kb) return QK_ERR_RANGE;
   } else if (chosen == 0) {
     chosen = 1;
   }
-  switch (chosen) {
+  switch (chosen) {  // launch_cluster_cfg never returns QK_ERR_RANGE
     case 8:
       return launch_cluster_cfg<SkinnyCfg<MT, 8, ST, MX>>(A, B, args, M, N, K, kernel_kind, dev, stream, false, nullptr);
     case 4:
@@ -198,6 +200,14 @@ int launch_cluster(const uint8_t* A, const uint8_t* B, const FewRowArgs& args, i
       return launch_cluster_cfg<SkinnyCfg<MT, 1, ST, MX>>(A, B, args, M, N, K, kernel_kind, dev, stream, false, nullptr);
   }
 }
+
+// Measured choice between the few-row kernels and the 2-SM tile kernel (both
+// modes behave alike): a cluster split that fits in one wave wins when each
+// CTA keeps at least kClusterMinKb K-blocks with M <= 64, or the split is at
+// least kClusterMinSplitWide with more rows; shallower splits lose to the
+// tile kernel (64 x 8192 x 1280, 128 x 7168 x 2048).
+constexpr int kClusterMinKb = 6;
+constexpr int kClusterMinSplitWide = 4;
 
 template <int MT, bool MX>
 int launch_streamk(const uint8_t* A, const uint8_t* B, const FewRowArgs& args, int M, int N, int K, int kernel_kind,

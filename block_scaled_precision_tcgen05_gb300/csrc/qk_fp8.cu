@@ -38,10 +38,13 @@ static int launch_fp8_cfg(const uint8_t* A, const uint8_t* B, const float* sa, c
 
 // Few rows (M <= 128): if the weight tiles times some split S in {8, 4, 2, 1}
 // fit on the GPU in one wave of clusters, the cluster split-K kernel with the
-// largest such S (one pass, on-chip reduction); otherwise stream-K, which
-// keeps every SM streaming whatever the tile count (qk_fewrow_launch.cuh).
+// largest such S (one pass, on-chip reduction) when that split is deep
+// enough, else the tile kernel; if no split fits, stream-K, which keeps every
+// SM streaming whatever the tile count (qk_fewrow_launch.cuh).  Cluster
+// against tile kernel (us): 16 x 7168 x 4096 16.9 / 24.7, 128 x 2112 x 7168
+// 19.2 / 31.2, 64 x 8192 x 1280 17.3 / 15.4, 128 x 7168 x 2048 23.3 / 17.5.
 // QK_FP8_SKINNY: 1 = the 2-SM tile kernel, 2 = always stream-K, 3 = always
-// cluster split-K.
+// cluster split-K.  Returns QK_ERR_RANGE when the tile kernel should run.
 std::atomic<unsigned long long> g_streamk_epoch{0};
 
 template <int MT>
@@ -54,8 +57,12 @@ static int launch_fewrow_fp8(const uint8_t* A, const uint8_t* B, const float* sa
   args.bias = bias;
   args.out = out;
   if (variant != 2) {
-    const int st = launch_cluster<MT, false>(A, B, args, M, N, K, kKGemmFp8, dev, stream, variant == 3);
+    bool fits = false;
+    const int st = launch_cluster<MT, false>(A, B, args, M, N, K, kKGemmFp8, dev, stream, variant == 3,
+                                             MT <= 64 ? 1 : kClusterMinSplitWide, MT <= 64 ? kClusterMinKb : 0,
+                                             &fits);
     if (st != QK_ERR_RANGE) return st;
+    if (fits) return QK_ERR_RANGE;
   }
   return launch_streamk<MT, false>(A, B, args, M, N, K, kKGemmFp8, dev, stream);
 }
@@ -63,8 +70,11 @@ static int launch_fewrow_fp8(const uint8_t* A, const uint8_t* B, const float* sa
 int launch_fp8_rowwise(const uint8_t* A, const uint8_t* B, const float* sa, const float* sb, const uint16_t* bias,
                        uint16_t* out, int M, int N, int K, const DeviceInfo& dev, cudaStream_t stream) {
   const int v = kernel_variant("QK_FP8_SKINNY");
-  if (M <= 64 && v != 1) return launch_fewrow_fp8<64>(A, B, sa, sb, bias, out, M, N, K, dev, stream, v);
-  if (M <= 128 && v != 1) return launch_fewrow_fp8<128>(A, B, sa, sb, bias, out, M, N, K, dev, stream, v);
+  if (M <= 128 && v != 1) {
+    const int st = M <= 64 ? launch_fewrow_fp8<64>(A, B, sa, sb, bias, out, M, N, K, dev, stream, v)
+                           : launch_fewrow_fp8<128>(A, B, sa, sb, bias, out, M, N, K, dev, stream, v);
+    if (st != QK_ERR_RANGE) return st;
+  }
   if (K <= 2048) return launch_fp8_cfg<CfgFp8Drain>(A, B, sa, sb, bias, out, M, N, K, dev, stream);
   return launch_fp8_cfg<CfgFp8>(A, B, sa, sb, bias, out, M, N, K, dev, stream);
 }

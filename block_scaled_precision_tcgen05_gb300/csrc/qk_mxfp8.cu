@@ -79,17 +79,20 @@ int launch_mxfp8(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const ui
       if (M <= 64) return launch_streamk<64, true>(A, B, args, M, N, K, kKGemmMxfp8, dev, stream);
       return launch_streamk<128, true>(A, B, args, M, N, K, kKGemmMxfp8, dev, stream);
     }
+    bool fits = false;
     if (skinny == 3) {
-      if (M <= 64) return launch_cluster<64, true>(A, B, args, M, N, K, kKGemmMxfp8, dev, stream, true);
-      return launch_cluster<128, true>(A, B, args, M, N, K, kKGemmMxfp8, dev, stream, true);
+      if (M <= 64) return launch_cluster<64, true>(A, B, args, M, N, K, kKGemmMxfp8, dev, stream, true, 1, 0, &fits);
+      return launch_cluster<128, true>(A, B, args, M, N, K, kKGemmMxfp8, dev, stream, true, 1, 0, &fits);
     }
     if (M <= 64) {
-      const int st = launch_cluster<64, true>(A, B, args, M, N, K, kKGemmMxfp8, dev, stream, false, 1, 6);
+      const int st = launch_cluster<64, true>(A, B, args, M, N, K, kKGemmMxfp8, dev, stream, false, 1,
+                                              kClusterMinKb, &fits);
       if (st != QK_ERR_RANGE) return st;
-      if (units >= 10LL * dev.sm_count)
+      if (!fits && units >= 10LL * dev.sm_count)
         return launch_streamk<64, true>(A, B, args, M, N, K, kKGemmMxfp8, dev, stream);
     } else {
-      const int st = launch_cluster<128, true>(A, B, args, M, N, K, kKGemmMxfp8, dev, stream, false, 4, 0);
+      const int st = launch_cluster<128, true>(A, B, args, M, N, K, kKGemmMxfp8, dev, stream, false,
+                                               kClusterMinSplitWide, 0, &fits);
       if (st != QK_ERR_RANGE) return st;
     }
   }

@@ -1,12 +1,14 @@
-"""FP8 per-token x per-channel GEMM with few rows (M <= 128), the stream-K
-weight-streaming path, against the oracle within |gpu - ref| <= 1e-2*|ref| +
-1e-2*rms(ref) and cosine >= 0.99999.
+"""FP8 per-token x per-channel GEMM with few rows (M <= 128) on the two
+few-row kernels, stream-K (QK_FP8_SKINNY=2) and cluster split-K
+(QK_FP8_SKINNY=3), and through the default dispatch, against the oracle
+within |gpu - ref| <= 1e-2*|ref| + 1e-2*rms(ref) and cosine >= 0.99999.
 
-The shapes make CTAs share tiles in every way the schedule allows: one tile
-split over 128 CTAs (its owner adds 127 partials), tiles split over two or
-three CTAs, CTAs that finish several whole tiles, a ragged last K-block and a
-ragged last tile.  Partials are added in a fixed order, so repeated calls are
-bit-identical."""
+The shapes make CTAs share tiles in every way the stream-K schedule allows:
+one tile split over 128 CTAs (its owner adds 127 partials), tiles split over
+two or three CTAs, CTAs that finish several whole tiles, a ragged last
+K-block and a ragged last tile; the cluster kernel sees splits of 8 down to 1
+(several waves when forced).  Partials are added in a fixed order, so
+repeated calls are bit-identical."""
 import numpy as np
 import pytest
 import torch
@@ -29,8 +31,14 @@ SHAPES = [
 ]
 
 
+@pytest.fixture(params=["0", "2", "3"], ids=["default", "streamk", "cluster"])
+def fewrow(request, monkeypatch):
+    monkeypatch.setenv("QK_FP8_SKINNY", request.param)
+    return request.param
+
+
 @pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
-def test_streamk_matches_oracle(shape):
+def test_fewrow_matches_oracle(fewrow, shape):
     M, N, K = shape
     p = qi.fp8_problem(M, N, K, seed=M + N)
     got = host_bits(run_fp8(p))
@@ -38,7 +46,7 @@ def test_streamk_matches_oracle(shape):
     assert_close(got, ref, f"fp8 {shape}")
 
 
-def test_streamk_bias_and_reproducible():
+def test_fewrow_bias_and_reproducible(fewrow):
     p = qi.fp8_problem(40, 3000, 3072, seed=5, bias=True)
     first = host_bits(run_fp8(p))
     assert_close(first, oracle.gemm_fp8_rowwise(p.A, p.B, p.sa, p.sb, bias=p.bias), "bias")
@@ -46,7 +54,7 @@ def test_streamk_bias_and_reproducible():
         assert np.array_equal(host_bits(run_fp8(p)), first), "fixed-order reduction must be reproducible"
 
 
-def test_streamk_exact_small_integers():
+def test_fewrow_exact_small_integers(fewrow):
     # E4M3 integers with unit scales: every partial and total is an exact
     # integer in fp32, so the split across CTAs cannot change any bit
     M, N, K = 48, 520, 8192

@@ -1,7 +1,8 @@
-"""Full-size workloads (the configurations the benchmark times), checked on a
-seeded sample of 128x128 output tiles plus every ragged edge tile, which the
-oracle computes one by one: INT8 bit-exact, MX/FP8 within tolerance (the rms
-in the bound is taken over the sampled outputs)."""
+"""Full-size workloads (the configurations the benchmark times, and the
+few-row decode shapes), checked on a seeded sample of 128x128 output tiles
+plus every ragged edge tile, which the oracle computes one by one: INT8
+bit-exact, MX/FP8 within tolerance (the rms in the bound is taken over the
+sampled outputs)."""
 import functools
 
 import numpy as np
@@ -105,3 +106,29 @@ def test_fp8_ptpc_sweep(shape):
         refs.append(oracle.gemm_fp8_rowwise(p.A, p.B, p.sa, p.sb, m0=m0, m1=m1, n0=n0, n1=n1).ravel())
     assert not torch.isnan(out).any().item()
     assert_close(np.concatenate(gots)[None, :], np.concatenate(refs)[None, :], f"fp8 {shape}")
+
+
+# MXFP8 with few rows at the decode shapes: every dispatch the few-row logic
+# can take (cluster split-K, stream-K, tile kernel) across M = 1 .. 128.
+MX_FEWROW = [(M, N, K) for (N, K) in ((2112, 7168), (7168, 2048), (8192, 1280), (21504, 5376))
+             for M in (1, 16, 64, 128)]
+
+
+@functools.lru_cache(maxsize=1)
+def _mx_weights(N, K):
+    return qi.mx_operand(qi.FMT_MXFP8_E4M3, N, K, 0, qi.TAG_B)
+
+
+@pytest.mark.parametrize("shape", MX_FEWROW, ids=lambda s: "x".join(map(str, s)))
+def test_mxfp8_fewrow_sweep(shape):
+    M, N, K = shape
+    A, sA = qi.mx_operand(qi.FMT_MXFP8_E4M3, M, K, 0, qi.TAG_A)
+    B, sB = _mx_weights(N, K)
+    p = qi.MxProblem(qi.FMT_MXFP8_E4M3, A, sA, B, sB, None, M, N, K)
+    out = run_mx(p)
+    gots, refs = [], []
+    for (m0, m1, n0, n1) in qi.sample_tiles(M, N, 4, 3):
+        gots.append(host_bits(out[m0:m1, n0:n1]).ravel())
+        refs.append(oracle.gemm_mx(p.fmt, A, sA, B, sB, m0=m0, m1=m1, n0=n0, n1=n1).ravel())
+    assert not torch.isnan(out).any().item()
+    assert_close(np.concatenate(gots)[None, :], np.concatenate(refs)[None, :], f"mxfp8 few-row {shape}")
