@@ -3,7 +3,9 @@ scale) against the oracle's quantizers: codes and scales bit-exact.
 
 The inputs mix the MXFP8 recipe's distribution (N(0,1) with 1% of entries
 x20) with rows scaled over a wide exponent range, all-zero and negative-zero
-blocks, bf16 subnormals and values near the bf16 maximum (saturation)."""
+blocks, bf16 subnormals and values near the bf16 maximum (saturation); one
+per-token case runs every bf16 value through the quotient for a range of
+scales."""
 import numpy as np
 import pytest
 import torch
@@ -48,9 +50,11 @@ def test_mx_quantize_matches_oracle(fmt):
         [(int(r), int(c), hex(int(got[r, c])), hex(int(ref_codes[r, c]))) for r, c in bad[:6]])
 
 
-@pytest.mark.parametrize("rows,K", [(41, 2048), (6, 16400)], ids=["row-in-registers", "row-read-twice"])
+@pytest.mark.parametrize("rows,K", [(41, 2048), (9, 8208), (6, 16400)],
+                         ids=["row-in-4-registers", "row-in-8-registers", "row-read-twice"])
 def test_ptpc_quantize_matches_oracle(rows, K):
-    # rows up to 16384 elements stay in registers between the two passes; longer rows are read twice
+    # rows up to 8192 / 16384 elements stay in 4 / 8 register vectors per thread between the two
+    # passes; longer rows are read twice
     bits, x = _inputs(rows, K, 9)
     x[5] = 0.0                           # an all-zero row takes scale 1
     bits[5] = 0
@@ -59,6 +63,50 @@ def test_ptpc_quantize_matches_oracle(rows, K):
     ref_codes, ref_scales = oracle.ptpc_quantize(x)
     assert np.array_equal(s.cpu().numpy(), ref_scales)
     assert np.array_equal(q.cpu().numpy(), ref_codes)
+
+
+def _all_bf16_up_to(amax_bits, tiny):
+    """Every finite bf16 value with magnitude <= the given bf16 amax (both
+    signs, both zeros); without `tiny`, none with 0 < |x| < 2^-60."""
+    codes = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    v = qi.from_bf16_bits(codes)
+    amax = float(qi.from_bf16_bits(np.array([amax_bits], np.uint16))[0])
+    keep = np.isfinite(v) & (np.abs(v) <= amax)
+    if not tiny:
+        keep &= (v == 0) | (np.abs(v) >= 2.0 ** -60)
+    return codes[keep]
+
+
+@pytest.mark.parametrize("tiny", [False, True], ids=["reciprocal-range", "with-tiny"])
+def test_ptpc_quantize_every_bf16_value(tiny):
+    # Each row holds every bf16 value up to its amax, so for the row's scale s
+    # every element's quotient x / s is checked, on both sides of each E4M3
+    # rounding boundary.  The amax values span scales inside the reciprocal
+    # path's range (2^-60 .. 2^60, rows whose elements all go through the
+    # reciprocal and its two corrections) and outside it (the library
+    # division), including its edges; one variant leaves out, the other
+    # keeps, the elements below 2^-60, where the corrections' residuals stop
+    # being exact and only the zero code of the tiny quotient must agree.
+    rng = np.random.default_rng(17)
+    exps = list(range(-70, 71, 7)) + [-58, -57, -52, 51, 52, 53, 60, 68]
+    amax_vals = [np.float32(np.ldexp(1.0 + rng.uniform(), e)) for e in exps]
+    amax_vals += [np.float32(448.0), np.float32(1.0), np.float32(np.ldexp(448.0, -60)),
+                  np.float32(np.ldexp(448.0, 60)), np.float32(np.ldexp(449.0, -61))]
+    amax_bits = [int(b) for b in qi.to_bf16_bits(np.array(amax_vals, np.float32))]
+    rows = [_all_bf16_up_to(b, tiny) for b in amax_bits]
+    K = (max(len(r) for r in rows) + 15) // 16 * 16
+    bits = np.zeros((len(rows), K), np.uint16)
+    for i, r in enumerate(rows):
+        bits[i, :len(r)] = rng.permutation(r)
+    q, s = qk.quantize_ptpc(_dev_bf16(bits))
+    torch.cuda.synchronize()
+    ref_codes, ref_scales = oracle.ptpc_quantize(qi.from_bf16_bits(bits))
+    assert np.array_equal(s.cpu().numpy(), ref_scales)
+    got = q.cpu().numpy()
+    bad = np.argwhere(got != ref_codes)
+    assert bad.size == 0, f"{len(bad)} codes differ, first (row, col, x, gpu, ref): " + str(
+        [(int(r), int(c), float(qi.from_bf16_bits(bits[r:r + 1, c])[0]), hex(int(got[r, c])), hex(int(ref_codes[r, c])))
+         for r, c in bad[:6]])
 
 
 def test_quantize_then_gemm_matches_oracle_on_the_same_bytes():
