@@ -236,6 +236,16 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                : "memory");
 }
 
+// Two fp32 fused multiply-adds in one instruction (fma.rn.f32x2, sm_100 and
+// later): (d0, d1) = (a0 * b + d0, a1 * b + d1), each half rounded to nearest
+// even exactly as a scalar fma.rn.f32 would round it.
+__device__ __forceinline__ void fma2_rn(uint32_t& d0, uint32_t& d1, uint32_t a0, uint32_t a1, float b) {
+  asm("{\n .reg .b64 rd, ra, rb;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %4};\n mov.b64 rd, {%0, %1};\n"
+      " fma.rn.f32x2 rd, ra, rb, rd;\n mov.b64 {%0, %1}, rd;\n}"
+      : "+r"(d0), "+r"(d1)
+      : "r"(a0), "r"(a1), "r"(__float_as_uint(b)));
+}
+
 __device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
   return __uint_as_float(static_cast<uint32_t>(b) << 16);
 }
@@ -974,6 +984,8 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
       if constexpr (C::BLOCKSCALE) {
         sa_next = row_ok ? __ldg(p.sa + static_cast<size_t>(m) * p.scale_kb) : 0.f;
         sb_next = col_in ? __ldg(p.sb + static_cast<size_t>(n_tile >> 7) * p.scale_kb) : 0.f;
+#pragma unroll
+        for (int i = 0; i < C::EPI_COLS; ++i) sums[i] = 0u;
       }
 #pragma unroll 1
       for (int c = 0; c < p.num_chunks; ++c) {
@@ -1012,16 +1024,15 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
         } else if constexpr (C::REG_SUMS && C::BLOCKSCALE) {
           // chunk c is K-block c: sums += partial * (sa[m, c] * sb[n / 128, c]);
           // this thread's columns lie in one 128-column block of B
+          // (the sums start at +0 for each tile, so the first K-block gives
+          // fma(partial, scale, +0); pairs of columns share one fma.rn.f32x2)
           const float scale = __fmul_rn(sa_next, sb_next);
           if constexpr (C::EPI_COLS == 32) {
             uint32_t v[32];
             tmem_ld_32cols(acc_col, v);
             tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const float prev = c == 0 ? 0.f : __uint_as_float(sums[i]);
-              sums[i] = __float_as_uint(__fmaf_rn(__uint_as_float(v[i]), scale, prev));
-            }
+            for (int i = 0; i < 32; i += 2) fma2_rn(sums[i], sums[i + 1], v[i], v[i + 1], scale);
           } else {
 #pragma unroll
             for (int g = 0; g < C::EPI_COLS / 16; ++g) {
@@ -1029,10 +1040,8 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
               tmem_ld_16cols(acc_col + 16 * g, v);
               tmem_wait_ld();
 #pragma unroll
-              for (int i = 0; i < 16; ++i) {
-                const float prev = c == 0 ? 0.f : __uint_as_float(sums[16 * g + i]);
-                sums[16 * g + i] = __float_as_uint(__fmaf_rn(__uint_as_float(v[i]), scale, prev));
-              }
+              for (int i = 0; i < 16; i += 2)
+                fma2_rn(sums[16 * g + i], sums[16 * g + i + 1], v[i], v[i + 1], scale);
             }
           }
           release(a);
