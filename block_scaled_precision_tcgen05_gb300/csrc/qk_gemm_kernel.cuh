@@ -250,10 +250,22 @@ __device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
   return __uint_as_float(static_cast<uint32_t>(b) << 16);
 }
 
+// Two fp32 products in one instruction (mul.rn.f32x2): each half rounded to
+// nearest even exactly as a scalar mul.rn.f32 would.  Only products use the
+// paired form: a paired multiply followed by a paired add was measured to
+// come out fused into one multiply-add, so additions that must round on
+// their own stay scalar __fadd_rn, which is never merged.
+__device__ __forceinline__ void mul2_rn(float& x0, float& x1, float b0, float b1) {
+  asm("{\n .reg .b64 rx, rb;\n mov.b64 rx, {%0, %1};\n mov.b64 rb, {%2, %3};\n"
+      " mul.rn.f32x2 rx, rx, rb;\n mov.b64 {%0, %1}, rx;\n}"
+      : "+f"(x0), "+f"(x1)
+      : "f"(b0), "f"(b1));
+}
+
+// Two fp32 values to bf16 (round to nearest even), lo in the low half.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-  const uint32_t l = __bfloat16_as_ushort(__float2bfloat16_rn(lo));
-  const uint32_t h = __bfloat16_as_ushort(__float2bfloat16_rn(hi));
-  return l | (h << 16);
+  const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
 }
 
 // Epilogue of 32 consecutive columns [n0, n0+32) of one row m, in four steps
@@ -291,20 +303,19 @@ __device__ __forceinline__ void epilogue_row32(const GemmParams& p, int n0, floa
     uint32_t packed[4];
 #pragma unroll
     for (int i = 0; i < 8; i += 2) {
-      float x[2];
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const uint32_t raw = v[OFF + 8 * s8 + i + j];
-        float t = INT_ACC ? __int2float_rn(static_cast<int>(raw)) : __uint_as_float(raw);
-        if constexpr (ROWWISE) {
-          t = __fmul_rn(t, sam);
-          t = __fmul_rn(t, sbv[i + j]);
-        }
-        if constexpr (ALPHA) t = __fmul_rn(t, sam);
-        if (has_bias) t = __fadd_rn(t, bv[i + j]);
-        x[j] = t;
+      const uint32_t r0 = v[OFF + 8 * s8 + i], r1 = v[OFF + 8 * s8 + i + 1];
+      float x0 = INT_ACC ? __int2float_rn(static_cast<int>(r0)) : __uint_as_float(r0);
+      float x1 = INT_ACC ? __int2float_rn(static_cast<int>(r1)) : __uint_as_float(r1);
+      if constexpr (ROWWISE) {
+        mul2_rn(x0, x1, sam, sam);
+        mul2_rn(x0, x1, sbv[i], sbv[i + 1]);
       }
-      packed[i / 2] = pack_bf16x2(x[0], x[1]);
+      if constexpr (ALPHA) mul2_rn(x0, x1, sam, sam);
+      if (has_bias) {
+        x0 = __fadd_rn(x0, bv[i]);
+        x1 = __fadd_rn(x1, bv[i + 1]);
+      }
+      packed[i / 2] = pack_bf16x2(x0, x1);
     }
     st_shared_v4(block + 64 * lane + 16 * (s8 ^ ((lane >> 1) & 3)), packed[0], packed[1], packed[2], packed[3]);
   }
@@ -341,20 +352,19 @@ __device__ __forceinline__ void epilogue_row32_global(const GemmParams& p, int m
       uint32_t packed[4];
 #pragma unroll
       for (int i = 0; i < 8; i += 2) {
-        float x[2];
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          const uint32_t raw = v[OFF + 8 * s8 + i + j];
-          float t = INT_ACC ? __int2float_rn(static_cast<int>(raw)) : __uint_as_float(raw);
-          if constexpr (ROWWISE) {
-            t = __fmul_rn(t, sam);
-            t = __fmul_rn(t, sbv[i + j]);
-          }
-          if constexpr (ALPHA) t = __fmul_rn(t, sam);
-          if (has_bias) t = __fadd_rn(t, bv[i + j]);
-          x[j] = t;
+        const uint32_t r0 = v[OFF + 8 * s8 + i], r1 = v[OFF + 8 * s8 + i + 1];
+        float x0 = INT_ACC ? __int2float_rn(static_cast<int>(r0)) : __uint_as_float(r0);
+        float x1 = INT_ACC ? __int2float_rn(static_cast<int>(r1)) : __uint_as_float(r1);
+        if constexpr (ROWWISE) {
+          mul2_rn(x0, x1, sam, sam);
+          mul2_rn(x0, x1, sbv[i], sbv[i + 1]);
         }
-        packed[i / 2] = pack_bf16x2(x[0], x[1]);
+        if constexpr (ALPHA) mul2_rn(x0, x1, sam, sam);
+        if (has_bias) {
+          x0 = __fadd_rn(x0, bv[i]);
+          x1 = __fadd_rn(x1, bv[i + 1]);
+        }
+        packed[i / 2] = pack_bf16x2(x0, x1);
       }
       reinterpret_cast<uint4*>(dst)[s8] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
     }
