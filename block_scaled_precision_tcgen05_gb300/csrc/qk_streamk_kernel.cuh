@@ -335,9 +335,15 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
 #pragma unroll 1
             for (int j = c + 1; j < jend; ++j) {
               const float* src = p.partials + static_cast<size_t>(j) * C::MT * C::NT;
+              // all the partial's loads in flight before the adds: interleaved
+              // with the adds they were waited for one by one, which made the
+              // owners' fixup several microseconds long
+              float pv[C::MT];
+#pragma unroll
+              for (int m = 0; m < C::MT; ++m) pv[m] = m < p.M ? __ldcg(src + m * C::NT + r) : 0.f;
 #pragma unroll
               for (int m = 0; m < C::MT; ++m)
-                if (m < p.M) acc[m] = __fadd_rn(acc[m], __ldcg(src + m * C::NT + r));
+                if (m < p.M) acc[m] = __fadd_rn(acc[m], pv[m]);
             }
           }
         }
@@ -345,6 +351,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
         if (n < p.N) {
           const float sbn = C::MX ? 1.f : __ldg(p.sb + n);
           const float bn = p.bias ? __uint_as_float(static_cast<uint32_t>(__ldg(p.bias + n)) << 16) : 0.f;
+          // the row scales of 16 rows loaded ahead of their stores
 #pragma unroll
           for (int m = 0; m < C::MT; ++m) {
             if (m < p.M) {
