@@ -526,6 +526,17 @@ def run_kernel_case(args):
         ga = _to_dev(np.array([p.global_a], np.float32), dev)
         gb = _to_dev(np.array([p.global_b], np.float32), dev)
         fn = lambda out: qk.gemm_nvfp4(A, sA, B, sB, ga, gb, None, out)
+    elif args.kernel_case in ("quantize_ptpc", "quantize_mxfp8"):
+        # bf16 [M, K] input (N is not used), the recipe of the benchmark's quantizer lines
+        import numpy as np
+        rng = np.random.default_rng(0)
+        xb = torch.from_numpy(qi.to_bf16_bits(rng.standard_normal((M, K), dtype=np.float32)).view(np.int16))
+        xb = xb.to(dev).view(torch.bfloat16)
+        if args.kernel_case == "quantize_ptpc":
+            fn = lambda out: qk.quantize_ptpc(xb)
+        else:
+            fn = lambda out: qk.quantize_mx(qi.FMT_MXFP8_E4M3, xb)
+        N = 1
     else:
         fmt = qi.FMT_MXFP8_E4M3 if args.kernel_case == "mxfp8" else qi.FMT_MXFP4_E2M1
         p = qi.mx_problem(fmt, M, N, K, seed=0)
@@ -554,7 +565,8 @@ def main(argv=None):
     ap.add_argument("--formats", choices=["default", "none", "full"], default="default")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
-    ap.add_argument("--kernel-case", choices=["int8", "fp8", "mxfp8", "mxfp4", "nvfp4", "blockscale"], default=None,
+    ap.add_argument("--kernel-case", choices=["int8", "fp8", "mxfp8", "mxfp4", "nvfp4", "blockscale", "quantize_ptpc",
+                                              "quantize_mxfp8"], default=None,
                     help="only run --iters calls of one kernel kind on --shape (profiler captures)")
     ap.add_argument("--shape", default="8192,8192,8192")
     ap.add_argument("--iters", type=int, default=3)
