@@ -243,27 +243,40 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
     const float sbn = (col_ok && !C::MX) ? __ldg(p.sb + n) : 0.f;
     const float bn = (col_ok && p.bias) ? __uint_as_float(static_cast<uint32_t>(__ldg(p.bias + n)) << 16) : 0.f;
     const uint32_t red_base = smem_u32(red);
+    // RG rows at a time: all their peers' loads are issued before the first
+    // sum (one row at a time, each row waited for its loads in turn)
+    constexpr int RG = C::ROWS_PER_CTA < 4 ? C::ROWS_PER_CTA : 4;
+    static_assert(C::ROWS_PER_CTA % RG == 0, "row groups");
 #pragma unroll 1
-    for (int i = 0; i < C::ROWS_PER_CTA; ++i) {
-      const int m = split * C::ROWS_PER_CTA + i;
-      if (m >= p.M) break;
-      const uint32_t off = red_base + static_cast<uint32_t>((m * C::NT + t) * 4);
-      float part[C::SPLITS];
+    for (int i0 = 0; i0 < C::ROWS_PER_CTA; i0 += RG) {
+      if (split * C::ROWS_PER_CTA + i0 >= p.M) break;
+      float part[RG][C::SPLITS];
 #pragma unroll
-      for (int r = 0; r < C::SPLITS; ++r)
-        part[r] = C::SPLITS > 1 ? ld_shared_cluster_f32(mapa_shared(off, static_cast<uint32_t>(r)))
-                                : red[m * C::NT + t];
-      float sum = 0.f;
+      for (int g = 0; g < RG; ++g) {
+        const int m = split * C::ROWS_PER_CTA + i0 + g;
+        const uint32_t off = red_base + static_cast<uint32_t>((m * C::NT + t) * 4);
 #pragma unroll
-      for (int r = 0; r < C::SPLITS; ++r) sum = __fadd_rn(sum, part[r]);  // fixed order over the cluster
-      if (col_ok) {
-        float x = sum;
-        if constexpr (!C::MX) {
-          x = __fmul_rn(x, __ldg(p.sa + m));
-          x = __fmul_rn(x, sbn);
+        for (int r = 0; r < C::SPLITS; ++r)
+          part[g][r] = m >= p.M ? 0.f
+                       : C::SPLITS > 1 ? ld_shared_cluster_f32(mapa_shared(off, static_cast<uint32_t>(r)))
+                                       : red[m * C::NT + t];
+      }
+#pragma unroll
+      for (int g = 0; g < RG; ++g) {
+        const int m = split * C::ROWS_PER_CTA + i0 + g;
+        if (m >= p.M) break;
+        float sum = 0.f;
+#pragma unroll
+        for (int r = 0; r < C::SPLITS; ++r) sum = __fadd_rn(sum, part[g][r]);  // fixed order over the cluster
+        if (col_ok) {
+          float x = sum;
+          if constexpr (!C::MX) {
+            x = __fmul_rn(x, __ldg(p.sa + m));
+            x = __fmul_rn(x, sbn);
+          }
+          if (p.bias) x = __fadd_rn(x, bn);
+          p.out[static_cast<size_t>(m) * static_cast<size_t>(p.N) + n] = __bfloat16_as_ushort(__float2bfloat16_rn(x));
         }
-        if (p.bias) x = __fadd_rn(x, bn);
-        p.out[static_cast<size_t>(m) * static_cast<size_t>(p.N) + n] = __bfloat16_as_ushort(__float2bfloat16_rn(x));
       }
     }
   }
