@@ -31,12 +31,17 @@ QK_ERR_TIMEOUT = 6
 QK_ERR_NOMEM = 7
 QK_ERR_SCRATCH = 8
 
+QK_OUT_BF16 = 0
+QK_OUT_FP16 = 1
+QK_OUT_FP32 = 2
+
 FMT_MXFP8_E4M3 = 1
 FMT_MXFP4_E2M1 = 2
 
 # every symbol include/qk.h declares
 EXPORTS = (
     "qk_gemm_int8_rowwise",
+    "qk_gemm_int8_rowwise_out",
     "qk_gemm_int8_rowwise_noalloc",
     "qk_gemm_mx",
     "qk_gemm_fp8_rowwise",
@@ -75,6 +80,8 @@ def _declare(lib):
     i64 = c.c_int64
     lib.qk_gemm_int8_rowwise.argtypes = [P, P, P, P, P, P, i64, i64, i64, P]
     lib.qk_gemm_int8_rowwise.restype = c.c_int
+    lib.qk_gemm_int8_rowwise_out.argtypes = [P, P, P, P, P, P, c.c_int, i64, i64, i64, P]
+    lib.qk_gemm_int8_rowwise_out.restype = c.c_int
     lib.qk_gemm_int8_rowwise_noalloc.argtypes = [P, P, P, P, P, P, i64, i64, i64, P]
     lib.qk_gemm_int8_rowwise_noalloc.restype = c.c_int
     lib.qk_gemm_fp8_rowwise.argtypes = [P, P, P, P, P, P, i64, i64, i64, P]
@@ -167,8 +174,10 @@ def _out(out, M, N, device):
     return out
 
 
-def gemm_int8_rowwise(A, B, sa, sb, bias=None, out=None):
-    """out = bf16(((float)(A @ B^T) * sa[:, None]) * sb[None, :] (+ bias)), bit-exact."""
+def gemm_int8_rowwise(A, B, sa, sb, bias=None, out=None, out_dtype=None):
+    """out = bf16(((float)(A @ B^T) * sa[:, None]) * sb[None, :] (+ bias)), bit-exact.  With
+    out_dtype torch.float16 or torch.float32 (or an `out` of that dtype) the same value is
+    written as fp16 (round to nearest even) or as fp32 itself."""
     import torch
     if A.dim() != 2 or B.dim() != 2:
         raise ValueError("A and B must be 2-D")
@@ -183,9 +192,20 @@ def gemm_int8_rowwise(A, B, sa, sb, bias=None, out=None):
     _expect(sb, "sb", torch.float32, (N,), dev)
     if bias is not None:
         _expect(bias, "bias", torch.bfloat16, (N,), dev)
-    out = _out(out, M, N, dev)
-    check(load_library().qk_gemm_int8_rowwise(_ptr(A), _ptr(B), _ptr(sa), _ptr(sb), _ptr(bias), _ptr(out),
-                                              M, N, K, _stream_handle(dev)))
+    if out_dtype is None:
+        out_dtype = torch.bfloat16 if out is None else out.dtype
+    codes = {torch.bfloat16: QK_OUT_BF16, torch.float16: QK_OUT_FP16, torch.float32: QK_OUT_FP32}
+    if out_dtype not in codes:
+        raise ValueError(f"out_dtype must be bfloat16, float16 or float32, not {out_dtype}")
+    if out is None:
+        out = torch.empty((M, N), dtype=out_dtype, device=dev)
+    _expect(out, "out", out_dtype, (M, N), dev)
+    if out_dtype == torch.bfloat16:
+        check(load_library().qk_gemm_int8_rowwise(_ptr(A), _ptr(B), _ptr(sa), _ptr(sb), _ptr(bias), _ptr(out),
+                                                  M, N, K, _stream_handle(dev)))
+    else:
+        check(load_library().qk_gemm_int8_rowwise_out(_ptr(A), _ptr(B), _ptr(sa), _ptr(sb), _ptr(bias),
+                                                      _ptr(out), codes[out_dtype], M, N, K, _stream_handle(dev)))
     return out
 
 

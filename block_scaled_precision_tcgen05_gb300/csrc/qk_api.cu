@@ -188,9 +188,12 @@ int encode_tmap_2d_plain(CUtensorMap* map, CUtensorMapDataType dtype, const void
   return encode_2d(map, dtype, base, inner, rows, row_pitch_bytes, box_inner, box_rows, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
-int encode_tmap_out(CUtensorMap* map, void* out, uint64_t rows, uint64_t cols) {
-  return encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, out, cols, rows, cols * 2, 32, 32,
-                   CU_TENSOR_MAP_SWIZZLE_64B);
+int encode_tmap_out(CUtensorMap* map, void* out, uint64_t rows, uint64_t cols, int out_type) {
+  if (out_type == QK_OUT_FP32)
+    return encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, out, cols, rows, cols * 4, 32, 32,
+                     CU_TENSOR_MAP_SWIZZLE_128B);
+  return encode_2d(map, out_type == QK_OUT_FP16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                   out, cols, rows, cols * 2, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
 int kernel_variant(const char* env_name) {
@@ -270,6 +273,19 @@ int qk_gemm_int8_rowwise(const int8_t* A, const int8_t* B, const float* sa, cons
   if (!dev) return st;
   return launch_int8_rowwise(A, B, sa, sb, bias, out, static_cast<int>(M), static_cast<int>(N),
                              static_cast<int>(K), *dev, static_cast<cudaStream_t>(stream));
+}
+
+int qk_gemm_int8_rowwise_out(const int8_t* A, const int8_t* B, const float* sa, const float* sb,
+                             const uint16_t* bias, void* out, int out_type, int64_t M, int64_t N, int64_t K,
+                             qk_stream_t stream) {
+  if (out_type != QK_OUT_BF16 && out_type != QK_OUT_FP16 && out_type != QK_OUT_FP32) return QK_ERR_ARG;
+  bool empty;
+  int st = check_rowwise(A, B, sa, sb, bias, static_cast<const uint16_t*>(out), M, N, K, 131056, &empty);
+  if (st != QK_OK || empty) return st;
+  const DeviceInfo* dev = current_device(&st);
+  if (!dev) return st;
+  return launch_int8_rowwise_out(A, B, sa, sb, bias, out, out_type, static_cast<int>(M), static_cast<int>(N),
+                                 static_cast<int>(K), *dev, static_cast<cudaStream_t>(stream));
 }
 
 int qk_gemm_fp8_rowwise(const uint8_t* A, const uint8_t* B, const float* sa, const float* sb, const uint16_t* bias,

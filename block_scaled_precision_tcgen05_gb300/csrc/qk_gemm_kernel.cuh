@@ -30,16 +30,22 @@
 // cached INT8 epilogue scale order exact"): x = float(acc); x = x*sa[m];
 // x = x*sb[n]; if bias: x = x + float(bias[n]); out = bf16_rne(x).  Without
 // bias no add happens, so a -0 survives ("Preserve signed zero without INT8
-// bias").  MX kinds: out = bf16_rne(acc (+ bias)).
+// bias").  MX kinds: out = bf16_rne(acc (+ bias)).  The same page's INT8
+// specialization also writes fp16 and fp32 outputs (update "rebased onto
+// v0.2.38", its resources paragraph): out = fp16_rne(x) or x itself.
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "qk_device.cuh"
 
 namespace qk {
 
 enum class Kind : int { F16 = 0, F8 = 1, MXF8 = 2, MXF4 = 3, NVF4 = 4, F8BS = 5 };
+
+// Output element type (the values of the public QK_OUT_* constants).
+enum class OutType : int { BF16 = 0, F16 = 1, F32 = 2 };
 
 // How the scale warp gets raw scale rows (MX kinds):
 //   kSfTma    TMA boxes of 16 bytes per row (K % 512 == 0, 16-byte aligned rows)
@@ -56,7 +62,7 @@ struct GemmParams {
   const float* sa;            // [M] row scales (F16, F8)
   const float* sb;            // [N] column scales (F16, F8)
   const uint16_t* bias;       // [N] bf16 bits, nullable
-  uint16_t* out;              // [M, N] bf16 bits
+  void* out;                  // [M, N] bf16 / fp16 bits or fp32 (the configuration's OutType)
   const uint8_t* sA;          // [M, sf_cols] scale bytes (MX: UE8M0, NVFP4: UE4M3)
   const uint8_t* sB;          // [N, sf_cols]
   int sf_cols;                // scale bytes per row: K / 32 (MX), K / 16 (NVFP4)
@@ -79,9 +85,11 @@ struct GemmParams {
 // OUT_BUFS_: shared-memory staging blocks per epilogue warp for bulk tensor
 // stores of the output; 0 = the epilogue stores straight to global memory.
 template <Kind KIND, int BN_, int STAGES_, int ACC_BUFS_, bool PAIR_ = false, int EPI_WARPS_ = 4,
-          int OUT_BUFS_ = 2>
+          int OUT_BUFS_ = 2, OutType OUT_ = OutType::BF16>
 struct GemmCfg {
   static constexpr Kind kind = KIND;
+  static constexpr OutType OUT = OUT_;
+  static constexpr int OUT_ELEM_BYTES = OUT_ == OutType::F32 ? 4 : 2;
   static constexpr bool PAIR = PAIR_;
   static constexpr int CTAS = PAIR ? 2 : 1;  // CTAs of a cluster
   static constexpr int BM = 128;                 // rows of A (and D) per CTA
@@ -144,11 +152,12 @@ struct GemmCfg {
   static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
   static constexpr int OFF_SF = OFF_B + STAGES * B_BYTES;
   static constexpr int OFF_RAW = OFF_SF + STAGES * SF_STAGE_BYTES;
-  // Output staging: each epilogue warp writes 32x32 bf16 blocks (2 KB, 64-byte
-  // swizzle) that a bulk tensor store copies to global memory.
+  // Output staging: each epilogue warp writes 32x32 blocks (bf16 / fp16: 2 KB
+  // with the 64-byte swizzle; fp32: 4 KB with the 128-byte swizzle) that a
+  // bulk tensor store copies to global memory.
   static constexpr int OUT_BUFS = OUT_BUFS_;
   static constexpr bool STORE_TMA = OUT_BUFS_ > 0;
-  static constexpr int OUT_BLOCK_BYTES = 32 * 32 * 2;
+  static constexpr int OUT_BLOCK_BYTES = 32 * 32 * OUT_ELEM_BYTES;
   static constexpr int OFF_OUT = ((OFF_RAW + RAW_BUFS * RAW_STAGE_BYTES) + 1023) & ~1023;
   static constexpr int OFF_BAR = OFF_OUT + EPI_WARPS * OUT_BUFS * OUT_BLOCK_BYTES;
   static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC_BUFS + 1 + RAW_BUFS;
@@ -268,14 +277,27 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
+// The same for fp16 (round to nearest even; beyond 65504 rounds to +-inf).
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+template <OutType OT>
+__device__ __forceinline__ uint32_t pack_out16x2(float lo, float hi) {
+  if constexpr (OT == OutType::F16) return pack_f16x2(lo, hi);
+  else return pack_bf16x2(lo, hi);
+}
+
 // Epilogue of 32 consecutive columns [n0, n0+32) of one row m, in four steps
-// of 8 columns (8 column scales, 8 biases live at a time), written as bf16 to
-// row `lane` of a 32x32 staging block with the 64-byte swizzle the output
-// tensor map uses (16-byte chunk c of row r at 64r + 16(c ^ ((r >> 1) & 3))).
+// of 8 columns (8 column scales, 8 biases live at a time), written to row
+// `lane` of a 32x32 staging block with the swizzle the output tensor map
+// uses: bf16 / fp16 rows of 64 bytes, 16-byte chunk c of row r at
+// 64r + 16(c ^ ((r >> 1) & 3)); fp32 rows of 128 bytes, at 128r + 16(c ^ (r & 7)).
 // INT_ACC: v holds int32 sums; otherwise fp32 bit patterns.  Columns past N
 // (N is a multiple of 8) read no scale or bias; the bulk store clips them.
 // ALPHA: multiply by `sam` (the NVFP4 per-tensor scale product) before the bias.
-template <bool ROWWISE, bool INT_ACC, int OFF = 0, bool ALPHA = false, int LEN = 32>
+template <bool ROWWISE, bool INT_ACC, int OFF = 0, bool ALPHA = false, OutType OT = OutType::BF16, int LEN = 32>
 __device__ __forceinline__ void epilogue_row32(const GemmParams& p, int n0, float sam, const uint32_t (&v)[LEN],
                                                uint32_t block, int lane) {
   const bool has_bias = p.bias != nullptr;
@@ -300,7 +322,7 @@ __device__ __forceinline__ void epilogue_row32(const GemmParams& p, int n0, floa
         bv[2 * j + 1] = __uint_as_float(wv[j] & 0xFFFF0000u);
       }
     }
-    uint32_t packed[4];
+    uint32_t packed[8];  // fp32: all 8 values; 16-bit types: 4 pairs
 #pragma unroll
     for (int i = 0; i < 8; i += 2) {
       const uint32_t r0 = v[OFF + 8 * s8 + i], r1 = v[OFF + 8 * s8 + i + 1];
@@ -315,19 +337,30 @@ __device__ __forceinline__ void epilogue_row32(const GemmParams& p, int n0, floa
         x0 = __fadd_rn(x0, bv[i]);
         x1 = __fadd_rn(x1, bv[i + 1]);
       }
-      packed[i / 2] = pack_bf16x2(x0, x1);
+      if constexpr (OT == OutType::F32) {
+        packed[i] = __float_as_uint(x0);
+        packed[i + 1] = __float_as_uint(x1);
+      } else {
+        packed[i / 2] = pack_out16x2<OT>(x0, x1);
+      }
     }
-    st_shared_v4(block + 64 * lane + 16 * (s8 ^ ((lane >> 1) & 3)), packed[0], packed[1], packed[2], packed[3]);
+    if constexpr (OT == OutType::F32) {
+      const uint32_t row = block + 128 * lane;
+      st_shared_v4(row + 16 * ((2 * s8) ^ (lane & 7)), packed[0], packed[1], packed[2], packed[3]);
+      st_shared_v4(row + 16 * ((2 * s8 + 1) ^ (lane & 7)), packed[4], packed[5], packed[6], packed[7]);
+    } else {
+      st_shared_v4(block + 64 * lane + 16 * (s8 ^ ((lane >> 1) & 3)), packed[0], packed[1], packed[2], packed[3]);
+    }
   }
 }
 
 // The same epilogue with the 8-column pieces stored straight to row m of the
 // output (16-byte stores; no staging).
-template <bool ROWWISE, bool INT_ACC, int OFF = 0, bool ALPHA = false, int LEN = 32>
+template <bool ROWWISE, bool INT_ACC, int OFF = 0, bool ALPHA = false, OutType OT = OutType::BF16, int LEN = 32>
 __device__ __forceinline__ void epilogue_row32_global(const GemmParams& p, int m, int n0, float sam,
                                                       const uint32_t (&v)[LEN]) {
   const bool has_bias = p.bias != nullptr;
-  uint16_t* dst = p.out + static_cast<size_t>(m) * static_cast<size_t>(p.N) + n0;
+  const size_t first = static_cast<size_t>(m) * static_cast<size_t>(p.N) + n0;
 #pragma unroll
   for (int s8 = 0; s8 < 4; ++s8) {
     const int n = n0 + 8 * s8;
@@ -349,7 +382,7 @@ __device__ __forceinline__ void epilogue_row32_global(const GemmParams& p, int m
           bv[2 * j + 1] = __uint_as_float(wv[j] & 0xFFFF0000u);
         }
       }
-      uint32_t packed[4];
+      uint32_t packed[8];
 #pragma unroll
       for (int i = 0; i < 8; i += 2) {
         const uint32_t r0 = v[OFF + 8 * s8 + i], r1 = v[OFF + 8 * s8 + i + 1];
@@ -364,9 +397,21 @@ __device__ __forceinline__ void epilogue_row32_global(const GemmParams& p, int m
           x0 = __fadd_rn(x0, bv[i]);
           x1 = __fadd_rn(x1, bv[i + 1]);
         }
-        packed[i / 2] = pack_bf16x2(x0, x1);
+        if constexpr (OT == OutType::F32) {
+          packed[i] = __float_as_uint(x0);
+          packed[i + 1] = __float_as_uint(x1);
+        } else {
+          packed[i / 2] = pack_out16x2<OT>(x0, x1);
+        }
       }
-      reinterpret_cast<uint4*>(dst)[s8] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+      if constexpr (OT == OutType::F32) {
+        uint4* dst = reinterpret_cast<uint4*>(static_cast<float*>(p.out) + first) + 2 * s8;
+        dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+        dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+      } else {
+        uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + first);
+        dst[s8] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+      }
     }
   }
 }
@@ -1015,10 +1060,10 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
           if (!(block_ok && n0 < p.N)) return;
           if constexpr (C::STORE_TMA) {
             const uint32_t block = out_block_acquire<C>(ostg, lane);
-            epilogue_row32<C::ROWWISE || kInt, kInt, kOff, C::ALPHA>(p, n0, sam, vals, block, lane);
+            epilogue_row32<C::ROWWISE || kInt, kInt, kOff, C::ALPHA, C::OUT>(p, n0, sam, vals, block, lane);
             out_block_release<C>(ostg, block, &tmOut, n0, m_block, lane);
           } else if (row_ok) {
-            epilogue_row32_global<C::ROWWISE || kInt, kInt, kOff, C::ALPHA>(p, m, n0, sam, vals);
+            epilogue_row32_global<C::ROWWISE || kInt, kInt, kOff, C::ALPHA, C::OUT>(p, m, n0, sam, vals);
           }
         };
         if constexpr (C::REG_DRAIN) {

@@ -22,6 +22,10 @@ namespace qk {
 // (all 512 TMEM columns); 16 epilogue warps keep the int32 running sums in
 // registers, so a chunk drains while the MMAs fill the other accumulator.
 using CfgInt8 = GemmCfg<Kind::F16, 256, 6, 2, true, 16, 1>;
+// fp16 output: the same layout; fp32 output: 4 KB staging blocks per
+// epilogue warp, so one ring stage fewer fits in shared memory.
+using CfgInt8F16 = GemmCfg<Kind::F16, 256, 6, 2, true, 16, 1, OutType::F16>;
+using CfgInt8F32 = GemmCfg<Kind::F16, 256, 5, 2, true, 16, 1, OutType::F32>;
 
 // Widens 16 int8 values per thread-iteration to f16.  Byte x becomes the f16
 // bit pattern 0x6400 | (x + 128), i.e. the value 1024 + x + 128, and one
@@ -59,11 +63,12 @@ static __global__ void __launch_bounds__(256) qk_int8_to_f16_kernel(const uint4*
 }
 
 // Widens A and B into a16 [M, K] and b16 [N, K] (caller-provided device
-// memory) and runs the GEMM over them, both on `stream`.
+// memory) and runs the GEMM over them, both on `stream`; C fixes the output
+// element type.
+template <class C = CfgInt8>
 static inline int widen_and_gemm_int8(const int8_t* A, const int8_t* B, const float* sa, const float* sb,
-                                      const uint16_t* bias, uint16_t* out, int M, int N, int K, uint16_t* a16,
+                                      const uint16_t* bias, void* out, int M, int N, int K, uint16_t* a16,
                                       uint16_t* b16, const DeviceInfo& dev, cudaStream_t stream) {
-  using C = CfgInt8;
   const size_t a_elems = static_cast<size_t>(M) * K;
   const size_t b_elems = static_cast<size_t>(N) * K;
   const long long na = static_cast<long long>(a_elems / 16), nb = static_cast<long long>(b_elems / 16);

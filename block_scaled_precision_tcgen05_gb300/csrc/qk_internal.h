@@ -35,7 +35,9 @@ int encode_tmap_2d_plain(CUtensorMap* map, CUtensorMapDataType dtype, const void
                          uint64_t rows, uint64_t row_pitch_bytes, uint32_t box_inner, uint32_t box_rows);
 
 // bf16 [rows, cols] output in 32x32 boxes with the 64-byte swizzle.
-int encode_tmap_out(CUtensorMap* map, void* out, uint64_t rows, uint64_t cols);
+// The output as 32x32 boxes: bf16 / fp16 with the 64-byte swizzle, fp32 with
+// the 128-byte swizzle (out_type: a QK_OUT_* value).
+int encode_tmap_out(CUtensorMap* map, void* out, uint64_t rows, uint64_t cols, int out_type);
 
 uint64_t wait_timeout_ns();
 void count_launches(uint64_t n);
@@ -64,6 +66,9 @@ struct LaunchTimer {
 };
 
 // Per-format launchers (arguments already validated).
+int launch_int8_rowwise_out(const int8_t* A, const int8_t* B, const float* sa, const float* sb,
+                            const uint16_t* bias, void* out, int out_type, int M, int N, int K, const DeviceInfo& dev,
+                            cudaStream_t stream);
 int launch_int8_rowwise(const int8_t* A, const int8_t* B, const float* sa, const float* sb, const uint16_t* bias,
                         uint16_t* out, int M, int N, int K, const DeviceInfo& dev, cudaStream_t stream);
 int launch_fp8_rowwise(const uint8_t* A, const uint8_t* B, const float* sa, const float* sb, const uint16_t* bias,

@@ -81,9 +81,10 @@ int launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap&
   }
   const int ctas = (p.num_tiles < slots ? p.num_tiles : slots) * C::CTAS;
   cfg.gridDim = dim3(ctas, 1, 1);
-  // the output as 32x32 bf16 boxes with the 64-byte swizzle of the staging blocks
+  // the output as 32x32 boxes with the swizzle of the staging blocks
   CUtensorMap tout;
-  if (encode_tmap_out(&tout, p.out, static_cast<uint64_t>(p.M), static_cast<uint64_t>(p.N)) != QK_OK)
+  if (encode_tmap_out(&tout, p.out, static_cast<uint64_t>(p.M), static_cast<uint64_t>(p.N),
+                      static_cast<int>(C::OUT)) != QK_OK)
     return QK_ERR_CUDA;
   LaunchTimer timer(kernel_kind<C>(), stream);
   e = cudaLaunchKernelEx(&cfg, kernel, ta, tb, tsa, tsb, tout, p);

@@ -60,6 +60,11 @@ typedef void* qk_stream_t;
 #define QK_FMT_MXFP8_E4M3 1 /* A, B: one E4M3 byte per element */
 #define QK_FMT_MXFP4_E2M1 2 /* A, B: two E2M1 codes per byte, element 2i in the low nibble */
 
+/* ---- output element types for qk_gemm_int8_rowwise_out ----------------- */
+#define QK_OUT_BF16 0 /* 2 bytes, bf16 round to nearest even */
+#define QK_OUT_FP16 1 /* 2 bytes, IEEE half round to nearest even (beyond 65504: +-inf) */
+#define QK_OUT_FP32 2 /* 4 bytes, the fp32 value x itself */
+
 /*
  * INT8 GEMM with per-row and per-column fp32 scales and an optional bias.
  * (comfy-kitchen PR #174, Summary: "cache row/column scales and bias values
@@ -85,6 +90,22 @@ typedef void* qk_stream_t;
 int qk_gemm_int8_rowwise(const int8_t* A, const int8_t* B, const float* sa, const float* sb,
                          const uint16_t* bias, uint16_t* out, int64_t M, int64_t N, int64_t K,
                          qk_stream_t stream);
+
+/*
+ * qk_gemm_int8_rowwise with a choice of output element type (comfy-kitchen
+ * PR #174, update "rebased onto v0.2.38": the page's INT8 kernel
+ * specialization serves bf16, fp16 and fp32 output types).  The same x as
+ * above, then
+ *   out_type QK_OUT_BF16: out bf16 [M, N] = bf16_rne(x)   (as qk_gemm_int8_rowwise)
+ *            QK_OUT_FP16: out fp16 [M, N] = fp16_rne(x)   (+-inf beyond the fp16 range)
+ *            QK_OUT_FP32: out fp32 [M, N] = x
+ * `out` points to M * N elements of that type.  Arguments, requirements,
+ * workspace and bit-exactness as for qk_gemm_int8_rowwise; an unknown
+ * out_type returns QK_ERR_ARG.
+ */
+int qk_gemm_int8_rowwise_out(const int8_t* A, const int8_t* B, const float* sa, const float* sb,
+                             const uint16_t* bias, void* out, int out_type, int64_t M, int64_t N, int64_t K,
+                             qk_stream_t stream);
 
 /*
  * qk_gemm_int8_rowwise without any memory allocation.  (The pages have no

@@ -63,6 +63,8 @@ def _declare(lib):
     lib.qko_decode_ue4m3.restype = c.c_double
     lib.qko_f32_to_bf16_rne.argtypes = [c.c_float]
     lib.qko_f32_to_bf16_rne.restype = c.c_uint16
+    lib.qko_f32_to_f16_rne.argtypes = [c.c_float]
+    lib.qko_f32_to_f16_rne.restype = c.c_uint16
     lib.qko_bf16_to_f32.argtypes = [c.c_uint16]
     lib.qko_bf16_to_f32.restype = c.c_float
     lib.qko_encode_e4m3.argtypes = [c.c_double]
@@ -75,6 +77,8 @@ def _declare(lib):
     lib.qko_ptpc_quantize_row.restype = None
     lib.qko_gemm_int8_rowwise.argtypes = [P, P, P, P, P, P, i64, i64, i64, i64, i64, i64, i64, i64, P]
     lib.qko_gemm_int8_rowwise.restype = c.c_int
+    lib.qko_gemm_int8_rowwise_out.argtypes = [P, P, P, P, P, P, c.c_int, i64, i64, i64, i64, i64, i64, i64, i64, P]
+    lib.qko_gemm_int8_rowwise_out.restype = c.c_int
     lib.qko_gemm_fp8_rowwise.argtypes = [P, P, P, P, P, P, i64, i64, i64, i64, i64, i64, i64, i64]
     lib.qko_gemm_fp8_rowwise.restype = c.c_int
     lib.qko_gemm_mx.argtypes = [c.c_int, P, P, P, P, P, P, i64, i64, i64, i64, i64, i64, i64, i64]
@@ -145,6 +149,13 @@ def f32_to_bf16(x, lib=None):
                     dtype=np.uint16).reshape(np.shape(x))
 
 
+def f32_to_f16(x, lib=None):
+    """IEEE binary16 bits (uint16) of fp32 values, round to nearest even."""
+    lib = lib or load()
+    return np.array([lib.qko_f32_to_f16_rne(float(v)) for v in np.ravel(np.asarray(x, np.float32))],
+                    dtype=np.uint16).reshape(np.shape(x))
+
+
 def bf16_to_f32(b, lib=None):
     lib = lib or load()
     return np.array([lib.qko_bf16_to_f32(int(v)) for v in np.ravel(b)], dtype=np.float32).reshape(np.shape(b))
@@ -204,8 +215,14 @@ def _region(M, N, m0, m1, n0, n1):
     return m0, m1, n0, n1
 
 
-def gemm_int8_rowwise(A, B, sa, sb, bias=None, m0=0, m1=None, n0=0, n1=None, return_acc=False, lib=None):
-    """bf16 bits (uint16) of the INT8 row/column-scaled GEMM over rows [m0,m1) x cols [n0,n1)."""
+OUT_TYPES = {"bf16": 0, "fp16": 1, "fp32": 2}
+
+
+def gemm_int8_rowwise(A, B, sa, sb, bias=None, m0=0, m1=None, n0=0, n1=None, return_acc=False, lib=None,
+                      out_dtype="bf16"):
+    """The INT8 row/column-scaled GEMM over rows [m0,m1) x cols [n0,n1): bf16 or
+    fp16 bits (uint16, round to nearest even) or the fp32 values themselves
+    (out_dtype "bf16", "fp16" or "fp32")."""
     lib = lib or load()
     A = _c(A, np.int8)
     B = _c(B, np.int8)
@@ -216,10 +233,14 @@ def gemm_int8_rowwise(A, B, sa, sb, bias=None, m0=0, m1=None, n0=0, n1=None, ret
     N = B.shape[0]
     assert B.shape[1] == K and sa.shape == (M,) and sb.shape == (N,)
     m0, m1, n0, n1 = _region(M, N, m0, m1, n0, n1)
-    out = np.zeros((m1 - m0, n1 - n0), np.uint16)
+    out = np.zeros((m1 - m0, n1 - n0), np.float32 if out_dtype == "fp32" else np.uint16)
     acc = np.zeros((m1 - m0, n1 - n0), np.int64) if return_acc else None
-    rc = lib.qko_gemm_int8_rowwise(_ptr(A), _ptr(B), _ptr(sa), _ptr(sb), _ptr(bias), _ptr(out),
-                                   n1 - n0, M, N, K, m0, m1, n0, n1, _ptr(acc))
+    if out_dtype == "bf16":
+        rc = lib.qko_gemm_int8_rowwise(_ptr(A), _ptr(B), _ptr(sa), _ptr(sb), _ptr(bias), _ptr(out),
+                                       n1 - n0, M, N, K, m0, m1, n0, n1, _ptr(acc))
+    else:
+        rc = lib.qko_gemm_int8_rowwise_out(_ptr(A), _ptr(B), _ptr(sa), _ptr(sb), _ptr(bias), _ptr(out),
+                                           OUT_TYPES[out_dtype], n1 - n0, M, N, K, m0, m1, n0, n1, _ptr(acc))
     if rc != OK:
         raise ValueError(f"oracle int8 gemm failed with code {rc}")
     return (out, acc) if return_acc else out

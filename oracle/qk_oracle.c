@@ -65,6 +65,10 @@
 #define QKO_FMT_MXFP8_E4M3 1
 #define QKO_FMT_MXFP4_E2M1 2
 
+#define QKO_OUT_BF16 0
+#define QKO_OUT_FP16 1
+#define QKO_OUT_FP32 2
+
 /* ------------------------------------------------------------------ */
 /* Format decode tables (OCP MX v1.0 element and scale formats)        */
 /* ------------------------------------------------------------------ */
@@ -148,6 +152,36 @@ uint16_t qko_f32_to_bf16_rne(float x) {
   uint32_t lsb = (u >> 16) & 1u;
   u += 0x7fffu + lsb;
   return (uint16_t)(u >> 16);
+}
+
+/* fp32 -> IEEE binary16 with round-to-nearest, ties to even, from the value:
+ * the result is the multiple of the binary16 spacing of x's binade (2^(e-10)
+ * for |x| in [2^e, 2^(e+1)), e >= -14; 2^-24 below 2^-14, the subnormals)
+ * nearest to |x|, ties to the even multiple.  A result above 65504 is +-Inf
+ * (from |x| >= 65520, the midpoint to 2^16).  The sign is kept (-0 stays
+ * -0); NaN stays NaN (quiet).  The division by the spacing and the product
+ * back are exact in double. */
+uint16_t qko_f32_to_f16_rne(float x) {
+  uint32_t u;
+  memcpy(&u, &x, sizeof u);
+  const uint16_t sign = (uint16_t)((u >> 16) & 0x8000u);
+  if (x != x) return (uint16_t)(sign | 0x7e00u);
+  double v = fabs((double)x);
+  if (isinf(v)) return (uint16_t)(sign | 0x7c00u);
+  if (v == 0.0) return sign;
+  int e2;
+  (void)frexp(v, &e2);                 /* v = f * 2^e2, f in [0.5, 1): binade e2 - 1 */
+  int e = e2 - 1;
+  if (e < -14) e = -14;                /* subnormals share the spacing 2^-24 */
+  const double spacing = ldexp(1.0, e - 10);
+  const double r = nearbyint(v / spacing) * spacing;  /* ties to even (default rounding mode) */
+  if (r > 65504.0) return (uint16_t)(sign | 0x7c00u);
+  if (r < ldexp(1.0, -14)) return (uint16_t)(sign | (uint16_t)(r / ldexp(1.0, -24)));
+  int re2;
+  const double f = frexp(r, &re2);     /* r = f * 2^re2, f in [0.5, 1) */
+  const uint32_t biased = (uint32_t)(re2 - 1 + 15);
+  const uint32_t mant = (uint32_t)((2.0 * f - 1.0) * 1024.0);
+  return (uint16_t)(sign | (biased << 10) | mant);
 }
 
 float qko_bf16_to_f32(uint16_t b) {
@@ -252,20 +286,25 @@ void qko_ptpc_quantize_row(const float* x, int64_t K, uint8_t* codes, float* sca
 /* INT8 row/column-scaled GEMM  [CK174]                                */
 /* ------------------------------------------------------------------ */
 
-/* Fills out[(m-m0)*ldo + (n-n0)] (bf16 bits) for m in [m0,m1), n in [n0,n1).
+/* Fills out[(m-m0)*ldo + (n-n0)] for m in [m0,m1), n in [n0,n1).
  *  1. acc = sum_k (int64)A[m,k] * (int64)B[n,k]; must fit in int32.
  *  2. x   = (float)acc                      (fp32, round to nearest even)
  *  3. x   = x * sa[m];  x = x * sb[n]       (two fp32 roundings, that order)
  *  4. if bias: x = x + (float)bias[n]       (bf16 widened exactly; one add)
  *     without bias no add happens, so a -0 from step 3 survives.
- *  5. out = bf16 round-to-nearest-even of x.
+ *  5. out = x in the output type: QKO_OUT_BF16 (uint16 bits, bf16 round to
+ *     nearest even), QKO_OUT_FP16 (uint16 bits, binary16 round to nearest
+ *     even) or QKO_OUT_FP32 (x itself).  The page's INT8 kernel
+ *     specialization serves all three output types (update "rebased onto
+ *     v0.2.38", its resources paragraph); bf16 is the one its numbers use.
  * acc_out (nullable) receives the int64 sums with the same indexing. */
-int qko_gemm_int8_rowwise(const int8_t* A, const int8_t* B, const float* sa, const float* sb,
-                          const uint16_t* bias, uint16_t* out, int64_t ldo, int64_t M, int64_t N,
-                          int64_t K, int64_t m0, int64_t m1, int64_t n0, int64_t n1,
-                          int64_t* acc_out) {
+int qko_gemm_int8_rowwise_out(const int8_t* A, const int8_t* B, const float* sa, const float* sb,
+                              const uint16_t* bias, void* out, int out_type, int64_t ldo, int64_t M, int64_t N,
+                              int64_t K, int64_t m0, int64_t m1, int64_t n0, int64_t n1,
+                              int64_t* acc_out) {
   if (!A || !B || !sa || !sb || !out || M < 0 || N < 0 || K < 0) return QKO_ERR_ARG;
   if (m0 < 0 || n0 < 0 || m1 > M || n1 > N || m0 > m1 || n0 > n1 || ldo < n1 - n0) return QKO_ERR_ARG;
+  if (out_type != QKO_OUT_BF16 && out_type != QKO_OUT_FP16 && out_type != QKO_OUT_FP32) return QKO_ERR_ARG;
   int bad = 0;
 #pragma omp parallel for collapse(2) schedule(static) reduction(| : bad)
   for (int64_t m = m0; m < m1; ++m) {
@@ -279,11 +318,25 @@ int qko_gemm_int8_rowwise(const int8_t* A, const int8_t* B, const float* sa, con
       x = x * sa[m];
       x = x * sb[n];
       if (bias) x = x + qko_bf16_to_f32(bias[n]);
-      out[(m - m0) * ldo + (n - n0)] = qko_f32_to_bf16_rne(x);
-      if (acc_out) acc_out[(m - m0) * ldo + (n - n0)] = acc;
+      const int64_t o = (m - m0) * ldo + (n - n0);
+      if (out_type == QKO_OUT_FP32)
+        ((float*)out)[o] = x;
+      else if (out_type == QKO_OUT_FP16)
+        ((uint16_t*)out)[o] = qko_f32_to_f16_rne(x);
+      else
+        ((uint16_t*)out)[o] = qko_f32_to_bf16_rne(x);
+      if (acc_out) acc_out[o] = acc;
     }
   }
   return bad ? QKO_ERR_INT32 : QKO_OK;
+}
+
+/* The bf16 output of qko_gemm_int8_rowwise_out. */
+int qko_gemm_int8_rowwise(const int8_t* A, const int8_t* B, const float* sa, const float* sb,
+                          const uint16_t* bias, uint16_t* out, int64_t ldo, int64_t M, int64_t N,
+                          int64_t K, int64_t m0, int64_t m1, int64_t n0, int64_t n1,
+                          int64_t* acc_out) {
+  return qko_gemm_int8_rowwise_out(A, B, sa, sb, bias, out, QKO_OUT_BF16, ldo, M, N, K, m0, m1, n0, n1, acc_out);
 }
 
 /* ------------------------------------------------------------------ */

@@ -110,6 +110,29 @@ def check_bf16_rne(lib):
     assert np.array_equal(oracle.f32_to_bf16(x, lib), _torch_bf16_bits(x))
 
 
+def check_f16_rne(lib):
+    # IEEE 754 binary16: 10 fraction bits, bias 15, subnormal spacing 2^-24, max 65504
+    f16 = lambda v: int(oracle.f32_to_f16([v], lib)[0])
+    assert f16(1.0) == 0x3C00 and f16(-2.0) == 0xC000 and f16(17.0) == 0x4C40
+    assert f16(1 + 2 ** -11) == 0x3C00        # tie, even stays
+    assert f16(1 + 3 * 2 ** -11) == 0x3C02    # tie, odd rounds up
+    assert f16(65504.0) == 0x7BFF and f16(65519.99) == 0x7BFF
+    assert f16(65520.0) == 0x7C00             # the midpoint to 2^16 rounds out of range
+    assert f16(2.0 ** -14) == 0x0400 and f16(2.0 ** -24) == 0x0001
+    assert f16(2.0 ** -25) == 0x0000 and f16(3 * 2.0 ** -25) == 0x0002  # subnormal ties to even
+    assert f16(-0.0) == 0x8000 and f16(float("inf")) == 0x7C00
+    nanh = f16(float("nan"))
+    assert (nanh & 0x7C00) == 0x7C00 and (nanh & 0x3FF) != 0
+    # every finite bf16 value, and random fp32 bit patterns, against numpy's conversion
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    v = qk_inputs.from_bf16_bits(bits)
+    rng = np.random.default_rng(12)
+    r = rng.integers(0, 2 ** 32, size=4000, dtype=np.uint64).astype(np.uint32).view(np.float32)
+    x = np.concatenate([v[np.isfinite(v)], r[np.isfinite(r)]]).astype(np.float32)
+    with np.errstate(over="ignore"):
+        assert np.array_equal(oracle.f32_to_f16(x, lib), x.astype(np.float16).view(np.uint16))
+
+
 def check_encoders(lib):
     # every finite code round-trips
     for c in range(256):
@@ -287,6 +310,30 @@ def check_int8_signed_zero(lib):
     out = oracle.gemm_int8_rowwise(a, b, np.array([1.0], np.float32), np.array([1.0], np.float32),
                                    bias=np.array([0x3F80], np.uint16), lib=lib)
     assert out[0, 0] == _torch_bf16_bits(np.array([-2.0], np.float32))[0]
+
+
+def check_int8_output_types(lib):
+    # by hand: 1+2+...+16 = 136, times 0.5 and 0.25 = 17.0 exactly in every type
+    A = np.arange(1, 17, dtype=np.int8).reshape(1, 16)
+    B = np.ones((1, 16), np.int8)
+    half, quarter = np.full(1, 0.5, np.float32), np.full(1, 0.25, np.float32)
+    assert oracle.gemm_int8_rowwise(A, B, half, quarter, out_dtype="fp32", lib=lib)[0, 0] == 17.0
+    assert oracle.gemm_int8_rowwise(A, B, half, quarter, out_dtype="fp16", lib=lib)[0, 0] == 0x4C40
+    # beyond the fp16 range: 127*127*16 = 258064 is +Inf in fp16, finite in bf16
+    A = np.full((1, 16), 127, np.int8)
+    one = np.ones(1, np.float32)
+    assert oracle.gemm_int8_rowwise(A, A, one, one, out_dtype="fp16", lib=lib)[0, 0] == 0x7C00
+    assert oracle.gemm_int8_rowwise(A, A, one, one, out_dtype="fp32", lib=lib)[0, 0] == 258064.0
+    # the three outputs are roundings of one fp32 value x (with and without bias)
+    for bias in (False, True):
+        p = qk_inputs.int8_problem(19, 40, 160, seed=23, bias=bias)
+        x = oracle.gemm_int8_rowwise(p.A, p.B, p.sa, p.sb, bias=p.bias, out_dtype="fp32", lib=lib)
+        assert x.dtype == np.float32
+        bf = oracle.gemm_int8_rowwise(p.A, p.B, p.sa, p.sb, bias=p.bias, lib=lib)
+        h = oracle.gemm_int8_rowwise(p.A, p.B, p.sa, p.sb, bias=p.bias, out_dtype="fp16", lib=lib)
+        assert np.array_equal(bf, _torch_bf16_bits(x))
+        with np.errstate(over="ignore"):
+            assert np.array_equal(h, x.astype(np.float16).view(np.uint16))
 
 
 def check_int8_pow2_invariance(lib):
@@ -515,10 +562,10 @@ def check_blockscale_reduces_to_ptpc(lib):
 
 
 ALL_CHECKS = [
-    check_e4m3_decode, check_e2m1_decode, check_ue8m0_decode, check_bf16_rne, check_encoders,
+    check_e4m3_decode, check_e2m1_decode, check_ue8m0_decode, check_bf16_rne, check_f16_rne, check_encoders,
     check_mx_quantize_block, check_ptpc_quantize, check_int8_acc_vs_numpy, check_int8_hand_examples,
     check_int8_identity_and_extremes, check_int8_epilogue_order, check_int8_signed_zero,
-    check_int8_pow2_invariance, check_fp8_vs_numpy, check_mx_block_structure,
+    check_int8_output_types, check_int8_pow2_invariance, check_fp8_vs_numpy, check_mx_block_structure,
     check_mx_scale_doubling, check_mx_vs_numpy, check_ue4m3_decode, check_nvfp4_block_structure,
     check_nvfp4_vs_numpy, check_nvfp4_reduces_to_mxfp4, check_blockscale_block_structure,
     check_blockscale_vs_numpy, check_blockscale_reduces_to_ptpc,

@@ -31,6 +31,12 @@ MUTANTS = {
     "e2m1_exponent_bias": ("mag = ldexp(1.0 + (double)m / 2.0, (int)e - 1);", "mag = ldexp(1.0 + (double)m / 2.0, (int)e - 2);"),
     "ue8m0_bias": ("return ldexp(1.0, (int)code - 127);", "return ldexp(1.0, (int)code - 128);"),
     "bf16_truncates": ("u += 0x7fffu + lsb;", "(void)lsb;"),
+    "f16_ties_away": ("nearbyint(v / spacing)", "floor(v / spacing + 0.5)"),
+    "f16_overflow_saturates": ("if (r > 65504.0) return (uint16_t)(sign | 0x7c00u);",
+                               "if (r > 65504.0) return (uint16_t)(sign | 0x7bffu);"),
+    "f16_subnormal_spacing": ("if (e < -14) e = -14;", "if (e < -15) e = -15;"),
+    "int8_fp32_out_rounded": ("((float*)out)[o] = x;", "((float*)out)[o] = qko_bf16_to_f32(qko_f32_to_bf16_rne(x));"),
+    "int8_fp16_out_is_bf16": ("((uint16_t*)out)[o] = qko_f32_to_f16_rne(x);", "((uint16_t*)out)[o] = qko_f32_to_bf16_rne(x);"),
     "fp4_decoded_as_e4m3": ("return g_e2m1[nib];", "return g_e4m3[nib];"),
     "mx_block_index_dropped": ("g_ue8m0[sB[n * kb + blk]]", "g_ue8m0[sB[n * kb]]"),
     "mx_b_scale_dropped": ("acc += g_ue8m0[sA[m * kb + blk]] * g_ue8m0[sB[n * kb + blk]] * inner;",
