@@ -17,7 +17,10 @@
  *           cached scales and bias; signed zero without bias), Validation
  *           (the results match the reference bit for bit, zero error), and
  *           the update "Keep the cached INT8 epilogue scale order exact"
- *           ((acc*sa)*sb, never acc*(sa*sb)).
+ *           ((acc*sa)*sb, never acc*(sa*sb)); the update "rebased onto
+ *           v0.2.38" (the INT8 kernel specialization serves bf16, fp16 and
+ *           fp32 outputs; read as the same x rounded per IEEE binary16 or
+ *           kept).
  *  [MORI806] ROCm/mori PR #806 "perf(gemm-ar): mxfp8 with row-major scales
  *           staged through LDS", section "What": 32-wide ue8m0 scales held
  *           raw, row-major, one byte per 32 K-elements.
@@ -46,7 +49,8 @@
  *  - MX and FP8 accumulate the exact products in fp64 (every product of
  *    decoded elements and power-of-two scales is exact in fp64).
  *  - The INT8 epilogue is evaluated in IEEE fp32 with round-to-nearest-even
- *    at every operation, in the order the pages fix.  Build with
+ *    at every operation, in the order the pages fix.  The bf16 and binary16
+ *    output conversions are written from the formats' definitions.  Build with
  *    -ffp-contract=off and without -ffast-math so no multiply-add is fused.
  *  - Parallelism (OpenMP) is over independent output elements only; each
  *    element's sum runs k = 0..K-1 in order.
