@@ -53,7 +53,9 @@ def test_python_binding_rejects_bad_tensors():
     with pytest.raises(qk.QkError) as e:
         qk.gemm_int8_rowwise(A[:, :40].contiguous(), B[:, :40].contiguous(), sa, sb)
     assert e.value.status == qk.QK_ERR_ALIGN
-    out = torch.empty((128, 64), dtype=torch.float16, device="cuda")
-    with pytest.raises(ValueError):
-        qk.gemm_int8_rowwise(A, B, sa, sb, out=out)
+    with pytest.raises(ValueError):             # no float64 output type
+        qk.gemm_int8_rowwise(A, B, sa, sb, out=torch.empty((128, 64), dtype=torch.float64, device="cuda"))
+    with pytest.raises(ValueError):             # out's dtype contradicts out_dtype
+        qk.gemm_int8_rowwise(A, B, sa, sb, out=torch.empty((128, 64), dtype=torch.float16, device="cuda"),
+                             out_dtype=torch.float32)
     np.testing.assert_array_equal(qk.gemm_int8_rowwise(A, B, sa, sb).float().cpu().numpy(), 0)
