@@ -168,13 +168,14 @@ int qk_gemm_mx(int fmt, const void* A, const uint8_t* sA, const void* B, const u
  *   A uint8 [M, K] E4M3FN; B uint8 [N, K] E4M3FN; sa fp32 [M]; sb fp32 [N];
  *   bias bf16 [N] or NULL; out bf16 [M, N].
  * Requirements: as qk_gemm_int8_rowwise, without the K upper bound.
- * With M <= 128 the weight-streaming path runs.  When the weight tiles do not
- * fit on the GPU in one wave of split-K clusters it is a cooperative
- * stream-K launch that takes a stream-ordered workspace from the library's
- * pool (one fp32 partial of at most 128 x 128 values and four 8-byte flags
- * per SM, returned at the end of the call); QK_ERR_NOMEM if that allocation
- * fails.  Partials of a shared tile are added in a fixed order, so repeated
- * calls give identical bits.
+ * With M <= 128 a weight-streaming kernel runs: split-K over clusters when
+ * all weight tiles' clusters fit on the GPU at once and each CTA keeps a deep
+ * enough K range (otherwise, in that case, the regular tile kernel), else a
+ * cooperative stream-K launch that takes a stream-ordered workspace from the
+ * library's pool (one fp32 partial of at most 128 x 128 values and four
+ * 8-byte flags per SM, returned at the end of the call); QK_ERR_NOMEM if that
+ * allocation fails.  Partials of a shared tile are added in a fixed order, so
+ * repeated calls give identical bits.
  */
 int qk_gemm_fp8_rowwise(const uint8_t* A, const uint8_t* B, const float* sa, const float* sb,
                         const uint16_t* bias, uint16_t* out, int64_t M, int64_t N, int64_t K,
