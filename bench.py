@@ -17,7 +17,8 @@ needed between headline steps; the secondary workloads, some of which fit in
 L2, flush it before every timed call by reading a 256 MB buffer.
 
 --impl reference times the CPU oracle on a bounded sample of the same
-workload (the reference arm of this build: the pages hold no runnable code).
+workload (the source pages hold no runnable code, so the oracle stands in as
+the reference).
 """
 from __future__ import annotations
 
