@@ -24,6 +24,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import os
 import statistics
@@ -107,13 +108,22 @@ HEADLINE_SOURCES = ("qk_api.cu", "qk_device.cuh", "qk_gemm_kernel.cuh", "qk_int8
                     "qk_internal.h", "qk_launch.cuh")
 
 
+def _strip_comments(text: str) -> str:
+    """C/C++ source without its comments (none of the hashed files has a
+    comment marker inside a string literal)."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return re.sub(r"//[^\n]*", "", text)
+
+
 def kernel_source_hash() -> str:
-    """Hash of the headline kernel's sources: a committed DRAM-traffic figure counts only while it matches."""
+    """Hash of the headline kernel's sources, comments left out: a committed
+    DRAM-traffic figure counts only while the code it was captured on is
+    unchanged."""
     h = hashlib.sha1()
     for path in [os.path.join(CSRC, n) for n in HEADLINE_SOURCES]:
-        with open(path, "rb") as f:
+        with open(path, encoding="utf-8") as f:
             h.update(os.path.basename(path).encode())
-            h.update(f.read())
+            h.update(_strip_comments(f.read()).encode())
     return h.hexdigest()[:16]
 
 
