@@ -109,10 +109,11 @@ HEADLINE_SOURCES = ("qk_api.cu", "qk_device.cuh", "qk_gemm_kernel.cuh", "qk_int8
 
 
 def _strip_comments(text: str) -> str:
-    """C/C++ source without its comments (none of the hashed files has a
-    comment marker inside a string literal)."""
+    """C/C++ source without its comments, trailing blanks and empty lines
+    (none of the hashed files has a comment marker inside a string literal)."""
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return re.sub(r"//[^\n]*", "", text)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(line.rstrip() for line in text.split("\n") if line.strip())
 
 
 def kernel_source_hash() -> str:

@@ -1,30 +1,41 @@
 // qk_gemm_kernel.cuh -- the persistent, warp-specialised tcgen05 GEMM
 //
-//     out[m,n] = bf16( epilogue( sum_k A[m,k] * B[n,k] ) )
+//     out[m,n] = round_out( epilogue( sum_k A[m,k] * B[n,k] ) )
 //
-// A [M,K] and B [N,K] are K-major.  One CTA per SM walks output tiles of
-// 128 x BN in a grouped-M raster.  Roles (256 threads):
+// A [M,K] and B [N,K] are K-major; round_out is bf16 round-to-nearest-even
+// unless the configuration's OutType says fp16 or fp32.  Persistent CTAs
+// (one per SM, or one 2-SM pair per two SMs) walk output tiles of
+// 128 x BN (a pair: 256 x BN) in a grouped-M raster.  Roles:
 //   warp 0      TMA producer: A/B tiles of 128-byte K rows into a STAGES-deep
 //               shared-memory ring (128-byte swizzle).
 //   warp 1      MMA issuer: allocates TMEM, copies stage scale factors to TMEM
-//               (MX kinds), issues tcgen05.mma into a TMEM accumulator and
-//               releases ring slots / accumulators with tcgen05.commit.
-//   warp 2      scale stager (MX kinds): reads the raw row-major UE8M0 bytes
-//               and writes them into the shared-memory order tcgen05.cp wants.
-//   warps 4..7  epilogue: TMEM -> registers, fixed-order scale/bias epilogue,
-//               round-to-nearest-even bf16, stores; warp 4+q owns TMEM lanes
-//               32q..32q+31, i.e. tile rows 32q..32q+31.
+//               (block-scaled kinds), issues tcgen05.mma into a TMEM
+//               accumulator and releases ring slots / accumulators with
+//               tcgen05.commit; in a pair's peer CTA it relays the peer's
+//               accumulator releases to the leader.
+//   warp 2      scale stager (block-scaled kinds): reads the raw row-major
+//               scale bytes and writes them into the shared-memory order
+//               tcgen05.cp wants.
+//   warp 3      in a block-scaled pair's peer CTA: relays the scale slots.
+//   warps 4..   EPI_WARPS epilogue warps (4 or 16): TMEM -> registers,
+//               fixed-order scale/bias epilogue, output rounding, staged bulk
+//               tensor stores; warp 4 + 4p + q owns TMEM lanes 32q..32q+31
+//               (tile rows) of column part p.
 //
 // Kinds:
 //   F16   exact INT8: int8 operands converted to f16 beforehand (exact), f16
 //         MMA with fp32 accumulation.  Accumulation restarts every chunk of
 //         at most 1024 K (every partial sum is then an integer below 2^24,
 //         exact in fp32); the epilogue drains each chunk to int32 and adds
-//         them in a TMEM-resident int32 sum, so the result is the exact
-//         integer dot product.
+//         the chunks in int32, so the result is the exact integer dot
+//         product.
 //   F8    E4M3 x E4M3 with fp32 accumulation (per-token x per-channel FP8).
+//   F8BS  E4M3 x E4M3, every 128-K block its own accumulation chunk, folded
+//         into fp32 register sums with its A and B block scales (blockscale).
 //   MXF8  E4M3 with one UE8M0 scale per 32 K (block_scale, scale_vec::1X).
 //   MXF4  packed E2M1 with one UE8M0 scale per 32 K (kind::mxf4, 2X).
+//   NVF4  packed E2M1 with one UE4M3 scale per 16 K (kind::mxf4nvf4, 4X) and
+//         the product of two per-tensor fp32 scales in the epilogue.
 //
 // Epilogue order (comfy-kitchen PR #174, Summary and the update "Keep the
 // cached INT8 epilogue scale order exact"): x = float(acc); x = x*sa[m];
