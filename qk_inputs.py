@@ -343,18 +343,26 @@ def fp8_problem(M: int, N: int, K: int, seed: int = 0, bias: bool = False, weigh
 def sample_tiles(M: int, N: int, count: int, seed: int, tile: int = 128):
     """A seeded sample of output tiles plus every ragged edge tile.
 
-    Returns a list of (m0, m1, n0, n1).  The last row-block and the last
-    column-block are always included (they hold the ragged edges)."""
+    Returns a sorted list of (m0, m1, n0, n1): `count` seeded random tiles,
+    the first and the last (corner) tile, every tile of the last row-block
+    when M is not a multiple of `tile`, every tile of the last column-block
+    when N is not, and otherwise one seeded tile of that last block."""
     rng = np.random.default_rng(seed + 7919)
     mt = (M + tile - 1) // tile
     nt = (N + tile - 1) // tile
     picks = set()
     for _ in range(count):
         picks.add((int(rng.integers(mt)), int(rng.integers(nt))))
-    picks.add((mt - 1, nt - 1))
-    picks.add((mt - 1, int(rng.integers(nt))))
-    picks.add((int(rng.integers(mt)), nt - 1))
     picks.add((0, 0))
+    picks.add((mt - 1, nt - 1))
+    if M % tile:
+        picks.update((mt - 1, bn) for bn in range(nt))
+    else:
+        picks.add((mt - 1, int(rng.integers(nt))))
+    if N % tile:
+        picks.update((bm, nt - 1) for bm in range(mt))
+    else:
+        picks.add((int(rng.integers(mt)), nt - 1))
     out = []
     for bm, bn in sorted(picks):
         out.append((bm * tile, min(M, bm * tile + tile), bn * tile, min(N, bn * tile + tile)))
