@@ -29,6 +29,8 @@ enum : uint32_t {
   kSiteProducerDrain = 7,
   kSiteProbe = 8,
   kSitePeerPartial = 9,  // stream-K: another CTA's partial of a shared tile
+  kSiteMmaScales = 10,    // MMA warp: a ring slot's scale factors copied to TMEM
+  kSiteScaleCopy = 11,    // scale-copy thread: a ring slot's scale atoms written
 };
 
 __device__ __forceinline__ void report_error(unsigned long long* err, uint32_t code, uint32_t site,

@@ -16,7 +16,11 @@
 //   warp 2      scale stager (block-scaled kinds): reads the raw row-major
 //               scale bytes and writes them into the shared-memory order
 //               tcgen05.cp wants.
-//   warp 3      in a block-scaled pair's peer CTA: relays the scale slots.
+//   warp 3      block-scaled kinds: in the MMA-issuing CTA, copies each ring
+//               slot's scale atoms to TMEM (tcgen05.cp) and signals the MMA
+//               warp with tcgen05.commit, so the copies run beside the MMAs
+//               instead of between them; in a pair's peer CTA, relays the
+//               peer's scale slots to the leader.
 //   warps 4..   EPI_WARPS epilogue warps (4 or 16): TMEM -> registers,
 //               fixed-order scale/bias epilogue, output rounding, staged bulk
 //               tensor stores; warp 4 + 4p + q owns TMEM lanes 32q..32q+31
@@ -171,7 +175,9 @@ struct GemmCfg {
   static constexpr int OUT_BLOCK_BYTES = 32 * 32 * OUT_ELEM_BYTES;
   static constexpr int OFF_OUT = ((OFF_RAW + RAW_BUFS * RAW_STAGE_BYTES) + 1023) & ~1023;
   static constexpr int OFF_BAR = OFF_OUT + EPI_WARPS * OUT_BUFS * OUT_BLOCK_BYTES;
-  static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC_BUFS + 1 + RAW_BUFS;
+  // ring full/empty, accumulator full/empty, drain, raw scale fetches, and
+  // (block-scaled kinds) per-slot scale-atom arrivals and scale-copy completions
+  static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC_BUFS + 1 + RAW_BUFS + (MX ? 2 * STAGES : 0);
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack to align the base to 1024
 
@@ -199,11 +205,13 @@ struct GemmCfg {
   static_assert(SMEM_BYTES <= 232448, "shared-memory budget");
   static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "swizzle atoms need 1024-byte alignment");
 
-  // Ring-slot arrivals: the producer's, plus (MX) the scale warp's; in a CTA
-  // pair each CTA stages the scale factors of its own 128 rows of A and of all
-  // BN rows of B at the same offsets, and the leader's barrier counts its own
-  // scale warp and the peer's relay.
-  static constexpr uint32_t FULL_ARRIVALS = 1 + (MX ? (PAIR ? 2 : 1) : 0);
+  // Ring-slot arrivals: the producer's (a pair's leader counts both CTAs' TMA
+  // bytes).  Scale-slot arrivals (block-scaled kinds), on the MMA-issuing CTA:
+  // its own scale warp and, in a pair, the peer's relay -- each CTA of a pair
+  // stages the scale factors of its own 128 rows of A and of all BN rows of B
+  // at the same offsets.
+  static constexpr uint32_t FULL_ARRIVALS = 1;
+  static constexpr uint32_t SF_ARRIVALS = PAIR ? 2 : 1;
 
   // kind::f16: D fp32 (1), A/B f16 (0).  kind::f8f6f4: A/B E4M3 (0).
   // kind::mxf8f6f4: E4M3 (0).  kind::mxf4: E2M1 (1), UE8M0 scales.
@@ -526,20 +534,20 @@ __device__ __forceinline__ void raw_fetch_async(const GemmParams& p, uint32_t ra
 // rearranges each stage's scale bytes into the 512-byte atoms tcgen05.cp
 // reads.  Shared loads and stores are 16 bytes per lane over contiguous
 // 512-byte spans (no bank conflicts).
-// Marks a ring slot's scale atoms as written, on this CTA's full barrier.  In
-// a CTA pair the peer's barrier is a local gather that the peer's relay warp
-// forwards to the leader's with one cluster-scope arrive per slot, so the
-// scale warp itself never waits on a cluster-wide fence.
+// Marks a ring slot's scale atoms as written, on this CTA's scale-slot
+// barrier.  In a CTA pair the peer's barrier is a local gather that the peer's
+// relay warp forwards to the leader's with one arrive per slot, so the scale
+// warp itself never waits on a cluster-wide fence.
 template <class C>
-__device__ __forceinline__ void scale_slot_ready(uint64_t* full, uint32_t /*full_leader*/, int stage) {
-  mbar_arrive(&full[stage]);
+__device__ __forceinline__ void scale_slot_ready(uint64_t* sf_full, int stage) {
+  mbar_arrive(&sf_full[stage]);
 }
 
 template <class C>
 __device__ __forceinline__ void scale_stager_raw(const GemmParams& p, const CUtensorMap* tmSA,
-                                                 const CUtensorMap* tmSB, uint8_t* smem, uint64_t* full,
+                                                 const CUtensorMap* tmSB, uint8_t* smem, uint64_t* sf_full,
                                                  uint64_t* empty, uint64_t* raw_full, const WaitCtl& w, int lane,
-                                                 int tile0, int tile_step, uint32_t rank, uint32_t full_leader) {
+                                                 int tile0, int tile_step, uint32_t rank) {
   const int n_raw = (p.num_kb + C::RAW_KB - 1) / C::RAW_KB;
   const bool by_tma = p.sf_mode == kSfTma;
   auto issue = [&](int t, int r, uint32_t slot) {
@@ -605,7 +613,7 @@ __device__ __forceinline__ void scale_stager_raw(const GemmParams& p, const CUte
                              sub * C::SF_ATOMS_K);
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) scale_slot_ready<C>(full, full_leader, stage);
+        if (lane == 0) scale_slot_ready<C>(sf_full, stage);
         if (++stage == C::STAGES) {
           stage = 0;
           phase ^= 1u;
@@ -633,9 +641,8 @@ __device__ __forceinline__ void scale_stager_raw(const GemmParams& p, const CUte
 // Scale staging with plain loads (any K % 32 == 0): per ring stage, four
 // scale bytes per row and atom, one 32-bit load each.
 template <class C>
-__device__ __forceinline__ void scale_stager_ldg(const GemmParams& p, uint8_t* smem, uint64_t* full, uint64_t* empty,
-                                                 const WaitCtl& w, int lane, int tile0, int tile_step, uint32_t rank,
-                                                 uint32_t full_leader) {
+__device__ __forceinline__ void scale_stager_ldg(const GemmParams& p, uint8_t* smem, uint64_t* sf_full, uint64_t* empty,
+                                                 const WaitCtl& w, int lane, int tile0, int tile_step, uint32_t rank) {
   int stage = 0;
   uint32_t phase = 0;
   bool ok = true;
@@ -673,7 +680,7 @@ __device__ __forceinline__ void scale_stager_ldg(const GemmParams& p, uint8_t* s
       }
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) scale_slot_ready<C>(full, full_leader, stage);
+      if (lane == 0) scale_slot_ready<C>(sf_full, stage);
       if (++stage == C::STAGES) {
         stage = 0;
         phase ^= 1u;
@@ -695,6 +702,8 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
   uint64_t* acc_empty = acc_full + C::ACC_BUFS;
   uint64_t* drain = acc_empty + C::ACC_BUFS;
   uint64_t* raw_full = drain + 1;
+  uint64_t* sf_full = raw_full + C::RAW_BUFS;  // block-scaled kinds: scale atoms of a slot written
+  uint64_t* sf_ready = sf_full + C::STAGES;    // block-scaled kinds: a slot's scale copies in TMEM
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_MISC + 4);
 
@@ -710,9 +719,13 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
   if (threadIdx.x == 0) {
 #pragma unroll 1
     for (int s = 0; s < C::STAGES; ++s) {
-      // a pair's peer counts only its own scale warp (forwarded by its relay)
-      mbar_init(&full[s], C::PAIR && !leader ? 1u : C::FULL_ARRIVALS);
+      mbar_init(&full[s], C::FULL_ARRIVALS);
       mbar_init(&empty[s], 1u);
+      if constexpr (C::MX) {
+        // a pair's peer gathers only its own scale warp (forwarded by its relay)
+        mbar_init(&sf_full[s], C::PAIR && !leader ? 1u : C::SF_ARRIVALS);
+        mbar_init(&sf_ready[s], 1u);
+      }
     }
 #pragma unroll 1
     for (int a = 0; a < C::ACC_BUFS; ++a) {
@@ -836,30 +849,15 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
           const int kb1 = min(p.num_kb, kb0 + p.chunk_kb);
 #pragma unroll 1
           for (int kb = kb0; kb < kb1; ++kb) {
-            // scale slots of a pair are released by the peer's scale warp too
-            const bool landed = (C::PAIR && C::MX) ? mbar_wait_cluster(&full[stage], phase, w, kSiteMmaFull)
-                                                   : mbar_wait(&full[stage], phase, w, kSiteMmaFull);
+            bool landed = mbar_wait(&full[stage], phase, w, kSiteMmaFull);
+            // block-scaled kinds: the slot's scale factors are in TMEM (copied by warp 3)
+            if constexpr (C::MX) landed = landed && mbar_wait(&sf_ready[stage], phase, w, kSiteMmaScales);
             if (!landed) {
               ok = false;
               break;
             }
             tc_fence_after_sync();
             const uint32_t sf_tmem = tmem + static_cast<uint32_t>(C::COL_SF + stage * C::SF_COLS_STAGE);
-            if constexpr (C::MX) {
-              const uint32_t sf_smem = smem_u32(smem + C::OFF_SF + stage * C::SF_STAGE_BYTES);
-#pragma unroll
-              for (int i = 0; i < C::SF_ATOMS_K + C::SF_ATOMS_K * C::NB128; ++i) {
-                // atoms: A's first, then B's; TMEM columns in the same order
-                const uint32_t col = i < C::SF_ATOMS_K ? 4 * i : C::SF_COLS_A + 4 * (i - C::SF_ATOMS_K);
-                const uint32_t src = i < C::SF_ATOMS_K ? sf_smem + 512 * i
-                                                        : sf_smem + C::SFA_BYTES + 512 * (i - C::SF_ATOMS_K);
-                if constexpr (C::PAIR) {
-                  tmem_cp_32x128b_warpx4_pair(sf_tmem + col, make_smem_desc(src, 128, 128, 0));
-                } else {
-                  tmem_cp_32x128b_warpx4(sf_tmem + col, make_smem_desc(src, 128, 128, 0));
-                }
-              }
-            }
             const uint64_t adesc = make_desc_kmajor_sw128(smem_u32(smem + C::OFF_A + stage * C::A_BYTES));
             const uint64_t bdesc = make_desc_kmajor_sw128(smem_u32(smem + C::OFF_B + stage * C::B_BYTES));
             int ksteps = C::K_STEPS;
@@ -971,20 +969,81 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
   } else if (warp == 2) {
     // ---------------- scale stager (MX) ----------------
     if constexpr (C::MX) {
-      const uint32_t full_leader = C::PAIR ? mapa_shared(smem_u32(&full[0]), 0u) : 0u;
       if (p.sf_mode == kSfTma || p.sf_mode == kSfAsync) {
-        scale_stager_raw<C>(p, &tmSA, &tmSB, smem, full, empty, raw_full, w, lane, tile0, tile_step, rank,
-                            full_leader);
+        scale_stager_raw<C>(p, &tmSA, &tmSB, smem, sf_full, empty, raw_full, w, lane, tile0, tile_step, rank);
       } else {
-        scale_stager_ldg<C>(p, smem, full, empty, w, lane, tile0, tile_step, rank, full_leader);
+        scale_stager_ldg<C>(p, smem, sf_full, empty, w, lane, tile0, tile_step, rank);
       }
     }
     __syncwarp();
   } else if (warp == 3) {
+    if constexpr (C::MX) {
+      if (issues_mma && lane == 0) {
+        // ---------------- scale-factor copies (the MMA-issuing CTA) ----------------
+        // Per ring slot: once the atoms are written (both CTAs' in a pair),
+        // copy them into the slot's TMEM columns and commit to sf_ready.  A
+        // slot's atoms are rewritten only after the MMAs that read its
+        // previous copies have completed (the scale warp waits on `empty`).
+        int stage = 0;
+        uint32_t phase = 0;
+        long long issued = 0;
+        bool ok = true;
+#pragma unroll 1
+        for (int t = tile0; ok && t < p.num_tiles; t += tile_step) {
+#pragma unroll 1
+          for (int kb = 0; kb < p.num_kb; ++kb) {
+            const bool ready = C::PAIR ? mbar_wait_cluster(&sf_full[stage], phase, w, kSiteScaleCopy)
+                                       : mbar_wait(&sf_full[stage], phase, w, kSiteScaleCopy);
+            if (!ready) {
+              ok = false;
+              break;
+            }
+            tc_fence_after_sync();
+            const uint32_t sf_tmem = tmem + static_cast<uint32_t>(C::COL_SF + stage * C::SF_COLS_STAGE);
+            const uint32_t sf_smem = smem_u32(smem + C::OFF_SF + stage * C::SF_STAGE_BYTES);
+#pragma unroll
+            for (int i = 0; i < C::SF_ATOMS_K + C::SF_ATOMS_K * C::NB128; ++i) {
+              // atoms: A's first, then B's; TMEM columns in the same order
+              const uint32_t col = i < C::SF_ATOMS_K ? 4 * i : C::SF_COLS_A + 4 * (i - C::SF_ATOMS_K);
+              const uint32_t src = i < C::SF_ATOMS_K ? sf_smem + 512 * i
+                                                      : sf_smem + C::SFA_BYTES + 512 * (i - C::SF_ATOMS_K);
+              if constexpr (C::PAIR) {
+                tmem_cp_32x128b_warpx4_pair(sf_tmem + col, make_smem_desc(src, 128, 128, 0));
+              } else {
+                tmem_cp_32x128b_warpx4(sf_tmem + col, make_smem_desc(src, 128, 128, 0));
+              }
+            }
+            if constexpr (C::PAIR) {
+              umma_commit_pair(&sf_ready[stage]);
+            } else {
+              umma_commit(&sf_ready[stage]);
+            }
+            ++issued;
+            if (++stage == C::STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+        }
+        // leave no copy in flight: the last commit covers every earlier copy
+        if (issued > 0) {
+          const long long L = issued - 1;
+          const uint32_t a = smem_u32(&sf_ready[static_cast<int>(L % C::STAGES)]);
+          const uint32_t par = static_cast<uint32_t>((L / C::STAGES) & 1);
+          const uint64_t t0 = global_timer_ns();
+          while (!mbar_try_wait(a, par)) {
+            if (global_timer_ns() - t0 > p.timeout_ns) {
+              report_error(p.err, kDevErrTimeout, kSiteScaleCopy, static_cast<uint32_t>(L));
+              break;
+            }
+          }
+        }
+      }
+    }
     // ---------------- scale relay (the peer CTA of an MX pair) ----------------
     if constexpr (C::MX && C::PAIR) {
       if (!leader && lane == 0) {
-        const uint32_t full_leader = mapa_shared(smem_u32(&full[0]), 0u);
+        const uint32_t sf_full_leader = mapa_shared(smem_u32(&sf_full[0]), 0u);
         int stage = 0;
         uint32_t phase = 0;
         bool ok = true;
@@ -992,7 +1051,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
         for (int t = tile0; ok && t < p.num_tiles; t += tile_step) {
 #pragma unroll 1
           for (int kb = 0; kb < p.num_kb; ++kb) {
-            if (!mbar_wait(&full[stage], phase, w, kSiteScaleEmpty)) {
+            if (!mbar_wait(&sf_full[stage], phase, w, kSiteScaleEmpty)) {
               ok = false;
               break;
             }
@@ -1000,7 +1059,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
             // CTA's shared memory, where the scale warp's fence.proxy.async and
             // its completed local arrive (observed above) have already put them
             // for the leader's copy to read.
-            mbar_arrive_remote(full_leader + 8u * static_cast<uint32_t>(stage));
+            mbar_arrive_remote(sf_full_leader + 8u * static_cast<uint32_t>(stage));
             if (++stage == C::STAGES) {
               stage = 0;
               phase ^= 1u;
