@@ -16,11 +16,21 @@
 //   warp 2      scale stager (block-scaled kinds): reads the raw row-major
 //               scale bytes and writes them into the shared-memory order
 //               tcgen05.cp wants.
-//   warp 3      block-scaled kinds: in the MMA-issuing CTA, copies each ring
-//               slot's scale atoms to TMEM (tcgen05.cp) and signals the MMA
+//   warp 3      block-scaled kinds: in the MMA-issuing CTA, copies each
+//               k-block's scale atoms to TMEM (tcgen05.cp) and signals the MMA
 //               warp with tcgen05.commit, so the copies run beside the MMAs
-//               instead of between them; in a pair's peer CTA, relays the
-//               peer's scale slots to the leader.
+//               instead of between them (copies issued by the MMA thread run in
+//               series with its MMAs); in a pair's peer CTA, relays the peer's
+//               scale slots to the leader.
+//
+// Scale factors (block-scaled kinds), per ring slot: the scale warp writes the
+// slot's atoms in shared memory (sf_full) once the copies of the slot's
+// previous round have completed (sf_ready of that round); the copy thread
+// copies them into the slot's TMEM columns once the MMAs of the previous round
+// have completed (empty) and commits to sf_ready, multicast to both CTAs of a
+// pair; the MMA warp waits on full and sf_ready.  So the scale warp is gated by
+// the copies, not by the MMAs, and the MMA thread issues nothing but MMAs and
+// its ring commits.
 //   warps 4..   EPI_WARPS epilogue warps (4 or 16): TMEM -> registers,
 //               fixed-order scale/bias epilogue, output rounding, staged bulk
 //               tensor stores; warp 4 + 4p + q owns TMEM lanes 32q..32q+31
@@ -176,7 +186,7 @@ struct GemmCfg {
   static constexpr int OFF_OUT = ((OFF_RAW + RAW_BUFS * RAW_STAGE_BYTES) + 1023) & ~1023;
   static constexpr int OFF_BAR = OFF_OUT + EPI_WARPS * OUT_BUFS * OUT_BLOCK_BYTES;
   // ring full/empty, accumulator full/empty, drain, raw scale fetches, and
-  // (block-scaled kinds) per-slot scale-atom arrivals and scale-copy completions
+  // (block-scaled kinds) per-slot scale atoms written and scales in TMEM
   static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC_BUFS + 1 + RAW_BUFS + (MX ? 2 * STAGES : 0);
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack to align the base to 1024
@@ -546,7 +556,7 @@ __device__ __forceinline__ void scale_slot_ready(uint64_t* sf_full, int stage) {
 template <class C>
 __device__ __forceinline__ void scale_stager_raw(const GemmParams& p, const CUtensorMap* tmSA,
                                                  const CUtensorMap* tmSB, uint8_t* smem, uint64_t* sf_full,
-                                                 uint64_t* empty, uint64_t* raw_full, const WaitCtl& w, int lane,
+                                                 uint64_t* sf_ready, uint64_t* raw_full, const WaitCtl& w, int lane,
                                                  int tile0, int tile_step, uint32_t rank) {
   const int n_raw = (p.num_kb + C::RAW_KB - 1) / C::RAW_KB;
   const bool by_tma = p.sf_mode == kSfTma;
@@ -577,14 +587,14 @@ __device__ __forceinline__ void scale_stager_raw(const GemmParams& p, const CUte
   }
 #pragma unroll 1
   while (t < p.num_tiles) {
-    // prefetch the next fetch into the other slot (its previous contents were
-    // consumed by this warp in the previous iteration)
+    // prefetch the next fetch into the other slot: its previous contents were
+    // read by this warp in the previous iteration (the loaded values were
+    // consumed there, so the reads are complete; all lanes are past them)
     int t2 = t, r2 = r + 1;
     if (r2 == n_raw) {
       t2 = t + tile_step;
       r2 = 0;
     }
-    fence_proxy_async_smem();
     __syncwarp();
     if (t2 < p.num_tiles) {
       issue(t2, r2, (seq + 1) & 1u);
@@ -600,26 +610,42 @@ __device__ __forceinline__ void scale_stager_raw(const GemmParams& p, const CUte
 #pragma unroll
     for (int i = 0; i < 4 * C::NB128; ++i) b[i] = ld_shared_v4(raw + C::RAW_A_BYTES + 16 * (32 * i + lane));
     ++seq;
+    // the fetch's k-blocks, published in pairs: one proxy fence for two atom
+    // slots (larger batches would hold atom slots back from the copies)
     bool ok = true;
+    int pending = 0;  // atom slots written and not yet published
+    auto publish = [&]() {
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        int s = stage - pending;
+        if (s < 0) s += C::STAGES;
+#pragma unroll 1
+        for (int i = 0; i < pending; ++i) {
+          scale_slot_ready<C>(sf_full, s);
+          if (++s == C::STAGES) s = 0;
+        }
+      }
+      pending = 0;
+    };
 #pragma unroll
     for (int sub = 0; sub < C::RAW_KB; ++sub) {
       const int kb = r * C::RAW_KB + sub;
       if (kb < p.num_kb) {
-        if (!mbar_wait(&empty[stage], phase ^ 1u, w, kSiteScaleEmpty)) {
+        if (!mbar_wait(&sf_ready[stage], phase ^ 1u, w, kSiteScaleEmpty)) {
           ok = false;
           break;
         }
         write_scale_atoms<C>(smem_u32(smem + C::OFF_SF + stage * C::SF_STAGE_BYTES), lane, a, b,
                              sub * C::SF_ATOMS_K);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) scale_slot_ready<C>(sf_full, stage);
         if (++stage == C::STAGES) {
           stage = 0;
           phase ^= 1u;
         }
+        if (++pending == 2) publish();
       }
     }
+    if (pending > 0) publish();
     if (!ok) break;
     t = t2;
     r = r2;
@@ -641,7 +667,7 @@ __device__ __forceinline__ void scale_stager_raw(const GemmParams& p, const CUte
 // Scale staging with plain loads (any K % 32 == 0): per ring stage, four
 // scale bytes per row and atom, one 32-bit load each.
 template <class C>
-__device__ __forceinline__ void scale_stager_ldg(const GemmParams& p, uint8_t* smem, uint64_t* sf_full, uint64_t* empty,
+__device__ __forceinline__ void scale_stager_ldg(const GemmParams& p, uint8_t* smem, uint64_t* sf_full, uint64_t* sf_ready,
                                                  const WaitCtl& w, int lane, int tile0, int tile_step, uint32_t rank) {
   int stage = 0;
   uint32_t phase = 0;
@@ -653,7 +679,7 @@ __device__ __forceinline__ void scale_stager_ldg(const GemmParams& p, uint8_t* s
     const int a_row = mb * C::TILE_M + static_cast<int>(rank) * C::BM;
 #pragma unroll 1
     for (int kb = 0; kb < p.num_kb; ++kb) {
-      if (!mbar_wait(&empty[stage], phase ^ 1u, w, kSiteScaleEmpty)) {
+      if (!mbar_wait(&sf_ready[stage], phase ^ 1u, w, kSiteScaleEmpty)) {
         ok = false;
         break;
       }
@@ -689,6 +715,72 @@ __device__ __forceinline__ void scale_stager_ldg(const GemmParams& p, uint8_t* s
   }
 }
 
+// Scale-factor copies of the MMA-issuing CTA (block-scaled kinds): per ring
+// slot, once its atoms are written (both CTAs' in a pair) and the MMAs of the
+// slot's previous round have completed (empty), copy the atoms (A's first,
+// then B's) into the slot's TMEM columns and commit to sf_ready, multicast to
+// both CTAs of a pair: the MMA warp waits on it, and so does each CTA's scale
+// warp before it rewrites the atoms.
+template <class C>
+__device__ __forceinline__ void scale_copier(const GemmParams& p, uint8_t* smem, uint32_t tmem, uint64_t* sf_full,
+                                             uint64_t* sf_ready, uint64_t* empty, const WaitCtl& w, int tile0,
+                                             int tile_step) {
+  int stage = 0;
+  uint32_t phase = 0;
+  long long issued = 0;
+  bool ok = true;
+#pragma unroll 1
+  for (int t = tile0; ok && t < p.num_tiles; t += tile_step) {
+#pragma unroll 1
+    for (int kb = 0; kb < p.num_kb; ++kb) {
+      bool ready = C::PAIR ? mbar_wait_cluster(&sf_full[stage], phase, w, kSiteScaleCopy)
+                           : mbar_wait(&sf_full[stage], phase, w, kSiteScaleCopy);
+      // the slot's TMEM scales of the previous round have been read by their MMAs
+      ready = ready && mbar_wait(&empty[stage], phase ^ 1u, w, kSiteScaleCopy);
+      if (!ready) {
+        ok = false;
+        break;
+      }
+      tc_fence_after_sync();
+      const uint32_t sf_tmem = tmem + static_cast<uint32_t>(C::COL_SF + stage * C::SF_COLS_STAGE);
+      const uint32_t sf_smem = smem_u32(smem + C::OFF_SF + stage * C::SF_STAGE_BYTES);
+#pragma unroll
+      for (int i = 0; i < C::SF_ATOMS_K + C::SF_ATOMS_K * C::NB128; ++i) {
+        const uint32_t col = i < C::SF_ATOMS_K ? 4 * i : C::SF_COLS_A + 4 * (i - C::SF_ATOMS_K);
+        const uint32_t src = i < C::SF_ATOMS_K ? sf_smem + 512 * i : sf_smem + C::SFA_BYTES + 512 * (i - C::SF_ATOMS_K);
+        if constexpr (C::PAIR) {
+          tmem_cp_32x128b_warpx4_pair(sf_tmem + col, make_smem_desc(src, 128, 128, 0));
+        } else {
+          tmem_cp_32x128b_warpx4(sf_tmem + col, make_smem_desc(src, 128, 128, 0));
+        }
+      }
+      if constexpr (C::PAIR) {
+        umma_commit_pair_multicast(&sf_ready[stage], 0x3);
+      } else {
+        umma_commit(&sf_ready[stage]);
+      }
+      ++issued;
+      if (++stage == C::STAGES) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+  }
+  // leave no copy in flight: the last commit covers every earlier copy
+  if (issued > 0) {
+    const long long L = issued - 1;
+    const uint32_t a = smem_u32(&sf_ready[static_cast<int>(L % C::STAGES)]);
+    const uint32_t par = static_cast<uint32_t>((L / C::STAGES) & 1);
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait(a, par)) {
+      if (global_timer_ns() - t0 > p.timeout_ns) {
+        report_error(p.err, kDevErrTimeout, kSiteScaleCopy, static_cast<uint32_t>(L));
+        break;
+      }
+    }
+  }
+}
+
 template <class C>
 __global__ void __launch_bounds__(C::NUM_THREADS, 1)
     qk_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -702,8 +794,10 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
   uint64_t* acc_empty = acc_full + C::ACC_BUFS;
   uint64_t* drain = acc_empty + C::ACC_BUFS;
   uint64_t* raw_full = drain + 1;
-  uint64_t* sf_full = raw_full + C::RAW_BUFS;  // block-scaled kinds: scale atoms of a slot written
-  uint64_t* sf_ready = sf_full + C::STAGES;    // block-scaled kinds: a slot's scale copies in TMEM
+  // block-scaled kinds: a slot's scale atoms written (sf_full) and copied to
+  // TMEM (sf_ready, which also frees the atoms for the next round)
+  uint64_t* sf_full = raw_full + C::RAW_BUFS;
+  uint64_t* sf_ready = sf_full + C::STAGES;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_MISC + 4);
 
@@ -850,7 +944,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
 #pragma unroll 1
           for (int kb = kb0; kb < kb1; ++kb) {
             bool landed = mbar_wait(&full[stage], phase, w, kSiteMmaFull);
-            // block-scaled kinds: the slot's scale factors are in TMEM (copied by warp 3)
+            // block-scaled kinds: the k-block's scale factors are in TMEM (copied by warp 3)
             if constexpr (C::MX) landed = landed && mbar_wait(&sf_ready[stage], phase, w, kSiteMmaScales);
             if (!landed) {
               ok = false;
@@ -970,75 +1064,15 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
     // ---------------- scale stager (MX) ----------------
     if constexpr (C::MX) {
       if (p.sf_mode == kSfTma || p.sf_mode == kSfAsync) {
-        scale_stager_raw<C>(p, &tmSA, &tmSB, smem, sf_full, empty, raw_full, w, lane, tile0, tile_step, rank);
+        scale_stager_raw<C>(p, &tmSA, &tmSB, smem, sf_full, sf_ready, raw_full, w, lane, tile0, tile_step, rank);
       } else {
-        scale_stager_ldg<C>(p, smem, sf_full, empty, w, lane, tile0, tile_step, rank);
+        scale_stager_ldg<C>(p, smem, sf_full, sf_ready, w, lane, tile0, tile_step, rank);
       }
     }
     __syncwarp();
   } else if (warp == 3) {
     if constexpr (C::MX) {
-      if (issues_mma && lane == 0) {
-        // ---------------- scale-factor copies (the MMA-issuing CTA) ----------------
-        // Per ring slot: once the atoms are written (both CTAs' in a pair),
-        // copy them into the slot's TMEM columns and commit to sf_ready.  A
-        // slot's atoms are rewritten only after the MMAs that read its
-        // previous copies have completed (the scale warp waits on `empty`).
-        int stage = 0;
-        uint32_t phase = 0;
-        long long issued = 0;
-        bool ok = true;
-#pragma unroll 1
-        for (int t = tile0; ok && t < p.num_tiles; t += tile_step) {
-#pragma unroll 1
-          for (int kb = 0; kb < p.num_kb; ++kb) {
-            const bool ready = C::PAIR ? mbar_wait_cluster(&sf_full[stage], phase, w, kSiteScaleCopy)
-                                       : mbar_wait(&sf_full[stage], phase, w, kSiteScaleCopy);
-            if (!ready) {
-              ok = false;
-              break;
-            }
-            tc_fence_after_sync();
-            const uint32_t sf_tmem = tmem + static_cast<uint32_t>(C::COL_SF + stage * C::SF_COLS_STAGE);
-            const uint32_t sf_smem = smem_u32(smem + C::OFF_SF + stage * C::SF_STAGE_BYTES);
-#pragma unroll
-            for (int i = 0; i < C::SF_ATOMS_K + C::SF_ATOMS_K * C::NB128; ++i) {
-              // atoms: A's first, then B's; TMEM columns in the same order
-              const uint32_t col = i < C::SF_ATOMS_K ? 4 * i : C::SF_COLS_A + 4 * (i - C::SF_ATOMS_K);
-              const uint32_t src = i < C::SF_ATOMS_K ? sf_smem + 512 * i
-                                                      : sf_smem + C::SFA_BYTES + 512 * (i - C::SF_ATOMS_K);
-              if constexpr (C::PAIR) {
-                tmem_cp_32x128b_warpx4_pair(sf_tmem + col, make_smem_desc(src, 128, 128, 0));
-              } else {
-                tmem_cp_32x128b_warpx4(sf_tmem + col, make_smem_desc(src, 128, 128, 0));
-              }
-            }
-            if constexpr (C::PAIR) {
-              umma_commit_pair(&sf_ready[stage]);
-            } else {
-              umma_commit(&sf_ready[stage]);
-            }
-            ++issued;
-            if (++stage == C::STAGES) {
-              stage = 0;
-              phase ^= 1u;
-            }
-          }
-        }
-        // leave no copy in flight: the last commit covers every earlier copy
-        if (issued > 0) {
-          const long long L = issued - 1;
-          const uint32_t a = smem_u32(&sf_ready[static_cast<int>(L % C::STAGES)]);
-          const uint32_t par = static_cast<uint32_t>((L / C::STAGES) & 1);
-          const uint64_t t0 = global_timer_ns();
-          while (!mbar_try_wait(a, par)) {
-            if (global_timer_ns() - t0 > p.timeout_ns) {
-              report_error(p.err, kDevErrTimeout, kSiteScaleCopy, static_cast<uint32_t>(L));
-              break;
-            }
-          }
-        }
-      }
+      if (issues_mma && lane == 0) scale_copier<C>(p, smem, tmem, sf_full, sf_ready, empty, w, tile0, tile_step);
     }
     // ---------------- scale relay (the peer CTA of an MX pair) ----------------
     if constexpr (C::MX && C::PAIR) {
