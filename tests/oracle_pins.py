@@ -29,7 +29,13 @@ What each pin rests on:
 * FP8 blockscale (fp32 scales per 1x128 of A and 128x128 of B): a closed
   form over ragged K- and N-blocks, a numpy matmul of the blocks, and the
   reduction to the per-token x per-channel GEMM when the scales do not vary
-  along K.
+  along K;
+* the quantizers that feed the GEMMs: the MX shared exponent from
+  torch.frexp, the elements through PyTorch's float8_e4m3fn cast or a brute
+  force over the E2M1 values; the per-token scale and codes through PyTorch's
+  fp32 divisions and float8_e4m3fn cast, hand-worked midpoint quotients, and
+  searched rows where the fp32 rounding of the quotient (not a division in
+  double, not a reciprocal multiply) decides the code.
 """
 from __future__ import annotations
 
@@ -158,6 +164,18 @@ def check_encoders(lib):
     assert np.array_equal(ours, theirs)
 
 
+def _e2m1_code_nearest(y):
+    """The E2M1 code nearest to y by brute force over the OCP value list, ties
+    to the even code (the value with an even significand), saturating at 6."""
+    mag = abs(float(y))
+    best, best_err = 0, float("inf")
+    for c, v in enumerate(E2M1_OCP_VALUES):
+        err = abs(v - mag)
+        if err < best_err or (err == best_err and c % 2 == 0):
+            best, best_err = c, err
+    return (0x8 if y < 0 else 0) | best
+
+
 def check_mx_quantize_block(lib):
     codes, sc = oracle.mx_quantize_block(oracle.FMT_MXFP8_E4M3, np.ones(32), lib)
     assert sc == 127 - 8 and np.all(codes == 0x78)          # 1.0 * 2^8 = 256
@@ -165,18 +183,95 @@ def check_mx_quantize_block(lib):
     assert sc == 127 - 2 and np.all(codes == 0x6)           # 1.0 * 2^2 = 4
     codes, sc = oracle.mx_quantize_block(oracle.FMT_MXFP8_E4M3, np.zeros(32), lib)
     assert sc == 0 and np.all(codes == 0)
-    # an independent vectorised encoder (the input generator's) agrees
+    # Independent pin: the shared exponent from torch.frexp (amax = f * 2^e,
+    # f in [0.5, 1): floor(log2 amax) = e - 1), the elements x * 2^-s exactly
+    # (a power-of-two scaling) and then PyTorch's float8_e4m3fn cast after
+    # saturation at +-448, or the nearest E2M1 value by brute force.
     rng = np.random.default_rng(3)
-    for fmt in (oracle.FMT_MXFP8_E4M3, oracle.FMT_MXFP4_E2M1):
+    for fmt, emax in ((oracle.FMT_MXFP8_E4M3, 8), (oracle.FMT_MXFP4_E2M1, 2)):
         x = (rng.standard_normal((6, 32)) * np.exp(rng.uniform(-8, 8, (6, 1)))).astype(np.float32)
         x[0, 5] *= 30.0
-        qc, qs = qk_inputs.mx_quantize(x, fmt)
-        if fmt == oracle.FMT_MXFP4_E2M1:
-            qc = qk_inputs.unpack_e2m1(qc)
         for r in range(6):
             c, s = oracle.mx_quantize_block(fmt, x[r], lib)
-            assert s == qs[r, 0]
-            assert np.array_equal(c, qc[r])
+            xt = torch.from_numpy(x[r].copy())
+            _, e = torch.frexp(xt.abs().max())
+            sexp = min(max(int(e) - 1 - emax, -127), 127)
+            assert s == sexp + 127
+            y = torch.ldexp(xt, torch.tensor(-sexp, dtype=torch.int32))
+            if fmt == oracle.FMT_MXFP8_E4M3:
+                want = y.clamp(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+            else:
+                want = np.array([_e2m1_code_nearest(v) for v in y.numpy()], np.uint8)
+            assert np.array_equal(c, want), (fmt, r)
+
+
+def _e4m3_neighbours(t):
+    """The E4M3 values just below and above t (t strictly inside the normal range)."""
+    vals = sorted(v for v in oracle.decode_e4m3(np.arange(0x7F, dtype=np.uint8)) if np.isfinite(v))
+    lo = max(v for v in vals if v < t)
+    hi = min(v for v in vals if v > t)
+    return lo, hi
+
+
+def _division_rounding_cases():
+    """Rows (amax, x) whose fp32 quotient x / fl(amax / 448) lands exactly on the
+    midpoint of two E4M3 values while the exact quotient lies strictly on one
+    side: rounding the fp32 quotient gives the even neighbour, rounding the
+    exact quotient (a division in double) may give the other one.  Found by a
+    seeded search; the exact side is decided with rationals."""
+    from fractions import Fraction
+    rng = np.random.default_rng(29)
+    mids = [1.0625, 1.1875, 1.3125, 2.125, 2.375, 0.53125, 17.0, 19.0, 0.0390625]
+    cases = []
+    for _ in range(4000):
+        amax = np.float32(rng.uniform(1.0, 100.0))
+        s = np.float32(amax / np.float32(448.0))
+        for t in mids:
+            x0 = np.float32(s * np.float32(t))
+            for k in range(-3, 4):
+                x = x0
+                for _ in range(abs(k)):
+                    x = np.nextafter(x, np.float32(np.inf if k > 0 else -np.inf), dtype=np.float32)
+                if not abs(x) < amax:
+                    continue
+                if np.float32(x / s) != np.float32(t):
+                    continue
+                exact = Fraction(float(x)) / Fraction(float(s))
+                if exact == Fraction(t):
+                    continue
+                lo, hi = _e4m3_neighbours(t)
+                cases.append((amax, x, t, lo if exact < Fraction(t) else hi))
+        if len(cases) >= 12:
+            break
+    return cases
+
+
+def _reciprocal_differs_cases():
+    """Rows (amax, x) where the code of the fp32 quotient x / s differs from the
+    code of x * fl(1 / s) (a reciprocal multiply, one rounding more), s =
+    fl(amax / 448); found by a seeded search near E4M3 midpoints."""
+    rng = np.random.default_rng(31)
+    mids = [1.0625, 1.1875, 1.3125, 2.125, 2.375, 0.53125, 17.0, 19.0, 0.0390625, 5.25, 88.0]
+    to_code = lambda v: int(torch.tensor([v], dtype=torch.float32).to(torch.float8_e4m3fn).view(torch.uint8)[0])
+    cases = []
+    for _ in range(20000):
+        amax = np.float32(rng.uniform(0.5, 300.0))
+        s = np.float32(amax / np.float32(448.0))
+        r = np.float32(np.float32(1.0) / s)
+        for t in mids:
+            x0 = np.float32(s * np.float32(t))
+            for k in (-2, -1, 1, 2):
+                x = x0
+                for _ in range(abs(k)):
+                    x = np.nextafter(x, np.float32(np.inf if k > 0 else -np.inf), dtype=np.float32)
+                if not abs(x) < amax:
+                    continue
+                qd, qr = np.float32(x / s), np.float32(x * r)
+                if qd != qr and to_code(qd) != to_code(qr):
+                    cases.append((amax, x, to_code(qd)))
+        if len(cases) >= 8:
+            break
+    return cases
 
 
 def check_ptpc_quantize(lib):
@@ -186,15 +281,45 @@ def check_ptpc_quantize(lib):
     assert s[0] == np.float32(7.0) / np.float32(448.0) and s[1] == 1.0
     assert codes[0, 3] == 0x7E and codes[2, 0] == 0xFE and codes[2, 3] == 0x7E   # +-448
     assert np.all(codes[1] == 0)
-    # every code decodes to within half an E4M3 step of x / s, and the codes agree
-    # with an independent vectorised implementation (the input generator's)
+    # hand-worked: amax 1344 gives s = 3 exactly; 3.1875 / 3 = 1.0625 and
+    # 3.5625 / 3 = 1.1875 are exact E4M3 midpoints, which round to the even
+    # neighbours 1.0 (0x38) and 1.25 (0x3A); amax 448 gives s = 1
+    x = np.array([[1344.0, 3.1875, 3.5625, -3.1875], [448.0, 1.0625, 1.1875, -0.0]], np.float32)
+    codes, s = oracle.ptpc_quantize(x, lib)
+    assert s.tolist() == [3.0, 1.0]
+    assert codes.tolist() == [[0x7E, 0x38, 0x3A, 0xB8], [0x7E, 0x38, 0x3A, 0x80]]
+    # Independent pin (PyTorch): the fp32 row maximum, the fp32 division
+    # amax / 448, the fp32 division x / s and PyTorch's float8_e4m3fn cast
     rng = np.random.default_rng(17)
     x = (rng.standard_normal((5, 300)) * np.exp(rng.uniform(-6, 6, (5, 1)))).astype(np.float32)
+    x[2, :7] = 0.0
     codes, s = oracle.ptpc_quantize(x, lib)
-    q2, s2 = qk_inputs.ptpc_quantize(x)
-    assert np.array_equal(s, s2) and np.array_equal(codes, q2)
-    dec = oracle.decode_e4m3(codes, lib) * s.astype(np.float64)[:, None]
-    assert np.all(np.abs(dec - x) <= np.abs(x) * 2.0 ** -4 + s[:, None] * 2.0 ** -10)
+    xt = torch.from_numpy(x)
+    amax = xt.abs().amax(dim=1)
+    st = torch.where(amax > 0, amax / 448.0, torch.ones_like(amax))
+    assert st.dtype == torch.float32 and np.array_equal(s, st.numpy())
+    want = (xt / st[:, None]).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(codes, want)
+    # the division rounds in fp32 before the E4M3 rounding: quotients that
+    # land on an E4M3 midpoint only after the fp32 rounding take the even
+    # neighbour, as PyTorch's cast of the fp32 quotient does
+    cases = _division_rounding_cases()
+    assert len(cases) >= 6
+    checked_other_side = 0
+    for amax_v, xv, t, other in cases:
+        row = np.array([[amax_v, xv]], np.float32)
+        c, sv = oracle.ptpc_quantize(row, lib)
+        tie_code = int(torch.tensor([t], dtype=torch.float32).to(torch.float8_e4m3fn).view(torch.uint8)[0])
+        assert int(c[0, 1]) == tie_code, (amax_v, xv, t)
+        other_code = int(torch.tensor([other], dtype=torch.float32).to(torch.float8_e4m3fn).view(torch.uint8)[0])
+        checked_other_side += other_code != tie_code
+    assert checked_other_side >= 3
+    # a division, not a reciprocal multiply: rows where the two round apart
+    rcp = _reciprocal_differs_cases()
+    assert len(rcp) >= 4
+    for amax_v, xv, code in rcp:
+        c, _ = oracle.ptpc_quantize(np.array([[amax_v, xv]], np.float32), lib)
+        assert int(c[0, 1]) == code, (amax_v, xv)
 
 
 # ---------------------------------------------------------------- INT8

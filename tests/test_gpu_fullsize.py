@@ -52,7 +52,8 @@ def test_mxfp8_full(shape):
     _mx_sampled(qi.FMT_MXFP8_E4M3, *shape)
 
 
-@pytest.mark.parametrize("shape", [(8192, 8192, 8192), (8192, 8192, 16384), (16384, 16384, 8192)],
+@pytest.mark.parametrize("shape", [(8192, 8192, 8192), (8192, 8192, 16384), (16384, 16384, 8192),
+                                   (16384, 16384, 16384)],
                          ids=lambda s: "x".join(map(str, s)))
 def test_mxfp4_full(shape):
     _mx_sampled(qi.FMT_MXFP4_E2M1, *shape)

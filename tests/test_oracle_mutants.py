@@ -47,6 +47,10 @@ MUTANTS = {
     "encoder_ties_away": ("(err == best_err && (c & 1u) == 0u)", "(err == best_err && c > best)"),
     "ptpc_scale_divisor": ("float s = amax / 448.0f;", "float s = amax / 240.0f;"),
     "ptpc_zero_row_scale": ("if (amax == 0.0f) s = 1.0f;", "if (amax == 0.0f) s = 0.5f;"),
+    "ptpc_division_in_double": ("float q = x[k] / s;", "double q = (double)x[k] / (double)s;"),
+    "ptpc_reciprocal_multiply": ("float q = x[k] / s;", "float q = x[k] * (1.0f / s);"),
+    "mx_quantize_floor_off_by_one": ("sexp = (e - 1) - emax;", "sexp = e - emax;"),
+    "e2m1_encoder_ties_up": ("(err == best_err && (c & 1u) == 0u)", "(err <= best_err)"),
     "mx_emax": ("int emax = (fmt == QKO_FMT_MXFP8_E4M3) ? 8 : 2;", "int emax = (fmt == QKO_FMT_MXFP8_E4M3) ? 7 : 2;"),
     "ue4m3_exponent_bias": ("return ldexp(1.0 + (double)m / 8.0, (int)e - 7);",
                             "return ldexp(1.0 + (double)m / 8.0, (int)e - 6);"),
