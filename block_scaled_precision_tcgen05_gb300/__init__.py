@@ -166,6 +166,14 @@ def _expect(t, name, dtype, shape, device):
         raise ValueError(f"{name} must be contiguous")
 
 
+def _on_device(device):
+    """Makes the operands' device current for the call: the library keeps its
+    per-device state (SM count, status word, workspace pool, scratch address)
+    for the current device and launches on that device's stream."""
+    import torch
+    return torch.cuda.device(device)
+
+
 def _out(out, M, N, device):
     import torch
     if out is None:
@@ -201,11 +209,13 @@ def gemm_int8_rowwise(A, B, sa, sb, bias=None, out=None, out_dtype=None):
         out = torch.empty((M, N), dtype=out_dtype, device=dev)
     _expect(out, "out", out_dtype, (M, N), dev)
     if out_dtype == torch.bfloat16:
-        check(load_library().qk_gemm_int8_rowwise(_ptr(A), _ptr(B), _ptr(sa), _ptr(sb), _ptr(bias), _ptr(out),
-                                                  M, N, K, _stream_handle(dev)))
+        with _on_device(dev):
+            check(load_library().qk_gemm_int8_rowwise(_ptr(A), _ptr(B), _ptr(sa), _ptr(sb), _ptr(bias), _ptr(out),
+                                                      M, N, K, _stream_handle(dev)))
     else:
-        check(load_library().qk_gemm_int8_rowwise_out(_ptr(A), _ptr(B), _ptr(sa), _ptr(sb), _ptr(bias),
-                                                      _ptr(out), codes[out_dtype], M, N, K, _stream_handle(dev)))
+        with _on_device(dev):
+            check(load_library().qk_gemm_int8_rowwise_out(_ptr(A), _ptr(B), _ptr(sa), _ptr(sb), _ptr(bias),
+                                                          _ptr(out), codes[out_dtype], M, N, K, _stream_handle(dev)))
     return out
 
 
@@ -217,9 +227,13 @@ def gemm_int8_rowwise_noalloc(A, B, sa, sb, bias=None, out=None):
     import torch
     if out is None:
         raise ValueError("out must be provided: this entry point allocates nothing")
+    if A.dim() != 2 or B.dim() != 2:
+        raise ValueError("A and B must be 2-D")
     M, K = A.shape
     N = B.shape[0]
     dev = A.device
+    if dev.type != "cuda":
+        raise ValueError("operands must be CUDA tensors")
     _expect(A, "A", torch.int8, (M, K), dev)
     _expect(B, "B", torch.int8, (N, K), dev)
     _expect(sa, "sa", torch.float32, (M,), dev)
@@ -227,8 +241,9 @@ def gemm_int8_rowwise_noalloc(A, B, sa, sb, bias=None, out=None):
     if bias is not None:
         _expect(bias, "bias", torch.bfloat16, (N,), dev)
     _expect(out, "out", torch.bfloat16, (M, N), dev)
-    check(load_library().qk_gemm_int8_rowwise_noalloc(_ptr(A), _ptr(B), _ptr(sa), _ptr(sb), _ptr(bias), _ptr(out),
-                                                      M, N, K, _stream_handle(dev)))
+    with _on_device(dev):
+        check(load_library().qk_gemm_int8_rowwise_noalloc(_ptr(A), _ptr(B), _ptr(sa), _ptr(sb), _ptr(bias), _ptr(out),
+                                                          M, N, K, _stream_handle(dev)))
     return out
 
 
@@ -247,8 +262,9 @@ def gemm_fp8_rowwise(A, B, sa, sb, bias=None, out=None):
     if bias is not None:
         _expect(bias, "bias", torch.bfloat16, (N,), dev)
     out = _out(out, M, N, dev)
-    check(load_library().qk_gemm_fp8_rowwise(_ptr(A), _ptr(B), _ptr(sa), _ptr(sb), _ptr(bias), _ptr(out),
-                                             M, N, K, _stream_handle(dev)))
+    with _on_device(dev):
+        check(load_library().qk_gemm_fp8_rowwise(_ptr(A), _ptr(B), _ptr(sa), _ptr(sb), _ptr(bias), _ptr(out),
+                                                 M, N, K, _stream_handle(dev)))
     return out
 
 
@@ -271,8 +287,9 @@ def gemm_mx(fmt, A, sA, B, sB, bias=None, out=None):
     if bias is not None:
         _expect(bias, "bias", torch.bfloat16, (N,), dev)
     out = _out(out, M, N, dev)
-    check(load_library().qk_gemm_mx(int(fmt), _ptr(A), _ptr(sA), _ptr(B), _ptr(sB), _ptr(bias), _ptr(out),
-                                    M, N, K, _stream_handle(dev)))
+    with _on_device(dev):
+        check(load_library().qk_gemm_mx(int(fmt), _ptr(A), _ptr(sA), _ptr(B), _ptr(sB), _ptr(bias), _ptr(out),
+                                        M, N, K, _stream_handle(dev)))
     return out
 
 
@@ -292,8 +309,9 @@ def gemm_fp8_blockscale(A, B, sa, sb, bias=None, out=None):
     if bias is not None:
         _expect(bias, "bias", torch.bfloat16, (N,), dev)
     out = _out(out, M, N, dev)
-    check(load_library().qk_gemm_fp8_blockscale(_ptr(A), _ptr(B), _ptr(sa), _ptr(sb), _ptr(bias), _ptr(out), M, N, K,
-                                                _stream_handle(dev)))
+    with _on_device(dev):
+        check(load_library().qk_gemm_fp8_blockscale(_ptr(A), _ptr(B), _ptr(sa), _ptr(sb), _ptr(bias), _ptr(out), M, N, K,
+                                                    _stream_handle(dev)))
     return out
 
 
@@ -317,8 +335,9 @@ def gemm_nvfp4(A, sA, B, sB, global_a=None, global_b=None, bias=None, out=None):
     if bias is not None:
         _expect(bias, "bias", torch.bfloat16, (N,), dev)
     out = _out(out, M, N, dev)
-    check(load_library().qk_gemm_nvfp4(_ptr(A), _ptr(sA), _ptr(B), _ptr(sB), _ptr(global_a), _ptr(global_b),
-                                       _ptr(bias), _ptr(out), M, N, K, _stream_handle(dev)))
+    with _on_device(dev):
+        check(load_library().qk_gemm_nvfp4(_ptr(A), _ptr(sA), _ptr(B), _ptr(sB), _ptr(global_a), _ptr(global_b),
+                                           _ptr(bias), _ptr(out), M, N, K, _stream_handle(dev)))
     return out
 
 
@@ -336,7 +355,8 @@ def quantize_mx(fmt, x, q=None, scales=None):
     scales = torch.empty((rows, K // 32), dtype=torch.uint8, device=dev) if scales is None else scales
     _expect(q, "q", torch.uint8, (rows, width), dev)
     _expect(scales, "scales", torch.uint8, (rows, K // 32), dev)
-    check(load_library().qk_quantize_mx(int(fmt), _ptr(x), _ptr(q), _ptr(scales), rows, K, _stream_handle(dev)))
+    with _on_device(dev):
+        check(load_library().qk_quantize_mx(int(fmt), _ptr(x), _ptr(q), _ptr(scales), rows, K, _stream_handle(dev)))
     return q, scales
 
 
@@ -350,7 +370,8 @@ def quantize_ptpc(x, q=None, scales=None):
     scales = torch.empty((rows,), dtype=torch.float32, device=dev) if scales is None else scales
     _expect(q, "q", torch.uint8, (rows, K), dev)
     _expect(scales, "scales", torch.float32, (rows,), dev)
-    check(load_library().qk_quantize_ptpc(_ptr(x), _ptr(q), _ptr(scales), rows, K, _stream_handle(dev)))
+    with _on_device(dev):
+        check(load_library().qk_quantize_ptpc(_ptr(x), _ptr(q), _ptr(scales), rows, K, _stream_handle(dev)))
     return q, scales
 
 

@@ -114,17 +114,20 @@ int launch_cluster_cfg(const uint8_t* A, const uint8_t* B, const FewRowArgs& arg
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   if (probe_only) {
-    static int cached[64];  // value + 1; 0 = not yet known
-    int& slot = cached[dev.device >= 0 && dev.device < 64 ? dev.device : 0];
-    if (slot == 0) {
+    // value + 1; 0 = not yet known (threads racing on the first call store the same value)
+    static std::atomic<int> cached[64];
+    std::atomic<int>& slot = cached[dev.device >= 0 && dev.device < 64 ? dev.device : 0];
+    int v = slot.load(std::memory_order_relaxed);
+    if (v == 0) {
       int n = 0;
       if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) {
         cudaGetLastError();
         n = 0;
       }
-      slot = n + 1;
+      v = n + 1;
+      slot.store(v, std::memory_order_relaxed);
     }
-    *fits = slot - 1;
+    *fits = v - 1;
     return QK_OK;
   }
   CUtensorMap tw, ta;

@@ -11,14 +11,12 @@
 
 namespace qk {
 
-// Default: 128 x 256 tiles on one CTA, two 256-column accumulators, 16
-// epilogue warps with 64 columns each: 1500-1700 TFLOP/s.  Variant 1: 256 x
-// 256 tiles on a CTA pair (the peer's MMA warp relays each accumulator
-// release to the leader), within 2% of the default.  Variant 2: pair tiles of
-// 256 x 128 with four 128-column accumulators.
+// 128 x 256 tiles on one CTA, two 256-column accumulators, 16 epilogue warps
+// with 64 columns each.  Measured alternatives, not built: 256 x 256 tiles on
+// a CTA pair (the peer's MMA warp relays each accumulator release to the
+// leader), within 2% of this one; pair tiles of 256 x 128 with four
+// 128-column accumulators, slower.
 using CfgFp8BlockscaleSingle = GemmCfg<Kind::F8BS, 256, 4, 2, false, 16, 1>;
-using CfgFp8BlockscalePair = GemmCfg<Kind::F8BS, 256, 6, 2, true, 16, 1>;
-using CfgFp8BlockscaleNarrow = GemmCfg<Kind::F8BS, 128, 8, 4, true, 16, 1>;
 
 template <class C>
 static int launch_fp8_blockscale_cfg(const uint8_t* A, const uint8_t* B, const float* sa, const float* sb,
@@ -43,10 +41,6 @@ static int launch_fp8_blockscale_cfg(const uint8_t* A, const uint8_t* B, const f
 int launch_fp8_blockscale(const uint8_t* A, const uint8_t* B, const float* sa, const float* sb,
                           const uint16_t* bias, uint16_t* out, int M, int N, int K, const DeviceInfo& dev,
                           cudaStream_t stream) {
-  const int v = kernel_variant("QK_BS_VARIANT");
-  if (v == 1) return launch_fp8_blockscale_cfg<CfgFp8BlockscalePair>(A, B, sa, sb, bias, out, M, N, K, dev, stream);
-  if (v == 2)
-    return launch_fp8_blockscale_cfg<CfgFp8BlockscaleNarrow>(A, B, sa, sb, bias, out, M, N, K, dev, stream);
   return launch_fp8_blockscale_cfg<CfgFp8BlockscaleSingle>(A, B, sa, sb, bias, out, M, N, K, dev, stream);
 }
 

@@ -1,6 +1,8 @@
 // qk_launch.cuh -- host-side launch of one GEMM kernel configuration.
 #pragma once
 
+#include <atomic>
+
 #include "qk_gemm_kernel.cuh"
 #include "qk_internal.h"
 
@@ -11,7 +13,8 @@ inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
 // Fills the tile/k-block bookkeeping of GemmParams for configuration C.
 // Row-blocks per raster group: QK_GROUP_M from the environment, else 8.
 int raster_group_m();
-// Kernel variant index from an environment variable (0 if unset).
+// Test-only selector of the few-row kernels (QK_FP8_SKINNY, QK_MX_SKINNY): the
+// integer value of the environment variable, 0 if unset.
 int kernel_variant(const char* env_name);
 
 template <class C>
@@ -65,19 +68,20 @@ int launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap&
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    // how many clusters fit at once (SMs pair up within a GPC), computed once per device
-    static int cached[64];
-    int& clusters = cached[dev.device >= 0 && dev.device < 64 ? dev.device : 0];
-    if (clusters == 0) {
+    // how many clusters fit at once (SMs pair up within a GPC), computed once per
+    // device; threads racing on the first call store the same value
+    static std::atomic<int> cached[64];
+    std::atomic<int>& clusters = cached[dev.device >= 0 && dev.device < 64 ? dev.device : 0];
+    int n = clusters.load(std::memory_order_relaxed);
+    if (n == 0) {
       cfg.gridDim = dim3(2 * (dev.sm_count / 2), 1, 1);
-      int n = 0;
       if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess || n <= 0) {
         cudaGetLastError();
         n = dev.sm_count / 2;
       }
-      clusters = n;
+      clusters.store(n, std::memory_order_relaxed);
     }
-    slots = clusters;
+    slots = n;
   }
   const int ctas = (p.num_tiles < slots ? p.num_tiles : slots) * C::CTAS;
   cfg.gridDim = dim3(ctas, 1, 1);

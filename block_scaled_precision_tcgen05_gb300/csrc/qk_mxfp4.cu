@@ -6,18 +6,16 @@
 
 namespace qk {
 
-// Default: 256 x 256 tiles on a 2-SM CTA pair (each SM loads half of B: 32 KB
-// of operands per 256-K stage instead of 48), five stages, one accumulator
-// that 16 epilogue warps drain into registers (64 columns each) and release
-// before the epilogue math, so the next tile's MMAs start after the drain:
-// 4430-4940 TFLOP/s.  Each CTA stages its own A scales and all of B's; the
-// peer's relay warp forwards each slot to the leader, whose cta_group::2
-// copies fill both CTAs' TMEM.  Variant 1: the same pair with 8 epilogue
-// warps working from TMEM (4100-4780).  Variant 4: one CTA, 128 x 256
-// (3830-4560).
+// 256 x 256 tiles on a 2-SM CTA pair (each SM loads half of B: 32 KB of
+// operands per 256-K stage instead of 48), five stages, one accumulator that
+// 16 epilogue warps drain into registers (64 columns each) and release before
+// the epilogue math, so the next tile's MMAs start after the drain.  Each CTA
+// stages its own A scales and all of B's; the peer's relay warp forwards each
+// slot to the leader, whose scale-copy thread fills both CTAs' TMEM with
+// cta_group::2 copies beside the MMAs.  Measured alternatives (the same pair
+// with 8 epilogue warps working from TMEM; one CTA with 128 x 256 tiles) were
+// slower and are not built.
 using CfgMxfp4PairDrain = GemmCfg<Kind::MXF4, 256, 5, 1, true, 16, 1>;
-using CfgMxfp4Pair = GemmCfg<Kind::MXF4, 256, 5, 1, true, 8, 2>;
-using CfgMxfp4Single = GemmCfg<Kind::MXF4, 256, 4, 1, false, 4, 1>;
 
 template <class C>
 static int launch_mxfp4_cfg(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const uint8_t* sB,
@@ -53,9 +51,6 @@ static int launch_mxfp4_cfg(const uint8_t* A, const uint8_t* sA, const uint8_t* 
 
 int launch_mxfp4(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const uint8_t* sB, const uint16_t* bias,
                  uint16_t* out, int M, int N, int K, const DeviceInfo& dev, cudaStream_t stream) {
-  const int v = kernel_variant("QK_MX_VARIANT");
-  if (v == 1) return launch_mxfp4_cfg<CfgMxfp4Pair>(A, sA, B, sB, bias, out, M, N, K, dev, stream);
-  if (v == 4) return launch_mxfp4_cfg<CfgMxfp4Single>(A, sA, B, sB, bias, out, M, N, K, dev, stream);
   return launch_mxfp4_cfg<CfgMxfp4PairDrain>(A, sA, B, sB, bias, out, M, N, K, dev, stream);
 }
 

@@ -7,17 +7,13 @@
 
 namespace qk {
 
-// Default: 256 x 256 tiles on a 2-SM CTA pair, five stages, one accumulator
-// drained by 16 epilogue warps into registers (64 columns each) and released
-// before the epilogue math: 2500-2510 TFLOP/s.  Variant 4: one CTA with
-// 128 x 224 tiles and two TMEM accumulators (448 columns) beside the 4-slot
-// scale ring, so each tile's epilogue overlaps the next tile's MMAs
-// (2370-2400).  Variant 1: the pair with 8 epilogue warps working from TMEM
-// (2010-2060).  One CTA with 128 x 256 tiles and one accumulator, whose
-// epilogue stalls the MMAs, measured 1780-2270.
+// 256 x 256 tiles on a 2-SM CTA pair, five stages, one accumulator drained by
+// 16 epilogue warps into registers (64 columns each) and released before the
+// epilogue math.  Measured alternatives, slower and not built: one CTA with
+// 128 x 224 tiles and two TMEM accumulators beside the scale ring; the pair
+// with 8 epilogue warps working from TMEM; one CTA with 128 x 256 tiles and
+// one accumulator, whose epilogue stalls the MMAs.
 using CfgMxfp8PairDrain = GemmCfg<Kind::MXF8, 256, 5, 1, true, 16, 1>;
-using CfgMxfp8Double = GemmCfg<Kind::MXF8, 224, 4, 2, false, 4, 2>;
-using CfgMxfp8Pair = GemmCfg<Kind::MXF8, 256, 5, 1, true, 8, 2>;
 
 template <class C>
 static int launch_mxfp8_cfg(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const uint8_t* sB,
@@ -66,7 +62,6 @@ static int launch_mxfp8_cfg(const uint8_t* A, const uint8_t* sA, const uint8_t* 
 // kernel, 2 = stream-K, 3 = cluster split-K, whenever M <= 128.
 int launch_mxfp8(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const uint8_t* sB, const uint16_t* bias,
                  uint16_t* out, int M, int N, int K, const DeviceInfo& dev, cudaStream_t stream) {
-  const int v = kernel_variant("QK_MX_VARIANT");
   const int skinny = kernel_variant("QK_MX_SKINNY");
   if (M <= 128 && skinny != 1) {
     FewRowArgs args;
@@ -96,8 +91,6 @@ int launch_mxfp8(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const ui
       if (st != QK_ERR_RANGE) return st;
     }
   }
-  if (v == 1) return launch_mxfp8_cfg<CfgMxfp8Pair>(A, sA, B, sB, bias, out, M, N, K, dev, stream);
-  if (v == 4) return launch_mxfp8_cfg<CfgMxfp8Double>(A, sA, B, sB, bias, out, M, N, K, dev, stream);
   return launch_mxfp8_cfg<CfgMxfp8PairDrain>(A, sA, B, sB, bias, out, M, N, K, dev, stream);
 }
 

@@ -8,15 +8,13 @@
 
 namespace qk {
 
-// Default: 256 x 256 tiles on a 2-SM CTA pair, four stages, one accumulator
-// drained by 16 epilogue warps into registers and released before the
-// epilogue math (3400-3580 TFLOP/s).  Variant 1: the pair with five stages
-// and 8 epilogue warps working from TMEM (3260-3430).  Variant 4: 128 x 256
-// tiles on one CTA; the 16 scale bytes per row per stage take 6 KB of shared
-// memory and 48 TMEM columns per slot, so three stages fit (3180-3330).
+// 256 x 256 tiles on a 2-SM CTA pair, four stages, one accumulator drained
+// by 16 epilogue warps into registers and released before the epilogue math.
+// Measured alternatives, slower and not built: the pair with five stages and
+// 8 epilogue warps working from TMEM; 128 x 256 tiles on one CTA, where the
+// 16 scale bytes per row per stage (6 KB of shared memory and 48 TMEM columns
+// per slot) leave room for three stages.
 using CfgNvfp4PairDrain = GemmCfg<Kind::NVF4, 256, 4, 1, true, 16, 1>;
-using CfgNvfp4Pair = GemmCfg<Kind::NVF4, 256, 5, 1, true, 8, 1>;
-using CfgNvfp4Single = GemmCfg<Kind::NVF4, 256, 3, 1, false, 4, 1>;
 
 template <class C>
 static int launch_nvfp4_cfg(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const uint8_t* sB,
@@ -78,8 +76,5 @@ extern "C" int qk_gemm_nvfp4(const uint8_t* A, const uint8_t* sA, const uint8_t*
   if (!dev) return st;
   const auto s = static_cast<cudaStream_t>(stream);
   const int m = static_cast<int>(M), n = static_cast<int>(N), k = static_cast<int>(K);
-  const int v = kernel_variant("QK_MX_VARIANT");
-  if (v == 1) return launch_nvfp4_cfg<CfgNvfp4Pair>(A, sA, B, sB, ga, gb, bias, out, m, n, k, *dev, s);
-  if (v == 4) return launch_nvfp4_cfg<CfgNvfp4Single>(A, sA, B, sB, ga, gb, bias, out, m, n, k, *dev, s);
   return launch_nvfp4_cfg<CfgNvfp4PairDrain>(A, sA, B, sB, ga, gb, bias, out, m, n, k, *dev, s);
 }

@@ -67,9 +67,10 @@ typedef void* qk_stream_t;
 
 /*
  * INT8 GEMM with per-row and per-column fp32 scales and an optional bias.
- * (comfy-kitchen PR #174, Summary: "cache row/column scales and bias values
- * in the rowwise epilogue"; update "Keep the cached INT8 epilogue scale order
- * exact"; Validation: bit-exact, "max absolute error 0.0".)
+ * Scales and bias are read once per output tile and applied in a fixed order
+ * (comfy-kitchen PR #174, Summary and the update "Keep the cached INT8
+ * epilogue scale order exact"); the page validates the result as an exact
+ * match of its reference (Validation).
  *
  *   acc      = sum_k A[m,k] * B[n,k]                  exact, int32
  *   x        = (float)acc                             round to nearest even

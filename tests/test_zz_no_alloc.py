@@ -71,3 +71,57 @@ def test_noalloc_rejects_problems_beyond_its_scratch():
     assert rc == qk.QK_ERR_SCRATCH
     assert "32 MiB" in qk.status_string(rc)
     assert lib.qk_gemm_int8_rowwise_noalloc(fake, fake, fake, fake, None, fake, 0, N, K, None) == qk.QK_OK
+
+
+_FRESH_PROCESS = r"""
+import ctypes, sys
+import numpy as np
+import torch
+sys.path.insert(0, ROOT)
+import block_scaled_precision_tcgen05_gb300 as qk
+import oracle
+import qk_inputs as qi
+
+lib = qk.load_library()
+M, N, K = 512, 768, 1024                    # (M + N) * K * 2 = 2.6 MB of scratch
+pr = qi.int8_problem(M, N, K, seed=5, bias=True)
+dev = lambda x: torch.from_numpy(np.ascontiguousarray(x)).cuda()
+A, B, sa, sb = dev(pr.A), dev(pr.B), dev(pr.sa), dev(pr.sb)
+bias = dev(pr.bias.view(np.int16)).view(torch.bfloat16)
+outs = [torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+p = lambda t: ctypes.c_void_p(t.data_ptr())
+stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+torch.cuda.synchronize()
+torch.cuda.mem_get_info()
+free = []
+for out in outs:
+    free.append(torch.cuda.mem_get_info()[0])
+    rc = lib.qk_gemm_int8_rowwise_noalloc(p(A), p(B), p(sa), p(sb), p(bias), p(out), M, N, K, stream)
+    assert rc == qk.QK_OK, rc
+    torch.cuda.synchronize()
+free.append(torch.cuda.mem_get_info()[0])
+# the first call on the device looks up the scratch array (and loads the
+# kernels' module); the second one must not change the device's free memory
+assert free[2] == free[1], free
+ref = oracle.gemm_int8_rowwise(pr.A, pr.B, pr.sa, pr.sb, bias=pr.bias)
+for i, out in enumerate(outs):
+    got = out.view(torch.int16).cpu().numpy().view(np.uint16)
+    assert np.array_equal(got, ref), f"call {i} differs from the oracle"
+assert qk.device_status(clear=False) == 0
+print("FRESH_PROCESS_OK")
+"""
+
+
+@pytest.mark.gpu
+def test_noalloc_first_calls_in_a_fresh_process():
+    # Only the no-allocation entry point runs in this process, so nothing else
+    # has created the library's memory pool or touched the scratch array before
+    # it: two calls, bit-exact against the CPU oracle, free device memory
+    # unchanged across the second.
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    code = f"ROOT = {root!r}\n" + _FRESH_PROCESS
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0 and "FRESH_PROCESS_OK" in r.stdout, r.stdout + r.stderr
