@@ -1,7 +1,7 @@
 #!/usr/bin/env python
 """Benchmark of the quantized GEMM library on GB300.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl qk|reference] [--formats default|none|full]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl qk|reference] [--formats default|none]
 
 One step is one full GEMM call (operand staging, scale staging, contraction,
 tile scheduling, fused epilogue, ragged edges) over one batch of synthetic
@@ -360,37 +360,85 @@ def time_calls(fn, iters, warmup, dev, flush):
     return statistics.median(times), kstats
 
 
+# Every configuration's shapes beside the headline: INT8 256x256x512 (the
+# latency configuration) and 30000x21504x5376 with bias, MXFP8 and MXFP4 at
+# their configuration shapes, the 15-point FP8 per-token sweep, and one shape
+# each of the NEXT rows (NVFP4, FP8 blockscale).
+FP8_SWEEP = [(M, N, K) for (N, K) in ((2112, 7168), (7168, 1792), (21504, 5376)) for M in (64, 1024, 4096, 16384, 30000)]
+FORMAT_CASES = ([("int8", (256, 256, 512)), ("int8_bias", (30000, 21504, 5376)),
+                 ("mxfp8", (16384, 7168, 2048)), ("mxfp8", (32768, 7168, 1792)),
+                 ("mxfp4", (8192, 8192, 8192)), ("mxfp4", (8192, 8192, 16384)), ("mxfp4", (16384, 16384, 8192)),
+                 ("mxfp4", (16384, 16384, 16384))]
+                + [("fp8_ptpc", s) for s in FP8_SWEEP]
+                + [("nvfp4", (8192, 8192, 16384)), ("fp8_blockscale", (16384, 7168, 2048))])
+
+
+def _device_bf16(gen, rows, K, std, dev, spike=False):
+    """bf16 N(0, std^2) [rows, K] drawn on the device (seeded); with `spike`, 1% of the
+    entries (a uniform mask) are multiplied by 20, the MXFP8 activation recipe."""
+    import torch
+    x = torch.randn((rows, K), generator=gen, device=dev, dtype=torch.float32)
+    if std != 1.0:
+        x.mul_(std)
+    if spike:
+        x[torch.rand((rows, K), generator=gen, device=dev) < 0.01] *= 20.0
+    return x.to(torch.bfloat16)
+
+
+def _hot_kernel_ms(qk, fn, kname, iters, dev):
+    """Mean kernel time (the library's own events) over back-to-back calls with no L2
+    flush between them: the operands are partly L2-resident."""
+    import torch
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize(dev)
+    qk.profile_read(reset=True)
+    qk.profile_enable(True)
+    for _ in range(iters):
+        fn()
+    torch.cuda.synchronize(dev)
+    qk.profile_enable(False)
+    n, ms = qk.profile_read(reset=True).get(kname, (0, 0.0))
+    return ms / n if n else None
+
+
 def secondary_formats(qk, dev, peaks, which):
-    """Other formats and shapes of the configurations, one line each (median of flushed calls)."""
+    """Every configuration shape, one line each: the median of 10 calls, each after an L2
+    flush (reading 256 MB), kernel times from the library's own events; few-row shapes also
+    the kernel time over back-to-back calls (hot_kernel_ms).  Operands are drawn on the device with the configurations' distributions
+    and quantized by the library's quantizers (INT8, NVFP4 and blockscale use the host
+    recipe); the parity tests check the same kernels on the host recipe."""
     import numpy as np
     import torch
     import qk_inputs as qi
-    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
     if which == "none":
         return []
-    cases = [("mxfp8", (16384, 7168, 2048)), ("mxfp8", (32768, 7168, 1792)),
-             ("mxfp4", (8192, 8192, 16384)), ("nvfp4", (8192, 8192, 16384)),
-             ("fp8_blockscale", (16384, 7168, 2048)),
-             ("fp8_ptpc", (64, 2112, 7168)), ("fp8_ptpc", (64, 21504, 5376)), ("fp8_ptpc", (16384, 7168, 1792)),
-             ("fp8_ptpc", (32768, 7168, 1792)),
-             ("int8_bias", (30000, 21504, 5376))]
-    if which == "full":
-        cases += [("mxfp4", (8192, 8192, 8192)), ("mxfp4", (16384, 16384, 8192)), ("mxfp4", (16384, 16384, 16384)),
-                  ("fp8_ptpc", (1024, 7168, 1792)), ("fp8_ptpc", (30000, 21504, 5376)), ("fp8_ptpc", (64, 21504, 5376)),
-                  ("nvfp4", (16384, 16384, 16384)), ("fp8_blockscale", (32768, 7168, 1792)),
-                  ("fp8_blockscale", (30000, 21504, 5376))]
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(0)
+    weights = {}
     results = []
-    for kind, (M, N, K) in cases:
+    for kind, (M, N, K) in FORMAT_CASES:
         t_gen = time.time()
-        if kind.startswith("mx"):
+        kname2 = None
+        if kind in ("mxfp8", "mxfp4"):
             fmt = qi.FMT_MXFP8_E4M3 if kind == "mxfp8" else qi.FMT_MXFP4_E2M1
-            p = qi.mx_problem(fmt, M, N, K, seed=0)
-            A, sA, B, sB = (_to_dev(x, dev) for x in (p.A, p.sA, p.B, p.sB))
+            A, sA = qk.quantize_mx(fmt, _device_bf16(gen, M, K, 1.0, dev, spike=kind == "mxfp8"))
+            B, sB = qk.quantize_mx(fmt, _device_bf16(gen, N, K, 0.02 if kind == "mxfp8" else 1.0, dev))
             out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
             fn = lambda: qk.gemm_mx(fmt, A, sA, B, sB, None, out)
             dtype = "fp8" if kind == "mxfp8" else "fp4"
             kname = "gemm_mxfp8" if kind == "mxfp8" else "gemm_mxfp4"
             in_bytes = A.numel() + B.numel() + sA.numel() + sB.numel()
+        elif kind == "fp8_ptpc":
+            A, sa = qk.quantize_ptpc(_device_bf16(gen, M, K, 1.0, dev))
+            if (N, K) not in weights:
+                weights[(N, K)] = qk.quantize_ptpc(_device_bf16(gen, N, K, 0.02, dev))
+            B, sb = weights[(N, K)]
+            out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+            fn = lambda: qk.gemm_fp8_rowwise(A, B, sa, sb, None, out)
+            dtype, kname = "fp8", "gemm_fp8"
+            in_bytes = A.numel() + B.numel() + 4 * (M + N)
         elif kind == "nvfp4":
             p = qi.nvfp4_problem(M, N, K, seed=0)
             A, sA, B, sB = (_to_dev(x, dev) for x in (p.A, p.sA, p.B, p.sB))
@@ -407,21 +455,15 @@ def secondary_formats(qk, dev, peaks, which):
             fn = lambda: qk.gemm_fp8_blockscale(A, B, sa, sb, None, out)
             dtype, kname = "fp8", "gemm_fp8_blockscale"
             in_bytes = A.numel() + B.numel() + 4 * (sa.numel() + sb.numel())
-        elif kind == "fp8_ptpc":
-            p = qi.fp8_problem(M, N, K, seed=0)
-            A, B, sa, sb = (_to_dev(x, dev) for x in (p.A, p.B, p.sa, p.sb))
-            out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
-            fn = lambda: qk.gemm_fp8_rowwise(A, B, sa, sb, None, out)
-            dtype, kname = "fp8", "gemm_fp8"
-            in_bytes = A.numel() + B.numel() + 4 * (M + N)
         else:
             p = qi.int8_problem(M, N, K, seed=0, bias=True)
             A, B, sa, sb = (_to_dev(x, dev) for x in (p.A, p.B, p.sa, p.sb))
             bias = _bias_dev(p.bias, dev)
             out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
             fn = lambda: qk.gemm_int8_rowwise(A, B, sa, sb, bias, out)
-            dtype, kname = "f16", "gemm_int8_f16"
+            dtype, kname, kname2 = "f16", "gemm_int8_f16", "int8_to_f16"
             in_bytes = A.numel() + B.numel() + 4 * (M + N) + 2 * N
+        torch.cuda.synchronize(dev)
         gen_s = time.time() - t_gen
         ms, kstats = time_calls(fn, 10, 3, dev, flush)
         flops = 2.0 * M * N * K
@@ -429,21 +471,33 @@ def secondary_formats(qk, dev, peaks, which):
         kavg = kms / max(klaunch, 1)
         peak = peaks["bf16_tflops"] * RATIO[dtype]
         alg_bytes = in_bytes + 2 * M * N
-        results.append({
+        tfl = flops / kavg / 1e9
+        gbs = alg_bytes / kavg / 1e6
+        few = M <= 128
+        line = {
             "format": kind, "M": M, "N": N, "K": K,
             "ms": round(ms, 4), "tflops": round(flops / ms / 1e9, 1),
-            "kernel_ms": round(kavg, 4), "kernel_tflops": round(flops / kavg / 1e9, 1),
-            "peak_tflops": round(peak, 1), "frac_of_peak": round(flops / kavg / 1e9 / peak, 4),
-            "kernel_gbs": round(alg_bytes / kavg / 1e6, 1), "frac_of_hbm": round(alg_bytes / kavg / 1e6 / peaks["hbm_gbs"], 4),
+            "kernel_ms": round(kavg, 4), "kernel_tflops": round(tfl, 1),
+            "peak_tflops": round(peak, 1), "frac_of_peak": round(tfl / peak, 4),
+            "kernel_gbs": round(gbs, 1), "frac_of_hbm": round(gbs / peaks["hbm_gbs"], 4),
+            "bound": "hbm" if few else "tensor",
+            "frac": round(gbs / peaks["hbm_gbs"] if few else tfl / peak, 4),
             "gen_s": round(gen_s, 1),
-        })
+        }
+        if kname2:
+            l2, ms2 = kstats.get(kname2, (0, 0.0))
+            if l2:
+                line["widen_ms"] = round(ms2 / l2, 4)
+        if few:
+            hot = _hot_kernel_ms(qk, fn, kname, 20, dev)
+            line["hot_kernel_ms"] = round(hot, 4) if hot else None
+        results.append(line)
         del A, B, out
         torch.cuda.empty_cache()
+    weights.clear()
     # the quantizers that feed the GEMMs (bandwidth-bound: bf16 in, codes + scales out)
     rows, K = 16384, 7168
-    rng = np.random.default_rng(0)
-    xb = torch.from_numpy(qi.to_bf16_bits(rng.standard_normal((rows, K), dtype=np.float32)).view(np.int16))
-    xb = xb.to(dev).view(torch.bfloat16)
+    xb = _device_bf16(gen, rows, K, 1.0, dev)
     for name, fn, out_bytes in (
             ("quantize_mxfp8", lambda: qk.quantize_mx(qi.FMT_MXFP8_E4M3, xb), rows * K + rows * K // 32),
             ("quantize_mxfp4", lambda: qk.quantize_mx(qi.FMT_MXFP4_E2M1, xb), rows * K // 2 + rows * K // 32),
@@ -453,7 +507,8 @@ def secondary_formats(qk, dev, peaks, which):
         kavg = kms / max(klaunch, 1)
         alg = 2 * rows * K + out_bytes
         results.append({"format": name, "M": rows, "K": K, "ms": round(ms, 4), "kernel_ms": round(kavg, 4),
-                        "kernel_gbs": round(alg / kavg / 1e6, 1), "frac_of_hbm": round(alg / kavg / 1e6 / peaks["hbm_gbs"], 4)})
+                        "kernel_gbs": round(alg / kavg / 1e6, 1), "frac_of_hbm": round(alg / kavg / 1e6 / peaks["hbm_gbs"], 4),
+                        "bound": "hbm", "frac": round(alg / kavg / 1e6 / peaks["hbm_gbs"], 4)})
     del xb
     torch.cuda.empty_cache()
     return results
@@ -574,7 +629,8 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["qk", "reference"], default="qk")
-    ap.add_argument("--formats", choices=["default", "none", "full"], default="default")
+    ap.add_argument("--formats", choices=["default", "none"], default="default",
+                    help="none: the headline only (no per-configuration lines)")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--kernel-case", choices=["int8", "fp8", "mxfp8", "mxfp4", "nvfp4", "blockscale", "quantize_ptpc",
@@ -628,9 +684,14 @@ def main(argv=None):
     traffic = profiled_traffic("gemm_int8_f16", f"{M}x{N}x{K}")
 
     fmt_results = []
+    fmt_clocks = None
     cpu = None
     if rank == 0 and world == 1:
+        fsampler = ClockSampler(gpu_index_for(local))
+        fsampler.start()
+        t_f0 = time.time()
         fmt_results = secondary_formats(qk, dev, peaks, args.formats)
+        fmt_clocks = fsampler.stop(t_f0, time.time())
         secs, ntiles, macs, cores = oracle_tiles(p, args.cpu_seconds)
         cpu = {"value": round(2.0 * macs / secs / 1e12, 6), "unit": "TOPS", "cores": cores, "kind": "oracle",
                "sample": f"{ntiles} output tiles of up to 128x128 (full K={K}) of this GEMM, seeded positions, "
@@ -662,6 +723,7 @@ def main(argv=None):
             "clocks": clocks,
             "cpu_baseline": cpu,
             "formats": fmt_results,
+            "formats_clocks": fmt_clocks,
             "kernel_source_sha1": kernel_source_hash(),
         }
         print(json.dumps(line), flush=True)
