@@ -83,6 +83,8 @@ def _declare(lib):
     lib.qko_gemm_fp8_rowwise.restype = c.c_int
     lib.qko_gemm_mx.argtypes = [c.c_int, P, P, P, P, P, P, i64, i64, i64, i64, i64, i64, i64, i64]
     lib.qko_gemm_mx.restype = c.c_int
+    lib.qko_gemm_mx_b32.argtypes = [c.c_int, P, P, P, P, P, P, i64, i64, i64, i64, i64, i64, i64, i64]
+    lib.qko_gemm_mx_b32.restype = c.c_int
     lib.qko_gemm_nvfp4.argtypes = [P, P, P, P, c.c_float, c.c_float, P, P, i64, i64, i64, i64, i64, i64, i64, i64]
     lib.qko_gemm_nvfp4.restype = c.c_int
     lib.qko_gemm_fp8_blockscale.argtypes = [P, P, P, P, P, P, i64, i64, i64, i64, i64, i64, i64, i64]
@@ -289,6 +291,30 @@ def gemm_mx(fmt, A, sA, B, sB, bias=None, K=None, m0=0, m1=None, n0=0, n1=None, 
                          n1 - n0, M, N, K, m0, m1, n0, n1)
     if rc != OK:
         raise ValueError(f"oracle mx gemm failed with code {rc}")
+    return ref
+
+
+def gemm_mx_b32(fmt, A, sA, B, sB32, bias=None, K=None, m0=0, m1=None, n0=0, n1=None, lib=None):
+    """fp64 value, before bf16 rounding, of the MX GEMM whose B scales cover 32x32
+    blocks: ``sA`` [M, K/32] as in gemm_mx, ``sB32`` [ceil(N/32), K/32], row n of B
+    taking scale row n // 32 (ROCm/mori PR #806, "What": the mxfp8_raw form)."""
+    lib = lib or load()
+    A = _c(A, np.uint8)
+    B = _c(B, np.uint8)
+    sA = _c(sA, np.uint8)
+    sB32 = _c(sB32, np.uint8)
+    bias = _c(bias, np.uint16)
+    M = A.shape[0]
+    N = B.shape[0]
+    if K is None:
+        K = A.shape[1] * (2 if fmt == FMT_MXFP4_E2M1 else 1)
+    assert sA.shape == (M, K // 32) and sB32.shape == ((N + 31) // 32, K // 32)
+    m0, m1, n0, n1 = _region(M, N, m0, m1, n0, n1)
+    ref = np.zeros((m1 - m0, n1 - n0), np.float64)
+    rc = lib.qko_gemm_mx_b32(int(fmt), _ptr(A), _ptr(sA), _ptr(B), _ptr(sB32), _ptr(bias), _ptr(ref),
+                             n1 - n0, M, N, K, m0, m1, n0, n1)
+    if rc != OK:
+        raise ValueError(f"oracle mx b32 gemm failed with code {rc}")
     return ref
 
 

@@ -30,6 +30,9 @@
  *  [AITER6262] ROCm/aiter PR #6262, "Technical Details": FP8 A8W8 GEMM with
  *           per-token x per-channel scales; its gemm_a4w4 signature takes
  *           optional per-tensor global A and B scales for NVFP4.
+ *  [MORI806-RAW] ROCm/mori PR #806, section "What" and the review thread's
+ *           scale reader (B_scale read with rows_per 32): the mxfp8_raw form
+ *           takes B's scales as [N/32, K/32], one byte per 32 rows x 32 K.
  *  [MORI806-BS] ROCm/mori PR #806, the pipeline-drain fix's measurements:
  *           a "blockscale" FP8 GEMM kind (16384x7168x2048) beside ptpc and
  *           mxfp8.  The block sizes are not stated on the page.
@@ -412,6 +415,47 @@ int qko_gemm_mx(int fmt, const uint8_t* A, const uint8_t* sA, const uint8_t* B, 
           inner += mx_elem(fmt, a, k) * mx_elem(fmt, b, k);
         }
         acc += g_ue8m0[sA[m * kb + blk]] * g_ue8m0[sB[n * kb + blk]] * inner;
+      }
+      if (bias) acc += (double)qko_bf16_to_f32(bias[n]);
+      ref[(m - m0) * ldr + (n - n0)] = acc;
+    }
+  }
+  return QKO_OK;
+}
+
+/* MX block-scaled GEMM with 32x32 scale blocks for B  [MORI806-RAW]
+ *
+ * ref[(m-m0)*ldr + (n-n0)] = sum_b 2^(sA[m,b]-127) * 2^(sB32[n/32,b]-127)
+ *                                * sum_{j<32} dec(A[m,32b+j]) * dec(B[n,32b+j])
+ *                            (+ bias[n])
+ * in fp64.  A's scales as in qko_gemm_mx, one per (row, 32 K): sA [M, K/32];
+ * B's one per 32 rows and 32 K: sB32 [ceil(N/32), K/32], row n of B taking
+ * scale row n / 32 (integer division; the last group may hold fewer than 32
+ * rows).  K must be a multiple of 32.  This is the value before bf16
+ * rounding. */
+int qko_gemm_mx_b32(int fmt, const uint8_t* A, const uint8_t* sA, const uint8_t* B, const uint8_t* sB32,
+                    const uint16_t* bias, double* ref, int64_t ldr, int64_t M, int64_t N, int64_t K,
+                    int64_t m0, int64_t m1, int64_t n0, int64_t n1) {
+  if (fmt != QKO_FMT_MXFP8_E4M3 && fmt != QKO_FMT_MXFP4_E2M1) return QKO_ERR_ARG;
+  if (!A || !sA || !B || !sB32 || !ref || M < 0 || N < 0 || K < 0 || (K % 32) != 0) return QKO_ERR_ARG;
+  if (m0 < 0 || n0 < 0 || m1 > M || n1 > N || m0 > m1 || n0 > n1 || ldr < n1 - n0) return QKO_ERR_ARG;
+  build_tables();
+  const int64_t kb = K / 32;
+  const int64_t row_bytes = (fmt == QKO_FMT_MXFP8_E4M3) ? K : K / 2;
+#pragma omp parallel for collapse(2) schedule(static)
+  for (int64_t m = m0; m < m1; ++m) {
+    for (int64_t n = n0; n < n1; ++n) {
+      const uint8_t* a = A + m * row_bytes;
+      const uint8_t* b = B + n * row_bytes;
+      const int64_t g = n / 32;  /* B's 32-row scale group */
+      double acc = 0.0;
+      for (int64_t blk = 0; blk < kb; ++blk) {
+        double inner = 0.0;
+        for (int64_t j = 0; j < 32; ++j) {
+          int64_t k = blk * 32 + j;
+          inner += mx_elem(fmt, a, k) * mx_elem(fmt, b, k);
+        }
+        acc += g_ue8m0[sA[m * kb + blk]] * g_ue8m0[sB32[g * kb + blk]] * inner;
       }
       if (bias) acc += (double)qko_bf16_to_f32(bias[n]);
       ref[(m - m0) * ldr + (n - n0)] = acc;

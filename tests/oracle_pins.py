@@ -21,6 +21,8 @@ What each pin rests on:
 * the MX block structure against closed forms (constant elements with
   per-block scale codes), the exact doubling when every scale code of A
   grows by one, and a numpy float64 matmul of independently decoded values;
+  the 32x32 B-scale form against a closed form over ragged 32-row groups and
+  its exact reduction to the 1x32 form on row-repeated scales;
 * NVFP4 (UE4M3 scales per 16 elements, per-tensor scales): the UE4M3 anchor
   values and PyTorch's float8_e4m3fn cast, a closed form over the 16-element
   blocks, a numpy matmul of independently decoded values, and the exact
@@ -563,6 +565,43 @@ def check_mx_vs_numpy(lib):
 
 # ---------------------------------------------------------------- NVFP4
 
+def check_mx_b32(lib):
+    """MX GEMM with B scales per 32x32 block (ROCm/mori PR #806, "What": B's
+    scales [N/32, K/32]): a closed form over ragged 32-row groups, and the
+    exact reduction to the 1x32 form when each group's scale row is repeated
+    for its 32 rows."""
+    for fmt in (oracle.FMT_MXFP8_E4M3, oracle.FMT_MXFP4_E2M1):
+        M, N, K = 5, 72, 128            # groups of rows 0-31, 32-63, 64-71
+        nb, ng = K // 32, (N + 31) // 32
+        A, B = _mx_ones(fmt, M, N, K)
+        da = (np.arange(M)[:, None] * 2 + np.arange(nb)[None, :]) % 5 - 2
+        db = (np.arange(ng)[:, None] * 3 + np.arange(nb)[None, :] * 2) % 7 - 3
+        sA = (127 + da).astype(np.uint8)
+        sB32 = (127 + db).astype(np.uint8)
+        ref = oracle.gemm_mx_b32(fmt, A, sA, B, sB32, lib=lib)
+        n = np.arange(N)
+        want = (32.0 * np.exp2(da[:, None, :] + db[n // 32][None, :, :])).sum(axis=2)
+        assert np.array_equal(ref, want), fmt
+        # random elements: equal to the 1x32 form on row-repeated scales, also
+        # on a sub-region with a bias
+        rng = np.random.default_rng(13)
+        M, N, K = 7, 104, 256
+        width = K if fmt == oracle.FMT_MXFP8_E4M3 else K // 2
+        A = rng.integers(0, 256, (M, width), dtype=np.uint8)
+        B = rng.integers(0, 256, (N, width), dtype=np.uint8)
+        if fmt == oracle.FMT_MXFP8_E4M3:   # no NaN codes
+            A[(A & 0x7F) == 0x7F] = 0x40
+            B[(B & 0x7F) == 0x7F] = 0x40
+        sA = rng.integers(110, 140, (M, K // 32), dtype=np.uint8)
+        sB32 = rng.integers(110, 140, ((N + 31) // 32, K // 32), dtype=np.uint8)
+        sB = np.repeat(sB32, 32, axis=0)[:N]
+        bias = qk_inputs.bias_bits(N, 3)
+        full = oracle.gemm_mx(fmt, A, sA, B, sB, bias=bias, lib=lib)
+        assert np.array_equal(oracle.gemm_mx_b32(fmt, A, sA, B, sB32, bias=bias, lib=lib), full)
+        sub = oracle.gemm_mx_b32(fmt, A, sA, B, sB32, bias=bias, m0=2, m1=6, n0=30, n1=97, lib=lib)
+        assert np.array_equal(sub, full[2:6, 30:97])
+
+
 def check_ue4m3_decode(lib):
     d = oracle.decode_ue4m3(np.arange(256), lib)
     assert d[0x38] == 1.0 and d[0x7E] == 448.0
@@ -693,5 +732,5 @@ ALL_CHECKS = [
     check_int8_output_types, check_int8_pow2_invariance, check_fp8_vs_numpy, check_mx_block_structure,
     check_mx_scale_doubling, check_mx_vs_numpy, check_ue4m3_decode, check_nvfp4_block_structure,
     check_nvfp4_vs_numpy, check_nvfp4_reduces_to_mxfp4, check_blockscale_block_structure,
-    check_blockscale_vs_numpy, check_blockscale_reduces_to_ptpc,
+    check_blockscale_vs_numpy, check_blockscale_reduces_to_ptpc, check_mx_b32,
 ]

@@ -58,6 +58,8 @@ MUTANTS = {
     "nvfp4_global_b_dropped": ("acc *= (double)ga * (double)gb;", "acc *= (double)ga;"),
     "nvfp4_scales_read_as_ue8m0": ("acc += g_ue4m3[sA[m * kb + blk]] * g_ue4m3[sB[n * kb + blk]] * inner;",
                                    "acc += g_ue8m0[sA[m * kb + blk]] * g_ue4m3[sB[n * kb + blk]] * inner;"),
+    "mx_b32_groups_of_64": ("const int64_t g = n / 32;", "const int64_t g = n / 64;"),
+    "mx_b32_b_block_index_dropped": ("g_ue8m0[sB32[g * kb + blk]]", "g_ue8m0[sB32[g * kb]]"),
     "blockscale_b_block_index_dropped": ("(double)sb[(n / 128) * KB + g]", "(double)sb[g]"),
     "blockscale_a_block_index_dropped": ("(double)sa[m * KB + g]", "(double)sa[m * KB]"),
     "blockscale_bias_dropped": ("if (bias) acc += (double)qko_bf16_to_f32(bias[n]);\n      ref[(m - m0) * ldr + (n - n0)] = acc;\n    }\n  }\n  return QKO_OK;\n}\n\n/* Number",
