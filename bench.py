@@ -366,7 +366,7 @@ def time_calls(fn, iters, warmup, dev, flush):
 # each of the NEXT rows (NVFP4, FP8 blockscale).
 FP8_SWEEP = [(M, N, K) for (N, K) in ((2112, 7168), (7168, 1792), (21504, 5376)) for M in (64, 1024, 4096, 16384, 30000)]
 FORMAT_CASES = ([("int8", (256, 256, 512)), ("int8_bias", (30000, 21504, 5376)),
-                 ("mxfp8", (16384, 7168, 2048)), ("mxfp8", (32768, 7168, 1792)),
+                 ("mxfp8", (16384, 7168, 2048)), ("mxfp8", (32768, 7168, 1792)), ("mxfp8_b32", (16384, 7168, 2048)),
                  ("mxfp4", (8192, 8192, 8192)), ("mxfp4", (8192, 8192, 16384)), ("mxfp4", (16384, 16384, 8192)),
                  ("mxfp4", (16384, 16384, 16384))]
                 + [("fp8_ptpc", s) for s in FP8_SWEEP]
@@ -421,14 +421,20 @@ def secondary_formats(qk, dev, peaks, which):
     for kind, (M, N, K) in FORMAT_CASES:
         t_gen = time.time()
         kname2 = None
-        if kind in ("mxfp8", "mxfp4"):
-            fmt = qi.FMT_MXFP8_E4M3 if kind == "mxfp8" else qi.FMT_MXFP4_E2M1
-            A, sA = qk.quantize_mx(fmt, _device_bf16(gen, M, K, 1.0, dev, spike=kind == "mxfp8"))
-            B, sB = qk.quantize_mx(fmt, _device_bf16(gen, N, K, 0.02 if kind == "mxfp8" else 1.0, dev))
+        if kind in ("mxfp8", "mxfp4", "mxfp8_b32"):
+            fp8 = kind != "mxfp4"
+            fmt = qi.FMT_MXFP8_E4M3 if fp8 else qi.FMT_MXFP4_E2M1
+            A, sA = qk.quantize_mx(fmt, _device_bf16(gen, M, K, 1.0, dev, spike=fp8))
+            B, sB = qk.quantize_mx(fmt, _device_bf16(gen, N, K, 0.02 if fp8 else 1.0, dev))
             out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
-            fn = lambda: qk.gemm_mx(fmt, A, sA, B, sB, None, out)
-            dtype = "fp8" if kind == "mxfp8" else "fp4"
-            kname = "gemm_mxfp8" if kind == "mxfp8" else "gemm_mxfp4"
+            if kind == "mxfp8_b32":
+                # B's scales per 32x32 block: the first row's scales of each 32-row group
+                sB = sB[::32].contiguous()
+                fn = lambda: qk.gemm_mx_b32(fmt, A, sA, B, sB, None, out)
+            else:
+                fn = lambda: qk.gemm_mx(fmt, A, sA, B, sB, None, out)
+            dtype = "fp8" if fp8 else "fp4"
+            kname = "gemm_mxfp8" if fp8 else "gemm_mxfp4"
             in_bytes = A.numel() + B.numel() + sA.numel() + sB.numel()
         elif kind == "fp8_ptpc":
             A, sa = qk.quantize_ptpc(_device_bf16(gen, M, K, 1.0, dev))

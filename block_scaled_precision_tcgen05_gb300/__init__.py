@@ -44,6 +44,7 @@ EXPORTS = (
     "qk_gemm_int8_rowwise_out",
     "qk_gemm_int8_rowwise_noalloc",
     "qk_gemm_mx",
+    "qk_gemm_mx_b32",
     "qk_gemm_fp8_rowwise",
     "qk_gemm_nvfp4",
     "qk_gemm_fp8_blockscale",
@@ -88,6 +89,8 @@ def _declare(lib):
     lib.qk_gemm_fp8_rowwise.restype = c.c_int
     lib.qk_gemm_mx.argtypes = [c.c_int, P, P, P, P, P, P, i64, i64, i64, P]
     lib.qk_gemm_mx.restype = c.c_int
+    lib.qk_gemm_mx_b32.argtypes = [c.c_int, P, P, P, P, P, P, i64, i64, i64, P]
+    lib.qk_gemm_mx_b32.restype = c.c_int
     lib.qk_gemm_nvfp4.argtypes = [P, P, P, P, P, P, P, P, i64, i64, i64, P]
     lib.qk_gemm_nvfp4.restype = c.c_int
     lib.qk_gemm_fp8_blockscale.argtypes = [P, P, P, P, P, P, i64, i64, i64, P]
@@ -290,6 +293,31 @@ def gemm_mx(fmt, A, sA, B, sB, bias=None, out=None):
     with _on_device(dev):
         check(load_library().qk_gemm_mx(int(fmt), _ptr(A), _ptr(sA), _ptr(B), _ptr(sB), _ptr(bias), _ptr(out),
                                         M, N, K, _stream_handle(dev)))
+    return out
+
+
+def gemm_mx_b32(fmt, A, sA, B, sB32, bias=None, out=None):
+    """MX GEMM with B's scales per 32x32 block: sA [M, K/32], sB32 [ceil(N/32), K/32] raw UE8M0
+    bytes (row n of B takes scale row n // 32); operands as for gemm_mx."""
+    import torch
+    if fmt not in (FMT_MXFP8_E4M3, FMT_MXFP4_E2M1):
+        raise ValueError("unknown MX format")
+    M, kbytes = A.shape
+    N = B.shape[0]
+    K = kbytes * (2 if fmt == FMT_MXFP4_E2M1 else 1)
+    dev = A.device
+    if dev.type != "cuda":
+        raise ValueError("operands must be CUDA tensors")
+    _expect(A, "A", torch.uint8, (M, kbytes), dev)
+    _expect(B, "B", torch.uint8, (N, kbytes), dev)
+    _expect(sA, "sA", torch.uint8, (M, K // 32), dev)
+    _expect(sB32, "sB32", torch.uint8, ((N + 31) // 32, K // 32), dev)
+    if bias is not None:
+        _expect(bias, "bias", torch.bfloat16, (N,), dev)
+    out = _out(out, M, N, dev)
+    with _on_device(dev):
+        check(load_library().qk_gemm_mx_b32(int(fmt), _ptr(A), _ptr(sA), _ptr(B), _ptr(sB32), _ptr(bias), _ptr(out),
+                                            M, N, K, _stream_handle(dev)))
     return out
 
 

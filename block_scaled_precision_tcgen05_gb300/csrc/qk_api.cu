@@ -324,6 +324,29 @@ int qk_gemm_mx(int fmt, const void* A, const uint8_t* sA, const void* B, const u
                       s);
 }
 
+int qk_gemm_mx_b32(int fmt, const void* A, const uint8_t* sA, const void* B, const uint8_t* sB32,
+                   const uint16_t* bias, uint16_t* out, int64_t M, int64_t N, int64_t K, qk_stream_t stream) {
+  if (fmt != QK_FMT_MXFP8_E4M3 && fmt != QK_FMT_MXFP4_E2M1) return QK_ERR_ARG;
+  if (M < 0 || N < 0 || K < 1) return QK_ERR_ARG;
+  if (M == 0 || N == 0) return QK_OK;
+  if (!A || !sA || !B || !sB32 || !out) return QK_ERR_ARG;
+  if (!aligned(A, 16) || !aligned(B, 16) || !aligned(out, 16) || (bias && !aligned(bias, 16)) ||
+      !aligned(sA, 4) || !aligned(sB32, 4))
+    return QK_ERR_ALIGN;
+  if (N % 8 != 0 || K % 32 != 0) return QK_ERR_ALIGN;
+  if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return QK_ERR_RANGE;
+  if (((M + 127) / 128) * ((N + 31) / 32) > INT32_MAX) return QK_ERR_RANGE;
+  int st;
+  const DeviceInfo* dev = current_device(&st);
+  if (!dev) return st;
+  const auto s = static_cast<cudaStream_t>(stream);
+  const auto* a = static_cast<const uint8_t*>(A);
+  const auto* b = static_cast<const uint8_t*>(B);
+  const int m = static_cast<int>(M), n = static_cast<int>(N), k = static_cast<int>(K);
+  if (fmt == QK_FMT_MXFP8_E4M3) return launch_mxfp8_b32(a, sA, b, sB32, bias, out, m, n, k, *dev, s);
+  return launch_mxfp4_b32(a, sA, b, sB32, bias, out, m, n, k, *dev, s);
+}
+
 const char* qk_status_string(int status) {
   switch (status) {
     case QK_OK: return "QK_OK";

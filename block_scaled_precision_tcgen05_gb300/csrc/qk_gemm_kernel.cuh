@@ -89,7 +89,7 @@ struct GemmParams {
   const uint16_t* bias;       // [N] bf16 bits, nullable
   void* out;                  // [M, N] bf16 / fp16 bits or fp32 (the configuration's OutType)
   const uint8_t* sA;          // [M, sf_cols] scale bytes (MX: UE8M0, NVFP4: UE4M3)
-  const uint8_t* sB;          // [N, sf_cols]
+  const uint8_t* sB;          // [N, sf_cols]; with 32x32 B-scale blocks [ceil(N/32), sf_cols]
   int sf_cols;                // scale bytes per row: K / 32 (MX), K / 16 (NVFP4)
   const float* ga;            // NVFP4 per-tensor scales (nullable: 1)
   const float* gb;
@@ -109,8 +109,10 @@ struct GemmParams {
 // thread) instead of TMEM, which frees TMEM for two accumulators.
 // OUT_BUFS_: shared-memory staging blocks per epilogue warp for bulk tensor
 // stores of the output; 0 = the epilogue stores straight to global memory.
+// SFB32_ (block-scaled kinds): B's scales cover 32 rows x 32 K each, raw
+// [ceil(N/32), K/32] bytes; tile row n takes scale row n / 32.
 template <Kind KIND, int BN_, int STAGES_, int ACC_BUFS_, bool PAIR_ = false, int EPI_WARPS_ = 4,
-          int OUT_BUFS_ = 2, OutType OUT_ = OutType::BF16>
+          int OUT_BUFS_ = 2, OutType OUT_ = OutType::BF16, bool SFB32_ = false>
 struct GemmCfg {
   static constexpr Kind kind = KIND;
   static constexpr OutType OUT = OUT_;
@@ -151,6 +153,7 @@ struct GemmCfg {
   // kinds whose one-chunk accumulator is drained into registers and released before the epilogue math
   static constexpr bool REG_DRAIN = REG_SUMS && (MX || KIND == Kind::F8);
 
+  static constexpr bool SFB32 = MX && SFB32_;                      // B scales per 32x32 block
   static constexpr int SF_PER_STAGE = MX ? K_ELEMS / SF_BLOCK : 0;  // scale bytes per row per stage
   static constexpr int SF_ATOMS_K = SF_PER_STAGE / 4;         // 4 scale bytes per 32-bit TMEM column
   static constexpr int NB128 = (BN + 127) / 128;              // 128-row blocks of the B tile
@@ -168,9 +171,11 @@ struct GemmCfg {
   // i.e. RAW_KB ring stages' worth, double-buffered.
   static constexpr int RAW_KB = MX ? 16 / SF_PER_STAGE : 1;
   static constexpr int RAW_A_BYTES = MX ? BM * 16 : 0;
-  static constexpr int RAW_B_BYTES = MX ? NB128 * 128 * 16 : 0;
+  // raw B scale rows per fetch: one per tile row, or (SFB32) one per 32 tile rows
+  static constexpr int SFB_RAW_ROWS = SFB32 ? BN / 32 : NB128 * 128;
+  static constexpr int RAW_B_BYTES = MX ? SFB_RAW_ROWS * 16 : 0;
   static constexpr int RAW_STAGE_BYTES = RAW_A_BYTES + RAW_B_BYTES;
-  static constexpr uint32_t RAW_TX = MX ? 16 * (BM + BN) : 0;
+  static constexpr uint32_t RAW_TX = MX ? 16 * (BM + (SFB32 ? BN / 32 : BN)) : 0;
   static constexpr int RAW_BUFS = MX ? 2 : 0;
 
   static constexpr int OFF_A = 0;
@@ -518,8 +523,22 @@ template <class C>
 __device__ __forceinline__ void raw_fetch_async(const GemmParams& p, uint32_t raw, uint64_t* bar, int a_row0, int nb,
                                                 int r, int lane) {
   const int col0 = r * 16;
+  if constexpr (C::SFB32) {
+    // B: one scale row per 32 tile rows, lane l copying group row l
+    const int grow = nb * (C::BN / 32) + lane;
+    const int grows = (p.N + 31) / 32;
+    if (lane < C::BN / 32) {
 #pragma unroll
-  for (int i = 0; i < 4 + 4 * C::NB128; ++i) {
+      for (int q = 0; q < 4; ++q) {
+        const int col = col0 + 4 * q;
+        const bool ok = grow < grows && col < p.sf_cols;
+        const uint8_t* src = ok ? p.sB + static_cast<size_t>(grow) * static_cast<size_t>(p.sf_cols) + col : p.sB;
+        cp_async_4(raw + C::RAW_A_BYTES + 16 * lane + 4 * q, src, ok ? 4u : 0u);
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 4 + (C::SFB32 ? 0 : 4 * C::NB128); ++i) {
     const bool is_a = i < 4;
     const int local = 32 * (is_a ? i : i - 4) + lane;
     const int row = is_a ? a_row0 + local : nb * C::BN + local;
@@ -569,7 +588,7 @@ __device__ __forceinline__ void scale_stager_raw(const GemmParams& p, const CUte
       if (lane == 0) {
         mbar_arrive_expect_tx(&raw_full[slot], C::RAW_TX);
         tma_load_2d(raw, tmSA, &raw_full[slot], r * 16, a_row);
-        tma_load_2d(raw + C::RAW_A_BYTES, tmSB, &raw_full[slot], r * 16, nb * C::BN);
+        tma_load_2d(raw + C::RAW_A_BYTES, tmSB, &raw_full[slot], r * 16, C::SFB32 ? nb * (C::BN / 32) : nb * C::BN);
       }
     } else {
       raw_fetch_async<C>(p, smem_u32(raw), &raw_full[slot], a_row, nb, r, lane);
@@ -608,7 +627,14 @@ __device__ __forceinline__ void scale_stager_raw(const GemmParams& p, const CUte
 #pragma unroll
     for (int j = 0; j < 4; ++j) a[j] = ld_shared_v4(raw + 16 * (32 * j + lane));
 #pragma unroll
-    for (int i = 0; i < 4 * C::NB128; ++i) b[i] = ld_shared_v4(raw + C::RAW_A_BYTES + 16 * (32 * i + lane));
+    for (int i = 0; i < 4 * C::NB128; ++i) {
+      if constexpr (C::SFB32) {
+        // tile rows 32i + lane all take the scale row of 32-row group i
+        b[i] = i < C::BN / 32 ? ld_shared_v4(raw + C::RAW_A_BYTES + 16 * i) : make_uint4(0u, 0u, 0u, 0u);
+      } else {
+        b[i] = ld_shared_v4(raw + C::RAW_A_BYTES + 16 * (32 * i + lane));
+      }
+    }
     ++seq;
     // the fetch's k-blocks, published in pairs: one proxy fence for two atom
     // slots (larger batches would hold atom slots back from the copies)
@@ -699,8 +725,13 @@ __device__ __forceinline__ void scale_stager_ldg(const GemmParams& p, uint8_t* s
         for (int rb = 0; rb < C::NB128; ++rb) {
           uint32_t v[4];
 #pragma unroll
-          for (int j = 0; j < 4; ++j)
-            v[j] = load_sf4(p.sB, nb * C::BN + rb * 128 + 32 * j + lane, p.N, col0 + 4 * g, p.sf_cols);
+          for (int j = 0; j < 4; ++j) {
+            if constexpr (C::SFB32) {
+              v[j] = load_sf4(p.sB, (nb * C::BN + rb * 128 + 32 * j) / 32, (p.N + 31) / 32, col0 + 4 * g, p.sf_cols);
+            } else {
+              v[j] = load_sf4(p.sB, nb * C::BN + rb * 128 + 32 * j + lane, p.N, col0 + 4 * g, p.sf_cols);
+            }
+          }
           st_shared_v4(sf + C::SFA_BYTES + 512 * (g * C::NB128 + rb) + 16 * lane, v[0], v[1], v[2], v[3]);
         }
       }

@@ -14,6 +14,10 @@ namespace qk {
 // with 8 epilogue warps working from TMEM; one CTA with 128 x 256 tiles and
 // one accumulator, whose epilogue stalls the MMAs.
 using CfgMxfp8PairDrain = GemmCfg<Kind::MXF8, 256, 5, 1, true, 16, 1>;
+// The same kernel with B's scales per 32x32 block (ROCm/mori PR #806's
+// mxfp8_raw form): the scale warp stages one raw scale row per 32 tile rows
+// and writes it into all 32 rows' places of the atoms.
+using CfgMxfp8PairDrainB32 = GemmCfg<Kind::MXF8, 256, 5, 1, true, 16, 1, OutType::BF16, true>;
 
 template <class C>
 static int launch_mxfp8_cfg(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const uint8_t* sB,
@@ -40,7 +44,11 @@ static int launch_mxfp8_cfg(const uint8_t* A, const uint8_t* sA, const uint8_t* 
   p.sf_mode = (p.sf_cols % 16 == 0 && a16) ? kSfTma : (p.sf_cols % 4 == 0 ? kSfAsync : kSfLoads);
   if (p.sf_mode == kSfTma) {
     st = encode_tmap_2d_plain(&tsa, CU_TENSOR_MAP_DATA_TYPE_UINT8, sA, p.sf_cols, M, p.sf_cols, 16, C::BM);
-    if (st == QK_OK) st = encode_tmap_2d_plain(&tsb, CU_TENSOR_MAP_DATA_TYPE_UINT8, sB, p.sf_cols, N, p.sf_cols, 16, C::BN);
+    // B's scale rows: one per row of B, or one per 32 rows (C::SFB32)
+    const uint64_t sb_rows = C::SFB32 ? static_cast<uint64_t>((N + 31) / 32) : static_cast<uint64_t>(N);
+    if (st == QK_OK)
+      st = encode_tmap_2d_plain(&tsb, CU_TENSOR_MAP_DATA_TYPE_UINT8, sB, p.sf_cols, sb_rows, p.sf_cols, 16,
+                                C::SFB32 ? C::BN / 32 : C::BN);
     if (st != QK_OK) return st;
   }
   return launch_gemm<C>(ta, tb, tsa, tsb, p, dev, stream);
@@ -92,6 +100,14 @@ int launch_mxfp8(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const ui
     }
   }
   return launch_mxfp8_cfg<CfgMxfp8PairDrain>(A, sA, B, sB, bias, out, M, N, K, dev, stream);
+}
+
+// B scales per 32x32 block: the tile kernel for every M (the few-row kernels
+// stage per-row scales only).
+int launch_mxfp8_b32(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const uint8_t* sB32,
+                     const uint16_t* bias, uint16_t* out, int M, int N, int K, const DeviceInfo& dev,
+                     cudaStream_t stream) {
+  return launch_mxfp8_cfg<CfgMxfp8PairDrainB32>(A, sA, B, sB32, bias, out, M, N, K, dev, stream);
 }
 
 }  // namespace qk

@@ -161,6 +161,29 @@ int qk_gemm_mx(int fmt, const void* A, const uint8_t* sA, const void* B, const u
                const uint16_t* bias, uint16_t* out, int64_t M, int64_t N, int64_t K, qk_stream_t stream);
 
 /*
+ * MX block-scaled GEMM with B's scales per 32x32 block (ROCm/mori PR #806,
+ * section "What": the mxfp8_raw form takes B's scales as [N/32, K/32] uint8,
+ * row major, read with 32 rows per scale row in the review thread's scale
+ * reader).  A's scales are as in qk_gemm_mx.
+ *
+ *   out[m,n] = bf16_rne( sum_b 2^(sA[m,b]-127) * 2^(sB32[n/32,b]-127)
+ *                          * sum_{j<32} A[m,32b+j] * B[n,32b+j]   (+ bias[n]) )
+ * accumulated in fp32 on the tensor cores (the summation order is free).
+ *
+ *   fmt   QK_FMT_MXFP8_E4M3 or QK_FMT_MXFP4_E2M1, operands as for qk_gemm_mx
+ *   sA    uint8 [M, K/32]              raw row-major UE8M0 exponents
+ *   sB32  uint8 [ceil(N/32), K/32]     one row per 32 rows of B (integer division;
+ *                                      the last group may hold fewer rows)
+ *   bias  bf16 [N] or NULL;  out bf16 [M, N]
+ * Requirements and errors as for qk_gemm_mx.  Every M runs the 2-SM tile
+ * kernel (no few-row mode in this form); on chip the scale warp writes each
+ * 32-row group's scale bytes into the places of its 32 rows, so the form
+ * reads 32x fewer B scale bytes and no expanded copy exists in HBM.
+ */
+int qk_gemm_mx_b32(int fmt, const void* A, const uint8_t* sA, const void* B, const uint8_t* sB32,
+                   const uint16_t* bias, uint16_t* out, int64_t M, int64_t N, int64_t K, qk_stream_t stream);
+
+/*
  * FP8 E4M3 GEMM with per-token (row) and per-channel (column) fp32 scales
  * (ROCm/aiter PR #6262, gemm_a8w8_bpreshuffle with per-token/per-channel
  * scales; ROCm/mori PR #806, the "ptpc" kind).  Same epilogue as

@@ -112,6 +112,22 @@ def test_mx_argument_errors(lib):
     assert mx_call(lib, M=0) == qk.QK_OK
 
 
+def test_mx_b32_argument_errors(lib):
+    def call(fmt=1, sA=FAKE, sB32=FAKE, out=FAKE, M=128, N=128, K=128):
+        return lib.qk_gemm_mx_b32(fmt, _p(FAKE), _p(sA), _p(FAKE), _p(sB32), None, _p(out), M, N, K, None)
+    assert call(fmt=0) == qk.QK_ERR_ARG
+    assert call(fmt=3) == qk.QK_ERR_ARG
+    assert call(sB32=0) == qk.QK_ERR_ARG
+    assert call(sA=0) == qk.QK_ERR_ARG
+    assert call(K=48) == qk.QK_ERR_ALIGN
+    assert call(N=20) == qk.QK_ERR_ALIGN
+    assert call(sB32=FAKE + 2) == qk.QK_ERR_ALIGN
+    assert call(out=FAKE + 4) == qk.QK_ERR_ALIGN
+    assert call(K=-32) == qk.QK_ERR_ARG
+    assert call(M=0) == qk.QK_OK
+    assert call(N=0, sB32=0) == qk.QK_OK
+
+
 def test_binding_fails_loudly_without_library(tmp_path):
     missing = str(tmp_path / "libqk.so")
     with pytest.raises(OSError):
