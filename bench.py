@@ -580,9 +580,11 @@ def run_kernel_case(args):
     M, N, K = (int(v) for v in args.shape.split(","))
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
-    if args.kernel_case == "int8":
+    out_dtype = torch.bfloat16
+    if args.kernel_case in ("int8", "int8_fp16", "int8_fp32"):
         p = qi.int8_problem(M, N, K, seed=0, bias=False)
         A, B, sa, sb = (_to_dev(x, dev) for x in (p.A, p.B, p.sa, p.sb))
+        out_dtype = {"int8": torch.bfloat16, "int8_fp16": torch.float16, "int8_fp32": torch.float32}[args.kernel_case]
         fn = lambda out: qk.gemm_int8_rowwise(A, B, sa, sb, None, out)
     elif args.kernel_case == "fp8":
         p = qi.fp8_problem(M, N, K, seed=0)
@@ -610,12 +612,17 @@ def run_kernel_case(args):
         else:
             fn = lambda out: qk.quantize_mx(qi.FMT_MXFP8_E4M3, xb)
         N = 1
+    elif args.kernel_case == "mxfp8_b32":
+        p = qi.mx_problem(qi.FMT_MXFP8_E4M3, M, N, K, seed=0)
+        A, sA, B = (_to_dev(x, dev) for x in (p.A, p.sA, p.B))
+        sB32 = _to_dev(p.sB[::32], dev)   # the first row's scales of each 32-row group of B
+        fn = lambda out: qk.gemm_mx_b32(qi.FMT_MXFP8_E4M3, A, sA, B, sB32, None, out)
     else:
         fmt = qi.FMT_MXFP8_E4M3 if args.kernel_case == "mxfp8" else qi.FMT_MXFP4_E2M1
         p = qi.mx_problem(fmt, M, N, K, seed=0)
         A, sA, B, sB = (_to_dev(x, dev) for x in (p.A, p.sA, p.B, p.sB))
         fn = lambda out: qk.gemm_mx(fmt, A, sA, B, sB, None, out)
-    out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    out = torch.empty((M, N), dtype=out_dtype, device=dev)
     torch.cuda.synchronize(dev)
     t0 = time.time()
     for _ in range(args.iters):
@@ -639,8 +646,8 @@ def main(argv=None):
                     help="none: the headline only (no per-configuration lines)")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
-    ap.add_argument("--kernel-case", choices=["int8", "fp8", "mxfp8", "mxfp4", "nvfp4", "blockscale", "quantize_ptpc",
-                                              "quantize_mxfp8"], default=None,
+    ap.add_argument("--kernel-case", choices=["int8", "int8_fp16", "int8_fp32", "fp8", "mxfp8", "mxfp8_b32", "mxfp4",
+                                              "nvfp4", "blockscale", "quantize_ptpc", "quantize_mxfp8"], default=None,
                     help="only run --iters calls of one kernel kind on --shape (profiler captures)")
     ap.add_argument("--shape", default="8192,8192,8192")
     ap.add_argument("--iters", type=int, default=3)
