@@ -51,7 +51,8 @@ namespace {
 
 const char* const kKernelNames[kKNumKinds] = {"int8_to_f16", "gemm_int8_f16", "gemm_fp8",
                                               "gemm_mxfp8",  "gemm_mxfp4",    "wait_probe",
-                                              "quantize",    "gemm_nvfp4",    "gemm_fp8_blockscale"};
+                                              "quantize",    "gemm_nvfp4",    "gemm_fp8_blockscale",
+                                              "sf_atoms"};
 
 struct PendingTiming {
   int kind;

@@ -20,6 +20,19 @@ namespace qk {
 
 constexpr int kFewRowSfBytes = 1024;  // shared memory per stage: two atoms
 
+// Four consecutive UE8M0 bytes of one scale row, little-endian; zero outside
+// the matrix (the matching operand elements are zero-filled by TMA).
+__device__ __forceinline__ uint32_t load_sf4(const uint8_t* s, int row, int rows, int col, int cols) {
+  if (row >= rows || col >= cols) return 0u;
+  const uint8_t* rp = s + static_cast<size_t>(row) * static_cast<size_t>(cols);
+  if ((cols & 3) == 0) return __ldg(reinterpret_cast<const uint32_t*>(rp + col));
+  uint32_t v = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    if (col + i < cols) v |= static_cast<uint32_t>(__ldg(rp + col + i)) << (8 * i);
+  return v;
+}
+
 // Runs on one whole warp.  unit(i, w_row0, col) gives the i-th unit's first
 // weight row and its scale column (4 x its K-block).  Returns false when a
 // bounded wait gave up (the error is recorded by mbar_wait).

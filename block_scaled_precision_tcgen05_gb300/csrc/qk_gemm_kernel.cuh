@@ -7,30 +7,27 @@
 // (one per SM, or one 2-SM pair per two SMs) walk output tiles of
 // 128 x BN (a pair: 256 x BN) in a grouped-M raster.  Roles:
 //   warp 0      TMA producer: A/B tiles of 128-byte K rows into a STAGES-deep
-//               shared-memory ring (128-byte swizzle).
-//   warp 1      MMA issuer: allocates TMEM, copies stage scale factors to TMEM
-//               (block-scaled kinds), issues tcgen05.mma into a TMEM
+//               shared-memory ring (128-byte swizzle); block-scaled kinds: the
+//               stage's scale-factor atoms with them (see qk_sf_atoms.cuh).
+//   warp 1      MMA issuer: allocates TMEM, issues tcgen05.mma into a TMEM
 //               accumulator and releases ring slots / accumulators with
 //               tcgen05.commit; in a pair's peer CTA it relays the peer's
 //               accumulator releases to the leader.
-//   warp 2      scale stager (block-scaled kinds): reads the raw row-major
-//               scale bytes and writes them into the shared-memory order
-//               tcgen05.cp wants.
-//   warp 3      block-scaled kinds: in the MMA-issuing CTA, copies each
-//               k-block's scale atoms to TMEM (tcgen05.cp) and signals the MMA
-//               warp with tcgen05.commit, so the copies run beside the MMAs
-//               instead of between them (copies issued by the MMA thread run in
-//               series with its MMAs); in a pair's peer CTA, relays the peer's
-//               scale slots to the leader.
+//   warps 2, 3  block-scaled kinds, in the MMA-issuing CTA: scale-factor
+//               copies (tcgen05.cp), each warp half of every ring slot's
+//               atoms, committed to a per-slot barrier the MMA warp waits on,
+//               so the copies run beside the MMAs instead of between them
+//               (copies issued by the MMA thread run in series with its MMAs,
+//               and one thread issues a copy about every 100 cycles).
 //
-// Scale factors (block-scaled kinds), per ring slot: the scale warp writes the
-// slot's atoms in shared memory (sf_full) once the copies of the slot's
-// previous round have completed (sf_ready of that round); the copy thread
-// copies them into the slot's TMEM columns once the MMAs of the previous round
-// have completed (empty) and commits to sf_ready, multicast to both CTAs of a
-// pair; the MMA warp waits on full and sf_ready.  So the scale warp is gated by
-// the copies, not by the MMAs, and the MMA thread issues nothing but MMAs and
-// its ring commits.
+// Scale factors (block-scaled kinds) arrive with the operands: the caller's
+// raw row-major scale bytes are rearranged once per call into 512-byte atoms
+// in the order tcgen05.cp reads (qk_sf_atoms.cuh), and the producer loads each
+// ring stage's atoms by TMA beside its A/B tiles, counted on the same full
+// barrier.  The copy threads move a slot's atoms into the slot's TMEM columns
+// once the slot has landed and the MMAs of its previous round have completed
+// (empty), and commit to sf_ready; the MMA warp waits on full and sf_ready, so
+// it issues nothing but MMAs and its ring commits.
 //   warps 4..   EPI_WARPS epilogue warps (4 or 16): TMEM -> registers,
 //               fixed-order scale/bias epilogue, output rounding, staged bulk
 //               tensor stores; warp 4 + 4p + q owns TMEM lanes 32q..32q+31
@@ -72,12 +69,6 @@ enum class Kind : int { F16 = 0, F8 = 1, MXF8 = 2, MXF4 = 3, NVF4 = 4, F8BS = 5 
 // Output element type (the values of the public QK_OUT_* constants).
 enum class OutType : int { BF16 = 0, F16 = 1, F32 = 2 };
 
-// How the scale warp gets raw scale rows (MX kinds):
-//   kSfTma    TMA boxes of 16 bytes per row (K % 512 == 0, 16-byte aligned rows)
-//   kSfAsync  per-lane 4-byte cp.async into the same raw buffers (K % 128 == 0)
-//   kSfLoads  per-stage 32-bit loads straight into the atoms (any K % 32 == 0)
-enum : int { kSfLoads = 0, kSfTma = 1, kSfAsync = 2 };
-
 struct GemmParams {
   int M, N, K;
   int num_kb;                 // k-blocks (ring stages) per tile
@@ -88,13 +79,10 @@ struct GemmParams {
   const float* sb;            // [N] column scales (F16, F8)
   const uint16_t* bias;       // [N] bf16 bits, nullable
   void* out;                  // [M, N] bf16 / fp16 bits or fp32 (the configuration's OutType)
-  const uint8_t* sA;          // [M, sf_cols] scale bytes (MX: UE8M0, NVFP4: UE4M3)
-  const uint8_t* sB;          // [N, sf_cols]; with 32x32 B-scale blocks [ceil(N/32), sf_cols]
-  int sf_cols;                // scale bytes per row: K / 32 (MX), K / 16 (NVFP4)
+  int sf_gpad;                // block-scaled kinds: atoms per 128-row block in the atom buffers (num_kb * SF_ATOMS_K)
   const float* ga;            // NVFP4 per-tensor scales (nullable: 1)
   const float* gb;
   int scale_kb;               // FP8 blockscale: K-blocks of 128 per scale row (sa [M, kb], sb [ceil(N/128), kb])
-  int sf_mode;                // MX scale staging: kSfTma, kSfAsync or kSfLoads
   int group_m;                // row-blocks per raster group
   unsigned long long* err;    // device error word
   uint64_t timeout_ns;        // bound on every barrier wait
@@ -109,10 +97,8 @@ struct GemmParams {
 // thread) instead of TMEM, which frees TMEM for two accumulators.
 // OUT_BUFS_: shared-memory staging blocks per epilogue warp for bulk tensor
 // stores of the output; 0 = the epilogue stores straight to global memory.
-// SFB32_ (block-scaled kinds): B's scales cover 32 rows x 32 K each, raw
-// [ceil(N/32), K/32] bytes; tile row n takes scale row n / 32.
 template <Kind KIND, int BN_, int STAGES_, int ACC_BUFS_, bool PAIR_ = false, int EPI_WARPS_ = 4,
-          int OUT_BUFS_ = 2, OutType OUT_ = OutType::BF16, bool SFB32_ = false>
+          int OUT_BUFS_ = 2, OutType OUT_ = OutType::BF16>
 struct GemmCfg {
   static constexpr Kind kind = KIND;
   static constexpr OutType OUT = OUT_;
@@ -153,7 +139,6 @@ struct GemmCfg {
   // kinds whose one-chunk accumulator is drained into registers and released before the epilogue math
   static constexpr bool REG_DRAIN = REG_SUMS && (MX || KIND == Kind::F8);
 
-  static constexpr bool SFB32 = MX && SFB32_;                      // B scales per 32x32 block
   static constexpr int SF_PER_STAGE = MX ? K_ELEMS / SF_BLOCK : 0;  // scale bytes per row per stage
   static constexpr int SF_ATOMS_K = SF_PER_STAGE / 4;         // 4 scale bytes per 32-bit TMEM column
   static constexpr int NB128 = (BN + 127) / 128;              // 128-row blocks of the B tile
@@ -163,36 +148,26 @@ struct GemmCfg {
 
   static constexpr int A_BYTES = BM * ROW_BYTES;
   static constexpr int B_BYTES = B_ROWS * ROW_BYTES;
-  // bytes a ring stage's full barrier counts: a pair's leader counts both CTAs'
-  // loads
-  static constexpr uint32_t STAGE_TX = PAIR ? 2 * (A_BYTES + B_BYTES) : A_BYTES + B_BYTES;
-
-  // Raw scale rows fetched by TMA: 16 bytes (16 scales) per row per fetch,
-  // i.e. RAW_KB ring stages' worth, double-buffered.
-  static constexpr int RAW_KB = MX ? 16 / SF_PER_STAGE : 1;
-  static constexpr int RAW_A_BYTES = MX ? BM * 16 : 0;
-  // raw B scale rows per fetch: one per tile row, or (SFB32) one per 32 tile rows
-  static constexpr int SFB_RAW_ROWS = SFB32 ? BN / 32 : NB128 * 128;
-  static constexpr int RAW_B_BYTES = MX ? SFB_RAW_ROWS * 16 : 0;
-  static constexpr int RAW_STAGE_BYTES = RAW_A_BYTES + RAW_B_BYTES;
-  static constexpr uint32_t RAW_TX = MX ? 16 * (BM + (SFB32 ? BN / 32 : BN)) : 0;
-  static constexpr int RAW_BUFS = MX ? 2 : 0;
+  // bytes a ring stage's full barrier counts: A and B tiles and (block-scaled
+  // kinds) the stage's scale atoms; a pair's leader counts both CTAs' loads
+  static constexpr uint32_t STAGE_TX =
+      PAIR ? 2 * (A_BYTES + B_BYTES + SF_STAGE_BYTES) : A_BYTES + B_BYTES + SF_STAGE_BYTES;
 
   static constexpr int OFF_A = 0;
   static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
   static constexpr int OFF_SF = OFF_B + STAGES * B_BYTES;
-  static constexpr int OFF_RAW = OFF_SF + STAGES * SF_STAGE_BYTES;
+  static constexpr int OFF_SF_END = OFF_SF + STAGES * SF_STAGE_BYTES;
   // Output staging: each epilogue warp writes 32x32 blocks (bf16 / fp16: 2 KB
   // with the 64-byte swizzle; fp32: 4 KB with the 128-byte swizzle) that a
   // bulk tensor store copies to global memory.
   static constexpr int OUT_BUFS = OUT_BUFS_;
   static constexpr bool STORE_TMA = OUT_BUFS_ > 0;
   static constexpr int OUT_BLOCK_BYTES = 32 * 32 * OUT_ELEM_BYTES;
-  static constexpr int OFF_OUT = ((OFF_RAW + RAW_BUFS * RAW_STAGE_BYTES) + 1023) & ~1023;
+  static constexpr int OFF_OUT = (OFF_SF_END + 1023) & ~1023;
   static constexpr int OFF_BAR = OFF_OUT + EPI_WARPS * OUT_BUFS * OUT_BLOCK_BYTES;
-  // ring full/empty, accumulator full/empty, drain, raw scale fetches, and
-  // (block-scaled kinds) per-slot scale atoms written and scales in TMEM
-  static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC_BUFS + 1 + RAW_BUFS + (MX ? 2 * STAGES : 0);
+  // ring full/empty, accumulator full/empty, drain, and (block-scaled kinds)
+  // a slot's scales copied to TMEM
+  static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC_BUFS + 1 + (MX ? STAGES : 0);
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack to align the base to 1024
 
@@ -219,14 +194,14 @@ struct GemmCfg {
   static_assert(COLS_USED <= 512, "TMEM budget");
   static_assert(SMEM_BYTES <= 232448, "shared-memory budget");
   static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "swizzle atoms need 1024-byte alignment");
+  static_assert(!MX || BN % 128 == 0, "scale atoms cover 128 rows of B");
 
   // Ring-slot arrivals: the producer's (a pair's leader counts both CTAs' TMA
-  // bytes).  Scale-slot arrivals (block-scaled kinds), on the MMA-issuing CTA:
-  // its own scale warp and, in a pair, the peer's relay -- each CTA of a pair
-  // stages the scale factors of its own 128 rows of A and of all BN rows of B
-  // at the same offsets.
+  // bytes; each CTA of a pair loads the scale atoms of its own 128 rows of A
+  // and of all BN rows of B at the same offsets).  Scale copies to TMEM: one
+  // commit from each of the two copy threads.
   static constexpr uint32_t FULL_ARRIVALS = 1;
-  static constexpr uint32_t SF_ARRIVALS = PAIR ? 2 : 1;
+  static constexpr uint32_t SF_COPIERS = 2;
 
   // kind::f16: D fp32 (1), A/B f16 (0).  kind::f8f6f4: A/B E4M3 (0).
   // kind::mxf8f6f4: E4M3 (0).  kind::mxf4: E2M1 (1), UE8M0 scales.
@@ -248,23 +223,6 @@ __device__ __forceinline__ void tile_coords(const GemmParams& p, int t, int& mb,
   const int local = t - g * group_tiles;
   mb = first_m + local % gm;
   nb = local / gm;
-}
-
-// Four consecutive UE8M0 bytes of one scale row, little-endian; zero outside
-// the matrix (the matching operand elements are zero-filled by TMA).
-__device__ __forceinline__ uint32_t load_sf4(const uint8_t* s, int row, int rows, int col, int cols) {
-  if (row >= rows || col >= cols) return 0u;
-  const uint8_t* rp = s + static_cast<size_t>(row) * static_cast<size_t>(cols);
-  if ((cols & 3) == 0) return __ldg(reinterpret_cast<const uint32_t*>(rp + col));
-  uint32_t v = 0;
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-    if (col + i < cols) v |= static_cast<uint32_t>(__ldg(rp + col + i)) << (8 * i);
-  return v;
-}
-
-__device__ __forceinline__ uint32_t word_of(const uint4& v, int w) {
-  return w == 0 ? v.x : w == 1 ? v.y : w == 2 ? v.z : v.w;
 }
 
 __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
@@ -483,24 +441,6 @@ __device__ __forceinline__ void out_block_release(OutStager& o, uint32_t block, 
   ++o.count;
 }
 
-// Writes one ring stage's scale atoms from per-lane scale words.
-// a[j] holds 4 scale bytes of tile row 32j + lane (A), b[rb*4 + j] of B row
-// rb*128 + 32j + lane; atom g of the stage takes word `w0 + g`.
-template <class C>
-__device__ __forceinline__ void write_scale_atoms(uint32_t sf, int lane, const uint4 (&a)[4],
-                                                  const uint4 (&b)[4 * C::NB128], int w0) {
-#pragma unroll
-  for (int g = 0; g < C::SF_ATOMS_K; ++g) {
-    const int wd = w0 + g;
-    st_shared_v4(sf + 512 * g + 16 * lane, word_of(a[0], wd), word_of(a[1], wd), word_of(a[2], wd),
-                 word_of(a[3], wd));
-#pragma unroll
-    for (int rb = 0; rb < C::NB128; ++rb)
-      st_shared_v4(sf + C::SFA_BYTES + 512 * (g * C::NB128 + rb) + 16 * lane, word_of(b[4 * rb + 0], wd),
-                   word_of(b[4 * rb + 1], wd), word_of(b[4 * rb + 2], wd), word_of(b[4 * rb + 3], wd));
-  }
-}
-
 __device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src, uint32_t src_bytes) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
 }
@@ -512,250 +452,18 @@ __device__ __forceinline__ void cp_async_wait_group() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
-// Raw fetch by the whole warp with 4-byte cp.async: lane l copies the 16-byte
-// chunk `r` of scale rows l + 32i (A: 128 rows, B: NB128*128 rows), zero-filled
-// past the matrix; each lane's copies arrive once on `bar` when they land.
+// Scale-factor copies of the MMA-issuing CTA (block-scaled kinds), one of
+// two threads: per ring slot, once the slot has landed (full: both CTAs'
+// tiles and scale atoms in a pair) and the MMAs of the slot's previous round
+// have completed (empty), copy the atoms i with i % 2 == part into the slot's
+// TMEM columns and commit to sf_ready, which counts both threads.  Atoms in
+// shared memory: A's SF_ATOMS_K first, then B's 128-row blocks one after the
+// other (each SF_ATOMS_K atoms); in TMEM: A's, then B's grouped by K-group
+// (the NB128 row blocks of a K-group side by side, as the MMA reads them).
 template <class C>
-__device__ __forceinline__ void raw_fetch_async(const GemmParams& p, uint32_t raw, uint64_t* bar, int a_row0, int nb,
-                                                int r, int lane) {
-  const int col0 = r * 16;
-  if constexpr (C::SFB32) {
-    // B: one scale row per 32 tile rows, lane l copying group row l
-    const int grow = nb * (C::BN / 32) + lane;
-    const int grows = (p.N + 31) / 32;
-    if (lane < C::BN / 32) {
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int col = col0 + 4 * q;
-        const bool ok = grow < grows && col < p.sf_cols;
-        const uint8_t* src = ok ? p.sB + static_cast<size_t>(grow) * static_cast<size_t>(p.sf_cols) + col : p.sB;
-        cp_async_4(raw + C::RAW_A_BYTES + 16 * lane + 4 * q, src, ok ? 4u : 0u);
-      }
-    }
-  }
-#pragma unroll
-  for (int i = 0; i < 4 + (C::SFB32 ? 0 : 4 * C::NB128); ++i) {
-    const bool is_a = i < 4;
-    const int local = 32 * (is_a ? i : i - 4) + lane;
-    const int row = is_a ? a_row0 + local : nb * C::BN + local;
-    const int rows = is_a ? p.M : p.N;
-    const uint8_t* base = is_a ? p.sA : p.sB;
-    const uint32_t dst = raw + (is_a ? 0 : C::RAW_A_BYTES) + 16 * local;
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int col = col0 + 4 * q;
-      const bool ok = row < rows && col < p.sf_cols;
-      const uint8_t* src = ok ? base + static_cast<size_t>(row) * static_cast<size_t>(p.sf_cols) + col : base;
-      cp_async_4(dst + 4 * q, src, ok ? 4u : 0u);
-    }
-  }
-  cp_async_arrive_noinc(bar);
-}
-
-// Scale staging from raw rows: 16 bytes of every scale row of the tile
-// (RAW_KB ring stages' worth) are fetched into a double-buffered raw area, one
-// fetch ahead (also across tiles) -- by TMA from one elected lane, or by
-// per-lane cp.async when the row pitch rules TMA out; the warp then
-// rearranges each stage's scale bytes into the 512-byte atoms tcgen05.cp
-// reads.  Shared loads and stores are 16 bytes per lane over contiguous
-// 512-byte spans (no bank conflicts).
-// Marks a ring slot's scale atoms as written, on this CTA's scale-slot
-// barrier.  In a CTA pair the peer's barrier is a local gather that the peer's
-// relay warp forwards to the leader's with one arrive per slot, so the scale
-// warp itself never waits on a cluster-wide fence.
-template <class C>
-__device__ __forceinline__ void scale_slot_ready(uint64_t* sf_full, int stage) {
-  mbar_arrive(&sf_full[stage]);
-}
-
-template <class C>
-__device__ __forceinline__ void scale_stager_raw(const GemmParams& p, const CUtensorMap* tmSA,
-                                                 const CUtensorMap* tmSB, uint8_t* smem, uint64_t* sf_full,
-                                                 uint64_t* sf_ready, uint64_t* raw_full, const WaitCtl& w, int lane,
-                                                 int tile0, int tile_step, uint32_t rank) {
-  const int n_raw = (p.num_kb + C::RAW_KB - 1) / C::RAW_KB;
-  const bool by_tma = p.sf_mode == kSfTma;
-  auto issue = [&](int t, int r, uint32_t slot) {
-    int mb, nb;
-    tile_coords(p, t, mb, nb);
-    uint8_t* raw = smem + C::OFF_RAW + slot * C::RAW_STAGE_BYTES;
-    const int a_row = mb * C::TILE_M + static_cast<int>(rank) * C::BM;
-    if (by_tma) {
-      if (lane == 0) {
-        mbar_arrive_expect_tx(&raw_full[slot], C::RAW_TX);
-        tma_load_2d(raw, tmSA, &raw_full[slot], r * 16, a_row);
-        tma_load_2d(raw + C::RAW_A_BYTES, tmSB, &raw_full[slot], r * 16, C::SFB32 ? nb * (C::BN / 32) : nb * C::BN);
-      }
-    } else {
-      raw_fetch_async<C>(p, smem_u32(raw), &raw_full[slot], a_row, nb, r, lane);
-    }
-  };
-  int stage = 0;
-  uint32_t phase = 0;
-  uint32_t seq = 0;     // raw fetches consumed so far
-  uint32_t issued = 0;  // raw fetches issued so far (same value in every lane)
-  int t = tile0;
-  int r = 0;
-  if (t < p.num_tiles) {
-    issue(t, 0, 0);
-    issued = 1;
-  }
-#pragma unroll 1
-  while (t < p.num_tiles) {
-    // prefetch the next fetch into the other slot: its previous contents were
-    // read by this warp in the previous iteration (the loaded values were
-    // consumed there, so the reads are complete; all lanes are past them)
-    int t2 = t, r2 = r + 1;
-    if (r2 == n_raw) {
-      t2 = t + tile_step;
-      r2 = 0;
-    }
-    __syncwarp();
-    if (t2 < p.num_tiles) {
-      issue(t2, r2, (seq + 1) & 1u);
-      ++issued;
-    }
-    const uint32_t slot = seq & 1u;
-    if (!mbar_wait(&raw_full[slot], (seq >> 1) & 1u, w, kSiteScaleEmpty)) break;
-    const uint32_t raw = smem_u32(smem + C::OFF_RAW + slot * C::RAW_STAGE_BYTES);
-    uint4 a[4];
-    uint4 b[4 * C::NB128];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) a[j] = ld_shared_v4(raw + 16 * (32 * j + lane));
-#pragma unroll
-    for (int i = 0; i < 4 * C::NB128; ++i) {
-      if constexpr (C::SFB32) {
-        // tile rows 32i + lane all take the scale row of 32-row group i
-        b[i] = i < C::BN / 32 ? ld_shared_v4(raw + C::RAW_A_BYTES + 16 * i) : make_uint4(0u, 0u, 0u, 0u);
-      } else {
-        b[i] = ld_shared_v4(raw + C::RAW_A_BYTES + 16 * (32 * i + lane));
-      }
-    }
-    ++seq;
-    // the fetch's k-blocks, published in pairs: one proxy fence for two atom
-    // slots (larger batches would hold atom slots back from the copies)
-    bool ok = true;
-    int pending = 0;  // atom slots written and not yet published
-    auto publish = [&]() {
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        int s = stage - pending;
-        if (s < 0) s += C::STAGES;
-#pragma unroll 1
-        for (int i = 0; i < pending; ++i) {
-          scale_slot_ready<C>(sf_full, s);
-          if (++s == C::STAGES) s = 0;
-        }
-      }
-      pending = 0;
-    };
-#pragma unroll
-    for (int sub = 0; sub < C::RAW_KB; ++sub) {
-      const int kb = r * C::RAW_KB + sub;
-      if (kb < p.num_kb) {
-        if (!mbar_wait(&sf_ready[stage], phase ^ 1u, w, kSiteScaleEmpty)) {
-          ok = false;
-          break;
-        }
-        write_scale_atoms<C>(smem_u32(smem + C::OFF_SF + stage * C::SF_STAGE_BYTES), lane, a, b,
-                             sub * C::SF_ATOMS_K);
-        if (++stage == C::STAGES) {
-          stage = 0;
-          phase ^= 1u;
-        }
-        if (++pending == 2) publish();
-      }
-    }
-    if (pending > 0) publish();
-    if (!ok) break;
-    t = t2;
-    r = r2;
-  }
-  // leave no fetch in flight: wait (bounded) for every issued, unconsumed one
-#pragma unroll 1
-  for (uint32_t i = seq; i < issued; ++i) {
-    const uint32_t a = smem_u32(&raw_full[i & 1u]);
-    const uint64_t t0 = global_timer_ns();
-    while (!mbar_try_wait(a, (i >> 1) & 1u)) {
-      if (global_timer_ns() - t0 > p.timeout_ns) {
-        report_error(p.err, kDevErrTimeout, kSiteProducerDrain, i);
-        break;
-      }
-    }
-  }
-}
-
-// Scale staging with plain loads (any K % 32 == 0): per ring stage, four
-// scale bytes per row and atom, one 32-bit load each.
-template <class C>
-__device__ __forceinline__ void scale_stager_ldg(const GemmParams& p, uint8_t* smem, uint64_t* sf_full, uint64_t* sf_ready,
-                                                 const WaitCtl& w, int lane, int tile0, int tile_step, uint32_t rank) {
-  int stage = 0;
-  uint32_t phase = 0;
-  bool ok = true;
-#pragma unroll 1
-  for (int t = tile0; ok && t < p.num_tiles; t += tile_step) {
-    int mb, nb;
-    tile_coords(p, t, mb, nb);
-    const int a_row = mb * C::TILE_M + static_cast<int>(rank) * C::BM;
-#pragma unroll 1
-    for (int kb = 0; kb < p.num_kb; ++kb) {
-      if (!mbar_wait(&sf_ready[stage], phase ^ 1u, w, kSiteScaleEmpty)) {
-        ok = false;
-        break;
-      }
-      const uint32_t sf = smem_u32(smem + C::OFF_SF + stage * C::SF_STAGE_BYTES);
-      const int col0 = kb * C::SF_PER_STAGE;
-      // atom g: 128 rows x 4 bytes; row r = 32j + lane lives in 16-byte line `lane`, word j
-#pragma unroll
-      for (int g = 0; g < C::SF_ATOMS_K; ++g) {
-        uint32_t v[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) v[j] = load_sf4(p.sA, a_row + 32 * j + lane, p.M, col0 + 4 * g, p.sf_cols);
-        st_shared_v4(sf + 512 * g + 16 * lane, v[0], v[1], v[2], v[3]);
-      }
-#pragma unroll
-      for (int g = 0; g < C::SF_ATOMS_K; ++g) {
-#pragma unroll
-        for (int rb = 0; rb < C::NB128; ++rb) {
-          uint32_t v[4];
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            if constexpr (C::SFB32) {
-              v[j] = load_sf4(p.sB, (nb * C::BN + rb * 128 + 32 * j) / 32, (p.N + 31) / 32, col0 + 4 * g, p.sf_cols);
-            } else {
-              v[j] = load_sf4(p.sB, nb * C::BN + rb * 128 + 32 * j + lane, p.N, col0 + 4 * g, p.sf_cols);
-            }
-          }
-          st_shared_v4(sf + C::SFA_BYTES + 512 * (g * C::NB128 + rb) + 16 * lane, v[0], v[1], v[2], v[3]);
-        }
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) scale_slot_ready<C>(sf_full, stage);
-      if (++stage == C::STAGES) {
-        stage = 0;
-        phase ^= 1u;
-      }
-    }
-  }
-}
-
-// Scale-factor copies of the MMA-issuing CTA (block-scaled kinds): per ring
-// slot, once its atoms are written (both CTAs' in a pair) and the MMAs of the
-// slot's previous round have completed (empty), copy the atoms (A's first,
-// then B's) into the slot's TMEM columns and commit to sf_ready, multicast to
-// both CTAs of a pair: the MMA warp waits on it, and so does each CTA's scale
-// warp before it rewrites the atoms.
-template <class C>
-__device__ __forceinline__ void scale_copier(const GemmParams& p, uint8_t* smem, uint32_t tmem, uint64_t* sf_full,
+__device__ __forceinline__ void scale_copier(const GemmParams& p, uint8_t* smem, uint32_t tmem, uint64_t* full,
                                              uint64_t* sf_ready, uint64_t* empty, const WaitCtl& w, int tile0,
-                                             int tile_step) {
+                                             int tile_step, int part) {
   int stage = 0;
   uint32_t phase = 0;
   long long issued = 0;
@@ -764,8 +472,7 @@ __device__ __forceinline__ void scale_copier(const GemmParams& p, uint8_t* smem,
   for (int t = tile0; ok && t < p.num_tiles; t += tile_step) {
 #pragma unroll 1
     for (int kb = 0; kb < p.num_kb; ++kb) {
-      bool ready = C::PAIR ? mbar_wait_cluster(&sf_full[stage], phase, w, kSiteScaleCopy)
-                           : mbar_wait(&sf_full[stage], phase, w, kSiteScaleCopy);
+      bool ready = mbar_wait(&full[stage], phase, w, kSiteScaleCopy);
       // the slot's TMEM scales of the previous round have been read by their MMAs
       ready = ready && mbar_wait(&empty[stage], phase ^ 1u, w, kSiteScaleCopy);
       if (!ready) {
@@ -776,9 +483,16 @@ __device__ __forceinline__ void scale_copier(const GemmParams& p, uint8_t* smem,
       const uint32_t sf_tmem = tmem + static_cast<uint32_t>(C::COL_SF + stage * C::SF_COLS_STAGE);
       const uint32_t sf_smem = smem_u32(smem + C::OFF_SF + stage * C::SF_STAGE_BYTES);
 #pragma unroll
-      for (int i = 0; i < C::SF_ATOMS_K + C::SF_ATOMS_K * C::NB128; ++i) {
-        const uint32_t col = i < C::SF_ATOMS_K ? 4 * i : C::SF_COLS_A + 4 * (i - C::SF_ATOMS_K);
-        const uint32_t src = i < C::SF_ATOMS_K ? sf_smem + 512 * i : sf_smem + C::SFA_BYTES + 512 * (i - C::SF_ATOMS_K);
+      for (int i = part; i < C::SF_ATOMS_K + C::SF_ATOMS_K * C::NB128; i += 2) {
+        uint32_t col, src;
+        if (i < C::SF_ATOMS_K) {
+          col = 4 * i;
+          src = sf_smem + 512 * i;
+        } else {
+          const int b = i - C::SF_ATOMS_K;  // TMEM order: K-group g = b / NB128, row block rb = b % NB128
+          col = C::SF_COLS_A + 4 * b;
+          src = sf_smem + C::SFA_BYTES + 512 * ((b % C::NB128) * C::SF_ATOMS_K + b / C::NB128);
+        }
         if constexpr (C::PAIR) {
           tmem_cp_32x128b_warpx4_pair(sf_tmem + col, make_smem_desc(src, 128, 128, 0));
         } else {
@@ -786,7 +500,7 @@ __device__ __forceinline__ void scale_copier(const GemmParams& p, uint8_t* smem,
         }
       }
       if constexpr (C::PAIR) {
-        umma_commit_pair_multicast(&sf_ready[stage], 0x3);
+        umma_commit_pair(&sf_ready[stage]);
       } else {
         umma_commit(&sf_ready[stage]);
       }
@@ -797,7 +511,7 @@ __device__ __forceinline__ void scale_copier(const GemmParams& p, uint8_t* smem,
       }
     }
   }
-  // leave no copy in flight: the last commit covers every earlier copy
+  // leave no copy in flight: this thread's last commit covers its earlier copies
   if (issued > 0) {
     const long long L = issued - 1;
     const uint32_t a = smem_u32(&sf_ready[static_cast<int>(L % C::STAGES)]);
@@ -824,11 +538,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
   uint64_t* acc_full = empty + C::STAGES;
   uint64_t* acc_empty = acc_full + C::ACC_BUFS;
   uint64_t* drain = acc_empty + C::ACC_BUFS;
-  uint64_t* raw_full = drain + 1;
-  // block-scaled kinds: a slot's scale atoms written (sf_full) and copied to
-  // TMEM (sf_ready, which also frees the atoms for the next round)
-  uint64_t* sf_full = raw_full + C::RAW_BUFS;
-  uint64_t* sf_ready = sf_full + C::STAGES;
+  uint64_t* sf_ready = drain + 1;  // block-scaled kinds: a slot's scales copied to TMEM
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_MISC + 4);
 
@@ -846,11 +556,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(&full[s], C::FULL_ARRIVALS);
       mbar_init(&empty[s], 1u);
-      if constexpr (C::MX) {
-        // a pair's peer gathers only its own scale warp (forwarded by its relay)
-        mbar_init(&sf_full[s], C::PAIR && !leader ? 1u : C::SF_ARRIVALS);
-        mbar_init(&sf_ready[s], 1u);
-      }
+      if constexpr (C::MX) mbar_init(&sf_ready[s], C::SF_COPIERS);
     }
 #pragma unroll 1
     for (int a = 0; a < C::ACC_BUFS; ++a) {
@@ -861,14 +567,12 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
       mbar_init(&acc_empty[a], static_cast<uint32_t>(C::EPI_WARPS + (C::PAIR && leader ? 1 : 0)));
     }
     mbar_init(drain, 1u);
-#pragma unroll 1
-    for (int b = 0; b < C::RAW_BUFS; ++b) mbar_init(&raw_full[b], p.sf_mode == kSfAsync ? 32u : 1u);
     *abort_flag = 0u;
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
     tma_prefetch_desc(&tmOut);
-    if (C::MX && p.sf_mode == kSfTma) {
+    if (C::MX) {
       tma_prefetch_desc(&tmSA);
       tma_prefetch_desc(&tmSB);
     }
@@ -892,6 +596,9 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
   if (warp == 0) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
+      // block-scaled kinds: the scale-atom pre-pass (the previous kernel of the
+      // stream, launched before this one may start) has completed
+      if constexpr (C::MX) griddep_wait();
       int stage = 0;
       uint32_t phase = 0;
       long long issued = 0;
@@ -919,6 +626,27 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
             mbar_arrive_expect_tx(&full[stage], C::STAGE_TX);
             tma_load_2d(smem + C::OFF_A + stage * C::A_BYTES, &tmA, &full[stage], kb * C::TMA_K, a_row);
             tma_load_2d(smem + C::OFF_B + stage * C::B_BYTES, &tmB, &full[stage], kb * C::TMA_K, b_row);
+          }
+          if constexpr (C::MX) {
+            // the stage's scale atoms: A's 128-row block, then each 128-row block
+            // of the B tile; atom maps are [blocks * gpad * 2, 256 bytes], a box
+            // being SF_ATOMS_K consecutive atoms of one block
+            uint8_t* sf = smem + C::OFF_SF + stage * C::SF_STAGE_BYTES;
+            const int ya = ((a_row / 128) * p.sf_gpad + kb * C::SF_ATOMS_K) * 2;
+            if constexpr (C::PAIR) {
+              const uint32_t fb = full_leader + 8u * static_cast<uint32_t>(stage);
+              tma_load_2d_pair(sf, &tmSA, fb, 0, ya);
+#pragma unroll
+              for (int rb = 0; rb < C::NB128; ++rb)
+                tma_load_2d_pair(sf + C::SFA_BYTES + rb * C::SF_ATOMS_K * 512, &tmSB, fb, 0,
+                                 ((nb * C::NB128 + rb) * p.sf_gpad + kb * C::SF_ATOMS_K) * 2);
+            } else {
+              tma_load_2d(sf, &tmSA, &full[stage], 0, ya);
+#pragma unroll
+              for (int rb = 0; rb < C::NB128; ++rb)
+                tma_load_2d(sf + C::SFA_BYTES + rb * C::SF_ATOMS_K * 512, &tmSB, &full[stage], 0,
+                            ((nb * C::NB128 + rb) * p.sf_gpad + kb * C::SF_ATOMS_K) * 2);
+            }
           }
           ++issued;
           if (++stage == C::STAGES) {
@@ -1091,47 +819,10 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
       }
     }
     __syncwarp();
-  } else if (warp == 2) {
-    // ---------------- scale stager (MX) ----------------
+  } else if (warp == 2 || warp == 3) {
+    // ---------------- scale-factor copies (block-scaled kinds, the MMA-issuing CTA) ----------------
     if constexpr (C::MX) {
-      if (p.sf_mode == kSfTma || p.sf_mode == kSfAsync) {
-        scale_stager_raw<C>(p, &tmSA, &tmSB, smem, sf_full, sf_ready, raw_full, w, lane, tile0, tile_step, rank);
-      } else {
-        scale_stager_ldg<C>(p, smem, sf_full, sf_ready, w, lane, tile0, tile_step, rank);
-      }
-    }
-    __syncwarp();
-  } else if (warp == 3) {
-    if constexpr (C::MX) {
-      if (issues_mma && lane == 0) scale_copier<C>(p, smem, tmem, sf_full, sf_ready, empty, w, tile0, tile_step);
-    }
-    // ---------------- scale relay (the peer CTA of an MX pair) ----------------
-    if constexpr (C::MX && C::PAIR) {
-      if (!leader && lane == 0) {
-        const uint32_t sf_full_leader = mapa_shared(smem_u32(&sf_full[0]), 0u);
-        int stage = 0;
-        uint32_t phase = 0;
-        bool ok = true;
-#pragma unroll 1
-        for (int t = tile0; ok && t < p.num_tiles; t += tile_step) {
-#pragma unroll 1
-          for (int kb = 0; kb < p.num_kb; ++kb) {
-            if (!mbar_wait(&sf_full[stage], phase, w, kSiteScaleEmpty)) {
-              ok = false;
-              break;
-            }
-            // CTA-scope release, no cluster-wide fence: the atoms stay in this
-            // CTA's shared memory, where the scale warp's fence.proxy.async and
-            // its completed local arrive (observed above) have already put them
-            // for the leader's copy to read.
-            mbar_arrive_remote(sf_full_leader + 8u * static_cast<uint32_t>(stage));
-            if (++stage == C::STAGES) {
-              stage = 0;
-              phase ^= 1u;
-            }
-          }
-        }
-      }
+      if (issues_mma && lane == 0) scale_copier<C>(p, smem, tmem, full, sf_ready, empty, w, tile0, tile_step, warp - 2);
     }
     __syncwarp();
   } else if (warp >= 4) {

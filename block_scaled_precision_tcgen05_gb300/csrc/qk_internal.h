@@ -53,7 +53,8 @@ enum KernelKind : int {
   kKQuantize = 6,
   kKGemmNvfp4 = 7,
   kKGemmFp8Blockscale = 8,
-  kKNumKinds = 9,
+  kKSfAtoms = 9,
+  kKNumKinds = 10,
 };
 
 // Brackets one kernel launch with an event pair when timing is enabled.

@@ -48,10 +48,13 @@ constexpr int kernel_kind() {
                                  : kKGemmFp8Blockscale;
 }
 
-// tsa / tsb: tensor maps of the raw scale rows (MX with p.sf_tma), else any map.
+// tsa / tsb: tensor maps of the scale atoms (block-scaled kinds), else any map.
+// after_prepass: launch with programmatic stream serialization, so the kernel's
+// prologue overlaps the kernel before it in the stream (the scale-atom
+// pre-pass, which the producer waits for before its first load).
 template <class C>
 int launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsa, const CUtensorMap& tsb,
-                const GemmParams& p, const DeviceInfo& dev, cudaStream_t stream) {
+                const GemmParams& p, const DeviceInfo& dev, cudaStream_t stream, bool after_prepass = false) {
   auto kernel = qk_gemm_kernel<C>;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return QK_ERR_CUDA;
@@ -59,7 +62,7 @@ int launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap&
   cfg.blockDim = dim3(C::NUM_THREADS, 1, 1);
   cfg.dynamicSmemBytes = C::SMEM_BYTES;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   int slots = dev.sm_count;  // concurrently resident CTAs (one per SM) or CTA pairs
   if constexpr (C::CTAS > 1) {
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -85,6 +88,12 @@ int launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap&
   }
   const int ctas = (p.num_tiles < slots ? p.num_tiles : slots) * C::CTAS;
   cfg.gridDim = dim3(ctas, 1, 1);
+  if (after_prepass) {
+    attr[cfg.numAttrs].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[cfg.numAttrs].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    ++cfg.numAttrs;
+  }
   // the output as 32x32 boxes with the swizzle of the staging blocks
   CUtensorMap tout;
   if (encode_tmap_out(&tout, p.out, static_cast<uint64_t>(p.M), static_cast<uint64_t>(p.N),

@@ -2,7 +2,7 @@
 // tcgen05.mma kind::mxf8f6f4.block_scale.scale_vec::1X.  The raw row-major
 // [rows, K/32] scale bytes (ROCm/mori PR #806, "What") are staged per ring
 // slot by the kernel's scale warp and moved to TMEM with tcgen05.cp.
-#include "qk_launch.cuh"
+#include "qk_sf_atoms.cuh"
 #include "qk_fewrow_launch.cuh"
 
 namespace qk {
@@ -14,45 +14,6 @@ namespace qk {
 // with 8 epilogue warps working from TMEM; one CTA with 128 x 256 tiles and
 // one accumulator, whose epilogue stalls the MMAs.
 using CfgMxfp8PairDrain = GemmCfg<Kind::MXF8, 256, 5, 1, true, 16, 1>;
-// The same kernel with B's scales per 32x32 block (ROCm/mori PR #806's
-// mxfp8_raw form): the scale warp stages one raw scale row per 32 tile rows
-// and writes it into all 32 rows' places of the atoms.
-using CfgMxfp8PairDrainB32 = GemmCfg<Kind::MXF8, 256, 5, 1, true, 16, 1, OutType::BF16, true>;
-
-template <class C>
-static int launch_mxfp8_cfg(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const uint8_t* sB,
-                      const uint16_t* bias, uint16_t* out, int M, int N, int K, const DeviceInfo& dev,
-                      cudaStream_t stream) {
-  CUtensorMap ta, tb;
-  int st = encode_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, K, M, K, C::TMA_K, C::BM);
-  if (st == QK_OK) st = encode_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, K, N, K, C::TMA_K, C::B_LOAD_ROWS);
-  if (st != QK_OK) return st;
-  GemmParams p{};
-  plan_tiles<C>(p, M, N, K);
-  p.bias = bias;
-  p.out = out;
-  p.sA = sA;
-  p.sB = sB;
-  p.sf_cols = K / 32;
-  p.err = dev.err_word;
-  p.timeout_ns = wait_timeout_ns();
-  // Raw scale rows go through TMA when their pitch (K/32 bytes) and base
-  // addresses are 16-byte multiples, through cp.async when they are 4-byte
-  // multiples, else through per-stage loads.
-  CUtensorMap tsa = ta, tsb = tb;
-  const bool a16 = ((reinterpret_cast<uintptr_t>(sA) | reinterpret_cast<uintptr_t>(sB)) & 15u) == 0;
-  p.sf_mode = (p.sf_cols % 16 == 0 && a16) ? kSfTma : (p.sf_cols % 4 == 0 ? kSfAsync : kSfLoads);
-  if (p.sf_mode == kSfTma) {
-    st = encode_tmap_2d_plain(&tsa, CU_TENSOR_MAP_DATA_TYPE_UINT8, sA, p.sf_cols, M, p.sf_cols, 16, C::BM);
-    // B's scale rows: one per row of B, or one per 32 rows (C::SFB32)
-    const uint64_t sb_rows = C::SFB32 ? static_cast<uint64_t>((N + 31) / 32) : static_cast<uint64_t>(N);
-    if (st == QK_OK)
-      st = encode_tmap_2d_plain(&tsb, CU_TENSOR_MAP_DATA_TYPE_UINT8, sB, p.sf_cols, sb_rows, p.sf_cols, 16,
-                                C::SFB32 ? C::BN / 32 : C::BN);
-    if (st != QK_OK) return st;
-  }
-  return launch_gemm<C>(ta, tb, tsa, tsb, p, dev, stream);
-}
 
 // Few rows (M <= 128): the few-row kernels' MXFP8 mode (qk_fewrow_launch.cuh).
 // Against the tile kernel (us): the cluster split-K kernel, when all tiles'
@@ -99,15 +60,17 @@ int launch_mxfp8(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const ui
       if (st != QK_ERR_RANGE) return st;
     }
   }
-  return launch_mxfp8_cfg<CfgMxfp8PairDrain>(A, sA, B, sB, bias, out, M, N, K, dev, stream);
+  return launch_block_scaled<CfgMxfp8PairDrain>(A, sA, B, sB, 1, nullptr, nullptr, bias, out, M, N, K, dev, stream);
 }
 
-// B scales per 32x32 block: the tile kernel for every M (the few-row kernels
-// stage per-row scales only).
+// B scales per 32x32 block (ROCm/mori PR #806's mxfp8_raw form): the scale-atom
+// pre-pass places each 32-row group's scale bytes at all 32 rows; the tile
+// kernel runs for every M (the few-row kernels stage per-row scales only).
 int launch_mxfp8_b32(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const uint8_t* sB32,
                      const uint16_t* bias, uint16_t* out, int M, int N, int K, const DeviceInfo& dev,
                      cudaStream_t stream) {
-  return launch_mxfp8_cfg<CfgMxfp8PairDrainB32>(A, sA, B, sB32, bias, out, M, N, K, dev, stream);
+  return launch_block_scaled<CfgMxfp8PairDrain>(A, sA, B, sB32, 32, nullptr, nullptr, bias, out, M, N, K, dev,
+                                                stream);
 }
 
 }  // namespace qk

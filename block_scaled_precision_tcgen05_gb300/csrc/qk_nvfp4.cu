@@ -4,52 +4,16 @@
 // of K = 64).  The per-tensor scales are the optional NVFP4 arguments of
 // ROCm/aiter PR #6262's gemm_a4w4; the epilogue multiplies the fp32
 // accumulator by their fp32 product before the bias.
-#include "qk_launch.cuh"
+#include "qk_sf_atoms.cuh"
 
 namespace qk {
 
-// 256 x 256 tiles on a 2-SM CTA pair, four stages, one accumulator drained
-// by 16 epilogue warps into registers and released before the epilogue math.
-// Measured alternatives, slower and not built: the pair with five stages and
-// 8 epilogue warps working from TMEM; 128 x 256 tiles on one CTA, where the
-// 16 scale bytes per row per stage (6 KB of shared memory and 48 TMEM columns
-// per slot) leave room for three stages.
-using CfgNvfp4PairDrain = GemmCfg<Kind::NVF4, 256, 4, 1, true, 16, 1>;
-
-template <class C>
-static int launch_nvfp4_cfg(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const uint8_t* sB,
-                            const float* ga, const float* gb, const uint16_t* bias, uint16_t* out, int M, int N,
-                            int K, const DeviceInfo& dev, cudaStream_t stream) {
-  CUtensorMap ta, tb;
-  const uint64_t kb = static_cast<uint64_t>(K) / 2;  // bytes per row
-  int st = encode_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, kb, M, kb, C::TMA_K, C::BM);
-  if (st == QK_OK) st = encode_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, kb, N, kb, C::TMA_K, C::B_LOAD_ROWS);
-  if (st != QK_OK) return st;
-  GemmParams p{};
-  plan_tiles<C>(p, M, N, K);
-  p.bias = bias;
-  p.out = out;
-  p.sA = sA;
-  p.sB = sB;
-  p.sf_cols = K / 16;
-  p.ga = ga;
-  p.gb = gb;
-  p.err = dev.err_word;
-  p.timeout_ns = wait_timeout_ns();
-  // Raw scale rows (K/16 bytes) through TMA when the pitch and base addresses
-  // are 16-byte multiples, through cp.async at 4-byte multiples, else loads.
-  CUtensorMap tsa = ta, tsb = tb;
-  const bool a16 = ((reinterpret_cast<uintptr_t>(sA) | reinterpret_cast<uintptr_t>(sB)) & 15u) == 0;
-  const bool a4 = ((reinterpret_cast<uintptr_t>(sA) | reinterpret_cast<uintptr_t>(sB)) & 3u) == 0;
-  p.sf_mode = (p.sf_cols % 16 == 0 && a16) ? kSfTma : ((p.sf_cols % 4 == 0 && a4) ? kSfAsync : kSfLoads);
-  if (p.sf_mode == kSfTma) {
-    st = encode_tmap_2d_plain(&tsa, CU_TENSOR_MAP_DATA_TYPE_UINT8, sA, p.sf_cols, M, p.sf_cols, 16, C::BM);
-    if (st == QK_OK)
-      st = encode_tmap_2d_plain(&tsb, CU_TENSOR_MAP_DATA_TYPE_UINT8, sB, p.sf_cols, N, p.sf_cols, 16, C::BN);
-    if (st != QK_OK) return st;
-  }
-  return launch_gemm<C>(ta, tb, tsa, tsb, p, dev, stream);
-}
+// 256 x 256 tiles on a 2-SM CTA pair, five stages (32 KB of operands and 6 KB
+// of scale atoms each), one accumulator drained by 16 epilogue warps into
+// registers and released before the epilogue math.  Four stages measured 8%
+// slower.  Measured alternatives, slower and not built: the pair with 8
+// epilogue warps working from TMEM; 128 x 256 tiles on one CTA.
+using CfgNvfp4PairDrain = GemmCfg<Kind::NVF4, 256, 5, 1, true, 16, 1>;
 
 }  // namespace qk
 
@@ -76,5 +40,5 @@ extern "C" int qk_gemm_nvfp4(const uint8_t* A, const uint8_t* sA, const uint8_t*
   if (!dev) return st;
   const auto s = static_cast<cudaStream_t>(stream);
   const int m = static_cast<int>(M), n = static_cast<int>(N), k = static_cast<int>(K);
-  return launch_nvfp4_cfg<CfgNvfp4PairDrain>(A, sA, B, sB, ga, gb, bias, out, m, n, k, *dev, s);
+  return launch_block_scaled<CfgNvfp4PairDrain>(A, sA, B, sB, 1, ga, gb, bias, out, m, n, k, *dev, s);
 }
