@@ -494,6 +494,9 @@ def secondary_formats(qk, dev, peaks, which):
             l2, ms2 = kstats.get(kname2, (0, 0.0))
             if l2:
                 line["widen_ms"] = round(ms2 / l2, 4)
+        if "sf_atoms" in kstats:   # the block-scaled kinds' scale-atom pre-pass
+            l3, ms3 = kstats["sf_atoms"]
+            line["sf_atoms_ms"] = round(ms3 / max(l3, 1), 4)
         if few:
             hot = _hot_kernel_ms(qk, fn, kname, 20, dev)
             line["hot_kernel_ms"] = round(hot, 4) if hot else None
