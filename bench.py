@@ -334,30 +334,38 @@ def time_e2e(qk, p, steps, dev):
 
 
 def time_calls(fn, iters, warmup, dev, flush):
-    """Per-call event pairs with an L2 flush before each timed call; returns (median ms, kernel stats)."""
+    """Median call time over `iters` calls, each after an L2 flush, with the library's own
+    timing off (its event records would sit between a call's kernels); then the same calls
+    again with it on for the per-kernel times.  Returns (median ms, kernel stats)."""
     import torch
     import block_scaled_precision_tcgen05_gb300 as qk
     for _ in range(warmup):
         fn()
     torch.cuda.synchronize(dev)
     stream = torch.cuda.current_stream(dev)
-    times = []
+
+    def flushed_calls():
+        times = []
+        for _ in range(iters):
+            # read (not write) twice the L2's size: the timed call starts cold, with no
+            # dirty lines of the flush left in L2 for its own loads to write back
+            flush.sum(dtype=torch.int32)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            e1.synchronize()
+            times.append(e0.elapsed_time(e1))
+        return statistics.median(times)
+
+    ms = flushed_calls()
     qk.profile_read(reset=True)
     qk.profile_enable(True)
-    for _ in range(iters):
-        # read (not write) twice the L2's size: the timed call starts cold, with no
-        # dirty lines of the flush left in L2 for its own loads to write back
-        flush.sum(dtype=torch.int32)
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        fn()
-        e1.record(stream)
-        e1.synchronize()
-        times.append(e0.elapsed_time(e1))
+    flushed_calls()
     qk.profile_enable(False)
     kstats = qk.profile_read(reset=True)
-    return statistics.median(times), kstats
+    return ms, kstats
 
 
 # Every configuration's shapes beside the headline: INT8 256x256x512 (the
