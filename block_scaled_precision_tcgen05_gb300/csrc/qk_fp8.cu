@@ -17,6 +17,22 @@ using CfgFp8 = GemmCfg<Kind::F8, 256, 6, 2, true, 8, 1>;
 // the epilogue math: 2945 / 3068 TFLOP/s against 2840 / 3026 at K = 1792
 // (and 1% slower than CfgFp8 at K = 5376 and 8192).
 using CfgFp8Drain = GemmCfg<Kind::F8, 256, 6, 2, true, 16, 1>;
+// 256 x 128 tiles per CTA pair (each SM loads 24 KB per 128-K stage instead of
+// 32 for half the work), eight stages, two 128-column accumulators: twice the
+// tiles of CfgFp8, for problems whose 256 x 256 tiles leave pairs idle.
+using CfgFp8Narrow = GemmCfg<Kind::F8, 128, 8, 2, true, 8, 1>;
+
+// Whether 256 x 128 pair tiles finish sooner than 256 x 256 ones: waves of
+// tiles over the SM pairs, a narrow tile's k-block costing about 3/4 of a wide
+// one's per SM (24 against 32 KB of operands at the per-SM ingress that bounds
+// both), with a 10% margin for the narrow tiles' extra epilogues.
+static bool narrow_tiles_win(int M, int N, const DeviceInfo& dev) {
+  const long long pairs = dev.sm_count / 2;
+  const long long mb = (M + 255) / 256;
+  const long long wide = mb * ((N + 255) / 256), narrow = mb * ((N + 127) / 128);
+  const long long waves_wide = (wide + pairs - 1) / pairs, waves_narrow = (narrow + pairs - 1) / pairs;
+  return waves_narrow * 3 * 10 < waves_wide * 4 * 9;
+}
 
 template <class C>
 static int launch_fp8_cfg(const uint8_t* A, const uint8_t* B, const float* sa, const float* sb, const uint16_t* bias,
@@ -75,6 +91,7 @@ int launch_fp8_rowwise(const uint8_t* A, const uint8_t* B, const float* sa, cons
                            : launch_fewrow_fp8<128>(A, B, sa, sb, bias, out, M, N, K, dev, stream, v);
     if (st != QK_ERR_RANGE) return st;
   }
+  if (narrow_tiles_win(M, N, dev)) return launch_fp8_cfg<CfgFp8Narrow>(A, B, sa, sb, bias, out, M, N, K, dev, stream);
   if (K <= 2048) return launch_fp8_cfg<CfgFp8Drain>(A, B, sa, sb, bias, out, M, N, K, dev, stream);
   return launch_fp8_cfg<CfgFp8>(A, B, sa, sb, bias, out, M, N, K, dev, stream);
 }
