@@ -189,12 +189,13 @@ int encode_tmap_2d_plain(CUtensorMap* map, CUtensorMapDataType dtype, const void
   return encode_2d(map, dtype, base, inner, rows, row_pitch_bytes, box_inner, box_rows, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
-int encode_tmap_out(CUtensorMap* map, void* out, uint64_t rows, uint64_t cols, int out_type) {
+int encode_tmap_out(CUtensorMap* map, void* out, uint64_t rows, uint64_t cols, int out_type, int block_cols) {
   if (out_type == QK_OUT_FP32)
     return encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, out, cols, rows, cols * 4, 32, 32,
                      CU_TENSOR_MAP_SWIZZLE_128B);
   return encode_2d(map, out_type == QK_OUT_FP16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-                   out, cols, rows, cols * 2, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
+                   out, cols, rows, cols * 2, block_cols == 16 ? 16 : 32, 32,
+                   block_cols == 16 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
 int kernel_variant(const char* env_name) {

@@ -17,6 +17,7 @@ namespace qk {
 // ---------------------------------------------------------------------------
 enum : uint32_t {
   kDevErrTimeout = 1,
+  kDevErrSmemBase = 2,  // a layout without alignment slack found its shared-memory base unaligned
 };
 
 enum : uint32_t {
@@ -31,6 +32,7 @@ enum : uint32_t {
   kSitePeerPartial = 9,  // stream-K: another CTA's partial of a shared tile
   kSiteMmaScales = 10,    // MMA warp: a ring slot's scale factors copied to TMEM
   kSiteScaleCopy = 11,    // scale-copy thread: a ring slot's scale atoms written
+  kSiteSmemBase = 12,     // kernel entry: the dynamic shared-memory base
 };
 
 __device__ __forceinline__ void report_error(unsigned long long* err, uint32_t code, uint32_t site,

@@ -97,8 +97,10 @@ struct GemmParams {
 // thread) instead of TMEM, which frees TMEM for two accumulators.
 // OUT_BUFS_: shared-memory staging blocks per epilogue warp for bulk tensor
 // stores of the output; 0 = the epilogue stores straight to global memory.
+// OUT_COLS_: columns of a staging block (32 rows each): 32, or 16 for 16-bit
+// outputs (half the staging memory, twice the bulk stores).
 template <Kind KIND, int BN_, int STAGES_, int ACC_BUFS_, bool PAIR_ = false, int EPI_WARPS_ = 4,
-          int OUT_BUFS_ = 2, OutType OUT_ = OutType::BF16>
+          int OUT_BUFS_ = 2, OutType OUT_ = OutType::BF16, int OUT_COLS_ = 32>
 struct GemmCfg {
   static constexpr Kind kind = KIND;
   static constexpr OutType OUT = OUT_;
@@ -157,19 +159,26 @@ struct GemmCfg {
   static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
   static constexpr int OFF_SF = OFF_B + STAGES * B_BYTES;
   static constexpr int OFF_SF_END = OFF_SF + STAGES * SF_STAGE_BYTES;
-  // Output staging: each epilogue warp writes 32x32 blocks (bf16 / fp16: 2 KB
-  // with the 64-byte swizzle; fp32: 4 KB with the 128-byte swizzle) that a
-  // bulk tensor store copies to global memory.
+  // Output staging: each epilogue warp writes blocks of 32 rows that a bulk
+  // tensor store copies to global memory: 32 columns (bf16 / fp16: 2 KB with
+  // the 64-byte swizzle; fp32: 4 KB with the 128-byte swizzle) or 16 columns
+  // of a 16-bit type (1 KB with the 32-byte swizzle).
   static constexpr int OUT_BUFS = OUT_BUFS_;
   static constexpr bool STORE_TMA = OUT_BUFS_ > 0;
-  static constexpr int OUT_BLOCK_BYTES = 32 * 32 * OUT_ELEM_BYTES;
+  static constexpr int OUT_COLS = OUT_COLS_;
+  static constexpr int OUT_BLOCK_BYTES = 32 * OUT_COLS * OUT_ELEM_BYTES;
   static constexpr int OFF_OUT = (OFF_SF_END + 1023) & ~1023;
   static constexpr int OFF_BAR = OFF_OUT + EPI_WARPS * OUT_BUFS * OUT_BLOCK_BYTES;
   // ring full/empty, accumulator full/empty, drain, and (block-scaled kinds)
   // a slot's scales copied to TMEM
   static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC_BUFS + 1 + (MX ? STAGES : 0);
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
-  static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack to align the base to 1024
+  static constexpr int SMEM_USED = OFF_MISC + 16;
+  // + slack to align the base to 1024 bytes where it fits; a layout without it
+  // takes the dynamic shared-memory base as it comes (1024-aligned when the
+  // kernel has no static shared memory) and checks that at entry
+  static constexpr int ALIGN_SLACK = SMEM_USED + 1024 <= 232448 ? 1024 : 0;
+  static constexpr int SMEM_BYTES = SMEM_USED + ALIGN_SLACK;
 
   static constexpr int COL_ACC = 0;
   static constexpr int COL_SUM = ACC_BUFS * BN;
@@ -193,6 +202,7 @@ struct GemmCfg {
   static_assert(!BLOCKSCALE || REG_SUMS, "blockscale sums live in registers");
   static_assert(COLS_USED <= 512, "TMEM budget");
   static_assert(SMEM_BYTES <= 232448, "shared-memory budget");
+  static_assert(OUT_COLS == 32 || (OUT_COLS == 16 && OUT_ELEM_BYTES == 2), "staging block width");
   static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "swizzle atoms need 1024-byte alignment");
   static_assert(!MX || BN % 128 == 0, "scale atoms cover 128 rows of B");
 
@@ -281,20 +291,24 @@ __device__ __forceinline__ uint32_t pack_out16x2(float lo, float hi) {
   else return pack_bf16x2(lo, hi);
 }
 
-// Epilogue of 32 consecutive columns [n0, n0+32) of one row m, in four steps
-// of 8 columns (8 column scales, 8 biases live at a time), written to row
-// `lane` of a 32x32 staging block with the swizzle the output tensor map
-// uses: bf16 / fp16 rows of 64 bytes, 16-byte chunk c of row r at
-// 64r + 16(c ^ ((r >> 1) & 3)); fp32 rows of 128 bytes, at 128r + 16(c ^ (r & 7)).
+// Epilogue of COLS (32 or 16) consecutive columns [n0, n0+COLS) of one row m,
+// in steps of 8 columns (8 column scales, 8 biases live at a time), written to
+// row `lane` of a 32-row staging block with the swizzle the output tensor map
+// uses: 32 bf16 / fp16 columns: rows of 64 bytes, 16-byte chunk c of row r at
+// 64r + 16(c ^ ((r >> 1) & 3)); 16 columns: rows of 32 bytes, chunk c at
+// 32r + 16(c ^ ((r >> 2) & 1)); 32 fp32 columns: rows of 128 bytes, at
+// 128r + 16(c ^ (r & 7)).
 // INT_ACC: v holds int32 sums; otherwise fp32 bit patterns.  Columns past N
 // (N is a multiple of 8) read no scale or bias; the bulk store clips them.
 // ALPHA: multiply by `sam` (the NVFP4 per-tensor scale product) before the bias.
-template <bool ROWWISE, bool INT_ACC, int OFF = 0, bool ALPHA = false, OutType OT = OutType::BF16, int LEN = 32>
+template <bool ROWWISE, bool INT_ACC, int OFF = 0, bool ALPHA = false, OutType OT = OutType::BF16, int COLS = 32,
+          int LEN = 32>
 __device__ __forceinline__ void epilogue_row32(const GemmParams& p, int n0, float sam, const uint32_t (&v)[LEN],
                                                uint32_t block, int lane) {
+  static_assert(COLS == 32 || (COLS == 16 && OT != OutType::F32), "staging block width");
   const bool has_bias = p.bias != nullptr;
 #pragma unroll
-  for (int s8 = 0; s8 < 4; ++s8) {
+  for (int s8 = 0; s8 < COLS / 8; ++s8) {
     const int n = n0 + 8 * s8;
     const bool in = n < p.N;
     float sbv[8];
@@ -340,8 +354,10 @@ __device__ __forceinline__ void epilogue_row32(const GemmParams& p, int n0, floa
       const uint32_t row = block + 128 * lane;
       st_shared_v4(row + 16 * ((2 * s8) ^ (lane & 7)), packed[0], packed[1], packed[2], packed[3]);
       st_shared_v4(row + 16 * ((2 * s8 + 1) ^ (lane & 7)), packed[4], packed[5], packed[6], packed[7]);
-    } else {
+    } else if constexpr (COLS == 32) {
       st_shared_v4(block + 64 * lane + 16 * (s8 ^ ((lane >> 1) & 3)), packed[0], packed[1], packed[2], packed[3]);
+    } else {
+      st_shared_v4(block + 32 * lane + 16 * (s8 ^ ((lane >> 2) & 1)), packed[0], packed[1], packed[2], packed[3]);
     }
   }
 }
@@ -531,7 +547,15 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
     qk_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
                    const __grid_constant__ CUtensorMap tmOut, const GemmParams p) {
-  extern __shared__ uint8_t smem_raw[];
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  if constexpr (C::ALIGN_SLACK == 0) {
+    // no room to align the base: give up (before any barrier, TMEM or cluster
+    // step, in every CTA alike) if it is not aligned
+    if ((smem_u32(smem_raw) & 1023u) != 0u) {
+      if (threadIdx.x == 0) report_error(p.err, kDevErrSmemBase, kSiteSmemBase, smem_u32(smem_raw));
+      return;
+    }
+  }
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* empty = full + C::STAGES;
@@ -884,10 +908,21 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
           constexpr bool kInt = decltype(tag)::kInt;
           constexpr int kOff = decltype(tag)::kOff;
           if (!(block_ok && n0 < p.N)) return;
-          if constexpr (C::STORE_TMA) {
+          if constexpr (C::STORE_TMA && C::OUT_COLS == 32) {
             const uint32_t block = out_block_acquire<C>(ostg, lane);
             epilogue_row32<C::ROWWISE || kInt, kInt, kOff, C::ALPHA, C::OUT>(p, n0, sam, vals, block, lane);
             out_block_release<C>(ostg, block, &tmOut, n0, m_block, lane);
+          } else if constexpr (C::STORE_TMA) {
+            // two 16-column blocks (the second one only where it starts inside N)
+            uint32_t block = out_block_acquire<C>(ostg, lane);
+            epilogue_row32<C::ROWWISE || kInt, kInt, kOff, C::ALPHA, C::OUT, 16>(p, n0, sam, vals, block, lane);
+            out_block_release<C>(ostg, block, &tmOut, n0, m_block, lane);
+            if (n0 + 16 < p.N) {
+              block = out_block_acquire<C>(ostg, lane);
+              epilogue_row32<C::ROWWISE || kInt, kInt, kOff + 16, C::ALPHA, C::OUT, 16>(p, n0 + 16, sam, vals, block,
+                                                                                      lane);
+              out_block_release<C>(ostg, block, &tmOut, n0 + 16, m_block, lane);
+            }
           } else if (row_ok) {
             epilogue_row32_global<C::ROWWISE || kInt, kInt, kOff, C::ALPHA, C::OUT>(p, m, n0, sam, vals);
           }

@@ -37,7 +37,8 @@ int encode_tmap_2d_plain(CUtensorMap* map, CUtensorMapDataType dtype, const void
 // bf16 [rows, cols] output in 32x32 boxes with the 64-byte swizzle.
 // The output as 32x32 boxes: bf16 / fp16 with the 64-byte swizzle, fp32 with
 // the 128-byte swizzle (out_type: a QK_OUT_* value).
-int encode_tmap_out(CUtensorMap* map, void* out, uint64_t rows, uint64_t cols, int out_type);
+// the output in boxes of 32 rows x block_cols (32, or 16 for 16-bit types) columns
+int encode_tmap_out(CUtensorMap* map, void* out, uint64_t rows, uint64_t cols, int out_type, int block_cols);
 
 uint64_t wait_timeout_ns();
 void count_launches(uint64_t n);

@@ -94,10 +94,10 @@ int launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap&
     cfg.attrs = attr;
     ++cfg.numAttrs;
   }
-  // the output as 32x32 boxes with the swizzle of the staging blocks
+  // the output as boxes of the staging blocks (32 rows x OUT_COLS), with their swizzle
   CUtensorMap tout;
   if (encode_tmap_out(&tout, p.out, static_cast<uint64_t>(p.M), static_cast<uint64_t>(p.N),
-                      static_cast<int>(C::OUT)) != QK_OK)
+                      static_cast<int>(C::OUT), C::OUT_COLS) != QK_OK)
     return QK_ERR_CUDA;
   LaunchTimer timer(kernel_kind<C>(), stream);
   e = cudaLaunchKernelEx(&cfg, kernel, ta, tb, tsa, tsb, tout, p);

@@ -7,15 +7,17 @@
 namespace qk {
 
 // 256 x 256 tiles on a 2-SM CTA pair (each SM loads half of B: 32 KB of
-// operands per 256-K stage instead of 48), five stages, one accumulator that
+// operands per 256-K stage instead of 48), six stages, one accumulator that
 // 16 epilogue warps drain into registers (64 columns each) and release before
-// the epilogue math, so the next tile's MMAs start after the drain.  Each CTA
+// the epilogue math, so the next tile's MMAs start after the drain.  The
+// output leaves in 32x16 staging blocks (1 KB), which leaves room for the
+// sixth stage (no room for alignment slack: the kernel checks its base).  Each CTA
 // loads the scale atoms of its own A rows and of all the tile's B rows; the
 // leader's two copy threads fill both CTAs' TMEM with cta_group::2 copies
 // beside the MMAs.  Measured alternatives (the same pair
 // with 8 epilogue warps working from TMEM; one CTA with 128 x 256 tiles) were
 // slower and are not built.
-using CfgMxfp4PairDrain = GemmCfg<Kind::MXF4, 256, 5, 1, true, 16, 1>;
+using CfgMxfp4PairDrain = GemmCfg<Kind::MXF4, 256, 6, 1, true, 16, 1, OutType::BF16, 16>;
 
 int launch_mxfp4(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const uint8_t* sB, const uint16_t* bias,
                  uint16_t* out, int M, int N, int K, const DeviceInfo& dev, cudaStream_t stream) {

@@ -7,13 +7,14 @@
 
 namespace qk {
 
-// 256 x 256 tiles on a 2-SM CTA pair, five stages, one accumulator drained by
+// 256 x 256 tiles on a 2-SM CTA pair, six stages, one accumulator drained by
 // 16 epilogue warps into registers (64 columns each) and released before the
-// epilogue math.  Measured alternatives, slower and not built: one CTA with
+// epilogue math; the output leaves in 32x16 staging blocks (1 KB each, so the
+// sixth stage fits).  Measured alternatives, slower and not built: one CTA with
 // 128 x 224 tiles and two TMEM accumulators beside the scale ring; the pair
 // with 8 epilogue warps working from TMEM; one CTA with 128 x 256 tiles and
 // one accumulator, whose epilogue stalls the MMAs.
-using CfgMxfp8PairDrain = GemmCfg<Kind::MXF8, 256, 5, 1, true, 16, 1>;
+using CfgMxfp8PairDrain = GemmCfg<Kind::MXF8, 256, 6, 1, true, 16, 1, OutType::BF16, 16>;
 
 // Few rows (M <= 128): the few-row kernels' MXFP8 mode (qk_fewrow_launch.cuh).
 // Against the tile kernel (us): the cluster split-K kernel, when all tiles'

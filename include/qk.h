@@ -279,8 +279,9 @@ const char* qk_status_string(int status);
 /*
  * Reads (and with clear != 0, resets) the current device's status word that
  * kernels set when a bounded wait gives up.  0 means no failure was recorded.
- * Layout: bits 63..56 code (1 = timeout), 55..48 site, 47..32 CTA index,
- * 31..0 detail.  Synchronises the device first.  Returns QK_OK or
+ * Layout: bits 63..56 code (1 = timeout; 2 = a kernel whose shared-memory
+ * layout needs a 1024-byte-aligned base found it unaligned and returned
+ * without doing anything), 55..48 site, 47..32 CTA index, 31..0 detail.  Synchronises the device first.  Returns QK_OK or
  * QK_ERR_CUDA; *word may be NULL.
  */
 int qk_device_status(uint64_t* word, int clear);
