@@ -65,6 +65,18 @@ int launch_streamk_cfg(const uint8_t* A, const uint8_t* B, const FewRowArgs& arg
   p.units = units;
   p.partials = static_cast<float*>(ws);
   p.flags = reinterpret_cast<unsigned long long*>(static_cast<uint8_t*>(ws) + part_bytes);
+  // the epilogue's bulk stores: the output in [OUT_ROWS x 32] boxes, the
+  // partials ([G * MT, 128] fp32) in 32 x 32 boxes
+  CUtensorMap tout, tpart;
+  st = encode_tmap_2d_plain(&tout, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, args.out, N, M,
+                            static_cast<uint64_t>(N) * 2, 32, C::OUT_ROWS);
+  if (st == QK_OK)
+    st = encode_tmap_2d_plain(&tpart, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p.partials, C::NT,
+                              static_cast<uint64_t>(G) * C::MT, C::NT * 4, 32, 32);
+  if (st != QK_OK) {
+    cudaFreeAsync(ws, stream);
+    return st;
+  }
   // a 64-bit value no earlier call used (odd multiplier: a bijection of the counter)
   p.epoch = (g_streamk_epoch.fetch_add(1) + 1) * 0x9E3779B97F4A7C15ull;
   p.err = dev.err_word;
@@ -80,7 +92,7 @@ int launch_streamk_cfg(const uint8_t* A, const uint8_t* B, const FewRowArgs& arg
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   LaunchTimer timer(kernel_kind, stream);
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, tw, ta, p);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, tw, ta, tout, tpart, p);
   timer.done();
   const cudaError_t f = cudaFreeAsync(ws, stream);
   if (e != cudaSuccess || f != cudaSuccess) {

@@ -14,13 +14,18 @@
 //  * A segment that covers a whole tile is finished in place.
 //  * A segment that does not start at K-block 0 can only be the CTA's first;
 //    its fp32 partial goes to a workspace slot of that CTA.  Each epilogue
-//    warp writes its 32 weight rows and then releases its own flag with this
-//    call's epoch, so no barrier across warps is needed.
+//    warp writes its 32 weight rows (bulk tensor stores from shared memory),
+//    waits for those writes to complete and then releases its own flag with
+//    this call's epoch, so no barrier across warps is needed.
 //  * The segment holding K-block 0 owns the tile: each epilogue warp waits
 //    (bounded) for the matching warp flags of the CTAs that carry the rest of
 //    the tile, adds their partials in CTA order (a fixed order, so results
 //    are reproducible) and runs the epilogue (x*sa[m])*sb[n] (+bias[n]) ->
 //    bf16.
+// Every epilogue warp stages what it writes (a partial's 32 x 32 fp32 blocks,
+// the output's 32-column blocks of up to 64 rows) in 4 KB of shared memory
+// and writes it with a bulk tensor store: per-thread stores of one element
+// per row took microseconds at the end of the kernel.
 // A contributor's segment is the first thing it computes and never waits on
 // another CTA, so the waits cannot form a cycle; the launch is cooperative,
 // which guarantees that all CTAs are resident at once.
@@ -71,10 +76,15 @@ struct StreamKCfg {
   static constexpr int OFF_A = OFF_W + STAGES * W_BYTES;
   static constexpr int SF_BYTES = MX ? kFewRowSfBytes : 0;  // per stage: the weight atom, then the activation atom
   static constexpr int OFF_SF = OFF_A + STAGES * A_BYTES;
-  static constexpr int OFF_BAR = OFF_SF + STAGES * SF_BYTES;
+  // per epilogue warp 4 KB: fp32 [32 rows][32 cols] or bf16 [OUT_ROWS][32 cols]
+  static constexpr int STG_BYTES = 4096;
+  static constexpr int OUT_ROWS = MT < 64 ? MT : 64;  // output rows per bulk store
+  static constexpr int OFF_STG = (OFF_SF + STAGES * SF_BYTES + 1023) & ~1023;
+  static constexpr int OFF_BAR = OFF_STG + 4 * STG_BYTES;
   static constexpr int NUM_BARS = 2 * STAGES + 2 * 2 + 1;  // ring, accumulators, drain
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
-  static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
+  static constexpr int OFF_SA = OFF_MISC + 16;  // FP8: the MT per-token scales (fp32)
+  static constexpr int SMEM_BYTES = OFF_SA + MT * 4 + 1024;
   static constexpr int COL_SF = 2 * MT;        // after the two accumulators
   static constexpr int COLS_USED = COL_SF + (MX ? 8 * STAGES : 0);  // 8 scale columns per stage
   static constexpr int TMEM_COLS = COLS_USED <= 64 ? 64 : COLS_USED <= 128 ? 128 : COLS_USED <= 256 ? 256 : 512;
@@ -104,6 +114,7 @@ __device__ __forceinline__ unsigned long long ld_acquire_gpu_u64(const unsigned 
 template <class C>
 __global__ void __launch_bounds__(C::NUM_THREADS, 1)
     qk_streamk_fp8_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmA,
+                          const __grid_constant__ CUtensorMap tmOut, const __grid_constant__ CUtensorMap tmPart,
                           const StreamKParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -138,6 +149,8 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
     fence_mbar_init();
     tma_prefetch_desc(&tmW);
     tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmOut);
+    tma_prefetch_desc(&tmPart);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, C::TMEM_COLS);
@@ -264,6 +277,30 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
     const int q = warp - 4;
     const int r = q * 32 + lane;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16);
+    const uint32_t stg = smem_u32(smem + C::OFF_STG + q * C::STG_BYTES);
+    // the staging block may be rewritten once the previous bulk store has read it
+    auto stg_acquire = [&]() {
+      if (lane == 0) bulk_wait_group_read<0>();
+      __syncwarp();
+    };
+    auto stg_store = [&](const CUtensorMap* map, int x, int y) {
+      fence_proxy_async_smem();  // the block's generic writes before the bulk copy reads it
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_2d(map, stg, x, y);
+        bulk_commit_group();
+      }
+    };
+    // FP8: the per-token scales once, into shared memory, while the first units stream
+    float* sa_s = reinterpret_cast<float*>(smem + C::OFF_SA);
+    if constexpr (!C::MX) {
+      if (r < C::MT) sa_s[r] = r < p.M ? __ldg(p.sa + r) : 0.f;
+      named_barrier_sync(1, 128);  // the four epilogue warps
+    }
+    // With at most 64 rows, the head of a shared tile waits for its
+    // contributors' flags and loads the first partial before its own
+    // accumulator (the registers do not hold two 128-row partials).
+    constexpr bool kEarlyPartial = C::MT <= 64;
     uint32_t seg = 0;
 #pragma unroll 1
     for (long long u = u0; u < u1;) {
@@ -271,6 +308,57 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
       const int kb0 = static_cast<int>(u - static_cast<long long>(t) * p.num_kb);
       const int n_seg = static_cast<int>(min(static_cast<long long>(p.num_kb - kb0), u1 - u));
       const int a = static_cast<int>(seg & 1u);
+      const int n = t * C::NT + r;
+      // this row's column scale and bias, requested before the accumulator
+      float sbn = 1.f, bn = 0.f;
+      if (n < p.N) {
+        if constexpr (!C::MX) sbn = __ldg(p.sb + n);
+        if (p.bias) bn = __uint_as_float(static_cast<uint32_t>(__ldg(p.bias + n)) << 16);
+      }
+      const bool head_of_shared = kb0 == 0 && kb0 + n_seg != p.num_kb;
+      int jend = c + 1;
+      bool peers_ok = true;
+      float pv[C::MT];
+      // the contributors are CTAs c+1 .. jend-1: wait for all their flags at
+      // once (one per lane); contributors publish their first segment and
+      // never wait, so the wait ends
+      auto wait_peers = [&]() {
+        const long long tile_end = static_cast<long long>(t + 1) * p.num_kb;
+        while (jend < G && streamk_begin(p.units, jend, G) < tile_end) ++jend;
+#pragma unroll 1
+        for (int base = c + 1; peers_ok && base < jend; base += 32) {
+          const int j = base + lane;
+          int seen = 1;
+          if (j < jend) {
+            const uint64_t t0 = global_timer_ns();
+            while (ld_acquire_gpu_u64(p.flags + 4 * j + q) != p.epoch) {
+              if (*abort_flag) {
+                seen = 0;
+                break;
+              }
+              if (global_timer_ns() - t0 > p.timeout_ns) {
+                report_error(p.err, kDevErrTimeout, kSitePeerPartial, static_cast<uint32_t>(j));
+                *abort_flag = 1u;
+                seen = 0;
+                break;
+              }
+            }
+          }
+          // each lane's acquire, then the warp barrier, orders every lane's loads after it
+          peers_ok = __all_sync(0xffffffffu, seen != 0);
+        }
+        __syncwarp();
+      };
+      auto load_partial = [&](int j) {
+        const float* src = p.partials + static_cast<size_t>(j) * C::MT * C::NT;
+        // all the partial's loads in flight before the adds
+#pragma unroll
+        for (int m = 0; m < C::MT; ++m) pv[m] = m < p.M ? __ldcg(src + m * C::NT + r) : 0.f;
+      };
+      if (kEarlyPartial && head_of_shared) {
+        wait_peers();
+        if (peers_ok) load_partial(c + 1);
+      }
       // warp-uniform outcome: the TMEM loads below are warp-collective
       const bool got = mbar_wait(&acc_full[a], (seg >> 1) & 1u, w, kSiteEpiAccFull);
       if (!__all_sync(0xffffffffu, got)) break;
@@ -290,79 +378,54 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
 
       if (kb0 != 0) {
         // the tail of a tile owned by an earlier CTA: publish the partial
-        float* dst = p.partials + static_cast<size_t>(c) * C::MT * C::NT;
+        // (workspace rows c*MT .. c*MT+MT-1, this warp's 32 columns)
 #pragma unroll
-        for (int m = 0; m < C::MT; ++m)
-          if (m < p.M) dst[m * C::NT + r] = acc[m];
-        __syncwarp();
+        for (int h = 0; h < C::MT / 32; ++h) {
+          stg_acquire();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) st_shared_f32(stg + static_cast<uint32_t>((i * 32 + lane) * 4), acc[32 * h + i]);
+          stg_store(&tmPart, q * 32, c * C::MT + 32 * h);
+        }
         if (lane == 0) {
+          bulk_wait_group_all();       // the partial's writes are complete
+          fence_proxy_async_global();  // ... and ordered before the flag
           __threadfence();
           st_release_gpu_u64(p.flags + 4 * c + q, p.epoch);
         }
+        __syncwarp();
       } else {
-        if (kb0 + n_seg != p.num_kb) {
-          // the head of a tile whose rest later CTAs carry: add their partials in CTA order
-          const long long tile_end = static_cast<long long>(t + 1) * p.num_kb;
-          // the contributors are CTAs c+1 .. jend-1; wait for all their flags at
-          // once (one per lane), then add the partials in CTA order
-          int jend = c + 1;
-          while (jend < G && streamk_begin(p.units, jend, G) < tile_end) ++jend;
-          bool ok = true;
-#pragma unroll 1
-          for (int base = c + 1; ok && base < jend; base += 32) {
-            const int j = base + lane;
-            int seen = 1;
-            if (j < jend) {
-              const uint64_t t0 = global_timer_ns();
-              while (ld_acquire_gpu_u64(p.flags + 4 * j + q) != p.epoch) {
-                if (*abort_flag) {
-                  seen = 0;
-                  break;
-                }
-                if (global_timer_ns() - t0 > p.timeout_ns) {
-                  report_error(p.err, kDevErrTimeout, kSitePeerPartial, static_cast<uint32_t>(j));
-                  *abort_flag = 1u;
-                  seen = 0;
-                  break;
-                }
-              }
-            }
-            // each lane's acquire, then the warp barrier, orders every lane's loads after it
-            ok = __all_sync(0xffffffffu, seen != 0);
-          }
-          __syncwarp();
-          if (ok) {
+        if (head_of_shared) {
+          if (!kEarlyPartial) wait_peers();
+          if (peers_ok) {
+            // add the contributors' partials in CTA order
 #pragma unroll 1
             for (int j = c + 1; j < jend; ++j) {
-              const float* src = p.partials + static_cast<size_t>(j) * C::MT * C::NT;
-              // all the partial's loads in flight before the adds: interleaved
-              // with the adds they were waited for one by one, which made the
-              // owners' fixup several microseconds long
-              float pv[C::MT];
-#pragma unroll
-              for (int m = 0; m < C::MT; ++m) pv[m] = m < p.M ? __ldcg(src + m * C::NT + r) : 0.f;
+              if (!kEarlyPartial || j > c + 1) load_partial(j);
 #pragma unroll
               for (int m = 0; m < C::MT; ++m)
                 if (m < p.M) acc[m] = __fadd_rn(acc[m], pv[m]);
             }
           }
         }
-        const int n = t * C::NT + r;
-        if (n < p.N) {
-          const float sbn = C::MX ? 1.f : __ldg(p.sb + n);
-          const float bn = p.bias ? __uint_as_float(static_cast<uint32_t>(__ldg(p.bias + n)) << 16) : 0.f;
-          // the row scales of 16 rows loaded ahead of their stores
+        // the output block [rows, this warp's 32 columns] in bulk stores of OUT_ROWS rows
+        if (t * C::NT + q * 32 < p.N) {
 #pragma unroll
-          for (int m = 0; m < C::MT; ++m) {
-            if (m < p.M) {
-              float x = acc[m];
-              if constexpr (!C::MX) {
-                x = __fmul_rn(x, __ldg(p.sa + m));
-                x = __fmul_rn(x, sbn);
+          for (int h = 0; h < C::MT / C::OUT_ROWS; ++h) {
+            if (h * C::OUT_ROWS < p.M) {
+              stg_acquire();
+#pragma unroll
+              for (int i = 0; i < C::OUT_ROWS; ++i) {
+                const int m = h * C::OUT_ROWS + i;
+                float x = acc[m];
+                if constexpr (!C::MX) {
+                  x = __fmul_rn(x, sa_s[m]);
+                  x = __fmul_rn(x, sbn);
+                }
+                if (p.bias) x = __fadd_rn(x, bn);
+                st_shared_u16(stg + static_cast<uint32_t>((i * 32 + lane) * 2),
+                              __bfloat16_as_ushort(__float2bfloat16_rn(x)));
               }
-              if (p.bias) x = __fadd_rn(x, bn);
-              p.out[static_cast<size_t>(m) * static_cast<size_t>(p.N) + n] =
-                  __bfloat16_as_ushort(__float2bfloat16_rn(x));
+              stg_store(&tmOut, t * C::NT + q * 32, h * C::OUT_ROWS);
             }
           }
         }
@@ -370,6 +433,9 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
       ++seg;
       u += n_seg;
     }
+    // no bulk store of this warp still reads shared memory or is in flight
+    if (lane == 0) bulk_wait_group_all();
+    __syncwarp();
   }
 
   tc_fence_before_sync();
