@@ -393,27 +393,58 @@ def _device_bf16(gen, rows, K, std, dev, spike=False):
     return x.to(torch.bfloat16)
 
 
-def _hot_kernel_ms(qk, fn, kname, iters, dev):
-    """Mean kernel time (the library's own events) over back-to-back calls with no L2
-    flush between them: the operands are partly L2-resident."""
+def _b2b_call_ms(call, weights, dev, min_calls=40):
+    """Per-call time of back-to-back calls that rotate through `weights`, copies of the
+    weight operands whose total is over twice the L2: each call finds its weight evicted
+    and streams it from HBM, as successive layers' GEMMs do.  The calls are captured once
+    in a CUDA graph and replayed, so the host's per-call work (argument checks, tensor-map
+    encoding) is not what is timed; CUDA events around one replay.  If capture fails the
+    calls are timed as a plain loop.  Returns (ms per call, whether a graph was used)."""
     import torch
-    for _ in range(3):
-        fn()
+    n = len(weights)
+    calls = max(min_calls, 2 * n)
+    for i in range(n):
+        call(weights[i])
     torch.cuda.synchronize(dev)
-    qk.profile_read(reset=True)
-    qk.profile_enable(True)
-    for _ in range(iters):
-        fn()
-    torch.cuda.synchronize(dev)
-    qk.profile_enable(False)
-    n, ms = qk.profile_read(reset=True).get(kname, (0, 0.0))
-    return ms / n if n else None
+    stream = torch.cuda.current_stream(dev)
+    graph = None
+    try:
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(stream)
+        with torch.cuda.graph(g, stream=side, capture_error_mode="thread_local"):
+            for i in range(calls):
+                call(weights[i % n])
+        g.replay()
+        torch.cuda.synchronize(dev)
+        graph = g
+    except Exception:
+        torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    if graph is not None:
+        graph.replay()
+    else:
+        for i in range(calls):
+            call(weights[i % n])
+    e1.record(stream)
+    e1.synchronize()
+    return e0.elapsed_time(e1) / calls, graph is not None
+
+
+def _weight_copies(weight_bytes, dev):
+    """How many copies of a weight exceed twice the device's L2 (at least 2)."""
+    import torch
+    l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or 132 * 1024 * 1024
+    return max(2, -(-2 * l2 // weight_bytes) + 1)
 
 
 def secondary_formats(qk, dev, peaks, which):
     """Every configuration shape, one line each: the median of 10 calls, each after an L2
-    flush (reading 256 MB), kernel times from the library's own events; few-row shapes also
-    the kernel time over back-to-back calls (hot_kernel_ms).  Operands are drawn on the device with the configurations' distributions
+    flush (reading 256 MB), kernel times from the library's own events; the few-row FP8
+    shapes also the per-call time of back-to-back calls over rotating weight copies larger
+    than twice the L2 (b2b_ms, b2b_frac_of_hbm).  Operands are drawn on the device with the configurations' distributions
     and quantized by the library's quantizers (INT8, NVFP4 and blockscale use the host
     recipe); the parity tests check the same kernels on the host recipe."""
     import numpy as np
@@ -505,9 +536,16 @@ def secondary_formats(qk, dev, peaks, which):
         if "sf_atoms" in kstats:   # the block-scaled kinds' scale-atom pre-pass
             l3, ms3 = kstats["sf_atoms"]
             line["sf_atoms_ms"] = round(ms3 / max(l3, 1), 4)
-        if few:
-            hot = _hot_kernel_ms(qk, fn, kname, 20, dev)
-            line["hot_kernel_ms"] = round(hot, 4) if hot else None
+        if few and kind == "fp8_ptpc":
+            # back to back over rotating weight copies larger than twice the L2
+            ncopy = _weight_copies(B.numel() + 4 * N, dev)
+            wcopies = [(B.clone(), sb.clone()) for _ in range(ncopy)]
+            b2b, graphed = _b2b_call_ms(lambda wt: qk.gemm_fp8_rowwise(A, wt[0], sa, wt[1], None, out),
+                                        wcopies, dev)
+            b2b_gbs = alg_bytes / b2b / 1e6
+            line.update({"b2b_ms": round(b2b, 4), "b2b_weight_copies": ncopy, "b2b_graph": graphed,
+                         "b2b_gbs": round(b2b_gbs, 1), "b2b_frac_of_hbm": round(b2b_gbs / peaks["hbm_gbs"], 4)})
+            del wcopies
         results.append(line)
         del A, B, out
         torch.cuda.empty_cache()

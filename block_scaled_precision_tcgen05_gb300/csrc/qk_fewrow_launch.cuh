@@ -86,11 +86,15 @@ int launch_streamk_cfg(const uint8_t* A, const uint8_t* B, const FewRowArgs& arg
   cfg.blockDim = dim3(C::NUM_THREADS, 1, 1);
   cfg.dynamicSmemBytes = C::SMEM_BYTES;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = 1;
+  // the prologue may overlap the previous kernel of the stream (the kernel
+  // waits for it before touching memory)
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   LaunchTimer timer(kernel_kind, stream);
   const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, tw, ta, tout, tpart, p);
   timer.done();
@@ -118,7 +122,7 @@ int launch_cluster_cfg(const uint8_t* A, const uint8_t* B, const FewRowArgs& arg
   cfg.blockDim = dim3(C::NUM_THREADS, 1, 1);
   cfg.dynamicSmemBytes = C::SMEM_BYTES;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = C::SPLITS;
   attr[0].val.clusterDim.y = 1;
@@ -142,9 +146,18 @@ int launch_cluster_cfg(const uint8_t* A, const uint8_t* B, const FewRowArgs& arg
     *fits = v - 1;
     return QK_OK;
   }
-  CUtensorMap tw, ta;
+  // the prologue may overlap the previous kernel of the stream (the kernel
+  // waits for it before touching memory)
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.numAttrs = 2;
+  CUtensorMap tw, ta, tout;
   int st = encode_tmap_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, K, N, K, C::K_ELEMS, C::NT);
   if (st == QK_OK) st = encode_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, K, M, K, C::K_ELEMS, C::MT);
+  // the output in [OUT_ROWS x 32] boxes (the epilogue warps' staging blocks)
+  if (st == QK_OK)
+    st = encode_tmap_2d_plain(&tout, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, args.out, N, M, static_cast<uint64_t>(N) * 2, 32,
+                              C::OUT_ROWS);
   if (st != QK_OK) return st;
   SkinnyParams p{};
   p.M = M;
@@ -162,7 +175,7 @@ int launch_cluster_cfg(const uint8_t* A, const uint8_t* B, const FewRowArgs& arg
   p.err = dev.err_word;
   p.timeout_ns = wait_timeout_ns();
   LaunchTimer timer(kernel_kind, stream);
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, tw, ta, p);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, tw, ta, tout, p);
   timer.done();
   if (e != cudaSuccess) {
     cudaGetLastError();

@@ -9,11 +9,16 @@
 // cluster barrier every CTA sums, in fixed order over the cluster, the rows
 // m it owns by reading its peers' partials through distributed shared
 // memory, then applies the fixed-order epilogue (x*sa[m])*sb[n] (+bias[n])
-// and writes bf16 rows of the output with coalesced stores.
+// and stages its bf16 output rows in shared memory for bulk tensor stores.
 //
 // MXFP8 mode (MX_ = true): block-scaled MMAs (kind::mxf8f6f4, scale_vec::1X)
 // with the scale staging of qk_fewrow_scales.cuh (a scale warp, 8 TMEM
 // columns per stage after the accumulator), and the epilogue bf16(x (+bias)).
+// The kernel lets the next kernel of the stream launch at once (programmatic
+// dependent launch) and waits for the previous one after its prologue, before
+// its first global-memory access; before that wait it asks L2 for its slice of
+// the weight (a prefetch: L2 is where memory is coherent, so the loads after
+// the wait still see anything the previous kernel writes).
 #pragma once
 
 #include <cuda_bf16.h>
@@ -57,13 +62,17 @@ struct SkinnyCfg {
   static constexpr int OFF_RED = OFF_SF + STAGES * SF_BYTES;  // fp32 partial [MT][NT]
   static constexpr int RED_BYTES = MT * NT * 4;
   static constexpr int OFF_SA = OFF_RED + RED_BYTES;           // fp32 row scales of this CTA's output rows
-  static constexpr int OFF_BAR = OFF_SA + 512;
+  static constexpr int ROWS_PER_CTA = MT / SPLITS;  // output rows each CTA reduces
+  // output staging: per epilogue warp [OUT_ROWS][32] bf16, written by bulk tensor stores
+  static constexpr int OUT_ROWS = ROWS_PER_CTA < 32 ? ROWS_PER_CTA : 32;
+  static constexpr int OFF_STG = OFF_SA + 512;
+  static constexpr int STG_BYTES = 32 * 64;
+  static constexpr int OFF_BAR = OFF_STG + 4 * STG_BYTES;
   static constexpr int OFF_MISC = OFF_BAR + (2 * STAGES + 2) * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
   static constexpr int COL_SF = MT;  // after the accumulator
   static constexpr int COLS_USED = MT + (MX ? 8 * STAGES : 0);
   static constexpr int TMEM_COLS = COLS_USED <= 32 ? 32 : COLS_USED <= 64 ? 64 : COLS_USED <= 128 ? 128 : COLS_USED <= 256 ? 256 : 512;
-  static constexpr int ROWS_PER_CTA = MT / SPLITS;  // output rows each CTA reduces
   static constexpr int NUM_THREADS = 256;
   static_assert(MT % 32 == 0 && MT >= 32 && MT <= 128, "activation tile");
   static_assert(MT % SPLITS == 0, "rows per split");
@@ -83,8 +92,9 @@ __device__ __forceinline__ float ld_shared_cluster_f32(uint32_t cluster_addr) {
 template <class C>
 __global__ void __launch_bounds__(C::NUM_THREADS, 1)
     qk_skinny_fp8_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmA,
-                         const SkinnyParams p) {
+                         const __grid_constant__ CUtensorMap tmOut, const SkinnyParams p) {
   extern __shared__ uint8_t smem_raw[];
+  griddep_launch_dependents();
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* empty = full + C::STAGES;
@@ -115,6 +125,10 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
     fence_mbar_init();
     tma_prefetch_desc(&tmW);
     tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmOut);
+    // this CTA's weight slice into L2 while the previous kernel may still run
+#pragma unroll 1
+    for (int kb = kb0; kb < kb1; ++kb) tma_prefetch_l2_2d(&tmW, kb * C::K_ELEMS, n0);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, C::TMEM_COLS);
@@ -125,6 +139,8 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
   const WaitCtl w{abort_flag, p.err, p.timeout_ns};
+  // the previous kernel of the stream has completed and its writes are visible
+  griddep_wait();
 
   if (warp == 0) {
     if (lane == 0) {
@@ -248,24 +264,28 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
   if constexpr (C::SPLITS > 1) cluster_sync();
 
   if (warp >= 4) {
-    const int t = (warp - 4) * 32 + lane;  // weight row within the tile
+    const int q = warp - 4;
+    const int t = q * 32 + lane;  // weight row within the tile
     const int n = n0 + t;
     const bool col_ok = n < p.N;
     const float sbn = (col_ok && !C::MX) ? __ldg(p.sb + n) : 0.f;
     const float bn = (col_ok && p.bias) ? __uint_as_float(static_cast<uint32_t>(__ldg(p.bias + n)) << 16) : 0.f;
     const uint32_t red_base = smem_u32(red);
+    const uint32_t stg = smem_u32(smem + C::OFF_STG + q * C::STG_BYTES);
+    const int row0 = split * C::ROWS_PER_CTA;  // first output row of this CTA
+    const bool cols_in = n0 + q * 32 < p.N;    // warp-uniform: any of this warp's columns inside N
     // RG rows at a time: all their peers' loads are issued before the first
     // sum (one row at a time, each row waited for its loads in turn; four
     // rows at a time measured 0.5 us slower than sixteen at 64x2112x7168)
     constexpr int RG = C::ROWS_PER_CTA < 16 ? C::ROWS_PER_CTA : 16;
-    static_assert(C::ROWS_PER_CTA % RG == 0, "row groups");
+    static_assert(C::ROWS_PER_CTA % RG == 0 && C::OUT_ROWS % RG == 0, "row groups");
 #pragma unroll 1
     for (int i0 = 0; i0 < C::ROWS_PER_CTA; i0 += RG) {
-      if (split * C::ROWS_PER_CTA + i0 >= p.M) break;
+      if (row0 + i0 >= p.M) break;
       float part[RG][C::SPLITS];
 #pragma unroll
       for (int g = 0; g < RG; ++g) {
-        const int m = split * C::ROWS_PER_CTA + i0 + g;
+        const int m = row0 + i0 + g;
         const uint32_t off = red_base + static_cast<uint32_t>((m * C::NT + t) * 4);
 #pragma unroll
         for (int r = 0; r < C::SPLITS; ++r)
@@ -273,24 +293,40 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                        : C::SPLITS > 1 ? ld_shared_cluster_f32(mapa_shared(off, static_cast<uint32_t>(r)))
                                        : red[m * C::NT + t];
       }
+      float vals[RG];
 #pragma unroll
       for (int g = 0; g < RG; ++g) {
-        const int m = split * C::ROWS_PER_CTA + i0 + g;
-        if (m >= p.M) break;
         float sum = 0.f;
 #pragma unroll
         for (int r = 0; r < C::SPLITS; ++r) sum = __fadd_rn(sum, part[g][r]);  // fixed order over the cluster
-        if (col_ok) {
-          float x = sum;
-          if constexpr (!C::MX) {
-            x = __fmul_rn(x, sa_rows[m - split * C::ROWS_PER_CTA]);
-            x = __fmul_rn(x, sbn);
-          }
-          if (p.bias) x = __fadd_rn(x, bn);
-          p.out[static_cast<size_t>(m) * static_cast<size_t>(p.N) + n] = __bfloat16_as_ushort(__float2bfloat16_rn(x));
+        float x = sum;
+        if constexpr (!C::MX) {
+          x = __fmul_rn(x, sa_rows[i0 + g]);
+          x = __fmul_rn(x, sbn);
+        }
+        if (p.bias) x = __fadd_rn(x, bn);
+        vals[g] = x;
+      }
+      // stage the rows (rows past M and columns past N are clipped by the store)
+      const int srow = i0 % C::OUT_ROWS;
+      if (srow == 0) {
+        if (lane == 0) bulk_wait_group_read<0>();  // the previous store has read the block
+        __syncwarp();
+      }
+#pragma unroll
+      for (int g = 0; g < RG; ++g)
+        st_shared_u16(stg + static_cast<uint32_t>(((srow + g) * 32 + lane) * 2), __bfloat16_as_ushort(__float2bfloat16_rn(vals[g])));
+      if (srow + RG == C::OUT_ROWS || i0 + RG >= C::ROWS_PER_CTA || row0 + i0 + RG >= p.M) {
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0 && cols_in) {
+          tma_store_2d(&tmOut, stg, n0 + q * 32, row0 + i0 - srow);
+          bulk_commit_group();
         }
       }
     }
+    if (lane == 0) bulk_wait_group_all();
+    __syncwarp();
   }
 
   // peers may still read this CTA's partial until everyone is past here

@@ -28,7 +28,14 @@
 // per row took microseconds at the end of the kernel.
 // A contributor's segment is the first thing it computes and never waits on
 // another CTA, so the waits cannot form a cycle; the launch is cooperative,
-// which guarantees that all CTAs are resident at once.
+// which guarantees that all CTAs are resident at once.  Once an owner has
+// added a contributor's partial it sets that flag back to 0, so a call that
+// completes leaves every flag at 0: a replay of a captured graph, which reuses
+// the call's epoch, cannot mistake the previous replay's flags for its own.
+// The kernel lets the next kernel of the stream launch at once (programmatic
+// dependent launch) and waits for the previous one after its prologue,
+// before its first global-memory access other than an L2 prefetch of its
+// first weight tiles.
 //
 // MXFP8 mode (MX_ = true): the MMAs are block-scaled (kind::mxf8f6f4,
 // scale_vec::1X); a scale warp stages each unit's UE8M0 atoms
@@ -117,6 +124,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
                           const __grid_constant__ CUtensorMap tmOut, const __grid_constant__ CUtensorMap tmPart,
                           const StreamKParams p) {
   extern __shared__ uint8_t smem_raw[];
+  griddep_launch_dependents();
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* empty = full + C::STAGES;
@@ -151,6 +159,13 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmOut);
     tma_prefetch_desc(&tmPart);
+    // the first ring's worth of this CTA's weight into L2 before the wait for
+    // the previous kernel (a prefetch: L2 is where memory is coherent)
+#pragma unroll 1
+    for (long long u = u0; u < u1 && u < u0 + C::STAGES; ++u) {
+      const int t = static_cast<int>(u / p.num_kb);
+      tma_prefetch_l2_2d(&tmW, static_cast<int>(u - static_cast<long long>(t) * p.num_kb) * C::K_ELEMS, t * C::NT);
+    }
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, C::TMEM_COLS);
@@ -161,6 +176,8 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
   const WaitCtl w{abort_flag, p.err, p.timeout_ns};
+  // the previous kernel of the stream has completed and its writes are visible
+  griddep_wait();
 
   if (warp == 0) {
     // ---------------- TMA producer: one stage per unit of the range ----------------
@@ -405,26 +422,32 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
               for (int m = 0; m < C::MT; ++m)
                 if (m < p.M) acc[m] = __fadd_rn(acc[m], pv[m]);
             }
+            // the partials are read (their values are in the sums): clear their flags
+            __syncwarp();
+            for (int j = c + 1 + lane; j < jend; j += 32) p.flags[4 * j + q] = 0ull;
           }
         }
         // the output block [rows, this warp's 32 columns] in bulk stores of OUT_ROWS rows
         if (t * C::NT + q * 32 < p.N) {
+          // every row's epilogue first (its scale loads batched), then the staging stores
+#pragma unroll
+          for (int m = 0; m < C::MT; ++m) {
+            float x = acc[m];
+            if constexpr (!C::MX) {
+              x = __fmul_rn(x, sa_s[m]);
+              x = __fmul_rn(x, sbn);
+            }
+            if (p.bias) x = __fadd_rn(x, bn);
+            acc[m] = x;
+          }
 #pragma unroll
           for (int h = 0; h < C::MT / C::OUT_ROWS; ++h) {
             if (h * C::OUT_ROWS < p.M) {
               stg_acquire();
 #pragma unroll
-              for (int i = 0; i < C::OUT_ROWS; ++i) {
-                const int m = h * C::OUT_ROWS + i;
-                float x = acc[m];
-                if constexpr (!C::MX) {
-                  x = __fmul_rn(x, sa_s[m]);
-                  x = __fmul_rn(x, sbn);
-                }
-                if (p.bias) x = __fadd_rn(x, bn);
+              for (int i = 0; i < C::OUT_ROWS; ++i)
                 st_shared_u16(stg + static_cast<uint32_t>((i * 32 + lane) * 2),
-                              __bfloat16_as_ushort(__float2bfloat16_rn(x)));
-              }
+                              __bfloat16_as_ushort(__float2bfloat16_rn(acc[h * C::OUT_ROWS + i])));
               stg_store(&tmOut, t * C::NT + q * 32, h * C::OUT_ROWS);
             }
           }
