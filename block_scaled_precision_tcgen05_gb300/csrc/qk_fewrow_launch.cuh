@@ -1,7 +1,7 @@
 // qk_fewrow_launch.cuh -- host launch of the few-row kernels (M <= 128):
 // the cluster split-K kernel (qk_skinny_kernel.cuh) and the stream-K kernel
-// (qk_streamk_kernel.cuh), each in its FP8 per-token and MXFP8 modes, and
-// the choice between them.
+// (qk_streamk_kernel.cuh), each in its FP8 per-token, MXFP8, MXFP4 and NVFP4
+// modes (MODE 0..3), and the choice between them.
 #pragma once
 #include <atomic>
 
@@ -12,12 +12,15 @@
 namespace qk {
 
 // The operation's operands beyond A and B: per-token / per-channel fp32
-// scales (FP8) or UE8M0 scale rows (MXFP8), bias and output.
+// scales (FP8) or scale rows (UE8M0 for MXFP8 / MXFP4, UE4M3 for NVFP4, with
+// NVFP4's per-tensor scales ga, gb), bias and output.
 struct FewRowArgs {
   const float* sa = nullptr;
   const float* sb = nullptr;
   const uint8_t* sfa = nullptr;
   const uint8_t* sfw = nullptr;
+  const float* ga = nullptr;
+  const float* gb = nullptr;
   const uint16_t* bias = nullptr;
   uint16_t* out = nullptr;
 };
@@ -29,6 +32,13 @@ struct FewRowArgs {
 // reused memory by earlier calls never read as finished.
 extern std::atomic<unsigned long long> g_streamk_epoch;
 
+// Bytes of K per operand row (packed FP4 modes: two elements per byte), and
+// scale bytes per row (NVFP4: one per 16 K, else one per 32 K).
+template <class C>
+inline int fewrow_k_bytes(int K) { return C::FP4 ? K / 2 : K; }
+template <class C>
+inline int fewrow_sf_cols(int K) { return C::MODE == 3 ? K / 16 : K / 32; }
+
 template <class C>
 int launch_streamk_cfg(const uint8_t* A, const uint8_t* B, const FewRowArgs& args, int M, int N, int K,
                        int kernel_kind, const DeviceInfo& dev, cudaStream_t stream) {
@@ -39,9 +49,10 @@ int launch_streamk_cfg(const uint8_t* A, const uint8_t* B, const FewRowArgs& arg
   const int num_kb = ceil_div(K, C::K_ELEMS);
   const long long units = static_cast<long long>(n_tiles) * num_kb;
   const int G = static_cast<int>(units < dev.sm_count ? units : dev.sm_count);
+  const int kbytes = fewrow_k_bytes<C>(K);
   CUtensorMap tw, ta;
-  int st = encode_tmap_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, K, N, K, C::K_ELEMS, C::NT);
-  if (st == QK_OK) st = encode_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, K, M, K, C::K_ELEMS, C::MT);
+  int st = encode_tmap_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, kbytes, N, kbytes, C::KB_BYTES, C::NT);
+  if (st == QK_OK) st = encode_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, kbytes, M, kbytes, C::KB_BYTES, C::MT);
   if (st != QK_OK) return st;
   const size_t part_bytes = static_cast<size_t>(G) * C::MT * C::NT * sizeof(float);
   void* ws = nullptr;
@@ -55,7 +66,9 @@ int launch_streamk_cfg(const uint8_t* A, const uint8_t* B, const FewRowArgs& arg
   p.sb = args.sb;
   p.sfa = args.sfa;
   p.sfw = args.sfw;
-  p.sf_cols = K / 32;
+  p.sf_cols = fewrow_sf_cols<C>(K);
+  p.ga = args.ga;
+  p.gb = args.gb;
   p.bias = args.bias;
   p.out = args.out;
   p.M = M;
@@ -152,8 +165,9 @@ int launch_cluster_cfg(const uint8_t* A, const uint8_t* B, const FewRowArgs& arg
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.numAttrs = 2;
   CUtensorMap tw, ta, tout;
-  int st = encode_tmap_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, K, N, K, C::K_ELEMS, C::NT);
-  if (st == QK_OK) st = encode_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, K, M, K, C::K_ELEMS, C::MT);
+  const int kbytes = fewrow_k_bytes<C>(K);
+  int st = encode_tmap_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, kbytes, N, kbytes, C::KB_BYTES, C::NT);
+  if (st == QK_OK) st = encode_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, kbytes, M, kbytes, C::KB_BYTES, C::MT);
   // the output in [OUT_ROWS x 32] boxes (the epilogue warps' staging blocks)
   if (st == QK_OK)
     st = encode_tmap_2d_plain(&tout, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, args.out, N, M, static_cast<uint64_t>(N) * 2, 32,
@@ -169,7 +183,9 @@ int launch_cluster_cfg(const uint8_t* A, const uint8_t* B, const FewRowArgs& arg
   p.sb = args.sb;
   p.sfa = args.sfa;
   p.sfw = args.sfw;
-  p.sf_cols = K / 32;
+  p.sf_cols = fewrow_sf_cols<C>(K);
+  p.ga = args.ga;
+  p.gb = args.gb;
   p.bias = args.bias;
   p.out = args.out;
   p.err = dev.err_word;
@@ -188,59 +204,95 @@ int launch_cluster_cfg(const uint8_t* A, const uint8_t* B, const FewRowArgs& arg
 // The cluster split-K kernel with the largest S in {8, 4, 2, 1} (S no larger
 // than the K-blocks) whose clusters for all weight tiles fit on the GPU in one
 // wave (one pass, on-chip reduction).  Returns QK_ERR_RANGE without launching
-// when no S fits (*fits_one_wave = false), or when that S is below min_s or
-// leaves a CTA fewer than min_kb K-blocks (*fits_one_wave = true); with
-// `force` S = 1 runs in several waves if nothing fits.
-template <int MT, bool MX>
+// when no S fits (*fits_one_wave = false); with `force` S = 1 runs in several
+// waves if nothing fits.
+template <int MT, int MODE>
 int launch_cluster(const uint8_t* A, const uint8_t* B, const FewRowArgs& args, int M, int N, int K,
-                   int kernel_kind, const DeviceInfo& dev, cudaStream_t stream, bool force, int min_s,
-                   int min_kb, bool* fits_one_wave) {
+                   int kernel_kind, const DeviceInfo& dev, cudaStream_t stream, bool force, bool* fits_one_wave) {
   constexpr int ST = MT <= 64 ? 6 : 4;
   const int n_tiles = ceil_div(N, 128);
-  const int num_kb = ceil_div(K, 128);
+  const int num_kb = ceil_div(MODE >= 2 ? K / 2 : K, 128);  // 128-byte K-blocks
   int chosen = 0;
   for (int S : {8, 4, 2, 1}) {
     if (S > num_kb && S > 1) continue;
     int fits = 0;
-    if (S == 8) launch_cluster_cfg<SkinnyCfg<MT, 8, ST, MX>>(A, B, args, M, N, K, kernel_kind, dev, stream, true, &fits);
-    if (S == 4) launch_cluster_cfg<SkinnyCfg<MT, 4, ST, MX>>(A, B, args, M, N, K, kernel_kind, dev, stream, true, &fits);
-    if (S == 2) launch_cluster_cfg<SkinnyCfg<MT, 2, ST, MX>>(A, B, args, M, N, K, kernel_kind, dev, stream, true, &fits);
-    if (S == 1) launch_cluster_cfg<SkinnyCfg<MT, 1, ST, MX>>(A, B, args, M, N, K, kernel_kind, dev, stream, true, &fits);
+    if (S == 8) launch_cluster_cfg<SkinnyCfg<MT, 8, ST, MODE>>(A, B, args, M, N, K, kernel_kind, dev, stream, true, &fits);
+    if (S == 4) launch_cluster_cfg<SkinnyCfg<MT, 4, ST, MODE>>(A, B, args, M, N, K, kernel_kind, dev, stream, true, &fits);
+    if (S == 2) launch_cluster_cfg<SkinnyCfg<MT, 2, ST, MODE>>(A, B, args, M, N, K, kernel_kind, dev, stream, true, &fits);
+    if (S == 1) launch_cluster_cfg<SkinnyCfg<MT, 1, ST, MODE>>(A, B, args, M, N, K, kernel_kind, dev, stream, true, &fits);
     if (n_tiles <= fits) {
       chosen = S;
       break;
     }
   }
   *fits_one_wave = chosen != 0;
-  if (!force) {
-    if (chosen == 0 || chosen < min_s || ceil_div(num_kb, chosen) < min_kb) return QK_ERR_RANGE;
-  } else if (chosen == 0) {
+  if (chosen == 0) {
+    if (!force) return QK_ERR_RANGE;
     chosen = 1;
   }
   switch (chosen) {  // launch_cluster_cfg never returns QK_ERR_RANGE
     case 8:
-      return launch_cluster_cfg<SkinnyCfg<MT, 8, ST, MX>>(A, B, args, M, N, K, kernel_kind, dev, stream, false, nullptr);
+      return launch_cluster_cfg<SkinnyCfg<MT, 8, ST, MODE>>(A, B, args, M, N, K, kernel_kind, dev, stream, false, nullptr);
     case 4:
-      return launch_cluster_cfg<SkinnyCfg<MT, 4, ST, MX>>(A, B, args, M, N, K, kernel_kind, dev, stream, false, nullptr);
+      return launch_cluster_cfg<SkinnyCfg<MT, 4, ST, MODE>>(A, B, args, M, N, K, kernel_kind, dev, stream, false, nullptr);
     case 2:
-      return launch_cluster_cfg<SkinnyCfg<MT, 2, ST, MX>>(A, B, args, M, N, K, kernel_kind, dev, stream, false, nullptr);
+      return launch_cluster_cfg<SkinnyCfg<MT, 2, ST, MODE>>(A, B, args, M, N, K, kernel_kind, dev, stream, false, nullptr);
     default:
-      return launch_cluster_cfg<SkinnyCfg<MT, 1, ST, MX>>(A, B, args, M, N, K, kernel_kind, dev, stream, false, nullptr);
+      return launch_cluster_cfg<SkinnyCfg<MT, 1, ST, MODE>>(A, B, args, M, N, K, kernel_kind, dev, stream, false, nullptr);
   }
 }
 
-// Measured choice between the few-row kernels and the 2-SM tile kernel (both
-// modes behave alike): a cluster split that fits in one wave wins when each
-// CTA keeps at least kClusterMinKb K-blocks with M <= 64, or the split is at
-// least kClusterMinSplitWide with more rows; shallower splits lose to the
-// tile kernel (64 x 8192 x 1280, 128 x 7168 x 2048).
-constexpr int kClusterMinKb = 6;
-constexpr int kClusterMinSplitWide = 4;
-
-template <int MT, bool MX>
+// Stages: 8 (MT <= 64) or 6; the FP4 modes' larger scale atoms leave room for 6 or 5.
+template <int MT, int MODE>
 int launch_streamk(const uint8_t* A, const uint8_t* B, const FewRowArgs& args, int M, int N, int K, int kernel_kind,
                    const DeviceInfo& dev, cudaStream_t stream) {
-  return launch_streamk_cfg<StreamKCfg<MT, MT <= 64 ? 8 : 6, MX>>(A, B, args, M, N, K, kernel_kind, dev, stream);
+  constexpr int ST = MODE >= 2 ? (MT <= 64 ? 6 : 5) : (MT <= 64 ? 8 : 6);
+  return launch_streamk_cfg<StreamKCfg<MT, ST, MODE>>(A, B, args, M, N, K, kernel_kind, dev, stream);
+}
+
+// The few-row choice of the block-scaled modes, measured on all three
+// (event times in us, tile kernel / few-row kernel): the cluster split-K
+// kernel whenever one wave of clusters covers all weight tiles, whatever the
+// split and the K range per CTA (MXFP8 128x7168x2048 21.5 / 14.4, 64x8192x1280
+// 19.5 / 12.3; MXFP4 64x7168x1024 17.4 / 10.2; NVFP4 96x2112x8192 29.7 /
+// 22.5); otherwise stream-K for MXFP8 and MXFP4 (MXFP8 128x21504x5376 50.2 /
+// 40.0, 8x28672x8192 85.0 / 50.2; MXFP4 64x28672x8192 42.0 / 40.0), and for
+// NVFP4 only with at most 64 rows and 10 to 30 units of 128 weight rows x 128
+// bytes of K per SM (64x21504x5376 35.8 / 31.8; its four scale words per row
+// and unit make longer ranges slower than the tile kernel: 64x28672x8192
+// 48.2 / 56.3); else nothing (*launched = false: the caller runs the tile
+// kernel).  QK_MX_SKINNY (test-only): 1 = never, 2 = stream-K, 3 = cluster
+// split-K, whenever M <= 128.
+template <int MODE>
+int launch_fewrow_block_scaled(const uint8_t* A, const uint8_t* B, const FewRowArgs& args, int M, int N, int K,
+                               int kernel_kind, const DeviceInfo& dev, cudaStream_t stream, bool* launched) {
+  *launched = false;
+  const int skinny = kernel_variant("QK_MX_SKINNY");
+  if (M > 128 || skinny == 1) return QK_OK;
+  *launched = true;
+  const long long units =
+      static_cast<long long>(ceil_div(N, 128)) * ceil_div(MODE >= 2 ? K / 2 : K, 128);
+  if (skinny == 2) {
+    if (M <= 64) return launch_streamk<64, MODE>(A, B, args, M, N, K, kernel_kind, dev, stream);
+    return launch_streamk<128, MODE>(A, B, args, M, N, K, kernel_kind, dev, stream);
+  }
+  bool fits = false;
+  if (skinny == 3) {
+    if (M <= 64) return launch_cluster<64, MODE>(A, B, args, M, N, K, kernel_kind, dev, stream, true, &fits);
+    return launch_cluster<128, MODE>(A, B, args, M, N, K, kernel_kind, dev, stream, true, &fits);
+  }
+  const int st = M <= 64
+                     ? launch_cluster<64, MODE>(A, B, args, M, N, K, kernel_kind, dev, stream, false, &fits)
+                     : launch_cluster<128, MODE>(A, B, args, M, N, K, kernel_kind, dev, stream, false, &fits);
+  if (st != QK_ERR_RANGE) return st;
+  const long long sm = dev.sm_count;
+  const bool streamk = MODE != 3 || (M <= 64 && units >= 10 * sm && units < 30 * sm);
+  if (streamk) {
+    if (M <= 64) return launch_streamk<64, MODE>(A, B, args, M, N, K, kernel_kind, dev, stream);
+    return launch_streamk<128, MODE>(A, B, args, M, N, K, kernel_kind, dev, stream);
+  }
+  *launched = false;
+  return QK_OK;
 }
 
 }  // namespace qk

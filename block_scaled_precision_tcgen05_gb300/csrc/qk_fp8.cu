@@ -54,13 +54,13 @@ static int launch_fp8_cfg(const uint8_t* A, const uint8_t* B, const float* sa, c
 
 // Few rows (M <= 128): if the weight tiles times some split S in {8, 4, 2, 1}
 // fit on the GPU in one wave of clusters, the cluster split-K kernel with the
-// largest such S (one pass, on-chip reduction) when that split is deep
-// enough, else the tile kernel; if no split fits, stream-K, which keeps every
-// SM streaming whatever the tile count (qk_fewrow_launch.cuh).  Cluster
-// against tile kernel (us): 16 x 7168 x 4096 16.9 / 24.7, 128 x 2112 x 7168
-// 19.2 / 31.2, 64 x 8192 x 1280 17.3 / 15.4, 128 x 7168 x 2048 23.3 / 17.5.
-// QK_FP8_SKINNY: 1 = the 2-SM tile kernel, 2 = always stream-K, 3 = always
-// cluster split-K.  Returns QK_ERR_RANGE when the tile kernel should run.
+// largest such S (one pass, on-chip reduction); if no split fits, stream-K,
+// which keeps every SM streaming whatever the tile count
+// (qk_fewrow_launch.cuh).  Tile kernel against cluster (event times, us):
+// 64 x 8192 x 1280 14.3 / 12.3, 128 x 7168 x 2048 16.4 / 14.3, 32 x 4096 x
+// 2048 16.4 / 11.3, 128 x 2112 x 7168 26.6 / 16.4, 16 x 7168 x 4096 20.5 /
+// 16.4.  QK_FP8_SKINNY: 1 = the 2-SM tile kernel, 2 = always stream-K, 3 =
+// always cluster split-K.  Returns QK_ERR_RANGE when the tile kernel should run.
 std::atomic<unsigned long long> g_streamk_epoch{0};
 
 template <int MT>
@@ -74,13 +74,10 @@ static int launch_fewrow_fp8(const uint8_t* A, const uint8_t* B, const float* sa
   args.out = out;
   if (variant != 2) {
     bool fits = false;
-    const int st = launch_cluster<MT, false>(A, B, args, M, N, K, kKGemmFp8, dev, stream, variant == 3,
-                                             MT <= 64 ? 1 : kClusterMinSplitWide, MT <= 64 ? kClusterMinKb : 0,
-                                             &fits);
+    const int st = launch_cluster<MT, 0>(A, B, args, M, N, K, kKGemmFp8, dev, stream, variant == 3, &fits);
     if (st != QK_ERR_RANGE) return st;
-    if (fits) return QK_ERR_RANGE;
   }
-  return launch_streamk<MT, false>(A, B, args, M, N, K, kKGemmFp8, dev, stream);
+  return launch_streamk<MT, 0>(A, B, args, M, N, K, kKGemmFp8, dev, stream);
 }
 
 int launch_fp8_rowwise(const uint8_t* A, const uint8_t* B, const float* sa, const float* sb, const uint16_t* bias,

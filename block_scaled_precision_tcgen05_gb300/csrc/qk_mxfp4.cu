@@ -3,6 +3,7 @@
 // packed 4-bit operands directly (ROCm/FlyDSL PR #990: MXFP4 with per-1x32
 // scales).  Operands are [rows, K/2] bytes, element 2i in the low nibble.
 #include "qk_sf_atoms.cuh"
+#include "qk_fewrow_launch.cuh"
 
 namespace qk {
 
@@ -19,8 +20,18 @@ namespace qk {
 // slower and are not built.
 using CfgMxfp4PairDrain = GemmCfg<Kind::MXF4, 256, 6, 1, true, 16, 1, OutType::BF16, 16>;
 
+// Few rows (M <= 128): the few-row kernels' MXFP4 mode where they are
+// faster (launch_fewrow_block_scaled, qk_fewrow_launch.cuh).
 int launch_mxfp4(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const uint8_t* sB, const uint16_t* bias,
                  uint16_t* out, int M, int N, int K, const DeviceInfo& dev, cudaStream_t stream) {
+  FewRowArgs args;
+  args.sfa = sA;
+  args.sfw = sB;
+  args.bias = bias;
+  args.out = out;
+  bool launched = false;
+  const int st = launch_fewrow_block_scaled<2>(A, B, args, M, N, K, kKGemmMxfp4, dev, stream, &launched);
+  if (launched) return st;
   return launch_block_scaled<CfgMxfp4PairDrain>(A, sA, B, sB, 1, nullptr, nullptr, bias, out, M, N, K, dev, stream);
 }
 

@@ -5,6 +5,7 @@
 // ROCm/aiter PR #6262's gemm_a4w4; the epilogue multiplies the fp32
 // accumulator by their fp32 product before the bias.
 #include "qk_sf_atoms.cuh"
+#include "qk_fewrow_launch.cuh"
 
 namespace qk {
 
@@ -40,5 +41,17 @@ extern "C" int qk_gemm_nvfp4(const uint8_t* A, const uint8_t* sA, const uint8_t*
   if (!dev) return st;
   const auto s = static_cast<cudaStream_t>(stream);
   const int m = static_cast<int>(M), n = static_cast<int>(N), k = static_cast<int>(K);
+  // few rows: the few-row kernels' NVFP4 mode where they are faster
+  // (launch_fewrow_block_scaled, qk_fewrow_launch.cuh)
+  FewRowArgs args;
+  args.sfa = sA;
+  args.sfw = sB;
+  args.ga = ga;
+  args.gb = gb;
+  args.bias = bias;
+  args.out = out;
+  bool launched = false;
+  st = launch_fewrow_block_scaled<3>(A, B, args, m, n, k, kKGemmNvfp4, *dev, s, &launched);
+  if (launched) return st;
   return launch_block_scaled<CfgNvfp4PairDrain>(A, sA, B, sB, 1, ga, gb, bias, out, m, n, k, *dev, s);
 }

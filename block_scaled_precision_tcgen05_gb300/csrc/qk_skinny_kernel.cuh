@@ -11,9 +11,12 @@
 // memory, then applies the fixed-order epilogue (x*sa[m])*sb[n] (+bias[n])
 // and stages its bf16 output rows in shared memory for bulk tensor stores.
 //
-// MXFP8 mode (MX_ = true): block-scaled MMAs (kind::mxf8f6f4, scale_vec::1X)
-// with the scale staging of qk_fewrow_scales.cuh (a scale warp, 8 TMEM
-// columns per stage after the accumulator), and the epilogue bf16(x (+bias)).
+// Block-scaled modes (MODE_ 1 MXFP8, 2 MXFP4, 3 NVFP4): block-scaled MMAs
+// with the scale staging of qk_fewrow_scales.cuh (two scale warps that also
+// copy each stage's atoms into 8 SW TMEM columns after the accumulator),
+// and the epilogue bf16(x (+bias)), NVFP4: bf16(x * (ga * gb) (+bias)).  A
+// stage is 128 bytes of K per row in every mode (128 E4M3 or 256 packed E2M1
+// elements).
 // The kernel lets the next kernel of the stream launch at once (programmatic
 // dependent launch) and waits for the previous one after its prologue, before
 // its first global-memory access; before that wait it asks L2 for its slice of
@@ -38,26 +41,34 @@ struct SkinnyParams {
   const uint8_t* sfa;  // MXFP8: activation UE8M0 scales [M, sf_cols]
   const uint8_t* sfw;  // MXFP8: weight UE8M0 scales [N, sf_cols]
   int sf_cols;         // K / 32
+  const float* ga;     // NVFP4 per-tensor scales (nullable: 1)
+  const float* gb;
   const uint16_t* bias;
   uint16_t* out;
   unsigned long long* err;
   uint64_t timeout_ns;
 };
 
-template <int MT_, int SPLITS_, int STAGES_, bool MX_ = false>
+// MODE_: 0 FP8 per-token x per-channel, 1 MXFP8, 2 MXFP4, 3 NVFP4.
+template <int MT_, int SPLITS_, int STAGES_, int MODE_ = 0>
 struct SkinnyCfg {
-  static constexpr bool MX = MX_;         // MXFP8 block-scaled MMAs
+  static constexpr int MODE = MODE_;
+  static constexpr bool MX = MODE_ != 0;  // block-scaled MMAs
+  static constexpr bool FP4 = MODE_ >= 2;
   static constexpr int MT = MT_;          // padded activation rows (MMA N)
   static constexpr int NT = 128;          // weight rows per tile (MMA M)
   static constexpr int SPLITS = SPLITS_;  // CTAs of a cluster splitting K
   static constexpr int STAGES = STAGES_;
-  static constexpr int K_ELEMS = 128;     // E4M3 elements per stage (one 128-byte swizzle row)
+  static constexpr int KB_BYTES = 128;          // bytes of K per row per stage (one 128-byte swizzle row)
+  static constexpr int K_ELEMS = FP4 ? 256 : 128;  // elements per stage
+  static constexpr int UMMA_K = FP4 ? 64 : 32;     // elements per MMA (32 bytes)
   static constexpr int W_BYTES = NT * 128;
   static constexpr int A_BYTES = MT * 128;
   static constexpr uint32_t STAGE_TX = W_BYTES + A_BYTES;
   static constexpr int OFF_W = 0;
   static constexpr int OFF_A = OFF_W + STAGES * W_BYTES;
-  static constexpr int SF_BYTES = MX ? kFewRowSfBytes : 0;  // per stage: the weight atom, then the activation atom
+  static constexpr int SF_BYTES = MX ? FewRowMx<MX ? MODE_ : 1>::SF_BYTES : 0;  // per stage: weight atoms, then activation atoms
+  static constexpr int SF_COLS_STAGE = MX ? FewRowMx<MX ? MODE_ : 1>::SF_COLS : 0;
   static constexpr int OFF_SF = OFF_A + STAGES * A_BYTES;
   static constexpr int OFF_RED = OFF_SF + STAGES * SF_BYTES;  // fp32 partial [MT][NT]
   static constexpr int RED_BYTES = MT * NT * 4;
@@ -71,7 +82,7 @@ struct SkinnyCfg {
   static constexpr int OFF_MISC = OFF_BAR + (2 * STAGES + 2) * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
   static constexpr int COL_SF = MT;  // after the accumulator
-  static constexpr int COLS_USED = MT + (MX ? 8 * STAGES : 0);
+  static constexpr int COLS_USED = MT + STAGES * SF_COLS_STAGE;
   static constexpr int TMEM_COLS = COLS_USED <= 32 ? 32 : COLS_USED <= 64 ? 64 : COLS_USED <= 128 ? 128 : COLS_USED <= 256 ? 256 : 512;
   static constexpr int NUM_THREADS = 256;
   static_assert(MT % 32 == 0 && MT >= 32 && MT <= 128, "activation tile");
@@ -116,7 +127,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
   if (threadIdx.x == 0) {
 #pragma unroll 1
     for (int s = 0; s < C::STAGES; ++s) {
-      mbar_init(&full[s], C::MX ? 2u : 1u);  // the TMA bytes (+ the scale warp's atoms)
+      mbar_init(&full[s], C::MX ? 3u : 1u);  // the TMA bytes (+ the two scale warps' copies)
       mbar_init(&empty[s], 1u);
     }
     mbar_init(acc_full, 1u);
@@ -128,7 +139,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
     tma_prefetch_desc(&tmOut);
     // this CTA's weight slice into L2 while the previous kernel may still run
 #pragma unroll 1
-    for (int kb = kb0; kb < kb1; ++kb) tma_prefetch_l2_2d(&tmW, kb * C::K_ELEMS, n0);
+    for (int kb = kb0; kb < kb1; ++kb) tma_prefetch_l2_2d(&tmW, kb * C::KB_BYTES, n0);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, C::TMEM_COLS);
@@ -151,8 +162,8 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
       for (int kb = kb0; kb < kb1; ++kb) {
         if (!mbar_wait(&empty[stage], phase ^ 1u, w, kSiteProducerEmpty)) break;
         mbar_arrive_expect_tx(&full[stage], C::STAGE_TX);
-        tma_load_2d(smem + C::OFF_W + stage * C::W_BYTES, &tmW, &full[stage], kb * C::K_ELEMS, n0);
-        tma_load_2d(smem + C::OFF_A + stage * C::A_BYTES, &tmA, &full[stage], kb * C::K_ELEMS, 0);
+        tma_load_2d(smem + C::OFF_W + stage * C::W_BYTES, &tmW, &full[stage], kb * C::KB_BYTES, n0);
+        tma_load_2d(smem + C::OFF_A + stage * C::A_BYTES, &tmA, &full[stage], kb * C::KB_BYTES, 0);
         ++issued;
         if (++stage == C::STAGES) {
           stage = 0;
@@ -189,10 +200,10 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
         const uint64_t wdesc = make_desc_kmajor_sw128(smem_u32(smem + C::OFF_W + stage * C::W_BYTES));
         const uint64_t adesc = make_desc_kmajor_sw128(smem_u32(smem + C::OFF_A + stage * C::A_BYTES));
         int ksteps = 4;
-        if (kb == p.num_kb - 1) ksteps = min(4, (p.K - kb * C::K_ELEMS + 31) / 32);
+        if (kb == p.num_kb - 1) ksteps = min(4, (p.K - kb * C::K_ELEMS + C::UMMA_K - 1) / C::UMMA_K);
         if constexpr (C::MX) {
-          fewrow_mx_mmas(tmem, wdesc, adesc, tmem + static_cast<uint32_t>(C::COL_SF + 8 * stage),
-                         smem_u32(smem + C::OFF_SF + stage * C::SF_BYTES), ksteps, kb > kb0, C::NT, C::MT);
+          fewrow_mx_mmas<C::MODE>(tmem, wdesc, adesc, tmem + static_cast<uint32_t>(C::COL_SF + C::SF_COLS_STAGE * stage),
+                                  ksteps, kb > kb0, C::NT, C::MT);
         } else {
 #pragma unroll
           for (int j = 0; j < 4; ++j)
@@ -218,14 +229,16 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
       }
     }
     __syncwarp();
-  } else if (warp == 2) {
+  } else if (warp == 2 || warp == 3) {
     if constexpr (C::MX) {
+      constexpr int SW = FewRowMx<C::MODE>::SW;
       auto unit = [&](long long i, int& w_row0, int& col) {
         w_row0 = n0;
-        col = (kb0 + static_cast<int>(i)) * 4;
+        col = (kb0 + static_cast<int>(i)) * 4 * SW;
       };
-      fewrow_stage_scales<C::STAGES>(p.sfw, p.sfa, p.N, p.M, p.sf_cols, smem + C::OFF_SF, full, empty,
-                                     kb1 > kb0 ? kb1 - kb0 : 0, unit, lane, w);
+      fewrow_stage_scales<C::STAGES, SW>(p.sfw, p.sfa, p.N, p.M, p.sf_cols, smem + C::OFF_SF,
+                                         tmem + static_cast<uint32_t>(C::COL_SF), full, empty,
+                                         kb1 > kb0 ? kb1 - kb0 : 0, unit, lane, w, warp - 2);
     }
     __syncwarp();
   } else if (warp >= 4) {
@@ -272,6 +285,9 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
     const float bn = (col_ok && p.bias) ? __uint_as_float(static_cast<uint32_t>(__ldg(p.bias + n)) << 16) : 0.f;
     const uint32_t red_base = smem_u32(red);
     const uint32_t stg = smem_u32(smem + C::OFF_STG + q * C::STG_BYTES);
+    // NVFP4: the product of the per-tensor scales, one fp32 rounding
+    [[maybe_unused]] float alpha = 1.f;
+    if constexpr (C::MODE == 3) alpha = __fmul_rn(p.ga ? __ldg(p.ga) : 1.f, p.gb ? __ldg(p.gb) : 1.f);
     const int row0 = split * C::ROWS_PER_CTA;  // first output row of this CTA
     const bool cols_in = n0 + q * 32 < p.N;    // warp-uniform: any of this warp's columns inside N
     // RG rows at a time: all their peers' loads are issued before the first
@@ -304,6 +320,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
           x = __fmul_rn(x, sa_rows[i0 + g]);
           x = __fmul_rn(x, sbn);
         }
+        if constexpr (C::MODE == 3) x = __fmul_rn(x, alpha);
         if (p.bias) x = __fadd_rn(x, bn);
         vals[g] = x;
       }

@@ -37,10 +37,11 @@
 // before its first global-memory access other than an L2 prefetch of its
 // first weight tiles.
 //
-// MXFP8 mode (MX_ = true): the MMAs are block-scaled (kind::mxf8f6f4,
-// scale_vec::1X); a scale warp stages each unit's UE8M0 atoms
-// (qk_fewrow_scales.cuh), the MMA warp copies them into the stage's 8 TMEM
-// columns, and the epilogue is bf16(acc (+bias)) with no per-row scales.
+// Block-scaled modes (MODE_ 1 MXFP8, 2 MXFP4, 3 NVFP4): the MMAs are
+// block-scaled; two scale warps stage each unit's scale atoms and copy them
+// into the stage's TMEM columns (qk_fewrow_scales.cuh), and the epilogue is
+// bf16(acc (+bias)), NVFP4 bf16(acc * (ga * gb) (+bias)), with no per-row
+// scales.  A unit is 128 bytes of K per row in every mode.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -60,6 +61,8 @@ struct StreamKParams {
   const uint8_t* sfa;         // MXFP8: activation UE8M0 scales [M, sf_cols]
   const uint8_t* sfw;         // MXFP8: weight UE8M0 scales [N, sf_cols]
   int sf_cols;                // K / 32
+  const float* ga;            // NVFP4 per-tensor scales (nullable: 1)
+  const float* gb;
   const uint16_t* bias;
   uint16_t* out;
   float* partials;            // [gridDim.x][MT][128] fp32
@@ -69,19 +72,25 @@ struct StreamKParams {
   uint64_t timeout_ns;
 };
 
-template <int MT_, int STAGES_, bool MX_ = false>
+// MODE_: 0 FP8 per-token x per-channel, 1 MXFP8, 2 MXFP4, 3 NVFP4.
+template <int MT_, int STAGES_, int MODE_ = 0>
 struct StreamKCfg {
-  static constexpr bool MX = MX_;         // MXFP8 block-scaled MMAs
+  static constexpr int MODE = MODE_;
+  static constexpr bool MX = MODE_ != 0;  // block-scaled MMAs
+  static constexpr bool FP4 = MODE_ >= 2;
   static constexpr int MT = MT_;          // padded activation rows (MMA N)
   static constexpr int NT = 128;          // weight rows per tile (MMA M)
   static constexpr int STAGES = STAGES_;
-  static constexpr int K_ELEMS = 128;     // E4M3 elements per stage (one 128-byte swizzle row)
+  static constexpr int KB_BYTES = 128;             // bytes of K per row per stage (one 128-byte swizzle row)
+  static constexpr int K_ELEMS = FP4 ? 256 : 128;  // elements per stage
+  static constexpr int UMMA_K = FP4 ? 64 : 32;     // elements per MMA (32 bytes)
   static constexpr int W_BYTES = NT * 128;
   static constexpr int A_BYTES = MT * 128;
   static constexpr uint32_t STAGE_TX = W_BYTES + A_BYTES;
   static constexpr int OFF_W = 0;
   static constexpr int OFF_A = OFF_W + STAGES * W_BYTES;
-  static constexpr int SF_BYTES = MX ? kFewRowSfBytes : 0;  // per stage: the weight atom, then the activation atom
+  static constexpr int SF_BYTES = MX ? FewRowMx<MX ? MODE_ : 1>::SF_BYTES : 0;  // per stage: weight atoms, then activation atoms
+  static constexpr int SF_COLS_STAGE = MX ? FewRowMx<MX ? MODE_ : 1>::SF_COLS : 0;
   static constexpr int OFF_SF = OFF_A + STAGES * A_BYTES;
   // per epilogue warp 4 KB: fp32 [32 rows][32 cols] or bf16 [OUT_ROWS][32 cols]
   static constexpr int STG_BYTES = 4096;
@@ -93,9 +102,9 @@ struct StreamKCfg {
   static constexpr int OFF_SA = OFF_MISC + 16;  // FP8: the MT per-token scales (fp32)
   static constexpr int SMEM_BYTES = OFF_SA + MT * 4 + 1024;
   static constexpr int COL_SF = 2 * MT;        // after the two accumulators
-  static constexpr int COLS_USED = COL_SF + (MX ? 8 * STAGES : 0);  // 8 scale columns per stage
+  static constexpr int COLS_USED = COL_SF + STAGES * SF_COLS_STAGE;
   static constexpr int TMEM_COLS = COLS_USED <= 64 ? 64 : COLS_USED <= 128 ? 128 : COLS_USED <= 256 ? 256 : 512;
-  static constexpr int NUM_THREADS = 256;   // warp 0 TMA, warp 1 MMA, warps 4..7 epilogue
+  static constexpr int NUM_THREADS = 256;   // warp 0 TMA, warp 1 MMA, warps 2-3 scales, 4..7 epilogue
   static_assert(MT == 32 || MT == 64 || MT == 128, "activation tile");
   static_assert(A_BYTES % 1024 == 0, "swizzle atoms need 1024-byte alignment");
   static_assert(SMEM_BYTES <= 232448, "shared-memory budget");
@@ -144,7 +153,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
   if (threadIdx.x == 0) {
 #pragma unroll 1
     for (int s = 0; s < C::STAGES; ++s) {
-      mbar_init(&full[s], C::MX ? 2u : 1u);  // the TMA bytes (+ the scale warp's atoms)
+      mbar_init(&full[s], C::MX ? 3u : 1u);  // the TMA bytes (+ the two scale warps' copies)
       mbar_init(&empty[s], 1u);
     }
 #pragma unroll 1
@@ -164,7 +173,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
 #pragma unroll 1
     for (long long u = u0; u < u1 && u < u0 + C::STAGES; ++u) {
       const int t = static_cast<int>(u / p.num_kb);
-      tma_prefetch_l2_2d(&tmW, static_cast<int>(u - static_cast<long long>(t) * p.num_kb) * C::K_ELEMS, t * C::NT);
+      tma_prefetch_l2_2d(&tmW, static_cast<int>(u - static_cast<long long>(t) * p.num_kb) * C::KB_BYTES, t * C::NT);
     }
   }
   if (warp == 1) {
@@ -191,8 +200,8 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
         const int kb = static_cast<int>(u - static_cast<long long>(t) * p.num_kb);
         if (!mbar_wait(&empty[stage], phase ^ 1u, w, kSiteProducerEmpty)) break;
         mbar_arrive_expect_tx(&full[stage], C::STAGE_TX);
-        tma_load_2d(smem + C::OFF_W + stage * C::W_BYTES, &tmW, &full[stage], kb * C::K_ELEMS, t * C::NT);
-        tma_load_2d(smem + C::OFF_A + stage * C::A_BYTES, &tmA, &full[stage], kb * C::K_ELEMS, 0);
+        tma_load_2d(smem + C::OFF_W + stage * C::W_BYTES, &tmW, &full[stage], kb * C::KB_BYTES, t * C::NT);
+        tma_load_2d(smem + C::OFF_A + stage * C::A_BYTES, &tmA, &full[stage], kb * C::KB_BYTES, 0);
         ++issued;
         if (++stage == C::STAGES) {
           stage = 0;
@@ -242,10 +251,11 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
           const uint64_t wdesc = make_desc_kmajor_sw128(smem_u32(smem + C::OFF_W + stage * C::W_BYTES));
           const uint64_t adesc = make_desc_kmajor_sw128(smem_u32(smem + C::OFF_A + stage * C::A_BYTES));
           int ksteps = 4;
-          if (kb == p.num_kb - 1) ksteps = min(4, (p.K - kb * C::K_ELEMS + 31) / 32);
+          if (kb == p.num_kb - 1) ksteps = min(4, (p.K - kb * C::K_ELEMS + C::UMMA_K - 1) / C::UMMA_K);
           if constexpr (C::MX) {
-            fewrow_mx_mmas(d_tmem, wdesc, adesc, tmem + static_cast<uint32_t>(C::COL_SF + 8 * stage),
-                           smem_u32(smem + C::OFF_SF + stage * C::SF_BYTES), ksteps, i > 0, C::NT, C::MT);
+            fewrow_mx_mmas<C::MODE>(d_tmem, wdesc, adesc,
+                                    tmem + static_cast<uint32_t>(C::COL_SF + C::SF_COLS_STAGE * stage), ksteps, i > 0,
+                                    C::NT, C::MT);
           } else {
 #pragma unroll
             for (int j = 0; j < 4; ++j)
@@ -276,17 +286,18 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
       }
     }
     __syncwarp();
-  } else if (warp == 2) {
-    // ---------------- scale warp (MXFP8): one pair of atoms per unit ----------------
+  } else if (warp == 2 || warp == 3) {
+    // ---------------- scale warps (block-scaled modes): one operand's atoms each per unit ----------------
     if constexpr (C::MX) {
+      constexpr int SW = FewRowMx<C::MODE>::SW;
       auto unit = [&](long long i, int& w_row0, int& col) {
         const long long v = u0 + i;
         const int tv = static_cast<int>(v / p.num_kb);
         w_row0 = tv * C::NT;
-        col = static_cast<int>(v - static_cast<long long>(tv) * p.num_kb) * 4;
+        col = static_cast<int>(v - static_cast<long long>(tv) * p.num_kb) * 4 * SW;
       };
-      fewrow_stage_scales<C::STAGES>(p.sfw, p.sfa, p.N, p.M, p.sf_cols, smem + C::OFF_SF, full, empty, u1 - u0,
-                                     unit, lane, w);
+      fewrow_stage_scales<C::STAGES, SW>(p.sfw, p.sfa, p.N, p.M, p.sf_cols, smem + C::OFF_SF,
+                                         tmem + static_cast<uint32_t>(C::COL_SF), full, empty, u1 - u0, unit, lane, w, warp - 2);
     }
     __syncwarp();
   } else if (warp >= 4) {
@@ -308,6 +319,9 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
         bulk_commit_group();
       }
     };
+    // NVFP4: the product of the per-tensor scales, one fp32 rounding
+    [[maybe_unused]] float alpha = 1.f;
+    if constexpr (C::MODE == 3) alpha = __fmul_rn(p.ga ? __ldg(p.ga) : 1.f, p.gb ? __ldg(p.gb) : 1.f);
     // FP8: the per-token scales once, into shared memory, while the first units stream
     float* sa_s = reinterpret_cast<float*>(smem + C::OFF_SA);
     if constexpr (!C::MX) {
@@ -437,6 +451,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
               x = __fmul_rn(x, sa_s[m]);
               x = __fmul_rn(x, sbn);
             }
+            if constexpr (C::MODE == 3) x = __fmul_rn(x, alpha);
             if (p.bias) x = __fadd_rn(x, bn);
             acc[m] = x;
           }

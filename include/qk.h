@@ -150,12 +150,11 @@ int qk_gemm_int8_rowwise_noalloc(const int8_t* A, const int8_t* B, const float* 
  *   bias bf16 [N] or NULL;  out bf16 [M, N]
  * Requirements: A, B, out, bias 16-byte aligned; sA, sB 4-byte aligned;
  * N % 8 == 0; K % 32 == 0.  Any M >= 1 is accepted without padding.
- * MXFP8 with few rows runs the weight-streaming kernels described under
- * qk_gemm_fp8_rowwise where they are faster: the cluster split-K kernel when
- * all weight tiles' clusters fit on the GPU at once with a long enough K
- * range per CTA; else, for M <= 64 and at least ten 128 x 128 weight units
- * per SM, the cooperative stream-K launch, with the same pooled workspace,
- * the same QK_ERR_NOMEM case and the same reproducible fixed-order reduction.
+ * With M <= 128 both formats run the weight-streaming kernels described
+ * under qk_gemm_fp8_rowwise: the cluster split-K kernel when all weight
+ * tiles' clusters fit on the GPU at once, else the cooperative stream-K
+ * launch, with the same pooled workspace, the same QK_ERR_NOMEM case and the
+ * same reproducible fixed-order reduction.
  */
 int qk_gemm_mx(int fmt, const void* A, const uint8_t* sA, const void* B, const uint8_t* sB,
                const uint16_t* bias, uint16_t* out, int64_t M, int64_t N, int64_t K, qk_stream_t stream);
@@ -193,9 +192,8 @@ int qk_gemm_mx_b32(int fmt, const void* A, const uint8_t* sA, const void* B, con
  *   bias bf16 [N] or NULL; out bf16 [M, N].
  * Requirements: as qk_gemm_int8_rowwise, without the K upper bound.
  * With M <= 128 a weight-streaming kernel runs: split-K over clusters when
- * all weight tiles' clusters fit on the GPU at once and each CTA keeps a deep
- * enough K range (otherwise, in that case, the regular tile kernel), else a
- * cooperative stream-K launch that takes a stream-ordered workspace from the
+ * all weight tiles' clusters fit on the GPU at once, else a cooperative
+ * stream-K launch that takes a stream-ordered workspace from the
  * library's pool (one fp32 partial of at most 128 x 128 values and four
  * 8-byte flags per SM, returned at the end of the call); QK_ERR_NOMEM if that
  * allocation fails.  Partials of a shared tile are added in a fixed order, so
@@ -248,6 +246,10 @@ int qk_gemm_fp8_blockscale(const uint8_t* A, const uint8_t* B, const float* sa, 
  * Requirements: A, B, out, bias 16-byte aligned; N % 8 == 0; K % 32 == 0.
  * Any M >= 1 is accepted without padding.  Device-side reads of ga/gb happen
  * in the kernel, so their values may be produced earlier on the same stream.
+ * With M <= 128 the weight-streaming kernels run where they are faster: the
+ * cluster split-K kernel when all weight tiles' clusters fit on the GPU at
+ * once, the stream-K launch for M <= 64 with 10 to 30 units of 128 weight
+ * rows x 256 K per SM, otherwise the tile kernel.
  */
 int qk_gemm_nvfp4(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const uint8_t* sB, const float* ga,
                   const float* gb, const uint16_t* bias, uint16_t* out, int64_t M, int64_t N, int64_t K,
