@@ -370,15 +370,17 @@ def time_calls(fn, iters, warmup, dev, flush):
 
 # Every configuration's shapes beside the headline: INT8 256x256x512 (the
 # latency configuration) and 30000x21504x5376 with bias, MXFP8 and MXFP4 at
-# their configuration shapes, the 15-point FP8 per-token sweep, and one shape
-# each of the NEXT rows (NVFP4, FP8 blockscale).
+# their configuration shapes, the 15-point FP8 per-token sweep, one shape
+# each of the NEXT rows (NVFP4, FP8 blockscale), and MXFP4 / NVFP4 with 64
+# rows (the few-row kernels' FP4 modes).
 FP8_SWEEP = [(M, N, K) for (N, K) in ((2112, 7168), (7168, 1792), (21504, 5376)) for M in (64, 1024, 4096, 16384, 30000)]
 FORMAT_CASES = ([("int8", (256, 256, 512)), ("int8_bias", (30000, 21504, 5376)),
                  ("mxfp8", (16384, 7168, 2048)), ("mxfp8", (32768, 7168, 1792)), ("mxfp8_b32", (16384, 7168, 2048)),
                  ("mxfp4", (8192, 8192, 8192)), ("mxfp4", (8192, 8192, 16384)), ("mxfp4", (16384, 16384, 8192)),
                  ("mxfp4", (16384, 16384, 16384))]
                 + [("fp8_ptpc", s) for s in FP8_SWEEP]
-                + [("nvfp4", (8192, 8192, 16384)), ("fp8_blockscale", (16384, 7168, 2048))])
+                + [("nvfp4", (8192, 8192, 16384)), ("fp8_blockscale", (16384, 7168, 2048)),
+                   ("mxfp4", (64, 7168, 2048)), ("nvfp4", (64, 7168, 2048))])
 
 
 def _device_bf16(gen, rows, K, std, dev, spike=False):
@@ -442,9 +444,9 @@ def _weight_copies(weight_bytes, dev):
 
 def secondary_formats(qk, dev, peaks, which):
     """Every configuration shape, one line each: the median of 10 calls, each after an L2
-    flush (reading 256 MB), kernel times from the library's own events; the few-row FP8
-    shapes also the per-call time of back-to-back calls over rotating weight copies larger
-    than twice the L2 (b2b_ms, b2b_frac_of_hbm).  Operands are drawn on the device with the configurations' distributions
+    flush (reading 256 MB), kernel times from the library's own events; the few-row shapes
+    (M <= 128) also the per-call time of back-to-back calls over rotating weight copies
+    larger than twice the L2 (b2b_ms, b2b_frac_of_hbm).  Operands are drawn on the device with the configurations' distributions
     and quantized by the library's quantizers (INT8, NVFP4 and blockscale use the host
     recipe); the parity tests check the same kernels on the host recipe."""
     import numpy as np
@@ -460,6 +462,7 @@ def secondary_formats(qk, dev, peaks, which):
     for kind, (M, N, K) in FORMAT_CASES:
         t_gen = time.time()
         kname2 = None
+        weight = call_w = None  # few-row kinds: the weight operands and a call on a copy of them
         if kind in ("mxfp8", "mxfp4", "mxfp8_b32"):
             fp8 = kind != "mxfp4"
             fmt = qi.FMT_MXFP8_E4M3 if fp8 else qi.FMT_MXFP4_E2M1
@@ -472,6 +475,8 @@ def secondary_formats(qk, dev, peaks, which):
                 fn = lambda: qk.gemm_mx_b32(fmt, A, sA, B, sB, None, out)
             else:
                 fn = lambda: qk.gemm_mx(fmt, A, sA, B, sB, None, out)
+                weight = (B, sB)
+                call_w = lambda wt: qk.gemm_mx(fmt, A, sA, wt[0], wt[1], None, out)
             dtype = "fp8" if fp8 else "fp4"
             kname = "gemm_mxfp8" if fp8 else "gemm_mxfp4"
             in_bytes = A.numel() + B.numel() + sA.numel() + sB.numel()
@@ -482,6 +487,8 @@ def secondary_formats(qk, dev, peaks, which):
             B, sb = weights[(N, K)]
             out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
             fn = lambda: qk.gemm_fp8_rowwise(A, B, sa, sb, None, out)
+            weight = (B, sb)
+            call_w = lambda wt: qk.gemm_fp8_rowwise(A, wt[0], sa, wt[1], None, out)
             dtype, kname = "fp8", "gemm_fp8"
             in_bytes = A.numel() + B.numel() + 4 * (M + N)
         elif kind == "nvfp4":
@@ -491,6 +498,8 @@ def secondary_formats(qk, dev, peaks, which):
             gb = _to_dev(np.array([p.global_b], np.float32), dev)
             out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
             fn = lambda: qk.gemm_nvfp4(A, sA, B, sB, ga, gb, None, out)
+            weight = (B, sB)
+            call_w = lambda wt: qk.gemm_nvfp4(A, sA, wt[0], wt[1], ga, gb, None, out)
             dtype, kname = "fp4", "gemm_nvfp4"
             in_bytes = A.numel() + B.numel() + sA.numel() + sB.numel() + 8
         elif kind == "fp8_blockscale":
@@ -536,17 +545,17 @@ def secondary_formats(qk, dev, peaks, which):
         if "sf_atoms" in kstats:   # the block-scaled kinds' scale-atom pre-pass
             l3, ms3 = kstats["sf_atoms"]
             line["sf_atoms_ms"] = round(ms3 / max(l3, 1), 4)
-        if few and kind == "fp8_ptpc":
+        if few and weight is not None:
             # back to back over rotating weight copies larger than twice the L2
-            ncopy = _weight_copies(B.numel() + 4 * N, dev)
-            wcopies = [(B.clone(), sb.clone()) for _ in range(ncopy)]
-            b2b, graphed = _b2b_call_ms(lambda wt: qk.gemm_fp8_rowwise(A, wt[0], sa, wt[1], None, out),
-                                        wcopies, dev)
+            ncopy = _weight_copies(sum(x.numel() * x.element_size() for x in weight), dev)
+            wcopies = [tuple(x.clone() for x in weight) for _ in range(ncopy)]
+            b2b, graphed = _b2b_call_ms(call_w, wcopies, dev)
             b2b_gbs = alg_bytes / b2b / 1e6
             line.update({"b2b_ms": round(b2b, 4), "b2b_weight_copies": ncopy, "b2b_graph": graphed,
                          "b2b_gbs": round(b2b_gbs, 1), "b2b_frac_of_hbm": round(b2b_gbs / peaks["hbm_gbs"], 4)})
             del wcopies
         results.append(line)
+        weight = call_w = None
         del A, B, out
         torch.cuda.empty_cache()
     weights.clear()
