@@ -201,25 +201,57 @@ int launch_cluster_cfg(const uint8_t* A, const uint8_t* B, const FewRowArgs& arg
   return QK_OK;
 }
 
-// The cluster split-K kernel with the largest S in {8, 4, 2, 1} (S no larger
-// than the K-blocks) whose clusters for all weight tiles fit on the GPU in one
-// wave (one pass, on-chip reduction).  Returns QK_ERR_RANGE without launching
-// when no S fits (*fits_one_wave = false); with `force` S = 1 runs in several
-// waves if nothing fits.
+// The cluster split-K kernel with the largest S (8 down to 1 for up to 64
+// activation rows; 8, 4, 2, 1 for 128, whose rows then split evenly; S no
+// larger than the K-blocks) whose clusters for all weight tiles fit on the
+// GPU in one wave (one pass, on-chip reduction): the most SMs streaming.
+// Clusters need not be powers of two: 17 tiles fit as clusters of 6 (102
+// CTAs, three per GPC) where clusters of 8 do not.  Returns QK_ERR_RANGE
+// without launching when no S fits (*fits_one_wave = false); with `force`
+// S = 1 runs in several waves if nothing fits.
+template <int MT, int MODE, int S>
+int launch_cluster_s(const uint8_t* A, const uint8_t* B, const FewRowArgs& args, int M, int N, int K,
+                     int kernel_kind, const DeviceInfo& dev, cudaStream_t stream, bool probe_only, int* fits) {
+  constexpr int ST = MT <= 64 ? 6 : 4;
+  return launch_cluster_cfg<SkinnyCfg<MT, S, ST, MODE>>(A, B, args, M, N, K, kernel_kind, dev, stream, probe_only,
+                                                        fits);
+}
+
+template <int MT, int MODE>
+int launch_cluster_split(int S, const uint8_t* A, const uint8_t* B, const FewRowArgs& args, int M, int N, int K,
+                         int kernel_kind, const DeviceInfo& dev, cudaStream_t stream, bool probe_only, int* fits) {
+  if constexpr (MT <= 64) {
+    switch (S) {
+      case 8: return launch_cluster_s<MT, MODE, 8>(A, B, args, M, N, K, kernel_kind, dev, stream, probe_only, fits);
+      case 7: return launch_cluster_s<MT, MODE, 7>(A, B, args, M, N, K, kernel_kind, dev, stream, probe_only, fits);
+      case 6: return launch_cluster_s<MT, MODE, 6>(A, B, args, M, N, K, kernel_kind, dev, stream, probe_only, fits);
+      case 5: return launch_cluster_s<MT, MODE, 5>(A, B, args, M, N, K, kernel_kind, dev, stream, probe_only, fits);
+      case 4: return launch_cluster_s<MT, MODE, 4>(A, B, args, M, N, K, kernel_kind, dev, stream, probe_only, fits);
+      case 3: return launch_cluster_s<MT, MODE, 3>(A, B, args, M, N, K, kernel_kind, dev, stream, probe_only, fits);
+      case 2: return launch_cluster_s<MT, MODE, 2>(A, B, args, M, N, K, kernel_kind, dev, stream, probe_only, fits);
+      default: return launch_cluster_s<MT, MODE, 1>(A, B, args, M, N, K, kernel_kind, dev, stream, probe_only, fits);
+    }
+  } else {
+    switch (S) {
+      case 8: return launch_cluster_s<MT, MODE, 8>(A, B, args, M, N, K, kernel_kind, dev, stream, probe_only, fits);
+      case 4: return launch_cluster_s<MT, MODE, 4>(A, B, args, M, N, K, kernel_kind, dev, stream, probe_only, fits);
+      case 2: return launch_cluster_s<MT, MODE, 2>(A, B, args, M, N, K, kernel_kind, dev, stream, probe_only, fits);
+      default: return launch_cluster_s<MT, MODE, 1>(A, B, args, M, N, K, kernel_kind, dev, stream, probe_only, fits);
+    }
+  }
+}
+
 template <int MT, int MODE>
 int launch_cluster(const uint8_t* A, const uint8_t* B, const FewRowArgs& args, int M, int N, int K,
                    int kernel_kind, const DeviceInfo& dev, cudaStream_t stream, bool force, bool* fits_one_wave) {
-  constexpr int ST = MT <= 64 ? 6 : 4;
   const int n_tiles = ceil_div(N, 128);
   const int num_kb = ceil_div(MODE >= 2 ? K / 2 : K, 128);  // 128-byte K-blocks
   int chosen = 0;
-  for (int S : {8, 4, 2, 1}) {
+  for (int S = 8; S >= 1; --S) {
+    if (MT > 64 && (S & (S - 1)) != 0) continue;  // 128 rows split evenly
     if (S > num_kb && S > 1) continue;
     int fits = 0;
-    if (S == 8) launch_cluster_cfg<SkinnyCfg<MT, 8, ST, MODE>>(A, B, args, M, N, K, kernel_kind, dev, stream, true, &fits);
-    if (S == 4) launch_cluster_cfg<SkinnyCfg<MT, 4, ST, MODE>>(A, B, args, M, N, K, kernel_kind, dev, stream, true, &fits);
-    if (S == 2) launch_cluster_cfg<SkinnyCfg<MT, 2, ST, MODE>>(A, B, args, M, N, K, kernel_kind, dev, stream, true, &fits);
-    if (S == 1) launch_cluster_cfg<SkinnyCfg<MT, 1, ST, MODE>>(A, B, args, M, N, K, kernel_kind, dev, stream, true, &fits);
+    launch_cluster_split<MT, MODE>(S, A, B, args, M, N, K, kernel_kind, dev, stream, true, &fits);
     if (n_tiles <= fits) {
       chosen = S;
       break;
@@ -230,16 +262,8 @@ int launch_cluster(const uint8_t* A, const uint8_t* B, const FewRowArgs& args, i
     if (!force) return QK_ERR_RANGE;
     chosen = 1;
   }
-  switch (chosen) {  // launch_cluster_cfg never returns QK_ERR_RANGE
-    case 8:
-      return launch_cluster_cfg<SkinnyCfg<MT, 8, ST, MODE>>(A, B, args, M, N, K, kernel_kind, dev, stream, false, nullptr);
-    case 4:
-      return launch_cluster_cfg<SkinnyCfg<MT, 4, ST, MODE>>(A, B, args, M, N, K, kernel_kind, dev, stream, false, nullptr);
-    case 2:
-      return launch_cluster_cfg<SkinnyCfg<MT, 2, ST, MODE>>(A, B, args, M, N, K, kernel_kind, dev, stream, false, nullptr);
-    default:
-      return launch_cluster_cfg<SkinnyCfg<MT, 1, ST, MODE>>(A, B, args, M, N, K, kernel_kind, dev, stream, false, nullptr);
-  }
+  // launch_cluster_cfg never returns QK_ERR_RANGE
+  return launch_cluster_split<MT, MODE>(chosen, A, B, args, M, N, K, kernel_kind, dev, stream, false, nullptr);
 }
 
 // Stages: 8 (MT <= 64) or 6; the FP4 modes' larger scale atoms leave room for 6 or 5.

@@ -4,7 +4,7 @@
 // The product is computed transposed, D^T[n, m] = sum_k B[n,k] A[m,k]: a
 // tile of 128 weight rows is the MMA's M operand (TMEM lanes = n), the M
 // activation rows, padded to MT, are its N operand (TMEM columns = m).  K is
-// split over a cluster of SPLITS CTAs; each CTA accumulates its K range in
+// split over a cluster of SPLITS (1..8) CTAs; each CTA accumulates its K range in
 // TMEM, stages the fp32 partial in shared memory as [m][n], and after a
 // cluster barrier every CTA sums, in fixed order over the cluster, the rows
 // m it owns by reading its peers' partials through distributed shared
@@ -73,7 +73,9 @@ struct SkinnyCfg {
   static constexpr int OFF_RED = OFF_SF + STAGES * SF_BYTES;  // fp32 partial [MT][NT]
   static constexpr int RED_BYTES = MT * NT * 4;
   static constexpr int OFF_SA = OFF_RED + RED_BYTES;           // fp32 row scales of this CTA's output rows
-  static constexpr int ROWS_PER_CTA = MT / SPLITS;  // output rows each CTA reduces
+  // output rows each CTA reduces (the last CTA's range may run past MT: those
+  // rows lie past M, read as zero and are clipped by the output store)
+  static constexpr int ROWS_PER_CTA = (MT + SPLITS - 1) / SPLITS;
   // output staging: per epilogue warp [OUT_ROWS][32] bf16, written by bulk tensor stores
   static constexpr int OUT_ROWS = ROWS_PER_CTA < 32 ? ROWS_PER_CTA : 32;
   static constexpr int OFF_STG = OFF_SA + 512;
@@ -86,7 +88,7 @@ struct SkinnyCfg {
   static constexpr int TMEM_COLS = COLS_USED <= 32 ? 32 : COLS_USED <= 64 ? 64 : COLS_USED <= 128 ? 128 : COLS_USED <= 256 ? 256 : 512;
   static constexpr int NUM_THREADS = 256;
   static_assert(MT % 32 == 0 && MT >= 32 && MT <= 128, "activation tile");
-  static_assert(MT % SPLITS == 0, "rows per split");
+  static_assert(SPLITS >= 1 && SPLITS <= 8, "portable cluster sizes");
   static_assert(SMEM_BYTES <= 232448, "shared-memory budget");
   static constexpr uint32_t IDESC = make_idesc_dense(1, 0, 0, NT, MT);  // fp32 D, E4M3 x E4M3
 };
@@ -293,7 +295,8 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
     // RG rows at a time: all their peers' loads are issued before the first
     // sum (one row at a time, each row waited for its loads in turn; four
     // rows at a time measured 0.5 us slower than sixteen at 64x2112x7168)
-    constexpr int RG = C::ROWS_PER_CTA < 16 ? C::ROWS_PER_CTA : 16;
+    constexpr int RG = C::ROWS_PER_CTA <= 16 ? C::ROWS_PER_CTA
+                       : C::ROWS_PER_CTA % 16 == 0 ? 16 : C::ROWS_PER_CTA / 2;
     static_assert(C::ROWS_PER_CTA % RG == 0 && C::OUT_ROWS % RG == 0, "row groups");
 #pragma unroll 1
     for (int i0 = 0; i0 < C::ROWS_PER_CTA; i0 += RG) {

@@ -6,7 +6,8 @@ few-row kernels, stream-K (QK_MX_SKINNY=2) and cluster split-K
 A ring stage holds 128 bytes of K per row, 256 packed E2M1 elements, with two
 UE8M0 (MXFP4, ROCm/FlyDSL PR #990) or four UE4M3 (NVFP4, ROCm/aiter PR #6262)
 scale words per row.  The shapes cover one tile split over many CTAs (or a
-cluster of 8), tiles shared by two or three CTAs, whole tiles per CTA, a
+cluster of 8), tiles shared by two or three CTAs, clusters of 3 and 6
+(uneven output rows per CTA), whole tiles per CTA, a
 ragged last K-block (K % 256 == 224 or 32: the last MMAs of K = 64 run on
 zero-filled elements, and the scale rows end inside a stage, so the scale
 warp loads bytes into registers; with K % 256 == 0 it copies words by
@@ -29,6 +30,8 @@ SHAPES = [
     (7, 4096, 4096),     # K % 256 == 0: cp.async scale copies
     (65, 1000, 640),     # 128-row activation tile, ragged last weight tile
     (128, 19456, 256),   # whole tiles per CTA
+    (48, 5120, 2048),    # 40 tiles: clusters of 3 (uneven rows per CTA)
+    (64, 3072, 3072),    # 24 tiles: clusters of 6
 ]
 IDS = ["x".join(map(str, s)) for s in SHAPES]
 

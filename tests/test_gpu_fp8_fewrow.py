@@ -28,6 +28,8 @@ SHAPES = [
     (65, 1000, 640),     # 128-row activation tile, ragged last weight tile
     (100, 264, 2048),
     (128, 19456, 256),   # 152 tiles x 2 K-blocks: whole tiles per CTA
+    (48, 5120, 2048),    # 40 tiles: clusters of 3 (22 rows per CTA, the last 4)
+    (64, 3072, 3072),    # 24 tiles: clusters of 6 (11 rows per CTA, the last 9)
 ]
 
 

@@ -26,6 +26,7 @@ SHAPES = [
     (7, 4096, 4096),     # K % 128 == 0: cp.async scale copies
     (65, 1000, 640),     # 128-row activation tile, ragged last weight tile
     (128, 19456, 256),   # whole tiles per CTA
+    (48, 5120, 2048),    # 40 tiles: clusters of 3 (uneven rows per CTA)
 ]
 
 
