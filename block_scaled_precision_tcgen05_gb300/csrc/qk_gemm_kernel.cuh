@@ -23,11 +23,12 @@
 // Scale factors (block-scaled kinds) arrive with the operands: the caller's
 // raw row-major scale bytes are rearranged once per call into 512-byte atoms
 // in the order tcgen05.cp reads (qk_sf_atoms.cuh), and the producer loads each
-// ring stage's atoms by TMA beside its A/B tiles, counted on the same full
-// barrier.  The copy threads move a slot's atoms into the slot's TMEM columns
-// once the slot has landed and the MMAs of its previous round have completed
-// (empty), and commit to sf_ready; the MMA warp waits on full and sf_ready, so
-// it issues nothing but MMAs and its ring commits.
+// ring stage's atoms by TMA just before its A/B tiles, counted on a barrier of
+// their own (sf_full).  The copy threads move a slot's atoms into the slot's
+// TMEM columns once they have landed and the MMAs of the slot's previous round
+// have completed (empty), while the operands are still in flight, and commit
+// to sf_ready; the MMA warp waits on full and sf_ready, so it issues nothing
+// but MMAs and its ring commits.
 //   warps 4..   EPI_WARPS epilogue warps (4 or 16): TMEM -> registers,
 //               fixed-order scale/bias epilogue, output rounding, staged bulk
 //               tensor stores; warp 4 + 4p + q owns TMEM lanes 32q..32q+31
@@ -150,10 +151,12 @@ struct GemmCfg {
 
   static constexpr int A_BYTES = BM * ROW_BYTES;
   static constexpr int B_BYTES = B_ROWS * ROW_BYTES;
-  // bytes a ring stage's full barrier counts: A and B tiles and (block-scaled
-  // kinds) the stage's scale atoms; a pair's leader counts both CTAs' loads
-  static constexpr uint32_t STAGE_TX =
-      PAIR ? 2 * (A_BYTES + B_BYTES + SF_STAGE_BYTES) : A_BYTES + B_BYTES + SF_STAGE_BYTES;
+  // bytes a ring stage's full barrier counts (A and B tiles) and, for the
+  // block-scaled kinds, its sf_full barrier (the stage's scale atoms, loaded
+  // first, so their copies to TMEM overlap the operands' flight); a pair's
+  // leader counts both CTAs' loads
+  static constexpr uint32_t STAGE_TX = PAIR ? 2 * (A_BYTES + B_BYTES) : A_BYTES + B_BYTES;
+  static constexpr uint32_t SF_TX = PAIR ? 2 * SF_STAGE_BYTES : SF_STAGE_BYTES;
 
   static constexpr int OFF_A = 0;
   static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
@@ -170,8 +173,8 @@ struct GemmCfg {
   static constexpr int OFF_OUT = (OFF_SF_END + 1023) & ~1023;
   static constexpr int OFF_BAR = OFF_OUT + EPI_WARPS * OUT_BUFS * OUT_BLOCK_BYTES;
   // ring full/empty, accumulator full/empty, drain, and (block-scaled kinds)
-  // a slot's scales copied to TMEM
-  static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC_BUFS + 1 + (MX ? STAGES : 0);
+  // a slot's scales copied to TMEM and a slot's scale atoms landed
+  static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC_BUFS + 1 + (MX ? 2 * STAGES : 0);
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int SMEM_USED = OFF_MISC + 16;
   // + slack to align the base to 1024 bytes where it fits; a layout without it
@@ -469,15 +472,16 @@ __device__ __forceinline__ void cp_async_wait_group() {
 }
 
 // Scale-factor copies of the MMA-issuing CTA (block-scaled kinds), one of
-// two threads: per ring slot, once the slot has landed (full: both CTAs'
-// tiles and scale atoms in a pair) and the MMAs of the slot's previous round
-// have completed (empty), copy the atoms i with i % 2 == part into the slot's
+// two threads: per ring slot, once the slot's scale atoms have landed
+// (sf_full: both CTAs' atoms in a pair; the producer loads them before the
+// operand tiles) and the MMAs of the slot's previous round have completed
+// (empty), copy the atoms i with i % 2 == part into the slot's
 // TMEM columns and commit to sf_ready, which counts both threads.  Atoms in
 // shared memory: A's SF_ATOMS_K first, then B's 128-row blocks one after the
 // other (each SF_ATOMS_K atoms); in TMEM: A's, then B's grouped by K-group
 // (the NB128 row blocks of a K-group side by side, as the MMA reads them).
 template <class C>
-__device__ __forceinline__ void scale_copier(const GemmParams& p, uint8_t* smem, uint32_t tmem, uint64_t* full,
+__device__ __forceinline__ void scale_copier(const GemmParams& p, uint8_t* smem, uint32_t tmem, uint64_t* sf_full,
                                              uint64_t* sf_ready, uint64_t* empty, const WaitCtl& w, int tile0,
                                              int tile_step, int part) {
   int stage = 0;
@@ -488,7 +492,7 @@ __device__ __forceinline__ void scale_copier(const GemmParams& p, uint8_t* smem,
   for (int t = tile0; ok && t < p.num_tiles; t += tile_step) {
 #pragma unroll 1
     for (int kb = 0; kb < p.num_kb; ++kb) {
-      bool ready = mbar_wait(&full[stage], phase, w, kSiteScaleCopy);
+      bool ready = mbar_wait(&sf_full[stage], phase, w, kSiteScaleCopy);
       // the slot's TMEM scales of the previous round have been read by their MMAs
       ready = ready && mbar_wait(&empty[stage], phase ^ 1u, w, kSiteScaleCopy);
       if (!ready) {
@@ -563,6 +567,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
   uint64_t* acc_empty = acc_full + C::ACC_BUFS;
   uint64_t* drain = acc_empty + C::ACC_BUFS;
   uint64_t* sf_ready = drain + 1;  // block-scaled kinds: a slot's scales copied to TMEM
+  uint64_t* sf_full = sf_ready + C::STAGES;  // block-scaled kinds: a slot's scale atoms landed
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_MISC + 4);
 
@@ -580,7 +585,10 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(&full[s], C::FULL_ARRIVALS);
       mbar_init(&empty[s], 1u);
-      if constexpr (C::MX) mbar_init(&sf_ready[s], C::SF_COPIERS);
+      if constexpr (C::MX) {
+        mbar_init(&sf_ready[s], C::SF_COPIERS);
+        mbar_init(&sf_full[s], 1u);
+      }
     }
 #pragma unroll 1
     for (int a = 0; a < C::ACC_BUFS; ++a) {
@@ -629,6 +637,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
       bool ok = true;
       // in a pair, both CTAs' loads complete on the leader's ring barriers
       const uint32_t full_leader = C::PAIR ? mapa_shared(smem_u32(&full[0]), 0u) : 0u;
+      [[maybe_unused]] const uint32_t sf_full_leader = C::MX && C::PAIR ? mapa_shared(smem_u32(&sf_full[0]), 0u) : 0u;
 #pragma unroll 1
       for (int t = tile0; ok && t < p.num_tiles; t += tile_step) {
         int mb, nb;
@@ -641,6 +650,30 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
             ok = false;
             break;
           }
+          if constexpr (C::MX) {
+            // the stage's scale atoms first, on their own barrier: A's 128-row
+            // block, then each 128-row block of the B tile; atom maps are
+            // [blocks * gpad * 2, 256 bytes], a box being SF_ATOMS_K
+            // consecutive atoms of one block
+            uint8_t* sf = smem + C::OFF_SF + stage * C::SF_STAGE_BYTES;
+            const int ya = ((a_row / 128) * p.sf_gpad + kb * C::SF_ATOMS_K) * 2;
+            if constexpr (C::PAIR) {
+              if (leader) mbar_arrive_expect_tx(&sf_full[stage], C::SF_TX);
+              const uint32_t fb = sf_full_leader + 8u * static_cast<uint32_t>(stage);
+              tma_load_2d_pair(sf, &tmSA, fb, 0, ya);
+#pragma unroll
+              for (int rb = 0; rb < C::NB128; ++rb)
+                tma_load_2d_pair(sf + C::SFA_BYTES + rb * C::SF_ATOMS_K * 512, &tmSB, fb, 0,
+                                 ((nb * C::NB128 + rb) * p.sf_gpad + kb * C::SF_ATOMS_K) * 2);
+            } else {
+              mbar_arrive_expect_tx(&sf_full[stage], C::SF_TX);
+              tma_load_2d(sf, &tmSA, &sf_full[stage], 0, ya);
+#pragma unroll
+              for (int rb = 0; rb < C::NB128; ++rb)
+                tma_load_2d(sf + C::SFA_BYTES + rb * C::SF_ATOMS_K * 512, &tmSB, &sf_full[stage], 0,
+                            ((nb * C::NB128 + rb) * p.sf_gpad + kb * C::SF_ATOMS_K) * 2);
+            }
+          }
           if constexpr (C::PAIR) {
             if (leader) mbar_arrive_expect_tx(&full[stage], C::STAGE_TX);
             const uint32_t fb = full_leader + 8u * static_cast<uint32_t>(stage);
@@ -650,27 +683,6 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
             mbar_arrive_expect_tx(&full[stage], C::STAGE_TX);
             tma_load_2d(smem + C::OFF_A + stage * C::A_BYTES, &tmA, &full[stage], kb * C::TMA_K, a_row);
             tma_load_2d(smem + C::OFF_B + stage * C::B_BYTES, &tmB, &full[stage], kb * C::TMA_K, b_row);
-          }
-          if constexpr (C::MX) {
-            // the stage's scale atoms: A's 128-row block, then each 128-row block
-            // of the B tile; atom maps are [blocks * gpad * 2, 256 bytes], a box
-            // being SF_ATOMS_K consecutive atoms of one block
-            uint8_t* sf = smem + C::OFF_SF + stage * C::SF_STAGE_BYTES;
-            const int ya = ((a_row / 128) * p.sf_gpad + kb * C::SF_ATOMS_K) * 2;
-            if constexpr (C::PAIR) {
-              const uint32_t fb = full_leader + 8u * static_cast<uint32_t>(stage);
-              tma_load_2d_pair(sf, &tmSA, fb, 0, ya);
-#pragma unroll
-              for (int rb = 0; rb < C::NB128; ++rb)
-                tma_load_2d_pair(sf + C::SFA_BYTES + rb * C::SF_ATOMS_K * 512, &tmSB, fb, 0,
-                                 ((nb * C::NB128 + rb) * p.sf_gpad + kb * C::SF_ATOMS_K) * 2);
-            } else {
-              tma_load_2d(sf, &tmSA, &full[stage], 0, ya);
-#pragma unroll
-              for (int rb = 0; rb < C::NB128; ++rb)
-                tma_load_2d(sf + C::SFA_BYTES + rb * C::SF_ATOMS_K * 512, &tmSB, &full[stage], 0,
-                            ((nb * C::NB128 + rb) * p.sf_gpad + kb * C::SF_ATOMS_K) * 2);
-            }
           }
           ++issued;
           if (++stage == C::STAGES) {
@@ -688,14 +700,17 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
 #pragma unroll 1
       for (long long i = 0; i < drain_n; ++i) {
         const long long L = issued - 1 - i;
-        uint64_t* bar = &full[static_cast<int>(L % C::STAGES)];
         const uint32_t par = static_cast<uint32_t>((L / C::STAGES) & 1);
-        const uint32_t a = smem_u32(bar);
-        const uint64_t t0 = global_timer_ns();
-        while (!mbar_try_wait(a, par)) {
-          if (global_timer_ns() - t0 > wd.timeout_ns) {
-            report_error(p.err, kDevErrTimeout, kSiteProducerDrain, static_cast<uint32_t>(L));
-            break;
+#pragma unroll
+        for (int which = 0; which < (C::MX ? 2 : 1); ++which) {
+          uint64_t* bar = which == 0 ? &full[static_cast<int>(L % C::STAGES)] : &sf_full[static_cast<int>(L % C::STAGES)];
+          const uint32_t a = smem_u32(bar);
+          const uint64_t t0 = global_timer_ns();
+          while (!mbar_try_wait(a, par)) {
+            if (global_timer_ns() - t0 > wd.timeout_ns) {
+              report_error(p.err, kDevErrTimeout, kSiteProducerDrain, static_cast<uint32_t>(L));
+              break;
+            }
           }
         }
       }
@@ -846,7 +861,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
   } else if (warp == 2 || warp == 3) {
     // ---------------- scale-factor copies (block-scaled kinds, the MMA-issuing CTA) ----------------
     if constexpr (C::MX) {
-      if (issues_mma && lane == 0) scale_copier<C>(p, smem, tmem, full, sf_ready, empty, w, tile0, tile_step, warp - 2);
+      if (issues_mma && lane == 0) scale_copier<C>(p, smem, tmem, sf_full, sf_ready, empty, w, tile0, tile_step, warp - 2);
     }
     __syncwarp();
   } else if (warp >= 4) {
