@@ -14,8 +14,15 @@ namespace qk {
 // 128 x 256 tiles on one CTA, two 256-column accumulators, 16 epilogue warps
 // with 64 columns each.  Measured alternatives, not built: 256 x 256 tiles on
 // a CTA pair (the peer's MMA warp relays each accumulator release to the
-// leader), within 2% of this one; pair tiles of 256 x 128 with four
-// 128-column accumulators, slower.
+// leader; 32 instead of 48 KB of operands per SM and chunk), 1651-1665
+// against 1737 TFLOP/s at 16384 x 7168 x 2048 with 4 or 6 stages, and 1643
+// with the peer's warps releasing straight on the leader's barrier; pair
+// tiles of 256 x 128 with four 128-column accumulators, slower.  A cycle
+// probe of the MMA thread puts this kernel's limit in the tensor pipe: each
+// single-CTA 128 x 256 x 32 MMA takes ~281 cycles to issue (~1124 per
+// 128-K block), about half the per-SM rate of the pair form (~158 cycles
+// per 256 x 256 x 32 pair MMA), while the pair form is limited by its
+// accumulator turnover every 128 K.
 using CfgFp8BlockscaleSingle = GemmCfg<Kind::F8BS, 256, 4, 2, false, 16, 1>;
 
 template <class C>
