@@ -18,11 +18,12 @@ namespace qk {
 // against 1737 TFLOP/s at 16384 x 7168 x 2048 with 4 or 6 stages, and 1643
 // with the peer's warps releasing straight on the leader's barrier; pair
 // tiles of 256 x 128 with four 128-column accumulators, slower.  A cycle
-// probe of the MMA thread puts this kernel's limit in the tensor pipe: each
-// single-CTA 128 x 256 x 32 MMA takes ~281 cycles to issue (~1124 per
-// 128-K block), about half the per-SM rate of the pair form (~158 cycles
-// per 256 x 256 x 32 pair MMA), while the pair form is limited by its
-// accumulator turnover every 128 K.
+// probe of the MMA thread puts this kernel's limit in the tensor pipe: with
+// the epilogue draining the other accumulator meanwhile, each 128 x 256 x 32
+// MMA takes ~281 cycles to issue (~1124 per 128-K block), about half the
+// per-SM rate the pair MMAs reach without a drain beside them (~158 cycles
+// per 256 x 256 x 32 pair MMA in the FP8 per-token kernel); the pair form
+// here is limited by its accumulator turnover every 128 K.
 using CfgFp8BlockscaleSingle = GemmCfg<Kind::F8BS, 256, 4, 2, false, 16, 1>;
 
 template <class C>
