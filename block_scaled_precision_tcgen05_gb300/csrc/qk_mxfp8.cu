@@ -1,7 +1,9 @@
 // qk_mxfp8.cu -- MXFP8 (E4M3 elements, one UE8M0 scale per 32 K) GEMM on
 // tcgen05.mma kind::mxf8f6f4.block_scale.scale_vec::1X.  The raw row-major
-// [rows, K/32] scale bytes (ROCm/mori PR #806, "What") are staged per ring
-// slot by the kernel's scale warp and moved to TMEM with tcgen05.cp.
+// [rows, K/32] scale bytes (ROCm/mori PR #806, "What") are rearranged once per
+// call into the atoms tcgen05.cp reads (qk_sf_atoms.cuh), loaded by TMA with
+// each ring stage and moved to TMEM by two copy warps; with few rows the
+// few-row kernels' scale warps stage them on chip (qk_fewrow_scales.cuh).
 #include "qk_sf_atoms.cuh"
 #include "qk_fewrow_launch.cuh"
 

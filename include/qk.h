@@ -175,9 +175,10 @@ int qk_gemm_mx(int fmt, const void* A, const uint8_t* sA, const void* B, const u
  *                                      the last group may hold fewer rows)
  *   bias  bf16 [N] or NULL;  out bf16 [M, N]
  * Requirements and errors as for qk_gemm_mx.  Every M runs the 2-SM tile
- * kernel (no few-row mode in this form); on chip the scale warp writes each
- * 32-row group's scale bytes into the places of its 32 rows, so the form
- * reads 32x fewer B scale bytes and no expanded copy exists in HBM.
+ * kernel (no few-row mode in this form); the per-call scale pre-pass writes
+ * each 32-row group's scale bytes into the places of its 32 rows in the
+ * atom buffer, so the form reads 32x fewer B scale bytes from the caller and
+ * the GEMM kernel is the same as qk_gemm_mx's.
  */
 int qk_gemm_mx_b32(int fmt, const void* A, const uint8_t* sA, const void* B, const uint8_t* sB32,
                    const uint16_t* bias, uint16_t* out, int64_t M, int64_t N, int64_t K, qk_stream_t stream);

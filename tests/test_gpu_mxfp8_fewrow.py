@@ -6,8 +6,8 @@ few-row kernels, stream-K (QK_MX_SKINNY=2) and cluster split-K
 The shapes cover one tile split over many CTAs (or over a cluster of 8),
 tiles shared by two or three CTAs, whole tiles per CTA, a ragged last
 K-block (K % 128 == 32 or 96), where the scale rows' length K/32 is not a
-multiple of 4 and the scale warp loads bytes into registers (with K % 128 ==
-0 it copies 4-byte words by cp.async), a ragged last weight tile and both
+multiple of 4 and the scale warps load bytes into registers (with K % 128 ==
+0 they copy 4-byte words by cp.async), a ragged last weight tile and both
 activation tile heights (64 and 128 rows)."""
 import numpy as np
 import pytest
