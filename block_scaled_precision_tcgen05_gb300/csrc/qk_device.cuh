@@ -241,15 +241,6 @@ __device__ __forceinline__ void bulk_wait_group_read() {
 // Waits until all bulk groups of this thread have completed.
 __device__ __forceinline__ void bulk_wait_group_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
-// Prefetches a tile of a 2-D tensor into L2 (no shared memory, no barrier).
-// L2 is where the GPU's memory is coherent, so a later load of the same
-// addresses still sees any write made after the prefetch.
-__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int32_t c0, int32_t c1) {
-  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(reinterpret_cast<uint64_t>(map)),
-               "r"(c0), "r"(c1)
-               : "memory");
-}
-
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }

@@ -19,9 +19,9 @@
 // elements).
 // The kernel lets the next kernel of the stream launch at once (programmatic
 // dependent launch) and waits for the previous one after its prologue, before
-// its first global-memory access; before that wait it asks L2 for its slice of
-// the weight (a prefetch: L2 is where memory is coherent, so the loads after
-// the wait still see anything the previous kernel writes).
+// its first global-memory access.  (An L2 prefetch of the CTA's weight slice
+// before that wait measured no faster back to back and 2 us slower for one
+// call: its requests competed with the loads.)
 #pragma once
 
 #include <cuda_bf16.h>
@@ -139,9 +139,6 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
     tma_prefetch_desc(&tmW);
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmOut);
-    // this CTA's weight slice into L2 while the previous kernel may still run
-#pragma unroll 1
-    for (int kb = kb0; kb < kb1; ++kb) tma_prefetch_l2_2d(&tmW, kb * C::KB_BYTES, n0);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, C::TMEM_COLS);

@@ -33,9 +33,11 @@
 // completes leaves every flag at 0: a replay of a captured graph, which reuses
 // the call's epoch, cannot mistake the previous replay's flags for its own.
 // The kernel lets the next kernel of the stream launch at once (programmatic
-// dependent launch) and waits for the previous one after its prologue,
-// before its first global-memory access other than an L2 prefetch of its
-// first weight tiles.
+// dependent launch) and waits for the previous one after its prologue, before
+// its first global-memory access.  (An L2 prefetch of the first weight tiles
+// before that wait measured slower: the cooperative launch starts no CTA
+// before the previous kernel's CTAs have all left, so it only lengthened the
+// prologue.)
 //
 // Block-scaled modes (MODE_ 1 MXFP8, 2 MXFP4, 3 NVFP4): the MMAs are
 // block-scaled; two scale warps stage each unit's scale atoms and copy them
@@ -168,13 +170,6 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmOut);
     tma_prefetch_desc(&tmPart);
-    // the first ring's worth of this CTA's weight into L2 before the wait for
-    // the previous kernel (a prefetch: L2 is where memory is coherent)
-#pragma unroll 1
-    for (long long u = u0; u < u1 && u < u0 + C::STAGES; ++u) {
-      const int t = static_cast<int>(u / p.num_kb);
-      tma_prefetch_l2_2d(&tmW, static_cast<int>(u - static_cast<long long>(t) * p.num_kb) * C::KB_BYTES, t * C::NT);
-    }
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, C::TMEM_COLS);

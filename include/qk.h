@@ -200,9 +200,9 @@ int qk_gemm_mx_b32(int fmt, const void* A, const uint8_t* sA, const void* B, con
  * allocation fails.  Partials of a shared tile are added in a fixed order, so
  * repeated calls give identical bits.  The few-row kernels may start while
  * the previous kernel of the stream finishes (programmatic dependent launch;
- * they touch memory only after it has completed, apart from L2 prefetches of
- * the weight), and a call may be captured in a CUDA graph and replayed (the
- * stream-K flags are cleared by the time a call completes).
+ * they touch memory only after it has completed), and a call may be captured
+ * in a CUDA graph and replayed (the stream-K flags are cleared by the time a
+ * call completes).
  */
 int qk_gemm_fp8_rowwise(const uint8_t* A, const uint8_t* B, const float* sa, const float* sb,
                         const uint16_t* bias, uint16_t* out, int64_t M, int64_t N, int64_t K,
