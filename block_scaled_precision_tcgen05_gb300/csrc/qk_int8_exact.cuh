@@ -27,7 +27,7 @@ using CfgInt8 = GemmCfg<Kind::F16, 256, 6, 2, true, 16, 1>;
 using CfgInt8F16 = GemmCfg<Kind::F16, 256, 6, 2, true, 16, 1, OutType::F16>;
 using CfgInt8F32 = GemmCfg<Kind::F16, 256, 5, 2, true, 16, 1, OutType::F32>;
 
-// Widens 16 int8 values per thread-iteration to f16.  Byte x becomes the f16
+// Widens 16 int8 values per thread to f16.  Byte x becomes the f16
 // bit pattern 0x6400 | (x + 128), i.e. the value 1024 + x + 128, and one
 // exact subtraction of 1152 leaves x.
 __device__ __forceinline__ uint4 widen8(uint32_t w, uint32_t w2) {
@@ -72,9 +72,13 @@ static inline int widen_and_gemm_int8(const int8_t* A, const int8_t* B, const fl
   const size_t a_elems = static_cast<size_t>(M) * K;
   const size_t b_elems = static_cast<size_t>(N) * K;
   const long long na = static_cast<long long>(a_elems / 16), nb = static_cast<long long>(b_elems / 16);
+  // one 16-byte element per thread and a block per 256 of them, hundreds of
+  // waves of short blocks: at 30000 + 21504 rows x 5376 this moves 6.78 TB/s
+  // (the measured copy rate), where a grid-stride loop over one wave of 8
+  // blocks per SM moved 4.9 (more loads in flight per SM did not help: 4.5 to
+  // 5.6 TB/s for 2 to 8 elements per thread)
   long long blocks = (na + nb + 255) / 256;
-  const long long cap = static_cast<long long>(dev.sm_count) * 8;
-  if (blocks > cap) blocks = cap;
+  if (blocks > 0x7fffffffLL) blocks = 0x7fffffffLL;  // the loop covers any rest
   LaunchTimer timer(kKInt8ToF16, stream);
   qk_int8_to_f16_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(
       reinterpret_cast<const uint4*>(A), reinterpret_cast<uint4*>(a16), na, reinterpret_cast<const uint4*>(B),
