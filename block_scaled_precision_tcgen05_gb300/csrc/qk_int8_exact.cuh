@@ -75,8 +75,8 @@ static inline int widen_and_gemm_int8(const int8_t* A, const int8_t* B, const fl
   // one 16-byte element per thread and a block per 256 of them, hundreds of
   // waves of short blocks: at 30000 + 21504 rows x 5376 this moves 6.78 TB/s
   // (the measured copy rate), where a grid-stride loop over one wave of 8
-  // blocks per SM moved 4.9 (more loads in flight per SM did not help: 4.5 to
-  // 5.6 TB/s for 2 to 8 elements per thread)
+  // blocks per SM moved 4.9 (2 to 8 elements in flight per thread: 4.5 to 6.1
+  // TB/s, the rate rising and falling with the grid size)
   long long blocks = (na + nb + 255) / 256;
   if (blocks > 0x7fffffffLL) blocks = 0x7fffffffLL;  // the loop covers any rest
   LaunchTimer timer(kKInt8ToF16, stream);
