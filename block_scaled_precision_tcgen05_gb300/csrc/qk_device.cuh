@@ -33,6 +33,7 @@ enum : uint32_t {
   kSiteMmaScales = 10,    // MMA warp: a ring slot's scale factors copied to TMEM
   kSiteScaleCopy = 11,    // scale-copy thread: a ring slot's scale atoms written
   kSiteSmemBase = 12,     // kernel entry: the dynamic shared-memory base
+  kSiteSplitArrive = 13,  // tail split: a K-part's arrival word kept changing
 };
 
 __device__ __forceinline__ void report_error(unsigned long long* err, uint32_t code, uint32_t site,

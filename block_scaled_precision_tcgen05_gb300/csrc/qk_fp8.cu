@@ -22,16 +22,27 @@ using CfgFp8Drain = GemmCfg<Kind::F8, 256, 6, 2, true, 16, 1>;
 // tiles of CfgFp8, for problems whose 256 x 256 tiles leave pairs idle.
 using CfgFp8Narrow = GemmCfg<Kind::F8, 128, 8, 2, true, 8, 1>;
 
-// Whether 256 x 128 pair tiles finish sooner than 256 x 256 ones: waves of
-// tiles over the SM pairs, a narrow tile's k-block costing about 3/4 of a wide
-// one's per SM (24 against 32 KB of operands at the per-SM ingress that bounds
-// both), with a 10% margin for the narrow tiles' extra epilogues.
-static bool narrow_tiles_win(int M, int N, const DeviceInfo& dev) {
+// Time of a tile configuration in tile periods: whole waves of tiles over the
+// SM pairs, plus the last partial wave, which the tail split (qk_launch.cuh)
+// shortens to 1/S of a tile plus the partials' round trip (about 7 k-blocks).
+static double tile_waves(long long tiles, long long slots, int num_kb) {
+  const long long W = tiles / slots, R = tiles % slots;
+  if (R == 0) return static_cast<double>(W);
+  const int S = tail_split_parts(tiles, slots, num_kb);
+  return static_cast<double>(W) + (S > 1 ? 1.0 / S + 7.0 / num_kb : 1.0);
+}
+
+// Whether 256 x 128 pair tiles finish sooner than 256 x 256 ones, a narrow
+// tile's period costing about 3/4 of a wide one's per SM (24 against 32 KB of
+// operands per k-block at the per-SM ingress that bounds both), with a 10%
+// margin for the narrow tiles' extra epilogues.
+static bool narrow_tiles_win(int M, int N, int K, const DeviceInfo& dev) {
   const long long pairs = dev.sm_count / 2;
   const long long mb = (M + 255) / 256;
-  const long long wide = mb * ((N + 255) / 256), narrow = mb * ((N + 127) / 128);
-  const long long waves_wide = (wide + pairs - 1) / pairs, waves_narrow = (narrow + pairs - 1) / pairs;
-  return waves_narrow * 3 * 10 < waves_wide * 4 * 9;
+  const int num_kb = (K + 127) / 128;
+  const double wide = tile_waves(mb * ((N + 255) / 256), pairs, num_kb);
+  const double narrow = tile_waves(mb * ((N + 127) / 128), pairs, num_kb);
+  return narrow * 0.75 < wide * 0.9;
 }
 
 template <class C>
@@ -88,7 +99,7 @@ int launch_fp8_rowwise(const uint8_t* A, const uint8_t* B, const float* sa, cons
                            : launch_fewrow_fp8<128>(A, B, sa, sb, bias, out, M, N, K, dev, stream, v);
     if (st != QK_ERR_RANGE) return st;
   }
-  if (narrow_tiles_win(M, N, dev)) return launch_fp8_cfg<CfgFp8Narrow>(A, B, sa, sb, bias, out, M, N, K, dev, stream);
+  if (narrow_tiles_win(M, N, K, dev)) return launch_fp8_cfg<CfgFp8Narrow>(A, B, sa, sb, bias, out, M, N, K, dev, stream);
   if (K <= 2048) return launch_fp8_cfg<CfgFp8Drain>(A, B, sa, sb, bias, out, M, N, K, dev, stream);
   return launch_fp8_cfg<CfgFp8>(A, B, sa, sb, bias, out, M, N, K, dev, stream);
 }

@@ -5,7 +5,12 @@
 // A [M,K] and B [N,K] are K-major; round_out is bf16 round-to-nearest-even
 // unless the configuration's OutType says fp16 or fp32.  Persistent CTAs
 // (one per SM, or one 2-SM pair per two SMs) walk output tiles of
-// 128 x BN (a pair: 256 x BN) in a grouped-M raster.  Roles:
+// 128 x BN (a pair: 256 x BN) in a grouped-M raster.  Tail split (kinds with
+// one accumulation chunk per tile): when the last wave of tiles would leave
+// at least half of the CTAs idle, its tiles run as S K-parts each (work
+// units after the whole tiles); every part writes its fp32 partial to a
+// workspace, and per epilogue warp the part that finishes last adds the S
+// partials in K order and runs the epilogue on the sum.  Roles:
 //   warp 0      TMA producer: A/B tiles of 128-byte K rows into a STAGES-deep
 //               shared-memory ring (128-byte swizzle); block-scaled kinds: the
 //               stage's scale-factor atoms with them (see qk_sf_atoms.cuh).
@@ -85,6 +90,13 @@ struct GemmParams {
   const float* gb;
   int scale_kb;               // FP8 blockscale: K-blocks of 128 per scale row (sa [M, kb], sb [ceil(N/128), kb])
   int group_m;                // row-blocks per raster group
+  // tail split: units [0, full_tiles) are whole tiles; unit full_tiles + v is
+  // K-part v % split of tile full_tiles + v / split, k-blocks
+  // [part * split_kb, min(num_kb, (part + 1) * split_kb))
+  int num_units, full_tiles, split, split_kb;
+  float* split_ws;                   // fp32 partials [tail tile][CTA][epilogue warp][part][EPI_COLS/4][32 lanes][4]
+  unsigned long long* split_cnt;     // arrival words [tail tile][CTA][epilogue warp]
+  unsigned long long split_tag;      // this call's tag (low 8 bits zero)
   unsigned long long* err;    // device error word
   uint64_t timeout_ns;        // bound on every barrier wait
 };
@@ -141,6 +153,8 @@ struct GemmCfg {
   static constexpr bool REG_SUMS = (INT_CHUNKS || BLOCKSCALE || MX || KIND == Kind::F8) && EPI_WARPS == 16;
   // kinds whose one-chunk accumulator is drained into registers and released before the epilogue math
   static constexpr bool REG_DRAIN = REG_SUMS && (MX || KIND == Kind::F8);
+  // kinds whose tiles may be split along K (one accumulation chunk per tile)
+  static constexpr bool SPLITTABLE = !INT_CHUNKS && !BLOCKSCALE;
 
   static constexpr int SF_PER_STAGE = MX ? K_ELEMS / SF_BLOCK : 0;  // scale bytes per row per stage
   static constexpr int SF_ATOMS_K = SF_PER_STAGE / 4;         // 4 scale bytes per 32-bit TMEM column
@@ -227,6 +241,49 @@ struct GemmCfg {
                                 : make_idesc_block_scaled(1, 1, MMA_M, BN, a_sf_id, b_sf_id, false);
   }
 };
+
+// Work unit u: its tile t, its k-blocks [kb0, kb1) and its K-part (-1: the
+// whole tile).
+template <class C>
+__device__ __forceinline__ void unit_of(const GemmParams& p, int u, int& t, int& kb0, int& kb1, int& kpart) {
+  if (!C::SPLITTABLE || u < p.full_tiles) {
+    t = u;
+    kb0 = 0;
+    kb1 = p.num_kb;
+    kpart = -1;
+    return;
+  }
+  const int v = u - p.full_tiles;
+  t = p.full_tiles + v / p.split;
+  kpart = v % p.split;
+  kb0 = kpart * p.split_kb;
+  kb1 = min(p.num_kb, kb0 + p.split_kb);
+}
+
+template <class C>
+__device__ __forceinline__ int num_units(const GemmParams& p) {
+  return C::SPLITTABLE ? p.num_units : p.num_tiles;
+}
+
+// One K-part's arrival at its region's word (the call's tag in the high 56
+// bits, the arrivals so far in the low 8; a word holding another tag counts
+// as none).  Returns true for the last of `parts` arrivals, which leaves the
+// word at 0 for the next call (or graph replay).  Each failed exchange means
+// another arrival succeeded, so the loop ends within `parts` rounds.
+__device__ __forceinline__ bool split_arrive(unsigned long long* word, unsigned long long tag, int parts,
+                                             unsigned long long* err) {
+  unsigned long long old = atomicAdd(word, 0ull);
+#pragma unroll 1
+  for (int i = 0; i < 64; ++i) {
+    const unsigned long long cnt = (old & ~0xFFull) == tag ? (old & 0xFFull) : 0ull;
+    const bool last = cnt + 1 == static_cast<unsigned long long>(parts);
+    const unsigned long long seen = atomicCAS(word, old, last ? 0ull : (tag | (cnt + 1)));
+    if (seen == old) return last;
+    old = seen;
+  }
+  report_error(err, kDevErrTimeout, kSiteSplitArrive, 0u);
+  return false;
+}
 
 __device__ __forceinline__ void tile_coords(const GemmParams& p, int t, int& mb, int& nb) {
   const int group_tiles = p.group_m * p.num_n_blocks;
@@ -489,9 +546,11 @@ __device__ __forceinline__ void scale_copier(const GemmParams& p, uint8_t* smem,
   long long issued = 0;
   bool ok = true;
 #pragma unroll 1
-  for (int t = tile0; ok && t < p.num_tiles; t += tile_step) {
+  for (int u = tile0; ok && u < num_units<C>(p); u += tile_step) {
+    int t, ukb0, ukb1, kpart;
+    unit_of<C>(p, u, t, ukb0, ukb1, kpart);
 #pragma unroll 1
-    for (int kb = 0; kb < p.num_kb; ++kb) {
+    for (int kb = ukb0; kb < ukb1; ++kb) {
       bool ready = mbar_wait(&sf_full[stage], phase, w, kSiteScaleCopy);
       // the slot's TMEM scales of the previous round have been read by their MMAs
       ready = ready && mbar_wait(&empty[stage], phase ^ 1u, w, kSiteScaleCopy);
@@ -639,13 +698,15 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
       const uint32_t full_leader = C::PAIR ? mapa_shared(smem_u32(&full[0]), 0u) : 0u;
       [[maybe_unused]] const uint32_t sf_full_leader = C::MX && C::PAIR ? mapa_shared(smem_u32(&sf_full[0]), 0u) : 0u;
 #pragma unroll 1
-      for (int t = tile0; ok && t < p.num_tiles; t += tile_step) {
+      for (int u = tile0; ok && u < num_units<C>(p); u += tile_step) {
+        int t, ukb0, ukb1, kpart;
+        unit_of<C>(p, u, t, ukb0, ukb1, kpart);
         int mb, nb;
         tile_coords(p, t, mb, nb);
         const int a_row = mb * C::TILE_M + static_cast<int>(rank) * C::BM;
         const int b_row = nb * C::BN + static_cast<int>(rank) * C::B_LOAD_ROWS;
 #pragma unroll 1
-        for (int kb = 0; kb < p.num_kb; ++kb) {
+        for (int kb = ukb0; kb < ukb1; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, w, kSiteProducerEmpty)) {
             ok = false;
             break;
@@ -724,7 +785,9 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
       uint32_t acc_iter = 0;
       bool ok = true;
 #pragma unroll 1
-      for (int t = tile0; ok && t < p.num_tiles; t += tile_step) {
+      for (int u = tile0; ok && u < num_units<C>(p); u += tile_step) {
+        int t, ukb0, ukb1, kpart;
+        unit_of<C>(p, u, t, ukb0, ukb1, kpart);
 #pragma unroll 1
         for (int c = 0; ok && c < p.num_chunks; ++c) {
           const int a = static_cast<int>(acc_iter % C::ACC_BUFS);
@@ -737,8 +800,9 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
           }
           tc_fence_after_sync();
           const uint32_t d_tmem = tmem + static_cast<uint32_t>(C::COL_ACC + a * C::BN);
-          const int kb0 = c * p.chunk_kb;
-          const int kb1 = min(p.num_kb, kb0 + p.chunk_kb);
+          // one chunk per unit for the splittable kinds (its k-blocks)
+          const int kb0 = C::SPLITTABLE ? ukb0 : c * p.chunk_kb;
+          const int kb1 = C::SPLITTABLE ? ukb1 : min(p.num_kb, kb0 + p.chunk_kb);
 #pragma unroll 1
           for (int kb = kb0; kb < kb1; ++kb) {
             bool landed = mbar_wait(&full[stage], phase, w, kSiteMmaFull);
@@ -842,7 +906,7 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
       uint32_t acc_iter = 0;
       bool ok = true;
 #pragma unroll 1
-      for (int t = tile0; ok && t < p.num_tiles; t += tile_step) {
+      for (int u = tile0; ok && u < num_units<C>(p); u += tile_step) {
 #pragma unroll 1
         for (int c = 0; c < p.num_chunks; ++c) {
           const int a = static_cast<int>(acc_iter % C::ACC_BUFS);
@@ -886,7 +950,9 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
       if (lane == 0) mbar_arrive(&acc_empty[a]);
     };
 #pragma unroll 1
-    for (int t = tile0; ok && t < p.num_tiles; t += tile_step) {
+    for (int u = tile0; ok && u < num_units<C>(p); u += tile_step) {
+      int t, ukb0, ukb1, kpart;
+      unit_of<C>(p, u, t, ukb0, ukb1, kpart);
       int mb, nb;
       tile_coords(p, t, mb, nb);
       const int m_block = mb * C::TILE_M + static_cast<int>(rank) * C::BM + q * 32;  // row of lane 0
@@ -942,7 +1008,73 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
             epilogue_row32_global<C::ROWWISE || kInt, kInt, kOff, C::ALPHA, C::OUT>(p, m, n0, sam, vals);
           }
         };
-        if constexpr (C::REG_DRAIN) {
+        if (C::SPLITTABLE && kpart >= 0) {
+          // a K-part of a split tile: this warp's 32 rows x EPI_COLS columns go
+          // to the workspace as fp32 (lane-contiguous 16-byte pieces), the
+          // accumulator is released, and the warp whose part arrives last adds
+          // the parts in K order, ((p0 + p1) + p2) ..., and emits the sum
+          constexpr int PIECES = C::EPI_COLS / 4;
+          const size_t region =
+              (static_cast<size_t>(t - p.full_tiles) * C::CTAS + rank) * C::EPI_WARPS + static_cast<size_t>(warp - 4);
+          float4* ws = reinterpret_cast<float4*>(p.split_ws) + region * static_cast<size_t>(p.split) * PIECES * 32;
+          float4* mine = ws + static_cast<size_t>(kpart) * PIECES * 32;
+#pragma unroll 1
+          for (int g = 0; g < C::EPI_COLS / 32; ++g) {
+            uint32_t v[32];
+            tmem_ld_32cols(acc_col + 32 * g, v);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              __stcg(mine + (8 * g + i) * 32 + lane,
+                     make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                 __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3])));
+          }
+          release(a);
+          __threadfence();  // this lane's partial before the arrival
+          __syncwarp();
+          int last = 0;
+          if (lane == 0) last = split_arrive(p.split_cnt + region, p.split_tag, p.split, p.err) ? 1 : 0;
+          last = __shfl_sync(0xffffffffu, last, 0);
+          if (last) {
+            __threadfence();  // the other parts' partials after their arrivals
+            // BC columns at a time, all of a part's pieces in flight at once
+            // (a one-piece-at-a-time loop waited for two L2 round trips per
+            // piece; 64-column batches in the 8-warp configurations measured
+            // no faster and took 168 registers against 110)
+            constexpr int BC = 32;
+            constexpr int NP = BC / 4;
+#pragma unroll 1
+            for (int g = 0; g < C::EPI_COLS / BC; ++g) {
+              const float4* src = ws + (NP * g) * 32 + lane;
+              float4 x[NP];
+#pragma unroll
+              for (int i = 0; i < NP; ++i) x[i] = __ldcg(src + 32 * i);
+#pragma unroll 1
+              for (int j = 1; j < p.split; ++j) {
+                float4 y[NP];
+#pragma unroll
+                for (int i = 0; i < NP; ++i) y[i] = __ldcg(src + static_cast<size_t>(j) * PIECES * 32 + 32 * i);
+#pragma unroll
+                for (int i = 0; i < NP; ++i) {
+                  x[i].x = __fadd_rn(x[i].x, y[i].x);
+                  x[i].y = __fadd_rn(x[i].y, y[i].y);
+                  x[i].z = __fadd_rn(x[i].z, y[i].z);
+                  x[i].w = __fadd_rn(x[i].w, y[i].w);
+                }
+              }
+              uint32_t v[BC];
+#pragma unroll
+              for (int i = 0; i < NP; ++i) {
+                v[4 * i] = __float_as_uint(x[i].x);
+                v[4 * i + 1] = __float_as_uint(x[i].y);
+                v[4 * i + 2] = __float_as_uint(x[i].z);
+                v[4 * i + 3] = __float_as_uint(x[i].w);
+              }
+              emit(EmitTag<false, 0>{}, n_tile + BC * g, v);
+              if constexpr (BC == 64) emit(EmitTag<false, 32>{}, n_tile + BC * g + 32, v);
+            }
+          }
+        } else if constexpr (C::REG_DRAIN) {
           // one chunk per tile: four TMEM loads in flight, one wait, release the
           // accumulator, then the epilogue from registers while the MMAs go on
 #pragma unroll

@@ -11,6 +11,8 @@
   their first global access.  A quantizer writes the activations and the GEMM
   reads them with nothing in between on the stream; the result matches the
   oracle on the quantizer's own outputs.
+* The switches QK_FP8_SKINNY=1 and QK_MX_SKINNY=1 send few rows to the 2-SM
+  tile kernels instead; their results match the oracle as well.
 """
 import numpy as np
 import pytest
@@ -19,7 +21,7 @@ import torch
 import block_scaled_precision_tcgen05_gb300 as qk
 import oracle
 import qk_inputs as qi
-from gpu_util import assert_close, host_bits, to_dev
+from gpu_util import assert_close, host_bits, run_fp8, run_mx, run_nvfp4, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -86,4 +88,22 @@ def test_mx_quantizer_then_fewrow_gemm():
     torch.cuda.synchronize()
     ref = oracle.gemm_mx(qi.FMT_MXFP4_E2M1, A.cpu().numpy(), sA.cpu().numpy(), p.B, p.sB)
     assert_close(host_bits(out), ref, "quantize_mx -> few-row MXFP4 gemm")
+    assert qk.device_status() == 0
+
+
+@pytest.mark.parametrize("shape", [(7, 4096, 4096), (100, 2112, 4096)], ids=["M7", "M100"])
+def test_tile_kernel_forced_for_few_rows(monkeypatch, shape):
+    # QK_FP8_SKINNY=1 / QK_MX_SKINNY=1: few rows through the 2-SM tile kernels
+    # (one 256-row tile, mostly zero-filled rows) instead of the few-row kernels
+    monkeypatch.setenv("QK_FP8_SKINNY", "1")
+    monkeypatch.setenv("QK_MX_SKINNY", "1")
+    M, N, K = shape
+    p = qi.fp8_problem(M, N, K, seed=M, bias=True)
+    assert_close(host_bits(run_fp8(p)), oracle.gemm_fp8_rowwise(p.A, p.B, p.sa, p.sb, bias=p.bias), f"fp8 {shape}")
+    for fmt in (qi.FMT_MXFP8_E4M3, qi.FMT_MXFP4_E2M1):
+        q = qi.mx_problem(fmt, M, N, K, seed=M + 1)
+        assert_close(host_bits(run_mx(q)), oracle.gemm_mx(fmt, q.A, q.sA, q.B, q.sB), f"fmt {fmt} {shape}")
+    r = qi.nvfp4_problem(M, N, K, seed=M + 2)
+    assert_close(host_bits(run_nvfp4(r)), oracle.gemm_nvfp4(r.A, r.sA, r.B, r.sB, r.global_a, r.global_b),
+                 f"nvfp4 {shape}")
     assert qk.device_status() == 0
