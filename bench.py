@@ -702,7 +702,9 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["qk", "reference"], default="qk")
     ap.add_argument("--formats", choices=["default", "none"], default="default",
                     help="none: the headline only (no per-configuration lines)")
-    ap.add_argument("--e2e-steps", type=int, default=10)
+    # steps of the end-to-end leg: enough that the pipeline's fill (the first input copy and GEMM,
+    # ~5 ms) stays a small part of a region bound by the output's read-back (~6.7 ms per step)
+    ap.add_argument("--e2e-steps", type=int, default=24)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--kernel-case", choices=["int8", "int8_fp16", "int8_fp32", "fp8", "mxfp8", "mxfp8_b32", "mxfp4",
                                               "nvfp4", "blockscale", "quantize_ptpc", "quantize_mxfp8"], default=None,
