@@ -203,6 +203,13 @@ int qk_gemm_mx_b32(int fmt, const void* A, const uint8_t* sA, const void* B, con
  * they touch memory only after it has completed), and a call may be captured
  * in a CUDA graph and replayed (the stream-K flags are cleared by the time a
  * call completes).
+ * With more rows the 2-SM tile kernel runs; when its last wave of tiles would
+ * leave at least half of the SM pairs idle after at least one full wave (and
+ * K is long enough), those tiles run as 2-4 K-parts whose fp32 partials go
+ * through a stream-ordered workspace from the same pool (QK_ERR_NOMEM is not
+ * raised for it: without a workspace the tiles run whole) and are added in a
+ * fixed order, so repeated calls and graph replays give identical bits.  The
+ * same holds for qk_gemm_mx, qk_gemm_mx_b32 and qk_gemm_nvfp4.
  */
 int qk_gemm_fp8_rowwise(const uint8_t* A, const uint8_t* B, const float* sa, const float* sb,
                         const uint16_t* bias, uint16_t* out, int64_t M, int64_t N, int64_t K,
