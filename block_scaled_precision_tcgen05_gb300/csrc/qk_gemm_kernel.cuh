@@ -687,9 +687,10 @@ __global__ void __launch_bounds__(C::NUM_THREADS, 1)
   if (warp == 0) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
-      // block-scaled kinds: the scale-atom pre-pass (the previous kernel of the
-      // stream, launched before this one may start) has completed
-      if constexpr (C::MX) griddep_wait();
+      // the kernel this one may overlap (programmatic launch) has completed:
+      // the scale-atom pre-pass (block-scaled kinds) or the int8 -> f16
+      // widening pass (exact INT8), whose outputs the first loads read
+      if constexpr (C::MX || C::INT_CHUNKS) griddep_wait();
       int stage = 0;
       uint32_t phase = 0;
       long long issued = 0;

@@ -49,6 +49,9 @@ __device__ __forceinline__ uint4 widen8(uint32_t w, uint32_t w2) {
 static __global__ void __launch_bounds__(256) qk_int8_to_f16_kernel(const uint4* __restrict__ a, uint4* __restrict__ a16,
                                                               long long na, const uint4* __restrict__ b,
                                                               uint4* __restrict__ b16, long long nb) {
+  // the GEMM that reads a16 / b16 may launch once every block of this pass
+  // has started (it waits for the pass to complete before its first load)
+  griddep_launch_dependents();
   const long long total = na + nb;
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
 #pragma unroll 1
@@ -101,7 +104,9 @@ static inline int widen_and_gemm_int8(const int8_t* A, const int8_t* B, const fl
     p.out = out;
     p.err = dev.err_word;
     p.timeout_ns = wait_timeout_ns();
-    st = launch_gemm<C>(ta, tb, ta, tb, p, dev, stream);
+    // programmatic launch: the GEMM's prologue overlaps the widening pass's
+    // last wave, and its producer waits for the pass before the first load
+    st = launch_gemm<C>(ta, tb, ta, tb, p, dev, stream, true);
   }
   return st;
 }

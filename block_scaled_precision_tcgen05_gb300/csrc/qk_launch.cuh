@@ -80,7 +80,9 @@ constexpr int kernel_kind() {
 // tsa / tsb: tensor maps of the scale atoms (block-scaled kinds), else any map.
 // after_prepass: launch with programmatic stream serialization, so the kernel's
 // prologue overlaps the kernel before it in the stream (the scale-atom
-// pre-pass, which the producer waits for before its first load).
+// pre-pass, or the int8 -> f16 widening pass, which the producer waits for
+// before its first load; nothing else in the kernel reads what that pass
+// writes, and every earlier kernel of the stream completed before it began).
 template <class C>
 int launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsa, const CUtensorMap& tsb,
                 const GemmParams& p, const DeviceInfo& dev, cudaStream_t stream, bool after_prepass = false) {
