@@ -8,7 +8,8 @@ QK_TAIL_SPLIT=n (a test switch) splits the last min(tiles, pairs) tiles into
 n parts whatever it costs, so small problems reach every epilogue the split
 runs through: FP8 with 16 epilogue warps (K <= 2048), with 8 (K > 2048) and
 on 256 x 128 pair tiles, MXFP8, MXFP4 and NVFP4; 2, 3 and 4 parts, with a
-short last part where the K-blocks do not divide evenly; ragged M and N; a
+short last part where the K-blocks do not divide evenly, and a last K-block
+shorter than a ring stage; ragged M and N; a
 problem with more tiles than pairs, where whole tiles and K-parts mix.  Checked
 on sampled tiles (every ragged edge tile included) against the oracle within
 the FP8 / MX tolerance.  With small-integer operands every partial sum is an
@@ -44,8 +45,10 @@ def _sampled(out, ref_fn, M, N, what, seed=5, count=6):
 
 # (M, N, K): 256 x 256 pair tiles with 16 epilogue warps (K <= 2048, 15
 # K-blocks) and with 8 (K > 2048, 18 K-blocks); 100 tiles, more than the
-# pairs; 256 x 128 pair tiles (the narrow configuration wins at 600 x 776)
-FP8_SHAPES = [(1536, 1792, 1920), (1536, 1792, 2304), (2560, 2560, 1920), (600, 776, 2304)]
+# pairs; 256 x 128 pair tiles (the narrow configuration wins at 600 x 776);
+# 19 K-blocks, the last one 16 elements long
+FP8_SHAPES = [(1536, 1792, 1920), (1536, 1792, 2304), (2560, 2560, 1920), (600, 776, 2304),
+              (1536, 1792, 2320)]  # a ragged last K-block (16 of 128) in the last K-part
 
 
 @pytest.mark.parametrize("shape", FP8_SHAPES, ids=lambda s: "x".join(map(str, s)))
@@ -58,7 +61,8 @@ def test_fp8_tail_split_matches_oracle(split, shape):
     assert qk.device_status() == 0
 
 
-@pytest.mark.parametrize("fmt,K", [(qi.FMT_MXFP8_E4M3, 1920), (qi.FMT_MXFP4_E2M1, 3840)], ids=["mxfp8", "mxfp4"])
+@pytest.mark.parametrize("fmt,K", [(qi.FMT_MXFP8_E4M3, 1920), (qi.FMT_MXFP4_E2M1, 3840), (qi.FMT_MXFP4_E2M1, 3872)],
+                         ids=["mxfp8", "mxfp4", "mxfp4-ragged-k"])
 def test_mx_tail_split_matches_oracle(split, fmt, K):
     M, N = 600, 776
     p = qi.mx_problem(fmt, M, N, K, seed=K, bias=True)
@@ -68,8 +72,9 @@ def test_mx_tail_split_matches_oracle(split, fmt, K):
     assert qk.device_status() == 0
 
 
-def test_nvfp4_tail_split_matches_oracle(split):
-    M, N, K = 600, 776, 3840
+@pytest.mark.parametrize("K", [3840, 3872], ids=["k3840", "ragged-k"])
+def test_nvfp4_tail_split_matches_oracle(split, K):
+    M, N = 600, 776
     p = qi.nvfp4_problem(M, N, K, seed=3, bias=True)
     out = run_nvfp4(p)
     _sampled(out, lambda m0, m1, n0, n1: oracle.gemm_nvfp4(p.A, p.sA, p.B, p.sB, p.global_a, p.global_b, bias=p.bias,
