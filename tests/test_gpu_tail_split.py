@@ -14,8 +14,10 @@ problem with more tiles than pairs, where whole tiles and K-parts mix.  Checked
 on sampled tiles (every ragged edge tile included) against the oracle within
 the FP8 / MX tolerance.  With small-integer operands every partial sum is an
 exact integer in fp32, so the split result equals the oracle bit for bit.
-Repeated calls and CUDA graph replays repeat the bits: the reduction order is
-fixed, and the last arrival leaves its arrival word cleared."""
+Repeated calls and CUDA graph replays (FP8 and MXFP4) repeat the bits: the
+reduction order is fixed, and the last arrival leaves its arrival word
+cleared.  Split calls on two streams at once repeat the bits of the same
+calls made alone: each call draws its own workspace and tag."""
 import numpy as np
 import pytest
 import torch
@@ -174,4 +176,57 @@ def test_tail_split_default_rule(case):
         refs.append(ref_fn(m0, m1, n0, n1).ravel())
     assert not torch.isnan(out).any().item(), f"{case}: unwritten outputs"
     assert_close(np.concatenate(gots)[None, :], np.concatenate(refs)[None, :], case)
+    assert qk.device_status() == 0
+
+
+def test_tail_split_on_two_streams(monkeypatch):
+    # split calls on two streams at once draw separate workspaces and tags:
+    # each result repeats the bits of the same call made alone
+    monkeypatch.setenv("QK_TAIL_SPLIT", "2")
+    shapes = [(1536, 1792, 2304), (2560, 2560, 1920)]
+    probs = [qi.fp8_problem(M, N, K, seed=20 + i) for i, (M, N, K) in enumerate(shapes)]
+    devs = [[to_dev(x) for x in (p.A, p.B, p.sa, p.sb)] for p in probs]
+    outs = [torch.empty((M, N), dtype=torch.bfloat16, device="cuda") for (M, N, K) in shapes]
+    alone = []
+    for (A, B, sa, sb), out in zip(devs, outs):
+        qk.gemm_fp8_rowwise(A, B, sa, sb, None, out)
+        torch.cuda.synchronize()
+        alone.append(host_bits(out))
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    for rep in range(3):
+        for o in outs:
+            o.fill_(float("nan"))
+        torch.cuda.synchronize()
+        for s, (A, B, sa, sb), out in zip(streams, devs, outs):
+            with torch.cuda.stream(s):
+                for _ in range(2):
+                    qk.gemm_fp8_rowwise(A, B, sa, sb, None, out)
+        torch.cuda.synchronize()
+        for o, bits, shape in zip(outs, alone, shapes):
+            assert np.array_equal(host_bits(o), bits), f"{shape} on two streams, repetition {rep}"
+    assert qk.device_status() == 0
+
+
+def test_mxfp4_tail_split_graph_replay(monkeypatch):
+    # a block-scaled split call (scale pre-pass + GEMM) captured once and
+    # replayed: every replay repeats the plain call's bits
+    monkeypatch.setenv("QK_TAIL_SPLIT", "3")
+    M, N, K = 600, 776, 3872
+    p = qi.mx_problem(qi.FMT_MXFP4_E2M1, M, N, K, seed=31)
+    A, sA, B, sB = (to_dev(x) for x in (p.A, p.sA, p.B, p.sB))
+    out = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    qk.gemm_mx(p.fmt, A, sA, B, sB, None, out)
+    torch.cuda.synchronize()
+    first = host_bits(out)
+    assert_close(first, oracle.gemm_mx(p.fmt, p.A, p.sA, p.B, p.sB), "plain split call")
+    graph = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.graph(graph, stream=side, capture_error_mode="thread_local"):
+        qk.gemm_mx(p.fmt, A, sA, B, sB, None, out)
+    for replay in range(3):
+        out.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert np.array_equal(host_bits(out), first), f"replay {replay} differs from the plain call"
     assert qk.device_status() == 0
