@@ -46,6 +46,7 @@ EXPORTS = (
     "qk_gemm_mx",
     "qk_gemm_mx_b32",
     "qk_gemm_fp8_rowwise",
+    "qk_gemm_fp8_rowwise_out",
     "qk_gemm_nvfp4",
     "qk_gemm_fp8_blockscale",
     "qk_quantize_mx",
@@ -87,6 +88,8 @@ def _declare(lib):
     lib.qk_gemm_int8_rowwise_noalloc.restype = c.c_int
     lib.qk_gemm_fp8_rowwise.argtypes = [P, P, P, P, P, P, i64, i64, i64, P]
     lib.qk_gemm_fp8_rowwise.restype = c.c_int
+    lib.qk_gemm_fp8_rowwise_out.argtypes = [P, P, P, P, P, P, c.c_int, i64, i64, i64, P]
+    lib.qk_gemm_fp8_rowwise_out.restype = c.c_int
     lib.qk_gemm_mx.argtypes = [c.c_int, P, P, P, P, P, P, i64, i64, i64, P]
     lib.qk_gemm_mx.restype = c.c_int
     lib.qk_gemm_mx_b32.argtypes = [c.c_int, P, P, P, P, P, P, i64, i64, i64, P]
@@ -250,9 +253,13 @@ def gemm_int8_rowwise_noalloc(A, B, sa, sb, bias=None, out=None):
     return out
 
 
-def gemm_fp8_rowwise(A, B, sa, sb, bias=None, out=None):
-    """FP8 E4M3 GEMM with per-token sa[M] and per-channel sb[N] fp32 scales (uint8 E4M3 bytes in)."""
+def gemm_fp8_rowwise(A, B, sa, sb, bias=None, out=None, out_dtype=None):
+    """FP8 E4M3 GEMM with per-token sa[M] and per-channel sb[N] fp32 scales (uint8 E4M3 bytes in).
+    With out_dtype torch.float16 or torch.float32 (or an `out` of that dtype) the same value is
+    written as fp16 (round to nearest even) or as fp32 itself."""
     import torch
+    if A.dim() != 2 or B.dim() != 2:
+        raise ValueError("A and B must be 2-D")
     M, K = A.shape
     N = B.shape[0]
     dev = A.device
@@ -264,10 +271,21 @@ def gemm_fp8_rowwise(A, B, sa, sb, bias=None, out=None):
     _expect(sb, "sb", torch.float32, (N,), dev)
     if bias is not None:
         _expect(bias, "bias", torch.bfloat16, (N,), dev)
-    out = _out(out, M, N, dev)
+    if out_dtype is None:
+        out_dtype = torch.bfloat16 if out is None else out.dtype
+    codes = {torch.bfloat16: QK_OUT_BF16, torch.float16: QK_OUT_FP16, torch.float32: QK_OUT_FP32}
+    if out_dtype not in codes:
+        raise ValueError(f"out_dtype must be bfloat16, float16 or float32, not {out_dtype}")
+    if out is None:
+        out = torch.empty((M, N), dtype=out_dtype, device=dev)
+    _expect(out, "out", out_dtype, (M, N), dev)
     with _on_device(dev):
-        check(load_library().qk_gemm_fp8_rowwise(_ptr(A), _ptr(B), _ptr(sa), _ptr(sb), _ptr(bias), _ptr(out),
-                                                 M, N, K, _stream_handle(dev)))
+        if out_dtype == torch.bfloat16:
+            check(load_library().qk_gemm_fp8_rowwise(_ptr(A), _ptr(B), _ptr(sa), _ptr(sb), _ptr(bias), _ptr(out),
+                                                     M, N, K, _stream_handle(dev)))
+        else:
+            check(load_library().qk_gemm_fp8_rowwise_out(_ptr(A), _ptr(B), _ptr(sa), _ptr(sb), _ptr(bias),
+                                                         _ptr(out), codes[out_dtype], M, N, K, _stream_handle(dev)))
     return out
 
 

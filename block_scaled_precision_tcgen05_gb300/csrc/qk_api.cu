@@ -301,6 +301,19 @@ int qk_gemm_fp8_rowwise(const uint8_t* A, const uint8_t* B, const float* sa, con
                             static_cast<int>(K), *dev, static_cast<cudaStream_t>(stream));
 }
 
+int qk_gemm_fp8_rowwise_out(const uint8_t* A, const uint8_t* B, const float* sa, const float* sb,
+                            const uint16_t* bias, void* out, int out_type, int64_t M, int64_t N, int64_t K,
+                            qk_stream_t stream) {
+  if (out_type != QK_OUT_BF16 && out_type != QK_OUT_FP16 && out_type != QK_OUT_FP32) return QK_ERR_ARG;
+  bool empty;
+  int st = check_rowwise(A, B, sa, sb, bias, static_cast<const uint16_t*>(out), M, N, K, INT32_MAX, &empty);
+  if (st != QK_OK || empty) return st;
+  const DeviceInfo* dev = current_device(&st);
+  if (!dev) return st;
+  return launch_fp8_rowwise_out(A, B, sa, sb, bias, out, out_type, static_cast<int>(M), static_cast<int>(N),
+                                static_cast<int>(K), *dev, static_cast<cudaStream_t>(stream));
+}
+
 int qk_gemm_mx(int fmt, const void* A, const uint8_t* sA, const void* B, const uint8_t* sB, const uint16_t* bias,
                uint16_t* out, int64_t M, int64_t N, int64_t K, qk_stream_t stream) {
   if (fmt != QK_FMT_MXFP8_E4M3 && fmt != QK_FMT_MXFP4_E2M1) return QK_ERR_ARG;

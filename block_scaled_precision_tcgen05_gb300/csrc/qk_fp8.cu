@@ -21,6 +21,11 @@ using CfgFp8Drain = GemmCfg<Kind::F8, 256, 6, 2, true, 16, 1>;
 // 32 for half the work), eight stages, two 128-column accumulators: twice the
 // tiles of CfgFp8, for problems whose 256 x 256 tiles leave pairs idle.
 using CfgFp8Narrow = GemmCfg<Kind::F8, 128, 8, 2, true, 8, 1>;
+// fp16 / fp32 outputs (the same x, another rounding): CfgFp8's tiles and ring
+// with 16-bit or 32-bit staging blocks (the fp32 blocks of 4 KB still leave
+// room for six stages)
+using CfgFp8F16 = GemmCfg<Kind::F8, 256, 6, 2, true, 8, 1, OutType::F16>;
+using CfgFp8F32 = GemmCfg<Kind::F8, 256, 6, 2, true, 8, 1, OutType::F32>;
 
 // Time of a tile configuration in tile periods: whole waves of tiles over the
 // SM pairs, plus the last partial wave, which the tail split (qk_launch.cuh)
@@ -47,7 +52,7 @@ static bool narrow_tiles_win(int M, int N, int K, const DeviceInfo& dev) {
 
 template <class C>
 static int launch_fp8_cfg(const uint8_t* A, const uint8_t* B, const float* sa, const float* sb, const uint16_t* bias,
-                          uint16_t* out, int M, int N, int K, const DeviceInfo& dev, cudaStream_t stream) {
+                          void* out, int M, int N, int K, const DeviceInfo& dev, cudaStream_t stream) {
   CUtensorMap ta, tb;
   int st = encode_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, K, M, K, C::TMA_K, C::BM);
   if (st == QK_OK) st = encode_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, K, N, K, C::TMA_K, C::B_LOAD_ROWS);
@@ -102,6 +107,15 @@ int launch_fp8_rowwise(const uint8_t* A, const uint8_t* B, const float* sa, cons
   if (narrow_tiles_win(M, N, K, dev)) return launch_fp8_cfg<CfgFp8Narrow>(A, B, sa, sb, bias, out, M, N, K, dev, stream);
   if (K <= 2048) return launch_fp8_cfg<CfgFp8Drain>(A, B, sa, sb, bias, out, M, N, K, dev, stream);
   return launch_fp8_cfg<CfgFp8>(A, B, sa, sb, bias, out, M, N, K, dev, stream);
+}
+
+// Output types other than bf16: the 2-SM tile kernel for every M (the
+// few-row kernels write bf16 only).
+int launch_fp8_rowwise_out(const uint8_t* A, const uint8_t* B, const float* sa, const float* sb, const uint16_t* bias,
+                           void* out, int out_type, int M, int N, int K, const DeviceInfo& dev, cudaStream_t stream) {
+  if (out_type == QK_OUT_FP32) return launch_fp8_cfg<CfgFp8F32>(A, B, sa, sb, bias, out, M, N, K, dev, stream);
+  if (out_type == QK_OUT_FP16) return launch_fp8_cfg<CfgFp8F16>(A, B, sa, sb, bias, out, M, N, K, dev, stream);
+  return launch_fp8_rowwise(A, B, sa, sb, bias, static_cast<uint16_t*>(out), M, N, K, dev, stream);
 }
 
 }  // namespace qk

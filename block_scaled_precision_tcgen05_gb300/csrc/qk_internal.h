@@ -75,6 +75,8 @@ int launch_int8_rowwise(const int8_t* A, const int8_t* B, const float* sa, const
                         uint16_t* out, int M, int N, int K, const DeviceInfo& dev, cudaStream_t stream);
 int launch_fp8_rowwise(const uint8_t* A, const uint8_t* B, const float* sa, const float* sb, const uint16_t* bias,
                        uint16_t* out, int M, int N, int K, const DeviceInfo& dev, cudaStream_t stream);
+int launch_fp8_rowwise_out(const uint8_t* A, const uint8_t* B, const float* sa, const float* sb, const uint16_t* bias,
+                           void* out, int out_type, int M, int N, int K, const DeviceInfo& dev, cudaStream_t stream);
 int launch_mxfp8(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const uint8_t* sB, const uint16_t* bias,
                  uint16_t* out, int M, int N, int K, const DeviceInfo& dev, cudaStream_t stream);
 int launch_mxfp4(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const uint8_t* sB, const uint16_t* bias,

@@ -60,7 +60,7 @@ typedef void* qk_stream_t;
 #define QK_FMT_MXFP8_E4M3 1 /* A, B: one E4M3 byte per element */
 #define QK_FMT_MXFP4_E2M1 2 /* A, B: two E2M1 codes per byte, element 2i in the low nibble */
 
-/* ---- output element types for qk_gemm_int8_rowwise_out ----------------- */
+/* ---- output element types for qk_gemm_int8_rowwise_out and qk_gemm_fp8_rowwise_out */
 #define QK_OUT_BF16 0 /* 2 bytes, bf16 round to nearest even */
 #define QK_OUT_FP16 1 /* 2 bytes, IEEE half round to nearest even (beyond 65504: +-inf) */
 #define QK_OUT_FP32 2 /* 4 bytes, the fp32 value x itself */
@@ -214,6 +214,23 @@ int qk_gemm_mx_b32(int fmt, const void* A, const uint8_t* sA, const void* B, con
 int qk_gemm_fp8_rowwise(const uint8_t* A, const uint8_t* B, const float* sa, const float* sb,
                         const uint16_t* bias, uint16_t* out, int64_t M, int64_t N, int64_t K,
                         qk_stream_t stream);
+
+/*
+ * qk_gemm_fp8_rowwise with a choice of output element type (ROCm/aiter PR
+ * #6262: gemm_a8w8_bpreshuffle takes the output dtype as an argument, bf16 by
+ * default, and checks a caller-owned out against it).  The same x as
+ * qk_gemm_fp8_rowwise computes, then
+ *   out_type QK_OUT_BF16: out bf16 [M, N] = bf16_rne(x)   (as qk_gemm_fp8_rowwise)
+ *            QK_OUT_FP16: out fp16 [M, N] = fp16_rne(x)   (+-inf beyond the fp16 range)
+ *            QK_OUT_FP32: out fp32 [M, N] = x
+ * `out` points to M * N elements of that type.  fp16 and fp32 outputs run
+ * the 2-SM tile kernel for every M (the few-row kernels write bf16 only), so
+ * for a given problem the two hold the same x.  Arguments, requirements and
+ * errors as for qk_gemm_fp8_rowwise; an unknown out_type returns QK_ERR_ARG.
+ */
+int qk_gemm_fp8_rowwise_out(const uint8_t* A, const uint8_t* B, const float* sa, const float* sb,
+                            const uint16_t* bias, void* out, int out_type, int64_t M, int64_t N, int64_t K,
+                            qk_stream_t stream);
 
 /*
  * FP8 E4M3 GEMM with fp32 block scales (the "blockscale" kind of ROCm/mori PR

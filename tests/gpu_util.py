@@ -80,7 +80,12 @@ def assert_bit_exact(gpu_bits, ref_bits, what=""):
 
 
 def tolerance_report(gpu_bits, ref):
-    g = qi.from_bf16_bits(gpu_bits).astype(np.float64)
+    return tolerance_report_values(qi.from_bf16_bits(gpu_bits).astype(np.float64), ref)
+
+
+def tolerance_report_values(g, ref):
+    """The report on output values already widened to fp64 (fp16 / fp32 outputs)."""
+    g = np.asarray(g, np.float64)
     rms = float(np.sqrt(np.mean(ref ** 2)))
     err = np.abs(g - ref)
     bound = RTOL * np.abs(ref) + ATOL_RMS * rms
@@ -92,5 +97,11 @@ def tolerance_report(gpu_bits, ref):
 
 def assert_close(gpu_bits, ref, what=""):
     r = tolerance_report(gpu_bits, ref)
+    assert r["nan"] == 0 and r["bad"] == 0 and r["cos"] >= COS_MIN, f"{what}: {r}"
+    return r
+
+
+def assert_close_values(gpu_values, ref, what=""):
+    r = tolerance_report_values(gpu_values, ref)
     assert r["nan"] == 0 and r["bad"] == 0 and r["cos"] >= COS_MIN, f"{what}: {r}"
     return r
