@@ -44,10 +44,12 @@ EXPORTS = (
     "qk_gemm_int8_rowwise_out",
     "qk_gemm_int8_rowwise_noalloc",
     "qk_gemm_mx",
+    "qk_gemm_mx_out",
     "qk_gemm_mx_b32",
     "qk_gemm_fp8_rowwise",
     "qk_gemm_fp8_rowwise_out",
     "qk_gemm_nvfp4",
+    "qk_gemm_nvfp4_out",
     "qk_gemm_fp8_blockscale",
     "qk_quantize_mx",
     "qk_quantize_ptpc",
@@ -92,10 +94,14 @@ def _declare(lib):
     lib.qk_gemm_fp8_rowwise_out.restype = c.c_int
     lib.qk_gemm_mx.argtypes = [c.c_int, P, P, P, P, P, P, i64, i64, i64, P]
     lib.qk_gemm_mx.restype = c.c_int
+    lib.qk_gemm_mx_out.argtypes = [c.c_int, P, P, P, P, P, P, c.c_int, i64, i64, i64, P]
+    lib.qk_gemm_mx_out.restype = c.c_int
     lib.qk_gemm_mx_b32.argtypes = [c.c_int, P, P, P, P, P, P, i64, i64, i64, P]
     lib.qk_gemm_mx_b32.restype = c.c_int
     lib.qk_gemm_nvfp4.argtypes = [P, P, P, P, P, P, P, P, i64, i64, i64, P]
     lib.qk_gemm_nvfp4.restype = c.c_int
+    lib.qk_gemm_nvfp4_out.argtypes = [P, P, P, P, P, P, P, P, c.c_int, i64, i64, i64, P]
+    lib.qk_gemm_nvfp4_out.restype = c.c_int
     lib.qk_gemm_fp8_blockscale.argtypes = [P, P, P, P, P, P, i64, i64, i64, P]
     lib.qk_gemm_fp8_blockscale.restype = c.c_int
     lib.qk_quantize_mx.argtypes = [c.c_int, P, P, P, i64, i64, P]
@@ -253,6 +259,21 @@ def gemm_int8_rowwise_noalloc(A, B, sa, sb, bias=None, out=None):
     return out
 
 
+def _out_typed(out, out_dtype, M, N, dev):
+    """The output tensor and its QK_OUT_* code: `out` (its dtype must agree with out_dtype when both
+    are given) or a new [M, N] tensor of out_dtype (bf16 by default)."""
+    import torch
+    if out_dtype is None:
+        out_dtype = torch.bfloat16 if out is None else out.dtype
+    codes = {torch.bfloat16: QK_OUT_BF16, torch.float16: QK_OUT_FP16, torch.float32: QK_OUT_FP32}
+    if out_dtype not in codes:
+        raise ValueError(f"out_dtype must be bfloat16, float16 or float32, not {out_dtype}")
+    if out is None:
+        out = torch.empty((M, N), dtype=out_dtype, device=dev)
+    _expect(out, "out", out_dtype, (M, N), dev)
+    return out, codes[out_dtype]
+
+
 def gemm_fp8_rowwise(A, B, sa, sb, bias=None, out=None, out_dtype=None):
     """FP8 E4M3 GEMM with per-token sa[M] and per-channel sb[N] fp32 scales (uint8 E4M3 bytes in).
     With out_dtype torch.float16 or torch.float32 (or an `out` of that dtype) the same value is
@@ -271,27 +292,21 @@ def gemm_fp8_rowwise(A, B, sa, sb, bias=None, out=None, out_dtype=None):
     _expect(sb, "sb", torch.float32, (N,), dev)
     if bias is not None:
         _expect(bias, "bias", torch.bfloat16, (N,), dev)
-    if out_dtype is None:
-        out_dtype = torch.bfloat16 if out is None else out.dtype
-    codes = {torch.bfloat16: QK_OUT_BF16, torch.float16: QK_OUT_FP16, torch.float32: QK_OUT_FP32}
-    if out_dtype not in codes:
-        raise ValueError(f"out_dtype must be bfloat16, float16 or float32, not {out_dtype}")
-    if out is None:
-        out = torch.empty((M, N), dtype=out_dtype, device=dev)
-    _expect(out, "out", out_dtype, (M, N), dev)
+    out, code = _out_typed(out, out_dtype, M, N, dev)
     with _on_device(dev):
-        if out_dtype == torch.bfloat16:
+        if code == QK_OUT_BF16:
             check(load_library().qk_gemm_fp8_rowwise(_ptr(A), _ptr(B), _ptr(sa), _ptr(sb), _ptr(bias), _ptr(out),
                                                      M, N, K, _stream_handle(dev)))
         else:
             check(load_library().qk_gemm_fp8_rowwise_out(_ptr(A), _ptr(B), _ptr(sa), _ptr(sb), _ptr(bias),
-                                                         _ptr(out), codes[out_dtype], M, N, K, _stream_handle(dev)))
+                                                         _ptr(out), code, M, N, K, _stream_handle(dev)))
     return out
 
 
-def gemm_mx(fmt, A, sA, B, sB, bias=None, out=None):
+def gemm_mx(fmt, A, sA, B, sB, bias=None, out=None, out_dtype=None):
     """MX block-scaled GEMM.  fmt FMT_MXFP8_E4M3 ([rows, K] bytes) or FMT_MXFP4_E2M1 ([rows, K/2] bytes);
-    sA [M, K/32], sB [N, K/32] raw UE8M0 bytes."""
+    sA [M, K/32], sB [N, K/32] raw UE8M0 bytes.  With out_dtype torch.float16 or torch.float32 (or an
+    `out` of that dtype) the value is written as fp16 (round to nearest even) or as fp32 itself."""
     import torch
     if fmt not in (FMT_MXFP8_E4M3, FMT_MXFP4_E2M1):
         raise ValueError("unknown MX format")
@@ -307,10 +322,14 @@ def gemm_mx(fmt, A, sA, B, sB, bias=None, out=None):
     _expect(sB, "sB", torch.uint8, (N, K // 32), dev)
     if bias is not None:
         _expect(bias, "bias", torch.bfloat16, (N,), dev)
-    out = _out(out, M, N, dev)
+    out, code = _out_typed(out, out_dtype, M, N, dev)
     with _on_device(dev):
-        check(load_library().qk_gemm_mx(int(fmt), _ptr(A), _ptr(sA), _ptr(B), _ptr(sB), _ptr(bias), _ptr(out),
-                                        M, N, K, _stream_handle(dev)))
+        if code == QK_OUT_BF16:
+            check(load_library().qk_gemm_mx(int(fmt), _ptr(A), _ptr(sA), _ptr(B), _ptr(sB), _ptr(bias), _ptr(out),
+                                            M, N, K, _stream_handle(dev)))
+        else:
+            check(load_library().qk_gemm_mx_out(int(fmt), _ptr(A), _ptr(sA), _ptr(B), _ptr(sB), _ptr(bias),
+                                                _ptr(out), code, M, N, K, _stream_handle(dev)))
     return out
 
 
@@ -361,9 +380,11 @@ def gemm_fp8_blockscale(A, B, sa, sb, bias=None, out=None):
     return out
 
 
-def gemm_nvfp4(A, sA, B, sB, global_a=None, global_b=None, bias=None, out=None):
+def gemm_nvfp4(A, sA, B, sB, global_a=None, global_b=None, bias=None, out=None, out_dtype=None):
     """NVFP4 GEMM.  A [M, K/2], B [N, K/2] packed E2M1 bytes; sA [M, K/16], sB [N, K/16] raw UE4M3
-    bytes; global_a / global_b optional one-element fp32 CUDA tensors (per-tensor scales)."""
+    bytes; global_a / global_b optional one-element fp32 CUDA tensors (per-tensor scales).  With
+    out_dtype torch.float16 or torch.float32 (or an `out` of that dtype) the value is written as fp16
+    (round to nearest even) or as fp32 itself."""
     import torch
     M, kbytes = A.shape
     N = B.shape[0]
@@ -380,10 +401,11 @@ def gemm_nvfp4(A, sA, B, sB, global_a=None, global_b=None, bias=None, out=None):
             _expect(g, name, torch.float32, (1,), dev)
     if bias is not None:
         _expect(bias, "bias", torch.bfloat16, (N,), dev)
-    out = _out(out, M, N, dev)
+    out, code = _out_typed(out, out_dtype, M, N, dev)
     with _on_device(dev):
-        check(load_library().qk_gemm_nvfp4(_ptr(A), _ptr(sA), _ptr(B), _ptr(sB), _ptr(global_a), _ptr(global_b),
-                                           _ptr(bias), _ptr(out), M, N, K, _stream_handle(dev)))
+        check(load_library().qk_gemm_nvfp4_out(_ptr(A), _ptr(sA), _ptr(B), _ptr(sB), _ptr(global_a),
+                                               _ptr(global_b), _ptr(bias), _ptr(out), code, M, N, K,
+                                               _stream_handle(dev)))
     return out
 
 

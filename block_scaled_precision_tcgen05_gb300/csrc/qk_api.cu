@@ -262,6 +262,27 @@ int check_rowwise(const void* A, const void* B, const float* sa, const float* sb
   return QK_OK;
 }
 
+// Shared checks of the MX entry points (sB: the per-row or the per-32-row
+// scales), in the same order.
+int check_mx(int fmt, const void* A, const uint8_t* sA, const void* B, const uint8_t* sB, const uint16_t* bias,
+             const void* out, int64_t M, int64_t N, int64_t K, bool* empty) {
+  *empty = false;
+  if (fmt != QK_FMT_MXFP8_E4M3 && fmt != QK_FMT_MXFP4_E2M1) return QK_ERR_ARG;
+  if (M < 0 || N < 0 || K < 1) return QK_ERR_ARG;
+  if (M == 0 || N == 0) {
+    *empty = true;
+    return QK_OK;
+  }
+  if (!A || !sA || !B || !sB || !out) return QK_ERR_ARG;
+  if (!aligned(A, 16) || !aligned(B, 16) || !aligned(out, 16) || (bias && !aligned(bias, 16)) ||
+      !aligned(sA, 4) || !aligned(sB, 4))
+    return QK_ERR_ALIGN;
+  if (N % 8 != 0 || K % 32 != 0) return QK_ERR_ALIGN;
+  if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return QK_ERR_RANGE;
+  if (((M + 127) / 128) * ((N + 31) / 32) > INT32_MAX) return QK_ERR_RANGE;
+  return QK_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -316,42 +337,40 @@ int qk_gemm_fp8_rowwise_out(const uint8_t* A, const uint8_t* B, const float* sa,
 
 int qk_gemm_mx(int fmt, const void* A, const uint8_t* sA, const void* B, const uint8_t* sB, const uint16_t* bias,
                uint16_t* out, int64_t M, int64_t N, int64_t K, qk_stream_t stream) {
-  if (fmt != QK_FMT_MXFP8_E4M3 && fmt != QK_FMT_MXFP4_E2M1) return QK_ERR_ARG;
-  if (M < 0 || N < 0 || K < 1) return QK_ERR_ARG;
-  if (M == 0 || N == 0) return QK_OK;
-  if (!A || !sA || !B || !sB || !out) return QK_ERR_ARG;
-  if (!aligned(A, 16) || !aligned(B, 16) || !aligned(out, 16) || (bias && !aligned(bias, 16)) ||
-      !aligned(sA, 4) || !aligned(sB, 4))
-    return QK_ERR_ALIGN;
-  if (N % 8 != 0 || K % 32 != 0) return QK_ERR_ALIGN;
-  if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return QK_ERR_RANGE;
-  if (((M + 127) / 128) * ((N + 31) / 32) > INT32_MAX) return QK_ERR_RANGE;
-  int st;
+  bool empty;
+  int st = check_mx(fmt, A, sA, B, sB, bias, out, M, N, K, &empty);
+  if (st != QK_OK || empty) return st;
   const DeviceInfo* dev = current_device(&st);
   if (!dev) return st;
   const auto s = static_cast<cudaStream_t>(stream);
   const auto* a = static_cast<const uint8_t*>(A);
   const auto* b = static_cast<const uint8_t*>(B);
-  if (fmt == QK_FMT_MXFP8_E4M3)
-    return launch_mxfp8(a, sA, b, sB, bias, out, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K),
-                        *dev, s);
-  return launch_mxfp4(a, sA, b, sB, bias, out, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), *dev,
-                      s);
+  const int m = static_cast<int>(M), n = static_cast<int>(N), k = static_cast<int>(K);
+  if (fmt == QK_FMT_MXFP8_E4M3) return launch_mxfp8(a, sA, b, sB, bias, out, m, n, k, *dev, s);
+  return launch_mxfp4(a, sA, b, sB, bias, out, m, n, k, *dev, s);
+}
+
+int qk_gemm_mx_out(int fmt, const void* A, const uint8_t* sA, const void* B, const uint8_t* sB, const uint16_t* bias,
+                   void* out, int out_type, int64_t M, int64_t N, int64_t K, qk_stream_t stream) {
+  if (out_type != QK_OUT_BF16 && out_type != QK_OUT_FP16 && out_type != QK_OUT_FP32) return QK_ERR_ARG;
+  bool empty;
+  int st = check_mx(fmt, A, sA, B, sB, bias, out, M, N, K, &empty);
+  if (st != QK_OK || empty) return st;
+  const DeviceInfo* dev = current_device(&st);
+  if (!dev) return st;
+  const auto s = static_cast<cudaStream_t>(stream);
+  const auto* a = static_cast<const uint8_t*>(A);
+  const auto* b = static_cast<const uint8_t*>(B);
+  const int m = static_cast<int>(M), n = static_cast<int>(N), k = static_cast<int>(K);
+  if (fmt == QK_FMT_MXFP8_E4M3) return launch_mxfp8_out(a, sA, b, sB, bias, out, out_type, m, n, k, *dev, s);
+  return launch_mxfp4_out(a, sA, b, sB, bias, out, out_type, m, n, k, *dev, s);
 }
 
 int qk_gemm_mx_b32(int fmt, const void* A, const uint8_t* sA, const void* B, const uint8_t* sB32,
                    const uint16_t* bias, uint16_t* out, int64_t M, int64_t N, int64_t K, qk_stream_t stream) {
-  if (fmt != QK_FMT_MXFP8_E4M3 && fmt != QK_FMT_MXFP4_E2M1) return QK_ERR_ARG;
-  if (M < 0 || N < 0 || K < 1) return QK_ERR_ARG;
-  if (M == 0 || N == 0) return QK_OK;
-  if (!A || !sA || !B || !sB32 || !out) return QK_ERR_ARG;
-  if (!aligned(A, 16) || !aligned(B, 16) || !aligned(out, 16) || (bias && !aligned(bias, 16)) ||
-      !aligned(sA, 4) || !aligned(sB32, 4))
-    return QK_ERR_ALIGN;
-  if (N % 8 != 0 || K % 32 != 0) return QK_ERR_ALIGN;
-  if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return QK_ERR_RANGE;
-  if (((M + 127) / 128) * ((N + 31) / 32) > INT32_MAX) return QK_ERR_RANGE;
-  int st;
+  bool empty;
+  int st = check_mx(fmt, A, sA, B, sB32, bias, out, M, N, K, &empty);
+  if (st != QK_OK || empty) return st;
   const DeviceInfo* dev = current_device(&st);
   if (!dev) return st;
   const auto s = static_cast<cudaStream_t>(stream);

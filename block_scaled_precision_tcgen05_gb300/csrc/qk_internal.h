@@ -81,6 +81,11 @@ int launch_mxfp8(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const ui
                  uint16_t* out, int M, int N, int K, const DeviceInfo& dev, cudaStream_t stream);
 int launch_mxfp4(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const uint8_t* sB, const uint16_t* bias,
                  uint16_t* out, int M, int N, int K, const DeviceInfo& dev, cudaStream_t stream);
+// the same with a QK_OUT_* output type (fp16 / fp32: the tile kernel for every M)
+int launch_mxfp8_out(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const uint8_t* sB, const uint16_t* bias,
+                     void* out, int out_type, int M, int N, int K, const DeviceInfo& dev, cudaStream_t stream);
+int launch_mxfp4_out(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const uint8_t* sB, const uint16_t* bias,
+                     void* out, int out_type, int M, int N, int K, const DeviceInfo& dev, cudaStream_t stream);
 // MX with B scales per 32x32 block ([ceil(N/32), K/32] bytes).
 int launch_mxfp8_b32(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const uint8_t* sB32,
                      const uint16_t* bias, uint16_t* out, int M, int N, int K, const DeviceInfo& dev,

@@ -17,6 +17,12 @@ namespace qk {
 // with 8 epilogue warps working from TMEM; one CTA with 128 x 256 tiles and
 // one accumulator, whose epilogue stalls the MMAs.
 using CfgMxfp8PairDrain = GemmCfg<Kind::MXF8, 256, 6, 1, true, 16, 1, OutType::BF16, 16>;
+// fp16 / fp32 outputs (the same value, another rounding) run this tile kernel
+// for every M (the few-row kernels write bf16 only): fp16 through the same
+// 32x16 staging blocks, fp32 with 16-byte stores straight from registers
+// (4 KB fp32 staging blocks for 16 warps would cost ring stages).
+using CfgMxfp8F16 = GemmCfg<Kind::MXF8, 256, 6, 1, true, 16, 1, OutType::F16, 16>;
+using CfgMxfp8F32 = GemmCfg<Kind::MXF8, 256, 6, 1, true, 16, 0, OutType::F32>;
 
 // Few rows (M <= 128): the few-row kernels' MXFP8 mode where they are faster
 // (launch_fewrow_block_scaled, qk_fewrow_launch.cuh, with the measurements).
@@ -31,6 +37,15 @@ int launch_mxfp8(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const ui
   const int st = launch_fewrow_block_scaled<1>(A, B, args, M, N, K, kKGemmMxfp8, dev, stream, &launched);
   if (launched) return st;
   return launch_block_scaled<CfgMxfp8PairDrain>(A, sA, B, sB, 1, nullptr, nullptr, bias, out, M, N, K, dev, stream);
+}
+
+int launch_mxfp8_out(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const uint8_t* sB, const uint16_t* bias,
+                     void* out, int out_type, int M, int N, int K, const DeviceInfo& dev, cudaStream_t stream) {
+  if (out_type == QK_OUT_FP16)
+    return launch_block_scaled<CfgMxfp8F16>(A, sA, B, sB, 1, nullptr, nullptr, bias, out, M, N, K, dev, stream);
+  if (out_type == QK_OUT_FP32)
+    return launch_block_scaled<CfgMxfp8F32>(A, sA, B, sB, 1, nullptr, nullptr, bias, out, M, N, K, dev, stream);
+  return launch_mxfp8(A, sA, B, sB, bias, static_cast<uint16_t*>(out), M, N, K, dev, stream);
 }
 
 // B scales per 32x32 block (ROCm/mori PR #806's mxfp8_raw form): the scale-atom

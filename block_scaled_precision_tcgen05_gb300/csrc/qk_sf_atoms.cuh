@@ -134,7 +134,7 @@ inline int write_sf_atoms(const uint8_t* sA, uint8_t* dA, int M, const uint8_t* 
 // [ceil(N / b_rows_per), K / SF_BLOCK]; ga, gb: NVFP4 per-tensor scales.
 template <class C>
 int launch_block_scaled(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const uint8_t* sB, int b_rows_per,
-                        const float* ga, const float* gb, const uint16_t* bias, uint16_t* out, int M, int N, int K,
+                        const float* ga, const float* gb, const uint16_t* bias, void* out, int M, int N, int K,
                         const DeviceInfo& dev, cudaStream_t stream) {
   static_assert(C::MX, "block-scaled configurations only");
   const uint64_t kbytes = C::FP4 ? static_cast<uint64_t>(K) / 2 : static_cast<uint64_t>(K);

@@ -60,7 +60,7 @@ typedef void* qk_stream_t;
 #define QK_FMT_MXFP8_E4M3 1 /* A, B: one E4M3 byte per element */
 #define QK_FMT_MXFP4_E2M1 2 /* A, B: two E2M1 codes per byte, element 2i in the low nibble */
 
-/* ---- output element types for qk_gemm_int8_rowwise_out and qk_gemm_fp8_rowwise_out */
+/* ---- output element types of the *_out entry points ----------------------- */
 #define QK_OUT_BF16 0 /* 2 bytes, bf16 round to nearest even */
 #define QK_OUT_FP16 1 /* 2 bytes, IEEE half round to nearest even (beyond 65504: +-inf) */
 #define QK_OUT_FP32 2 /* 4 bytes, the fp32 value x itself */
@@ -184,6 +184,22 @@ int qk_gemm_mx_b32(int fmt, const void* A, const uint8_t* sA, const void* B, con
                    const uint16_t* bias, uint16_t* out, int64_t M, int64_t N, int64_t K, qk_stream_t stream);
 
 /*
+ * qk_gemm_mx with a choice of output element type (ROCm/aiter PR #6262: its
+ * FP4 GEMM, gemm_a4w4, takes the output dtype as an argument, bf16 by
+ * default).  The same fp32 value as qk_gemm_mx computes, then
+ *   out_type QK_OUT_BF16: out bf16 [M, N]   (exactly qk_gemm_mx)
+ *            QK_OUT_FP16: out fp16 [M, N]   round to nearest even, +-inf beyond the fp16 range
+ *            QK_OUT_FP32: out fp32 [M, N]   the value itself
+ * fp16 and fp32 outputs run the 2-SM tile kernel for every M (the few-row
+ * kernels write bf16 only), so for a given problem the two hold the same
+ * value.  Arguments, requirements and errors as for qk_gemm_mx; an unknown
+ * out_type returns QK_ERR_ARG.
+ */
+int qk_gemm_mx_out(int fmt, const void* A, const uint8_t* sA, const void* B, const uint8_t* sB,
+                   const uint16_t* bias, void* out, int out_type, int64_t M, int64_t N, int64_t K,
+                   qk_stream_t stream);
+
+/*
  * FP8 E4M3 GEMM with per-token (row) and per-channel (column) fp32 scales
  * (ROCm/aiter PR #6262, gemm_a8w8_bpreshuffle with per-token/per-channel
  * scales; ROCm/mori PR #806, the "ptpc" kind).  Same epilogue as
@@ -279,6 +295,15 @@ int qk_gemm_fp8_blockscale(const uint8_t* A, const uint8_t* B, const float* sa, 
 int qk_gemm_nvfp4(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const uint8_t* sB, const float* ga,
                   const float* gb, const uint16_t* bias, uint16_t* out, int64_t M, int64_t N, int64_t K,
                   qk_stream_t stream);
+
+/*
+ * qk_gemm_nvfp4 with a choice of output element type (ROCm/aiter PR #6262:
+ * gemm_a4w4 takes the output dtype beside the NVFP4 per-tensor scales), with
+ * the output types, kernels and errors of qk_gemm_mx_out.
+ */
+int qk_gemm_nvfp4_out(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const uint8_t* sB, const float* ga,
+                      const float* gb, const uint16_t* bias, void* out, int out_type, int64_t M, int64_t N,
+                      int64_t K, qk_stream_t stream);
 
 /*
  * Quantizers that produce the operands above from bf16 data.

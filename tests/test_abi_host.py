@@ -108,6 +108,30 @@ def test_fp8_out_type_argument_errors(lib):
         assert call(out_type=ot, M=0, A=0, out=0) == qk.QK_OK   # empty product: nothing launched
 
 
+@pytest.mark.parametrize("entry", ["mx", "nvfp4"])
+def test_block_scaled_out_type_argument_errors(lib, entry):
+    def call(out_type=qk.QK_OUT_FP32, **kw):
+        A, out = _p(kw.get("A", FAKE)), _p(kw.get("out", FAKE))
+        M, N, K = kw.get("M", 128), kw.get("N", 128), kw.get("K", 128)
+        if entry == "mx":
+            return lib.qk_gemm_mx_out(kw.get("fmt", qk.FMT_MXFP8_E4M3), A, _p(FAKE), _p(FAKE), _p(FAKE), None, out,
+                                      out_type, M, N, K, None)
+        return lib.qk_gemm_nvfp4_out(A, _p(FAKE), _p(FAKE), _p(FAKE), None, None, None, out, out_type, M, N, K,
+                                     None)
+    for bad in (-1, 3, 99):
+        assert call(out_type=bad) == qk.QK_ERR_ARG       # checked before anything else
+        assert call(out_type=bad, M=0) == qk.QK_ERR_ARG
+    for ot in (qk.QK_OUT_BF16, qk.QK_OUT_FP16, qk.QK_OUT_FP32):
+        assert call(out_type=ot, A=0) == qk.QK_ERR_ARG
+        assert call(out_type=ot, out=0) == qk.QK_ERR_ARG
+        assert call(out_type=ot, out=FAKE + 8) == qk.QK_ERR_ALIGN
+        assert call(out_type=ot, N=100) == qk.QK_ERR_ALIGN
+        assert call(out_type=ot, K=48) == qk.QK_ERR_ALIGN
+        assert call(out_type=ot, M=0, A=0, out=0) == qk.QK_OK   # empty product: nothing launched
+        if entry == "mx":
+            assert call(out_type=ot, fmt=7) == qk.QK_ERR_ARG
+
+
 def test_fp8_argument_errors(lib):
     call = lambda **kw: lib.qk_gemm_fp8_rowwise(_p(FAKE), _p(kw.get("B", FAKE)), _p(FAKE), _p(FAKE), None,
                                                 _p(FAKE), kw.get("M", 64), kw.get("N", 64), kw.get("K", 64), None)
