@@ -13,6 +13,9 @@ fp32 itself.
   bit (both run the same tiles): checked on whole outputs, and with A's
   scales raised by 2^16 so that many values pass the fp16 range (+-inf
   there, the finite value in fp32).
+* With every tile split into K-parts (QK_TAIL_SPLIT=3), the part that
+  arrives last emits the sum through the same fp16 and fp32 paths (FP8
+  per-token, MXFP4, NVFP4).
 """
 import numpy as np
 import pytest
@@ -110,3 +113,35 @@ def test_block_scaled_out_dtype_argument():
     q = _problem("nvfp4", 64, 128, 256, 1, False)
     out = qk.gemm_nvfp4(*[to_dev(v) for v in (q.A, q.sA, q.B, q.sB)], out_dtype=torch.float16)
     assert out.dtype == torch.float16 and out.shape == (64, 128)
+
+
+@pytest.mark.parametrize("fmt", ["fp8", "mxfp4", "nvfp4"])
+def test_out_types_with_tail_split(fmt, monkeypatch):
+    # every tile split into three K-parts: the part that arrives last emits
+    # the sum through the fp16 staging blocks or the fp32 direct stores
+    monkeypatch.setenv("QK_TAIL_SPLIT", "3")
+    M, N, K = 600, 776, 3872
+    if fmt == "fp8":
+        p = qi.fp8_problem(M, N, K, seed=41, bias=True)
+        outs = {}
+        for dt in (torch.float32, torch.float16):
+            o = torch.full((M, N), float("nan"), dtype=dt, device="cuda")
+            qk.gemm_fp8_rowwise(to_dev(p.A), to_dev(p.B), to_dev(p.sa), to_dev(p.sb), bias_dev(p.bias), o)
+            outs[dt] = o
+        torch.cuda.synchronize()
+        ref_fn = lambda **r: oracle.gemm_fp8_rowwise(p.A, p.B, p.sa, p.sb, bias=p.bias, **r)
+    else:
+        p = _problem(fmt, M, N, K, 41, True)
+        outs = {dt: _run(fmt, p, dt) for dt in (torch.float32, torch.float16)}
+        ref_fn = lambda **r: _ref(fmt, p, **r)
+    g32, g16, refs = [], [], []
+    for (m0, m1, n0, n1) in qi.sample_tiles(M, N, 3, 12):
+        refs.append(ref_fn(m0=m0, m1=m1, n0=n0, n1=n1).ravel())
+        g32.append(outs[torch.float32][m0:m1, n0:n1].cpu().numpy().astype(np.float64).ravel())
+        g16.append(outs[torch.float16][m0:m1, n0:n1].cpu().numpy().astype(np.float64).ravel())
+    ref = np.concatenate(refs)[None, :]
+    assert_close_values(np.concatenate(g32)[None, :], ref, f"{fmt} fp32 out, split")
+    assert_close_values(np.concatenate(g16)[None, :], ref, f"{fmt} fp16 out, split")
+    x = outs[torch.float32].cpu().numpy()
+    assert np.array_equal(_f16_bits(outs[torch.float16])[:128], oracle.f32_to_f16(x[:128])), "fp16 != rne(fp32)"
+    assert qk.device_status() == 0
